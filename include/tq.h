@@ -1,0 +1,209 @@
+/*
+ * tq.h -- C ABI of libtq: GB300-native TurboQuant KV-cache compression.
+ *
+ * The operations restate these pages:
+ *   [spec]   "TurboQuant KV Cache Compression — Spec" (Foundry attention/spec.md)
+ *   [fork]   "TurboQuant KV Cache (turboq2 / turboq3 / turboq4)" (llama.cpp fork,
+ *            turboquant-kv-base.md)
+ *   [rotor]  "RotorQuant KV Cache Compression" (RotorQuant docs)
+ *   [serde]  "lmcache.v1.distributed.serde.turboquant" (LMCache serde design)
+ *
+ * Conventions for every call:
+ *   - head_dim is 128 ([fork] section 2, "head_dim multiple of 128": the block
+ *     size of all types is 128); any other value returns TQ_ERR_UNSUPPORTED.
+ *   - bits is 2, 3 or 4 ([spec] fa_tq_config); blocks are 2 + 16*bits bytes:
+ *     34 / 50 / 66 ([fork] section 4 block structures, without the legacy rnorm).
+ *   - Every device buffer is owned by the caller.  The library allocates no
+ *     device memory and keeps no per-call state; codebooks and signs travel
+ *     by value into the kernels.
+ *   - Calls that take a `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) only enqueue work and return without synchronising.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check returns a negative tq_status and enqueues nothing.  A CUDA
+ *     launch error returns TQ_ERR_CUDA.  Nothing throws across this ABI and no
+ *     kernel traps or asserts.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_ARG = -1,          /* null pointer, negative count, bad stride, T range */
+    TQ_ERR_UNSUPPORTED = -2,  /* head_dim != 128, bits not in {2,3,4}, dtype, G > 8 */
+    TQ_ERR_ALIGN = -3,        /* a base pointer or stride breaks the stated alignment */
+    TQ_ERR_WORKSPACE = -4,    /* workspace smaller than tq_attn_workspace_bytes() */
+    TQ_ERR_CUDA = -5          /* a CUDA runtime call or kernel launch failed */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+/* Lloyd-Max codebook of one (head_dim, bits) pair ([spec] Algorithm Detail,
+ * Step 2, fa_tq_codebook, plus head_dim).  Values are in the unit-sphere
+ * coordinate y = 2u - 1, u ~ Beta(d/2, d/2), ascending; boundaries[i] lies
+ * between centroids[i] and centroids[i+1]; only the first `levels` centroids
+ * and `levels - 1` boundaries are meaningful. */
+typedef struct {
+    int head_dim;
+    int bits;
+    int levels;
+    float centroids[16];
+    float boundaries[15];
+} tq_codebook;
+
+/* Random sign diagonal D of the rotation R x = H (D x) / sqrt(d) ([spec]
+ * As-Built Notes, Step 1).  Bit j of the 128-bit mask (word j / 32, bit
+ * j % 32) set means D_jj = -1. */
+typedef struct {
+    uint32_t w[4];
+} tq_signs;
+
+/* Fill *out with the Lloyd-Max codebook of Beta(head_dim/2, head_dim/2)
+ * for `bits` ([spec] Codebook Generation: conditional means of cells,
+ * midpoint boundaries, iterated to a fixed point).  Host only; the first
+ * call per (head_dim, bits) runs the iteration (milliseconds) and caches it;
+ * thread-safe.  head_dim must be 128.  Errors: TQ_ERR_ARG (out NULL),
+ * TQ_ERR_UNSUPPORTED. */
+int tq_codebook_load(int head_dim, int bits, tq_codebook *out);
+
+/* Fill *out with the sign diagonal drawn from `seed` ([spec] Lifecycle,
+ * fa_tq_init(head_dim, config, seed)): output j of splitmix64 started at
+ * `seed` gives sign j, top bit set => -1.  Host only. */
+int tq_signs_from_seed(uint64_t seed, int head_dim, tq_signs *out);
+
+/* Bytes of one 128-element block: 34, 50 or 66; 0 for unsupported bits. */
+size_t tq_block_bytes(int bits);
+
+/* Quantise-on-insert ([spec] As-Built Notes and Steps 1-3; [fork] section 4
+ * encode pipeline steps 1-3): for each of n_vec rows x of 128 elements,
+ * n = ||x||, y = H (D x) / (sqrt(128) n), code_j = #{i : boundaries[i] <= y_j},
+ * codes bit-packed after the fp16 (round-to-nearest-even) norm n.
+ *   x                 device, row i at x + i * x_stride_elems elements, dtype
+ *                     x_dtype (TQ_F32 / TQ_BF16 / TQ_F16); base 16-byte aligned,
+ *                     x_stride_elems * sizeof(dtype) a multiple of 16.
+ *   cb, signs         codebook (cb->bits selects 2/3/4) and sign diagonal.
+ *   blocks            device output; block of row i at
+ *                     blocks + dst(i) * block_stride_bytes, dst(i) = i or
+ *                     dst_index[i] (device int64, n_vec entries) when given;
+ *                     block_stride_bytes >= tq_block_bytes(bits) and even,
+ *                     blocks 2-byte aligned.  Rows must not share a block.
+ *   n_vec == 0 is a no-op.  Zero rows store norm 0 and every code = levels/2.
+ * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
+                 const tq_codebook *cb, tq_signs signs,
+                 uint8_t *blocks, int64_t block_stride_bytes,
+                 const int64_t *dst_index, void *stream);
+
+/* Dequantise ([spec] Overview "look up reconstruction values, then rotate
+ * back"; Quantize / Dequantize fa_tq_dequantize): x_hat = n16 * D H c[code]
+ * / sqrt(128) for n_vec blocks, written as out_dtype (float32, or bf16 / fp16
+ * rounded to nearest even) at out + i * out_stride_elems elements.
+ *   blocks            device, block i at blocks + i * block_stride_bytes
+ *                     (even stride >= block bytes; base 2-byte aligned).
+ *   out               device, base 16-byte aligned, out_stride_elems *
+ *                     sizeof(out_dtype) a multiple of 16.
+ * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_decode_kv(const uint8_t *blocks, int64_t block_stride_bytes, int64_t n_vec,
+                 const tq_codebook *cb, tq_signs signs,
+                 void *out, int out_dtype, int64_t out_stride_elems, void *stream);
+
+/* QJL residual sketch of keys ([rotor] Implementation Requirements 1-2):
+ * k_mse = decode(k_blocks[i]), r = k - k_mse, res_norm_f16[i] = fp16(||r||),
+ * bit j of qjl_bits[i] (byte j / 8, position j % 8) = [(S r)_j >= 0].
+ *   k                 device original keys (dtype k_dtype, same alignment
+ *                     rules as tq_encode_kv's x).
+ *   k_blocks          device blocks of the same keys made by tq_encode_kv
+ *                     with the same cb / signs.
+ *   S                 device float32 [128][128] row-major sketch, m = 128.
+ *   qjl_bits          device [n_vec][16] bytes; res_norm_f16 device [n_vec].
+ * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_qjl_encode(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_elems,
+                  const uint8_t *k_blocks, int64_t block_stride_bytes,
+                  const tq_codebook *cb, tq_signs signs, const float *S,
+                  uint8_t *qjl_bits, uint16_t *res_norm_f16, void *stream);
+
+/* Workspace bytes tq_attn_decode needs for this shape (split-K partials).
+ * Returns 0 for an invalid shape. */
+size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap);
+
+/* Fused decode attention over a packed cache ([spec] Optimization: Fused
+ * dequant-dot; [fork] section 2 "fused flash-attention path required";
+ * [rotor] Fused Kernel Logic for the QJL term).  One query token per
+ * (batch, query head):
+ *   s_t = scale * ( n_t * <R q, cK[code_t]> + term2_t ),
+ *   term2_t = rn_t * sqrt(pi/2) / 128 * <S q, sign_t>   (only when qjl_bits),
+ *   o = sum_t softmax(s)_t * v_hat_t,  v_hat_t = R^T (nv_t cV[vcode_t])
+ *                                     (or the raw fp16 value when vcb NULL),
+ * computed as: rotate q once, score in the rotated domain, online softmax,
+ * accumulate values in the rotated domain, one inverse rotation per output.
+ *   q           device [B][Hq][128], dtype q_dtype (TQ_F32 / TQ_BF16 / TQ_F16).
+ *   k_blocks    device [B][Hkv][T_cap] blocks of kcb->bits, contiguous.
+ *   v           device: [B][Hkv][T_cap] blocks of vcb->bits, or, when vcb is
+ *               NULL, raw fp16 values [B][Hkv][T_cap][128].
+ *   seq_lens    device int32 [B] (each clamped to [0, T]; length 0 gives a
+ *               zero output row) or NULL for T tokens in every sequence.
+ *   Hq % Hkv == 0, G = Hq / Hkv <= 8 (query head h reads KV head h / G);
+ *   1 <= T <= T_cap; T_cap a multiple of 8; k_blocks, v, q and out 16-byte
+ *   aligned.
+ *   qjl_bits    device [B][Hkv][T_cap][16], res_norm_f16 device [B][Hkv][T_cap],
+ *               S device float32 [128][128]: all three NULL (plain score) or
+ *               all three set (two-term score).
+ *   out         device float32 [B][Hq][128].
+ *   workspace   device scratch of >= tq_attn_workspace_bytes(B, Hq, Hkv, T_cap)
+ *               bytes, 256-byte aligned; clobbered; calls that overlap on the
+ *               GPU must use different workspaces.
+ * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_WORKSPACE,
+ * TQ_ERR_CUDA. */
+int tq_attn_decode(const void *q, int q_dtype,
+                   const uint8_t *k_blocks, const tq_codebook *kcb,
+                   const void *v, const tq_codebook *vcb,
+                   const int32_t *seq_lens, int B, int Hq, int Hkv, int T_cap, int T,
+                   float scale, tq_signs signs,
+                   const uint8_t *qjl_bits, const uint16_t *res_norm_f16, const float *S,
+                   float *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Serialised size of one KV object ([serde] Tensor Layout and
+ * estimate_serialized_size): raw first layers | compressed middle layers |
+ * raw last layers, with quant_start = min(skip_first, L) and quant_end =
+ * max(quant_start, L - skip_last) ([serde] Configuration); compressed layers
+ * are [L_c][ceil(T / block_size)][block_size][hidden / 128][slot], slot =
+ * key block + value block bytes.  elem_bytes is 2 (bf16 / fp16).  Returns 0
+ * for invalid arguments. */
+size_t tq_serde_size(int num_layers, int num_tokens, int hidden_dim, int head_dim,
+                     int block_size, int skip_first, int skip_last,
+                     int key_bits, int value_bits, int elem_bytes);
+
+/* Serialise src (device, [2][L][T][hidden] of elem_dtype TQ_BF16 / TQ_F16,
+ * 16-byte aligned) into dst (device, tq_serde_size() bytes, 16-byte aligned):
+ * raw layers copied byte for byte, middle layers encoded with kcb / vcb.
+ * Token slots past T in the last token block are written as zero bytes.
+ * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_serde_serialize(const void *src, int elem_dtype, int num_layers, int num_tokens,
+                       int hidden_dim, int head_dim, int block_size,
+                       int skip_first, int skip_last,
+                       const tq_codebook *kcb, const tq_codebook *vcb, tq_signs signs,
+                       uint8_t *dst, void *stream);
+
+/* Inverse of tq_serde_serialize ([serde] Decompression Path): restores the
+ * [2][L][T][hidden] tensor in dst (raw layers byte-identical, middle layers
+ * dequantised and rounded to elem_dtype). */
+int tq_serde_deserialize(const uint8_t *src, int elem_dtype, int num_layers, int num_tokens,
+                         int hidden_dim, int head_dim, int block_size,
+                         int skip_first, int skip_last,
+                         const tq_codebook *kcb, const tq_codebook *vcb, tq_signs signs,
+                         void *dst, void *stream);
+
+/* Static, human-readable name of a tq_status value. */
+const char *tq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

@@ -13,16 +13,25 @@ operation", which holds only with the factors reversed: R^-1 = R^T =
 D H / sqrt(d) (H is symmetric and H H = d I, D D = I).
 """
 
+import functools
+
 import numpy as np
+
+
+@functools.lru_cache(maxsize=None)
+def _hadamard(d: int) -> np.ndarray:
+    i = np.arange(d)
+    pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    h = np.where(pc % 2 == 0, 1.0, -1.0)
+    h.setflags(write=False)
+    return h
 
 
 def hadamard(d: int = 128) -> np.ndarray:
     """Sylvester-Hadamard matrix of order d (d a power of two), float64."""
     if d <= 0 or d & (d - 1):
         raise ValueError("d must be a power of two")
-    i = np.arange(d)
-    pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
-    return np.where(pc % 2 == 0, 1.0, -1.0)
+    return _hadamard(d)
 
 
 def rotate(x: np.ndarray, signs: np.ndarray) -> np.ndarray:

@@ -1,0 +1,202 @@
+// Device helpers shared by libtq's kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kD = 128;
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Kernel-parameter copy of a codebook: centroids, boundaries and the
+// non-negative boundaries b[L/2 .. L-2] ("positive" half; b[L/2 - 1] == 0).
+struct DevCodebook {
+    float c[16];
+    float b[15];
+    int bits;
+};
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+// a - b rounded once: fma(b, -1, a).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
+}
+
+// Unnormalised Walsh-Hadamard transform of 128 values held as 64 packed pairs
+// p[i] = (e_i, e_{i+64}).  Stages 1..32 act on both halves at once with
+// packed float2 adds; stage 64 combines the two halves of each pair.  The
+// result is H e in Sylvester order (H[i][j] = (-1)^popcount(i & j)), in the
+// same pair layout.
+__device__ __forceinline__ void fwht128(float2 (&p)[64]) {
+#pragma unroll
+    for (int L = 1; L < 64; L <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            if ((i & L) == 0) {
+                float2 a = p[i], b = p[i + L];
+                p[i] = add2(a, b);
+                p[i + L] = sub2(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        float x = p[i].x, y = p[i].y;
+        p[i] = make_float2(x + y, x - y);
+    }
+}
+
+// Value j (0..127) of the pair layout.
+template <int J>
+__device__ __forceinline__ float pair_get(const float2 (&p)[64]) {
+    return J < 64 ? p[J & 63].x : p[J & 63].y;
+}
+
+__device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Sum of squares of the 128 values by 8 packed accumulator chains and a
+// pairwise tree (relative error below 12 * 2^-24 for these non-negative terms).
+__device__ __forceinline__ float sumsq128(const float2 (&p)[64]) {
+    float2 acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = __fmul2_rn(p[k], p[k]);
+#pragma unroll
+    for (int i = 8; i < 64; ++i) acc[i & 7] = __ffma2_rn(p[i], p[i], acc[i & 7]);
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1)
+#pragma unroll
+        for (int k = 0; k < s; ++k) acc[k] = add2(acc[k], acc[k + s]);
+    return acc[0].x + acc[0].y;
+}
+
+// Error-free sum a + b = s + e (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// True when n (>= 0) lies within rel * n of a rounding boundary of fp16
+// round-to-nearest, i.e. when a small error in n could change fp16(n).
+__device__ __forceinline__ bool near_fp16_tie(float n, float rel) {
+    __half h = __float2half_rn(n);
+    unsigned short hb = __half_as_ushort(h);
+    if (hb >= 0x7C00u) return n >= 65504.f * (1.f - 4.f * rel);   // overflow side
+    float hv = __half2float(h);
+    float tol = n * rel;
+    if (hb > 0) {
+        float lo = __half2float(__ushort_as_half((unsigned short)(hb - 1)));
+        if (fabsf(n - 0.5f * (lo + hv)) <= tol) return true;
+    }
+    float hi = (hb + 1 >= 0x7C00u) ? 65520.f : __half2float(__ushort_as_half((unsigned short)(hb + 1)));
+    return fabsf(n - 0.5f * (hv + hi)) <= tol;
+}
+
+// Double-float accumulation of a sum of squares (TwoProduct via FMA, TwoSum).
+struct SumSq2 {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float v) {
+        float pr = v * v;
+        float pe = fmaf(v, v, -pr);
+        float t, e;
+        two_sum(s, pr, t, e);
+        s = t;
+        c += e + pe;
+    }
+    // sqrt of the sum, rounded once to fp16 (round to nearest even).
+    __device__ __forceinline__ unsigned short sqrt_fp16() const {
+        float hi, lo;
+        two_sum(s, c, hi, lo);
+        return __half_as_ushort(__double2half(sqrt((double)hi + (double)lo)));
+    }
+};
+
+// fp16 of the L2 norm of a row of 128 values (dtype DT) held in shared memory,
+// accurate to far below an fp16 rounding step.  Used only when the fast
+// float estimate lies within 2^-20 of an fp16 rounding boundary; out of line
+// because it is rare.
+template <int DT>
+__device__ __noinline__ unsigned short exact_norm_fp16_smem(const uint8_t *row) {
+    SumSq2 acc;
+    for (int j = 0; j < kD; ++j) {
+        float v;
+        if (DT == TQ_F32) v = reinterpret_cast<const float *>(row)[j];
+        else if (DT == TQ_BF16) v = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(row)[j] << 16);
+        else v = __half2float(reinterpret_cast<const __half *>(row)[j]);
+        acc.add(v);
+    }
+    return acc.sqrt_fp16();
+}
+
+// Norm of a row of 128 values in shared memory, in double (exact squares).
+template <int DT>
+__device__ __noinline__ double norm_double_smem(const uint8_t *row) {
+    double acc = 0.0;
+    for (int j = 0; j < kD; ++j) {
+        float v;
+        if (DT == TQ_F32) v = reinterpret_cast<const float *>(row)[j];
+        else if (DT == TQ_BF16) v = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(row)[j] << 16);
+        else v = __half2float(reinterpret_cast<const __half *>(row)[j]);
+        acc = fma((double)v, (double)v, acc);
+    }
+    return sqrt(acc);
+}
+
+// Norm of the vector whose (sign-flipped) values are in p and whose raw row
+// is still in shared memory at `row`.  Returns the fp16 bits of ||x|| and, in
+// n_out, a float32 norm in the same units as p on return.  When the sum of
+// squares leaves [2^-100, 2^100] (tiny or huge vectors, where float32 squares
+// underflow or overflow) p is first rescaled by an exact power of two so the
+// transform and the quantiser work in range; codes do not depend on the
+// scale, and the stored norm comes from a double-precision sum.
+template <int DT>
+__device__ __forceinline__ unsigned short norm_fp16(float2 (&p)[64], const uint8_t *row, float &n_out) {
+    const float ss = sumsq128(p);
+    if (ss >= 7.888609052210118e-31f /* 2^-100 */ && ss <= 1.2676506002282294e30f /* 2^100 */) {
+        const float n = sqrtf(ss);
+        n_out = n;
+        if (!near_fp16_tie(n, 9.5367431640625e-07f /* 2^-20 */))
+            return __half_as_ushort(__float2half_rn(n));
+        return exact_norm_fp16_smem<DT>(row);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fmaxf(fabsf(p[i].x), fabsf(p[i].y)));
+    if (amax == 0.f) {
+        n_out = 0.f;
+        return 0;
+    }
+    int e;
+    frexpf(amax, &e);                       // amax = m 2^e, m in [0.5, 1)
+    const int e1 = -e / 2, e2 = -e - e1;    // two factors, each a normal float
+    const float2 s1 = make_float2(ldexpf(1.f, e1), ldexpf(1.f, e1));
+    const float2 s2 = make_float2(ldexpf(1.f, e2), ldexpf(1.f, e2));
+#pragma unroll
+    for (int i = 0; i < 64; ++i) p[i] = __fmul2_rn(__fmul2_rn(p[i], s1), s2);
+    n_out = sqrtf(sumsq128(p));
+    return __half_as_ushort(__double2half(norm_double_smem<DT>(row)));
+}
+
+// 16-byte async copy global -> shared (L2 only, no L1 allocation).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// 32-bit word at a 2-byte aligned shared-memory address.
+__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t *p) {
+    const uint16_t *h = reinterpret_cast<const uint16_t *>(p);
+    return (uint32_t)h[0] | ((uint32_t)h[1] << 16);
+}
+
+}  // namespace tq

@@ -1,0 +1,32 @@
+// Host-side helpers shared by libtq's CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+inline bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+inline int dtype_bytes(int dt) {
+    switch (dt) {
+        case TQ_F32: return 4;
+        case TQ_BF16: return 2;
+        case TQ_F16: return 2;
+        default: return 0;
+    }
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// Raise a kernel's dynamic shared-memory limit once per process and device.
+int set_smem_limit(const void *kernel, int bytes, int *done_for_device);
+
+inline int launch_status() {
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace tq
