@@ -168,6 +168,36 @@ int tq_attn_decode(const void *q, int q_dtype,
                    const uint8_t *qjl_bits, const uint16_t *res_norm_f16, const float *S,
                    float *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the device array that tq_attn_decode_noalloc uses as its split-K
+ * scratch (8 MiB; it covers, e.g., batch 64 x 28 query heads at any context). */
+#define TQ_ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* tq_attn_decode for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is a library convenience).  A serving engine
+ * that owns all device memory in its own pool, or a plugin interface that
+ * passes a kernel only its inputs and outputs, cannot supply the split-K
+ * workspace, and a cudaMalloc inside a latency-critical decode loop is not
+ * acceptable either.  This call takes the same arguments as tq_attn_decode
+ * minus the workspace and uses a fixed TQ_ATTN_NOALLOC_SCRATCH_BYTES array of
+ * device memory inside the library instead; it allocates nothing.
+ *   - Shapes whose workspace (tq_attn_workspace_bytes) exceeds the array
+ *     return TQ_ERR_WORKSPACE; an invalid shape returns TQ_ERR_ARG.
+ *   - The array's device address is looked up once per device, on the first
+ *     call made with that device current; make that first call before any
+ *     stream capture.
+ *   - All calls share the array, which keeps the last call's contents (no
+ *     part of it needs to start at zero); calls that overlap on the GPU race
+ *     on it, so serialise them (one stream, or events).
+ *   - Every GPU that loads the library holds the array until process exit.
+ * Errors: as tq_attn_decode. */
+int tq_attn_decode_noalloc(const void *q, int q_dtype,
+                           const uint8_t *k_blocks, const tq_codebook *kcb,
+                           const void *v, const tq_codebook *vcb,
+                           const int32_t *seq_lens, int B, int Hq, int Hkv, int T_cap, int T,
+                           float scale, tq_signs signs,
+                           const uint8_t *qjl_bits, const uint16_t *res_norm_f16, const float *S,
+                           float *out, void *stream);
+
 /* Serialised size of one KV object ([serde] Tensor Layout and
  * estimate_serialized_size): raw first layers | compressed middle layers |
  * raw last layers, with quant_start = min(skip_first, L) and quant_end =
