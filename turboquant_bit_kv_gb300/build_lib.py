@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtq.so")
 
-SOURCES = ["tq_host.cpp", "tq_codec.cu", "tq_attn.cu", "tq_attn_g1.cu", "tq_attn_g2.cu",
+SOURCES = ["tq_host.cpp", "tq_encode.cu", "tq_codec.cu", "tq_attn.cu", "tq_attn_g1.cu", "tq_attn_g2.cu",
            "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_attn_noalloc.cu"]
 HEADERS = ["tq_device.cuh", "tq_attn.cuh", "tq_internal.h"]
 

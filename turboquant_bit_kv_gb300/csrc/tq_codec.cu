@@ -14,14 +14,13 @@
 //  * "lmcache.v1.distributed.serde.turboquant": Configuration and Tensor
 //    Layout (raw first | compressed middle | raw last layers).
 //
-// Design: one thread owns one 128-element vector.  A CTA of 128 threads
-// stages a tile of 128 input rows into shared memory with 16-byte cp.async
-// copies (double buffered across a persistent grid), each thread then holds
-// its vector in registers as 64 packed float2 pairs and runs the whole
-// Walsh-Hadamard transform there with packed adds (no shuffles), quantises
-// against boundaries pre-scaled by the vector's norm (so no per-coordinate
-// division), packs the codes, and writes its block into a shared staging
-// tile that the CTA stores to HBM with coalesced 16-byte stores.
+// Design (decode and QJL): one thread owns one 128-element vector.  A CTA of
+// 128 threads stages a tile of 128 rows into shared memory with 16-byte
+// cp.async copies (double buffered across a persistent grid), each thread
+// holds its vector in registers as 64 packed float2 pairs and runs the whole
+// Walsh-Hadamard transform there with packed adds, and the CTA stores its
+// tile to HBM with coalesced 16-byte stores.  The quantise-on-insert kernel
+// lives in tq_encode.cu.
 
 #include <algorithm>
 #include <cmath>
@@ -55,19 +54,6 @@ int set_smem_limit(const void *kernel, int bytes, int *done_for_device) {
     if (dev < 64) done_for_device[dev] = bytes;
     return TQ_OK;
 }
-
-template <int BITS>
-struct BlockFmt {
-    static constexpr int kBytes = 2 + 16 * BITS;  // 34 / 50 / 66
-    static constexpr int kWords = 4 * BITS;       // 32-bit code words after the norm
-    static constexpr int kLevels = 1 << BITS;
-};
-
-template <int DT>
-struct InFmt {
-    static constexpr int kRowBytes = DT == TQ_F32 ? 512 : 256;
-    static constexpr int kPitch = kRowBytes + 16;  // conflict-free 16-byte row reads
-};
 
 // Sign table in shared memory.  For 16-bit inputs/outputs: word w holds the
 // sign bits of elements 2w (bit 15) and 2w+1 (bit 31).  For float32: word j
@@ -130,53 +116,6 @@ __device__ __forceinline__ void load_signed_pairs(const uint8_t *row, const uint
     }
 }
 
-// Codes of a transformed vector u (pairs, unnormalised H D x) against the
-// positive boundaries scaled by sqrt(128) * n, packed into code words.
-template <int BITS>
-__device__ __forceinline__ void quantize_pack(const float2 (&p)[64], const float (&thr)[(1 << BITS) / 2 - 1],
-                                              uint32_t (&cw)[BlockFmt<BITS>::kWords]) {
-    constexpr int H = (1 << BITS) / 2;
-#pragma unroll
-    for (int k = 0; k < BlockFmt<BITS>::kWords; ++k) cw[k] = 0u;
-#pragma unroll
-    for (int j = 0; j < kD; ++j) {
-        float u = (j < 64) ? p[j & 63].x : p[j & 63].y;
-        float a = fabsf(u);
-        int cnt = 0;
-#pragma unroll
-        for (int k = 0; k < H - 1; ++k) cnt += (a >= thr[k]) ? 1 : 0;
-        uint32_t idx = (u < 0.f) ? (uint32_t)(H - 1 - cnt) : (uint32_t)(H + cnt);
-        if constexpr (BITS == 4) {
-            cw[j >> 3] |= idx << (4 * (j & 7));
-        } else if constexpr (BITS == 2) {
-            cw[j >> 4] |= idx << (2 * (j & 15));
-        } else {
-            cw[j >> 4] |= (idx & 3u) << (2 * (j & 15));
-            cw[8 + (j >> 5)] |= (idx >> 2) << (j & 31);
-        }
-    }
-}
-
-// Write norm + code words as one block at a 2-byte aligned shared address.
-// `odd` tells whether base + 2 is 4-byte aligned.
-template <int BITS>
-__device__ __forceinline__ void store_block_smem(uint8_t *base, bool odd, unsigned short n16,
-                                                 const uint32_t (&cw)[BlockFmt<BITS>::kWords]) {
-    constexpr int NW = BlockFmt<BITS>::kWords;
-    if (odd) {
-        *reinterpret_cast<uint16_t *>(base) = n16;
-        uint32_t *w = reinterpret_cast<uint32_t *>(base + 2);
-#pragma unroll
-        for (int k = 0; k < NW; ++k) w[k] = cw[k];
-    } else {
-        uint32_t *w = reinterpret_cast<uint32_t *>(base);
-        w[0] = (uint32_t)n16 | (cw[0] << 16);
-#pragma unroll
-        for (int k = 1; k < NW; ++k) w[k] = (cw[k - 1] >> 16) | (cw[k] << 16);
-        *reinterpret_cast<uint16_t *>(base + 4 * NW) = (uint16_t)(cw[NW - 1] >> 16);
-    }
-}
-
 // Read a block (norm + code words) from a 2-byte aligned shared address.
 template <int BITS>
 __device__ __forceinline__ unsigned short load_block_smem(const uint8_t *base,
@@ -202,98 +141,12 @@ __device__ __forceinline__ void lut_pairs(const uint32_t (&cw)[BlockFmt<BITS>::k
     for (int i = 0; i < 64; ++i) p[i] = make_float2(lut[code_at<BITS>(cw, i)], lut[code_at<BITS>(cw, i + 64)]);
 }
 
-struct EncodeArgs {
-    const uint8_t *x;
-    int64_t n_vec;
-    int64_t x_stride;  // bytes
-    uint8_t *out;
-    int64_t out_stride;  // bytes
-    const int64_t *dst_index;
-    int contiguous;
-    DevCodebook cb;
-    uint32_t signs[4];
-};
-
 template <int DT>
 __device__ __forceinline__ void stage_rows(uint8_t *st, const uint8_t *x, int64_t stride, int nv) {
     constexpr int cpr = InFmt<DT>::kRowBytes / 16;
     for (int c = threadIdx.x; c < nv * cpr; c += kThreads) {
         int r = c / cpr, col = c - r * cpr;
         cp_async16(st + r * InFmt<DT>::kPitch + col * 16, x + r * stride + col * 16);
-    }
-}
-
-template <int BITS>
-__device__ __forceinline__ void copy_out_blocks(const uint8_t *sm_out, uint8_t *out, int64_t v0, int nv,
-                                                int64_t out_stride, const int64_t *dst_index, int contiguous) {
-    constexpr int BB = BlockFmt<BITS>::kBytes;
-    if (contiguous) {
-        uint8_t *dst = out + v0 * BB;
-        int nbytes = nv * BB;
-        int nch = nbytes >> 4;
-        for (int c = threadIdx.x; c < nch; c += kThreads)
-            reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(sm_out)[c];
-        for (int h = (nch << 3) + threadIdx.x; h < (nbytes >> 1); h += kThreads)
-            reinterpret_cast<uint16_t *>(dst)[h] = reinterpret_cast<const uint16_t *>(sm_out)[h];
-    } else {
-        int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        for (int r = warp * 32; r < min(nv, warp * 32 + 32); ++r) {
-            int64_t di = dst_index ? dst_index[v0 + r] : (v0 + r);
-            uint16_t *dst = reinterpret_cast<uint16_t *>(out + di * out_stride);
-            const uint16_t *src = reinterpret_cast<const uint16_t *>(sm_out + r * BB);
-            for (int h = lane; h < BB / 2; h += 32) dst[h] = src[h];
-        }
-    }
-}
-
-template <int BITS, int DT>
-__global__ void __launch_bounds__(kThreads) encode_kernel(EncodeArgs a) {
-    constexpr int BB = BlockFmt<BITS>::kBytes;
-    constexpr int H = (1 << BITS) / 2;
-    constexpr int STAGE = kThreads * InFmt<DT>::kPitch;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *stage = smem;                          // 2 stages
-    uint8_t *sm_out = smem + 2 * STAGE;             // kThreads * BB
-    uint32_t *sg16 = reinterpret_cast<uint32_t *>(sm_out + ((kThreads * BB + 15) & ~15));
-    uint32_t *sg32 = sg16 + 64;
-    build_sign_tables(sg16, sg32, a.signs);
-
-    const int64_t ntiles = (a.n_vec + kThreads - 1) / kThreads;
-    int64_t tile = blockIdx.x;
-    if (tile < ntiles)
-        stage_rows<DT>(stage, a.x + tile * kThreads * a.x_stride, a.x_stride,
-                       (int)min64(kThreads, a.n_vec - tile * kThreads));
-    cp_async_commit();
-    const float rs = 11.313708498984761f;  // sqrt(128)
-    for (int it = 0; tile < ntiles; ++it, tile += gridDim.x) {
-        const int64_t next = tile + gridDim.x;
-        if (next < ntiles)
-            stage_rows<DT>(stage + ((it + 1) & 1) * STAGE, a.x + next * kThreads * a.x_stride, a.x_stride,
-                           (int)min64(kThreads, a.n_vec - next * kThreads));
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const int64_t v0 = tile * kThreads;
-        const int nv = (int)min64(kThreads, a.n_vec - v0);
-        const int t = threadIdx.x;
-        if (t < nv) {
-            float2 p[64];
-            const uint8_t *row = stage + (it & 1) * STAGE + t * InFmt<DT>::kPitch;
-            load_signed_pairs<DT>(row, sg16, sg32, p);
-            float n;
-            unsigned short n16 = norm_fp16<DT>(p, row, n);
-            fwht128(p);
-            const float sc = n > 0.f ? n * rs : 1.f;
-            float thr[H - 1 > 0 ? H - 1 : 1];
-#pragma unroll
-            for (int k = 0; k < H - 1; ++k) thr[k] = a.cb.b[H + k] * sc;
-            uint32_t cw[BlockFmt<BITS>::kWords];
-            quantize_pack<BITS>(p, thr, cw);
-            store_block_smem<BITS>(sm_out + t * BB, (t & 1) != 0, n16, cw);
-        }
-        __syncthreads();
-        copy_out_blocks<BITS>(sm_out, a.out, v0, nv, a.out_stride, a.dst_index, a.contiguous);
-        __syncthreads();
     }
 }
 
@@ -515,18 +368,6 @@ bool codebook_ok(const tq_codebook *cb) {
 }
 
 template <int BITS, int DT>
-int launch_encode(const EncodeArgs &a, cudaStream_t st) {
-    static int done[64] = {0};
-    const int smem = 2 * kThreads * InFmt<DT>::kPitch + ((kThreads * BlockFmt<BITS>::kBytes + 15) & ~15) + 192 * 4;
-    if (set_smem_limit((const void *)encode_kernel<BITS, DT>, smem, done) != TQ_OK) return TQ_ERR_CUDA;
-    const int64_t ntiles = (a.n_vec + kThreads - 1) / kThreads;
-    int per_sm = DT == TQ_F32 ? 2 : 3;
-    int grid = (int)min64(ntiles, (int64_t)per_sm * sm_count());
-    encode_kernel<BITS, DT><<<grid, kThreads, smem, st>>>(a);
-    return launch_status();
-}
-
-template <int BITS, int DT>
 int launch_decode(const DecodeArgs &a, cudaStream_t st) {
     static int done[64] = {0};
     const int in_stage = (kThreads * BlockFmt<BITS>::kBytes + 15) & ~15;
@@ -572,30 +413,6 @@ using namespace tq;
         }                                                                              \
         return _r;                                                                     \
     } while (0)
-
-extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
-                            const tq_codebook *cb, tq_signs signs, uint8_t *blocks,
-                            int64_t block_stride_bytes, const int64_t *dst_index, void *stream) {
-    if (n_vec < 0 || !cb) return TQ_ERR_ARG;
-    if (!codebook_ok(cb) || dtype_bytes(x_dtype) == 0) return TQ_ERR_UNSUPPORTED;
-    if (n_vec == 0) return TQ_OK;
-    const int es = dtype_bytes(x_dtype);
-    const int64_t bb = (int64_t)tq_block_bytes(cb->bits);
-    if (!x || !blocks || x_stride_elems < kD || block_stride_bytes < bb) return TQ_ERR_ARG;
-    if (!aligned(x, 16) || (x_stride_elems * es) % 16 || !aligned(blocks, 2) || (block_stride_bytes & 1))
-        return TQ_ERR_ALIGN;
-    EncodeArgs a;
-    a.x = static_cast<const uint8_t *>(x);
-    a.n_vec = n_vec;
-    a.x_stride = x_stride_elems * es;
-    a.out = blocks;
-    a.out_stride = block_stride_bytes;
-    a.dst_index = dst_index;
-    a.contiguous = (!dst_index && block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
-    a.cb = to_dev(cb);
-    for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
-    TQ_DISPATCH(launch_encode, cb->bits, x_dtype, a, (cudaStream_t)stream);
-}
 
 extern "C" int tq_decode_kv(const uint8_t *blocks, int64_t block_stride_bytes, int64_t n_vec,
                             const tq_codebook *cb, tq_signs signs, void *out, int out_dtype,

@@ -14,6 +14,20 @@ constexpr int kD = 128;
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
+template <int BITS>
+struct BlockFmt {
+    static constexpr int kBytes = 2 + 16 * BITS;  // 34 / 50 / 66
+    static constexpr int kWords = 4 * BITS;       // 32-bit code words after the norm
+    static constexpr int kLevels = 1 << BITS;
+};
+
+template <int DT>
+struct InFmt {
+    static constexpr int kRowBytes = DT == TQ_F32 ? 512 : 256;
+    static constexpr int kPitch = kRowBytes + 16;  // conflict-free 16-byte row reads
+};
+
+
 // Kernel-parameter copy of a codebook: centroids, boundaries and the
 // non-negative boundaries b[L/2 .. L-2] ("positive" half; b[L/2 - 1] == 0).
 struct DevCodebook {

@@ -1,0 +1,807 @@
+// Quantise-on-insert (tq_encode_kv) for sm_103a.
+//
+// Restates "TurboQuant KV Cache Compression — Spec": As-Built Notes (random
+// signs before the Walsh-Hadamard transform, H (D x); normalise by the L2
+// norm), Algorithm Detail Step 2 (level index from the boundaries) and
+// Step 3 (bit packing); and "TurboQuant KV Cache (turboq2 / turboq3 /
+// turboq4)" section 4 (block = fp16 norm + packed codes).
+//
+// Work split: two threads own one 128-element vector, 64 elements each.
+// Thread h of a pair reads the 16-byte chunks 2c + h (c = 0..7) of its row
+// straight into registers (each 32-byte sector is consumed by one pair in
+// one instruction); it therefore holds elements e = 16c + 8h + k, k = 0..7.
+// The next tile's rows are loaded while the current tile is processed.
+//   * Six of the seven butterfly stages (element-index bits 0-2 and 4-6) run
+//     in registers on packed float2 pairs; the stage on bit 3 is one full
+//     exchange with the partner thread (shfl.xor 1) and one packed FMA with a
+//     per-thread sign, which leaves both threads with exact butterfly
+//     outputs (no role-dependent selects).
+//   * The norm comes from a float32 sum of squares; when it falls within
+//     2^-20 of an fp16 rounding boundary it is recomputed exactly
+//     (double-float), and tiny/huge vectors (sum of squares outside
+//     [2^-100, 2^100]) are rescaled by an exact power of two first.
+//   * Quantisation never divides by the norm: u (u = H D x) is scaled once
+//     to G y (y = u / (sqrt(128) n)), G chosen so that no cell of width 1
+//     holds two boundaries; adding 64 + 1.5 * 2^23 puts the cell index
+//     round(G y + 64) in the low bits of the float, a 128-entry table gives
+//     the cell's count of boundaries below it and the boundary inside it, and
+//     one comparison finishes #{i : b_i <= y} (3- and 4-bit).  The 2-bit code
+//     is three comparisons against -b, 0, +b (scaled by sqrt(128) n).
+//   * Codes are packed per 8 elements and written into a shared-memory block
+//     tile, which the CTA stores with coalesced 16-byte stores (or block by
+//     block for strided / scattered destinations).
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kEncThreads = 128;
+constexpr int kEncVecs = kEncThreads / 2;  // vectors per tile
+constexpr int kBuckets = 128;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct EncArgs {
+    const uint8_t *x;
+    int64_t n_vec;
+    int64_t x_stride;   // bytes
+    uint8_t *out;
+    int64_t out_stride; // bytes
+    const int64_t *dst_index;
+    int contiguous;
+    float b0;           // 2-bit: the positive boundary
+    float grid;         // 3/4-bit: cells per unit of y
+    float2 table[kBuckets];  // cell j: (boundary inside it in G*y units | +inf, bits of #boundaries below it)
+    uint32_t signs[4];
+};
+
+// Raw 64-element share of a row, as loaded (16-bit inputs: 8 chunks;
+// float32: 16 chunks).
+template <int DT>
+struct Raw {
+    uint4 r[DT == TQ_F32 ? 16 : 8];
+};
+
+template <int DT>
+__device__ __forceinline__ void load_raw(Raw<DT> &raw, const uint8_t *row, bool valid, int h) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        if constexpr (DT == TQ_F32) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(row + (2 * c + h) * 32);
+            raw.r[2 * c] = valid ? __ldcs(p) : make_uint4(0, 0, 0, 0);
+            raw.r[2 * c + 1] = valid ? __ldcs(p + 1) : make_uint4(0, 0, 0, 0);
+        } else {
+            const uint4 *p = reinterpret_cast<const uint4 *>(row + (2 * c + h) * 16);
+            raw.r[c] = valid ? __ldcs(p) : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// Sign-flipped values as pairs p[c'][k] = (e(c', k), e(c' + 4, k)) with
+// e(c, k) = element 16c + 8h + k.
+template <int DT>
+__device__ __forceinline__ void to_pairs(const Raw<DT> &raw, const uint32_t *sg16, const uint32_t *sg32, int h,
+                                         float2 (&p)[4][8]) {
+    float v[8][8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        if constexpr (DT == TQ_F32) {
+            const uint4 s0 = reinterpret_cast<const uint4 *>(sg32 + 16 * c + 8 * h)[0];
+            const uint4 s1 = reinterpret_cast<const uint4 *>(sg32 + 16 * c + 8 * h)[1];
+            const uint4 a = raw.r[2 * c], b = raw.r[2 * c + 1];
+            v[c][0] = __uint_as_float(a.x ^ s0.x);
+            v[c][1] = __uint_as_float(a.y ^ s0.y);
+            v[c][2] = __uint_as_float(a.z ^ s0.z);
+            v[c][3] = __uint_as_float(a.w ^ s0.w);
+            v[c][4] = __uint_as_float(b.x ^ s1.x);
+            v[c][5] = __uint_as_float(b.y ^ s1.y);
+            v[c][6] = __uint_as_float(b.z ^ s1.z);
+            v[c][7] = __uint_as_float(b.w ^ s1.w);
+        } else {
+            const uint4 s = reinterpret_cast<const uint4 *>(sg16 + 8 * c + 4 * h)[0];
+            const uint32_t w[4] = {raw.r[c].x ^ s.x, raw.r[c].y ^ s.y, raw.r[c].z ^ s.z, raw.r[c].w ^ s.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if constexpr (DT == TQ_BF16) {
+                    v[c][2 * m] = bf16_bits_lo(w[m]);
+                    v[c][2 * m + 1] = bf16_bits_hi(w[m]);
+                } else {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[m]));
+                    v[c][2 * m] = f.x;
+                    v[c][2 * m + 1] = f.y;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p[c][k] = make_float2(v[c][k], v[c + 4][k]);
+}
+
+// 0xFFFFFFFF when a >= b, else 0 (one set instruction).
+__device__ __forceinline__ uint32_t set_ge(float a, float b) {
+    uint32_t r;
+    asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// 8-byte shared-memory load at a 32-bit shared address.
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float2 sub2x(float2 a, float2 b) {
+    float2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;"
+        : "=l"(*reinterpret_cast<unsigned long long *>(&r))
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return r;
+}
+
+// Unnormalised Walsh-Hadamard transform of the pair's 128 elements.
+__device__ __forceinline__ void fwht_pair(float2 (&p)[4][8], float sgn) {
+#pragma unroll
+    for (int L = 1; L < 8; L <<= 1)              // element bits 0..2 (k)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if ((k & L) == 0) {
+                    const float2 a = p[c][k], b = p[c][k + L];
+                    p[c][k] = __fadd2_rn(a, b);
+                    p[c][k + L] = sub2x(a, b);
+                }
+#pragma unroll
+    for (int L = 1; L < 4; L <<= 1)              // element bits 4..5 (c')
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if ((c & L) == 0)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 a = p[c][k], b = p[c + L][k];
+                    p[c][k] = __fadd2_rn(a, b);
+                    p[c + L][k] = sub2x(a, b);
+                }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)                  // element bit 6 (inside a pair)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float x = p[c][k].x, y = p[c][k].y;
+            p[c][k] = make_float2(x + y, x - y);
+        }
+    // element bit 3: the partner holds e ^ 8.  h = 0 keeps e + partner,
+    // h = 1 (partner holds e - 8) keeps partner - own: fma(own, sgn, partner).
+    const float2 s2 = make_float2(sgn, sgn);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float2 o;
+            o.x = __shfl_xor_sync(kFull, p[c][k].x, 1);
+            o.y = __shfl_xor_sync(kFull, p[c][k].y, 1);
+            p[c][k] = __ffma2_rn(p[c][k], s2, o);
+        }
+}
+
+__device__ __forceinline__ float sumsq_pairs(const float2 (&p)[4][8]) {
+    float2 acc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = __fmul2_rn(p[c][0], p[c][0]);
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = __ffma2_rn(p[c][k], p[c][k], acc[c]);
+    acc[0] = __fadd2_rn(acc[0], acc[1]);
+    acc[2] = __fadd2_rn(acc[2], acc[3]);
+    acc[0] = __fadd2_rn(acc[0], acc[2]);
+    return acc[0].x + acc[0].y;
+}
+
+template <int BITS, int DT>
+__global__ void __launch_bounds__(kEncThreads, 3) encode_kernel(const __grid_constant__ EncArgs a) {
+    constexpr int L = 1 << BITS, H = L / 2, BB = BlockFmt<BITS>::kBytes;
+    __shared__ __align__(16) uint32_t sg16[64];
+    __shared__ __align__(16) uint32_t sg32[128];
+    __shared__ __align__(16) float2 tab[kBuckets];
+    __shared__ __align__(16) uint8_t sm_out[(kEncVecs * BB + 15) & ~15];
+
+    for (int j = threadIdx.x; j < kD; j += kEncThreads) sg32[j] = ((a.signs[j >> 5] >> (j & 31)) & 1u) << 31;
+    for (int w = threadIdx.x; w < 64; w += kEncThreads) {
+        const int j = 2 * w;
+        sg16[w] = (((a.signs[j >> 5] >> (j & 31)) & 1u) << 15) | (((a.signs[j >> 5] >> ((j + 1) & 31)) & 1u) << 31);
+    }
+    for (int j = threadIdx.x; j < kBuckets; j += kEncThreads) tab[j] = a.table[j];
+    __syncthreads();
+
+    const int pv = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const float sgn = h ? -1.f : 1.f;
+    const int64_t ntiles = (a.n_vec + kEncVecs - 1) / kEncVecs;
+    int64_t tile = blockIdx.x;
+    Raw<DT> raw;
+    if (tile < ntiles) {
+        const int64_t row = tile * kEncVecs + pv;
+        load_raw<DT>(raw, a.x + row * a.x_stride, row < a.n_vec, h);
+    }
+    for (; tile < ntiles; tile += gridDim.x) {
+        const int64_t v0 = tile * kEncVecs;
+        const int nv = (int)min64(kEncVecs, a.n_vec - v0);
+        float2 p[4][8];
+        to_pairs<DT>(raw, sg16, sg32, h, p);
+        const int64_t next = tile + gridDim.x;
+        if (next < ntiles) {
+            const int64_t row = next * kEncVecs + pv;
+            load_raw<DT>(raw, a.x + row * a.x_stride, row < a.n_vec, h);
+        }
+
+        // ---- norm
+        float ss = sumsq_pairs(p);
+        ss += __shfl_xor_sync(kFull, ss, 1);
+        const bool out_of_range = !(ss >= 7.888609052210118e-31f && ss <= 1.2676506002282294e30f);
+        float n = sqrtf(ss);
+        unsigned short n16 = __half_as_ushort(__float2half_rn(n));
+        const bool near = !out_of_range && near_fp16_tie(n, 9.5367431640625e-07f /* 2^-20 */);
+        if (__any_sync(kFull, near)) {
+            // exact: double-float sums of squares of both halves, one rounding
+            SumSq2 acc;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    acc.add(p[c][k].x);
+                    acc.add(p[c][k].y);
+                }
+            const float os = __shfl_xor_sync(kFull, acc.s, 1), oc = __shfl_xor_sync(kFull, acc.c, 1);
+            SumSq2 tot;
+            two_sum(acc.s, os, tot.s, tot.c);
+            tot.c += acc.c + oc;
+            if (near) n16 = tot.sqrt_fp16();
+        }
+        if (__any_sync(kFull, out_of_range)) {
+            // tiny, huge or zero vector: norm in double, values rescaled by 2^-e
+            double sd = 0.0;
+            float amax = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    sd = fma((double)p[c][k].x, (double)p[c][k].x, sd);
+                    sd = fma((double)p[c][k].y, (double)p[c][k].y, sd);
+                    amax = fmaxf(amax, fmaxf(fabsf(p[c][k].x), fabsf(p[c][k].y)));
+                }
+            sd += __shfl_xor_sync(kFull, sd, 1);
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            if (out_of_range) {
+                n16 = __half_as_ushort(__double2half(sqrt(sd)));
+                if (amax > 0.f) {
+                    int e;
+                    frexpf(amax, &e);
+                    const int e1 = -e / 2, e2 = -e - e1;
+                    const float2 f1 = make_float2(ldexpf(1.f, e1), ldexpf(1.f, e1));
+                    const float2 f2 = make_float2(ldexpf(1.f, e2), ldexpf(1.f, e2));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) p[c][k] = __fmul2_rn(__fmul2_rn(p[c][k], f1), f2);
+                }
+            }
+            float s2 = sumsq_pairs(p);
+            s2 += __shfl_xor_sync(kFull, s2, 1);
+            if (out_of_range) n = sqrtf(s2);
+        }
+
+        // ---- transform and quantise
+        fwht_pair(p, sgn);
+        const float sc = n > 0.f ? n * 11.313708498984761f : 1.f;  // sqrt(128) n
+        uint8_t *blk = sm_out + pv * BB;
+        if constexpr (BITS == 2) {
+            const float t = a.b0 * sc;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float u = cc < 4 ? p[cc][k].x : p[cc - 4][k].y;
+                    // code = [u >= -t] + [u >= 0] + [u >= t]; set.ge gives -1 / 0
+                    const uint32_t m = set_ge(u, -t) + set_ge(u, 0.f) + set_ge(u, t);
+                    w -= m << (2 * k);
+                }
+                *reinterpret_cast<uint16_t *>(blk + 2 + 4 * cc + 2 * h) = (uint16_t)w;
+            }
+        } else {
+            const float cs = a.grid / sc;
+            const float2 cs2 = make_float2(cs, cs);
+            const float2 off2 = make_float2(12582976.f, 12582976.f);  // 64 + 1.5 * 2^23
+            const uint32_t tab_base = (uint32_t)__cvta_generic_to_shared(tab);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t wx = 0, wy = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 yp = __fmul2_rn(p[cc][k], cs2);
+                    const float2 t = __fadd2_rn(yp, off2);
+                    // cell index = low 7 bits (masked, so even a NaN input stays in the table)
+                    const float2 ex = lds_f2(tab_base + (__float_as_uint(t.x) & (kBuckets - 1)) * 8u);
+                    const float2 ey = lds_f2(tab_base + (__float_as_uint(t.y) & (kBuckets - 1)) * 8u);
+                    const uint32_t cx = __float_as_uint(ex.y) - set_ge(yp.x, ex.x);
+                    const uint32_t cy = __float_as_uint(ey.y) - set_ge(yp.y, ey.x);
+                    wx += cx << (4 * k);
+                    wy += cy << (4 * k);
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c8 = cc + 4 * half;
+                    const uint32_t w = half ? wy : wx;
+                    if constexpr (BITS == 4) {
+                        uint16_t *d = reinterpret_cast<uint16_t *>(blk + 2 + 8 * c8 + 4 * h);
+                        d[0] = (uint16_t)w;
+                        d[1] = (uint16_t)(w >> 16);
+                    } else {
+                        // split the 8 nibble-held 3-bit codes into the 2-bit and 1-bit planes
+                        uint32_t lo = w & 0x33333333u;
+                        lo = (lo | (lo >> 2)) & 0x0F0F0F0Fu;
+                        lo = (lo | (lo >> 4)) & 0x00FF00FFu;
+                        lo = (lo | (lo >> 8)) & 0x0000FFFFu;
+                        uint32_t hi = (w >> 2) & 0x11111111u;
+                        hi = (hi | (hi >> 3)) & 0x03030303u;
+                        hi = (hi | (hi >> 6)) & 0x000F000Fu;
+                        hi = (hi | (hi >> 12)) & 0x000000FFu;
+                        *reinterpret_cast<uint16_t *>(blk + 2 + 4 * c8 + 2 * h) = (uint16_t)lo;
+                        blk[34 + 2 * c8 + h] = (uint8_t)hi;
+                    }
+                }
+            }
+        }
+        if (h == 0) *reinterpret_cast<uint16_t *>(blk) = n16;
+        __syncthreads();
+
+        // ---- store the tile
+        if (a.contiguous) {
+            uint8_t *dst = a.out + v0 * BB;
+            const int nbytes = nv * BB, nch = nbytes >> 4;
+            for (int c = threadIdx.x; c < nch; c += kEncThreads)
+                reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(sm_out)[c];
+            for (int q = (nch << 3) + threadIdx.x; q < (nbytes >> 1); q += kEncThreads)
+                reinterpret_cast<uint16_t *>(dst)[q] = reinterpret_cast<const uint16_t *>(sm_out)[q];
+        } else {
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            for (int r = warp * 16; r < min(nv, warp * 16 + 16); ++r) {
+                const int64_t di = a.dst_index ? a.dst_index[v0 + r] : (v0 + r);
+                uint16_t *d = reinterpret_cast<uint16_t *>(a.out + di * a.out_stride);
+                const uint16_t *s = reinterpret_cast<const uint16_t *>(sm_out + r * BB);
+                for (int q = lane; q < BB / 2; q += 32) d[q] = s[q];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Tensor-core variant for bf16 / fp16 inputs.
+//
+// H_128 = H_8 (x) H_16 in Sylvester order (element e = 16 i + j), so
+// u = H (D x) splits into a 16-point transform of each 16-element chunk c
+// (with the chunk's signs folded in) followed by an 8-point transform across
+// the chunks.  The first is a dense contraction: for 16 vectors at a time,
+// [16 vectors x 16 dims] x [16 dims x 16 outputs] per chunk, exact in one
+// mma.sync m16n8k16 (bf16/fp16 inputs times +-1, float32 accumulate).  The
+// A operand comes straight from the staged bf16 rows with ldmatrix (rows
+// padded to 272 bytes, conflict-free); the B operand (+-1 = H_16 D_c with
+// its output columns permuted so that thread t of a quad ends with outputs
+// 4t..4t+3) lives in registers.  The 8-point stage runs on the accumulator
+// registers, which already come in float2 pairs.
+// ---------------------------------------------------------------------------
+
+constexpr int kRowPitch = 272;              // 256-byte bf16 row + 16-byte pad
+constexpr int kWarpRows = 16;               // vectors per warp tile
+constexpr int kWarpStage = kWarpRows * kRowPitch;
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// d = a * b (fresh accumulator: the C operand is a zero register).
+template <int DT>
+__device__ __forceinline__ void mma_16816_zero(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    const float z = 0.f;
+    if constexpr (DT == TQ_BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%10, %10, %10, %10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%10, %10, %10, %10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ float elem_smem(const uint8_t *row, int j) {
+    const uint16_t b = reinterpret_cast<const uint16_t *>(row)[j];
+    if constexpr (DT == TQ_BF16) return __uint_as_float((uint32_t)b << 16);
+    else return __half2float(__ushort_as_half(b));
+}
+
+// Each warp is independent: it stages its own 16 rows (double buffered,
+// cp.async with zero fill past the end), transforms and quantises them, and
+// stores its own 16 blocks; warps never wait for each other.
+template <int BITS, int DT>
+__global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid_constant__ EncArgs a) {
+    constexpr int BB = BlockFmt<BITS>::kBytes;
+    constexpr int OUTB = (kWarpRows * BB + 15) & ~15;
+    constexpr int WARP_SMEM = 2 * kWarpStage + OUTB;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float2 *tab = reinterpret_cast<float2 *>(smem);                               // kBuckets entries
+    uint4 *bfrag = reinterpret_cast<uint4 *>(smem + kBuckets * sizeof(float2));    // [8][32]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    uint8_t *wsm = smem + kBuckets * sizeof(float2) + 8 * 32 * sizeof(uint4) + warp * WARP_SMEM;
+    uint8_t *sm_out = wsm + 2 * kWarpStage;
+
+    for (int j = threadIdx.x; j < kBuckets; j += kEncThreads) tab[j] = a.table[j];
+    // B fragments of lane l for chunk c: {nt0 k0-7, nt0 k8-15, nt1 k0-7, nt1 k8-15}; entry
+    // (k, n) = H16[o][k] * D[16c + k] with output column o = 4 (n >> 1) + 2 nt + (n & 1).
+    for (int q = threadIdx.x; q < 8 * 32; q += kEncThreads) {
+        const int c = q >> 5, l = q & 31, lg = l >> 2, lt = l & 3;
+        uint32_t w[4];
+        for (int nt = 0; nt < 2; ++nt)
+            for (int r = 0; r < 2; ++r) {
+                const int o = 4 * (lg >> 1) + 2 * nt + (lg & 1);
+                uint32_t pair = 0;
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 2 * lt + 8 * r + e, dim = 16 * c + k;
+                    const uint32_t neg = ((uint32_t)__popc(o & k) & 1u) ^ ((a.signs[dim >> 5] >> (dim & 31)) & 1u);
+                    const uint32_t one = DT == TQ_BF16 ? (neg ? 0xBF80u : 0x3F80u) : (neg ? 0xBC00u : 0x3C00u);
+                    pair |= one << (16 * e);
+                }
+                w[2 * nt + r] = pair;
+            }
+        bfrag[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+
+    const int64_t ntiles = (a.n_vec + kWarpRows - 1) / kWarpRows;
+    const int64_t nwarps = (int64_t)gridDim.x * (kEncThreads / 32);
+    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(wsm);
+    auto issue = [&](int buf, int64_t tl) {
+        const int64_t r0 = tl * kWarpRows;
+#pragma unroll
+        for (int q = lane; q < kWarpRows * 16; q += 32) {
+            const int r = q >> 4, col = q & 15;
+            const bool valid = r0 + r < a.n_vec;
+            const uint8_t *src = valid ? a.x + (r0 + r) * a.x_stride + col * 16 : a.x;
+            cp_async16_zfill(stage_s + buf * kWarpStage + r * kRowPitch + col * 16, src, valid);
+        }
+    };
+    int64_t tile = (int64_t)blockIdx.x * (kEncThreads / 32) + warp;
+    if (tile < ntiles) issue(0, tile);
+    cp_async_commit();
+    const float2 off2 = make_float2(12582976.f, 12582976.f);  // 64 + 1.5 * 2^23
+    const uint32_t tab_s = (uint32_t)__cvta_generic_to_shared(tab);
+    for (int it = 0; tile < ntiles; ++it, tile += nwarps) {
+        const int64_t next = tile + nwarps;
+        if (next < ntiles) issue((it + 1) & 1, next);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncwarp();
+        const int64_t v0 = tile * kWarpRows;
+        const int nv = (int)min64(kWarpRows, a.n_vec - v0);
+        const uint8_t *rows = wsm + (it & 1) * kWarpStage;
+        const uint32_t lrow = stage_s + (it & 1) * kWarpStage + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kRowPitch +
+                              (lane >> 4) * 16;
+
+        // ---- 16-point stage on the tensor cores
+        float acc[8][2][4];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t af[4];
+            ldsm_x4(lrow + c * 32, af);
+            const uint4 b = bfrag[c * 32 + lane];
+            mma_16816_zero<DT>(acc[c][0], af, b.x, b.y);
+            mma_16816_zero<DT>(acc[c][1], af, b.z, b.w);
+        }
+        // ---- 8-point stage across chunks, on the accumulator pairs
+        float2 u[8][2][2];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                u[c][nt][0] = make_float2(acc[c][nt][0], acc[c][nt][1]);
+                u[c][nt][1] = make_float2(acc[c][nt][2], acc[c][nt][3]);
+            }
+#pragma unroll
+        for (int L = 1; L < 8; L <<= 1)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                if ((c & L) == 0)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int vh = 0; vh < 2; ++vh) {
+                            const float2 x = u[c][nt][vh], y = u[c + L][nt][vh];
+                            u[c][nt][vh] = __fadd2_rn(x, y);
+                            u[c + L][nt][vh] = sub2x(x, y);
+                        }
+        // u[i][nt][vh] = (u_e, u_{e+1}), e = 16 i + 4 t + 2 nt, of row g + 8 vh.
+
+        // ---- norms (sum of squares of u = 128 ||x||^2), one per row half
+        float ss[2];
+#pragma unroll
+        for (int vh = 0; vh < 2; ++vh) {
+            float2 q2 = __fmul2_rn(u[0][0][vh], u[0][0][vh]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                    if (c | nt) q2 = __ffma2_rn(u[c][nt][vh], u[c][nt][vh], q2);
+            float v = q2.x + q2.y;
+            v += __shfl_xor_sync(kFull, v, 1);
+            v += __shfl_xor_sync(kFull, v, 2);
+            ss[vh] = v;
+        }
+        unsigned short n16[2];
+        float sc[2];
+        bool near[2], oor[2];
+#pragma unroll
+        for (int vh = 0; vh < 2; ++vh) {
+            oor[vh] = !(ss[vh] >= 1.0097419586828951e-28f /* 128 * 2^-100 */ && ss[vh] <= 1.2676506002282294e30f);
+            sc[vh] = sqrtf(ss[vh]);
+            const float n = sc[vh] * 0.08838834764831845f;
+            n16[vh] = __half_as_ushort(__float2half_rn(n));
+            near[vh] = !oor[vh] && near_fp16_tie(n, 9.5367431640625e-07f);
+        }
+        if (__any_sync(kFull, near[0] || near[1] || oor[0] || oor[1])) {
+            // exact norms from the staged rows: lane t of the quad sums elements 32t..32t+31
+#pragma unroll
+            for (int vh = 0; vh < 2; ++vh) {
+                const uint8_t *row = rows + (g + 8 * vh) * kRowPitch;
+                SumSq2 part;
+                double pd = 0.0;
+                for (int j = 32 * t; j < 32 * t + 32; ++j) {
+                    const float xv = elem_smem<DT>(row, j);
+                    part.add(xv);
+                    pd = fma((double)xv, (double)xv, pd);
+                }
+                float s1 = part.s, c1 = part.c;
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    const float os = __shfl_xor_sync(kFull, s1, o), oc = __shfl_xor_sync(kFull, c1, o);
+                    float ns, ne;
+                    two_sum(s1, os, ns, ne);
+                    s1 = ns;
+                    c1 = c1 + oc + ne;
+                    pd += __shfl_xor_sync(kFull, pd, o);
+                }
+                if (near[vh]) {
+                    SumSq2 tot;
+                    tot.s = s1;
+                    tot.c = c1;
+                    n16[vh] = tot.sqrt_fp16();
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        amax = fmaxf(amax, fmaxf(fabsf(u[c][nt][vh].x), fabsf(u[c][nt][vh].y)));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+                if (oor[vh]) {
+                    n16[vh] = __half_as_ushort(__double2half(sqrt(pd)));
+                    if (amax > 0.f && amax < INFINITY) {
+                        int e;
+                        frexpf(amax, &e);
+                        const int e1 = -e / 2, e2 = -e - e1;
+                        const float2 f1 = make_float2(ldexpf(1.f, e1), ldexpf(1.f, e1));
+                        const float2 f2 = make_float2(ldexpf(1.f, e2), ldexpf(1.f, e2));
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt)
+                                u[c][nt][vh] = __fmul2_rn(__fmul2_rn(u[c][nt][vh], f1), f2);
+                    }
+                }
+                float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) q2 = __ffma2_rn(u[c][nt][vh], u[c][nt][vh], q2);
+                float v = q2.x + q2.y;
+                v += __shfl_xor_sync(kFull, v, 1);
+                v += __shfl_xor_sync(kFull, v, 2);
+                if (oor[vh]) sc[vh] = (v > 0.f && v < INFINITY) ? sqrtf(v) : 1.f;
+            }
+        }
+
+        // ---- quantise and pack (four consecutive elements per thread and 16-block)
+#pragma unroll
+        for (int vh = 0; vh < 2; ++vh) {
+            const float cs = a.grid / sc[vh];
+            const float2 cs2 = make_float2(cs, cs);
+            uint8_t *blk = sm_out + (g + 8 * vh) * BB;
+            uint32_t hnib[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t code4[4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float2 yp = __fmul2_rn(u[i][nt][vh], cs2);
+                    const float2 tt = __fadd2_rn(yp, off2);
+                    // cell index = low 7 bits (masked: any input stays inside the table)
+                    const float2 ex = lds_f2(tab_s + (__float_as_uint(tt.x) & (kBuckets - 1)) * 8u);
+                    const float2 ey = lds_f2(tab_s + (__float_as_uint(tt.y) & (kBuckets - 1)) * 8u);
+                    code4[2 * nt] = __float_as_uint(ex.y) + (yp.x >= ex.x ? 1u : 0u);
+                    code4[2 * nt + 1] = __float_as_uint(ey.y) + (yp.y >= ey.x ? 1u : 0u);
+                }
+                if constexpr (BITS == 4) {
+                    const uint32_t w = code4[0] + code4[1] * 16u + code4[2] * 256u + code4[3] * 4096u;
+                    *reinterpret_cast<uint16_t *>(blk + 2 + 8 * i + 2 * t) = (uint16_t)w;
+                } else if constexpr (BITS == 2) {
+                    blk[2 + 4 * i + t] = (uint8_t)(code4[0] + code4[1] * 4u + code4[2] * 16u + code4[3] * 64u);
+                } else {
+                    blk[2 + 4 * i + t] = (uint8_t)((code4[0] & 3u) | ((code4[1] & 3u) << 2) | ((code4[2] & 3u) << 4) |
+                                                   ((code4[3] & 3u) << 6));
+                    hnib[i] = (code4[0] >> 2) | ((code4[1] >> 2) << 1) | ((code4[2] >> 2) << 2) | ((code4[3] >> 2) << 3);
+                }
+            }
+            if constexpr (BITS == 3) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t other = __shfl_xor_sync(kFull, hnib[i], 1);
+                    if ((t & 1) == 0) blk[34 + 2 * i + (t >> 1)] = (uint8_t)(hnib[i] | (other << 4));
+                }
+            }
+            if (t == 0) *reinterpret_cast<uint16_t *>(blk) = n16[vh];
+        }
+        __syncwarp();
+
+        // ---- store this warp's 16 blocks (16 * BB bytes, 16-byte aligned when contiguous)
+        if (a.contiguous) {
+            uint8_t *dst = a.out + v0 * BB;
+            const int nbytes = nv * BB, nch = nbytes >> 4;
+            for (int c = lane; c < nch; c += 32)
+                reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(sm_out)[c];
+            for (int q = (nch << 3) + lane; q < (nbytes >> 1); q += 32)
+                reinterpret_cast<uint16_t *>(dst)[q] = reinterpret_cast<const uint16_t *>(sm_out)[q];
+        } else {
+            for (int r = 0; r < nv; ++r) {
+                const int64_t di = a.dst_index ? a.dst_index[v0 + r] : (v0 + r);
+                uint16_t *d = reinterpret_cast<uint16_t *>(a.out + di * a.out_stride);
+                const uint16_t *s2p = reinterpret_cast<const uint16_t *>(sm_out + r * BB);
+                for (int q = lane; q < BB / 2; q += 32) d[q] = s2p[q];
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+}
+
+template <int BITS, int DT>
+int launch_mma(const EncArgs &a, cudaStream_t st) {
+    static int per_sm[64] = {0};
+    static int smem_set[64] = {0};
+    const int smem = kBuckets * (int)sizeof(float2) + 8 * 32 * 16 +
+                     (kEncThreads / 32) * (2 * kWarpStage + ((kWarpRows * BlockFmt<BITS>::kBytes + 15) & ~15));
+    if (set_smem_limit((const void *)encode_mma_kernel<BITS, DT>, smem, smem_set) != TQ_OK) return TQ_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    int occ = dev < 64 ? per_sm[dev] : 0;
+    if (occ == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_mma_kernel<BITS, DT>, kEncThreads, smem) !=
+                cudaSuccess ||
+            occ < 1)
+            occ = 1;
+        if (dev < 64) per_sm[dev] = occ;
+    }
+    const int64_t ntiles = (a.n_vec + kWarpRows - 1) / kWarpRows;
+    const int64_t cta_tiles = (ntiles + (kEncThreads / 32) - 1) / (kEncThreads / 32);
+    const int grid = (int)std::min<int64_t>(cta_tiles, (int64_t)occ * sm_count());
+    encode_mma_kernel<BITS, DT><<<grid, kEncThreads, smem, st>>>(a);
+    return launch_status();
+}
+
+template <int BITS, int DT>
+int launch(const EncArgs &a, cudaStream_t st) {
+    static int per_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    int occ = dev < 64 ? per_sm[dev] : 0;
+    if (occ == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_kernel<BITS, DT>, kEncThreads, 0) !=
+                cudaSuccess ||
+            occ < 1)
+            occ = 1;
+        if (dev < 64) per_sm[dev] = occ;
+    }
+    const int64_t ntiles = (a.n_vec + kEncVecs - 1) / kEncVecs;
+    const int grid = (int)std::min<int64_t>(ntiles, (int64_t)occ * sm_count());
+    encode_kernel<BITS, DT><<<grid, kEncThreads, 0, st>>>(a);
+    return launch_status();
+}
+
+// Cell table of a codebook.  With z = G y, cell j holds
+// z + 64 in [j - 1/2, j + 1/2); G is the smallest integer above
+// 1 / (smallest gap between adjacent boundaries), so no cell holds two
+// boundaries, and G <= 62 keeps |z| <= G (|y| <= 1) inside the table.
+void build_table(const tq_codebook *cb, EncArgs *a) {
+    const int L = 1 << cb->bits;
+    double gap = 1.0;
+    for (int i = 0; i + 1 < L - 1; ++i)
+        gap = std::min(gap, (double)cb->boundaries[i + 1] - (double)cb->boundaries[i]);
+    const float G = (float)std::min(62.0, std::floor(1.0 / gap) + 1.0);
+    a->grid = G;
+    for (int j = 0; j < kBuckets; ++j) {
+        int below = 0;
+        float inner = INFINITY;
+        for (int i = 0; i < L - 1; ++i) {
+            const float z = G * cb->boundaries[i];
+            if (z + 64.f < j - 0.5f) ++below;
+            else if (z + 64.f < j + 0.5f) inner = z;
+        }
+        const uint32_t code = (uint32_t)below;
+        float codef;
+        memcpy(&codef, &code, 4);
+        a->table[j] = make_float2(inner, codef);
+    }
+}
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
+                            const tq_codebook *cb, tq_signs signs, uint8_t *blocks,
+                            int64_t block_stride_bytes, const int64_t *dst_index, void *stream) {
+    if (n_vec < 0 || !cb) return TQ_ERR_ARG;
+    if (!codebook_ok(cb) || dtype_bytes(x_dtype) == 0) return TQ_ERR_UNSUPPORTED;
+    if (n_vec == 0) return TQ_OK;
+    const int es = dtype_bytes(x_dtype);
+    const int64_t bb = (int64_t)tq_block_bytes(cb->bits);
+    if (!x || !blocks || x_stride_elems < kD || block_stride_bytes < bb) return TQ_ERR_ARG;
+    if (!aligned(x, 16) || (x_stride_elems * es) % 16 || !aligned(blocks, 2) || (block_stride_bytes & 1))
+        return TQ_ERR_ALIGN;
+    EncArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = static_cast<const uint8_t *>(x);
+    a.n_vec = n_vec;
+    a.x_stride = x_stride_elems * es;
+    a.out = blocks;
+    a.out_stride = block_stride_bytes;
+    a.dst_index = dst_index;
+    a.contiguous = (!dst_index && block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
+    a.b0 = cb->boundaries[(1 << cb->bits) / 2];
+    build_table(cb, &a);
+    for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (cb->bits * 8 + x_dtype) {
+        case 2 * 8 + TQ_F32: return launch<2, TQ_F32>(a, st);
+        case 2 * 8 + TQ_BF16: return launch_mma<2, TQ_BF16>(a, st);
+        case 2 * 8 + TQ_F16: return launch_mma<2, TQ_F16>(a, st);
+        case 3 * 8 + TQ_F32: return launch<3, TQ_F32>(a, st);
+        case 3 * 8 + TQ_BF16: return launch_mma<3, TQ_BF16>(a, st);
+        case 3 * 8 + TQ_F16: return launch_mma<3, TQ_F16>(a, st);
+        case 4 * 8 + TQ_F32: return launch<4, TQ_F32>(a, st);
+        case 4 * 8 + TQ_BF16: return launch_mma<4, TQ_BF16>(a, st);
+        case 4 * 8 + TQ_F16: return launch_mma<4, TQ_F16>(a, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}

@@ -19,6 +19,9 @@ inline int dtype_bytes(int dt) {
     }
 }
 
+// Codebook sanity (head_dim 128, bits 2..4, levels 2^bits).
+bool codebook_ok(const tq_codebook *cb);
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
