@@ -4,6 +4,7 @@
 #include <cmath>
 
 #include "tq_attn.cuh"
+#include "tq_attn_mma.h"
 #include "tq_internal.h"
 
 namespace tq {
@@ -47,6 +48,39 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_kernel(const float 
     out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -v : v;
 }
 
+// Merge for the tensor-core kernel's partition: the slots of segment
+// j = (sequence, KV head) are the CTAs that touched it.
+__global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const float *ws, MmaPlan plan, int Hq,
+                                                                        int Hkv, uint32_t s0, uint32_t s1,
+                                                                        uint32_t s2, uint32_t s3, float *out) {
+    __shared__ float buf[kD];
+    const int d = threadIdx.x;
+    const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
+    const int G = Hq / Hkv;
+    const int64_t j = (int64_t)b * Hkv + h / G;
+    const int64_t first = mma_cta_of_chunk(j * plan.C, plan);
+    const int nslots = (int)(mma_cta_of_chunk((j + 1) * plan.C - 1, plan) - first + 1);
+    const float *base = ws + (int64_t)blockIdx.x * plan.Smax * kPartialFloats;
+    float M = -INFINITY;
+    for (int s = 0; s < nslots; ++s) M = fmaxf(M, base[s * kPartialFloats]);
+    float l = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < nslots; ++s) {
+            const float m = base[s * kPartialFloats];
+            if (m == -INFINITY) continue;
+            const float w = exp2f(m - M);
+            l = fmaf(w, base[s * kPartialFloats + 1], l);
+            acc = fmaf(w, base[s * kPartialFloats + 4 + d], acc);
+        }
+    }
+    buf[d] = l > 0.f ? acc / l : 0.f;
+    __syncthreads();
+    smem_fwht_rows<1>(buf);
+    const uint32_t sw[4] = {s0, s1, s2, s3};
+    const float v = buf[d] * 0.08838834764831845f;
+    out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -v : v;
+}
+
 static int attn_smem_bytes(int kb, int vb) {
     const int head = (1040 * 2 + 8 * kD + kTT * 8 + 8 * 4 + 32) * 4;
     const int kbb = 2 + 16 * kb, vbb = vb == 16 ? 256 : 2 + 16 * vb;
@@ -62,7 +96,9 @@ extern "C" size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv) return 0;
     int splits, tps;
     attn_split_plan(B, Hkv, T_cap, &splits, &tps);
-    return (size_t)B * Hq * splits * kPartialFloats * sizeof(float);
+    const MmaPlan mp = mma_plan(B, Hkv, T_cap);
+    const int slots = splits > mp.Smax ? splits : mp.Smax;
+    return (size_t)B * Hq * slots * kPartialFloats * sizeof(float);
 }
 
 extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
@@ -115,6 +151,14 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     const int smem = attn_smem_bytes(kb, vb);
     cudaStream_t st = (cudaStream_t)stream;
     dim3 grid(a.splits, Hkv, B);
+    if (attn_mma_supported(kb, vb, qjl)) {
+        const MmaPlan mp = mma_plan(B, Hkv, T);
+        int r = launch_attn_mma(a, mp, st);
+        if (r != TQ_OK) return r;
+        attn_combine_mma_kernel<<<B * Hq, kAttnThreads, 0, st>>>(a.ws, mp, Hq, Hkv, signs.w[0], signs.w[1],
+                                                                  signs.w[2], signs.w[3], out);
+        return launch_status();
+    }
     int r;
     if (G == 1) r = launch_attn_split_g1(kb, vb, a, grid, smem, st);
     else if (G == 2) r = launch_attn_split_g2(kb, vb, a, grid, smem, st);
