@@ -1,23 +1,39 @@
 """Benchmark of the TurboQuant KV hot path on GB300.
 
-One step = quantise-on-insert of the whole K and V cache (tq_encode_kv: K
-4-bit, V 2-bit) followed by one fused decode-attention step over it
-(tq_attn_decode), on the Llama-3-8B-shaped decode workload: batch 16,
-32 query heads, 8 KV heads, head_dim 128, context 8192, bf16 K/V with
-log-normal channel scales and AR(1) token correlation 0.9.
+Default workload (``--workload llama3_8b_decode``): one step = quantise-on-
+insert of the whole K and V cache (tq_encode_kv: K 4-bit, V 2-bit) followed
+by one fused decode-attention step over it (tq_attn_decode), Llama-3-8B
+shaped: batch 16, 32 query heads, 8 KV heads, head_dim 128, context 8192,
+bf16 K/V with log-normal channel scales and AR(1) token correlation 0.9.
 
-`value` is the algorithmic bytes of a step (K/V bf16 in + packed blocks out,
-packed blocks + q in + fp32 out) over the device time of a step, in GB/s.
-`e2e` is the same bytes over the time of a step run through the C ABI from
-pinned host buffers (host->device copy of K, V and q, the step, and the
-device->host copy of the output inside the timed region).
+Other workloads (one JSON line each, same keys):
+
+* ``single_head_fp32``   -- one head, 4096 fp32 K/V rows, K4/V2, one query;
+* ``qwen25_7b_append``   -- batch 64, 28/4 heads, context 32768 bf16 with 1%
+                            outlier channels, K3/V3: encode the prefix into a
+                            [B, Hkv, T_cap] cache through a destination index,
+                            append one token per sequence, attend over 32769;
+* ``qjl_two_term``       -- batch 8, 32/8 heads, context 16384: K3 encode,
+                            QJL sign bits + residual norms, attention with the
+                            two-term score and raw fp16 values;
+* ``storage_roundtrip``  -- [2, 32, 65536, 1024] bf16: serialise (4 raw
+                            layers, 28 layers K4/V4 in 132-byte slots) and
+                            deserialise.
+
+`value` is the algorithmic bytes of a step (what the method must move:
+inputs read and outputs written by each call) over the device time of a
+step, in GB/s.  `e2e` is the same bytes over the time of a step run through
+the C ABI from pinned host buffers (host->device copy of the inputs, the
+step, and the device->host copy of the result inside the timed region).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                       [--workload NAME]
 Under torchrun each rank runs an independent replica on its own GPU (weak
 scaling; the path has no exchange step); rank 0 prints one JSON line.
 """
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -33,12 +49,40 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "compressed-KV decode-attention GB/s & % HBM peak; encode Gvec/s (1xGB300)"
-WORKLOAD = dict(workload="llama3_8b_decode", B=16, Hq=32, Hkv=8, T=8192, head_dim=128,
-                key_bits=4, value_bits=2, kv_dtype="bf16", scale="1/sqrt(128)")
+DEFAULT_WORKLOAD = "llama3_8b_decode"
+WORKLOADS = {
+    "llama3_8b_decode": dict(B=16, Hq=32, Hkv=8, T=8192, head_dim=128, key_bits=4, value_bits=2,
+                             kv_dtype="bf16", scale="1/sqrt(128)"),
+    "single_head_fp32": dict(B=1, Hq=1, Hkv=1, T=4096, head_dim=128, key_bits=4, value_bits=2,
+                             kv_dtype="fp32", scale="1/sqrt(128)"),
+    "qwen25_7b_append": dict(B=64, Hq=28, Hkv=4, T=32769, T_cap=32776, head_dim=128, key_bits=3, value_bits=3,
+                             kv_dtype="bf16", outlier_channels="5 of 512 x20", append_tokens=1,
+                             scale="1/sqrt(128)"),
+    "qjl_two_term": dict(B=8, Hq=32, Hkv=8, T=16384, head_dim=128, key_bits=3, value="fp16 raw", qjl_m=128,
+                         kv_dtype="bf16 keys / fp16 values", scale="1/sqrt(128)"),
+    "storage_roundtrip": dict(layout="[2, 32, 65536, 1024]", L=32, T=65536, hidden=1024, head_dim=128,
+                              block_size=16, skip_first=2, skip_last=2, key_bits=4, value_bits=4, slot_bytes=132,
+                              kv_dtype="bf16"),
+}
 FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "turboquant_bit_kv_gb300", "csrc")
+# the sources each kernel group is built from (profiled DRAM traffic is only
+# reported while these are unchanged since the capture)
+KERNEL_SOURCES = {
+    "encode": ["tq_encode.cu", "tq_device.cuh"],
+    "append": ["tq_encode.cu", "tq_device.cuh"],
+    "attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_g1.cu",
+                  "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
+    "qjl": ["tq_codec.cu", "tq_device.cuh"],
+    "serialize": ["tq_encode.cu", "tq_codec.cu", "tq_device.cuh"],
+    "deserialize": ["tq_codec.cu", "tq_device.cuh"],
+}
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
 
 def step_bytes(B, Hq, Hkv, T, kbits=4, vbits=2):
+    """Algorithmic bytes of the decode step: encode K and V (bf16 rows in,
+    blocks out) and one attention step (blocks, bf16 q in, fp32 out)."""
     nvec = B * Hkv * T
     kbb, vbb = 2 + 16 * kbits, 2 + 16 * vbits
     enc_k = nvec * 128 * 2 + nvec * kbb
@@ -54,6 +98,34 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha(group):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[group]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, group):
+    """DRAM bytes (read + write) per step of a kernel group, from the ncu
+    table under profiles/, or None when absent or when the group's sources
+    changed since the capture."""
+    try:
+        with open(TRAFFIC_TABLE) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == group:
+            try:
+                val = int(cells[2].replace(",", ""))
+            except ValueError:
+                return None
+            return val if cells[3] == source_sha(group) else None
+    return None
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -126,32 +198,278 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ---------------------------------------------------------------- GPU arm
+# ---------------------------------------------------------------- workload plans (GPU arm)
 
-def run_gpu(args, rank, world, local_rank):
-    from turboquant_bit_kv_gb300 import tq, workloads
+class Op:
+    """One call of the path inside a step: `fn()` launches it on the bench
+    stream; `nbytes` is its algorithmic bytes, `launches` the kernels of this
+    library it launches, `nvec` the 128-element vectors it encodes/decodes."""
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    W = WORKLOAD
-    B, Hq, Hkv, T = args.batch or W["B"], W["Hq"], W["Hkv"], W["T"]
+    def __init__(self, name, group, fn, nbytes, launches, nvec=0):
+        self.name, self.group, self.fn, self.nbytes, self.launches, self.nvec = \
+            name, group, fn, nbytes, launches, nvec
+
+
+def _pinned(t):
+    return t.cpu().pin_memory()
+
+
+def plan_llama(tq, wl, dev, stream, seed, batch):
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS["llama3_8b_decode"]
+    B, Hq, Hkv, T = batch or W["B"], W["Hq"], W["Hkv"], W["T"]
     nb = step_bytes(B, Hq, Hkv, T)
     kcb, vcb = tq.tq_codebook_load(128, 4), tq.tq_codebook_load(128, 2)
     signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
-    data = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=args.seed + rank, device=dev)
+    data = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=seed, device=dev)
     k, v, q = data["k"], data["v"], data["q"]
     kb = torch.empty((B, Hkv, T, tq.tq_block_bytes(4)), dtype=torch.uint8, device=dev)
     vb = torch.empty((B, Hkv, T, tq.tq_block_bytes(2)), dtype=torch.uint8, device=dev)
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
     ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
     scale = 1.0 / np.sqrt(128.0)
+    nvec = B * Hkv * T
+
+    def attn(qq=q):
+        tq.tq_attn_decode(qq, kb, kcb, vb, vcb, out, ws, T, scale, signs, stream=stream)
+
+    ops = [Op("encode_k", "encode", lambda: tq.tq_encode_kv(k.view(-1, 128), kcb, signs, kb, stream=stream),
+              nb["enc_k"], 1, nvec),
+           Op("encode_v", "encode", lambda: tq.tq_encode_kv(v.view(-1, 128), vcb, signs, vb, stream=stream),
+              nb["enc_v"], 1, nvec),
+           Op("attention", "attention", attn, nb["attn"], 2)]
+
+    def e2e():
+        hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+
+        def step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            tq.tq_encode_kv(dk.view(-1, 128), kcb, signs, kb, stream=stream)
+            tq.tq_encode_kv(dv.view(-1, 128), vcb, signs, vb, stream=stream)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, k.numel() * 2 + v.numel() * 2 + q.numel() * 2, out.numel() * 4
+
+    cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2 (129 MB); attention also timed after an L2 flush")
+    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="bf16")
+
+
+def plan_single_head(tq, wl, dev, stream, seed, batch):
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS["single_head_fp32"]
+    T = W["T"]
+    kcb, vcb = tq.tq_codebook_load(128, 4), tq.tq_codebook_load(128, 2)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    data = workloads.single_head(T=T, seed=seed, device=dev)
+    k, v = data["k"], data["v"]
+    q = data["q"].view(1, 1, 128)
+    kb = torch.empty((1, 1, T, 66), dtype=torch.uint8, device=dev)
+    vb = torch.empty((1, 1, T, 34), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, 1, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(1, 1, 1, T), dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(128.0)
+
+    def attn(qq=q):
+        tq.tq_attn_decode(qq, kb, kcb, vb, vcb, out, ws, T, scale, signs, stream=stream)
+
+    ops = [Op("encode_k", "encode", lambda: tq.tq_encode_kv(k, kcb, signs, kb, stream=stream), T * (512 + 66),
+              1, T),
+           Op("encode_v", "encode", lambda: tq.tq_encode_kv(v, vcb, signs, vb, stream=stream), T * (512 + 34),
+              1, T),
+           Op("attention", "attention", attn, T * 100 + 512 + 512, 2)]
+
+    def e2e():
+        hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+
+        def step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            tq.tq_encode_kv(dk, kcb, signs, kb, stream=stream)
+            tq.tq_encode_kv(dv, vcb, signs, vb, stream=stream)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (k.numel() + v.numel() + q.numel()) * 4, out.numel() * 4
+
+    cfg = dict(W, l2="inputs (4.6 MB) fit in L2: launch-bound, report microseconds")
+    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="f32")
+
+
+def plan_qwen(tq, wl, dev, stream, seed, batch):
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS["qwen25_7b_append"]
+    B, Hq, Hkv, T, T_cap = batch or W["B"], W["Hq"], W["Hkv"], W["T"], W["T_cap"]
+    cb = tq.tq_codebook_load(128, 3)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    data = workloads.qwen_outlier(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=seed, device=dev)
+    q = data["q"]
+    pre = {n: data[n][:, :, :T - 1].contiguous().view(-1, 128) for n in ("k", "v")}
+    new = {n: data[n][:, :, T - 1].contiguous().view(-1, 128) for n in ("k", "v")}
+    del data
+    torch.cuda.empty_cache()
+    bh = torch.arange(B * Hkv, device=dev, dtype=torch.int64)
+    dst_pre = (bh[:, None] * T_cap + torch.arange(T - 1, device=dev, dtype=torch.int64)[None, :]).reshape(-1)
+    dst_new = bh * T_cap + (T - 1)
+    blk = {n: torch.zeros((B, Hkv, T_cap, 50), dtype=torch.uint8, device=dev) for n in ("k", "v")}
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T_cap), dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(128.0)
+    n_pre, n_new = B * Hkv * (T - 1), B * Hkv
+
+    def enc(x, n, dst):
+        return lambda: tq.tq_encode_kv(x, cb, signs, blk[n], dst_index=dst, stream=stream)
+
+    def attn(qq=q):
+        tq.tq_attn_decode(qq, blk["k"], cb, blk["v"], cb, out, ws, T, scale, signs, stream=stream)
+
+    ops = [Op("encode_k", "encode", enc(pre["k"], "k", dst_pre), n_pre * (256 + 50), 1, n_pre),
+           Op("encode_v", "encode", enc(pre["v"], "v", dst_pre), n_pre * (256 + 50), 1, n_pre),
+           Op("append_k", "append", enc(new["k"], "k", dst_new), n_new * (256 + 50), 1, n_new),
+           Op("append_v", "append", enc(new["v"], "v", dst_new), n_new * (256 + 50), 1, n_new),
+           Op("attention", "attention", attn, B * Hkv * T * 100 + B * Hq * 128 * (2 + 4), 2)]
+
+    def e2e():
+        hk, hv = _pinned(pre["k"]), _pinned(pre["v"])
+        hnk, hnv, hq = _pinned(new["k"]), _pinned(new["v"]), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv = torch.empty_like(pre["k"]), torch.empty_like(pre["v"])
+        dnk, dnv, dq = torch.empty_like(new["k"]), torch.empty_like(new["v"]), torch.empty_like(q)
+
+        def step():
+            for d, h in ((dk, hk), (dv, hv), (dnk, hnk), (dnv, hnv), (dq, hq)):
+                d.copy_(h, non_blocking=True)
+            enc(dk, "k", dst_pre)()
+            enc(dv, "v", dst_pre)()
+            enc(dnk, "k", dst_new)()
+            enc(dnv, "v", dst_new)()
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (2 * (n_pre + n_new) * 128 + q.numel()) * 2, out.numel() * 4
+
+    cfg = dict(W, B=B, l2="inputs (4.3 GB) larger than L2; attention also timed after an L2 flush",
+               note="destination-index reads (8 B per vector) are not counted as algorithmic bytes")
+    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="bf16")
+
+
+def plan_qjl(tq, wl, dev, stream, seed, batch):
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS["qjl_two_term"]
+    B, Hq, Hkv, T = batch or W["B"], W["Hq"], W["Hkv"], W["T"]
+    cb = tq.tq_codebook_load(128, 3)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    data = workloads.qjl_keys(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=seed, device=dev)
+    k, v, q, S = data["k"], data["v"], data["q"], data["S"]
+    n = B * Hkv * T
+    kb = torch.empty((B, Hkv, T, 50), dtype=torch.uint8, device=dev)
+    bits = torch.empty((B, Hkv, T, 16), dtype=torch.uint8, device=dev)
+    rn = torch.empty((B, Hkv, T), dtype=torch.int16, device=dev)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(128.0)
+
+    def enc(kk):
+        tq.tq_encode_kv(kk.view(-1, 128), cb, signs, kb, stream=stream)
+
+    def qjl(kk):
+        tq.tq_qjl_encode(kk.view(-1, 128), kb.view(-1, 50), cb, signs, S, bits.view(-1, 16), rn.view(-1),
+                         stream=stream)
+
+    def attn(qq=q, vv=v):
+        tq.tq_attn_decode(qq, kb, cb, vv, None, out, ws, T, scale, signs, qjl_bits=bits, res_norm_f16=rn, S=S,
+                          stream=stream)
+
+    ops = [Op("encode_k", "encode", lambda: enc(k), n * (256 + 50), 1, n),
+           Op("qjl_encode", "qjl", lambda: qjl(k), n * (256 + 50 + 16 + 2) + 128 * 128 * 4, 1, n),
+           Op("attention", "attention", attn, n * (50 + 16 + 2 + 256) + B * Hq * 128 * (2 + 4) + 128 * 128 * 4, 2)]
+
+    def e2e():
+        hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+
+        def step():
+            for d, h in ((dk, hk), (dv, hv), (dq, hq)):
+                d.copy_(h, non_blocking=True)
+            enc(dk)
+            qjl(dk)
+            attn(dq, dv)
+            hout.copy_(out, non_blocking=True)
+        return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
+
+    cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2; attention also timed after an L2 flush",
+               note="QJL sketch S: seeded 128x128 N(0,1) float32; resident on the device")
+    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="bf16")
+
+
+def plan_storage(tq, wl, dev, stream, seed, batch):
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS["storage_roundtrip"]
+    L, T, hidden, bs, sf, sl = W["L"], W["T"], W["hidden"], W["block_size"], W["skip_first"], W["skip_last"]
+    if batch:
+        T = batch * 1024                  # smaller cases for profiling
+    cb = tq.tq_codebook_load(128, 4)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    x = workloads.storage_kv(L=L, T=T, hidden=hidden, seed=seed, device=dev)["kv"]
+    size = tq.tq_serde_size(L, T, hidden, bs, sf, sl, 4, 4)
+    buf = torch.empty(size, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    Lc = L - sf - sl
+    nvec = 2 * Lc * T * (hidden // 128)
+    each_way = x.numel() * 2 + size
+
+    def ser(src=x):
+        tq.tq_serde_serialize(src, cb, cb, signs, buf, block_size=bs, skip_first=sf, skip_last=sl, stream=stream)
+
+    def des(dst=y):
+        tq.tq_serde_deserialize(buf, cb, cb, signs, dst, block_size=bs, skip_first=sf, skip_last=sl,
+                                stream=stream)
+
+    ops = [Op("serialize", "serialize", ser, each_way, 2, nvec),
+           Op("deserialize", "deserialize", des, each_way, 2 * Lc, nvec)]
+
+    def e2e():
+        hx = _pinned(x)
+        hy = torch.empty_like(x, device="cpu").pin_memory()
+        dx, dy = torch.empty_like(x), torch.empty_like(x)
+
+        def step():
+            dx.copy_(hx, non_blocking=True)
+            ser(dx)
+            des(dy)
+            hy.copy_(dy, non_blocking=True)
+        return step, x.numel() * 2, x.numel() * 2
+
+    cfg = dict(W, T=T, l2="inputs (8.6 GB) larger than L2",
+               note="raw layers are device-to-device copies; per way: tensor bytes + serialised bytes")
+    return dict(ops=ops, cold=None, e2e=e2e, config=cfg, dtype="bf16")
+
+
+PLANS = {"llama3_8b_decode": plan_llama, "single_head_fp32": plan_single_head, "qwen25_7b_append": plan_qwen,
+         "qjl_two_term": plan_qjl, "storage_roundtrip": plan_storage}
+
+
+def _mean_ms(evs, a, b):
+    return statistics.mean(e[a].elapsed_time(e[b]) for e in evs)
+
+
+def run_gpu(args, rank, world, local_rank):
+    from turboquant_bit_kv_gb300 import tq
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream(dev)
-    kf, vf = k.view(-1, 128), v.view(-1, 128)
+    plan = PLANS[args.workload](tq, args.workload, dev, stream, args.seed + rank, args.batch)
+    ops = plan["ops"]
 
     def step():
-        tq.tq_encode_kv(kf, kcb, signs, kb, stream=stream)
-        tq.tq_encode_kv(vf, vcb, signs, vb, stream=stream)
-        tq.tq_attn_decode(q, kb, kcb, vb, vcb, out, ws, T, scale, signs, stream=stream)
+        for op in ops:
+            op.fn()
 
     for _ in range(args.warmup):
         step()
@@ -163,8 +481,8 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         return None
 
-    # timed region: per-kernel events on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # timed region: an event after every call, on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -176,57 +494,41 @@ def run_gpu(args, rank, world, local_rank):
     for i in range(args.steps):
         e = evs[i]
         e[0].record(stream)
-        tq.tq_encode_kv(kf, kcb, signs, kb, stream=stream)
-        e[1].record(stream)
-        tq.tq_encode_kv(vf, vcb, signs, vb, stream=stream)
-        e[2].record(stream)
-        tq.tq_attn_decode(q, kb, kcb, vb, vcb, out, ws, T, scale, signs, stream=stream)
-        e[3].record(stream)
+        for j, op in enumerate(ops):
+            op.fn()
+            e[j + 1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    ms_step = reduce_max(ms_total / args.steps, world)
-    enc_k_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    enc_v_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    ms_step = reduce_max(t0.elapsed_time(t1) / args.steps, world)
+    op_ms = [_mean_ms(evs, j, j + 1) for j in range(len(ops))]
 
-    # attention alone with a cold L2 (the cache was just written by the encode)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cold = []
-    for _ in range(min(max(3, args.steps), 50)):
-        flush.zero_()
-        a0.record(stream)
-        tq.tq_attn_decode(q, kb, kcb, vb, vcb, out, ws, T, scale, signs, stream=stream)
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        cold.append(a0.elapsed_time(a1))
-    attn_cold_ms = statistics.median(cold)
-    del flush
+    # the attention call alone with a cold L2 (the cache was just written by
+    # the encode, so the in-step time partly reads L2)
+    cold_ms = None
+    if plan["cold"]:
+        cop = next(op for op in ops if op.name == plan["cold"])
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cold = []
+        for _ in range(min(max(3, args.steps), 50)):
+            flush.zero_()
+            a0.record(stream)
+            cop.fn()
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            cold.append(a0.elapsed_time(a1))
+        cold_ms = statistics.median(cold)
+        del flush
 
     # end to end through the C ABI from pinned host buffers
-    hk = k.cpu().pin_memory()
-    hv = v.cpu().pin_memory()
-    hq = q.cpu().pin_memory()
-    hout = torch.empty_like(out, device="cpu").pin_memory()
-    dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
-
-    def e2e_step():
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dq.copy_(hq, non_blocking=True)
-        tq.tq_encode_kv(dk.view(-1, 128), kcb, signs, kb, stream=stream)
-        tq.tq_encode_kv(dv.view(-1, 128), vcb, signs, vb, stream=stream)
-        tq.tq_attn_decode(dq, kb, kcb, vb, vcb, out, ws, T, scale, signs, stream=stream)
-        hout.copy_(out, non_blocking=True)
-
+    e2e_step, h2d, d2h = plan["e2e"]()
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize(dev)
+    n_e2e = max(1, min(args.steps, 200, int(2e10 // max(1, h2d + d2h))))
     barrier(world)
-    n_e2e = min(args.steps, 200)
     t0.record(stream)
     for _ in range(n_e2e):
         e2e_step()
@@ -235,34 +537,47 @@ def run_gpu(args, rank, world, local_rank):
     e2e_ms = reduce_max(t0.elapsed_time(t1) / n_e2e, world)
 
     peak, peak_kind = hbm_peak()
-    enc_bytes = nb["enc_k"] + nb["enc_v"]
-    enc_gbs = enc_bytes / ((enc_k_ms + enc_v_ms) * 1e-3) / 1e9
-    attn_gbs = nb["attn"] / (attn_ms * 1e-3) / 1e9
-    attn_cold_gbs = nb["attn"] / (attn_cold_ms * 1e-3) / 1e9
-    value = world * nb["total"] / (ms_step * 1e-3) / 1e9
+    total = sum(op.nbytes for op in ops)
+    value = world * total / (ms_step * 1e-3) / 1e9
+    parts, groups = {}, {}
+    for op, ms in zip(ops, op_ms):
+        gbs = op.nbytes / (ms * 1e-3) / 1e9
+        p = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
+             "bytes": op.nbytes}
+        if op.nvec:
+            p["gvec_s"] = round(op.nvec / (ms * 1e-3) / 1e9, 3)
+        if op.name == plan["cold"]:
+            cg = op.nbytes / (cold_ms * 1e-3) / 1e9
+            p.update(cold_l2_us=round(cold_ms * 1e3, 2), cold_l2_gbs=round(cg, 1),
+                     cold_l2_frac_hbm=round(cg / peak, 4))
+        parts[op.name] = p
+        g = groups.setdefault(op.group, {"ms": 0.0, "bytes": 0, "launches": 0})
+        g["ms"] += ms
+        g["bytes"] += op.nbytes
+        g["launches"] += op.launches
+
+    def roofline(name):
+        g = groups[name]
+        ach = g["bytes"] / (g["ms"] * 1e-3) / 1e9
+        tr = profiled_traffic(args.workload, name)
+        return {"bound": "hbm", "kernel": name, "launches_per_step": g["launches"], "achieved": round(ach, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "traffic": tr, "algorithmic_bytes": g["bytes"]}
+
+    dominant = max(groups, key=lambda n: groups[n]["ms"])
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no dataset or model weights)",
-        "config": dict(WORKLOAD, l2="inputs (537 MB) larger than L2 (129 MB); attention also timed after an "
-                       "L2 flush", parallelism="replicas" if world > 1 else "single GPU"),
-        "parts": {
-            "encode": {"us": round((enc_k_ms + enc_v_ms) * 1e3, 2), "gbs": round(enc_gbs, 1),
-                       "gvec_s": round(nb["nvec"] / ((enc_k_ms + enc_v_ms) * 1e-3) / 1e9, 3),
-                       "frac_hbm": round(enc_gbs / peak, 4)},
-            "attention": {"us": round(attn_ms * 1e3, 2), "gbs": round(attn_gbs, 1),
-                          "frac_hbm": round(attn_gbs / peak, 4), "cold_l2_us": round(attn_cold_ms * 1e3, 2),
-                          "cold_l2_gbs": round(attn_cold_gbs, 1),
-                          "cold_l2_frac_hbm": round(attn_cold_gbs / peak, 4)},
-        },
-        "roofline": {"bound": "hbm", "kernel": "encode_kernel (K 4-bit + V 2-bit launches)",
-                     "achieved": round(enc_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(enc_gbs / peak, 4), "traffic": None},
-        "e2e": {"value": round(world * nb["total"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": k.numel() * 2 + v.numel() * 2 + q.numel() * 2,
-                "d2h_bytes_per_step": out.numel() * 4},
-        "gpu_launches": 4 * args.steps,
+        "vs_baseline": None, "dtype": plan["dtype"], "data": "synthetic (seeded; no dataset or model weights)",
+        "config": dict(plan["config"], workload=args.workload,
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "parts": parts,
+        "roofline": roofline(dominant),
+        "roofline_by_kernel": {n: roofline(n) for n in groups},
+        "e2e": {"value": round(world * total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "steps": n_e2e, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(op.launches for op in ops) * args.steps,
         "clocks": clk,
     }
     return res
@@ -270,37 +585,113 @@ def run_gpu(args, rank, world, local_rank):
 
 # ---------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_sample(groups, seed=0):
-    """Time the oracle on `groups` (sequence, KV head) slices of the workload:
-    encode their K and V rows, then decode attention for their query heads.
-    Returns (seconds, algorithmic bytes of the sample)."""
+def _oracle_books():
+    import oracle
+    return {b: oracle.beta_codebook(128, b)[:2] for b in (2, 3, 4)}
+
+
+def _oracle_roundtrip(codec, x, s, c, bd, bits):
+    """Oracle encode + pack + unpack + decode of rows x (float64 [N, 128])."""
+    idx, n16, _ = codec.encode(x, s, bd.astype(np.float32))
+    blk = codec.pack_block(idx, n16, bits)
+    idx, n16 = codec.unpack_block(blk, bits)
+    return codec.decode(idx, n16, c, s), idx, n16
+
+
+_SAMPLE_INPUTS = {}
+
+
+def _sample_inputs(key, make):
+    """Seeded inputs of an oracle sample, drawn once per key (the draw is not
+    part of the timed oracle work)."""
+    if key not in _SAMPLE_INPUTS:
+        _SAMPLE_INPUTS.clear()
+        _SAMPLE_INPUTS[key] = make()
+    return _SAMPLE_INPUTS[key]
+
+
+def oracle_sample(workload, groups, seed=0, frac=1.0):
+    """Time the oracle on a bounded sample of `workload`: `groups` (sequence,
+    KV head) slices over the first `frac` of the context (or, for the storage
+    round trip, groups of 1024 tokens x 8 heads of one compressed layer).
+    Returns (seconds, algorithmic bytes of the sample, description)."""
     import oracle
     from oracle import codec
     from turboquant_bit_kv_gb300 import workloads
 
-    W = WORKLOAD
-    T, G = W["T"], W["Hq"] // W["Hkv"]
-    data = workloads.llama_decode(B=1, Hq=G * groups, Hkv=groups, T=T, seed=seed)
-    k = data["k"][0].double().numpy()
-    v = data["v"][0].double().numpy()
-    q = data["q"].double().numpy()
+    W = WORKLOADS[workload]
     s = oracle.sign_diagonal(workloads.SIGN_SEED)
-    kc, kbd, _ = oracle.beta_codebook(128, 4)
-    vc, vbd, _ = oracle.beta_codebook(128, 2)
+    books = _oracle_books()
+    scale = 1 / np.sqrt(128)
+    T = max(64, int(W["T"] * frac)) if "Hq" in W else 0
+    if workload in ("llama3_8b_decode", "single_head_fp32", "qwen25_7b_append"):
+        G = W["Hq"] // W["Hkv"]
+        kbits, vbits = W["key_bits"], W["value_bits"]
+        key = (workload, groups, T, seed)
+        if workload == "llama3_8b_decode":
+            data = _sample_inputs(key, lambda: workloads.llama_decode(B=1, Hq=G * groups, Hkv=groups, T=T,
+                                                                      seed=seed))
+        elif workload == "qwen25_7b_append":
+            data = _sample_inputs(key, lambda: workloads.qwen_outlier(B=1, Hq=G * groups, Hkv=groups, T=T,
+                                                                      seed=seed))
+        else:
+            groups = 1
+            d = _sample_inputs(key, lambda: workloads.single_head(T=T, seed=seed))
+            data = {"k": d["k"][None, None], "v": d["v"][None, None], "q": d["q"].view(1, 1, 128)}
+        k = data["k"][0].double().numpy()
+        v = data["v"][0].double().numpy()
+        q = data["q"].double().numpy()
+        t0 = time.perf_counter()
+        kh = [_oracle_roundtrip(codec, k[g], s, *books[kbits], kbits)[0] for g in range(groups)]
+        vh = [_oracle_roundtrip(codec, v[g], s, *books[vbits], vbits)[0] for g in range(groups)]
+        oracle.attention_dequantized(q, np.stack(kh)[None], np.stack(vh)[None], scale)
+        secs = time.perf_counter() - t0
+        ib = 4 if workload == "single_head_fp32" else 2
+        kbb, vbb = 2 + 16 * kbits, 2 + 16 * vbits
+        n = groups * T
+        nbytes = n * (128 * ib * 2 + kbb + vbb) + n * (kbb + vbb) + G * groups * 128 * (ib + 4)
+        desc = "%d (sequence, KV head) slice(s) at T=%d: encode K/V rows, attend %d query heads" % (groups, T, G)
+        return secs, nbytes, desc
+    if workload == "qjl_two_term":
+        G = W["Hq"] // W["Hkv"]
+        data = _sample_inputs((workload, groups, T, seed),
+                              lambda: workloads.qjl_keys(B=1, Hq=G * groups, Hkv=groups, T=T, seed=seed))
+        k = data["k"][0].double().numpy()
+        v = data["v"][0].double().numpy()
+        q = data["q"].double().numpy()
+        S = data["S"].double().numpy()
+        c3 = books[3][0]
+        t0 = time.perf_counter()
+        kh, t2 = [], np.zeros((1, G * groups, T))
+        for g in range(groups):
+            khat, idx, n16 = _oracle_roundtrip(codec, k[g], s, *books[3], 3)
+            bits, rn16, _ = oracle.qjl_encode(k[g], idx, n16, c3, s, S)
+            for h in range(G):
+                t2[0, g * G + h] = oracle.qjl_term2(q[0, g * G + h], bits, rn16, S)
+            kh.append(khat)
+        oracle.attention_dequantized(q, np.stack(kh)[None], v[None], scale, term2=t2)
+        secs = time.perf_counter() - t0
+        n = groups * T
+        nbytes = n * 306 + n * 324 + n * 324 + G * groups * 128 * 6 + 2 * 65536
+        desc = "%d (sequence, KV head) slice(s) at T=%d: K3 encode, QJL encode, two-term attention of %d " \
+               "query heads" % (groups, T, G)
+        return secs, nbytes, desc
+    # storage round trip: encode + decode of 1024-token x 8-head groups of K and V rows
+    x = _sample_inputs((workload, groups, seed),
+                       lambda: workloads.storage_kv(L=1, T=1024 * groups, hidden=1024, seed=seed))["kv"]
+    rows = x.double().numpy().reshape(2, -1, 128)
+    c4, b4 = books[4]
     t0 = time.perf_counter()
-    kh, vh = [], []
-    for g in range(groups):
-        ki, kn, _ = codec.encode(k[g], s, kbd.astype(np.float32))
-        vi, vn, _ = codec.encode(v[g], s, vbd.astype(np.float32))
-        kblk, vblk = codec.pack_block(ki, kn, 4), codec.pack_block(vi, vn, 2)
-        ki, kn = codec.unpack_block(kblk, 4)
-        vi, vn = codec.unpack_block(vblk, 2)
-        kh.append(codec.decode(ki, kn, kc, s))
-        vh.append(codec.decode(vi, vn, vc, s))
-    oracle.attention_dequantized(q, np.stack(kh)[None], np.stack(vh)[None], 1 / np.sqrt(128))
+    for kv in range(2):
+        _oracle_roundtrip(codec, rows[kv], s, c4, b4, 4)
     secs = time.perf_counter() - t0
-    nb = step_bytes(1, G * groups, groups, T)
-    return secs, nb["total"]
+    n = rows.shape[1] * 2
+    nbytes = 2 * n * (256 + 66)
+    return secs, nbytes, "%d K+V rows of a compressed layer: serialise + deserialise" % n
+
+
+CPU_GROUPS = {"llama3_8b_decode": 128, "single_head_fp32": 1, "qwen25_7b_append": 24, "qjl_two_term": 32,
+              "storage_roundtrip": 64}
 
 
 def cpu_cores():
@@ -311,36 +702,43 @@ def cpu_cores():
 
 
 def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores; each step is a
+    bounded sample sized so that warm-up + steps stay near a minute and a half."""
     if rank != 0:
         return None
-    groups = args.cpu_groups
-    oracle_sample(1)                  # warm caches (codebook iteration, Hadamard matrix)
-    times, nbytes = [], 0
+    wl = args.workload
+    t1, _, _ = oracle_sample(wl, 1)            # warms caches (codebooks, Hadamard) and calibrates
+    t1, _, _ = oracle_sample(wl, 1)
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    groups = args.cpu_groups or CPU_GROUPS[wl]
+    groups = max(1, min(groups, int(per_step / max(t1, 1e-3))))
+    frac = 1.0
+    if groups == 1 and t1 > per_step and "Hq" in WORKLOADS[wl]:
+        frac = max(1.0 / 64, per_step / t1)   # a leading part of one slice's context
     for _ in range(args.warmup):
-        oracle_sample(groups)
+        oracle_sample(wl, groups, frac=frac)
+    times, nbytes, desc = [], 0, ""
     for _ in range(args.steps):
-        secs, nbytes = oracle_sample(groups)
+        secs, nbytes, desc = oracle_sample(wl, groups, frac=frac)
         times.append(secs)
     sec = statistics.mean(times)
     val = nbytes / sec / 1e9
-    sample = "%d of 128 (sequence, KV head) slices per step: encode their K/V rows (T=8192) and attend " \
-             "their 4 query heads" % groups
     return {
         "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": dict(WORKLOAD), "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": cpu_cores(),
-                                                   "kind": "oracle", "sample": sample},
+        "config": dict(WORKLOADS[wl], workload=wl),
+        "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
         "e2e": {"value": round(val, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def cpu_baseline(groups):
-    oracle_sample(1)
-    secs, nbytes = oracle_sample(groups)
+def cpu_baseline(workload, groups):
+    oracle_sample(workload, 1)
+    secs, nbytes, desc = oracle_sample(workload, groups or CPU_GROUPS[workload])
     return {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": "%d of 128 (sequence, KV head) slices of the step (encode K/V rows, attend 4 query "
-                      "heads), %.1f s" % (groups, secs)}
+            "sample": "%s, %.1f s" % (desc, secs)}
 
 
 def main():
@@ -349,8 +747,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-groups", type=int, default=128)
+    ap.add_argument("--cpu-groups", type=int, default=0, help="oracle sample size (0: the workload's default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--profile-only", action="store_true",
@@ -366,13 +765,11 @@ def main():
             torch.cuda.set_device(local_rank)
         dist.init_process_group(backend=backend)
     if args.impl == "reference":
-        if args.cpu_groups == 128:
-            args.cpu_groups = 4
         res = run_reference(args, rank, world)
     else:
         res = run_gpu(args, rank, world, local_rank)
         if rank == 0 and res is not None and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(args.cpu_groups)
+            res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_groups)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and args.impl != "reference":

@@ -1,0 +1,278 @@
+"""GPU parity at the workloads' full sizes, in the launch configurations the
+benchmark uses.  The oracle is far too slow for whole caches, so each test
+checks sampled outputs the oracle computes one by one:
+
+* encode: codes and norms of sampled rows (and of every appended row);
+* attention: the caches of a few sampled (sequence, KV head) slices are
+  replaced by oracle-made blocks before the full-size launch, so those
+  slices hold identical packed caches on both sides, and their query heads
+  are compared with the oracle's brute-force attention;
+* storage round trip: raw layers byte-identical, sampled compressed rows
+  against the oracle, and the per-layer round-trip MSE against the closed
+  form of the 4-bit codebook (a property that holds at any size).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import codec
+from turboquant_bit_kv_gb300 import workloads
+
+from parity_util import ATTN_TOL, attn_rel_err, check_codes, oracle_books
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from turboquant_bit_kv_gb300 import tq
+    tq.lib()
+    return dict(tq=tq, dev=torch.device("cuda:0"), books=oracle_books(),
+                cbs={b: tq.tq_codebook_load(128, b) for b in (2, 3, 4)},
+                signs=tq.tq_signs_from_seed(workloads.SIGN_SEED),
+                s=oracle.sign_diagonal(workloads.SIGN_SEED))
+
+
+def _rows(x4):
+    """float64 numpy [T, 128] of one (sequence, KV head) slice."""
+    return x4.double().cpu().numpy()
+
+
+def _sampled_codes(env, blocks2d, x2d, bits, n, seed, label):
+    rng = np.random.default_rng(seed)
+    rows = torch.from_numpy(np.sort(rng.choice(x2d.shape[0], size=n, replace=False)))
+    g = blocks2d[rows.to(blocks2d.device)].cpu().numpy()
+    x = x2d[rows.to(x2d.device)].double().cpu().numpy()
+    return check_codes(g, bits, x, env["s"], env["books"][bits][2], label)
+
+
+def _oracle_slice(env, x, bits):
+    """Oracle encoding of one slice: (packed blocks, dequantised rows)."""
+    c, _, b32 = env["books"][bits]
+    idx, n16, _ = codec.encode(x, env["s"], b32)
+    return codec.pack_block(idx, n16, bits), codec.decode(idx, n16, c, env["s"]), (idx, n16)
+
+
+def _check_attention_slice(env, q, out, b, h, G, k_hat, v_hat, scale, term2=None):
+    qs = q[b, h * G:(h + 1) * G].double().cpu().numpy()[None]
+    ref = oracle.attention_dequantized(qs, k_hat[None, None], v_hat[None, None], scale,
+                                       term2=None if term2 is None else term2[None])
+    got = out[b, h * G:(h + 1) * G].double().cpu().numpy()[None]
+    err = attn_rel_err(got, ref)
+    assert np.all(err < ATTN_TOL), (b, h, err.max())
+
+
+def test_llama_decode_fullsize(env):
+    """Batch 16, 32/8 heads, context 8192, bf16 K/V, K4/V2."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T = 16, 32, 8, 8192
+    G = Hq // Hkv
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=0, device=dev)
+    k, v, q = w["k"], w["v"], w["q"]
+    kb = torch.empty((B, Hkv, T, 66), dtype=torch.uint8, device=dev)
+    vb = torch.empty((B, Hkv, T, 34), dtype=torch.uint8, device=dev)
+    tq.tq_encode_kv(k.view(-1, D), env["cbs"][4], env["signs"], kb)
+    tq.tq_encode_kv(v.view(-1, D), env["cbs"][2], env["signs"], vb)
+    torch.cuda.synchronize()
+    _sampled_codes(env, kb.view(-1, 66), k.view(-1, D), 4, 8192, 1, "llama K")
+    _sampled_codes(env, vb.view(-1, 34), v.view(-1, D), 2, 8192, 2, "llama V")
+
+    slices = [(0, 0), (7, 3), (15, 7)]
+    hats = {}
+    for b, h in slices:
+        kblk, khat, _ = _oracle_slice(env, _rows(k[b, h]), 4)
+        vblk, vhat, _ = _oracle_slice(env, _rows(v[b, h]), 2)
+        kb[b, h] = torch.from_numpy(kblk).to(dev)
+        vb[b, h] = torch.from_numpy(vblk).to(dev)
+        hats[(b, h)] = (khat, vhat)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+    scale = 1 / np.sqrt(D)
+    tq.tq_attn_decode(q, kb, env["cbs"][4], vb, env["cbs"][2], out, ws, T, scale, env["signs"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    for b, h in slices:
+        _check_attention_slice(env, q, out, b, h, G, *hats[(b, h)], scale)
+
+
+def test_qwen_outlier_append_fullsize(env):
+    """Batch 64, 28/4 heads, bf16 with 1% outlier channels, K3/V3: encode a
+    32768-token prefix into a [B, Hkv, T_cap] cache through a destination
+    index, append token 32768 of every sequence, attend over 32769."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T = 64, 28, 4, 32769
+    T_cap = 32776
+    G = Hq // Hkv
+    w = workloads.qwen_outlier(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=0, device=dev)
+    q = w["q"]
+    caches = {}
+    bh = torch.arange(B * Hkv, device=dev, dtype=torch.int64)
+    t = torch.arange(T - 1, device=dev, dtype=torch.int64)
+    dst_prefix = (bh[:, None] * T_cap + t[None, :]).reshape(-1)
+    dst_new = bh * T_cap + (T - 1)
+    for name in ("k", "v"):
+        x = w[name]
+        blk = torch.zeros((B, Hkv, T_cap, 50), dtype=torch.uint8, device=dev)
+        prefix = x[:, :, :T - 1].contiguous().view(-1, D)
+        tq.tq_encode_kv(prefix, env["cbs"][3], env["signs"], blk, dst_index=dst_prefix)
+        del prefix
+        new = x[:, :, T - 1].contiguous().view(-1, D)
+        tq.tq_encode_kv(new, env["cbs"][3], env["signs"], blk, dst_index=dst_new)
+        torch.cuda.synchronize()
+        # every appended row, and sampled prefix rows
+        check_codes(blk[:, :, T - 1].reshape(-1, 50).cpu().numpy(), 3, new.double().cpu().numpy(), env["s"],
+                    env["books"][3][2], "qwen append " + name)
+        rng = np.random.default_rng(3 if name == "k" else 4)
+        pick = np.sort(rng.choice(B * Hkv * (T - 1), size=8192, replace=False))
+        bi, ti = pick // (T - 1), pick % (T - 1)
+        g = blk.view(B * Hkv, T_cap, 50)[torch.from_numpy(bi).to(dev), torch.from_numpy(ti).to(dev)].cpu().numpy()
+        xs = x.view(B * Hkv, T, D)[torch.from_numpy(bi).to(dev), torch.from_numpy(ti).to(dev)]
+        check_codes(g, 3, xs.double().cpu().numpy(), env["s"], env["books"][3][2], "qwen prefix " + name)
+        assert torch.all(blk[:, :, T:] == 0)
+        caches[name] = blk
+
+    slices = [(0, 0), (31, 2), (63, 3)]
+    hats = {}
+    for b, h in slices:
+        kblk, khat, _ = _oracle_slice(env, _rows(w["k"][b, h]), 3)
+        vblk, vhat, _ = _oracle_slice(env, _rows(w["v"][b, h]), 3)
+        caches["k"][b, h, :T] = torch.from_numpy(kblk).to(dev)
+        caches["v"][b, h, :T] = torch.from_numpy(vblk).to(dev)
+        hats[(b, h)] = (khat, vhat)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T_cap), dtype=torch.uint8, device=dev)
+    scale = 1 / np.sqrt(D)
+    tq.tq_attn_decode(q, caches["k"], env["cbs"][3], caches["v"], env["cbs"][3], out, ws, T, scale, env["signs"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    for b, h in slices:
+        _check_attention_slice(env, q, out, b, h, G, *hats[(b, h)], scale)
+
+
+def test_qjl_two_term_fullsize(env):
+    """Batch 8, 32/8 heads, context 16384: K3 codes + QJL sign bits and fp16
+    residual norms, raw fp16 values."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T = 8, 32, 8, 16384
+    G = Hq // Hkv
+    w = workloads.qjl_keys(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=0, device=dev)
+    k, v, q, S = w["k"], w["v"], w["q"], w["S"]
+    kb = torch.empty((B, Hkv, T, 50), dtype=torch.uint8, device=dev)
+    tq.tq_encode_kv(k.view(-1, D), env["cbs"][3], env["signs"], kb)
+    torch.cuda.synchronize()
+    _sampled_codes(env, kb.view(-1, 50), k.view(-1, D), 3, 8192, 5, "qjl K")
+
+    Sd = S.double().cpu().numpy()
+    c3 = env["books"][3][0]
+    slices = [(0, 0), (3, 5), (7, 7)]
+    ref = {}
+    for b, h in slices:
+        x = _rows(k[b, h])
+        kblk, khat, (idx, n16) = _oracle_slice(env, x, 3)
+        bits, rn16, _ = oracle.qjl_encode(x, idx, n16, c3, env["s"], Sd)
+        kb[b, h] = torch.from_numpy(kblk).to(dev)
+        ref[(b, h)] = (khat, bits, rn16)
+    qbits = torch.empty((B, Hkv, T, 16), dtype=torch.uint8, device=dev)
+    rn = torch.empty((B, Hkv, T), dtype=torch.int16, device=dev)
+    tq.tq_qjl_encode(k.view(-1, D), kb.view(-1, 50), env["cbs"][3], env["signs"], S, qbits.view(-1, 16),
+                     rn.view(-1))
+    torch.cuda.synchronize()
+    for b, h in slices:
+        khat, bits, rn16 = ref[(b, h)]
+        gb = np.unpackbits(qbits[b, h].cpu().numpy(), axis=1, bitorder="little")
+        ob = np.unpackbits(bits, axis=1, bitorder="little")
+        r = _rows(k[b, h]) - khat
+        proj = r @ Sd.T
+        tol = 1e-5 * np.linalg.norm(Sd, axis=1)[None, :] * np.linalg.norm(r, axis=1)[:, None]
+        mism = gb != ob
+        assert np.all(np.abs(proj[mism]) <= tol[mism])
+        grn = rn[b, h].cpu().numpy().view(np.uint16).astype(np.int64)
+        assert np.all(np.abs(grn - rn16.astype(np.int64)) <= 1)
+        # the attention below reads the oracle's bits and norms for this slice
+        qbits[b, h] = torch.from_numpy(bits).to(dev)
+        rn[b, h] = torch.from_numpy(rn16.view(np.int16)).to(dev)
+
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+    scale = 1 / np.sqrt(D)
+    tq.tq_attn_decode(q, kb, env["cbs"][3], v, None, out, ws, T, scale, env["signs"], qjl_bits=qbits,
+                      res_norm_f16=rn, S=S)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    qn = q.double().cpu().numpy()
+    for b, h in slices:
+        khat, bits, rn16 = ref[(b, h)]
+        term2 = np.stack([oracle.qjl_term2(qn[b, hq], bits, rn16, Sd) for hq in range(h * G, (h + 1) * G)])
+        _check_attention_slice(env, q, out, b, h, G, khat, _rows(v[b, h]), scale, term2=term2)
+
+
+def test_storage_roundtrip_fullsize(env):
+    """[2, 32 layers, 65536 tokens, 8 heads x 128] bf16; layers [0,2) and
+    [30,32) raw, the rest K4/V4 in 16-token blocks with 132-byte slots."""
+    tq, dev = env["tq"], env["dev"]
+    L, T, hidden, bs, sf, sl = 32, 65536, 1024, 16, 2, 2
+    H = hidden // D
+    x = workloads.storage_kv(L=L, T=T, hidden=hidden, seed=0, device=dev)["kv"]
+    size = tq.tq_serde_size(L, T, hidden, bs, sf, sl, 4, 4)
+    assert size == oracle.serde_size(L, T, hidden, D, bs, sf, sl, 4, 4)
+    buf = torch.empty(size, dtype=torch.uint8, device=dev)
+    tq.tq_serde_serialize(x, env["cbs"][4], env["cbs"][4], env["signs"], buf, block_size=bs, skip_first=sf,
+                          skip_last=sl)
+    torch.cuda.synchronize()
+    qs, qe = oracle.serde_ranges(L, sf, sl)
+    xb = x.view(torch.uint8)
+    n_first = 2 * qs * T * hidden * 2
+    n_comp = (qe - qs) * T * H * 132
+    assert torch.equal(buf[:n_first].view(2, qs, T, hidden * 2), xb[:, :qs].reshape(2, qs, T, hidden * 2))
+    assert torch.equal(buf[n_first + n_comp:].view(2, L - qe, T, hidden * 2),
+                       xb[:, qe:].reshape(2, L - qe, T, hidden * 2))
+    comp = buf[n_first:n_first + n_comp].view(qe - qs, T, H, 132)
+    rng = np.random.default_rng(7)
+    c4, _, b32 = env["books"][4]
+    picks = []
+    for layer in (qs, 15, qe - 1):
+        ti = torch.from_numpy(np.sort(rng.choice(T, size=512, replace=False))).to(dev)
+        for kv, off in ((0, 0), (1, 66)):
+            rows = x[kv, layer].view(T, H, D)[ti].reshape(-1, D)
+            g = comp[layer - qs][ti][:, :, off:off + 66].reshape(-1, 66).cpu().numpy()
+            check_codes(g, 4, rows.double().cpu().numpy(), env["s"], b32, "serde l%d" % layer)
+        picks.append((layer, ti))
+    # the sampled slots get the oracle's blocks, so the decode of those rows
+    # is compared on identical input
+    expect = {}
+    for layer, ti in picks:
+        for kv, off in ((0, 0), (1, 66)):
+            rows = x[kv, layer].view(T, H, D)[ti].reshape(-1, D).double().cpu().numpy()
+            idx, n16, _ = codec.encode(rows, env["s"], b32)
+            blk = torch.from_numpy(codec.pack_block(idx, n16, 4)).to(dev).view(len(ti), H, 66)
+            sub = comp[layer - qs][ti]
+            sub[:, :, off:off + 66] = blk
+            comp[layer - qs][ti] = sub
+            expect[(layer, kv)] = codec.decode(idx, n16, c4, env["s"])
+    y = torch.empty_like(x)
+    tq.tq_serde_deserialize(buf, env["cbs"][4], env["cbs"][4], env["signs"], y, block_size=bs, skip_first=sf,
+                            skip_last=sl)
+    torch.cuda.synchronize()
+    yb = y.view(torch.uint8)
+    assert torch.equal(yb[:, :qs], xb[:, :qs]) and torch.equal(yb[:, qe:], xb[:, qe:])
+    for layer, ti in picks:
+        for kv in (0, 1):
+            got = y[kv, layer].view(T, H, D)[ti].reshape(-1, D).double().cpu().numpy()
+            ref = expect[(layer, kv)]
+            tol = np.abs(ref) * 2.0**-8 + 1e-6 * np.linalg.norm(ref, axis=1, keepdims=True)
+            assert np.all(np.abs(got - ref) <= tol)
+    # per-layer round-trip MSE against the closed form d * E[(y - Q(y))^2] of
+    # the 4-bit codebook (inputs N(0, 1): E||x||^2 / d = 1)
+    c, bd, _ = env["books"][4]
+    expect_mse = D * oracle.beta_law_moments(c, bd, 64.0)
+    for layer in range(qs, qe):
+        for kv in (0, 1):
+            xd = x[kv, layer].float()
+            mse = float(((y[kv, layer].float() - xd) ** 2).mean() / (xd * xd).mean())
+            assert abs(mse / expect_mse - 1) < 0.03, (layer, kv, mse, expect_mse)
