@@ -432,3 +432,36 @@ def test_serde_roundtrip_matches_oracle(env, L, T, hidden, bs, sf, sl):
     for l in range(qs, qe):
         d = np.abs(grec[:, l] - rec[:, l])
         assert np.all(d <= np.abs(rec[:, l]) * 2.0**-7 + 1e-30)
+
+
+@pytest.mark.parametrize("kbits,packed_v", [(4, False), (2, True)])
+def test_attention_qjl_other_key_widths(env, kbits, packed_v):
+    """QJL with 4-bit keys and raw values, or 2-bit keys and 4-bit values
+    (the CUDA-core split kernel; the tensor-core kernel covers 3-bit keys)."""
+    B, Hq, Hkv, T, T_cap = 2, 6, 2, 150, 152
+    w = workloads.qjl_keys(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=15)
+    k = w["k"].double().numpy()
+    S = w["S"].double().numpy()
+    c, _, b32 = env["books"][kbits]
+    idx, n16, _ = codec.encode(k.reshape(-1, D), env["s"], b32)
+    bits, rn16, _ = oracle.qjl_encode(k.reshape(-1, D), idx, n16, c, env["s"], S)
+    kblk = codec.pack_block(idx, n16, kbits).reshape(B, Hkv, T, -1)
+    k_hat = codec.decode(idx, n16, c, env["s"]).reshape(B, Hkv, T, D)
+    q = w["q"].double().numpy()
+    G = Hq // Hkv
+    bits4, rn4 = bits.reshape(B, Hkv, T, 16), rn16.reshape(B, Hkv, T)
+    term2 = np.zeros((B, Hq, T))
+    for b in range(B):
+        for h in range(Hq):
+            term2[b, h] = oracle.qjl_term2(q[b, h], bits4[b, h // G], rn4[b, h // G], S)
+    scale = 1 / np.sqrt(D)
+    if packed_v:
+        cache = _oracle_cache(env, k, w["v"].double().numpy(), kbits, 4)
+        got = _run_attn(env, w["q"], kblk, cache["v_blk"], kbits, 4, T, T_cap, scale, qjl=(bits4, rn4, S))
+        v_hat = cache["v_hat"]
+    else:
+        got = _run_attn(env, w["q"], kblk, None, kbits, None, T, T_cap, scale, qjl=(bits4, rn4, S), v_raw=w["v"])
+        v_hat = w["v"].double().numpy()
+    ref = oracle.attention_dequantized(q, k_hat, v_hat, scale, term2=term2)
+    err = attn_rel_err(got, ref)
+    assert np.all(err < ATTN_TOL), err.max()

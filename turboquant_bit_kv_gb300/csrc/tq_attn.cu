@@ -51,8 +51,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_kernel(const float 
 // Merge for the tensor-core kernel's partition: the slots of segment
 // j = (sequence, KV head) are the CTAs that touched it.
 __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const float *ws, MmaPlan plan, int Hq,
-                                                                        int Hkv, uint32_t s0, uint32_t s1,
-                                                                        uint32_t s2, uint32_t s3, float *out) {
+                                                                        int Hkv, int rotate_back, uint32_t s0,
+                                                                        uint32_t s1, uint32_t s2, uint32_t s3,
+                                                                        float *out) {
     __shared__ float buf[kD];
     const int d = threadIdx.x;
     const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
@@ -73,7 +74,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const fl
             acc = fmaf(w, base[s * kPartialFloats + 4 + d], acc);
         }
     }
-    buf[d] = l > 0.f ? acc / l : 0.f;
+    const float o = l > 0.f ? acc / l : 0.f;
+    if (!rotate_back) {
+        out[(int64_t)blockIdx.x * kD + d] = o;
+        return;
+    }
+    buf[d] = o;
     __syncthreads();
     smem_fwht_rows<1>(buf);
     const uint32_t sw[4] = {s0, s1, s2, s3};
@@ -96,8 +102,8 @@ extern "C" size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv) return 0;
     int splits, tps;
     attn_split_plan(B, Hkv, T_cap, &splits, &tps);
-    const MmaPlan mp = mma_plan(B, Hkv, T_cap);
-    const int slots = splits > mp.Smax ? splits : mp.Smax;
+    const int ms = mma_max_slots(B, Hkv, T_cap);
+    const int slots = splits > ms ? splits : ms;
     return (size_t)B * Hq * slots * kPartialFloats * sizeof(float);
 }
 
@@ -151,12 +157,12 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     const int smem = attn_smem_bytes(kb, vb);
     cudaStream_t st = (cudaStream_t)stream;
     dim3 grid(a.splits, Hkv, B);
-    if (attn_mma_supported(kb, vb, qjl)) {
-        const MmaPlan mp = mma_plan(B, Hkv, T);
-        int r = launch_attn_mma(a, mp, st);
+    if (attn_mma_supported(kb, vb, qjl, G)) {
+        MmaPlan mp = mma_plan(B, Hkv, T, kb, vb, qjl, G);
+        int r = launch_attn_mma(a, mp, kb, vb, qjl, st);
         if (r != TQ_OK) return r;
-        attn_combine_mma_kernel<<<B * Hq, kAttnThreads, 0, st>>>(a.ws, mp, Hq, Hkv, signs.w[0], signs.w[1],
-                                                                  signs.w[2], signs.w[3], out);
+        attn_combine_mma_kernel<<<B * Hq, kAttnThreads, 0, st>>>(a.ws, mp, Hq, Hkv, vcb ? 1 : 0, signs.w[0],
+                                                                  signs.w[1], signs.w[2], signs.w[3], out);
         return launch_status();
     }
     int r;

@@ -1,0 +1,755 @@
+// Tensor-core decode attention over packed caches (sm_103a).
+//
+// Same computation as attn_split_kernel ("TurboQuant KV Cache Compression —
+// Spec", Optimization: Fused dequant-dot; "RotorQuant KV Cache Compression",
+// The QJL Estimator Formula and Fused Kernel Logic): rotated query, scores
+// against dequantised rotated keys (plus the QJL sign term), online softmax,
+// values accumulated in the rotated domain (raw values as they are), one
+// inverse rotation per output (in the combine kernel).
+//
+// Once a tile of codes is looked up, every product is a dense contraction,
+// run as mma.sync m16n8k16 (fp16 operands, float32 accumulate; the G <= 8
+// query heads sharing a KV head fill N = 8, zero-padded):
+//   scores  S[16 tokens x 8 heads]  = Khat[16 x 128] * Qrot^T[128 x 8]
+//   QJL     S2[16 tokens x 8 heads] = Sgn[16 x 128] * (S q)^T[128 x 8]
+//   values  O[128 dims x 8 heads]  += Vhat^T[128 x 16] * P[16 tokens x 8]
+//   * Keys: a thread reads the code slice of its dims 32t..32t+31 per token
+//     (the MMA's k-columns permuted to match) and turns each pair of codes
+//     into a half2 fragment register with one lookup in a lane-replicated
+//     table (word e * 32 + lane: every lane reads its own bank).  The pair's
+//     table index is the code byte (4-bit), the nibble (2-bit), or the low
+//     nibble of the 2-bit plane plus the two high-plane bits (3-bit).
+//   * 2-bit values: a thread owns dims 16g..16g+15 (the MMA's m-rows
+//     permuted), one 32-bit code word per token; a fragment register holds
+//     one dim of two tokens, built by one byte permute from an 8-byte
+//     register table of the four fp16 centroids.
+//   * 3- and 4-bit values: each lane dequantises half of one token's row
+//     into an fp16 tile in shared memory (pairs of dims through the same
+//     kind of table as keys), and the fragments are read back transposed
+//     with ldmatrix.trans; raw fp16 values are staged straight into that
+//     layout.
+//   * QJL: sign bits become +-1 fragments through a 16-entry nibble table;
+//     S q is computed once per (sequence, KV head) and query head.
+//   * Softmax runs on the score accumulators per 32-token chunk; the value
+//     norm is folded into P, which is transposed into the PV operand layout
+//     with movmatrix.
+//
+// Work partition: the B * Hkv * ceil(T / 32) chunks, ordered by (sequence,
+// KV head, position), are cut into P equal contiguous ranges, one per CTA
+// (all CTAs resident), so every CTA does the same work and there is no wave
+// tail.  A CTA walks the (sequence, KV head) segments its range touches; its
+// eight warps take the segment's chunks round-robin, each with its own
+// cp.async double buffer and softmax state, merge in a three-round tree, and
+// write one partial per query head into slot (CTA - first CTA of the
+// segment).  attn_combine_mma_kernel merges each segment's slots.
+//
+// This header holds the kernel template; tq_attn_mma_k{2,3,4}.cu instantiate
+// it per key width and tq_attn_mma.cu plans and dispatches.
+
+#pragma once
+
+#include <cmath>
+
+#include "tq_attn.cuh"
+#include "tq_attn_mma.h"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kW = 8;                          // warps per CTA
+constexpr int kThreadsMma = kW * 32;
+constexpr int kMergeSlot = 8 * 132;            // floats per warp slot in the merge buffer
+constexpr int kVtPitch = 272;                  // fp16 value tile row: 256 B + 16 B pad (conflict-free)
+constexpr unsigned kFull = 0xffffffffu;
+
+constexpr int align16(int x) { return (x + 15) & ~15; }
+
+// NT: n-tiles of the score / PV products.  Every tile has 8 columns = 4
+// query heads x (hi, lo) fp16 parts (query, sketched query and P are split
+// x = hi + lo so their products keep float32 precision); NT = 2 serves up to
+// 8 query heads per KV head.
+template <int KB, int VB, bool QJL, int NT>
+struct Cfg {
+    static constexpr int kKBytes = 2 + 16 * KB;
+    static constexpr bool kRawV = VB == 16;
+    static constexpr bool kRegV = VB == 2;                 // value fragments straight from registers
+    static constexpr int kVBytes = kRawV ? 256 : 2 + 16 * VB;
+    static constexpr int kKStage = align16(kMmaChunk * kKBytes);
+    static constexpr int kVStage = kRawV ? kMmaChunk * kVtPitch : align16(kMmaChunk * kVBytes);
+    static constexpr int kSStage = QJL ? kMmaChunk * 16 : 0;      // sign bits
+    static constexpr int kRStage = QJL ? kMmaChunk * 2 : 0;       // fp16 residual norms
+    // +16: word reads past a 2-byte aligned slice stay inside the warp's stage
+    static constexpr int kWarpStage = kKStage + kVStage + kSStage + kRStage + 16;
+    static constexpr int kVtile = (kRegV || kRawV) ? 0 : 16 * kVtPitch;   // per-warp dequantised tile
+    static constexpr int kKLutEntries = KB == 4 ? 256 : KB == 3 ? 64 : 16;
+    static constexpr int kVLutEntries = VB == 4 ? 256 : VB == 3 ? 64 : 0;
+    static constexpr int kSmemKLut = 0;
+    static constexpr int kSmemVLut = kSmemKLut + kKLutEntries * 128;
+    static constexpr int kSmemSLut = kSmemVLut + kVLutEntries * 128;
+    static constexpr int kSmemQ = kSmemSLut + (QJL ? 16 * 256 : 0);
+    static constexpr int kSmemSq = kSmemQ + 8 * 128 * 4;
+    static constexpr int kSmemVt = kSmemSq + (QJL ? 8 * 128 * 4 : 0);
+    static constexpr int kSmemStages = kSmemVt + kW * kVtile;
+    static constexpr int kSmemTotal = kSmemStages + kW * 2 * kWarpStage;
+    static constexpr int kMinBlocks = (NT == 1 && kSmemTotal <= 113 * 1024) ? 2 : 1;
+    static_assert(kW * 2 * kWarpStage >= 4 * kMergeSlot * 4, "merge buffer aliases the stages");
+    static_assert(kSmemTotal <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                              uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// NW 32-bit words starting at a 2-byte aligned shared address: the aligned
+// words around it, funnel-shifted by the misalignment.
+template <int NW>
+__device__ __forceinline__ void lds_words_a2(uint32_t addr, uint32_t (&w)[NW]) {
+    const uint32_t base = addr & ~3u, sh = (addr & 3u) * 8u;
+    uint32_t raw[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) raw[i] = lds32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void cp16_zfill(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+// Codes of the two dims of a table entry.  4-bit: entry = byte (low nibble
+// first dim); 2-bit: entry = nibble; 3-bit: entry = the pair's 2-bit-plane
+// nibble | high-plane bits << 4.
+template <int BITS>
+__device__ __forceinline__ void pair_codes(int e, int &c0, int &c1) {
+    if constexpr (BITS == 4) {
+        c0 = e & 15;
+        c1 = e >> 4;
+    } else if constexpr (BITS == 2) {
+        c0 = e & 3;
+        c1 = (e >> 2) & 3;
+    } else {
+        c0 = (e & 3) | ((e >> 2) & 4);
+        c1 = ((e >> 2) & 3) | ((e >> 3) & 4);
+    }
+}
+
+// Lane-replicated half2 table of a codebook: word e * 32 + l = (c[c0(e)],
+// c[c1(e)]) for every lane l; stores rotated by e so a warp's stores are
+// conflict-free.
+template <int BITS>
+__device__ __forceinline__ void build_pair_lut(uint32_t *lut, const float *cb, int tid) {
+    constexpr int E = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
+    for (int e = tid; e < E; e += kThreadsMma) {
+        int c0, c1;
+        pair_codes<BITS>(e, c0, c1);
+        const uint32_t val = pack_half2(cb[c0], cb[c1]);
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) lut[e * 32 + ((j + e) & 31)] = val;
+    }
+}
+
+// Split table of a codebook for the keys: entry e at byte e * 128 + l * 8 for
+// l = 0..15 (lanes l and l + 16 share a copy; an 8-byte load serves half a
+// warp per pass, so this is conflict-free) holds (hi, lo) half2 words with
+// hi = fp16(c), lo = fp16(c - hi): hi + lo carries c to about 2^-22.
+template <int BITS>
+__device__ __forceinline__ void build_split_lut(uint2 *lut, const float *cb, int tid) {
+    constexpr int E = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
+    for (int q = tid; q < E * 16; q += kThreadsMma) {
+        const int e = q >> 4, l = q & 15;
+        int c0, c1;
+        pair_codes<BITS>(e, c0, c1);
+        const __half h0 = __float2half_rn(cb[c0]), h1 = __float2half_rn(cb[c1]);
+        const uint32_t hi = pack_half2(__half2float(h0), __half2float(h1));
+        const uint32_t lo = pack_half2(cb[c0] - __half2float(h0), cb[c1] - __half2float(h1));
+        lut[e * 16 + l] = make_uint2(hi, lo);
+    }
+}
+
+// (hi, lo) fp16 split of x packed as one half2: x = hi + lo to about 2^-22.
+__device__ __forceinline__ uint32_t split_half2(float x) {
+    const __half h = __float2half_rn(x);
+    return pack_half2(__half2float(h), x - __half2float(h));
+}
+
+// 3-bit pair indices of 8 pairs from one 2-bit-plane word L (dims 16h..16h+15
+// of the slice, pairs 8h..8h+7) and the 16 high-plane bits Hh of the same
+// dims: even pairs (8h + 2i) in byte i of `ev`, odd pairs in byte i of `od`.
+__device__ __forceinline__ void pair_index3(uint32_t L, uint32_t Hh, uint32_t &ev, uint32_t &od) {
+    const uint32_t v = prmt(Hh, 0, 0x1100u);   // bytes [Hh1, Hh1, Hh0, Hh0]
+    ev = (L & 0x0F0F0F0Fu) | ((v << 4) & 0x00300030u) | (v & 0x30003000u);
+    od = ((L >> 4) & 0x0F0F0F0Fu) | ((v << 2) & 0x00300030u) | ((v >> 2) & 0x30003000u);
+}
+
+// Half2 key fragments for k-step ks of one token row: pairs 2ks (dims
+// 32t + 4ks + {0, 1}) and 2ks + 1 (dims 32t + 4ks + {2, 3}) of the slice.
+template <int KB>
+struct KeySlice {
+    uint32_t w[4];   // 4-bit: the 16 code bytes; 2/3-bit: even / odd pair indices of halves 0, 1
+
+    __device__ __forceinline__ void load(uint32_t row_s, int t) {
+        if constexpr (KB == 4) {
+            lds_words_a2<4>(row_s + 2 + 16 * t, w);
+        } else if constexpr (KB == 2) {
+            uint32_t c[2];
+            lds_words_a2<2>(row_s + 2 + 8 * t, c);
+            w[0] = c[0] & 0x0F0F0F0Fu;
+            w[1] = (c[0] >> 4) & 0x0F0F0F0Fu;
+            w[2] = c[1] & 0x0F0F0F0Fu;
+            w[3] = (c[1] >> 4) & 0x0F0F0F0Fu;
+        } else {
+            uint32_t c[2], hb[1];
+            lds_words_a2<2>(row_s + 2 + 8 * t, c);
+            lds_words_a2<1>(row_s + 34 + 4 * t, hb);
+            pair_index3(c[0], hb[0], w[0], w[1]);
+            pair_index3(c[1], hb[0] >> 16, w[2], w[3]);
+        }
+    }
+    // prmt selectors of the table index of pair 2ks (first) and 2ks + 1 (second)
+    __device__ __forceinline__ void pick(int ks, uint32_t &x, uint32_t &y) const {
+        if constexpr (KB == 4) {
+            const uint32_t word = w[ks >> 1];
+            x = prmt(word, 0, 0x4440u + 2 * (ks & 1));
+            y = prmt(word, 0, 0x4441u + 2 * (ks & 1));
+        } else {
+            const int h = ks >> 2, i = ks & 3;
+            x = prmt(w[2 * h], 0, 0x4440u + i);
+            y = prmt(w[2 * h + 1], 0, 0x4440u + i);
+        }
+    }
+};
+
+// One lane dequantises 64 dims (half `hf`) of one token's packed value block
+// into an fp16 row of the value tile (pairs through the pair table).
+template <int VB>
+__device__ __forceinline__ void dequant_value_half(uint32_t blk_s, int hf, uint32_t lut_s, uint32_t row_s) {
+    if constexpr (VB == 4) {
+        uint32_t c[8];
+        lds_words_a2<8>(blk_s + 2 + 32 * hf, c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = lds32(lut_s + prmt(c[2 * q + (j >> 2)], 0, 0x4440u + (j & 3)) * 128u);
+            sts128(row_s + 128 * hf + 32 * q, h[0], h[1], h[2], h[3]);
+            sts128(row_s + 128 * hf + 32 * q + 16, h[4], h[5], h[6], h[7]);
+        }
+    } else {  // VB == 3
+        uint32_t c[4], hb[2];
+        lds_words_a2<4>(blk_s + 2 + 16 * hf, c);
+        lds_words_a2<2>(blk_s + 34 + 8 * hf, hb);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t ev, od;
+            pair_index3(c[q], hb[q >> 1] >> (16 * (q & 1)), ev, od);
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h[2 * i] = lds32(lut_s + prmt(ev, 0, 0x4440u + i) * 128u);
+                h[2 * i + 1] = lds32(lut_s + prmt(od, 0, 0x4440u + i) * 128u);
+            }
+            sts128(row_s + 128 * hf + 32 * q, h[0], h[1], h[2], h[3]);
+            sts128(row_s + 128 * hf + 32 * q + 16, h[4], h[5], h[6], h[7]);
+        }
+    }
+}
+
+// Dim of accumulator row `r` (0: fragment row g, 1: row g + 8) of m-tile m.
+template <bool REGV>
+__device__ __forceinline__ int acc_dim(int m, int r, int g) {
+    return REGV ? 16 * g + 2 * m + r : 16 * m + g + 8 * r;
+}
+
+template <int KB, int VB, bool QJL, int NT>
+__global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
+    attn_mma_kernel(const __grid_constant__ AttnArgs a, MmaPlan plan) {
+    using C = Cfg<KB, VB, QJL, NT>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const uint32_t smem_s = (uint32_t)__cvta_generic_to_shared(smem);
+    float *qbuf = reinterpret_cast<float *>(smem + C::kSmemQ);
+    float *sqbuf = reinterpret_cast<float *>(smem + C::kSmemSq);
+    float *merge = reinterpret_cast<float *>(smem + C::kSmemStages);   // aliases the stages after the loop
+
+    build_split_lut<KB>(reinterpret_cast<uint2 *>(smem + C::kSmemKLut), a.kc, tid);
+    if constexpr (VB == 3 || VB == 4) build_pair_lut<VB>(reinterpret_cast<uint32_t *>(smem + C::kSmemVLut), a.vc, tid);
+    if constexpr (QJL) {
+        // sign table: entry e (4 sign bits) = (half2(s0, s1), half2(s2, s3)), s = bit ? +1 : -1,
+        // at byte e * 256 + lane * 8
+        uint32_t *sl = reinterpret_cast<uint32_t *>(smem + C::kSmemSLut);
+        for (int q = tid; q < 16 * 32; q += kThreadsMma) {
+            const int e = q >> 5, l = q & 31;
+            const uint32_t p0 = (e & 1) ? 0x3C00u : 0xBC00u, p1 = (e & 2) ? 0x3C00u : 0xBC00u;
+            const uint32_t p2 = (e & 4) ? 0x3C00u : 0xBC00u, p3 = (e & 8) ? 0x3C00u : 0xBC00u;
+            sl[e * 64 + 2 * l] = p0 | (p1 << 16);
+            sl[e * 64 + 2 * l + 1] = p2 | (p3 << 16);
+        }
+    }
+    // 2-bit value table for prmt: bytes 0-3 = low bytes, 4-7 = high bytes of the four fp16 centroids
+    uint32_t vlo = 0, vhi = 0;
+    if constexpr (VB == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t hb = __half_as_ushort(__float2half_rn(a.vc[i]));
+            vlo |= (hb & 0xFFu) << (8 * i);
+            vhi |= (hb >> 8) << (8 * i);
+        }
+    }
+    const uint32_t klut_s = smem_s + C::kSmemKLut + (lane & 15) * 8;
+    const uint32_t vlut_s = smem_s + C::kSmemVLut + lane * 4;
+    const uint32_t slut_s = smem_s + C::kSmemSLut + lane * 8;
+    const uint32_t vt_s = smem_s + C::kSmemVt + warp * C::kVtile;
+    const uint32_t stage_s = smem_s + C::kSmemStages + warp * 2 * C::kWarpStage;
+
+    const int64_t lo = (int64_t)blockIdx.x * plan.Ctot / plan.P;
+    const int64_t hi = (int64_t)(blockIdx.x + 1) * plan.Ctot / plan.P;
+    for (int64_t x = lo; x < hi;) {
+        const int64_t j = x / plan.C;                       // segment = (sequence, KV head)
+        const int64_t seg_lo = j * plan.C;
+        const int64_t xe = min64(hi, seg_lo + plan.C);
+        const int b = (int)(j / a.Hkv), kvh = (int)(j % a.Hkv);
+        int L = a.T;
+        if (a.seq_lens) {
+            const int sl = a.seq_lens[b];
+            L = sl < 0 ? 0 : (sl > a.T ? a.T : sl);
+        }
+        const int slot = (int)(blockIdx.x - mma_cta_of_chunk(seg_lo, plan));
+
+        // ---- rotated, scaled query of head `warp` (zero for padded heads), warp-local transform
+        __syncthreads();   // previous segment's readers of qbuf / sqbuf / merge are done
+        {
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (warp < a.G) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[k] = load_q(a.q, a.q_dtype, ((int64_t)b * a.Hq + kvh * a.G + warp) * kD + 4 * lane + k);
+            }
+            if constexpr (QJL) {
+                // raw query (scaled) for the sketch product below
+                const float f = a.qscale * (1.2533141373155003f / 128.f);   // sqrt(pi / 2) / m, m = 128
+                reinterpret_cast<float4 *>(sqbuf + warp * 128)[lane] =
+                    make_float4(v[0] * f, v[1] * f, v[2] * f, v[3] * f);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int d = 4 * lane + k;
+                if ((a.signs[d >> 5] >> (d & 31)) & 1u) v[k] = -v[k];
+            }
+            float x0 = v[0] + v[1], x1 = v[0] - v[1], x2 = v[2] + v[3], x3 = v[2] - v[3];
+            v[0] = x0 + x2;
+            v[2] = x0 - x2;
+            v[1] = x1 + x3;
+            v[3] = x1 - x3;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float o = __shfl_xor_sync(kFull, v[k], m);
+                    v[k] = (lane & m) ? (o - v[k]) : (v[k] + o);
+                }
+            }
+            const float f = a.qscale * 0.08838834764831845f;
+            reinterpret_cast<float4 *>(qbuf + warp * 128)[lane] = make_float4(v[0] * f, v[1] * f, v[2] * f, v[3] * f);
+        }
+        __syncthreads();
+        // B fragments of n-tile nt: column g = (head 4 nt + g / 2, part g & 1: hi / lo); k-step ks,
+        // rows {2t, 2t+1, 2t+8, 2t+9} <-> dims 32t + 4ks + {0, 1, 2, 3}
+        auto split_frag = [&](const float *buf, int nt, int ks, uint32_t &b0, uint32_t &b1) {
+            const float4 q4 = reinterpret_cast<const float4 *>(buf + (4 * nt + (g >> 1)) * 128 + 32 * t + 4 * ks)[0];
+            float e[4] = {q4.x, q4.y, q4.z, q4.w};
+            if (g & 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) e[i] -= __half2float(__float2half_rn(e[i]));
+            }
+            b0 = pack_half2(e[0], e[1]);
+            b1 = pack_half2(e[2], e[3]);
+        };
+        uint32_t qb[NT][8][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) split_frag(qbuf, nt, ks, qb[nt][ks][0], qb[nt][ks][1]);
+        uint32_t sb[QJL ? 8 : 1][2];
+        if constexpr (QJL) {
+            // (S q)_j of every head: thread -> output j = tid & 127, heads 4 (tid >> 7) .. + 3
+            const int jo = tid & 127, h0 = 4 * (tid >> 7);
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+            const float4 *srow = reinterpret_cast<const float4 *>(a.S + (int64_t)jo * kD);
+#pragma unroll 4
+            for (int d4 = 0; d4 < 32; ++d4) {
+                const float4 s4 = __ldg(srow + d4);
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    const float4 q4 = reinterpret_cast<const float4 *>(sqbuf + (h0 + hh) * 128)[d4];
+                    acc4[hh] = fmaf(s4.x, q4.x, fmaf(s4.y, q4.y, fmaf(s4.z, q4.z, fmaf(s4.w, q4.w, acc4[hh]))));
+                }
+            }
+            __syncthreads();   // every raw query is read before the products overwrite them
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) sqbuf[(h0 + hh) * 128 + jo] = acc4[hh];
+            __syncthreads();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) split_frag(sqbuf, 0, ks, sb[ks][0], sb[ks][1]);
+        }
+
+        const int64_t bh = (int64_t)b * a.Hkv + kvh;
+        const uint8_t *kbase = a.k + bh * a.T_cap * C::kKBytes;
+        const uint8_t *vbase = a.v + bh * a.T_cap * C::kVBytes;
+        const uint8_t *sgbase = QJL ? a.qjl_bits + bh * a.T_cap * 16 : nullptr;
+        const uint8_t *rnbase = QJL ? reinterpret_cast<const uint8_t *>(a.rn + bh * a.T_cap) : nullptr;
+        auto tok0 = [&](int64_t c) { return (int)((c - seg_lo) * kMmaChunk); };
+        // stage of a chunk: K blocks | V blocks (raw: 272-byte rows) | sign rows | residual norms
+        auto issue = [&](int buf, int64_t c) {
+            const int t0 = tok0(c);
+            const int n = min(kMmaChunk, L - t0);
+            const uint32_t dk = stage_s + buf * C::kWarpStage, dv = dk + C::kKStage;
+            const int nk = (n * C::kKBytes + 15) >> 4;
+            const uint8_t *sk = kbase + (int64_t)t0 * C::kKBytes, *sv = vbase + (int64_t)t0 * C::kVBytes;
+            for (int q = lane; q < C::kKStage / 16; q += 32) cp16_zfill(dk + 16 * q, q < nk ? sk + 16 * q : kbase, q < nk);
+            if constexpr (C::kRawV) {
+                for (int q = lane; q < kMmaChunk * 16; q += 32) {
+                    const int r = q >> 4, col = q & 15;
+                    cp16_zfill(dv + r * kVtPitch + 16 * col, r < n ? sv + r * 256 + 16 * col : vbase, r < n);
+                }
+            } else {
+                const int nvb = (n * C::kVBytes + 15) >> 4;
+                for (int q = lane; q < C::kVStage / 16; q += 32)
+                    cp16_zfill(dv + 16 * q, q < nvb ? sv + 16 * q : vbase, q < nvb);
+            }
+            if constexpr (QJL) {
+                const uint32_t ds = dv + C::kVStage, dr = ds + C::kSStage;
+                const uint8_t *ss = sgbase + (int64_t)t0 * 16, *sr = rnbase + (int64_t)t0 * 2;
+                cp16_zfill(ds + 16 * lane, lane < n ? ss + 16 * lane : sgbase, lane < n);
+                const int nr = (2 * n + 15) >> 4;
+                if (lane < 4) cp16_zfill(dr + 16 * lane, lane < nr ? sr + 16 * lane : rnbase, lane < nr);
+            }
+        };
+
+        // accumulators: n-tile nt, m-tile m; columns (2t, 2t+1) = head 4 nt + t, (hi, lo) parts
+        float o[NT][8][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int m = 0; m < 8; ++m) o[nt][m][0] = o[nt][m][1] = o[nt][m][2] = o[nt][m][3] = 0.f;
+        float mrun[NT], lrun[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mrun[nt] = -INFINITY;
+            lrun[nt] = 0.f;
+        }
+
+        // this warp's chunks: x + warp, x + warp + 8, ... below xe and with tokens left (t0 < L)
+        int64_t c = x + warp;
+        auto live = [&](int64_t cc) { return cc < xe && tok0(cc) < L; };
+        if (live(c)) issue(0, c);
+        cp_async_commit();
+        for (int it = 0; live(c); ++it, c += kW) {
+            if (live(c + kW)) issue((it + 1) & 1, c + kW);
+            cp_async_commit();
+            cp_async_wait<1>();
+            __syncwarp();
+            const int nvalid = min(kMmaChunk, L - tok0(c));
+            const uint32_t ks_s = stage_s + (it & 1) * C::kWarpStage, vs_s = ks_s + C::kKStage;
+            const uint32_t sg_s = vs_s + C::kVStage, rn_s = sg_s + C::kSStage;
+
+            // ---- scores of 2 tiles of 16 tokens (rows g, g + 8): (Khi + Klo) x (Qhi | Qlo)
+            KeySlice<KB> ksl[2][2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int rh = 0; rh < 2; ++rh) ksl[mt][rh].load(ks_s + (16 * mt + g + 8 * rh) * C::kKBytes, t);
+            float acc[NT][2][4];                 // [n-tile][m-tile][fragment]
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    uint32_t x0, y0, x1, y1;
+                    ksl[mt][0].pick(ks, x0, y0);
+                    ksl[mt][1].pick(ks, x1, y1);
+                    const uint2 a0 = lds64(klut_s + x0 * 128u), a2 = lds64(klut_s + y0 * 128u);
+                    const uint2 a1 = lds64(klut_s + x1 * 128u), a3 = lds64(klut_s + y1 * 128u);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma16816(acc[nt][mt], a0.x, a1.x, a2.x, a3.x, qb[nt][ks][0], qb[nt][ks][1]);
+                        mma16816(acc[nt][mt], a0.y, a1.y, a2.y, a3.y, qb[nt][ks][0], qb[nt][ks][1]);
+                    }
+                }
+            }
+            float acc2[QJL ? 2 : 1][4];
+            if constexpr (QJL) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    acc2[mt][0] = acc2[mt][1] = acc2[mt][2] = acc2[mt][3] = 0.f;
+                    const uint32_t wa = lds32(sg_s + (16 * mt + g) * 16 + 4 * t);
+                    const uint32_t wb = lds32(sg_s + (16 * mt + g + 8) * 16 + 4 * t);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint2 fa = lds64(slut_s + ((wa >> (4 * ks)) & 15u) * 256u);
+                        const uint2 fb = lds64(slut_s + ((wb >> (4 * ks)) & 15u) * 256u);
+                        mma16816(acc2[mt], fa.x, fb.x, fa.y, fb.y, sb[ks][0], sb[ks][1]);
+                    }
+                }
+            }
+            // s[nt][mt][r]: head 4 nt + t, token 16 mt + g + 8 r
+            float s[NT][2][2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int ta = 16 * mt + g, tb = ta + 8;
+                const float na = __half2float(__ushort_as_half((unsigned short)lds_u16(ks_s + ta * C::kKBytes)));
+                const float nb = __half2float(__ushort_as_half((unsigned short)lds_u16(ks_s + tb * C::kKBytes)));
+                float ra = 0.f, rb = 0.f;
+                if constexpr (QJL) {
+                    ra = __half2float(__ushort_as_half((unsigned short)lds_u16(rn_s + 2 * ta)));
+                    rb = __half2float(__ushort_as_half((unsigned short)lds_u16(rn_s + 2 * tb)));
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float ea = (acc[nt][mt][0] + acc[nt][mt][1]) * na;
+                    float eb = (acc[nt][mt][2] + acc[nt][mt][3]) * nb;
+                    if constexpr (QJL) {
+                        ea = fmaf(acc2[mt][0] + acc2[mt][1], ra, ea);
+                        eb = fmaf(acc2[mt][2] + acc2[mt][3], rb, eb);
+                    }
+                    s[nt][mt][0] = ta < nvalid ? ea : -INFINITY;
+                    s[nt][mt][1] = tb < nvalid ? eb : -INFINITY;
+                }
+            }
+            // ---- online softmax per head (max over the rows g of the warp)
+            bool moved = false;
+            float corr[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float mx = fmaxf(fmaxf(s[nt][0][0], s[nt][0][1]), fmaxf(s[nt][1][0], s[nt][1][1]));
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+                const float mn = fmaxf(mrun[nt], mx);
+                moved |= mn != mrun[nt];
+                corr[nt] = mn == -INFINITY ? 1.f : exp2f(mrun[nt] - mn);
+                mrun[nt] = mn;
+                lrun[nt] *= corr[nt];
+            }
+            if (__any_sync(kFull, moved)) {   // the running max rarely moves once it has settled
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) o[nt][m][q] *= corr[nt];
+            }
+            // ---- P (times the value norm, split hi | lo) and P V for each 16-token tile
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int ta = 16 * mt + g, tb = ta + 8;
+                float nva = 1.f, nvb = 1.f;
+                if constexpr (!C::kRawV) {
+                    nva = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + ta * C::kVBytes)));
+                    nvb = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + tb * C::kVBytes)));
+                }
+                uint32_t b0[NT], b1[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float mm = mrun[nt];
+                    const float pa = mm == -INFINITY ? 0.f : exp2f(s[nt][mt][0] - mm);
+                    const float pb = mm == -INFINITY ? 0.f : exp2f(s[nt][mt][1] - mm);
+                    lrun[nt] += pa + pb;
+                    b0[nt] = movmatrix_trans(split_half2(pa * nva));
+                    b1[nt] = movmatrix_trans(split_half2(pb * nvb));
+                }
+                if constexpr (C::kRegV) {
+                    // value codes of tokens 2t, 2t+1, 2t+8, 2t+9 of the tile: dims 16g..16g+15
+                    uint32_t w0[1], w1[1], w2[1], w3[1];
+                    lds_words_a2<1>(vs_s + (16 * mt + 2 * t) * C::kVBytes + 2 + 4 * g, w0);
+                    lds_words_a2<1>(vs_s + (16 * mt + 2 * t + 1) * C::kVBytes + 2 + 4 * g, w1);
+                    lds_words_a2<1>(vs_s + (16 * mt + 2 * t + 8) * C::kVBytes + 2 + 4 * g, w2);
+                    lds_words_a2<1>(vs_s + (16 * mt + 2 * t + 9) * C::kVBytes + 2 + 4 * g, w3);
+                    // interleave the two tokens of each register: bytes [A0, B0, A1, B1] / [A2, B2, A3, B3]
+                    const uint32_t x01 = prmt(w0[0], w1[0], 0x5140u), x23 = prmt(w0[0], w1[0], 0x7362u);
+                    const uint32_t y01 = prmt(w2[0], w3[0], 0x5140u), y23 = prmt(w2[0], w3[0], 0x7362u);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        // m-tile m: row g <-> dim 16g + 2m, row g + 8 <-> dim 16g + 2m + 1
+                        const int j0 = 2 * m, j1 = 2 * m + 1;
+                        const uint32_t xs = (j0 < 8) ? x01 : x23, ys = (j0 < 8) ? y01 : y23;
+                        const int sh0 = 16 * ((j0 >> 2) & 1) + 2 * (j0 & 3), sh1 = 16 * ((j1 >> 2) & 1) + 2 * (j1 & 3);
+                        const uint32_t a0 = prmt(vlo, vhi, ((xs >> sh0) & 0x0303u) * 0x11u + 0x4040u);
+                        const uint32_t a1 = prmt(vlo, vhi, ((xs >> sh1) & 0x0303u) * 0x11u + 0x4040u);
+                        const uint32_t a2 = prmt(vlo, vhi, ((ys >> sh0) & 0x0303u) * 0x11u + 0x4040u);
+                        const uint32_t a3 = prmt(vlo, vhi, ((ys >> sh1) & 0x0303u) * 0x11u + 0x4040u);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], a0, a1, a2, a3, b0[nt], b1[nt]);
+                    }
+                } else {
+                    uint32_t tile_s;
+                    if constexpr (C::kRawV) {
+                        tile_s = vs_s + 16 * mt * kVtPitch;
+                    } else {
+                        // lane -> token (lane & 15) of the tile, dims 64 (lane >> 4) .. + 63
+                        dequant_value_half<VB>(vs_s + (16 * mt + (lane & 15)) * C::kVBytes, lane >> 4, vlut_s,
+                                               vt_s + (lane & 15) * kVtPitch);
+                        __syncwarp();
+                        tile_s = vt_s;
+                    }
+                    // A = Vhat^T of m-tile m (dims 16m..16m+15 x the 16 tokens), read transposed
+                    const uint32_t arow = tile_s + ((lane & 7) + 8 * (lane >> 4)) * kVtPitch + 16 * ((lane >> 3) & 1);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(arow + 32 * m, a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], a0, a1, a2, a3, b0[nt], b1[nt]);
+                    }
+                    if constexpr (!C::kRawV) __syncwarp();   // the tile is rewritten for the next 16 tokens
+                }
+            }
+            __syncwarp();
+        }
+        cp_async_wait<0>();
+
+        // ---- fold the (hi, lo) columns: ov[nt][m][r] = head 4 nt + t at dim acc_dim(m, r, g)
+        float ov[NT][8][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                ov[nt][m][0] = o[nt][m][0] + o[nt][m][1];
+                ov[nt][m][1] = o[nt][m][2] + o[nt][m][3];
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) lrun[nt] += __shfl_xor_sync(kFull, lrun[nt], off);
+        }
+        // ---- merge the eight warps (rounds: 4 -> 2 -> 1), then warp 0 writes the partials
+#pragma unroll
+        for (int half = kW / 2; half >= 1; half >>= 1) {
+            __syncthreads();
+            if (warp >= half && warp < 2 * half) {
+                float *mw = merge + (warp - half) * kMergeSlot;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float *mh = mw + (4 * nt + t) * 132;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) mh[4 + acc_dim<C::kRegV>(m, r, g)] = ov[nt][m][r];
+                    if (g == 0) {
+                        mh[0] = mrun[nt];
+                        mh[1] = lrun[nt];
+                    }
+                }
+            }
+            __syncthreads();
+            if (warp < half) {
+                const float *mw = merge + warp * kMergeSlot;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float *mh = mw + (4 * nt + t) * 132;
+                    const float mo = mh[0], lo2 = mh[1];
+                    const float M = fmaxf(mrun[nt], mo);
+                    const float fs = mrun[nt] == -INFINITY ? 0.f : exp2f(mrun[nt] - M);
+                    const float fo = mo == -INFINITY ? 0.f : exp2f(mo - M);
+                    lrun[nt] = lrun[nt] * fs + lo2 * fo;
+                    mrun[nt] = M;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+                            ov[nt][m][r] = ov[nt][m][r] * fs + mh[4 + acc_dim<C::kRegV>(m, r, g)] * fo;
+                }
+            }
+        }
+        if (warp == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int head = 4 * nt + t;
+                if (head < a.G) {
+                    float *pr = a.ws + (((int64_t)b * a.Hq + kvh * a.G + head) * plan.Smax + slot) * kPartialFloats;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) pr[4 + acc_dim<C::kRegV>(m, r, g)] = ov[nt][m][r];
+                    if (g == 0) {
+                        pr[0] = mrun[nt];
+                        pr[1] = lrun[nt];
+                    }
+                }
+            }
+        }
+        x = xe;
+    }
+}
+
+template <int KB, int VB, bool QJL, int NT>
+int launch_cfg(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
+    static_assert(!QJL || NT == 1, "the QJL term covers up to 4 query heads per KV head");
+    using C = Cfg<KB, VB, QJL, NT>;
+    static int done[64] = {0};
+    if (set_smem_limit((const void *)attn_mma_kernel<KB, VB, QJL, NT>, C::kSmemTotal, done) != TQ_OK)
+        return TQ_ERR_CUDA;
+    attn_mma_kernel<KB, VB, QJL, NT><<<plan.P, kThreadsMma, C::kSmemTotal, st>>>(a, plan);
+    return launch_status();
+}
+
+template <int KB, int VB, bool QJL, int NT>
+constexpr int ctas_per_sm() {
+    return Cfg<KB, VB, QJL, NT>::kMinBlocks;
+}
+
+}  // namespace
+}  // namespace tq

@@ -1,0 +1,28 @@
+// Tensor-core decode attention, 4-bit keys: instantiations of the kernel
+// template in tq_attn_mma.cuh for every value format (2/3/4-bit codes, raw
+// fp16).
+#include "tq_attn_mma.cuh"
+
+namespace tq {
+
+int mma_ctas_per_sm_k4(int vb, bool qjl, int nt) {
+#define TQ_CASE(V, Q, N) \
+    if (vb == V && qjl == Q && nt == N) return ctas_per_sm<4, V, Q, N>();
+    TQ_CASE(2, false, 1) TQ_CASE(3, false, 1) TQ_CASE(4, false, 1) TQ_CASE(16, false, 1)
+    TQ_CASE(2, false, 2) TQ_CASE(3, false, 2) TQ_CASE(4, false, 2) TQ_CASE(16, false, 2)
+
+#undef TQ_CASE
+    return 0;
+}
+
+int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st) {
+#define TQ_CASE(V, Q, N) \
+    if (vb == V && qjl == Q && nt == N) return launch_cfg<4, V, Q, N>(a, plan, st);
+    TQ_CASE(2, false, 1) TQ_CASE(3, false, 1) TQ_CASE(4, false, 1) TQ_CASE(16, false, 1)
+    TQ_CASE(2, false, 2) TQ_CASE(3, false, 2) TQ_CASE(4, false, 2) TQ_CASE(16, false, 2)
+
+#undef TQ_CASE
+    return TQ_ERR_UNSUPPORTED;
+}
+
+}  // namespace tq

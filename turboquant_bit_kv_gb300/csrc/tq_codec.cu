@@ -14,13 +14,13 @@
 //  * "lmcache.v1.distributed.serde.turboquant": Configuration and Tensor
 //    Layout (raw first | compressed middle | raw last layers).
 //
-// Design (decode and QJL): one thread owns one 128-element vector.  A CTA of
+// Design (QJL): one thread owns one 128-element vector.  A CTA of
 // 128 threads stages a tile of 128 rows into shared memory with 16-byte
 // cp.async copies (double buffered across a persistent grid), each thread
 // holds its vector in registers as 64 packed float2 pairs and runs the whole
 // Walsh-Hadamard transform there with packed adds, and the CTA stores its
 // tile to HBM with coalesced 16-byte stores.  The quantise-on-insert kernel
-// lives in tq_encode.cu.
+// lives in tq_encode.cu, the dequantise kernel in tq_decode.cu.
 
 #include <algorithm>
 #include <cmath>
@@ -150,16 +150,6 @@ __device__ __forceinline__ void stage_rows(uint8_t *st, const uint8_t *x, int64_
     }
 }
 
-struct DecodeArgs {
-    const uint8_t *blocks;
-    int64_t block_stride;
-    int64_t n_vec;
-    uint8_t *out;
-    int64_t out_stride;  // bytes
-    int contiguous_in;
-    DevCodebook cb;
-    uint32_t signs[4];
-};
 
 template <int BITS>
 __device__ __forceinline__ void stage_blocks(uint8_t *st, const uint8_t *src, int64_t stride, int nv,
@@ -177,92 +167,6 @@ __device__ __forceinline__ void stage_blocks(uint8_t *st, const uint8_t *src, in
             uint16_t *d = reinterpret_cast<uint16_t *>(st + r * BB);
             for (int h = lane; h < BB / 2; h += 32) d[h] = s[h];
         }
-    }
-}
-
-template <int BITS, int DT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
-    constexpr int BB = BlockFmt<BITS>::kBytes;
-    constexpr int IN_STAGE = (kThreads * BB + 15) & ~15;
-    constexpr int OPITCH = InFmt<DT>::kPitch;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *stage = smem;                                   // 2 input stages
-    uint8_t *sm_out = smem + 2 * IN_STAGE;                   // kThreads * OPITCH
-    uint32_t *sg16 = reinterpret_cast<uint32_t *>(sm_out + kThreads * OPITCH);
-    uint32_t *sg32 = sg16 + 64;
-    float *lut = reinterpret_cast<float *>(sg32 + 128);
-    build_sign_tables(sg16, sg32, a.signs);
-    for (int i = threadIdx.x; i < 16; i += kThreads) lut[i] = a.cb.c[i];
-
-    const int64_t ntiles = (a.n_vec + kThreads - 1) / kThreads;
-    int64_t tile = blockIdx.x;
-    if (tile < ntiles)
-        stage_blocks<BITS>(stage, a.blocks + tile * kThreads * a.block_stride, a.block_stride,
-                           (int)min64(kThreads, a.n_vec - tile * kThreads), a.contiguous_in);
-    cp_async_commit();
-    const float inv_rs = 0.08838834764831845f;  // 1/sqrt(128)
-    for (int it = 0; tile < ntiles; ++it, tile += gridDim.x) {
-        const int64_t next = tile + gridDim.x;
-        if (next < ntiles)
-            stage_blocks<BITS>(stage + ((it + 1) & 1) * IN_STAGE, a.blocks + next * kThreads * a.block_stride,
-                               a.block_stride, (int)min64(kThreads, a.n_vec - next * kThreads),
-                               a.contiguous_in);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const int64_t v0 = tile * kThreads;
-        const int nv = (int)min64(kThreads, a.n_vec - v0);
-        const int t = threadIdx.x;
-        if (t < nv) {
-            uint32_t cw[BlockFmt<BITS>::kWords];
-            unsigned short n16 = load_block_smem<BITS>(stage + (it & 1) * IN_STAGE + t * BB, cw);
-            float2 p[64];
-            lut_pairs<BITS>(cw, lut, p);
-            fwht128(p);
-            const float f = __half2float(__ushort_as_half(n16)) * inv_rs;
-            const float2 f2 = make_float2(f, f);
-#pragma unroll
-            for (int i = 0; i < 64; ++i) p[i] = __fmul2_rn(p[i], f2);
-            uint8_t *orow = sm_out + t * OPITCH;
-            if constexpr (DT == TQ_F32) {
-                uint32_t *o = reinterpret_cast<uint32_t *>(orow);
-#pragma unroll
-                for (int j = 0; j < kD; ++j) {
-                    float v = (j < 64) ? p[j & 63].x : p[j & 63].y;
-                    o[j] = __float_as_uint(v) ^ sg32[j];
-                }
-            } else {
-                uint4 *o4 = reinterpret_cast<uint4 *>(orow);
-                const uint4 *s4 = reinterpret_cast<const uint4 *>(sg16);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        int j = 8 * k + 2 * m;
-                        float v0 = (j < 64) ? p[j & 63].x : p[j & 63].y;
-                        float v1 = ((j + 1) < 64) ? p[(j + 1) & 63].x : p[(j + 1) & 63].y;
-                        if constexpr (DT == TQ_BF16) {
-                            __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
-                            w[m] = *reinterpret_cast<uint32_t *>(&h);
-                        } else {
-                            __half2 h = __floats2half2_rn(v0, v1);
-                            w[m] = *reinterpret_cast<uint32_t *>(&h);
-                        }
-                    }
-                    uint4 s = s4[k];
-                    o4[k] = make_uint4(w[0] ^ s.x, w[1] ^ s.y, w[2] ^ s.z, w[3] ^ s.w);
-                }
-            }
-        }
-        __syncthreads();
-        constexpr int cpr = InFmt<DT>::kRowBytes / 16;
-        for (int c = threadIdx.x; c < nv * cpr; c += kThreads) {
-            int r = c / cpr, col = c - r * cpr;
-            *reinterpret_cast<uint4 *>(a.out + (v0 + r) * a.out_stride + 16 * col) =
-                *reinterpret_cast<const uint4 *>(sm_out + r * OPITCH + 16 * col);
-        }
-        __syncthreads();
     }
 }
 
@@ -368,19 +272,6 @@ bool codebook_ok(const tq_codebook *cb) {
 }
 
 template <int BITS, int DT>
-int launch_decode(const DecodeArgs &a, cudaStream_t st) {
-    static int done[64] = {0};
-    const int in_stage = (kThreads * BlockFmt<BITS>::kBytes + 15) & ~15;
-    const int smem = 2 * in_stage + kThreads * InFmt<DT>::kPitch + (64 + 128 + 16) * 4;
-    if (set_smem_limit((const void *)decode_kernel<BITS, DT>, smem, done) != TQ_OK) return TQ_ERR_CUDA;
-    const int64_t ntiles = (a.n_vec + kThreads - 1) / kThreads;
-    int per_sm = DT == TQ_F32 ? 2 : 3;
-    int grid = (int)min64(ntiles, (int64_t)per_sm * sm_count());
-    decode_kernel<BITS, DT><<<grid, kThreads, smem, st>>>(a);
-    return launch_status();
-}
-
-template <int BITS, int DT>
 int launch_qjl(const QjlArgs &a, cudaStream_t st) {
     static int done[64] = {0};
     const int smem = 128 * 64 * 8 + kThreads * InFmt<DT>::kPitch + ((kThreads * BlockFmt<BITS>::kBytes + 15) & ~15) +
@@ -413,29 +304,6 @@ using namespace tq;
         }                                                                              \
         return _r;                                                                     \
     } while (0)
-
-extern "C" int tq_decode_kv(const uint8_t *blocks, int64_t block_stride_bytes, int64_t n_vec,
-                            const tq_codebook *cb, tq_signs signs, void *out, int out_dtype,
-                            int64_t out_stride_elems, void *stream) {
-    if (n_vec < 0 || !cb) return TQ_ERR_ARG;
-    if (!codebook_ok(cb) || dtype_bytes(out_dtype) == 0) return TQ_ERR_UNSUPPORTED;
-    if (n_vec == 0) return TQ_OK;
-    const int es = dtype_bytes(out_dtype);
-    const int64_t bb = (int64_t)tq_block_bytes(cb->bits);
-    if (!blocks || !out || out_stride_elems < kD || block_stride_bytes < bb) return TQ_ERR_ARG;
-    if (!aligned(out, 16) || (out_stride_elems * es) % 16 || !aligned(blocks, 2) || (block_stride_bytes & 1))
-        return TQ_ERR_ALIGN;
-    DecodeArgs a;
-    a.blocks = blocks;
-    a.block_stride = block_stride_bytes;
-    a.n_vec = n_vec;
-    a.out = static_cast<uint8_t *>(out);
-    a.out_stride = out_stride_elems * es;
-    a.contiguous_in = (block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
-    a.cb = to_dev(cb);
-    for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
-    TQ_DISPATCH(launch_decode, cb->bits, out_dtype, a, (cudaStream_t)stream);
-}
 
 extern "C" int tq_qjl_encode(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_elems,
                              const uint8_t *k_blocks, int64_t block_stride_bytes, const tq_codebook *cb,

@@ -66,6 +66,57 @@ __device__ __forceinline__ void fwht128(float2 (&p)[64]) {
     }
 }
 
+// Unnormalised Walsh-Hadamard transform (Sylvester order) of one 128-element
+// vector shared by a thread pair (partner = lane ^ 1).  Thread h of the pair
+// holds elements e(c, k) = 16c + 8h + k (c, k = 0..7) as packed pairs
+// p[c'][k] = (e(c', k), e(c' + 4, k)); sgn = +1 for h = 0 and -1 for h = 1.
+// Six stages (element bits 0-2, 4-6) run in registers; the stage on bit 3 is
+// one exchange with the partner and one packed FMA, which leaves both
+// threads with exact butterfly outputs.
+__device__ __forceinline__ void fwht_pair128(float2 (&p)[4][8], float sgn) {
+#pragma unroll
+    for (int L = 1; L < 8; L <<= 1)              // element bits 0..2 (k)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if ((k & L) == 0) {
+                    const float2 a = p[c][k], b = p[c][k + L];
+                    p[c][k] = __fadd2_rn(a, b);
+                    p[c][k + L] = sub2(a, b);
+                }
+#pragma unroll
+    for (int L = 1; L < 4; L <<= 1)              // element bits 4..5 (c')
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if ((c & L) == 0)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 a = p[c][k], b = p[c + L][k];
+                    p[c][k] = __fadd2_rn(a, b);
+                    p[c + L][k] = sub2(a, b);
+                }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)                  // element bit 6 (inside a pair)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float x = p[c][k].x, y = p[c][k].y;
+            p[c][k] = make_float2(x + y, x - y);
+        }
+    // element bit 3: the partner holds e ^ 8.  h = 0 keeps e + partner,
+    // h = 1 (partner holds e - 8) keeps partner - own: fma(own, sgn, partner).
+    const float2 s2 = make_float2(sgn, sgn);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float2 o;
+            o.x = __shfl_xor_sync(0xffffffffu, p[c][k].x, 1);
+            o.y = __shfl_xor_sync(0xffffffffu, p[c][k].y, 1);
+            p[c][k] = __ffma2_rn(p[c][k], s2, o);
+        }
+}
+
 // Value j (0..127) of the pair layout.
 template <int J>
 __device__ __forceinline__ float pair_get(const float2 (&p)[64]) {

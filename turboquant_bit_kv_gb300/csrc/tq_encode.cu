@@ -22,11 +22,14 @@
 //     [2^-100, 2^100]) are rescaled by an exact power of two first.
 //   * Quantisation never divides by the norm: u (u = H D x) is scaled once
 //     to G y (y = u / (sqrt(128) n)), G chosen so that no cell of width 1
-//     holds two boundaries; adding 64 + 1.5 * 2^23 puts the cell index
-//     round(G y + 64) in the low bits of the float, a 128-entry table gives
-//     the cell's count of boundaries below it and the boundary inside it, and
-//     one comparison finishes #{i : b_i <= y} (3- and 4-bit).  The 2-bit code
-//     is three comparisons against -b, 0, +b (scaled by sqrt(128) n).
+//     holds two boundaries; adding 64 + 1.5 * 2^20 rounds G y + 64 to a
+//     multiple of 1/8 whose integer part (the cell index, cells
+//     [j - 1/16, j + 15/16)) times 8 is bits 3..9 of the float, i.e. the byte
+//     offset of the cell's 8-byte entry after one AND.  The 128-entry table
+//     gives the cell's count of boundaries below it and the boundary inside
+//     it, and one comparison finishes #{i : b_i <= y} (3- and 4-bit).  The
+//     2-bit code is three comparisons against -b, 0, +b (scaled by
+//     sqrt(128) n) in the float32 kernel.
 //   * Codes are packed per 8 elements and written into a shared-memory block
 //     tile, which the CTA stores with coalesced 16-byte stores (or block by
 //     block for strided / scattered destinations).
@@ -138,59 +141,6 @@ __device__ __forceinline__ float2 lds_f2(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ float2 sub2x(float2 a, float2 b) {
-    float2 r;
-    asm("sub.rn.f32x2 %0, %1, %2;"
-        : "=l"(*reinterpret_cast<unsigned long long *>(&r))
-        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
-    return r;
-}
-
-// Unnormalised Walsh-Hadamard transform of the pair's 128 elements.
-__device__ __forceinline__ void fwht_pair(float2 (&p)[4][8], float sgn) {
-#pragma unroll
-    for (int L = 1; L < 8; L <<= 1)              // element bits 0..2 (k)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if ((k & L) == 0) {
-                    const float2 a = p[c][k], b = p[c][k + L];
-                    p[c][k] = __fadd2_rn(a, b);
-                    p[c][k + L] = sub2x(a, b);
-                }
-#pragma unroll
-    for (int L = 1; L < 4; L <<= 1)              // element bits 4..5 (c')
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if ((c & L) == 0)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 a = p[c][k], b = p[c + L][k];
-                    p[c][k] = __fadd2_rn(a, b);
-                    p[c + L][k] = sub2x(a, b);
-                }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)                  // element bit 6 (inside a pair)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float x = p[c][k].x, y = p[c][k].y;
-            p[c][k] = make_float2(x + y, x - y);
-        }
-    // element bit 3: the partner holds e ^ 8.  h = 0 keeps e + partner,
-    // h = 1 (partner holds e - 8) keeps partner - own: fma(own, sgn, partner).
-    const float2 s2 = make_float2(sgn, sgn);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float2 o;
-            o.x = __shfl_xor_sync(kFull, p[c][k].x, 1);
-            o.y = __shfl_xor_sync(kFull, p[c][k].y, 1);
-            p[c][k] = __ffma2_rn(p[c][k], s2, o);
-        }
-}
-
 __device__ __forceinline__ float sumsq_pairs(const float2 (&p)[4][8]) {
     float2 acc[4];
 #pragma unroll
@@ -298,7 +248,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) encode_kernel(const __grid_con
         }
 
         // ---- transform and quantise
-        fwht_pair(p, sgn);
+        fwht_pair128(p, sgn);
         const float sc = n > 0.f ? n * 11.313708498984761f : 1.f;  // sqrt(128) n
         uint8_t *blk = sm_out + pv * BB;
         if constexpr (BITS == 2) {
@@ -318,7 +268,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) encode_kernel(const __grid_con
         } else {
             const float cs = a.grid / sc;
             const float2 cs2 = make_float2(cs, cs);
-            const float2 off2 = make_float2(12582976.f, 12582976.f);  // 64 + 1.5 * 2^23
+            const float2 off2 = make_float2(1572928.f, 1572928.f);  // 64 + 1.5 * 2^20
             const uint32_t tab_base = (uint32_t)__cvta_generic_to_shared(tab);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -327,9 +277,8 @@ __global__ void __launch_bounds__(kEncThreads, 3) encode_kernel(const __grid_con
                 for (int k = 0; k < 8; ++k) {
                     const float2 yp = __fmul2_rn(p[cc][k], cs2);
                     const float2 t = __fadd2_rn(yp, off2);
-                    // cell index = low 7 bits (masked, so even a NaN input stays in the table)
-                    const float2 ex = lds_f2(tab_base + (__float_as_uint(t.x) & (kBuckets - 1)) * 8u);
-                    const float2 ey = lds_f2(tab_base + (__float_as_uint(t.y) & (kBuckets - 1)) * 8u);
+                    const float2 ex = lds_f2(tab_base + (__float_as_uint(t.x) & 0x3F8u));
+                    const float2 ey = lds_f2(tab_base + (__float_as_uint(t.y) & 0x3F8u));
                     const uint32_t cx = __float_as_uint(ex.y) - set_ge(yp.x, ex.x);
                     const uint32_t cy = __float_as_uint(ey.y) - set_ge(yp.y, ey.x);
                     wx += cx << (4 * k);
@@ -483,18 +432,28 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid
     const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(wsm);
     auto issue = [&](int buf, int64_t tl) {
         const int64_t r0 = tl * kWarpRows;
+        const uint32_t d0 = stage_s + buf * kWarpStage + (lane >> 4) * kRowPitch + (lane & 15) * 16;
+        if (r0 + kWarpRows <= a.n_vec) {
+            const uint8_t *s0 = a.x + (r0 + (lane >> 4)) * a.x_stride + (lane & 15) * 16;
+            const int64_t step = 2 * a.x_stride;
 #pragma unroll
-        for (int q = lane; q < kWarpRows * 16; q += 32) {
-            const int r = q >> 4, col = q & 15;
-            const bool valid = r0 + r < a.n_vec;
-            const uint8_t *src = valid ? a.x + (r0 + r) * a.x_stride + col * 16 : a.x;
-            cp_async16_zfill(stage_s + buf * kWarpStage + r * kRowPitch + col * 16, src, valid);
+            for (int i = 0; i < 8; ++i)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d0 + i * 2 * kRowPitch),
+                             "l"(s0 + i * step) : "memory");
+        } else {
+#pragma unroll
+            for (int q = lane; q < kWarpRows * 16; q += 32) {
+                const int r = q >> 4, col = q & 15;
+                const bool valid = r0 + r < a.n_vec;
+                const uint8_t *src = valid ? a.x + (r0 + r) * a.x_stride + col * 16 : a.x;
+                cp_async16_zfill(stage_s + buf * kWarpStage + r * kRowPitch + col * 16, src, valid);
+            }
         }
     };
     int64_t tile = (int64_t)blockIdx.x * (kEncThreads / 32) + warp;
     if (tile < ntiles) issue(0, tile);
     cp_async_commit();
-    const float2 off2 = make_float2(12582976.f, 12582976.f);  // 64 + 1.5 * 2^23
+    const float2 off2 = make_float2(1572928.f, 1572928.f);  // 64 + 1.5 * 2^20
     const uint32_t tab_s = (uint32_t)__cvta_generic_to_shared(tab);
     for (int it = 0; tile < ntiles; ++it, tile += nwarps) {
         const int64_t next = tile + nwarps;
@@ -538,7 +497,7 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid
                         for (int vh = 0; vh < 2; ++vh) {
                             const float2 x = u[c][nt][vh], y = u[c + L][nt][vh];
                             u[c][nt][vh] = __fadd2_rn(x, y);
-                            u[c + L][nt][vh] = sub2x(x, y);
+                            u[c + L][nt][vh] = sub2(x, y);
                         }
         // u[i][nt][vh] = (u_e, u_{e+1}), e = 16 i + 4 t + 2 nt, of row g + 8 vh.
 
@@ -645,9 +604,8 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid
                 for (int nt = 0; nt < 2; ++nt) {
                     const float2 yp = __fmul2_rn(u[i][nt][vh], cs2);
                     const float2 tt = __fadd2_rn(yp, off2);
-                    // cell index = low 7 bits (masked: any input stays inside the table)
-                    const float2 ex = lds_f2(tab_s + (__float_as_uint(tt.x) & (kBuckets - 1)) * 8u);
-                    const float2 ey = lds_f2(tab_s + (__float_as_uint(tt.y) & (kBuckets - 1)) * 8u);
+                    const float2 ex = lds_f2(tab_s + (__float_as_uint(tt.x) & 0x3F8u));
+                    const float2 ey = lds_f2(tab_s + (__float_as_uint(tt.y) & 0x3F8u));
                     code4[2 * nt] = __float_as_uint(ex.y) + (yp.x >= ex.x ? 1u : 0u);
                     code4[2 * nt + 1] = __float_as_uint(ey.y) + (yp.y >= ey.x ? 1u : 0u);
                 }
@@ -738,7 +696,8 @@ int launch(const EncArgs &a, cudaStream_t st) {
 }
 
 // Cell table of a codebook.  With z = G y, cell j holds
-// z + 64 in [j - 1/2, j + 1/2); G is the smallest integer above
+// z + 64 in [j - 1/16, j + 15/16) (the cells of rounding z + 64 to 1/8 and
+// taking the integer part); G is the smallest integer above
 // 1 / (smallest gap between adjacent boundaries), so no cell holds two
 // boundaries, and G <= 62 keeps |z| <= G (|y| <= 1) inside the table.
 void build_table(const tq_codebook *cb, EncArgs *a) {
@@ -753,8 +712,8 @@ void build_table(const tq_codebook *cb, EncArgs *a) {
         float inner = INFINITY;
         for (int i = 0; i < L - 1; ++i) {
             const float z = G * cb->boundaries[i];
-            if (z + 64.f < j - 0.5f) ++below;
-            else if (z + 64.f < j + 0.5f) inner = z;
+            if (z + 64.f < j - 0.0625f) ++below;
+            else if (z + 64.f < j + 0.9375f) inner = z;
         }
         const uint32_t code = (uint32_t)below;
         float codef;
