@@ -164,6 +164,15 @@ __device__ __forceinline__ bool near_fp16_tie(float n, float rel) {
     return fabsf(n - 0.5f * (hv + hi)) <= tol;
 }
 
+// Conservative, integer-only form of near_fp16_tie(n, 2^-20): true when the
+// 13 float bits below the fp16 mantissa are within 16 units of the half-way
+// pattern 0x1000 (16 float ulps are 2^-20 .. 2^-19 of n), or when n is
+// outside fp16's normal range (zero, subnormal, overflow).
+__device__ __forceinline__ bool near_fp16_tie_fast(float n) {
+    const uint32_t b = __float_as_uint(n);
+    return ((b & 0x1FFFu) - 0x0FF0u) <= 0x20u || !(n >= 6.103515625e-05f && n < 65504.f);
+}
+
 // Double-float accumulation of a sum of squares (TwoProduct via FMA, TwoSum).
 struct SumSq2 {
     float s = 0.f, c = 0.f;

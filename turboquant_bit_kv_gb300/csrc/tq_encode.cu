@@ -390,6 +390,88 @@ __device__ __forceinline__ float elem_smem(const uint8_t *row, int j) {
     else return __half2float(__ushort_as_half(b));
 }
 
+// fp16 of the L2 norm of row `row` (128 values of dtype DT in shared memory):
+// double-float sum of squares over the quad (lane t sums 32t..32t+31), one
+// rounding.  Every lane of the warp calls it (shuffles inside); out of line
+// because the fast float32 norm needs it only near an fp16 rounding boundary.
+template <int DT>
+__device__ __noinline__ unsigned short exact_norm_quad(const uint8_t *row, int t) {
+    SumSq2 part;
+    for (int j = 32 * t; j < 32 * t + 32; ++j) part.add(elem_smem<DT>(row, j));
+    float s1 = part.s, c1 = part.c;
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        const float os = __shfl_xor_sync(kFull, s1, o), oc = __shfl_xor_sync(kFull, c1, o);
+        float ns, ne;
+        two_sum(s1, os, ns, ne);
+        s1 = ns;
+        c1 = c1 + oc + ne;
+    }
+    SumSq2 tot;
+    tot.s = s1;
+    tot.c = c1;
+    return tot.sqrt_fp16();
+}
+
+// Block of one row whose sum of squares leaves float32's safe range (tiny,
+// huge or zero vectors), by one thread: norm from a double sum of the exact
+// squares; the row scaled by an exact power of two (2^-e, e the exponent of
+// its largest magnitude) so the float32 transform and the cell quantiser work
+// in range (codes do not depend on the scale); a zero row gets code L/2
+// everywhere.  Out of line: such rows essentially never occur.
+template <int BITS, int DT>
+__device__ __noinline__ void encode_row_slow(const uint8_t *row, const float2 *tab, float grid,
+                                             const uint32_t (&signs)[4], uint8_t *blk) {
+    constexpr int BB = BlockFmt<BITS>::kBytes;
+    float v[kD];
+    double sd = 0.0;
+    float amax = 0.f;
+    for (int j = 0; j < kD; ++j) {
+        v[j] = elem_smem<DT>(row, j);
+        sd = fma((double)v[j], (double)v[j], sd);
+        amax = fmaxf(amax, fabsf(v[j]));
+    }
+    for (int j = 2; j < BB; ++j) blk[j] = 0;
+    *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__double2half(sqrt(sd)));
+    uint32_t code[kD];
+    if (!(amax > 0.f && amax < INFINITY)) {
+        for (int j = 0; j < kD; ++j) code[j] = (1u << BITS) / 2;
+    } else {
+        int e;
+        frexpf(amax, &e);
+        for (int j = 0; j < kD; ++j) {
+            const float x = ldexpf(v[j], -e);
+            v[j] = ((signs[j >> 5] >> (j & 31)) & 1u) ? -x : x;
+        }
+        for (int L = 1; L < kD; L <<= 1)
+            for (int j = 0; j < kD; ++j)
+                if (!(j & L)) {
+                    const float x = v[j], y = v[j + L];
+                    v[j] = x + y;
+                    v[j + L] = x - y;
+                }
+        float ss = 0.f;
+        for (int j = 0; j < kD; ++j) ss = fmaf(v[j], v[j], ss);
+        const float cs = grid / sqrtf(ss);
+        for (int j = 0; j < kD; ++j) {
+            const float yp = v[j] * cs;
+            const float tt = yp + 1572928.f;   // 64 + 1.5 * 2^20
+            const float2 ent = tab[(__float_as_uint(tt) & 0x3F8u) >> 3];
+            code[j] = __float_as_uint(ent.y) + (yp >= ent.x ? 1u : 0u);
+        }
+    }
+    for (int j = 0; j < kD; ++j) {
+        if constexpr (BITS == 4) {
+            blk[2 + j / 2] |= (uint8_t)(code[j] << (4 * (j & 1)));
+        } else if constexpr (BITS == 2) {
+            blk[2 + j / 4] |= (uint8_t)(code[j] << (2 * (j & 3)));
+        } else {
+            blk[2 + j / 4] |= (uint8_t)((code[j] & 3u) << (2 * (j & 3)));
+            blk[34 + j / 8] |= (uint8_t)((code[j] >> 2) << (j & 7));
+        }
+    }
+}
+
 // Each warp is independent: it stages its own 16 rows (double buffered,
 // cp.async with zero fill past the end), transforms and quantises them, and
 // stores its own 16 blocks; warps never wait for each other.
@@ -525,71 +607,18 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid
             sc[vh] = sqrtf(ss[vh]);
             const float n = sc[vh] * 0.08838834764831845f;
             n16[vh] = __half_as_ushort(__float2half_rn(n));
-            near[vh] = !oor[vh] && near_fp16_tie(n, 9.5367431640625e-07f);
+            near[vh] = near_fp16_tie_fast(n);
         }
-        if (__any_sync(kFull, near[0] || near[1] || oor[0] || oor[1])) {
-            // exact norms from the staged rows: lane t of the quad sums elements 32t..32t+31
+        if (__any_sync(kFull, near[0] || near[1])) {
+            // exact norms (double-float sums of the staged rows, one rounding to fp16);
+            // lane t of the quad sums elements 32t..32t+31
 #pragma unroll
             for (int vh = 0; vh < 2; ++vh) {
-                const uint8_t *row = rows + (g + 8 * vh) * kRowPitch;
-                SumSq2 part;
-                double pd = 0.0;
-                for (int j = 32 * t; j < 32 * t + 32; ++j) {
-                    const float xv = elem_smem<DT>(row, j);
-                    part.add(xv);
-                    pd = fma((double)xv, (double)xv, pd);
-                }
-                float s1 = part.s, c1 = part.c;
-#pragma unroll
-                for (int o = 1; o <= 2; o <<= 1) {
-                    const float os = __shfl_xor_sync(kFull, s1, o), oc = __shfl_xor_sync(kFull, c1, o);
-                    float ns, ne;
-                    two_sum(s1, os, ns, ne);
-                    s1 = ns;
-                    c1 = c1 + oc + ne;
-                    pd += __shfl_xor_sync(kFull, pd, o);
-                }
-                if (near[vh]) {
-                    SumSq2 tot;
-                    tot.s = s1;
-                    tot.c = c1;
-                    n16[vh] = tot.sqrt_fp16();
-                }
-                float amax = 0.f;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-                        amax = fmaxf(amax, fmaxf(fabsf(u[c][nt][vh].x), fabsf(u[c][nt][vh].y)));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-                if (oor[vh]) {
-                    n16[vh] = __half_as_ushort(__double2half(sqrt(pd)));
-                    if (amax > 0.f && amax < INFINITY) {
-                        int e;
-                        frexpf(amax, &e);
-                        const int e1 = -e / 2, e2 = -e - e1;
-                        const float2 f1 = make_float2(ldexpf(1.f, e1), ldexpf(1.f, e1));
-                        const float2 f2 = make_float2(ldexpf(1.f, e2), ldexpf(1.f, e2));
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt)
-                                u[c][nt][vh] = __fmul2_rn(__fmul2_rn(u[c][nt][vh], f1), f2);
-                    }
-                }
-                float2 q2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) q2 = __ffma2_rn(u[c][nt][vh], u[c][nt][vh], q2);
-                float v = q2.x + q2.y;
-                v += __shfl_xor_sync(kFull, v, 1);
-                v += __shfl_xor_sync(kFull, v, 2);
-                if (oor[vh]) sc[vh] = (v > 0.f && v < INFINITY) ? sqrtf(v) : 1.f;
+                if (!__any_sync(kFull, near[vh])) continue;
+                const unsigned short ex = exact_norm_quad<DT>(rows + (g + 8 * vh) * kRowPitch, t);
+                if (near[vh]) n16[vh] = ex;
             }
         }
-
         // ---- quantise and pack (four consecutive elements per thread and 16-block)
 #pragma unroll
         for (int vh = 0; vh < 2; ++vh) {
@@ -630,6 +659,14 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid
             if (t == 0) *reinterpret_cast<uint16_t *>(blk) = n16[vh];
         }
         __syncwarp();
+        if (__any_sync(kFull, oor[0] || oor[1])) {
+            // rows outside float32's safe range: lane r (< 16) redoes row r on its own
+            const bool o0 = __shfl_sync(kFull, oor[0], (lane & 7) * 4);   // row lane & 7
+            const bool o1 = __shfl_sync(kFull, oor[1], (lane & 7) * 4);   // row 8 + (lane & 7)
+            if (lane < kWarpRows && ((lane >> 3) ? o1 : o0))
+                encode_row_slow<BITS, DT>(rows + lane * kRowPitch, tab, a.grid, a.signs, sm_out + lane * BB);
+            __syncwarp();
+        }
 
         // ---- store this warp's 16 blocks (16 * BB bytes, 16-byte aligned when contiguous)
         if (a.contiguous) {
