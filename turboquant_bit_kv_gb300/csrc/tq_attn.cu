@@ -49,12 +49,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_kernel(const float 
 }
 
 // Merge for the tensor-core kernel's partition: the slots of segment
-// j = (sequence, KV head) are the CTAs that touched it.
+// j = (sequence, KV head) are the CTAs that touched it.  Launched as a
+// programmatic dependent of the attention kernel: its CTAs may start while
+// the attention kernel drains and wait here until its writes are visible.
 __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const float *ws, MmaPlan plan, int Hq,
                                                                         int Hkv, int rotate_back, uint32_t s0,
                                                                         uint32_t s1, uint32_t s2, uint32_t s3,
                                                                         float *out) {
     __shared__ float buf[kD];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int d = threadIdx.x;
     const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int G = Hq / Hkv;
@@ -161,8 +164,19 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
         MmaPlan mp = mma_plan(B, Hkv, T, kb, vb, qjl, G);
         int r = launch_attn_mma(a, mp, kb, vb, qjl, st);
         if (r != TQ_OK) return r;
-        attn_combine_mma_kernel<<<B * Hq, kAttnThreads, 0, st>>>(a.ws, mp, Hq, Hkv, vcb ? 1 : 0, signs.w[0],
-                                                                  signs.w[1], signs.w[2], signs.w[3], out);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(B * Hq));
+        cfg.blockDim = dim3(kAttnThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, attn_combine_mma_kernel, (const float *)a.ws, mp, Hq, Hkv, vcb ? 1 : 0,
+                               signs.w[0], signs.w[1], signs.w[2], signs.w[3], out) != cudaSuccess)
+            return TQ_ERR_CUDA;
         return launch_status();
     }
     int r;

@@ -662,6 +662,7 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
             __syncwarp();
         }
         cp_async_wait<0>();
+        if (xe == hi) asm volatile("griddepcontrol.launch_dependents;");   // last segment: let the combine launch
 
         // ---- fold the (hi, lo) columns: ov[nt][m][r] = head 4 nt + t at dim acc_dim(m, r, g)
         float ov[NT][8][2];
