@@ -90,7 +90,11 @@ struct Cfg {
     static constexpr int kSmemQ = kSmemSLut + (QJL ? 16 * 256 : 0);
     static constexpr int kSmemSq = kSmemQ + 8 * 128 * 4;
     static constexpr int kSmemVt = kSmemSq + (QJL ? 8 * 128 * 4 : 0);
-    static constexpr int kSmemStages = kSmemVt + kW * kVtile;
+    static constexpr int kSmemBars = kSmemVt + kW * kVtile;       // 2 mbarriers per warp
+    static constexpr int kSmemStages = kSmemBars + kW * 2 * 8;
+    // bytes a full chunk brings in (bulk copies, one mbarrier phase)
+    static constexpr int kChunkBytes = kMmaChunk * kKBytes + kMmaChunk * (kRawV ? 256 : kVBytes) +
+                                       (QJL ? kMmaChunk * 16 + kMmaChunk * 2 : 0);
     static constexpr int kSmemTotal = kSmemStages + kW * 2 * kWarpStage;
     static constexpr int kMinBlocks = (NT == 1 && kSmemTotal <= 113 * 1024) ? 2 : 1;
     static_assert(kW * 2 * kWarpStage >= 4 * kMergeSlot * 4, "merge buffer aliases the stages");
@@ -168,6 +172,36 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ __forceinline__ void cp16_zfill(uint32_t dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
                  : "memory");
+}
+
+// ---- bulk (TMA engine) copies completing on an mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Wait for the phase with parity `parity` to complete; gives up (false)
+// after a bounded number of polls instead of hanging.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
 }
 
 // Codes of the two dims of a table entry.  4-bit: entry = byte (low nibble
@@ -354,6 +388,16 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
     const uint32_t slut_s = smem_s + C::kSmemSLut + lane * 8;
     const uint32_t vt_s = smem_s + C::kSmemVt + warp * C::kVtile;
     const uint32_t stage_s = smem_s + C::kSmemStages + warp * 2 * C::kWarpStage;
+    const uint32_t bar_s = smem_s + C::kSmemBars + warp * 16;
+    if (lane == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_s + 8, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    uint32_t phase = 0;        // bit b: parity of the next completion of barrier b
+    uint32_t bulk_mask = 0;    // bit b: buffer b was filled by bulk copies
+    bool copies_ok = true;
 
     const int64_t lo = (int64_t)blockIdx.x * plan.Ctot / plan.P;
     const int64_t hi = (int64_t)(blockIdx.x + 1) * plan.Ctot / plan.P;
@@ -457,8 +501,28 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
             const int t0 = tok0(c);
             const int n = min(kMmaChunk, L - t0);
             const uint32_t dk = stage_s + buf * C::kWarpStage, dv = dk + C::kKStage;
-            const int nk = (n * C::kKBytes + 15) >> 4;
             const uint8_t *sk = kbase + (int64_t)t0 * C::kKBytes, *sv = vbase + (int64_t)t0 * C::kVBytes;
+            if (n == kMmaChunk) {
+                // full chunk: contiguous 16-byte aligned ranges, bulk copies on barrier `buf`
+                const uint32_t bar = bar_s + 8 * buf;
+                if (lane == 0) mbar_expect_tx(bar, C::kChunkBytes);
+                __syncwarp();
+                if (lane == 0) {
+                    bulk_g2s(dk, sk, kMmaChunk * C::kKBytes, bar);
+                    if constexpr (!C::kRawV) bulk_g2s(dv, sv, kMmaChunk * C::kVBytes, bar);
+                    if constexpr (QJL) {
+                        const uint32_t ds = dv + C::kVStage;
+                        bulk_g2s(ds, sgbase + (int64_t)t0 * 16, kMmaChunk * 16, bar);
+                        bulk_g2s(ds + C::kSStage, rnbase + (int64_t)t0 * 2, kMmaChunk * 2, bar);
+                    }
+                }
+                if constexpr (C::kRawV) bulk_g2s(dv + lane * kVtPitch, sv + lane * 256, 256, bar);
+                bulk_mask |= 1u << buf;
+                return;
+            }
+            // partial chunk (the end of a sequence): 16-byte cp.async pieces, zero-filled past the tokens
+            bulk_mask &= ~(1u << buf);
+            const int nk = (n * C::kKBytes + 15) >> 4;
             for (int q = lane; q < C::kKStage / 16; q += 32) cp16_zfill(dk + 16 * q, q < nk ? sk + 16 * q : kbase, q < nk);
             if constexpr (C::kRawV) {
                 for (int q = lane; q < kMmaChunk * 16; q += 32) {
@@ -477,6 +541,7 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
                 const int nr = (2 * n + 15) >> 4;
                 if (lane < 4) cp16_zfill(dr + 16 * lane, lane < nr ? sr + 16 * lane : rnbase, lane < nr);
             }
+            cp_async_commit();
         };
 
         // accumulators: n-tile nt, m-tile m; columns (2t, 2t+1) = head 4 nt + t, (hi, lo) parts
@@ -496,11 +561,15 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
         int64_t c = x + warp;
         auto live = [&](int64_t cc) { return cc < xe && tok0(cc) < L; };
         if (live(c)) issue(0, c);
-        cp_async_commit();
         for (int it = 0; live(c); ++it, c += kW) {
             if (live(c + kW)) issue((it + 1) & 1, c + kW);
-            cp_async_commit();
-            cp_async_wait<1>();
+            const int cb = it & 1;
+            if (bulk_mask & (1u << cb)) {
+                copies_ok &= mbar_wait(bar_s + 8 * cb, (phase >> cb) & 1u);
+                phase ^= 1u << cb;
+            } else {
+                cp_async_wait<0>();
+            }
             __syncwarp();
             const int nvalid = min(kMmaChunk, L - tok0(c));
             const uint32_t ks_s = stage_s + (it & 1) * C::kWarpStage, vs_s = ks_s + C::kKStage;
@@ -676,6 +745,7 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) lrun[nt] += __shfl_xor_sync(kFull, lrun[nt], off);
         }
+        const bool seg_ok = __syncthreads_and(copies_ok ? 1 : 0) != 0;
         // ---- merge the eight warps (rounds: 4 -> 2 -> 1), then warp 0 writes the partials
 #pragma unroll
         for (int half = kW / 2; half >= 1; half >>= 1) {
@@ -727,7 +797,7 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
                         for (int r = 0; r < 2; ++r) pr[4 + acc_dim<C::kRegV>(m, r, g)] = ov[nt][m][r];
                     if (g == 0) {
                         pr[0] = mrun[nt];
-                        pr[1] = lrun[nt];
+                        pr[1] = seg_ok ? lrun[nt] : __int_as_float(0x7fc00000);   // NaN marks a failed copy
                     }
                 }
             }
