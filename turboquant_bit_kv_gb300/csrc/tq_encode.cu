@@ -34,9 +34,12 @@
 //     tile, which the CTA stores with coalesced 16-byte stores (or block by
 //     block for strided / scattered destinations).
 
+#include <cuda.h>   // CUtensorMap and its enums (the encoder itself comes from the driver entry point)
+
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -349,7 +352,8 @@ __global__ void __launch_bounds__(kEncThreads, 3) encode_kernel(const __grid_con
 // registers, which already come in float2 pairs.
 // ---------------------------------------------------------------------------
 
-constexpr int kRowPitch = 272;              // 256-byte bf16 row + 16-byte pad
+constexpr int kPlainPitch = 272;           // 256-byte bf16 row + 16-byte pad
+constexpr int kRowPitch = kPlainPitch;
 constexpr int kWarpRows = 16;               // vectors per warp tile
 constexpr int kWarpStage = kWarpRows * kRowPitch;
 
@@ -390,6 +394,22 @@ __device__ __forceinline__ float elem_smem(const uint8_t *row, int j) {
     else return __half2float(__ushort_as_half(b));
 }
 
+// Element j of row r of a staged tile: SW = false: rows of kPlainPitch bytes;
+// SW = true: the tensor-core layout of a 128-row tile (two 64-column blocks
+// of 16 KB, 128-byte rows whose 16-byte chunks are XOR-swizzled by the row's
+// position in its 8-row group).
+template <int DT, bool SW>
+__device__ __forceinline__ float elem_at(const uint8_t *base, int r, int j) {
+    if constexpr (SW) {
+        const int off = (j >> 6) * 16384 + r * 128 + ((((j & 63) >> 3) ^ (r & 7)) << 4) + (j & 7) * 2;
+        const uint16_t b = *reinterpret_cast<const uint16_t *>(base + off);
+        if constexpr (DT == TQ_BF16) return __uint_as_float((uint32_t)b << 16);
+        else return __half2float(__ushort_as_half(b));
+    } else {
+        return elem_smem<DT>(base + r * kPlainPitch, j);
+    }
+}
+
 // fp16 of the L2 norm of row `row` (128 values of dtype DT in shared memory):
 // double-float sum of squares over the quad (lane t sums 32t..32t+31), one
 // rounding.  Every lane of the warp calls it (shuffles inside); out of line
@@ -419,15 +439,15 @@ __device__ __noinline__ unsigned short exact_norm_quad(const uint8_t *row, int t
 // its largest magnitude) so the float32 transform and the cell quantiser work
 // in range (codes do not depend on the scale); a zero row gets code L/2
 // everywhere.  Out of line: such rows essentially never occur.
-template <int BITS, int DT>
-__device__ __noinline__ void encode_row_slow(const uint8_t *row, const float2 *tab, float grid,
+template <int BITS, int DT, bool SW>
+__device__ __noinline__ void encode_row_slow(const uint8_t *base, int r, const float2 *tab, float grid,
                                              const uint32_t (&signs)[4], uint8_t *blk) {
     constexpr int BB = BlockFmt<BITS>::kBytes;
     float v[kD];
     double sd = 0.0;
     float amax = 0.f;
     for (int j = 0; j < kD; ++j) {
-        v[j] = elem_smem<DT>(row, j);
+        v[j] = elem_at<DT, SW>(base, r, j);
         sd = fma((double)v[j], (double)v[j], sd);
         amax = fmaxf(amax, fabsf(v[j]));
     }
@@ -664,7 +684,7 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_mma_kernel(const __grid
             const bool o0 = __shfl_sync(kFull, oor[0], (lane & 7) * 4);   // row lane & 7
             const bool o1 = __shfl_sync(kFull, oor[1], (lane & 7) * 4);   // row 8 + (lane & 7)
             if (lane < kWarpRows && ((lane >> 3) ? o1 : o0))
-                encode_row_slow<BITS, DT>(rows + lane * kRowPitch, tab, a.grid, a.signs, sm_out + lane * BB);
+                encode_row_slow<BITS, DT, false>(rows, lane, tab, a.grid, a.signs, sm_out + lane * BB);
             __syncwarp();
         }
 
@@ -732,6 +752,416 @@ int launch(const EncArgs &a, cudaStream_t st) {
     return launch_status();
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 variant for bf16 / fp16 rows (the default path for them).
+//
+// The whole rotation u = H (D x) of 128 rows at a time is one dense
+// contraction U[128 rows x 128] = X[128 x 128] * (H D)^T, exact on the 5th-
+// generation tensor cores (bf16/fp16 inputs times +-1, float32 accumulate):
+// the row tile arrives by TMA (two 64-column boxes, 128-byte swizzle) into
+// shared memory, H D sits in shared memory in the same layout, eight
+// tcgen05.mma (M 128, N 128, K 16) accumulate into tensor memory, and each
+// of the 128 rows is read from tensor memory (tcgen05.ld) by two epilogue
+// threads, one per 64-column half, and quantised: norm from the sum of squares (Parseval), then the cell-table
+// quantiser of the mma.sync kernel, codes packed straight into its block.
+// One producer warp issues the TMA loads and the MMAs; two stages of row
+// tiles and accumulators let the loads and MMAs of tile i + 1 run under the
+// epilogue of tile i.  Every mbarrier wait is bounded.
+// ---------------------------------------------------------------------------
+
+constexpr int kTcRows = 128;                          // rows per tile = MMA M = tensor-memory lanes
+constexpr int kTcEpiWarps = 8;                      // two per 32-row group: column halves
+constexpr int kTcThreads = 32 * (kTcEpiWarps + 1);    // + one producer warp
+constexpr int kTcTileBytes = kTcRows * 256;           // one row tile (two 16 KB column blocks)
+constexpr uint32_t kTcCols = 256;                     // tensor-memory columns: two 128-column accumulators
+constexpr int kTcSpin = 1 << 22;                      // bound of every mbarrier wait (polls)
+
+template <int BITS>
+struct TcSmem {
+    static constexpr int BB = 2 + 16 * BITS;
+    static constexpr int kB = 0;                                     // H D, 32 KB (1024-byte aligned)
+    static constexpr int kA = kB + kTcTileBytes;                     // two row tiles
+    static constexpr int kOut = kA + 2 * kTcTileBytes;               // 128 blocks
+    static constexpr int kTab = kOut + ((kTcRows * BB + 15) & ~15);  // cell table, 128 x 8 B
+    static constexpr int kPart = kTab + kBuckets * 8;                // per-row partial sums of squares, [2][128]
+    static constexpr int kBars = kPart + 2 * kTcRows * 4;             // full[2], mma[2], empty[2]
+    static constexpr int kSlot = kBars + 6 * 8;                      // tensor-memory base address
+    static constexpr int kTotal = kSlot + 16 + 1024;                 // + alignment slack of the base
+};
+
+__device__ __forceinline__ void tc_mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void tc_mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tc_mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for the phase of parity `parity`; false when it gave up.
+__device__ __forceinline__ bool tc_mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kTcSpin; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (i >= 16) __nanosleep(64);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tc_tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle layout: start address >> 4, leading byte offset 1 (unused with this
+// swizzle), stride byte offset 1024 >> 4 (8 rows of 128 bytes), descriptor
+// version 1, layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: float32 accumulator, A and B of dtype
+// DT (bf16 = 1, fp16 = 0), both K-major, N = 128, M = 128.
+template <int DT>
+__host__ __device__ constexpr uint32_t tc_idesc() {
+    return (1u << 4) | ((DT == TQ_BF16 ? 1u : 0u) << 7) | ((DT == TQ_BF16 ? 1u : 0u) << 10) | ((128u >> 3) << 17) |
+           ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive float32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// fp16 of the L2 norm of row r of a tensor-core row tile: double-float sum of
+// the exact squares, one rounding (near an fp16 rounding boundary only).
+template <int DT>
+__device__ __noinline__ unsigned short exact_norm_row(const uint8_t *tile, int r) {
+    SumSq2 acc;
+    for (int j = 0; j < kD; ++j) acc.add(elem_at<DT, true>(tile, r, j));
+    return acc.sqrt_fp16();
+}
+
+template <int BITS, int DT>
+// two CTAs (2 x 288 threads) per SM
+__global__ void __launch_bounds__(kTcThreads, 2)
+    encode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ EncArgs a) {
+    using S = TcSmem<BITS>;
+    constexpr int BB = S::BB;
+    __shared__ __align__(16) float2 s_tab[kBuckets];   // cell table at a fixed shared address
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    // 1024-byte aligned base: the 128-byte swizzle is a function of address bits 4..9
+    const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base_s - raw_s);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bars = base_s + S::kBars;   // full[s] at 8s, mma[s] at 16 + 8s, empty[s] at 32 + 8s
+
+    // ---- setup: (H D) in the swizzled K-major layout, cell table, barriers, tensor memory
+    for (int q = threadIdx.x; q < kTcRows * 16; q += kTcThreads) {
+        const int n = q >> 4, kc = q & 15;   // row n of H D (an output of u), 8-column chunk kc
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t pair = 0;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int k = 8 * kc + 2 * j + e;
+                const uint32_t neg = ((uint32_t)__popc(n & k) & 1u) ^ ((a.signs[k >> 5] >> (k & 31)) & 1u);
+                const uint32_t one = DT == TQ_BF16 ? (neg ? 0xBF80u : 0x3F80u) : (neg ? 0xBC00u : 0x3C00u);
+                pair |= one << (16 * e);
+            }
+            w[j] = pair;
+        }
+        const int off = S::kB + (kc >> 3) * 16384 + n * 128 + (((kc & 7) ^ (n & 7)) << 4);
+        *reinterpret_cast<uint4 *>(smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    float2 *tab = s_tab;
+    for (int j = threadIdx.x; j < kBuckets; j += kTcThreads) tab[j] = a.table[j];
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(bars + 8 * i, 1);                 // full: the producer's arrival + the TMA bytes
+            tc_mbar_init(bars + 16 + 8 * i, 1);            // mma: tcgen05.commit
+            tc_mbar_init(bars + 32 + 8 * i, kTcEpiWarps);  // empty: one arrival per epilogue warp
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base_s + S::kSlot),
+                     "r"(kTcCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // (H D) was written by ordinary stores and is read by the tensor cores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kSlot);
+
+    const int64_t ntiles = (a.n_vec + kTcRows - 1) / kTcRows;
+    if (warp == kTcEpiWarps) {
+        // ---- producer: row tiles by TMA, then eight MMAs into the stage's accumulator
+        if (lane == 0) {
+            const uint32_t idesc = tc_idesc<DT>();
+            int i = 0;
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+                const int st = i & 1;
+                const uint32_t use = (uint32_t)(i >> 1);
+                if (i >= 2) tc_mbar_wait(bars + 32 + 8 * st, (use - 1u) & 1u);   // stage released
+                tc_fence_after();
+                const uint32_t a_s = base_s + S::kA + st * kTcTileBytes;
+                tc_mbar_expect_tx(bars + 8 * st, kTcTileBytes);
+                tc_tma_load_2d(a_s, &tmap, 0, (int)(tile * kTcRows), bars + 8 * st);
+                tc_tma_load_2d(a_s + 16384, &tmap, 64, (int)(tile * kTcRows), bars + 8 * st);
+                tc_mbar_wait(bars + 8 * st, use & 1u);
+                const uint32_t d = tmem + (uint32_t)(st * 128);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
+                    tc_mma(d, tc_desc_sw128(a_s + off), tc_desc_sw128(base_s + S::kB + off), idesc, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(bars + 16 + 8 * st);
+            }
+        }
+    } else {
+        // ---- epilogue: warp w reads tensor-memory lanes (= tile rows) 32 (w & 3) .. + 31, columns
+        // 64 hf .. + 63 (hf = w >> 2); the two warps of a row group meet on named barrier 1 + (w & 3)
+        const int grp = warp & 3, hf = warp >> 2;
+        const int r = 32 * grp + lane;
+        const uint32_t pair_bar = 1u + (uint32_t)grp;
+        float *part = reinterpret_cast<float *>(smem + S::kPart);
+        uint8_t *sm_out = smem + S::kOut;
+        const uint32_t tab_s = (uint32_t)__cvta_generic_to_shared(s_tab);
+        const float2 off2 = make_float2(1572928.f, 1572928.f);   // 64 + 1.5 * 2^20
+        int i = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+            const int st = i & 1;
+            tc_mbar_wait(bars + 16 + 8 * st, (uint32_t)(i >> 1) & 1u);
+            tc_fence_after();
+            const int64_t v0 = tile * kTcRows;
+            const int nv = (int)min64(kTcRows, a.n_vec - v0);
+            const uint8_t *tile_s = smem + S::kA + st * kTcTileBytes;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(st * 128 + 64 * hf);
+            // ---- norm: sum of squares of u (= 128 ||x||^2), the two halves added in a fixed order
+            float uu[2][32];
+            tc_ld32(taddr, uu[0]);
+            tc_ld32(taddr + 32, uu[1]);
+            tc_wait_ld();
+            float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const float2 p2 = make_float2(uu[c][k], uu[c][k + 1]);
+                    q2 = __ffma2_rn(p2, p2, q2);
+                }
+            part[hf * kTcRows + r] = q2.x + q2.y;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            const float ss = part[r] + part[kTcRows + r];
+            const bool oor = !(ss >= 1.0097419586828951e-28f /* 128 * 2^-100 */ && ss <= 1.2676506002282294e30f);
+            const float sc = sqrtf(ss);
+            const float nrm = sc * 0.08838834764831845f;
+            uint8_t *blk = sm_out + r * BB;
+            if (hf == 0) {
+                unsigned short n16 = __half_as_ushort(__float2half_rn(nrm));
+                // near an fp16 rounding boundary: exact norm, the warp working on one such row at a time
+                uint32_t need = __ballot_sync(kFull, near_fp16_tie_fast(nrm) && !oor && r < nv);
+                while (need) {
+                    const int src = __ffs(need) - 1;
+                    need &= need - 1;
+                    SumSq2 acc;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc.add(elem_at<DT, true>(tile_s, 32 * grp + src, 4 * lane + q));
+                    float s1 = acc.s, c1 = acc.c;
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+                        const float os = __shfl_xor_sync(kFull, s1, o), oc = __shfl_xor_sync(kFull, c1, o);
+                        float ns, ne;
+                        two_sum(s1, os, ns, ne);
+                        s1 = ns;
+                        c1 = c1 + oc + ne;
+                    }
+                    SumSq2 tot;
+                    tot.s = s1;
+                    tot.c = c1;
+                    if (lane == src) n16 = tot.sqrt_fp16();
+                }
+                *reinterpret_cast<uint16_t *>(blk) = n16;
+            }
+
+            // ---- quantise and pack this half of the row's codes: code = base - [y >= boundary]
+            // (set.ge gives 0 / -1), accumulated straight into the packed words
+            const float cs = a.grid / sc;
+            const float2 cs2 = make_float2(cs, cs);
+            uint16_t *b16 = reinterpret_cast<uint16_t *>(blk + 2);
+            constexpr int PER = BITS == 4 ? 4 : 8;   // codes per 16-bit word of the (low) plane
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float *u = uu[c];
+                const int cc = 2 * hf + c;   // 32-column chunk of the row
+                uint32_t hi = 0;             // 3-bit: the 32 high bits of the chunk
+#pragma unroll
+                for (int g = 0; g < 32 / PER; ++g) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int e = 0; e < PER; e += 2) {
+                        const int k = PER * g + e;
+                        const float2 yp = __fmul2_rn(make_float2(u[k], u[k + 1]), cs2);
+                        const float2 tt = __fadd2_rn(yp, off2);
+                        const float2 ex = lds_f2(tab_s + (__float_as_uint(tt.x) & 0x3F8u));
+                        const float2 ey = lds_f2(tab_s + (__float_as_uint(tt.y) & 0x3F8u));
+                        if constexpr (BITS == 3) {
+                            const uint32_t c0 = __float_as_uint(ex.y) - set_ge(yp.x, ex.x);
+                            const uint32_t c1 = __float_as_uint(ey.y) - set_ge(yp.y, ey.x);
+                            w |= ((c0 & 3u) << (2 * e)) | ((c1 & 3u) << (2 * e + 2));
+                            hi |= ((c0 >> 2) << k) | ((c1 >> 2) << (k + 1));
+                        } else {
+                            constexpr int B = BITS;
+                            w += __float_as_uint(ex.y) << (B * e);
+                            w -= set_ge(yp.x, ex.x) << (B * e);
+                            w += __float_as_uint(ey.y) << (B * e + B);
+                            w -= set_ge(yp.y, ey.x) << (B * e + B);
+                        }
+                    }
+                    b16[(32 / PER) * cc + g] = (uint16_t)w;
+                }
+                if constexpr (BITS == 3) {
+                    uint16_t *h16 = reinterpret_cast<uint16_t *>(blk + 34);
+                    h16[2 * cc] = (uint16_t)hi;
+                    h16[2 * cc + 1] = (uint16_t)(hi >> 16);
+                }
+            }
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");   // both halves of the 32 blocks written
+            if (hf == 0 && oor && r < nv) encode_row_slow<BITS, DT, true>(tile_s, r, tab, a.grid, a.signs, blk);
+            if (__any_sync(kFull, oor)) asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+
+            // ---- release the stage (accumulator and row tile), then store the group's 32 blocks
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(bars + 32 + 8 * st);
+            const int rows = max(0, min(32, nv - 32 * grp));
+            if (a.contiguous) {
+                uint8_t *dst = a.out + (v0 + 32 * grp) * BB;
+                const uint8_t *src = sm_out + 32 * grp * BB;
+                const int nbytes = rows * BB, nch = nbytes >> 4;
+                for (int q = lane + 32 * hf; q < nch; q += 64)
+                    reinterpret_cast<uint4 *>(dst)[q] = reinterpret_cast<const uint4 *>(src)[q];
+                for (int q = (nch << 3) + lane + 32 * hf; q < (nbytes >> 1); q += 64)
+                    reinterpret_cast<uint16_t *>(dst)[q] = reinterpret_cast<const uint16_t *>(src)[q];
+            } else {
+                for (int row = 32 * grp + hf; row < 32 * grp + rows; row += 2) {
+                    const int64_t di = a.dst_index ? a.dst_index[v0 + row] : (v0 + row);
+                    uint16_t *d = reinterpret_cast<uint16_t *>(a.out + di * a.out_stride);
+                    const uint16_t *sp = reinterpret_cast<const uint16_t *>(sm_out + row * BB);
+                    for (int q = lane; q < BB / 2; q += 32) d[q] = sp[q];
+                }
+            }
+        }
+    }
+
+    // ---- teardown: every MMA was waited for and every tensor-memory load completed
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
+}
+
+typedef CUresult (*TensorMapEncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                           const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                           const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                           CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once (the library links only the runtime).
+TensorMapEncodeTiledFn tensor_map_encoder() {
+    static TensorMapEncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<TensorMapEncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Launch the tcgen05 kernel; returns 1 when the rows cannot be described by a
+// tensor map (the caller then uses the mma.sync kernel).
+template <int BITS, int DT>
+int launch_tc(const EncArgs &a, cudaStream_t st) {
+    TensorMapEncodeTiledFn enc = tensor_map_encoder();
+    if (!enc || a.n_vec > 0x7FFFFFFFLL - kTcRows) return 1;
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)a.n_vec};
+    const cuuint64_t gstride[1] = {(cuuint64_t)a.x_stride};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTcRows};
+    const cuuint32_t estride[2] = {1, 1};
+    if (enc(&map, DT == TQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<uint8_t *>(a.x), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return 1;
+    static int done[64] = {0};
+    if (set_smem_limit((const void *)encode_tc_kernel<BITS, DT>, TcSmem<BITS>::kTotal, done) != TQ_OK)
+        return TQ_ERR_CUDA;
+    const int64_t ntiles = (a.n_vec + kTcRows - 1) / kTcRows;
+    const int grid = (int)std::min<int64_t>(ntiles, 2 * (int64_t)sm_count());
+    encode_tc_kernel<BITS, DT><<<grid, kTcThreads, TcSmem<BITS>::kTotal, st>>>(map, a);
+    return launch_status();
+}
+
+template <int BITS, int DT>
+int launch_16bit(const EncArgs &a, cudaStream_t st) {
+    const int r = launch_tc<BITS, DT>(a, st);
+    return r == 1 ? launch_mma<BITS, DT>(a, st) : r;
+}
+
 // Cell table of a codebook.  With z = G y, cell j holds
 // z + 64 in [j - 1/16, j + 15/16) (the cells of rounding z + 64 to 1/8 and
 // taking the integer part); G is the smallest integer above
@@ -790,14 +1220,14 @@ extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x
     cudaStream_t st = (cudaStream_t)stream;
     switch (cb->bits * 8 + x_dtype) {
         case 2 * 8 + TQ_F32: return launch<2, TQ_F32>(a, st);
-        case 2 * 8 + TQ_BF16: return launch_mma<2, TQ_BF16>(a, st);
-        case 2 * 8 + TQ_F16: return launch_mma<2, TQ_F16>(a, st);
+        case 2 * 8 + TQ_BF16: return launch_16bit<2, TQ_BF16>(a, st);
+        case 2 * 8 + TQ_F16: return launch_16bit<2, TQ_F16>(a, st);
         case 3 * 8 + TQ_F32: return launch<3, TQ_F32>(a, st);
-        case 3 * 8 + TQ_BF16: return launch_mma<3, TQ_BF16>(a, st);
-        case 3 * 8 + TQ_F16: return launch_mma<3, TQ_F16>(a, st);
+        case 3 * 8 + TQ_BF16: return launch_16bit<3, TQ_BF16>(a, st);
+        case 3 * 8 + TQ_F16: return launch_16bit<3, TQ_F16>(a, st);
         case 4 * 8 + TQ_F32: return launch<4, TQ_F32>(a, st);
-        case 4 * 8 + TQ_BF16: return launch_mma<4, TQ_BF16>(a, st);
-        case 4 * 8 + TQ_F16: return launch_mma<4, TQ_F16>(a, st);
+        case 4 * 8 + TQ_BF16: return launch_16bit<4, TQ_BF16>(a, st);
+        case 4 * 8 + TQ_F16: return launch_16bit<4, TQ_F16>(a, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
 }
