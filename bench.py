@@ -431,7 +431,7 @@ def plan_storage(tq, wl, dev, stream, seed, batch):
                                 stream=stream)
 
     ops = [Op("serialize", "serialize", ser, each_way, 2, nvec),
-           Op("deserialize", "deserialize", des, each_way, 2 * Lc, nvec)]
+           Op("deserialize", "deserialize", des, each_way, 2 if T % bs == 0 else 2 * Lc, nvec)]
 
     def e2e():
         hx = _pinned(x)

@@ -20,9 +20,10 @@
 //     table index is the code byte (4-bit), the nibble (2-bit), or the low
 //     nibble of the 2-bit plane plus the two high-plane bits (3-bit).
 //   * 2-bit values: a thread owns dims 16g..16g+15 (the MMA's m-rows
-//     permuted), one 32-bit code word per token; a fragment register holds
-//     one dim of two tokens, built by one byte permute from an 8-byte
-//     register table of the four fp16 centroids.
+//     permuted so that the two rows of an m-tile are dims d and d + 4), one
+//     32-bit code word per token; a fragment register holds one dim of two
+//     tokens, built by one byte permute from an 8-byte register table of the
+//     four fp16 centroids.
 //   * 3- and 4-bit values: each lane dequantises half of one token's row
 //     into an fp16 tile in shared memory (pairs of dims through the same
 //     kind of table as keys), and the fragments are read back transposed
@@ -345,7 +346,7 @@ __device__ __forceinline__ void dequant_value_half(uint32_t blk_s, int hf, uint3
 // Dim of accumulator row `r` (0: fragment row g, 1: row g + 8) of m-tile m.
 template <bool REGV>
 __device__ __forceinline__ int acc_dim(int m, int r, int g) {
-    return REGV ? 16 * g + 2 * m + r : 16 * m + g + 8 * r;
+    return REGV ? 16 * g + 8 * (m >> 2) + (m & 3) + 4 * r : 16 * m + g + 8 * r;
 }
 
 template <int KB, int VB, bool QJL, int NT>
@@ -694,14 +695,15 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
                     const uint32_t y01 = prmt(w2[0], w3[0], 0x5140u), y23 = prmt(w2[0], w3[0], 0x7362u);
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
-                        // m-tile m: row g <-> dim 16g + 2m, row g + 8 <-> dim 16g + 2m + 1
-                        const int j0 = 2 * m, j1 = 2 * m + 1;
-                        const uint32_t xs = (j0 < 8) ? x01 : x23, ys = (j0 < 8) ? y01 : y23;
-                        const int sh0 = 16 * ((j0 >> 2) & 1) + 2 * (j0 & 3), sh1 = 16 * ((j1 >> 2) & 1) + 2 * (j1 & 3);
-                        const uint32_t a0 = prmt(vlo, vhi, ((xs >> sh0) & 0x0303u) * 0x11u + 0x4040u);
-                        const uint32_t a1 = prmt(vlo, vhi, ((xs >> sh1) & 0x0303u) * 0x11u + 0x4040u);
-                        const uint32_t a2 = prmt(vlo, vhi, ((ys >> sh0) & 0x0303u) * 0x11u + 0x4040u);
-                        const uint32_t a3 = prmt(vlo, vhi, ((ys >> sh1) & 0x0303u) * 0x11u + 0x4040u);
+                        // m-tile m: row g <-> dim 16g + 8 (m >> 2) + (m & 3), row g + 8 <-> that dim + 4.
+                        // One spread of a code word gives the selectors of both: per byte
+                        // (code, code + 4) nibbles, low half = dim d, high half = dim d + 4.
+                        const uint32_t xs = (m < 4) ? x01 : x23, ys = (m < 4) ? y01 : y23;
+                        const int sh = 2 * (m & 3);
+                        const uint32_t sx = ((xs >> sh) & 0x03030303u) * 0x11u + 0x40404040u;
+                        const uint32_t sy = ((ys >> sh) & 0x03030303u) * 0x11u + 0x40404040u;
+                        const uint32_t a0 = prmt(vlo, vhi, sx), a1 = prmt(vlo, vhi, sx >> 16);
+                        const uint32_t a2 = prmt(vlo, vhi, sy), a3 = prmt(vlo, vhi, sy >> 16);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], a0, a1, a2, a3, b0[nt], b1[nt]);
                     }

@@ -452,7 +452,16 @@ extern "C" int tq_serde_deserialize(const uint8_t *src, int elem_dtype, int num_
     const uint8_t *comp = src + g.raw_first;
     const int64_t Lc = g.qe - g.qs;
     const int64_t layer_slots = g.nblk * g.bs * g.H;
-    for (int64_t li = 0; li < Lc; ++li) {
+    if (Lc > 0 && g.T % g.bs == 0) {
+        // no padding slots: the compressed keys (values) of all middle layers are one run of
+        // slots and one run of rows
+        r = tq_decode_kv(comp, g.slot, Lc * g.T * g.H, kcb, signs, d + g.qs * layer_bytes, elem_dtype, kD, stream);
+        if (r != TQ_OK) return r;
+        r = tq_decode_kv(comp + g.kbb, g.slot, Lc * g.T * g.H, vcb, signs, d + (g.L + g.qs) * layer_bytes,
+                         elem_dtype, kD, stream);
+        if (r != TQ_OK) return r;
+    }
+    for (int64_t li = 0; li < Lc && g.T % g.bs != 0; ++li) {
         const int64_t l = g.qs + li;
         const uint8_t *lay = comp + li * layer_slots * g.slot;
         r = tq_decode_kv(lay, g.slot, g.T * g.H, kcb, signs, d + l * layer_bytes, elem_dtype, kD, stream);

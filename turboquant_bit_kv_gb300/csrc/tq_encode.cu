@@ -1093,10 +1093,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 for (int q = (nch << 3) + lane + 32 * hf; q < (nbytes >> 1); q += 64)
                     reinterpret_cast<uint16_t *>(dst)[q] = reinterpret_cast<const uint16_t *>(src)[q];
             } else {
-                for (int row = 32 * grp + hf; row < 32 * grp + rows; row += 2) {
-                    const int64_t di = a.dst_index ? a.dst_index[v0 + row] : (v0 + row);
+                // destination rows of the group, fetched once (one coalesced load), then block by block
+                const int64_t my_di = lane < rows ? (a.dst_index ? a.dst_index[v0 + 32 * grp + lane]
+                                                                 : v0 + 32 * grp + lane)
+                                                  : 0;
+                for (int j = hf; j < rows; j += 2) {
+                    const int64_t di = __shfl_sync(kFull, my_di, j);
                     uint16_t *d = reinterpret_cast<uint16_t *>(a.out + di * a.out_stride);
-                    const uint16_t *sp = reinterpret_cast<const uint16_t *>(sm_out + row * BB);
+                    const uint16_t *sp = reinterpret_cast<const uint16_t *>(sm_out + (32 * grp + j) * BB);
                     for (int q = lane; q < BB / 2; q += 32) d[q] = sp[q];
                 }
             }
