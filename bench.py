@@ -69,13 +69,13 @@ CSRC = os.path.join(ROOT, "turboquant_bit_kv_gb300", "csrc")
 # the sources each kernel group is built from (profiled DRAM traffic is only
 # reported while these are unchanged since the capture)
 KERNEL_SOURCES = {
-    "encode": ["tq_encode.cu", "tq_device.cuh"],
-    "append": ["tq_encode.cu", "tq_device.cuh"],
+    "encode": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
+    "append": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
                   "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_g1.cu",
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
-    "qjl": ["tq_codec.cu", "tq_device.cuh"],
-    "serialize": ["tq_encode.cu", "tq_codec.cu", "tq_device.cuh"],
+    "qjl": ["tq_qjl.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
+    "serialize": ["tq_encode.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "deserialize": ["tq_decode.cu", "tq_codec.cu", "tq_device.cuh"],
 }
 TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")

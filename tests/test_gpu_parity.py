@@ -354,34 +354,72 @@ def test_attention_qjl_with_packed_values(env):
 
 # ------------------------------------------------------------------ QJL encode
 
-def test_qjl_encode_matches_oracle(env):
+def _check_qjl(env, k, bits, k_row_stride=None, block_pad=0):
+    """tq_qjl_encode on keys k (CPU tensor [n, 128]) and oracle-made blocks
+    against the oracle: bits may differ only where |(S r)_j| <= 1e-5 ||S_j|| ||r||,
+    the fp16 residual norm by one step only within 4e-6 of an fp16 tie."""
     tq = env["tq"]
     dev = env["dev"]
-    w = workloads.qjl_keys(B=1, Hq=4, Hkv=2, T=700, seed=6)
-    k = w["k"].reshape(-1, D)
-    S = w["S"]
-    c3, _, b32 = env["books"][3]
+    S = workloads.qjl_keys(B=1, Hq=1, Hkv=1, T=1, seed=0)["S"]
+    c, _, b32 = env["books"][bits]
     kx = k.double().numpy()
-    idx, n16, _ = codec.encode(kx, env["s"], b32)
-    blk = torch.from_numpy(codec.pack_block(idx, n16, 3)).to(dev)
     n = kx.shape[0]
-    bits = torch.zeros((n, 16), dtype=torch.uint8, device=dev)
-    rn = torch.zeros((n,), dtype=torch.int16, device=dev)
-    tq.tq_qjl_encode(k.to(dev), blk, env["cbs"][3], env["signs"], S.to(dev), bits, rn)
+    idx, n16, _ = codec.encode(kx, env["s"], b32)
+    packed = codec.pack_block(idx, n16, bits)
+    bb = packed.shape[1]
+    stride = bb + block_pad
+    blk_host = np.zeros((n, stride), dtype=np.uint8)
+    blk_host[:, :bb] = packed
+    blk = torch.from_numpy(blk_host.reshape(-1)).to(dev)
+    kd = k.to(dev)
+    if k_row_stride is not None:
+        wide = torch.zeros((n, k_row_stride), dtype=k.dtype, device=dev)
+        wide[:, :D] = kd
+        kd = wide[:, :D]
+    fb, bits_t = _guarded(n * 16, dev)
+    fr, rn_b = _guarded(n * 2, dev)
+    rn = rn_b.view(torch.int16)
+    tq.tq_qjl_encode(kd, blk, env["cbs"][bits], env["signs"], S.to(dev), bits_t, rn, block_stride_bytes=stride)
     torch.cuda.synchronize()
-    ob, orn, proj = oracle.qjl_encode(kx, idx, n16, c3, env["s"], S.double().numpy())
-    gb = bits.cpu().numpy()
-    gbits = np.unpackbits(gb, axis=1, bitorder="little")
+    assert _guards_intact(fb) and _guards_intact(fr)
+    ob, orn, proj = oracle.qjl_encode(kx, idx, n16, c, env["s"], S.double().numpy())
+    gbits = np.unpackbits(bits_t.view(n, 16).cpu().numpy(), axis=1, bitorder="little")
     obits = np.unpackbits(ob, axis=1, bitorder="little")
     mism = gbits != obits
-    r = kx - codec.decode(idx, n16, c3, env["s"])
+    r = kx - codec.decode(idx, n16, c, env["s"])
     scale = np.linalg.norm(S.double().numpy(), axis=1)[None, :] * np.linalg.norm(r, axis=1)[:, None]
-    assert np.all(np.abs(proj[mism]) <= 1e-5 * scale[mism])
+    assert np.all(np.abs(proj[mism]) <= 1e-5 * scale[mism]), "%d sign bits differ beyond the bound" % (
+        np.sum(np.abs(proj[mism]) > 1e-5 * scale[mism]))
     grn = rn.cpu().numpy().view(np.uint16)
     diff = grn.astype(np.int64) - orn.astype(np.int64)
     assert np.all(np.abs(diff) <= 1)
     if np.any(diff != 0):
         assert np.all(fp16_tie_distance(np.linalg.norm(r, axis=1)[diff != 0]) < 4e-6)
+
+
+def test_qjl_encode_matches_oracle(env):
+    w = workloads.qjl_keys(B=1, Hq=4, Hkv=2, T=700, seed=6)
+    _check_qjl(env, w["k"].reshape(-1, D), 3)
+
+
+@pytest.mark.parametrize("bits,dtype,n,row_stride,block_pad", [
+    (2, torch.bfloat16, 129, None, 0),        # one full tile + 1 row
+    (4, torch.float16, 128, None, 0),         # exactly one tile
+    (3, torch.float16, 1, None, 0),           # a single key
+    (4, torch.bfloat16, 40000, None, 0),      # several tiles per CTA (the producer / epilogue pipeline)
+    (3, torch.bfloat16, 1000, 192, 4),        # strided key rows, padded block slots (2-byte offsets)
+    (2, torch.float32, 300, None, 2),         # float32 keys: CUDA-core kernel
+])
+def test_qjl_encode_widths_dtypes_layouts(env, bits, dtype, n, row_stride, block_pad):
+    w = workloads.qjl_keys(B=1, Hq=1, Hkv=1, T=n, seed=7 + bits)
+    _check_qjl(env, w["k"].reshape(-1, D).to(dtype), bits, k_row_stride=row_stride, block_pad=block_pad)
+
+
+def test_qjl_encode_outlier_keys(env):
+    # keys with a few large channels and widely spread norms
+    w = workloads.qwen_outlier(B=1, Hq=7, Hkv=1, T=1500, seed=9)
+    _check_qjl(env, w["k"].reshape(-1, D), 4)
+    _check_qjl(env, w["k"].reshape(-1, D), 2)
 
 
 # ------------------------------------------------------------------ serde

@@ -319,6 +319,9 @@ extern "C" int tq_qjl_encode(const void *k, int k_dtype, int64_t n_vec, int64_t 
     if (!aligned(k, 16) || (k_stride_elems * es) % 16 || !aligned(k_blocks, 2) || (block_stride_bytes & 1) ||
         !aligned(qjl_bits, 16) || !aligned(res_norm_f16, 2) || !aligned(S, 4))
         return TQ_ERR_ALIGN;
+    const int tc = qjl_encode_tc(k, k_dtype, n_vec, k_stride_elems * es, k_blocks, block_stride_bytes, cb->bits,
+                                 cb->centroids, signs.w, S, qjl_bits, res_norm_f16, (cudaStream_t)stream);
+    if (tc != 1) return tc;
     QjlArgs a;
     a.k = static_cast<const uint8_t *>(k);
     a.k_stride = k_stride_elems * es;

@@ -34,15 +34,13 @@
 //     tile, which the CTA stores with coalesced 16-byte stores (or block by
 //     block for strided / scattered destinations).
 
-#include <cuda.h>   // CUtensorMap and its enums (the encoder itself comes from the driver entry point)
-
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <mutex>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_tc.cuh"
 
 namespace tq {
 namespace {
@@ -774,7 +772,6 @@ constexpr int kTcEpiWarps = 8;                      // two per 32-row group: col
 constexpr int kTcThreads = 32 * (kTcEpiWarps + 1);    // + one producer warp
 constexpr int kTcTileBytes = kTcRows * 256;           // one row tile (two 16 KB column blocks)
 constexpr uint32_t kTcCols = 256;                     // tensor-memory columns: two 128-column accumulators
-constexpr int kTcSpin = 1 << 22;                      // bound of every mbarrier wait (polls)
 
 template <int BITS>
 struct TcSmem {
@@ -788,92 +785,6 @@ struct TcSmem {
     static constexpr int kSlot = kBars + 6 * 8;                      // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;                 // + alignment slack of the base
 };
-
-__device__ __forceinline__ void tc_mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void tc_mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void tc_mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Bounded wait for the phase of parity `parity`; false when it gave up.
-__device__ __forceinline__ bool tc_mbar_wait(uint32_t bar, uint32_t parity) {
-    for (int i = 0; i < kTcSpin; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (i >= 16) __nanosleep(64);
-    }
-    return false;
-}
-
-__device__ __forceinline__ void tc_tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand in the 128-byte
-// swizzle layout: start address >> 4, leading byte offset 1 (unused with this
-// swizzle), stride byte offset 1024 >> 4 (8 rows of 128 bytes), descriptor
-// version 1, layout type 2 (128-byte swizzle).
-__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of kind::f16: float32 accumulator, A and B of dtype
-// DT (bf16 = 1, fp16 = 0), both K-major, N = 128, M = 128.
-template <int DT>
-__host__ __device__ constexpr uint32_t tc_idesc() {
-    return (1u << 4) | ((DT == TQ_BF16 ? 1u : 0u) << 7) | ((DT == TQ_BF16 ? 1u : 0u) << 10) | ((128u >> 3) << 17) |
-           ((128u >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::
-            "r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive float32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // fp16 of the L2 norm of row r of a tensor-core row tile: double-float sum of
 // the exact squares, one rounding (near an fp16 rounding boundary only).
@@ -1115,42 +1026,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
 }
 
-typedef CUresult (*TensorMapEncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                           const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                           const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                           CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once (the library links only the runtime).
-TensorMapEncodeTiledFn tensor_map_encoder() {
-    static TensorMapEncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<TensorMapEncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // Launch the tcgen05 kernel; returns 1 when the rows cannot be described by a
 // tensor map (the caller then uses the mma.sync kernel).
 template <int BITS, int DT>
 int launch_tc(const EncArgs &a, cudaStream_t st) {
-    TensorMapEncodeTiledFn enc = tensor_map_encoder();
-    if (!enc || a.n_vec > 0x7FFFFFFFLL - kTcRows) return 1;
     CUtensorMap map;
-    const cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)a.n_vec};
-    const cuuint64_t gstride[1] = {(cuuint64_t)a.x_stride};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kTcRows};
-    const cuuint32_t estride[2] = {1, 1};
-    if (enc(&map, DT == TQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-            const_cast<uint8_t *>(a.x), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return 1;
+    if (!make_row_tile_map(&map, a.x, DT, a.n_vec, a.x_stride)) return 1;
     static int done[64] = {0};
     if (set_smem_limit((const void *)encode_tc_kernel<BITS, DT>, TcSmem<BITS>::kTotal, done) != TQ_OK)
         return TQ_ERR_CUDA;

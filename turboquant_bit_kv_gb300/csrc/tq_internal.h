@@ -28,6 +28,13 @@ int sm_count();
 // Raise a kernel's dynamic shared-memory limit once per process and device.
 int set_smem_limit(const void *kernel, int bytes, int *done_for_device);
 
+// QJL sketch of bf16 / fp16 keys on the tensor cores (tq_qjl.cu).  Returns 1
+// when it does not handle the call (other key dtypes, or rows no tensor map
+// can describe), else a TQ_ status.
+int qjl_encode_tc(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_bytes, const uint8_t *blocks,
+                  int64_t block_stride, int bits, const float *centroids, const uint32_t *signs, const float *S,
+                  uint8_t *qjl_bits, uint16_t *res_norm_f16, cudaStream_t st);
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
