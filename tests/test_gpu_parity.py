@@ -98,6 +98,28 @@ def test_encode_edge_vectors(env):
         assert n16[0] == 0 and np.all(idx == (1 << bits) // 2)      # zero vector
 
 
+def test_encode_listed_rows_in_full_groups(env):
+    """Zero, tiny and huge rows scattered through full 32-row groups (whose
+    blocks leave by bulk copy before the listed rows are finished), and a
+    tensor of zero rows with a few random ones, which overflows every CTA's
+    list of rows to finish."""
+    gen = np.random.default_rng(11)
+    x = gen.standard_normal((4096, D))
+    special = gen.choice(4096, 200, replace=False)
+    x[special[:80]] = 0.0
+    x[special[80:140]] *= 2.0**-110
+    x[special[140:]] *= 2.0**60
+    xt = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+    for bits in (2, 3, 4):
+        g = _encode_gpu(env, xt.to(env["dev"]), bits)
+        check_codes(g, bits, xt.double().numpy(), env["s"], env["books"][bits][2], "listed rows")
+    z = np.zeros((128 * 700, D))
+    z[::997] = gen.standard_normal((z[::997].shape[0], D))
+    zt = torch.tensor(z, dtype=torch.float32).to(torch.bfloat16)
+    g = _encode_gpu(env, zt.to(env["dev"]), 4)
+    check_codes(g, 4, zt.double().numpy(), env["s"], env["books"][4][2], "zero rows")
+
+
 def test_encode_scatter_dst_index_and_slot_stride(env):
     """Append-style scatter into a slot layout (K block then V block per slot)."""
     tq = env["tq"]

@@ -772,6 +772,7 @@ constexpr int kTcEpiWarps = 8;                      // two per 32-row group: col
 constexpr int kTcThreads = 32 * (kTcEpiWarps + 1);    // + one producer warp
 constexpr int kTcTileBytes = kTcRows * 256;           // one row tile (two 16 KB column blocks)
 constexpr uint32_t kTcCols = 256;                     // tensor-memory columns: two 128-column accumulators
+constexpr int kTcFixCap = 240;                        // rows a CTA can list for finishing after its main loop
 
 template <int BITS>
 struct TcSmem {
@@ -781,7 +782,8 @@ struct TcSmem {
     static constexpr int kOut = kA + 2 * kTcTileBytes;               // 128 blocks
     static constexpr int kTab = kOut + ((kTcRows * BB + 15) & ~15);  // cell table, 128 x 8 B
     static constexpr int kPart = kTab + kBuckets * 8;                // per-row partial sums of squares, [2][128]
-    static constexpr int kBars = kPart + 2 * kTcRows * 4;             // full[2], mma[2], empty[2]
+    static constexpr int kFix = kPart + 2 * kTcRows * 4;             // rows finished after the main loop
+    static constexpr int kBars = kFix + (4 + kTcFixCap) * 4;          // full[2], mma[2], empty[2]
     static constexpr int kSlot = kBars + 6 * 8;                      // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;                 // + alignment slack of the base
 };
@@ -793,6 +795,38 @@ __device__ __noinline__ unsigned short exact_norm_row(const uint8_t *tile, int r
     SumSq2 acc;
     for (int j = 0; j < kD; ++j) acc.add(elem_at<DT, true>(tile, r, j));
     return acc.sqrt_fp16();
+}
+
+// Finish one listed row from its values in memory (the row tile is gone by
+// then): rows outside float32's safe range get their whole block from the
+// exact path; rows near an fp16 rounding boundary get the correctly rounded
+// norm (double-float sum of squares).  Cold: a few rows per CTA at most.
+template <int BITS, int DT>
+__device__ __forceinline__ void finish_row(const EncArgs &a, const float2 *tab, int64_t v, bool whole) {
+    const uint8_t *xrow = a.x + v * a.x_stride;
+    const int64_t di = a.dst_index ? a.dst_index[v] : v;
+    uint8_t *dst = a.out + di * a.out_stride;
+    if (whole) {
+        encode_row_slow<BITS, DT, false>(xrow, 0, tab, a.grid, a.signs, dst);
+    } else {
+        SumSq2 acc;
+        for (int j = 0; j < kD; ++j) acc.add(elem_smem<DT>(xrow, j));
+        *reinterpret_cast<uint16_t *>(dst) = acc.sqrt_fp16();
+    }
+}
+
+// After a CTA's list overflowed: every one of its rows is checked again from
+// memory.  128 ||x||^2 outside [2^-92, 2^99] (a superset of the rows the main
+// loop sends to the exact path, whose sum of squares of u = H D x carries
+// float32 rounding) gets the whole block; every other row gets the correctly
+// rounded norm.
+template <int BITS, int DT>
+__device__ __forceinline__ void recheck_row(const EncArgs &a, const float2 *tab, int64_t v) {
+    SumSq2 acc;
+    const uint8_t *xrow = a.x + v * a.x_stride;
+    for (int j = 0; j < kD; ++j) acc.add(elem_smem<DT>(xrow, j));
+    const float s128 = (acc.s + acc.c) * 128.f;
+    finish_row<BITS, DT>(a, tab, v, !(s128 >= 2.0194839173657902e-28f /* 2^-92 */ && s128 <= 6.338253001141147e29f));
 }
 
 template <int BITS, int DT>
@@ -833,6 +867,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     for (int j = threadIdx.x; j < kBuckets; j += kTcThreads) tab[j] = a.table[j];
     if (threadIdx.x == 0) {
 #pragma unroll
+        reinterpret_cast<int *>(smem + S::kFix)[0] = 0;   // listed rows
+        reinterpret_cast<int *>(smem + S::kFix)[1] = 0;   // list overflowed
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(bars + 8 * i, 1);                 // full: the producer's arrival + the TMA bytes
             tc_mbar_init(bars + 16 + 8 * i, 1);            // mma: tcgen05.commit
@@ -885,8 +921,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int r = 32 * grp + lane;
         const uint32_t pair_bar = 1u + (uint32_t)grp;
         float *part = reinterpret_cast<float *>(smem + S::kPart);
+        int *fix = reinterpret_cast<int *>(smem + S::kFix);   // [0] count, [1] overflow, [4 ..] rows
         uint8_t *sm_out = smem + S::kOut;
         const uint32_t tab_s = (uint32_t)__cvta_generic_to_shared(s_tab);
+        // full 32-block groups of a contiguous destination leave by one bulk copy each
+        const bool bulk_out = a.contiguous != 0;
         const float2 off2 = make_float2(1572928.f, 1572928.f);   // 64 + 1.5 * 2^20
         int i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
@@ -911,6 +950,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     q2 = __ffma2_rn(p2, p2, q2);
                 }
             part[hf * kTcRows + r] = q2.x + q2.y;
+            // the previous tile's bulk store has read the group's blocks before they are rewritten
+            if (bulk_out && hf == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             const float ss = part[r] + part[kTcRows + r];
             const bool oor = !(ss >= 1.0097419586828951e-28f /* 128 * 2^-100 */ && ss <= 1.2676506002282294e30f);
@@ -918,30 +959,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const float nrm = sc * 0.08838834764831845f;
             uint8_t *blk = sm_out + r * BB;
             if (hf == 0) {
-                unsigned short n16 = __half_as_ushort(__float2half_rn(nrm));
-                // near an fp16 rounding boundary: exact norm, the warp working on one such row at a time
-                uint32_t need = __ballot_sync(kFull, near_fp16_tie_fast(nrm) && !oor && r < nv);
-                while (need) {
-                    const int src = __ffs(need) - 1;
-                    need &= need - 1;
-                    SumSq2 acc;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc.add(elem_at<DT, true>(tile_s, 32 * grp + src, 4 * lane + q));
-                    float s1 = acc.s, c1 = acc.c;
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) {
-                        const float os = __shfl_xor_sync(kFull, s1, o), oc = __shfl_xor_sync(kFull, c1, o);
-                        float ns, ne;
-                        two_sum(s1, os, ns, ne);
-                        s1 = ns;
-                        c1 = c1 + oc + ne;
+                *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__float2half_rn(nrm));
+                // rows whose norm lies within 2^-20 of an fp16 rounding boundary, or whose sum of
+                // squares leaves float32's safe range, are listed and finished after the main loop
+                const bool need = (oor || near_fp16_tie_fast(nrm)) && r < nv;
+                const uint32_t m = __ballot_sync(kFull, need);
+                if (m) {
+                    const int leader = __ffs(m) - 1;
+                    int base = 0;
+                    if (lane == leader) base = atomicAdd(&fix[0], __popc(m));
+                    base = __shfl_sync(kFull, base, leader);
+                    if (need) {
+                        const int slot = base + __popc(m & ((1u << lane) - 1u));
+                        if (slot < kTcFixCap) fix[4 + slot] = (int)(v0 + r) | (oor ? (int)0x80000000 : 0);
+                        else fix[1] = 1;
                     }
-                    SumSq2 tot;
-                    tot.s = s1;
-                    tot.c = c1;
-                    if (lane == src) n16 = tot.sqrt_fp16();
                 }
-                *reinterpret_cast<uint16_t *>(blk) = n16;
             }
 
             // ---- quantise and pack this half of the row's codes: code = base - [y >= boundary]
@@ -986,16 +1019,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     h16[2 * cc + 1] = (uint16_t)(hi >> 16);
                 }
             }
+            if (bulk_out) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // blocks -> bulk copy
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");   // both halves of the 32 blocks written
-            if (hf == 0 && oor && r < nv) encode_row_slow<BITS, DT, true>(tile_s, r, tab, a.grid, a.signs, blk);
-            if (__any_sync(kFull, oor)) asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
 
             // ---- release the stage (accumulator and row tile), then store the group's 32 blocks
             tc_fence_before();
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bars + 32 + 8 * st);
             const int rows = max(0, min(32, nv - 32 * grp));
-            if (a.contiguous) {
+            if (bulk_out && rows == 32) {
+                // 32 * BB bytes at a 16-byte aligned offset (32 * BB is a multiple of 16)
+                if (hf == 0 && lane == 0) {
+                    uint8_t *dst = a.out + (v0 + 32 * grp) * BB;
+                    const uint32_t src = (uint32_t)__cvta_generic_to_shared(sm_out + 32 * grp * BB);
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                                 "r"(32 * BB)
+                                 : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
+            } else if (a.contiguous) {
                 uint8_t *dst = a.out + (v0 + 32 * grp) * BB;
                 const uint8_t *src = sm_out + 32 * grp * BB;
                 const int nbytes = rows * BB, nch = nbytes >> 4;
@@ -1015,6 +1057,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     for (int q = lane; q < BB / 2; q += 32) d[q] = sp[q];
                 }
             }
+        }
+
+        // ---- finish the listed rows once every block of this CTA is in memory
+        if (bulk_out && hf == 0 && lane == 0) {
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
+        const int et = threadIdx.x;   // 0 .. 32 * kTcEpiWarps - 1
+        if (fix[1] == 0) {
+            const int nfix = min(fix[0], kTcFixCap);
+            for (int q = et; q < nfix; q += 32 * kTcEpiWarps) {
+                const uint32_t e = (uint32_t)fix[4 + q];
+                finish_row<BITS, DT>(a, s_tab, (int64_t)(e & 0x7FFFFFFFu), (e >> 31) != 0);
+            }
+        } else {
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+                for (int rr = et; rr < kTcRows; rr += 32 * kTcEpiWarps)
+                    if (tile * kTcRows + rr < a.n_vec) recheck_row<BITS, DT>(a, s_tab, tile * kTcRows + rr);
         }
     }
 
