@@ -14,12 +14,12 @@
 //   P = (R r) S'^T       (fp16 hi / lo splits of R r and S': float32-grade)
 // and the per-element work in between is one centroid lookup and one FMA.
 //
-// One CTA per SM (the operands take ~205 KB of shared memory): a producer
-// warp issues the TMA loads of key tiles and all MMAs; eight epilogue warps
-// (two per 32-row group of tensor-memory lanes, one 64-column half each)
+// One CTA per SM (the operands take ~206 KB of shared memory): a producer
+// warp issues the TMA loads of key tiles and all MMAs; sixteen epilogue warps
+// (four per 32-row group of tensor-memory lanes, one 32-column slice each)
 // read U, form R r from the staged blocks, write its hi / lo fp16 tiles for
-// the second product, add the two halves' sums of squares in a fixed order
-// for ||r||, then read P and pack its signs.  R r is scaled by a power of two
+// the second product, add the slices' sums of squares in a fixed order for
+// ||r||, then read P and pack its signs.  R r is scaled by a power of two
 // chosen from the block norm before the fp16 split (signs and, after
 // undoing the scale, the norm are unchanged; the scale only keeps the split
 // inside fp16's normal range).  Every mbarrier wait is bounded.
@@ -34,7 +34,9 @@ namespace tq {
 namespace {
 
 constexpr int kQRows = 128;                          // keys per tile = MMA M = tensor-memory lanes
-constexpr int kQEpiWarps = 8;
+constexpr int kQEpiWarps = 16;                       // four per 32-row group of lanes
+constexpr int kQSlices = kQEpiWarps / 4;             // column slices of a row
+constexpr int kQNC = 128 / kQSlices;                 // columns (elements) per epilogue thread
 constexpr int kQThreads = 32 * (kQEpiWarps + 1);     // + one producer warp
 constexpr int kQTile = kQRows * 256;                 // one 128 x 128 16-bit operand tile
 constexpr uint32_t kQCols = 512;                     // U (two stages) at 0 / 128, P at 256
@@ -56,7 +58,7 @@ struct QjlSmem {
     static constexpr int BB = 2 + 16 * BITS;
     static constexpr int kHW = BB / 2;                          // 16-bit words per block
     static constexpr int kPitch = BB + 2;                       // staged row: 2 pad bytes, norm, codes (4-aligned)
-    static constexpr int kPre = (32 * kHW + 63) / 64;           // block words a thread prefetches per tile
+    static constexpr int kPre = (32 * kHW + 32 * kQSlices - 1) / (32 * kQSlices);   // block words a thread prefetches
     static constexpr int kHD = 0;                               // H D (key dtype)
     static constexpr int kSh = kHD + kQTile;                    // S' hi (fp16)
     static constexpr int kSl = kSh + kQTile;                    // S' lo (fp16)
@@ -64,8 +66,8 @@ struct QjlSmem {
     static constexpr int kA2 = kX + kQTile;                     // R r hi tile, then lo tile
     static constexpr int kBlk = kA2 + 2 * kQTile;               // the tile's blocks
     static constexpr int kCtab = kBlk + ((kQRows * kPitch + 15) & ~15);   // centroids, lane-replicated
-    static constexpr int kPart = kCtab + 16 * 32 * 4;           // per-row partial sums of squares [2][128]
-    static constexpr int kBars = kPart + 2 * kQRows * 4;        // 8 mbarriers
+    static constexpr int kPart = kCtab + 16 * 32 * 4;           // per-row partial sums of squares [slice][128]
+    static constexpr int kBars = kPart + kQSlices * kQRows * 4; // 8 mbarriers
     static constexpr int kSlot = kBars + 8 * 8;                 // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;            // + alignment slack of the base
 };
@@ -96,17 +98,17 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uin
     lo = pack_h2(x0 - f.x, x1 - f.y);
 }
 
-// Code of element e (0..63) of one half of a block row, from that half's
-// code words (4-bit: 8 words; 2-bit: 4 words; 3-bit: 4 low-plane words,
-// then 2 high-plane words).
-template <int BITS>
+// Code of element e of a slice of a block row, from the slice's code words
+// (4-bit: NC / 8 words; 2-bit: NC / 16 words; 3-bit: NC / 16 low-plane
+// words, then NC / 32 high-plane words).
+template <int BITS, int NC>
 __device__ __forceinline__ uint32_t code_at(const uint32_t *w, int e) {
     if constexpr (BITS == 4) {
         return (w[e >> 3] >> (4 * (e & 7))) & 15u;
     } else if constexpr (BITS == 2) {
         return (w[e >> 4] >> (2 * (e & 15))) & 3u;
     } else {
-        return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[4 + (e >> 5)] >> (e & 31)) & 1u) << 2);
+        return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[NC / 16 + (e >> 5)] >> (e & 31)) & 1u) << 2);
     }
 }
 
@@ -253,21 +255,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
     } else {
         // ---- epilogue: warp w owns tensor-memory lanes (= tile rows) 32 (w & 3) .. + 31 and columns
-        // 64 hf .. + 63 (hf = w >> 2); the two warps of a row group meet on named barrier 1 + (w & 3)
-        const int grp = warp & 3, hf = warp >> 2;
-        const int r = 32 * grp + lane, tid64 = 32 * hf + lane;
-        const uint32_t pair_bar = 1u + (uint32_t)grp;
+        // kQNC sl .. + kQNC - 1 (slice sl = w >> 2); a row group's warps meet on named barrier 1 + (w & 3)
+        const int grp = warp & 3, sl = warp >> 2;
+        const int r = 32 * grp + lane, tidg = 32 * sl + lane, c0 = kQNC * sl;
+        const uint32_t grp_bar = 1u + (uint32_t)grp;
         float *part = reinterpret_cast<float *>(smem + Q::kPart);
         uint8_t *blk = smem + Q::kBlk;
         const uint32_t ctab_s = base_s + Q::kCtab + 4u * lane;
-        const uint32_t a2_row = base_s + Q::kA2 + hf * 16384 + r * 128;
+        const uint32_t a2_row = base_s + Q::kA2 + (c0 >> 6) * 16384 + r * 128;
         // the row group's 32 blocks, as 16-bit words, loaded one tile ahead
         uint32_t pre[Q::kPre];
         auto prefetch = [&](int64_t tile) {
             const int64_t v0 = tile * kQRows + 32 * grp;
 #pragma unroll
             for (int k = 0; k < Q::kPre; ++k) {
-                const int q = tid64 + 64 * k, row = q / Q::kHW, h = q - row * Q::kHW;
+                const int q = tidg + 32 * kQSlices * k, row = q / Q::kHW, h = q - row * Q::kHW;
                 pre[k] = (q < 32 * Q::kHW && tile < ntiles && v0 + row < a.n_vec)
                              ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(
                                    a.blocks + (v0 + row) * a.block_stride + 2 * h))
@@ -277,11 +279,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
         auto stage = [&]() {
 #pragma unroll
             for (int k = 0; k < Q::kPre; ++k) {
-                const int q = tid64 + 64 * k, row = q / Q::kHW, h = q - row * Q::kHW;
+                const int q = tidg + 32 * kQSlices * k, row = q / Q::kHW, h = q - row * Q::kHW;
                 if (q < 32 * Q::kHW)
                     *reinterpret_cast<uint16_t *>(blk + (32 * grp + row) * Q::kPitch + 2 + 2 * h) = (uint16_t)pre[k];
             }
         };
+        auto grp_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(grp_bar), "n"(32 * kQSlices) : "memory"); };
         prefetch(blockIdx.x);
         bool ok = true;   // as in the producer: a wait that gave up is not repeated, the loop runs on
         auto wait = [&](int b, uint32_t parity) {
@@ -294,15 +297,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const int nv = (int)min64(kQRows, a.n_vec - v0);
             stage();
             prefetch(tile + gridDim.x);
-            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");   // the group's blocks are staged
+            grp_sync();   // the group's blocks are staged
 
-            // ---- U of this row half
+            // ---- U of this row slice
             wait(kBarURdy + st, (uint32_t)(i >> 1) & 1u);
             tc_fence_after();
-            float x[2][32];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(st * 128 + 64 * hf);
-            tc_ld32(taddr, x[0]);
-            tc_ld32(taddr + 32, x[1]);
+            float x[kQNC / 32][32];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(st * 128 + c0);
+#pragma unroll
+            for (int c = 0; c < kQNC / 32; ++c) tc_ld32(taddr + 32 * c, x[c]);
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -319,67 +322,76 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 scale = __uint_as_float((uint32_t)(127 + 7 - E) << 23);
             }
             const float inv_rs = 0.08838834764831845f * scale, nn = -(nf * scale);
-            uint32_t cw[BITS == 4 ? 8 : BITS == 3 ? 6 : 4];
+            constexpr int NW = BITS == 4 ? kQNC / 8 : BITS == 2 ? kQNC / 16 : kQNC / 16 + kQNC / 32;
+            uint32_t cw[NW];
             if constexpr (BITS == 4) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) cw[q] = *reinterpret_cast<const uint32_t *>(rb + 4 + 32 * hf + 4 * q);
+                for (int q = 0; q < NW; ++q) cw[q] = *reinterpret_cast<const uint32_t *>(rb + 4 + c0 / 2 + 4 * q);
             } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) cw[q] = *reinterpret_cast<const uint32_t *>(rb + 4 + 16 * hf + 4 * q);
+                for (int q = 0; q < kQNC / 16; ++q) cw[q] = *reinterpret_cast<const uint32_t *>(rb + 4 + c0 / 4 + 4 * q);
                 if constexpr (BITS == 3) {
-                    cw[4] = *reinterpret_cast<const uint32_t *>(rb + 36 + 8 * hf);
-                    cw[5] = *reinterpret_cast<const uint32_t *>(rb + 40 + 8 * hf);
+#pragma unroll
+                    for (int q = 0; q < kQNC / 32; ++q)
+                        cw[kQNC / 16 + q] = *reinterpret_cast<const uint32_t *>(rb + 36 + c0 / 8 + 4 * q);
                 }
             }
             float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                const float c0 = lds_f32(ctab_s + code_at<BITS>(cw, e) * 128u);
-                const float c1 = lds_f32(ctab_s + code_at<BITS>(cw, e + 1) * 128u);
+            for (int e = 0; e < kQNC; e += 2) {
+                const float cv0 = lds_f32(ctab_s + code_at<BITS, kQNC>(cw, e) * 128u);
+                const float cv1 = lds_f32(ctab_s + code_at<BITS, kQNC>(cw, e + 1) * 128u);
                 const float2 u2 = __fmul2_rn(make_float2(x[e >> 5][e & 31], x[e >> 5][(e & 31) + 1]),
                                              make_float2(inv_rs, inv_rs));
-                const float2 r2 = __ffma2_rn(make_float2(c0, c1), make_float2(nn, nn), u2);
+                const float2 r2 = __ffma2_rn(make_float2(cv0, cv1), make_float2(nn, nn), u2);
                 x[e >> 5][e & 31] = r2.x;
                 x[e >> 5][(e & 31) + 1] = r2.y;
                 q2 = __ffma2_rn(r2, r2, q2);
             }
-            part[hf * kQRows + r] = q2.x + q2.y;
+            part[sl * kQRows + r] = q2.x + q2.y;
             // fp16 hi / lo tiles of R r (K-major, 128-byte swizzle), then hand them to the tensor cores
 #pragma unroll
-            for (int kc = 0; kc < 8; ++kc) {
+            for (int kc = 0; kc < kQNC / 8; ++kc) {
                 uint32_t h[4], l[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     const int e = 8 * kc + 2 * p;
                     split_pair(x[e >> 5][e & 31], x[e >> 5][(e & 31) + 1], h[p], l[p]);
                 }
-                const uint32_t addr = a2_row + (uint32_t)(((kc ^ (r & 7)) << 4));
+                const int chunk = ((c0 & 63) >> 3) + kc;
+                const uint32_t addr = a2_row + (uint32_t)(((chunk ^ (r & 7)) << 4));
                 sts128_q(addr, h[0], h[1], h[2], h[3]);
                 sts128_q(addr + kQTile, l[0], l[1], l[2], l[3]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bars + 8 * kBarA2);
-            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");   // both halves' sums of squares
-            const float ss = part[r] + part[kQRows + r];
+            grp_sync();   // every slice's sum of squares
+            float ss = 0.f;
+#pragma unroll
+            for (int q = 0; q < kQSlices; ++q) ss += part[q * kQRows + r];
             const unsigned short rn16 = __half_as_ushort(__float2half_rn(sqrtf(ss) * (1.f / scale)));
 
-            // ---- signs of P = S r for this row half: bit j of the row's 128 = [(S r)_j >= 0]
+            // ---- signs of P = S r for this slice: bit j of the row's 128 = [(S r)_j >= 0]
             wait(kBarP, (uint32_t)i & 1u);
             tc_fence_after();
-            const uint32_t paddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(256 + 64 * hf);
-            tc_ld32(paddr, x[0]);
-            tc_ld32(paddr + 32, x[1]);
+            const uint32_t paddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(256 + c0);
+#pragma unroll
+            for (int c = 0; c < kQNC / 32; ++c) tc_ld32(paddr + 32 * c, x[c]);
             tc_wait_ld();
             tc_fence_before();
-            uint32_t wb[2] = {0u, 0u};
+            uint32_t wb[kQNC / 32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < kQNC / 32; ++c) {
+                wb[c] = 0u;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) wb[c] |= (x[c][k] >= 0.f ? 1u : 0u) << k;
+            }
             if (r < nv) {
-                *reinterpret_cast<uint2 *>(a.bits + (v0 + r) * 16 + 8 * hf) = make_uint2(wb[0], wb[1]);
-                if (hf == 0) a.rn[v0 + r] = rn16;
+                uint8_t *dst = a.bits + (v0 + r) * 16 + c0 / 8;
+                if constexpr (kQNC == 64) *reinterpret_cast<uint2 *>(dst) = make_uint2(wb[0], wb[1]);
+                else *reinterpret_cast<uint32_t *>(dst) = wb[0];
+                if (sl == 0) a.rn[v0 + r] = rn16;
             }
         }
     }
