@@ -100,9 +100,9 @@ def test_encode_edge_vectors(env):
 
 def test_encode_listed_rows_in_full_groups(env):
     """Zero, tiny and huge rows scattered through full 32-row groups (whose
-    blocks leave by bulk copy before the listed rows are finished), and a
-    tensor of zero rows with a few random ones, which overflows every CTA's
-    list of rows to finish."""
+    blocks leave by bulk copy before the listed rows are finished); a tensor
+    of zero rows with a few random ones; and a tensor of tiny rows, which
+    overflows every CTA's list of rows to finish."""
     gen = np.random.default_rng(11)
     x = gen.standard_normal((4096, D))
     special = gen.choice(4096, 200, replace=False)
@@ -116,8 +116,14 @@ def test_encode_listed_rows_in_full_groups(env):
     z = np.zeros((128 * 700, D))
     z[::997] = gen.standard_normal((z[::997].shape[0], D))
     zt = torch.tensor(z, dtype=torch.float32).to(torch.bfloat16)
-    g = _encode_gpu(env, zt.to(env["dev"]), 4)
-    check_codes(g, 4, zt.double().numpy(), env["s"], env["books"][4][2], "zero rows")
+    for bits in (3, 4):
+        g = _encode_gpu(env, zt.to(env["dev"]), bits)
+        check_codes(g, bits, zt.double().numpy(), env["s"], env["books"][bits][2], "zero rows")
+    # every row tiny: more listed rows than a CTA's list holds (each CTA rechecks all of its rows)
+    t = gen.standard_normal((128 * 400, D)) * 2.0**-110
+    tt = torch.tensor(t, dtype=torch.float32).to(torch.bfloat16)
+    g = _encode_gpu(env, tt.to(env["dev"]), 2)
+    check_codes(g, 2, tt.double().numpy(), env["s"], env["books"][2][2], "tiny rows")
 
 
 def test_encode_scatter_dst_index_and_slot_stride(env):

@@ -760,8 +760,14 @@ int launch(const EncArgs &a, cudaStream_t st) {
 // shared memory, H D sits in shared memory in the same layout, eight
 // tcgen05.mma (M 128, N 128, K 16) accumulate into tensor memory, and each
 // of the 128 rows is read from tensor memory (tcgen05.ld) by two epilogue
-// threads, one per 64-column half, and quantised: norm from the sum of squares (Parseval), then the cell-table
-// quantiser of the mma.sync kernel, codes packed straight into its block.
+// threads, one per 64-column half, and quantised: norm from the sum of
+// squares (Parseval), then the cell-table quantiser of the mma.sync kernel
+// over 16-column chunks re-read from tensor memory, codes packed straight
+// into the row's block.  A full group of 32 blocks leaves by one bulk async
+// copy.  Rows whose norm lies within 2^-20 of an fp16 rounding boundary, or
+// whose sum of squares leaves float32's safe range, are listed and finished
+// after the CTA's last tile from the rows in memory (correctly rounded norm;
+// exact power-of-two rescaled path), which keeps calls out of the hot loop.
 // One producer warp issues the TMA loads and the MMAs; two stages of row
 // tiles and accumulators let the loads and MMAs of tile i + 1 run under the
 // epilogue of tile i.  Every mbarrier wait is bounded.
@@ -788,6 +794,31 @@ struct TcSmem {
     static constexpr int kTotal = kSlot + 16 + 1024;                 // + alignment slack of the base
 };
 
+
+// 16 consecutive float32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Wait for this thread's tensor-memory loads; v (their destination) is tied to
+// the wait so no use of it is scheduled before it.
+__device__ __forceinline__ void tc_wait_ld16(float (&v)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]),
+                   "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15])
+                 :
+                 : "memory");
+}
+
 // fp16 of the L2 norm of row r of a tensor-core row tile: double-float sum of
 // the exact squares, one rounding (near an fp16 rounding boundary only).
 template <int DT>
@@ -797,36 +828,59 @@ __device__ __noinline__ unsigned short exact_norm_row(const uint8_t *tile, int r
     return acc.sqrt_fp16();
 }
 
-// Finish one listed row from its values in memory (the row tile is gone by
-// then): rows outside float32's safe range get their whole block from the
-// exact path; rows near an fp16 rounding boundary get the correctly rounded
-// norm (double-float sum of squares).  Cold: a few rows per CTA at most.
+// Finish one listed row, by a whole warp, from its values in memory (the
+// row tile is gone by then); lane j reads elements 4j .. 4j + 3 (16-bit
+// rows).  A zero row gets the constant block (norm 0, code L/2 everywhere);
+// a row outside float32's safe range (listed so, or, with `check`, 128
+// ||x||^2 outside [2^-92, 2^99], a superset of the rows the main loop sends
+// to the exact path) gets its whole block from the exact path; any other row
+// gets the correctly rounded norm (double-float sum of squares).
 template <int BITS, int DT>
-__device__ __forceinline__ void finish_row(const EncArgs &a, const float2 *tab, int64_t v, bool whole) {
+__device__ __forceinline__ void finish_row_warp(const EncArgs &a, const float2 *tab, int64_t v, bool whole, bool check,
+                                                int lane) {
+    static_assert(DT != TQ_F32, "16-bit rows");
+    constexpr int BB = BlockFmt<BITS>::kBytes;
     const uint8_t *xrow = a.x + v * a.x_stride;
+    const uint2 raw = *reinterpret_cast<const uint2 *>(xrow + 8 * lane);
+    const uint32_t h[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+    SumSq2 acc;
+    bool nz = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float f = DT == TQ_BF16 ? __uint_as_float(h[k] << 16) : __half2float(__ushort_as_half((unsigned short)h[k]));
+        acc.add(f);
+        nz |= f != 0.f;   // true for NaN as well
+    }
+    float s1 = acc.s, c1 = acc.c;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float os = __shfl_xor_sync(kFull, s1, o), oc = __shfl_xor_sync(kFull, c1, o);
+        float ns, ne;
+        two_sum(s1, os, ns, ne);
+        s1 = ns;
+        c1 = c1 + oc + ne;
+    }
     const int64_t di = a.dst_index ? a.dst_index[v] : v;
     uint8_t *dst = a.out + di * a.out_stride;
-    if (whole) {
-        encode_row_slow<BITS, DT, false>(xrow, 0, tab, a.grid, a.signs, dst);
-    } else {
-        SumSq2 acc;
-        for (int j = 0; j < kD; ++j) acc.add(elem_smem<DT>(xrow, j));
-        *reinterpret_cast<uint16_t *>(dst) = acc.sqrt_fp16();
+    if (!__any_sync(kFull, nz)) {
+        const uint8_t fill = BITS == 4 ? 0x88 : BITS == 2 ? 0xAA : 0x00;   // code L/2 in every field
+        for (int j = lane; j < BB; j += 32) dst[j] = j < 2 ? 0 : (BITS == 3 && j >= 34) ? 0xFF : fill;
+        return;
     }
-}
-
-// After a CTA's list overflowed: every one of its rows is checked again from
-// memory.  128 ||x||^2 outside [2^-92, 2^99] (a superset of the rows the main
-// loop sends to the exact path, whose sum of squares of u = H D x carries
-// float32 rounding) gets the whole block; every other row gets the correctly
-// rounded norm.
-template <int BITS, int DT>
-__device__ __forceinline__ void recheck_row(const EncArgs &a, const float2 *tab, int64_t v) {
-    SumSq2 acc;
-    const uint8_t *xrow = a.x + v * a.x_stride;
-    for (int j = 0; j < kD; ++j) acc.add(elem_smem<DT>(xrow, j));
-    const float s128 = (acc.s + acc.c) * 128.f;
-    finish_row<BITS, DT>(a, tab, v, !(s128 >= 2.0194839173657902e-28f /* 2^-92 */ && s128 <= 6.338253001141147e29f));
+    if (check) {
+        const float s128 = (s1 + c1) * 128.f;
+        whole = !(s128 >= 2.0194839173657902e-28f /* 2^-92 */ && s128 <= 6.338253001141147e29f /* 2^99 */);
+    }
+    if (lane == 0) {
+        if (whole) {
+            encode_row_slow<BITS, DT, false>(xrow, 0, tab, a.grid, a.signs, dst);
+        } else {
+            SumSq2 tot;
+            tot.s = s1;
+            tot.c = c1;
+            *reinterpret_cast<uint16_t *>(dst) = tot.sqrt_fp16();
+        }
+    }
 }
 
 template <int BITS, int DT>
@@ -937,24 +991,45 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const uint8_t *tile_s = smem + S::kA + st * kTcTileBytes;
             const uint32_t taddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(st * 128 + 64 * hf);
             // ---- norm: sum of squares of u (= 128 ||x||^2), the two halves added in a fixed order
-            float uu[2][32];
-            tc_ld32(taddr, uu[0]);
-            tc_ld32(taddr + 32, uu[1]);
-            tc_wait_ld();
             float2 q2 = make_float2(0.f, 0.f);
+            {
+                float uu[2][32];
+                tc_ld32(taddr, uu[0]);
+                tc_ld32(taddr + 32, uu[1]);
+                tc_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    const float2 p2 = make_float2(uu[c][k], uu[c][k + 1]);
-                    q2 = __ffma2_rn(p2, p2, q2);
-                }
+                    for (int k = 0; k < 32; k += 2) {
+                        const float2 p2 = make_float2(uu[c][k], uu[c][k + 1]);
+                        q2 = __ffma2_rn(p2, p2, q2);
+                    }
+            }
             part[hf * kTcRows + r] = q2.x + q2.y;
             // the previous tile's bulk store has read the group's blocks before they are rewritten
             if (bulk_out && hf == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             const float ss = part[r] + part[kTcRows + r];
-            const bool oor = !(ss >= 1.0097419586828951e-28f /* 128 * 2^-100 */ && ss <= 1.2676506002282294e30f);
+            // ss == 0 is a zero row or one whose squares underflow: the accumulator (still held)
+            // tells them apart; both warps of the pair see the same ss, so both take this branch
+            bool zero_row = false;
+            if (__any_sync(kFull, ss == 0.f)) {
+                float z[2][32];
+                tc_ld32(taddr, z[0]);
+                tc_ld32(taddr + 32, z[1]);
+                tc_wait_ld();
+                bool nz = false;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) nz |= z[c][k] != 0.f;
+                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");   // partial sums read
+                reinterpret_cast<int *>(part)[hf * kTcRows + r] = nz ? 1 : 0;
+                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                zero_row = ss == 0.f && reinterpret_cast<int *>(part)[r] == 0 &&
+                           reinterpret_cast<int *>(part)[kTcRows + r] == 0;
+            }
+            const bool oor = !zero_row && !(ss >= 1.0097419586828951e-28f /* 128 * 2^-100 */ && ss <= 1.2676506002282294e30f);
             const float sc = sqrtf(ss);
             const float nrm = sc * 0.08838834764831845f;
             uint8_t *blk = sm_out + r * BB;
@@ -962,7 +1037,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__float2half_rn(nrm));
                 // rows whose norm lies within 2^-20 of an fp16 rounding boundary, or whose sum of
                 // squares leaves float32's safe range, are listed and finished after the main loop
-                const bool need = (oor || near_fp16_tie_fast(nrm)) && r < nv;
+                const bool need = (oor || near_fp16_tie_fast(nrm)) && !zero_row && r < nv;
                 const uint32_t m = __ballot_sync(kFull, need);
                 if (m) {
                     const int leader = __ffs(m) - 1;
@@ -979,17 +1054,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
             // ---- quantise and pack this half of the row's codes: code = base - [y >= boundary]
             // (set.ge gives 0 / -1), accumulated straight into the packed words
-            const float cs = a.grid / sc;
+            const float cs = zero_row ? 0.f : a.grid / sc;   // a zero row: y = 0, code L/2
             const float2 cs2 = make_float2(cs, cs);
             uint16_t *b16 = reinterpret_cast<uint16_t *>(blk + 2);
             constexpr int PER = BITS == 4 ? 4 : 8;   // codes per 16-bit word of the (low) plane
+            // 16 columns at a time, re-read from tensor memory (the next chunk's load in flight)
+            float ub[2][16];
+            tc_ld16(taddr, ub[0]);
+            tc_wait_ld16(ub[0]);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const float *u = uu[c];
-                const int cc = 2 * hf + c;   // 32-column chunk of the row
-                uint32_t hi = 0;             // 3-bit: the 32 high bits of the chunk
+            for (int c = 0; c < 4; ++c) {
+                if (c < 3) tc_ld16(taddr + 16 * (c + 1), ub[(c + 1) & 1]);
+                const float *u = ub[c & 1];
+                const int cq = 4 * hf + c;   // 16-column chunk of the row
+                uint32_t hi = 0;             // 3-bit: the 16 high bits of the chunk
 #pragma unroll
-                for (int g = 0; g < 32 / PER; ++g) {
+                for (int g = 0; g < 16 / PER; ++g) {
                     uint32_t w = 0;
 #pragma unroll
                     for (int e = 0; e < PER; e += 2) {
@@ -1011,13 +1091,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                             w -= set_ge(yp.y, ey.x) << (B * e + B);
                         }
                     }
-                    b16[(32 / PER) * cc + g] = (uint16_t)w;
+                    b16[(16 / PER) * cq + g] = (uint16_t)w;
                 }
-                if constexpr (BITS == 3) {
-                    uint16_t *h16 = reinterpret_cast<uint16_t *>(blk + 34);
-                    h16[2 * cc] = (uint16_t)hi;
-                    h16[2 * cc + 1] = (uint16_t)(hi >> 16);
-                }
+                if constexpr (BITS == 3) reinterpret_cast<uint16_t *>(blk + 34)[cq] = (uint16_t)hi;
+                if (c < 3) tc_wait_ld16(ub[(c + 1) & 1]);
             }
             if (bulk_out) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // blocks -> bulk copy
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");   // both halves of the 32 blocks written
@@ -1065,17 +1142,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
-        const int et = threadIdx.x;   // 0 .. 32 * kTcEpiWarps - 1
         if (fix[1] == 0) {
             const int nfix = min(fix[0], kTcFixCap);
-            for (int q = et; q < nfix; q += 32 * kTcEpiWarps) {
+            for (int q = warp; q < nfix; q += kTcEpiWarps) {
                 const uint32_t e = (uint32_t)fix[4 + q];
-                finish_row<BITS, DT>(a, s_tab, (int64_t)(e & 0x7FFFFFFFu), (e >> 31) != 0);
+                finish_row_warp<BITS, DT>(a, s_tab, (int64_t)(e & 0x7FFFFFFFu), (e >> 31) != 0, false, lane);
             }
         } else {
             for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
-                for (int rr = et; rr < kTcRows; rr += 32 * kTcEpiWarps)
-                    if (tile * kTcRows + rr < a.n_vec) recheck_row<BITS, DT>(a, s_tab, tile * kTcRows + rr);
+                for (int rr = warp; rr < kTcRows; rr += kTcEpiWarps)
+                    if (tile * kTcRows + rr < a.n_vec)
+                        finish_row_warp<BITS, DT>(a, s_tab, tile * kTcRows + rr, false, true, lane);
         }
     }
 

@@ -39,7 +39,7 @@ constexpr int kQSlices = kQEpiWarps / 4;             // column slices of a row
 constexpr int kQNC = 128 / kQSlices;                 // columns (elements) per epilogue thread
 constexpr int kQThreads = 32 * (kQEpiWarps + 1);     // + one producer warp
 constexpr int kQTile = kQRows * 256;                 // one 128 x 128 16-bit operand tile
-constexpr uint32_t kQCols = 512;                     // U (two stages) at 0 / 128, P at 256
+constexpr uint32_t kQCols = 512;                     // U (two stages) at 0 / 128, P (two) at 256 / 384
 constexpr unsigned kQFull = 0xffffffffu;
 
 struct QjlTcArgs {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 }
                 wait(kBarA2, (uint32_t)i & 1u);          // R r of tile i staged
                 tc_fence_after();
-                const uint32_t p_t = tmem + 256u;
+                const uint32_t p_t = tmem + 256u + 128u * (uint32_t)(i & 1);   // P double-buffered
                 tc_mma_tile<TQ_F16>(p_t, a2_s, sh_s, false);
                 tc_mma_tile<TQ_F16>(p_t, a2_s, sl_s, true);
                 tc_mma_tile<TQ_F16>(p_t, a2_s + kQTile, sh_s, true);
@@ -290,6 +290,32 @@ __global__ void __launch_bounds__(kQThreads, 1)
         auto wait = [&](int b, uint32_t parity) {
             if (ok) ok = tc_mbar_wait(bars + 8 * b, parity);
         };
+        // signs of P = S r for tile j (this slice): bit k of the row's 128 = [(S r)_k >= 0]; run one
+        // tile late, so that the tensor cores compute P of tile j + 1 meanwhile
+        auto signs_out = [&](int j, int64_t pv0, int pnv, unsigned short prn) {
+            float y[kQNC / 32][32];
+            const uint32_t paddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(256 + 128 * (j & 1) + c0);
+#pragma unroll
+            for (int c = 0; c < kQNC / 32; ++c) tc_ld32(paddr + 32 * c, y[c]);
+            tc_wait_ld();
+            tc_fence_before();
+            uint32_t wb[kQNC / 32];
+#pragma unroll
+            for (int c = 0; c < kQNC / 32; ++c) {
+                wb[c] = 0u;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) wb[c] |= (y[c][k] >= 0.f ? 1u : 0u) << k;
+            }
+            if (r < pnv) {
+                uint8_t *dst = a.bits + (pv0 + r) * 16 + c0 / 8;
+                if constexpr (kQNC == 64) *reinterpret_cast<uint2 *>(dst) = make_uint2(wb[0], wb[1]);
+                else *reinterpret_cast<uint32_t *>(dst) = wb[0];
+                if (sl == 0) a.rn[pv0 + r] = prn;
+            }
+        };
+        int64_t pv0 = 0;
+        int pnv = 0;
+        unsigned short prn = 0;
         int i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
             const int st = i & 1;
@@ -349,6 +375,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 q2 = __ffma2_rn(r2, r2, q2);
             }
             part[sl * kQRows + r] = q2.x + q2.y;
+            // the previous tile's P is complete: its MMAs have read the R r tiles rewritten below
+            if (i >= 1) wait(kBarP, (uint32_t)(i - 1) & 1u);
+            tc_fence_after();
             // fp16 hi / lo tiles of R r (K-major, 128-byte swizzle), then hand them to the tensor cores
 #pragma unroll
             for (int kc = 0; kc < kQNC / 8; ++kc) {
@@ -372,27 +401,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
             for (int q = 0; q < kQSlices; ++q) ss += part[q * kQRows + r];
             const unsigned short rn16 = __half_as_ushort(__float2half_rn(sqrtf(ss) * (1.f / scale)));
 
-            // ---- signs of P = S r for this slice: bit j of the row's 128 = [(S r)_j >= 0]
-            wait(kBarP, (uint32_t)i & 1u);
+            if (i >= 1) signs_out(i - 1, pv0, pnv, prn);
+            pv0 = v0;
+            pnv = nv;
+            prn = rn16;
+        }
+        if (i >= 1) {
+            wait(kBarP, (uint32_t)(i - 1) & 1u);
             tc_fence_after();
-            const uint32_t paddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(256 + c0);
-#pragma unroll
-            for (int c = 0; c < kQNC / 32; ++c) tc_ld32(paddr + 32 * c, x[c]);
-            tc_wait_ld();
-            tc_fence_before();
-            uint32_t wb[kQNC / 32];
-#pragma unroll
-            for (int c = 0; c < kQNC / 32; ++c) {
-                wb[c] = 0u;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) wb[c] |= (x[c][k] >= 0.f ? 1u : 0u) << k;
-            }
-            if (r < nv) {
-                uint8_t *dst = a.bits + (v0 + r) * 16 + c0 / 8;
-                if constexpr (kQNC == 64) *reinterpret_cast<uint2 *>(dst) = make_uint2(wb[0], wb[1]);
-                else *reinterpret_cast<uint32_t *>(dst) = wb[0];
-                if (sl == 0) a.rn[v0 + r] = rn16;
-            }
+            signs_out(i - 1, pv0, pnv, prn);
         }
     }
 
