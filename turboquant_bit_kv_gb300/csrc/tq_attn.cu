@@ -48,36 +48,164 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_kernel(const float 
     out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -v : v;
 }
 
+// (hi, lo) fp16 halves of x packed as one half2: x = hi + lo to about 2^-22.
+__device__ __forceinline__ uint32_t prep_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Query prep of the tensor-core kernel, once per (sequence, KV head)
+// segment j: the rotated query R q = H (D q) / sqrt(128) of each of its G
+// heads times scale * log2(e) ("TurboQuant KV Cache Compression — Spec",
+// Optimization: Fused dequant-dot: the query is rotated once), and for the
+// two-term score the sketched raw query S q times scale * log2(e) *
+// sqrt(pi / 2) / m ("RotorQuant KV Cache Compression", The QJL Estimator
+// Formula), m = 128.  Each is split x = hi + lo into fp16 halves and stored
+// as the B fragments of the m16n8k16 products: part p (n-tiles 0, 1 of the
+// rotated query; 2: S q), lane (g, t), k-step ks -> words 2 ks, 2 ks + 1 =
+// rows {2t, 2t+1}, {2t+8, 2t+9} <-> dims 32t + 4ks + {0, 1}, {2, 3} of
+// column g = (head 4p + g / 2, part g & 1: hi / lo).
+__global__ void __launch_bounds__(kAttnThreads) attn_prep_mma_kernel(const __grid_constant__ AttnArgs a,
+                                                                     MmaPlan plan, int qjl) {
+    __shared__ __align__(16) float qs[8 * kD];
+    __shared__ __align__(16) float raw[8 * kD];   // two-term score: scaled raw queries, then S q
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t j = blockIdx.x;
+    const int b = (int)(j / a.Hkv), kvh = (int)(j % a.Hkv);
+    for (int h = warp; h < 8; h += 4) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (h < a.G) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                v[k] = load_q(a.q, a.q_dtype, ((int64_t)b * a.Hq + kvh * a.G + h) * kD + 4 * lane + k);
+        }
+        if (qjl) {
+            const float f = a.qscale * (1.2533141373155003f / 128.f);   // sqrt(pi / 2) / m, m = 128
+            reinterpret_cast<float4 *>(raw + h * kD)[lane] = make_float4(v[0] * f, v[1] * f, v[2] * f, v[3] * f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = 4 * lane + k;
+            if ((a.signs[d >> 5] >> (d & 31)) & 1u) v[k] = -v[k];
+        }
+        const float x0 = v[0] + v[1], x1 = v[0] - v[1], x2 = v[2] + v[3], x3 = v[2] - v[3];
+        v[0] = x0 + x2;
+        v[2] = x0 - x2;
+        v[1] = x1 + x3;
+        v[3] = x1 - x3;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[k], m);
+                v[k] = (lane & m) ? (o - v[k]) : (v[k] + o);
+            }
+        }
+        const float f = a.qscale * 0.08838834764831845f;
+        reinterpret_cast<float4 *>(qs + h * kD)[lane] = make_float4(v[0] * f, v[1] * f, v[2] * f, v[3] * f);
+    }
+    __syncthreads();
+    if (qjl) {
+        // (S q)_jo of heads 0..3 (the two-term score covers G <= 4)
+        const int jo = tid;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4 *srow = reinterpret_cast<const float4 *>(a.S + (int64_t)jo * kD);
+#pragma unroll 4
+        for (int d4 = 0; d4 < 32; ++d4) {
+            const float4 s4 = __ldg(srow + d4);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                const float4 q4 = reinterpret_cast<const float4 *>(raw + hh * kD)[d4];
+                acc4[hh] = fmaf(s4.x, q4.x, fmaf(s4.y, q4.y, fmaf(s4.z, q4.z, fmaf(s4.w, q4.w, acc4[hh]))));
+            }
+        }
+        __syncthreads();   // every raw query is read before the products overwrite them
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) raw[hh * kD + jo] = acc4[hh];
+        __syncthreads();
+    }
+    const int p = warp;
+    if (p < 2 || (p == 2 && qjl)) {
+        const float *buf = p == 2 ? raw : qs;
+        const int nt = p == 2 ? 0 : p, g = lane >> 2, t = lane & 3;
+        uint32_t w[16];
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const float4 q4 = reinterpret_cast<const float4 *>(buf + (4 * nt + (g >> 1)) * kD + 32 * t + 4 * ks)[0];
+            float e[4] = {q4.x, q4.y, q4.z, q4.w};
+            if (g & 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) e[i] -= __half2float(__float2half_rn(e[i]));
+            }
+            w[2 * ks] = prep_half2(e[0], e[1]);
+            w[2 * ks + 1] = prep_half2(e[2], e[3]);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(a.ws + plan.frag_off + j * kFragWords) + p * 128 + lane * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+}
+
 // Merge for the tensor-core kernel's partition: the slots of segment
-// j = (sequence, KV head) are the CTAs that touched it.  Launched as a
-// programmatic dependent of the attention kernel: its CTAs may start while
-// the attention kernel drains and wait here until its writes are visible.
+// j = (sequence, KV head) are the warps whose chunk ranges touch it.  One
+// CTA per (sequence, query head); every load is issued before its result is
+// needed (slot s's (m, l) by thread s, then each dim's values of up to 32
+// slots at once), so the merge costs a few L2 round trips.  Launched as a
+// programmatic dependent of the attention kernel: its CTAs wait here until
+// that grid has finished and its writes are visible.
 __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const float *ws, MmaPlan plan, int Hq,
                                                                         int Hkv, int rotate_back, uint32_t s0,
                                                                         uint32_t s1, uint32_t s2, uint32_t s3,
                                                                         float *out) {
     __shared__ float buf[kD];
+    __shared__ float wts[kAttnThreads];
+    __shared__ float red[2][kAttnThreads / 32];
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int d = threadIdx.x;
+    const int d = threadIdx.x, warp = d >> 5, lane = d & 31;
     const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int G = Hq / Hkv;
     const int64_t j = (int64_t)b * Hkv + h / G;
-    const int64_t first = mma_cta_of_chunk(j * plan.C, plan);
-    const int nslots = (int)(mma_cta_of_chunk((j + 1) * plan.C - 1, plan) - first + 1);
+    const int64_t first = mma_worker_of_chunk(j * plan.C, plan);
+    const int nslots = (int)(mma_worker_of_chunk((j + 1) * plan.C - 1, plan) - first + 1);
     const float *base = ws + (int64_t)blockIdx.x * plan.Smax * kPartialFloats;
+    // M = max over slots of m (thread s reads slot s, s + 128, ...)
     float M = -INFINITY;
-    for (int s = 0; s < nslots; ++s) M = fmaxf(M, base[s * kPartialFloats]);
+    for (int s = d; s < nslots; s += kAttnThreads) M = fmaxf(M, base[(int64_t)s * kPartialFloats]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red[0][warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
     float l = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < nslots; ++s) {
-            const float m = base[s * kPartialFloats];
-            if (m == -INFINITY) continue;
-            const float w = exp2f(m - M);
-            l = fmaf(w, base[s * kPartialFloats + 1], l);
-            acc = fmaf(w, base[s * kPartialFloats + 4 + d], acc);
+    for (int s0 = 0; s0 < nslots; s0 += kAttnThreads) {
+        // weights of this block of slots; their l sum
+        const int s = s0 + d;
+        float w = 0.f, lw = 0.f;
+        if (s < nslots) {
+            const float m = base[(int64_t)s * kPartialFloats];
+            w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+            lw = w * base[(int64_t)s * kPartialFloats + 1];
         }
+        wts[d] = w;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+        __syncthreads();   // wts ready; red[0] reads above are done
+        if (lane == 0) red[1][warp] = lw;
+        const int n = min(kAttnThreads, nslots - s0);
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                x[i] = (i0 + i < n) ? base[(int64_t)(s0 + i0 + i) * kPartialFloats + 4 + d] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc = fmaf(wts[i0 + i], x[i], acc);   // zero weight and value past n
+        }
+        __syncthreads();
+        l += (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+        __syncthreads();   // red[1] / wts are rewritten by the next block of slots
     }
-    const float o = l > 0.f ? acc / l : 0.f;
+    const float o = (l > 0.f || l != l) ? acc / l : 0.f;   // a NaN l (failed copy) propagates
     if (!rotate_back) {
         out[(int64_t)blockIdx.x * kD + d] = o;
         return;
@@ -105,9 +233,9 @@ extern "C" size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv) return 0;
     int splits, tps;
     attn_split_plan(B, Hkv, T_cap, &splits, &tps);
-    const int ms = mma_max_slots(B, Hkv, T_cap);
-    const int slots = splits > ms ? splits : ms;
-    return (size_t)B * Hq * slots * kPartialFloats * sizeof(float);
+    const int64_t split_floats = (int64_t)B * Hq * splits * kPartialFloats;
+    const int64_t mma_floats = mma_workspace_floats(B, Hq, Hkv, T_cap);
+    return (size_t)(split_floats > mma_floats ? split_floats : mma_floats) * sizeof(float);
 }
 
 extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
@@ -161,7 +289,9 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     cudaStream_t st = (cudaStream_t)stream;
     dim3 grid(a.splits, Hkv, B);
     if (attn_mma_supported(kb, vb, qjl, G)) {
-        MmaPlan mp = mma_plan(B, Hkv, T, kb, vb, qjl, G);
+        MmaPlan mp = mma_plan(B, Hq, Hkv, T, kb, vb, qjl, G);
+        attn_prep_mma_kernel<<<B * Hkv, kAttnThreads, 0, st>>>(a, mp, qjl ? 1 : 0);
+        if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
         int r = launch_attn_mma(a, mp, kb, vb, qjl, st);
         if (r != TQ_OK) return r;
         cudaLaunchConfig_t cfg = {};

@@ -6,9 +6,10 @@
 
 namespace tq {
 
-int mma_ctas_per_sm_k2(int vb, bool qjl, int nt);
-int mma_ctas_per_sm_k3(int vb, bool qjl, int nt);
-int mma_ctas_per_sm_k4(int vb, bool qjl, int nt);
+// CTAs per SM and warps per CTA of a configuration (0 CTAs: not covered).
+void mma_shape_k2(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps);
+void mma_shape_k3(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps);
+void mma_shape_k4(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps);
 int launch_attn_mma_k2(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 int launch_attn_mma_k3(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
@@ -16,38 +17,54 @@ int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int n
 // n-tiles of 4 query heads (times hi / lo parts) for G query heads per KV head
 static int mma_ntiles(int G) { return G <= 4 ? 1 : 2; }
 
-// CTAs per SM of a configuration (its shared memory and registers decide: 1
-// or 2); 0 when the tensor-core kernel does not cover it.
-static int mma_ctas_per_sm(int kb, int vb, bool qjl, int G) {
-    if (G < 1 || G > 8) return 0;
+static void mma_shape(int kb, int vb, bool qjl, int G, int *ctas_per_sm, int *warps) {
+    *ctas_per_sm = 0;
+    *warps = 0;
+    if (G < 1 || G > 8) return;
     const int nt = mma_ntiles(G);
     switch (kb) {
-        case 2: return mma_ctas_per_sm_k2(vb, qjl, nt);
-        case 3: return mma_ctas_per_sm_k3(vb, qjl, nt);
-        case 4: return mma_ctas_per_sm_k4(vb, qjl, nt);
-        default: return 0;
+        case 2: mma_shape_k2(vb, qjl, nt, ctas_per_sm, warps); break;
+        case 3: mma_shape_k3(vb, qjl, nt, ctas_per_sm, warps); break;
+        case 4: mma_shape_k4(vb, qjl, nt, ctas_per_sm, warps); break;
+        default: break;
     }
 }
 
-MmaPlan mma_plan(int B, int Hkv, int T, int kb, int vb, bool qjl, int G) {
+// Partial slots per query head: no segment of C chunks meets more than
+// ceil(W / segments) + 1 worker ranges (the ranges differ in length by at
+// most one chunk), nor more workers than it has chunks.
+static int mma_slots(int64_t segs, int64_t C, int64_t W) {
+    const int64_t s = (W + segs - 1) / segs + 1;
+    return (int)(s < C ? s : C);
+}
+
+MmaPlan mma_plan(int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G) {
     MmaPlan p;
-    p.C = (T + kMmaChunk - 1) / kMmaChunk;
-    p.Ctot = (int64_t)B * Hkv * p.C;
-    const int per_sm = mma_ctas_per_sm(kb, vb, qjl, G);
-    p.P = (int)min64(p.Ctot, (int64_t)(per_sm > 0 ? per_sm : 1) * sm_count());
+    int per_sm = 0, warps = 0;
+    mma_shape(kb, vb, qjl, G, &per_sm, &warps);
     const int64_t segs = (int64_t)B * Hkv;
-    p.Smax = (int)((p.P + segs - 1) / segs) + 1;
+    p.C = (T + kMmaChunk - 1) / kMmaChunk;
+    p.Ctot = segs * p.C;
+    p.P = (int)min64(p.Ctot, (int64_t)(per_sm > 0 ? per_sm : 1) * sm_count());
+    // at most one worker per chunk, so that every worker range is non-empty
+    p.W = (int)min64(p.Ctot, (int64_t)p.P * (warps > 0 ? warps : 1));
+    p.Smax = mma_slots(segs, p.C, p.W);
+    p.frag_off = (int64_t)B * Hq * p.Smax * kPartialFloats;
     return p;
 }
 
-int mma_max_slots(int B, int Hkv, int T_cap) {
-    // no configuration runs more than two CTAs per SM
+int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap) {
     const int64_t segs = (int64_t)B * Hkv;
-    const int64_t P = min64(segs * ((T_cap + kMmaChunk - 1) / kMmaChunk), 2 * (int64_t)sm_count());
-    return (int)((P + segs - 1) / segs) + 1;
+    const int64_t C = (T_cap + kMmaChunk - 1) / kMmaChunk;
+    const int smax = mma_slots(segs, C, (int64_t)kMmaMaxWarpsPerSm * sm_count());
+    return (int64_t)B * Hq * smax * kPartialFloats + segs * kFragWords;
 }
 
-bool attn_mma_supported(int kb, int vb, bool qjl, int G) { return mma_ctas_per_sm(kb, vb, qjl, G) > 0; }
+bool attn_mma_supported(int kb, int vb, bool qjl, int G) {
+    int per_sm = 0, warps = 0;
+    mma_shape(kb, vb, qjl, G, &per_sm, &warps);
+    return per_sm > 0;
+}
 
 int launch_attn_mma(const AttnArgs &a, MmaPlan &plan, int kb, int vb, bool qjl, cudaStream_t st) {
     const int nt = mma_ntiles(a.G);

@@ -36,13 +36,17 @@
 //     with movmatrix.
 //
 // Work partition: the B * Hkv * ceil(T / 32) chunks, ordered by (sequence,
-// KV head, position), are cut into P equal contiguous ranges, one per CTA
-// (all CTAs resident), so every CTA does the same work and there is no wave
-// tail.  A CTA walks the (sequence, KV head) segments its range touches; its
-// eight warps take the segment's chunks round-robin, each with its own
-// cp.async double buffer and softmax state, merge in a three-round tree, and
-// write one partial per query head into slot (CTA - first CTA of the
-// segment).  attn_combine_mma_kernel merges each segment's slots.
+// KV head, position), are cut into W equal contiguous ranges, one per warp
+// of the grid (all CTAs resident), so every warp does the same work (to one
+// chunk) and there is no wave tail.  Each warp works on its own: a two- or
+// three-stage ring of bulk copies on its own mbarriers, its own softmax
+// state, and one partial per query head for every (sequence, KV head)
+// segment its range touches, written to slot (warp - first warp of the
+// segment).  The query fragments come from attn_prep_mma_kernel (rotated,
+// scaled, split hi | lo once per segment); attn_combine_mma_kernel merges
+// each segment's slots and applies the inverse rotation.  The three kernels
+// are chained as programmatic dependents, so each one's launch and prologue
+// (the first copies, the lookup tables) overlap the previous one.
 //
 // This header holds the kernel template; tq_attn_mma_k{2,3,4}.cu instantiate
 // it per key width and tq_attn_mma.cu plans and dispatches.
@@ -58,9 +62,6 @@
 namespace tq {
 namespace {
 
-constexpr int kW = 8;                          // warps per CTA
-constexpr int kThreadsMma = kW * 32;
-constexpr int kMergeSlot = 8 * 132;            // floats per warp slot in the merge buffer
 constexpr int kVtPitch = 272;                  // fp16 value tile row: 256 B + 16 B pad (conflict-free)
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -72,6 +73,10 @@ constexpr int align16(int x) { return (x + 15) & ~15; }
 // 8 query heads per KV head.
 template <int KB, int VB, bool QJL, int NT>
 struct Cfg {
+    // 2-bit values with one n-tile fit in 128 registers: one CTA of 16 warps
+    // per SM; every other configuration runs CTAs of 8 warps.
+    static constexpr int kW = (VB == 2 && NT == 1) ? 16 : 8;
+    static constexpr int kThreads = kW * 32;
     static constexpr int kKBytes = 2 + 16 * KB;
     static constexpr bool kRawV = VB == 16;
     static constexpr bool kRegV = VB == 2;                 // value fragments straight from registers
@@ -85,22 +90,29 @@ struct Cfg {
     static constexpr int kVtile = (kRegV || kRawV) ? 0 : 16 * kVtPitch;   // per-warp dequantised tile
     static constexpr int kKLutEntries = KB == 4 ? 256 : KB == 3 ? 64 : 16;
     static constexpr int kVLutEntries = VB == 4 ? 256 : VB == 3 ? 64 : 0;
+    static constexpr int kVLutBytes = kVLutEntries * 128 + (QJL ? 16 * 256 : 0);
+    static constexpr int kVtileBytes = kW * kVtile + kW * 3 * 8;
+    // key-table rows of 256 bytes (offset from one byte permute) where they fit, else 128
+    static constexpr int kKRow =
+        kKLutEntries * 256 + kVLutBytes + kVtileBytes + kW * 2 * kWarpStage <= 227 * 1024 ? 256 : 128;
     static constexpr int kSmemKLut = 0;
-    static constexpr int kSmemVLut = kSmemKLut + kKLutEntries * 128;
+    static constexpr int kSmemVLut = kSmemKLut + kKLutEntries * kKRow;
     static constexpr int kSmemSLut = kSmemVLut + kVLutEntries * 128;
-    static constexpr int kSmemQ = kSmemSLut + (QJL ? 16 * 256 : 0);
-    static constexpr int kSmemSq = kSmemQ + 8 * 128 * 4;
-    static constexpr int kSmemVt = kSmemSq + (QJL ? 8 * 128 * 4 : 0);
-    static constexpr int kSmemBars = kSmemVt + kW * kVtile;       // 2 mbarriers per warp
-    static constexpr int kSmemStages = kSmemBars + kW * 2 * 8;
+    static constexpr int kSmemVt = kSmemSLut + (QJL ? 16 * 256 : 0);
+    static constexpr int kSmemBars = kSmemVt + kW * kVtile;
+    static constexpr int kFixed = kSmemBars + kW * 3 * 8;                 // up to 3 mbarriers per warp
+    // pipeline depth: three stages per warp where they fit, else two
+    static constexpr int kStages = kFixed + kW * 3 * kWarpStage <= 227 * 1024 ? 3 : 2;
+    static constexpr int kSmemStages = kFixed;
     // bytes a full chunk brings in (bulk copies, one mbarrier phase)
     static constexpr int kChunkBytes = kMmaChunk * kKBytes + kMmaChunk * (kRawV ? 256 : kVBytes) +
                                        (QJL ? kMmaChunk * 16 + kMmaChunk * 2 : 0);
-    static constexpr int kSmemTotal = kSmemStages + kW * 2 * kWarpStage;
-    static constexpr int kMinBlocks = (NT == 1 && kSmemTotal <= 113 * 1024) ? 2 : 1;
-    static_assert(kW * 2 * kWarpStage >= 4 * kMergeSlot * 4, "merge buffer aliases the stages");
+    static constexpr int kSmemTotal = kSmemStages + kW * kStages * kWarpStage;
+    static constexpr int kMinBlocks = (kW == 8 && NT == 1 && kSmemTotal <= 113 * 1024) ? 2 : 1;
     static_assert(kSmemTotal <= 227 * 1024, "shared memory");
+    static_assert(kW * kMinBlocks <= kMmaMaxWarpsPerSm, "warps per SM");
 };
+
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
@@ -108,28 +120,28 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
+// Dynamic shared memory of the kernel.  Loads are plain C++ dereferences
+// (shared-window address minus the base), which the compiler can schedule
+// and fold into immediate offsets; the bounded mbarrier waits, __syncwarp
+// and the asm stores (memory clobbers) still order them.
+extern __shared__ __align__(16) uint8_t tq_attn_dsmem[];
+
+template <class T>
+__device__ __forceinline__ T lds(uint32_t addr) {
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(tq_attn_dsmem);
+    return *reinterpret_cast<const T *>(tq_attn_dsmem + (addr - base));
 }
 
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-    return v;
-}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) { return lds<uint32_t>(addr); }
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) { return lds<uint2>(addr); }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
 
-__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
-}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) { return lds<unsigned short>(addr); }
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                               uint32_t &r3) {
@@ -152,8 +164,7 @@ __device__ __forceinline__ void lds_words_a2(uint32_t addr, uint32_t (&w)[NW]) {
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -161,7 +172,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
     uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
 }
 
@@ -226,9 +237,9 @@ __device__ __forceinline__ void pair_codes(int e, int &c0, int &c1) {
 // c[c1(e)]) for every lane l; stores rotated by e so a warp's stores are
 // conflict-free.
 template <int BITS>
-__device__ __forceinline__ void build_pair_lut(uint32_t *lut, const float *cb, int tid) {
+__device__ __forceinline__ void build_pair_lut(uint32_t *lut, const float *cb, int tid, int nthreads) {
     constexpr int E = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
-    for (int e = tid; e < E; e += kThreadsMma) {
+    for (int e = tid; e < E; e += nthreads) {
         int c0, c1;
         pair_codes<BITS>(e, c0, c1);
         const uint32_t val = pack_half2(cb[c0], cb[c1]);
@@ -237,21 +248,23 @@ __device__ __forceinline__ void build_pair_lut(uint32_t *lut, const float *cb, i
     }
 }
 
-// Split table of a codebook for the keys: entry e at byte e * 128 + l * 8 for
+// Split table of a codebook for the keys: entry e at byte e * row + l * 8 for
 // l = 0..15 (lanes l and l + 16 share a copy; an 8-byte load serves half a
-// warp per pass, so this is conflict-free) holds (hi, lo) half2 words with
-// hi = fp16(c), lo = fp16(c - hi): hi + lo carries c to about 2^-22.
+// warp per pass, so this is conflict-free; with 256-byte rows the upper half
+// is unused and one byte permute yields the offset e * 256 + l * 8) holds
+// (hi, lo) half2 words with hi = fp16(c), lo = fp16(c - hi): hi + lo
+// carries c to about 2^-22.
 template <int BITS>
-__device__ __forceinline__ void build_split_lut(uint2 *lut, const float *cb, int tid) {
+__device__ __forceinline__ void build_split_lut(uint2 *lut, const float *cb, int tid, int nthreads, int row_words) {
     constexpr int E = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
-    for (int q = tid; q < E * 16; q += kThreadsMma) {
+    for (int q = tid; q < E * 16; q += nthreads) {
         const int e = q >> 4, l = q & 15;
         int c0, c1;
         pair_codes<BITS>(e, c0, c1);
         const __half h0 = __float2half_rn(cb[c0]), h1 = __float2half_rn(cb[c1]);
         const uint32_t hi = pack_half2(__half2float(h0), __half2float(h1));
         const uint32_t lo = pack_half2(cb[c0] - __half2float(h0), cb[c1] - __half2float(h1));
-        lut[e * 16 + l] = make_uint2(hi, lo);
+        lut[e * row_words + l] = make_uint2(hi, lo);
     }
 }
 
@@ -294,16 +307,28 @@ struct KeySlice {
             pair_index3(c[1], hb[0] >> 16, w[2], w[3]);
         }
     }
-    // prmt selectors of the table index of pair 2ks (first) and 2ks + 1 (second)
-    __device__ __forceinline__ void pick(int ks, uint32_t &x, uint32_t &y) const {
+    // key-table byte offsets of pair 2ks (x) and pair 2ks + 1 (y) for rows of
+    // ROW bytes: with 256-byte rows one byte permute puts the pair index in
+    // byte 1 and the lane offset lo8 in byte 0
+    template <int ROW>
+    __device__ __forceinline__ void pick(int ks, uint32_t lo8, uint32_t &x, uint32_t &y) const {
+        uint32_t wx, wy, bx, by;
         if constexpr (KB == 4) {
-            const uint32_t word = w[ks >> 1];
-            x = prmt(word, 0, 0x4440u + 2 * (ks & 1));
-            y = prmt(word, 0, 0x4441u + 2 * (ks & 1));
+            wx = wy = w[ks >> 1];
+            bx = 2 * (ks & 1);
+            by = bx + 1;
         } else {
-            const int h = ks >> 2, i = ks & 3;
-            x = prmt(w[2 * h], 0, 0x4440u + i);
-            y = prmt(w[2 * h + 1], 0, 0x4440u + i);
+            const int h = ks >> 2;
+            wx = w[2 * h];
+            wy = w[2 * h + 1];
+            bx = by = ks & 3;
+        }
+        if constexpr (ROW == 256) {
+            x = prmt(wx, lo8, 0x6504u + bx * 16);
+            y = prmt(wy, lo8, 0x6504u + by * 16);
+        } else {
+            x = prmt(wx, 0, 0x4440u + bx) * ROW + lo8;
+            y = prmt(wy, 0, 0x4440u + by) * ROW + lo8;
         }
     }
 };
@@ -349,24 +374,145 @@ __device__ __forceinline__ int acc_dim(int m, int r, int g) {
     return REGV ? 16 * g + 8 * (m >> 2) + (m & 3) + 4 * r : 16 * m + g + 8 * r;
 }
 
+
 template <int KB, int VB, bool QJL, int NT>
-__global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
-    attn_mma_kernel(const __grid_constant__ AttnArgs a, MmaPlan plan) {
+__global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT>::kThreads, Cfg<KB, VB, QJL, NT>::kMinBlocks)
+    attn_mma_kernel(const __grid_constant__ AttnArgs a, const MmaPlan plan) {
     using C = Cfg<KB, VB, QJL, NT>;
-    extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int kS = C::kStages;
+    uint8_t *smem = tq_attn_dsmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const uint32_t smem_s = (uint32_t)__cvta_generic_to_shared(smem);
-    float *qbuf = reinterpret_cast<float *>(smem + C::kSmemQ);
-    float *sqbuf = reinterpret_cast<float *>(smem + C::kSmemSq);
-    float *merge = reinterpret_cast<float *>(smem + C::kSmemStages);   // aliases the stages after the loop
+    const uint32_t stage_s = smem_s + C::kSmemStages + warp * kS * C::kWarpStage;
+    const uint32_t bar_s = smem_s + C::kSmemBars + warp * 3 * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kS; ++s) mbar_init(bar_s + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    // the combine kernel may take its (idle) place on the SMs now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
 
-    build_split_lut<KB>(reinterpret_cast<uint2 *>(smem + C::kSmemKLut), a.kc, tid);
-    if constexpr (VB == 3 || VB == 4) build_pair_lut<VB>(reinterpret_cast<uint32_t *>(smem + C::kSmemVLut), a.vc, tid);
+    // this warp's chunks [lo, hi) in (segment, position) order: segments j0 .. j1, from chunk cb0
+    // of segment j0 to chunk ce1 (exclusive) of segment j1
+    const int gw = warp * plan.P + blockIdx.x;
+    const bool active = gw < plan.W;
+    int j0 = 0, j1 = -1, cb0 = 0, ce1 = 0;
+    if (active) {
+        const int64_t lo = (int64_t)gw * plan.Ctot / plan.W, hi = ((int64_t)gw + 1) * plan.Ctot / plan.W;
+        j0 = (int)(lo / plan.C);
+        j1 = (int)((hi - 1) / plan.C);
+        cb0 = (int)(lo - (int64_t)j0 * plan.C);
+        ce1 = (int)(hi - (int64_t)j1 * plan.C);
+    }
+    // live tokens of segment j: its sequence's length clamped to [0, T]
+    auto seg_len = [&](int j) {
+        int L = a.T;
+        if (a.seq_lens) {
+            const int sl = a.seq_lens[j / a.Hkv];
+            L = sl < 0 ? 0 : (sl > a.T ? a.T : sl);
+        }
+        return L;
+    };
+
+    uint32_t phase = 0;        // bit s: parity of the next completion of barrier s
+    uint32_t bulk_mask = 0;    // bit s: stage s was filled by bulk copies
+    bool copies_ok = true;
+
+    // stage of chunk ci of segment j: K blocks | V blocks (raw: 272-byte rows) | sign rows | residual norms
+    auto issue = [&](int buf, int j, int ci, int L) {
+        const int t0 = ci * kMmaChunk;
+        const int n = min(kMmaChunk, L - t0);
+        const int64_t row0 = (int64_t)j * a.T_cap;
+        const uint8_t *kbase = a.k + row0 * C::kKBytes;
+        const uint8_t *vbase = a.v + row0 * C::kVBytes;
+        const uint8_t *sgbase = QJL ? a.qjl_bits + row0 * 16 : nullptr;
+        const uint8_t *rnbase = QJL ? reinterpret_cast<const uint8_t *>(a.rn + row0) : nullptr;
+        const uint32_t dk = stage_s + buf * C::kWarpStage, dv = dk + C::kKStage;
+        const uint8_t *sk = kbase + (int64_t)t0 * C::kKBytes, *sv = vbase + (int64_t)t0 * C::kVBytes;
+        if (n == kMmaChunk) {
+            // full chunk: contiguous 16-byte aligned ranges, bulk copies on barrier `buf`
+            const uint32_t bar = bar_s + 8 * buf;
+            if (lane == 0) mbar_expect_tx(bar, C::kChunkBytes);
+            __syncwarp();
+            if (lane == 0) {
+                bulk_g2s(dk, sk, kMmaChunk * C::kKBytes, bar);
+                if constexpr (!C::kRawV) bulk_g2s(dv, sv, kMmaChunk * C::kVBytes, bar);
+                if constexpr (QJL) {
+                    const uint32_t ds = dv + C::kVStage;
+                    bulk_g2s(ds, sgbase + (int64_t)t0 * 16, kMmaChunk * 16, bar);
+                    bulk_g2s(ds + C::kSStage, rnbase + (int64_t)t0 * 2, kMmaChunk * 2, bar);
+                }
+            }
+            if constexpr (C::kRawV) bulk_g2s(dv + lane * kVtPitch, sv + lane * 256, 256, bar);
+            bulk_mask |= 1u << buf;
+            return;
+        }
+        // partial chunk (the end of a sequence): 16-byte cp.async pieces, zero-filled past the tokens
+        bulk_mask &= ~(1u << buf);
+        const int nk = (n * C::kKBytes + 15) >> 4;
+        for (int q = lane; q < C::kKStage / 16; q += 32) cp16_zfill(dk + 16 * q, q < nk ? sk + 16 * q : kbase, q < nk);
+        if constexpr (C::kRawV) {
+            for (int q = lane; q < kMmaChunk * 16; q += 32) {
+                const int r = q >> 4, col = q & 15;
+                cp16_zfill(dv + r * kVtPitch + 16 * col, r < n ? sv + r * 256 + 16 * col : vbase, r < n);
+            }
+        } else {
+            const int nvb = (n * C::kVBytes + 15) >> 4;
+            for (int q = lane; q < C::kVStage / 16; q += 32)
+                cp16_zfill(dv + 16 * q, q < nvb ? sv + 16 * q : vbase, q < nvb);
+        }
+        if constexpr (QJL) {
+            const uint32_t ds = dv + C::kVStage, dr = ds + C::kSStage;
+            const uint8_t *ss = sgbase + (int64_t)t0 * 16, *sr = rnbase + (int64_t)t0 * 2;
+            cp16_zfill(ds + 16 * lane, lane < n ? ss + 16 * lane : sgbase, lane < n);
+            const int nr = (2 * n + 15) >> 4;
+            if (lane < 4) cp16_zfill(dr + 16 * lane, lane < nr ? sr + 16 * lane : rnbase, lane < nr);
+        }
+        cp_async_commit();
+    };
+
+    // live chunks [cb, ce) of segment j within this warp's range
+    auto seg_end = [&](int j, int L) { return min(j == j1 ? ce1 : plan.C, (L + kMmaChunk - 1) / kMmaChunk); };
+    // issue cursor: chunk ici of segment ij, always at a live chunk (ici < iend) unless past the range
+    int ij = j0, ici = cb0, iL = 0, iend = 0;
+    if (active) {
+        iL = seg_len(j0);
+        iend = seg_end(j0, iL);
+    }
+    auto settle = [&]() {
+        while (ici >= iend && ij < j1) {
+            ++ij;
+            ici = 0;
+            iL = seg_len(ij);
+            iend = seg_end(ij, iL);
+        }
+    };
+    int ist = 0;   // stage of the next issue
+    auto issue_next = [&]() {
+        if (ici < iend) {
+            issue(ist, ij, ici, iL);
+            ++ici;
+            settle();
+        }
+        ist = ist + 1 == kS ? 0 : ist + 1;
+    };
+    // the first chunks are on their way while the tables are built
+    if (active) {
+        settle();
+#pragma unroll
+        for (int s = 0; s + 1 < kS; ++s) issue_next();
+    }
+
+    build_split_lut<KB>(reinterpret_cast<uint2 *>(smem + C::kSmemKLut), a.kc, tid, C::kThreads, C::kKRow / 8);
+    if constexpr (VB == 3 || VB == 4)
+        build_pair_lut<VB>(reinterpret_cast<uint32_t *>(smem + C::kSmemVLut), a.vc, tid, C::kThreads);
     if constexpr (QJL) {
         // sign table: entry e (4 sign bits) = (half2(s0, s1), half2(s2, s3)), s = bit ? +1 : -1,
         // at byte e * 256 + lane * 8
         uint32_t *sl = reinterpret_cast<uint32_t *>(smem + C::kSmemSLut);
-        for (int q = tid; q < 16 * 32; q += kThreadsMma) {
+        for (int q = tid; q < 16 * 32; q += C::kThreads) {
             const int e = q >> 5, l = q & 31;
             const uint32_t p0 = (e & 1) ? 0x3C00u : 0xBC00u, p1 = (e & 2) ? 0x3C00u : 0xBC00u;
             const uint32_t p2 = (e & 4) ? 0x3C00u : 0xBC00u, p3 = (e & 8) ? 0x3C00u : 0xBC00u;
@@ -384,166 +530,45 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
             vhi |= (hb >> 8) << (8 * i);
         }
     }
-    const uint32_t klut_s = smem_s + C::kSmemKLut + (lane & 15) * 8;
+    const uint32_t klut_s = smem_s + C::kSmemKLut, klane = (lane & 15) * 8;
     const uint32_t vlut_s = smem_s + C::kSmemVLut + lane * 4;
     const uint32_t slut_s = smem_s + C::kSmemSLut + lane * 8;
     const uint32_t vt_s = smem_s + C::kSmemVt + warp * C::kVtile;
-    const uint32_t stage_s = smem_s + C::kSmemStages + warp * 2 * C::kWarpStage;
-    const uint32_t bar_s = smem_s + C::kSmemBars + warp * 16;
-    if (lane == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_s + 8, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    uint32_t phase = 0;        // bit b: parity of the next completion of barrier b
-    uint32_t bulk_mask = 0;    // bit b: buffer b was filled by bulk copies
-    bool copies_ok = true;
+    __syncthreads();
+    // the query fragments come from the prep kernel this one depends on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    const int64_t lo = (int64_t)blockIdx.x * plan.Ctot / plan.P;
-    const int64_t hi = (int64_t)(blockIdx.x + 1) * plan.Ctot / plan.P;
-    for (int64_t x = lo; x < hi;) {
-        const int64_t j = x / plan.C;                       // segment = (sequence, KV head)
-        const int64_t seg_lo = j * plan.C;
-        const int64_t xe = min64(hi, seg_lo + plan.C);
-        const int b = (int)(j / a.Hkv), kvh = (int)(j % a.Hkv);
-        int L = a.T;
-        if (a.seq_lens) {
-            const int sl = a.seq_lens[b];
-            L = sl < 0 ? 0 : (sl > a.T ? a.T : sl);
-        }
-        const int slot = (int)(blockIdx.x - mma_cta_of_chunk(seg_lo, plan));
-
-        // ---- rotated, scaled query of head `warp` (zero for padded heads), warp-local transform
-        __syncthreads();   // previous segment's readers of qbuf / sqbuf / merge are done
-        {
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (warp < a.G) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    v[k] = load_q(a.q, a.q_dtype, ((int64_t)b * a.Hq + kvh * a.G + warp) * kD + 4 * lane + k);
-            }
-            if constexpr (QJL) {
-                // raw query (scaled) for the sketch product below
-                const float f = a.qscale * (1.2533141373155003f / 128.f);   // sqrt(pi / 2) / m, m = 128
-                reinterpret_cast<float4 *>(sqbuf + warp * 128)[lane] =
-                    make_float4(v[0] * f, v[1] * f, v[2] * f, v[3] * f);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int d = 4 * lane + k;
-                if ((a.signs[d >> 5] >> (d & 31)) & 1u) v[k] = -v[k];
-            }
-            float x0 = v[0] + v[1], x1 = v[0] - v[1], x2 = v[2] + v[3], x3 = v[2] - v[3];
-            v[0] = x0 + x2;
-            v[2] = x0 - x2;
-            v[1] = x1 + x3;
-            v[3] = x1 - x3;
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float o = __shfl_xor_sync(kFull, v[k], m);
-                    v[k] = (lane & m) ? (o - v[k]) : (v[k] + o);
-                }
-            }
-            const float f = a.qscale * 0.08838834764831845f;
-            reinterpret_cast<float4 *>(qbuf + warp * 128)[lane] = make_float4(v[0] * f, v[1] * f, v[2] * f, v[3] * f);
-        }
-        __syncthreads();
-        // B fragments of n-tile nt: column g = (head 4 nt + g / 2, part g & 1: hi / lo); k-step ks,
-        // rows {2t, 2t+1, 2t+8, 2t+9} <-> dims 32t + 4ks + {0, 1, 2, 3}
-        auto split_frag = [&](const float *buf, int nt, int ks, uint32_t &b0, uint32_t &b1) {
-            const float4 q4 = reinterpret_cast<const float4 *>(buf + (4 * nt + (g >> 1)) * 128 + 32 * t + 4 * ks)[0];
-            float e[4] = {q4.x, q4.y, q4.z, q4.w};
-            if (g & 1) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) e[i] -= __half2float(__float2half_rn(e[i]));
-            }
-            b0 = pack_half2(e[0], e[1]);
-            b1 = pack_half2(e[2], e[3]);
-        };
+    int cst = 0;   // stage of the next chunk to compute
+    for (int j = j0; j <= j1; ++j) {
+        const int L = seg_len(j);
+        const int cb = j == j0 ? cb0 : 0, ce = seg_end(j, L);
+        const int b = j / a.Hkv, kvh = j % a.Hkv;
+        // B fragments (n-tile nt, k-step ks) of the rotated, scaled query split hi | lo, and of S q
         uint32_t qb[NT][8][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) split_frag(qbuf, nt, ks, qb[nt][ks][0], qb[nt][ks][1]);
         uint32_t sb[QJL ? 8 : 1][2];
-        if constexpr (QJL) {
-            // (S q)_j of every head: thread -> output j = tid & 127, heads 4 (tid >> 7) .. + 3
-            const int jo = tid & 127, h0 = 4 * (tid >> 7);
-            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-            const float4 *srow = reinterpret_cast<const float4 *>(a.S + (int64_t)jo * kD);
-#pragma unroll 4
-            for (int d4 = 0; d4 < 32; ++d4) {
-                const float4 s4 = __ldg(srow + d4);
+        {
+            const uint4 *fr = reinterpret_cast<const uint4 *>(a.ws + plan.frag_off + (int64_t)j * kFragWords) + lane * 4;
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    const float4 q4 = reinterpret_cast<const float4 *>(sqbuf + (h0 + hh) * 128)[d4];
-                    acc4[hh] = fmaf(s4.x, q4.x, fmaf(s4.y, q4.y, fmaf(s4.z, q4.z, fmaf(s4.w, q4.w, acc4[hh]))));
-                }
-            }
-            __syncthreads();   // every raw query is read before the products overwrite them
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) sqbuf[(h0 + hh) * 128 + jo] = acc4[hh];
-            __syncthreads();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) split_frag(sqbuf, 0, ks, sb[ks][0], sb[ks][1]);
-        }
-
-        const int64_t bh = (int64_t)b * a.Hkv + kvh;
-        const uint8_t *kbase = a.k + bh * a.T_cap * C::kKBytes;
-        const uint8_t *vbase = a.v + bh * a.T_cap * C::kVBytes;
-        const uint8_t *sgbase = QJL ? a.qjl_bits + bh * a.T_cap * 16 : nullptr;
-        const uint8_t *rnbase = QJL ? reinterpret_cast<const uint8_t *>(a.rn + bh * a.T_cap) : nullptr;
-        auto tok0 = [&](int64_t c) { return (int)((c - seg_lo) * kMmaChunk); };
-        // stage of a chunk: K blocks | V blocks (raw: 272-byte rows) | sign rows | residual norms
-        auto issue = [&](int buf, int64_t c) {
-            const int t0 = tok0(c);
-            const int n = min(kMmaChunk, L - t0);
-            const uint32_t dk = stage_s + buf * C::kWarpStage, dv = dk + C::kKStage;
-            const uint8_t *sk = kbase + (int64_t)t0 * C::kKBytes, *sv = vbase + (int64_t)t0 * C::kVBytes;
-            if (n == kMmaChunk) {
-                // full chunk: contiguous 16-byte aligned ranges, bulk copies on barrier `buf`
-                const uint32_t bar = bar_s + 8 * buf;
-                if (lane == 0) mbar_expect_tx(bar, C::kChunkBytes);
-                __syncwarp();
-                if (lane == 0) {
-                    bulk_g2s(dk, sk, kMmaChunk * C::kKBytes, bar);
-                    if constexpr (!C::kRawV) bulk_g2s(dv, sv, kMmaChunk * C::kVBytes, bar);
-                    if constexpr (QJL) {
-                        const uint32_t ds = dv + C::kVStage;
-                        bulk_g2s(ds, sgbase + (int64_t)t0 * 16, kMmaChunk * 16, bar);
-                        bulk_g2s(ds + C::kSStage, rnbase + (int64_t)t0 * 2, kMmaChunk * 2, bar);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = fr[nt * 128 + q];
+                    qb[nt][2 * q][0] = w.x;
+                    qb[nt][2 * q][1] = w.y;
+                    qb[nt][2 * q + 1][0] = w.z;
+                    qb[nt][2 * q + 1][1] = w.w;
                 }
-                if constexpr (C::kRawV) bulk_g2s(dv + lane * kVtPitch, sv + lane * 256, 256, bar);
-                bulk_mask |= 1u << buf;
-                return;
-            }
-            // partial chunk (the end of a sequence): 16-byte cp.async pieces, zero-filled past the tokens
-            bulk_mask &= ~(1u << buf);
-            const int nk = (n * C::kKBytes + 15) >> 4;
-            for (int q = lane; q < C::kKStage / 16; q += 32) cp16_zfill(dk + 16 * q, q < nk ? sk + 16 * q : kbase, q < nk);
-            if constexpr (C::kRawV) {
-                for (int q = lane; q < kMmaChunk * 16; q += 32) {
-                    const int r = q >> 4, col = q & 15;
-                    cp16_zfill(dv + r * kVtPitch + 16 * col, r < n ? sv + r * 256 + 16 * col : vbase, r < n);
-                }
-            } else {
-                const int nvb = (n * C::kVBytes + 15) >> 4;
-                for (int q = lane; q < C::kVStage / 16; q += 32)
-                    cp16_zfill(dv + 16 * q, q < nvb ? sv + 16 * q : vbase, q < nvb);
-            }
             if constexpr (QJL) {
-                const uint32_t ds = dv + C::kVStage, dr = ds + C::kSStage;
-                const uint8_t *ss = sgbase + (int64_t)t0 * 16, *sr = rnbase + (int64_t)t0 * 2;
-                cp16_zfill(ds + 16 * lane, lane < n ? ss + 16 * lane : sgbase, lane < n);
-                const int nr = (2 * n + 15) >> 4;
-                if (lane < 4) cp16_zfill(dr + 16 * lane, lane < nr ? sr + 16 * lane : rnbase, lane < nr);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = fr[2 * 128 + q];
+                    sb[2 * q][0] = w.x;
+                    sb[2 * q][1] = w.y;
+                    sb[2 * q + 1][0] = w.z;
+                    sb[2 * q + 1][1] = w.w;
+                }
             }
-            cp_async_commit();
-        };
+        }
 
         // accumulators: n-tile nt, m-tile m; columns (2t, 2t+1) = head 4 nt + t, (hi, lo) parts
         float o[NT][8][4];
@@ -558,22 +583,17 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
             lrun[nt] = 0.f;
         }
 
-        // this warp's chunks: x + warp, x + warp + 8, ... below xe and with tokens left (t0 < L)
-        int64_t c = x + warp;
-        auto live = [&](int64_t cc) { return cc < xe && tok0(cc) < L; };
-        if (live(c)) issue(0, c);
-        for (int it = 0; live(c); ++it, c += kW) {
-            if (live(c + kW)) issue((it + 1) & 1, c + kW);
-            const int cb = it & 1;
-            if (bulk_mask & (1u << cb)) {
-                copies_ok &= mbar_wait(bar_s + 8 * cb, (phase >> cb) & 1u);
-                phase ^= 1u << cb;
+        for (int ci = cb; ci < ce; ++ci) {
+            issue_next();
+            if (bulk_mask & (1u << cst)) {
+                copies_ok &= mbar_wait(bar_s + 8 * cst, (phase >> cst) & 1u);
+                phase ^= 1u << cst;
             } else {
                 cp_async_wait<0>();
             }
             __syncwarp();
-            const int nvalid = min(kMmaChunk, L - tok0(c));
-            const uint32_t ks_s = stage_s + (it & 1) * C::kWarpStage, vs_s = ks_s + C::kKStage;
+            const int nvalid = min(kMmaChunk, L - ci * kMmaChunk);
+            const uint32_t ks_s = stage_s + cst * C::kWarpStage, vs_s = ks_s + C::kKStage;
             const uint32_t sg_s = vs_s + C::kVStage, rn_s = sg_s + C::kSStage;
 
             // ---- scores of 2 tiles of 16 tokens (rows g, g + 8): (Khi + Klo) x (Qhi | Qlo)
@@ -592,10 +612,10 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     uint32_t x0, y0, x1, y1;
-                    ksl[mt][0].pick(ks, x0, y0);
-                    ksl[mt][1].pick(ks, x1, y1);
-                    const uint2 a0 = lds64(klut_s + x0 * 128u), a2 = lds64(klut_s + y0 * 128u);
-                    const uint2 a1 = lds64(klut_s + x1 * 128u), a3 = lds64(klut_s + y1 * 128u);
+                    ksl[mt][0].template pick<C::kKRow>(ks, klane, x0, y0);
+                    ksl[mt][1].template pick<C::kKRow>(ks, klane, x1, y1);
+                    const uint2 a0 = lds64(klut_s + x0), a2 = lds64(klut_s + y0);
+                    const uint2 a1 = lds64(klut_s + x1), a3 = lds64(klut_s + y1);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         mma16816(acc[nt][mt], a0.x, a1.x, a2.x, a3.x, qb[nt][ks][0], qb[nt][ks][1]);
@@ -730,81 +750,44 @@ __global__ void __launch_bounds__(kThreadsMma, Cfg<KB, VB, QJL, NT>::kMinBlocks)
                     if constexpr (!C::kRawV) __syncwarp();   // the tile is rewritten for the next 16 tokens
                 }
             }
-            __syncwarp();
-        }
-        cp_async_wait<0>();
-        if (xe == hi) asm volatile("griddepcontrol.launch_dependents;");   // last segment: let the combine launch
 
-        // ---- fold the (hi, lo) columns: ov[nt][m][r] = head 4 nt + t at dim acc_dim(m, r, g)
-        float ov[NT][8][2];
+            __syncwarp();
+            cst = cst + 1 == kS ? 0 : cst + 1;
+        }
+
+        // ---- this warp's partial of segment j: fold the (hi, lo) columns, sum l over the rows g
+        const bool ok = __all_sync(kFull, copies_ok);
+        const int slot = (int)(gw - mma_worker_of_chunk((int64_t)j * plan.C, plan));
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+            float l = lrun[nt];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                ov[nt][m][0] = o[nt][m][0] + o[nt][m][1];
-                ov[nt][m][1] = o[nt][m][2] + o[nt][m][3];
-            }
+            for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(kFull, l, off);
+            const int head = 4 * nt + t;
+            if (head < a.G) {
+                float *pr = a.ws + (((int64_t)b * a.Hq + kvh * a.G + head) * plan.Smax + slot) * kPartialFloats;
+                if constexpr (C::kRegV) {
+                    // dims 16g .. 16g + 15: float4 q holds m-tiles 4 (q >> 1) .. + 3, row half q & 1
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) lrun[nt] += __shfl_xor_sync(kFull, lrun[nt], off);
-        }
-        const bool seg_ok = __syncthreads_and(copies_ok ? 1 : 0) != 0;
-        // ---- merge the eight warps (rounds: 4 -> 2 -> 1), then warp 0 writes the partials
-#pragma unroll
-        for (int half = kW / 2; half >= 1; half >>= 1) {
-            __syncthreads();
-            if (warp >= half && warp < 2 * half) {
-                float *mw = merge + (warp - half) * kMergeSlot;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float *mh = mw + (4 * nt + t) * 132;
-#pragma unroll
-                    for (int m = 0; m < 8; ++m)
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) mh[4 + acc_dim<C::kRegV>(m, r, g)] = ov[nt][m][r];
-                    if (g == 0) {
-                        mh[0] = mrun[nt];
-                        mh[1] = lrun[nt];
+                    for (int q = 0; q < 4; ++q) {
+                        const int m0 = 4 * (q >> 1), r = q & 1;
+                        reinterpret_cast<float4 *>(pr + 4 + 16 * g)[q] =
+                            make_float4(o[nt][m0][2 * r] + o[nt][m0][2 * r + 1], o[nt][m0 + 1][2 * r] + o[nt][m0 + 1][2 * r + 1],
+                                        o[nt][m0 + 2][2 * r] + o[nt][m0 + 2][2 * r + 1],
+                                        o[nt][m0 + 3][2 * r] + o[nt][m0 + 3][2 * r + 1]);
                     }
-                }
-            }
-            __syncthreads();
-            if (warp < half) {
-                const float *mw = merge + warp * kMergeSlot;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float *mh = mw + (4 * nt + t) * 132;
-                    const float mo = mh[0], lo2 = mh[1];
-                    const float M = fmaxf(mrun[nt], mo);
-                    const float fs = mrun[nt] == -INFINITY ? 0.f : exp2f(mrun[nt] - M);
-                    const float fo = mo == -INFINITY ? 0.f : exp2f(mo - M);
-                    lrun[nt] = lrun[nt] * fs + lo2 * fo;
-                    mrun[nt] = M;
+                } else {
 #pragma unroll
                     for (int m = 0; m < 8; ++m)
 #pragma unroll
-                        for (int r = 0; r < 2; ++r)
-                            ov[nt][m][r] = ov[nt][m][r] * fs + mh[4 + acc_dim<C::kRegV>(m, r, g)] * fo;
+                        for (int r = 0; r < 2; ++r) pr[4 + acc_dim<false>(m, r, g)] = o[nt][m][2 * r] + o[nt][m][2 * r + 1];
+                }
+                if (g == 0) {
+                    pr[0] = mrun[nt];
+                    pr[1] = ok ? l : __int_as_float(0x7fc00000);   // NaN marks a failed copy
                 }
             }
         }
-        if (warp == 0) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int head = 4 * nt + t;
-                if (head < a.G) {
-                    float *pr = a.ws + (((int64_t)b * a.Hq + kvh * a.G + head) * plan.Smax + slot) * kPartialFloats;
-#pragma unroll
-                    for (int m = 0; m < 8; ++m)
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) pr[4 + acc_dim<C::kRegV>(m, r, g)] = ov[nt][m][r];
-                    if (g == 0) {
-                        pr[0] = mrun[nt];
-                        pr[1] = seg_ok ? lrun[nt] : __int_as_float(0x7fc00000);   // NaN marks a failed copy
-                    }
-                }
-            }
-        }
-        x = xe;
     }
 }
 
@@ -815,13 +798,25 @@ int launch_cfg(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
     static int done[64] = {0};
     if (set_smem_limit((const void *)attn_mma_kernel<KB, VB, QJL, NT>, C::kSmemTotal, done) != TQ_OK)
         return TQ_ERR_CUDA;
-    attn_mma_kernel<KB, VB, QJL, NT><<<plan.P, kThreadsMma, C::kSmemTotal, st>>>(a, plan);
+    // a programmatic dependent of the query-prep kernel: its prologue (first copies, tables) overlaps it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.P);
+    cfg.blockDim = dim3((unsigned)C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemTotal;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn_mma_kernel<KB, VB, QJL, NT>, a, plan) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
 }
 
 template <int KB, int VB, bool QJL, int NT>
-constexpr int ctas_per_sm() {
-    return Cfg<KB, VB, QJL, NT>::kMinBlocks;
+void shape_of(int *ctas_per_sm, int *warps) {
+    *ctas_per_sm = Cfg<KB, VB, QJL, NT>::kMinBlocks;
+    *warps = Cfg<KB, VB, QJL, NT>::kW;
 }
 
 }  // namespace

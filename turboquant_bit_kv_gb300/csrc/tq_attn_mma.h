@@ -1,5 +1,5 @@
-// Work partition of the tensor-core decode-attention kernel (shared by the
-// launcher, the combine kernel and the workspace size query).
+// Work partition of the tensor-core decode-attention kernels (shared by the
+// launcher, the query-prep and combine kernels and the workspace size query).
 #pragma once
 
 #include <stdint.h>
@@ -9,27 +9,38 @@
 namespace tq {
 
 constexpr int kMmaChunk = 32;        // tokens per chunk
+constexpr int kMmaMaxWarpsPerSm = 16;   // no configuration runs more warps per SM
+// Query fragments per (sequence, KV head) segment, in 32-bit words: three
+// parts (n-tiles 0 and 1 of the rotated query, the sketched query) x 32
+// lanes x 16 words.
+constexpr int kFragWords = 3 * 32 * 16;
 
-// Chunks are ordered by (sequence, KV head, position); CTA i covers
-// [i * Ctot / P, (i + 1) * Ctot / P).  Smax bounds the number of CTAs that
-// touch one (sequence, KV head) segment, i.e. the partial slots per head.
+// Chunks are ordered by (sequence, KV head, position); worker w (warp
+// w / P of CTA w % P, so that small grids spread over every CTA) covers
+// chunks [w * Ctot / W, (w + 1) * Ctot / W), W <= Ctot (never empty).  Smax
+// bounds the number of workers that touch one (sequence, KV head) segment,
+// i.e. the partial slots per query head.  Workspace: partials
+// [B][Hq][Smax][132] floats | query fragments [B * Hkv][kFragWords] words.
 struct MmaPlan {
-    int C;          // chunks per segment, ceil(T / kMmaChunk)
-    int64_t Ctot;   // B * Hkv * C
-    int P;          // CTAs (all resident: CTAs per SM of the configuration x SMs, at most Ctot)
-    int Smax;       // partial slots per (sequence, query head)
+    int C;              // chunks per segment, ceil(T / kMmaChunk)
+    int64_t Ctot;       // B * Hkv * C
+    int P;              // CTAs (all resident)
+    int W;              // workers: min(Ctot, P x warps per CTA)
+    int Smax;           // partial slots per (sequence, query head)
+    int64_t frag_off;   // float offset of the query fragments in the workspace
 };
 
 // kb / vb: key / value bits (vb = 16: raw fp16 values); qjl: two-term
 // score; G: query heads per KV head.
-MmaPlan mma_plan(int B, int Hkv, int T, int kb, int vb, bool qjl, int G);
-int mma_max_slots(int B, int Hkv, int T_cap);   // Smax bound over every configuration
+MmaPlan mma_plan(int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G);
+// Workspace floats the tensor-core path needs for any T <= T_cap.
+int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap);
 bool attn_mma_supported(int kb, int vb, bool qjl, int G);
 int launch_attn_mma(const AttnArgs &a, MmaPlan &plan, int kb, int vb, bool qjl, cudaStream_t st);
 
-// CTA that owns chunk x: the largest i with floor(i * Ctot / P) <= x.
-__host__ __device__ inline int64_t mma_cta_of_chunk(int64_t x, const MmaPlan &p) {
-    return ((x + 1) * p.P - 1) / p.Ctot;
+// Worker that owns chunk x: the largest w with floor(w * Ctot / W) <= x.
+__host__ __device__ inline int64_t mma_worker_of_chunk(int64_t x, const MmaPlan &p) {
+    return ((x + 1) * p.W - 1) / p.Ctot;
 }
 
 }  // namespace tq

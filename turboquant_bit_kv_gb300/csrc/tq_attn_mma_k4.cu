@@ -5,14 +5,14 @@
 
 namespace tq {
 
-int mma_ctas_per_sm_k4(int vb, bool qjl, int nt) {
+void mma_shape_k4(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps) {
+    *ctas_per_sm = *warps = 0;
 #define TQ_CASE(V, Q, N) \
-    if (vb == V && qjl == Q && nt == N) return ctas_per_sm<4, V, Q, N>();
+    if (vb == V && qjl == Q && nt == N) return shape_of<4, V, Q, N>(ctas_per_sm, warps);
     TQ_CASE(2, false, 1) TQ_CASE(3, false, 1) TQ_CASE(4, false, 1) TQ_CASE(16, false, 1)
     TQ_CASE(2, false, 2) TQ_CASE(3, false, 2) TQ_CASE(4, false, 2) TQ_CASE(16, false, 2)
 
 #undef TQ_CASE
-    return 0;
 }
 
 int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st) {

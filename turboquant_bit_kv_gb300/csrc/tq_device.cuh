@@ -13,6 +13,7 @@ namespace tq {
 constexpr int kD = 128;
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
 template <int BITS>
 struct BlockFmt {
