@@ -150,6 +150,36 @@ def test_encode_scatter_dst_index_and_slot_stride(env):
     assert np.all(b[untouched] == 0x3C)
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_encode_dst_index_runs(env, bits):
+    """Destination indices mixing 32-row groups that form one aligned run of
+    consecutive slots (stored in bulk), an unaligned run, a run with one pair
+    swapped, a reversed group and a ragged tail: every block lands in its own
+    slot and no other slot changes."""
+    tq = env["tq"]
+    dev = env["dev"]
+    bb = tq.tq_block_bytes(bits)
+    slots = 600
+    runs = [np.arange(64, 96),                 # aligned run (64 * bb is a multiple of 16)
+            np.arange(101, 133),               # consecutive but unaligned
+            np.r_[np.arange(200, 216), 217, 216, np.arange(218, 232)],   # one pair swapped
+            np.arange(300, 332)[::-1],         # reversed
+            np.arange(400, 432),               # aligned run
+            np.arange(500, 507)]               # ragged tail
+    dst = torch.from_numpy(np.concatenate(runs).astype(np.int64))
+    n = dst.numel()
+    gen = torch.Generator().manual_seed(11 + bits)
+    x = torch.randn((n, D), generator=gen).to(torch.bfloat16)
+    full, buf = _guarded(slots * bb, dev, fill=0x3C)
+    tq.tq_encode_kv(x.to(dev), env["cbs"][bits], env["signs"], buf, dst_index=dst.to(dev))
+    torch.cuda.synchronize()
+    assert _guards_intact(full, 0x3C)
+    b = buf.view(slots, bb).cpu().numpy()
+    check_codes(b[dst.numpy()], bits, x.double().numpy(), env["s"], env["books"][bits][2], "runs")
+    untouched = np.setdiff1d(np.arange(slots), dst.numpy())
+    assert np.all(b[untouched] == 0x3C)
+
+
 def test_encode_empty_is_noop(env):
     tq = env["tq"]
     full, blk = _guarded(66, env["dev"])

@@ -58,6 +58,7 @@ struct EncArgs {
     int64_t out_stride; // bytes
     const int64_t *dst_index;
     int contiguous;
+    int idx_bulk;       // destination indices into contiguous, 16-byte aligned slots: runs may leave in bulk
     float b0;           // 2-bit: the positive boundary
     float grid;         // 3/4-bit: cells per unit of y
     float2 table[kBuckets];  // cell j: (boundary inside it in G*y units | +inf, bits of #boundaries below it)
@@ -978,8 +979,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         int *fix = reinterpret_cast<int *>(smem + S::kFix);   // [0] count, [1] overflow, [4 ..] rows
         uint8_t *sm_out = smem + S::kOut;
         const uint32_t tab_s = (uint32_t)__cvta_generic_to_shared(s_tab);
-        // full 32-block groups of a contiguous destination leave by one bulk copy each
-        const bool bulk_out = a.contiguous != 0;
+        // full 32-block groups of a contiguous destination (or whose destination indices form one
+        // aligned run) leave by one bulk copy each
+        const bool bulk_out = a.contiguous != 0 || a.idx_bulk != 0;
         const float2 off2 = make_float2(1572928.f, 1572928.f);   // 64 + 1.5 * 2^20
         int i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
@@ -1104,10 +1106,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bars + 32 + 8 * st);
             const int rows = max(0, min(32, nv - 32 * grp));
-            if (bulk_out && rows == 32) {
+            // destination rows of the group, fetched once (one coalesced load); a run of 32
+            // consecutive, 16-byte aligned slots goes out like a contiguous group
+            int64_t my_di = 0, di0 = v0 + 32 * grp;
+            bool run = a.contiguous != 0;
+            if (!a.contiguous) {
+                my_di = lane < rows ? (a.dst_index ? a.dst_index[v0 + 32 * grp + lane] : v0 + 32 * grp + lane) : 0;
+                di0 = __shfl_sync(kFull, my_di, 0);
+                run = __all_sync(kFull, a.idx_bulk && rows == 32 && my_di == di0 + lane && ((di0 * BB) & 15) == 0);
+            }
+            if (bulk_out && rows == 32 && run) {
                 // 32 * BB bytes at a 16-byte aligned offset (32 * BB is a multiple of 16)
                 if (hf == 0 && lane == 0) {
-                    uint8_t *dst = a.out + (v0 + 32 * grp) * BB;
+                    uint8_t *dst = a.out + di0 * BB;
                     const uint32_t src = (uint32_t)__cvta_generic_to_shared(sm_out + 32 * grp * BB);
                     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
                                  "r"(32 * BB)
@@ -1123,10 +1134,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 for (int q = (nch << 3) + lane + 32 * hf; q < (nbytes >> 1); q += 64)
                     reinterpret_cast<uint16_t *>(dst)[q] = reinterpret_cast<const uint16_t *>(src)[q];
             } else {
-                // destination rows of the group, fetched once (one coalesced load), then block by block
-                const int64_t my_di = lane < rows ? (a.dst_index ? a.dst_index[v0 + 32 * grp + lane]
-                                                                 : v0 + 32 * grp + lane)
-                                                  : 0;
+                // block by block to the destination rows
                 for (int j = hf; j < rows; j += 2) {
                     const int64_t di = __shfl_sync(kFull, my_di, j);
                     uint16_t *d = reinterpret_cast<uint16_t *>(a.out + di * a.out_stride);
@@ -1237,6 +1245,7 @@ extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x
     a.out_stride = block_stride_bytes;
     a.dst_index = dst_index;
     a.contiguous = (!dst_index && block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
+    a.idx_bulk = (dst_index && block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
     a.b0 = cb->boundaries[(1 << cb->bits) / 2];
     build_table(cb, &a);
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
