@@ -15,15 +15,17 @@
 //   values  O[128 dims x 8 heads]  += Vhat^T[128 x 16] * P[16 tokens x 8]
 //   * Keys: a thread reads the code slice of its dims 32t..32t+31 per token
 //     (the MMA's k-columns permuted to match) and turns each pair of codes
-//     into a half2 fragment register with one lookup in a lane-replicated
-//     table (word e * 32 + lane: every lane reads its own bank).  The pair's
-//     table index is the code byte (4-bit), the nibble (2-bit), or the low
-//     nibble of the 2-bit plane plus the two high-plane bits (3-bit).
+//     into the (hi, lo) pair of half2 fragment registers with one 8-byte
+//     lookup in a table replicated for 16 lanes; one byte permute yields
+//     the lookup offset (entry * 256 + lane offset).  The pair's table index
+//     is the code byte (4-bit), the nibble (2-bit), or the low nibble of the
+//     2-bit plane plus the two high-plane bits (3-bit).
 //   * 2-bit values: a thread owns dims 16g..16g+15 (the MMA's m-rows
-//     permuted so that the two rows of an m-tile are dims d and d + 4), one
-//     32-bit code word per token; a fragment register holds one dim of two
-//     tokens, built by one byte permute from an 8-byte register table of the
-//     four fp16 centroids.
+//     permuted so that the two rows of an m-tile are dims d and d + 1), one
+//     32-bit code word per token; the code words of two tokens are
+//     interleaved by nibbles so that one byte holds the codes of both dims
+//     of both tokens, and one 8-byte lookup in a 256-entry pair table (the
+//     upper halves of the key table's rows) yields both fragment registers.
 //   * 3- and 4-bit values: each lane dequantises half of one token's row
 //     into an fp16 tile in shared memory (pairs of dims through the same
 //     kind of table as keys), and the fragments are read back transposed
@@ -79,7 +81,7 @@ struct Cfg {
     static constexpr int kThreads = kW * 32;
     static constexpr int kKBytes = 2 + 16 * KB;
     static constexpr bool kRawV = VB == 16;
-    static constexpr bool kRegV = VB == 2;                 // value fragments straight from registers
+    static constexpr bool kRegV = VB == 2;                 // value fragments straight from a pair table
     static constexpr int kVBytes = kRawV ? 256 : 2 + 16 * VB;
     static constexpr int kKStage = align16(kMmaChunk * kKBytes);
     static constexpr int kVStage = kRawV ? kMmaChunk * kVtPitch : align16(kMmaChunk * kVBytes);
@@ -94,9 +96,12 @@ struct Cfg {
     static constexpr int kVtileBytes = kW * kVtile + kW * 3 * 8;
     // key-table rows of 256 bytes (offset from one byte permute) where they fit, else 128
     static constexpr int kKRow =
-        kKLutEntries * 256 + kVLutBytes + kVtileBytes + kW * 2 * kWarpStage <= 227 * 1024 ? 256 : 128;
+        (kRegV ? 256 : kKLutEntries) * 256 + kVLutBytes + kVtileBytes + kW * 2 * kWarpStage <= 227 * 1024 ? 256
+                                                                                                    : 128;
+    // 2-bit values: 256 rows, key entries in the lower and value-pair entries in the upper half
+    static constexpr int kKRows = kRegV ? 256 : kKLutEntries;
     static constexpr int kSmemKLut = 0;
-    static constexpr int kSmemVLut = kSmemKLut + kKLutEntries * kKRow;
+    static constexpr int kSmemVLut = kSmemKLut + kKRows * kKRow;
     static constexpr int kSmemSLut = kSmemVLut + kVLutEntries * 128;
     static constexpr int kSmemVt = kSmemSLut + (QJL ? 16 * 256 : 0);
     static constexpr int kSmemBars = kSmemVt + kW * kVtile;
@@ -110,6 +115,7 @@ struct Cfg {
     static constexpr int kSmemTotal = kSmemStages + kW * kStages * kWarpStage;
     static constexpr int kMinBlocks = (kW == 8 && NT == 1 && kSmemTotal <= 113 * 1024) ? 2 : 1;
     static_assert(kSmemTotal <= 227 * 1024, "shared memory");
+    static_assert(!kRegV || kKRow == 256, "2-bit value pairs live in the upper half of 256-byte rows");
     static_assert(kW * kMinBlocks <= kMmaMaxWarpsPerSm, "warps per SM");
 };
 
@@ -201,20 +207,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
-// Wait for the phase with parity `parity` to complete; gives up (false)
-// after a bounded number of polls instead of hanging.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (int i = 0; i < (1 << 22); ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
+// Wait for the phase with parity `parity` to complete (bounded; false when
+// it gave up).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
 
 // Codes of the two dims of a table entry.  4-bit: entry = byte (low nibble
 // first dim); 2-bit: entry = nibble; 3-bit: entry = the pair's 2-bit-plane
@@ -371,7 +366,21 @@ __device__ __forceinline__ void dequant_value_half(uint32_t blk_s, int hf, uint3
 // Dim of accumulator row `r` (0: fragment row g, 1: row g + 8) of m-tile m.
 template <bool REGV>
 __device__ __forceinline__ int acc_dim(int m, int r, int g) {
-    return REGV ? 16 * g + 8 * (m >> 2) + (m & 3) + 4 * r : 16 * m + g + 8 * r;
+    return REGV ? 16 * g + 2 * m + r : 16 * m + g + 8 * r;
+}
+
+// Pair table of a 2-bit value codebook: entry e = [code of token A, dim d |
+// A, d + 1 | token B, d | B, d + 1] (2 bits each, lowest first) holds the
+// fragment words half2(c[A, d], c[B, d]) and half2(c[A, d + 1], c[B, d + 1]);
+// stored at byte e * 256 + 128 + l * 8 for l = 0..15 (the upper half of the
+// key table's 256-byte rows).
+__device__ __forceinline__ void build_value_pair_lut(uint8_t *rows, const float *cb, int tid, int nthreads) {
+    for (int q = tid; q < 256 * 16; q += nthreads) {
+        const int e = q >> 4, l = q & 15;
+        const uint32_t x = pack_half2(cb[e & 3], cb[(e >> 4) & 3]);
+        const uint32_t y = pack_half2(cb[(e >> 2) & 3], cb[(e >> 6) & 3]);
+        *reinterpret_cast<uint2 *>(rows + e * 256 + 128 + l * 8) = make_uint2(x, y);
+    }
 }
 
 
@@ -520,17 +529,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT>::kThreads, Cfg<KB, VB, QJ
             sl[e * 64 + 2 * l + 1] = p2 | (p3 << 16);
         }
     }
-    // 2-bit value table for prmt: bytes 0-3 = low bytes, 4-7 = high bytes of the four fp16 centroids
-    uint32_t vlo = 0, vhi = 0;
-    if constexpr (VB == 2) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t hb = __half_as_ushort(__float2half_rn(a.vc[i]));
-            vlo |= (hb & 0xFFu) << (8 * i);
-            vhi |= (hb >> 8) << (8 * i);
-        }
-    }
-    const uint32_t klut_s = smem_s + C::kSmemKLut, klane = (lane & 15) * 8;
+    if constexpr (C::kRegV) build_value_pair_lut(smem + C::kSmemKLut, a.vc, tid, C::kThreads);
+    const uint32_t klut_s = smem_s + C::kSmemKLut, klane = (lane & 15) * 8, vlane = 128 + klane;
     const uint32_t vlut_s = smem_s + C::kSmemVLut + lane * 4;
     const uint32_t slut_s = smem_s + C::kSmemSLut + lane * 8;
     const uint32_t vt_s = smem_s + C::kSmemVt + warp * C::kVtile;
@@ -710,22 +710,22 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT>::kThreads, Cfg<KB, VB, QJ
                     lds_words_a2<1>(vs_s + (16 * mt + 2 * t + 1) * C::kVBytes + 2 + 4 * g, w1);
                     lds_words_a2<1>(vs_s + (16 * mt + 2 * t + 8) * C::kVBytes + 2 + 4 * g, w2);
                     lds_words_a2<1>(vs_s + (16 * mt + 2 * t + 9) * C::kVBytes + 2 + 4 * g, w3);
-                    // interleave the two tokens of each register: bytes [A0, B0, A1, B1] / [A2, B2, A3, B3]
-                    const uint32_t x01 = prmt(w0[0], w1[0], 0x5140u), x23 = prmt(w0[0], w1[0], 0x7362u);
-                    const uint32_t y01 = prmt(w2[0], w3[0], 0x5140u), y23 = prmt(w2[0], w3[0], 0x7362u);
+                    // interleave the two tokens of each register pair by nibbles: byte j of xl =
+                    // [2t: dims 4j, 4j+1 | 2t+1: dims 4j, 4j+1], of xh the same for dims 4j+2, 4j+3
+                    const uint32_t xl = (w0[0] & 0x0F0F0F0Fu) | ((w1[0] << 4) & 0xF0F0F0F0u);
+                    const uint32_t xh = ((w0[0] >> 4) & 0x0F0F0F0Fu) | (w1[0] & 0xF0F0F0F0u);
+                    const uint32_t yl = (w2[0] & 0x0F0F0F0Fu) | ((w3[0] << 4) & 0xF0F0F0F0u);
+                    const uint32_t yh = ((w2[0] >> 4) & 0x0F0F0F0Fu) | (w3[0] & 0xF0F0F0F0u);
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
-                        // m-tile m: row g <-> dim 16g + 8 (m >> 2) + (m & 3), row g + 8 <-> that dim + 4.
-                        // One spread of a code word gives the selectors of both: per byte
-                        // (code, code + 4) nibbles, low half = dim d, high half = dim d + 4.
-                        const uint32_t xs = (m < 4) ? x01 : x23, ys = (m < 4) ? y01 : y23;
-                        const int sh = 2 * (m & 3);
-                        const uint32_t sx = ((xs >> sh) & 0x03030303u) * 0x11u + 0x40404040u;
-                        const uint32_t sy = ((ys >> sh) & 0x03030303u) * 0x11u + 0x40404040u;
-                        const uint32_t a0 = prmt(vlo, vhi, sx), a1 = prmt(vlo, vhi, sx >> 16);
-                        const uint32_t a2 = prmt(vlo, vhi, sy), a3 = prmt(vlo, vhi, sy >> 16);
+                        // m-tile m: rows g, g + 8 <-> dims 16g + 2m, + 1: one byte of xl / xh (yl / yh)
+                        // is the pair-table entry of both rows (tokens 2t, 2t+1; 2t+8, 2t+9)
+                        const uint32_t xs = (m & 1) ? xh : xl, ys = (m & 1) ? yh : yl;
+                        const uint32_t sel = 0x6504u + 16u * (uint32_t)(m >> 1);
+                        const uint2 p = lds64(klut_s + prmt(xs, vlane, sel));
+                        const uint2 r = lds64(klut_s + prmt(ys, vlane, sel));
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], a0, a1, a2, a3, b0[nt], b1[nt]);
+                        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], p.x, p.y, r.x, r.y, b0[nt], b1[nt]);
                     }
                 } else {
                     uint32_t tile_s;
@@ -767,14 +767,13 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT>::kThreads, Cfg<KB, VB, QJ
             if (head < a.G) {
                 float *pr = a.ws + (((int64_t)b * a.Hq + kvh * a.G + head) * plan.Smax + slot) * kPartialFloats;
                 if constexpr (C::kRegV) {
-                    // dims 16g .. 16g + 15: float4 q holds m-tiles 4 (q >> 1) .. + 3, row half q & 1
+                    // dims 16g .. 16g + 15: float4 q holds dims 16g + 4q .. + 3 = m-tiles 2q, 2q + 1, rows g, g + 8
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int m0 = 4 * (q >> 1), r = q & 1;
+                        const int m0 = 2 * q;
                         reinterpret_cast<float4 *>(pr + 4 + 16 * g)[q] =
-                            make_float4(o[nt][m0][2 * r] + o[nt][m0][2 * r + 1], o[nt][m0 + 1][2 * r] + o[nt][m0 + 1][2 * r + 1],
-                                        o[nt][m0 + 2][2 * r] + o[nt][m0 + 2][2 * r + 1],
-                                        o[nt][m0 + 3][2 * r] + o[nt][m0 + 3][2 * r + 1]);
+                            make_float4(o[nt][m0][0] + o[nt][m0][1], o[nt][m0][2] + o[nt][m0][3],
+                                        o[nt][m0 + 1][0] + o[nt][m0 + 1][1], o[nt][m0 + 1][2] + o[nt][m0 + 1][3]);
                     }
                 } else {
 #pragma unroll

@@ -268,6 +268,29 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
+// Wait for the phase of parity `parity` of the mbarrier at shared address
+// `bar`.  mbarrier.try_wait suspends the warp in hardware for a while instead
+// of spinning on issue slots; the wait gives up (false) after about 100 ms
+// of device time (or 2^22 attempts), so a copy that never lands cannot hang
+// the kernel.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        uint64_t now;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+        if (i == 0) t0 = now;
+        else if (now - t0 > 100000000ull) break;
+    }
+    return false;
+}
+
 // 32-bit word at a 2-byte aligned shared-memory address.
 __device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t *p) {
     const uint16_t *h = reinterpret_cast<const uint16_t *>(p);

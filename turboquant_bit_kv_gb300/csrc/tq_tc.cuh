@@ -6,7 +6,7 @@
 // layout a TMA box of 64 columns x R rows lands in with SWIZZLE_128B): a
 // 128-column row tile is two 64-column blocks of R * 128 bytes, row m at
 // m * 128 within its block, 16-byte chunk c of the row at ((c ^ (m & 7)) << 4).
-// Every mbarrier wait is bounded (kTcSpin polls) and reports failure.
+// Every mbarrier wait is bounded (about 100 ms) and reports failure.
 
 #pragma once
 
@@ -17,10 +17,10 @@
 #include <mutex>
 
 #include "tq.h"
+#include "tq_device.cuh"
 
 namespace tq {
 
-constexpr int kTcSpin = 1 << 22;   // bound of every mbarrier wait (polls)
 
 __device__ __forceinline__ void tc_mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -35,19 +35,7 @@ __device__ __forceinline__ void tc_mbar_arrive(uint32_t bar) {
 }
 
 // Bounded wait for the phase of parity `parity`; false when it gave up.
-__device__ __forceinline__ bool tc_mbar_wait(uint32_t bar, uint32_t parity) {
-    for (int i = 0; i < kTcSpin; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (i >= 16) __nanosleep(64);
-    }
-    return false;
-}
+__device__ __forceinline__ bool tc_mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
 
 __device__ __forceinline__ void tc_tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar) {
     asm volatile(
