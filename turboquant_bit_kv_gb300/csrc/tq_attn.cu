@@ -149,61 +149,55 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prep_mma_kernel(const __gri
 
 // Merge for the tensor-core kernel's partition: the slots of segment
 // j = (sequence, KV head) are the warps whose chunk ranges touch it.  One
-// CTA per (sequence, query head); every load is issued before its result is
-// needed (slot s's (m, l) by thread s, then each dim's values of up to 32
-// slots at once), so the merge costs a few L2 round trips.  Launched as a
-// programmatic dependent of the attention kernel: its CTAs wait here until
-// that grid has finished and its writes are visible.
+// CTA per (sequence, query head), thread d = output dim d.  Reading what
+// other SMs just wrote costs a full L2 round trip, so each thread issues
+// every load of a batch of up to 32 slots at once (m and l of each slot --
+// the same address across the CTA -- and its dim of acc) and only then
+// reduces: one round trip per 32 slots, running max rescaled between
+// batches.  Launched as a programmatic dependent of the attention kernel:
+// its CTAs wait here until that grid has finished and its writes are
+// visible.
 __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const float *ws, MmaPlan plan, int Hq,
                                                                         int Hkv, int rotate_back, uint32_t s0,
                                                                         uint32_t s1, uint32_t s2, uint32_t s3,
                                                                         float *out) {
+    constexpr int kBatch = 32;
     __shared__ float buf[kD];
-    __shared__ float wts[kAttnThreads];
-    __shared__ float red[2][kAttnThreads / 32];
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int d = threadIdx.x, warp = d >> 5, lane = d & 31;
+    const int d = threadIdx.x;
     const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int G = Hq / Hkv;
     const int64_t j = (int64_t)b * Hkv + h / G;
     const int64_t first = mma_worker_of_chunk(j * plan.C, plan);
     const int nslots = (int)(mma_worker_of_chunk((j + 1) * plan.C - 1, plan) - first + 1);
     const float *base = ws + (int64_t)blockIdx.x * plan.Smax * kPartialFloats;
-    // M = max over slots of m (thread s reads slot s, s + 128, ...)
-    float M = -INFINITY;
-    for (int s = d; s < nslots; s += kAttnThreads) M = fmaxf(M, base[(int64_t)s * kPartialFloats]);
+    float M = -INFINITY, l = 0.f, acc = 0.f;
+    for (int sb = 0; sb < nslots; sb += kBatch) {
+        float mv[kBatch], lv[kBatch], xv[kBatch];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) red[0][warp] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-    float l = 0.f, acc = 0.f;
-    for (int s0 = 0; s0 < nslots; s0 += kAttnThreads) {
-        // weights of this block of slots; their l sum
-        const int s = s0 + d;
-        float w = 0.f, lw = 0.f;
-        if (s < nslots) {
-            const float m = base[(int64_t)s * kPartialFloats];
-            w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-            lw = w * base[(int64_t)s * kPartialFloats + 1];
+        for (int i = 0; i < kBatch; ++i) {
+            const bool ok = sb + i < nslots;
+            const float *ps = base + (int64_t)(sb + i) * kPartialFloats;
+            mv[i] = ok ? __ldcg(ps) : -INFINITY;
+            lv[i] = ok ? __ldcg(ps + 1) : 0.f;
+            xv[i] = ok ? __ldcg(ps + 4 + d) : 0.f;
         }
-        wts[d] = w;
+        float Mb = M;
 #pragma unroll
-        for (int off = 16; off; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
-        __syncthreads();   // wts ready; red[0] reads above are done
-        if (lane == 0) red[1][warp] = lw;
-        const int n = min(kAttnThreads, nslots - s0);
-        for (int i0 = 0; i0 < n; i0 += 32) {
-            float x[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                x[i] = (i0 + i < n) ? base[(int64_t)(s0 + i0 + i) * kPartialFloats + 4 + d] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc = fmaf(wts[i0 + i], x[i], acc);   // zero weight and value past n
+        for (int i = 0; i < kBatch; ++i) Mb = fmaxf(Mb, mv[i]);
+        if (Mb == -INFINITY) continue;   // nothing valid so far
+        if (M != -INFINITY && Mb != M) {
+            const float c = exp2f(M - Mb);
+            l *= c;
+            acc *= c;
         }
-        __syncthreads();
-        l += (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
-        __syncthreads();   // red[1] / wts are rewritten by the next block of slots
+        M = Mb;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const float w = mv[i] == -INFINITY ? 0.f : exp2f(mv[i] - M);
+            l = fmaf(w, lv[i], l);
+            acc = fmaf(w, xv[i], acc);
+        }
     }
     const float o = (l > 0.f || l != l) ? acc / l : 0.f;   // a NaN l (failed copy) propagates
     if (!rotate_back) {
