@@ -1134,12 +1134,29 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 for (int q = (nch << 3) + lane + 32 * hf; q < (nbytes >> 1); q += 64)
                     reinterpret_cast<uint16_t *>(dst)[q] = reinterpret_cast<const uint16_t *>(src)[q];
             } else {
-                // block by block to the destination rows
-                for (int j = hf; j < rows; j += 2) {
+                // to the destination rows (2-byte aligned slots) in pieces shared by both warps of the
+                // group: a block is (BB - 2) / 4 four-byte words and one 2-byte piece, the piece last
+                // when the block starts 4-byte aligned, else first
+                constexpr int NW = (BB - 2) / 4, NP = NW + 1;
+                for (int p0 = 32 * hf; p0 < rows * NP; p0 += 64) {
+                    const int p = p0 + lane;
+                    const bool valid = p < rows * NP;
+                    const int j = valid ? p / NP : 0, k = p - j * NP;
                     const int64_t di = __shfl_sync(kFull, my_di, j);
-                    uint16_t *d = reinterpret_cast<uint16_t *>(a.out + di * a.out_stride);
-                    const uint16_t *sp = reinterpret_cast<const uint16_t *>(sm_out + (32 * grp + j) * BB);
-                    for (int q = lane; q < BB / 2; q += 32) d[q] = sp[q];
+                    if (valid) {
+                        uint8_t *d = a.out + di * a.out_stride;
+                        const uint8_t *sp = sm_out + (32 * grp + j) * BB;
+                        const int lead = ((uint32_t)(uintptr_t)d & 2u) ? 1 : 0;   // 2-byte piece first
+                        if (k == (lead ? 0 : NW)) {
+                            const int o = lead ? 0 : 4 * NW;
+                            *reinterpret_cast<uint16_t *>(d + o) = *reinterpret_cast<const uint16_t *>(sp + o);
+                        } else {
+                            const int o = 4 * (k - lead) + 2 * lead;
+                            const uint32_t w = (uint32_t)*reinterpret_cast<const uint16_t *>(sp + o) |
+                                               ((uint32_t)*reinterpret_cast<const uint16_t *>(sp + o + 2) << 16);
+                            *reinterpret_cast<uint32_t *>(d + o) = w;
+                        }
+                    }
                 }
             }
         }
