@@ -76,20 +76,28 @@ def test_encode_bf16_workloads_ragged(env, bits, src):
         check_codes(g, bits, x.double().numpy(), env["s"], env["books"][bits][2], "%s %s" % (src, name))
 
 
-def test_encode_fp16_and_strided_rows(env):
+# Calls of up to 1024 rows use the mma.sync encode kernel, larger ones the
+# tcgen05 kernel: the layout and edge-case tests run at both sizes.
+SMALL_AND_TC = [333, 2333]
+
+
+@pytest.mark.parametrize("n", SMALL_AND_TC)
+def test_encode_fp16_and_strided_rows(env, n):
     tq = env["tq"]
     gen = torch.Generator().manual_seed(11)
-    base = torch.randn((333, 2 * D), generator=gen).to(torch.float16)
+    base = torch.randn((n, 2 * D), generator=gen).to(torch.float16)
     x = base[:, 64:64 + D]                   # row stride 256 elements, offset 64 (128 B)
     g = _encode_gpu(env, base.to(env["dev"])[:, 64:64 + D], 3)
     check_codes(g, 3, x.double().numpy(), env["s"], env["books"][3][2], "fp16 strided")
     assert tq.tq_block_bytes(3) == g.shape[1]
 
 
-def test_encode_edge_vectors(env):
+@pytest.mark.parametrize("pad", [0, 2048])
+def test_encode_edge_vectors(env, pad):
     rows = [np.zeros(D), np.full(D, 3.0), np.full(D, -0.5), np.eye(D)[5] * 7.0, np.eye(D)[127] * -2.0,
             np.linspace(-1, 1, D) * 1e4, np.linspace(-1, 1, D) * 2.0**-100,
             np.where(np.arange(D) % 2 == 0, 1.0, -1.0), np.r_[np.ones(64), np.zeros(64)]]
+    rows += list(np.random.default_rng(13).standard_normal((pad, D)))   # pad: through the tcgen05 kernel
     x = torch.tensor(np.array(rows), dtype=torch.float32).to(torch.bfloat16)
     for bits in (2, 3, 4):
         g = _encode_gpu(env, x.to(env["dev"]), bits)
@@ -126,11 +134,11 @@ def test_encode_listed_rows_in_full_groups(env):
     check_codes(g, 2, tt.double().numpy(), env["s"], env["books"][2][2], "tiny rows")
 
 
-def test_encode_scatter_dst_index_and_slot_stride(env):
+@pytest.mark.parametrize("n,slots", [(37, 100), (1500, 2000)])
+def test_encode_scatter_dst_index_and_slot_stride(env, n, slots):
     """Append-style scatter into a slot layout (K block then V block per slot)."""
     tq = env["tq"]
     dev = env["dev"]
-    n, slots = 37, 100
     slot = tq.tq_block_bytes(4) + tq.tq_block_bytes(2)
     gen = torch.Generator().manual_seed(5)
     k = torch.randn((n, D), generator=gen).to(torch.bfloat16)
@@ -151,7 +159,8 @@ def test_encode_scatter_dst_index_and_slot_stride(env):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4])
-def test_encode_dst_index_runs(env, bits):
+@pytest.mark.parametrize("reps", [1, 8])
+def test_encode_dst_index_runs(env, bits, reps):
     """Destination indices mixing 32-row groups that form one aligned run of
     consecutive slots (stored in bulk), an unaligned run, a run with one pair
     swapped, a reversed group and a ragged tail: every block lands in its own
@@ -159,13 +168,16 @@ def test_encode_dst_index_runs(env, bits):
     tq = env["tq"]
     dev = env["dev"]
     bb = tq.tq_block_bytes(bits)
-    slots = 600
-    runs = [np.arange(64, 96),                 # aligned run (64 * bb is a multiple of 16)
-            np.arange(101, 133),               # consecutive but unaligned
-            np.r_[np.arange(200, 216), 217, 216, np.arange(218, 232)],   # one pair swapped
-            np.arange(300, 332)[::-1],         # reversed
-            np.arange(400, 432),               # aligned run
-            np.arange(500, 507)]               # ragged tail
+    slots = 600 * reps
+    runs = []
+    for r in range(reps):                      # reps = 8: 1336 rows, through the tcgen05 kernel
+        o = 600 * r
+        runs += [np.arange(64, 96) + o,        # aligned run (64 * bb is a multiple of 16)
+                 np.arange(101, 133) + o,      # consecutive but unaligned
+                 np.r_[np.arange(200, 216), 217, 216, np.arange(218, 232)] + o,   # one pair swapped
+                 np.arange(300, 332)[::-1] + o,   # reversed
+                 np.arange(400, 432) + o]      # aligned run
+    runs.append(np.arange(500, 507) + 600 * (reps - 1))   # ragged tail
     dst = torch.from_numpy(np.concatenate(runs).astype(np.int64))
     n = dst.numel()
     gen = torch.Generator().manual_seed(11 + bits)

@@ -1204,8 +1204,15 @@ int launch_tc(const EncArgs &a, cudaStream_t st) {
     return launch_status();
 }
 
+// Up to this many rows (eight 128-row tiles) the tensor-core kernel's
+// per-CTA setup (H D in shared memory, tensor-memory allocation, barriers)
+// outweighs the work: the warp-independent mma.sync kernel serves such
+// calls (the append of one token per sequence and KV head).
+constexpr int64_t kTcMaxSmallRows = 1024;
+
 template <int BITS, int DT>
 int launch_16bit(const EncArgs &a, cudaStream_t st) {
+    if (a.n_vec <= kTcMaxSmallRows) return launch_mma<BITS, DT>(a, st);
     const int r = launch_tc<BITS, DT>(a, st);
     return r == 1 ? launch_mma<BITS, DT>(a, st) : r;
 }
