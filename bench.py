@@ -238,7 +238,7 @@ def plan_llama(tq, wl, dev, stream, seed, batch):
               nb["enc_k"], 1, nvec),
            Op("encode_v", "encode", lambda: tq.tq_encode_kv(v.view(-1, 128), vcb, signs, vb, stream=stream),
               nb["enc_v"], 1, nvec),
-           Op("attention", "attention", attn, nb["attn"], 2)]
+           Op("attention", "attention", attn, nb["attn"], 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
@@ -281,7 +281,7 @@ def plan_single_head(tq, wl, dev, stream, seed, batch):
               1, T),
            Op("encode_v", "encode", lambda: tq.tq_encode_kv(v, vcb, signs, vb, stream=stream), T * (512 + 34),
               1, T),
-           Op("attention", "attention", attn, T * 100 + 512 + 512, 2)]
+           Op("attention", "attention", attn, T * 100 + 512 + 512, 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
@@ -333,7 +333,7 @@ def plan_qwen(tq, wl, dev, stream, seed, batch):
            Op("encode_v", "encode", enc(pre["v"], "v", dst_pre), n_pre * (256 + 50), 1, n_pre),
            Op("append_k", "append", enc(new["k"], "k", dst_new), n_new * (256 + 50), 1, n_new),
            Op("append_v", "append", enc(new["v"], "v", dst_new), n_new * (256 + 50), 1, n_new),
-           Op("attention", "attention", attn, B * Hkv * T * 100 + B * Hq * 128 * (2 + 4), 2)]
+           Op("attention", "attention", attn, B * Hkv * T * 100 + B * Hq * 128 * (2 + 4), 3)]
 
     def e2e():
         hk, hv = _pinned(pre["k"]), _pinned(pre["v"])
@@ -387,7 +387,7 @@ def plan_qjl(tq, wl, dev, stream, seed, batch):
 
     ops = [Op("encode_k", "encode", lambda: enc(k), n * (256 + 50), 1, n),
            Op("qjl_encode", "qjl", lambda: qjl(k), n * (256 + 50 + 16 + 2) + 128 * 128 * 4, 1, n),
-           Op("attention", "attention", attn, n * (50 + 16 + 2 + 256) + B * Hq * 128 * (2 + 4) + 128 * 128 * 4, 2)]
+           Op("attention", "attention", attn, n * (50 + 16 + 2 + 256) + B * Hq * 128 * (2 + 4) + 128 * 128 * 4, 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
