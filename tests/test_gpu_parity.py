@@ -327,8 +327,16 @@ def test_attention_single_head(env, kbits, vbits):
     (1, 4, 2, 130, 136, 4, 4, [129]),               # G = 2
     (2, 16, 2, 200, 200, 2, 2, [0, 200]),           # G = 8, an empty sequence
     (1, 4, 1, 1, 8, 4, 2, None),                    # a single token
+    # many short segments: warp chunk ranges span several (sequence, KV head) segments,
+    # random lengths with empty sequences among them
+    (500, 8, 8, 20, 24, 4, 2, "random"),            # G = 1, one chunk per segment
+    (300, 32, 8, 70, 72, 3, 3, "random"),           # G = 4, three chunks per segment
+    (100, 56, 8, 45, 48, 3, 3, "random"),           # G = 7 (two n-tiles)
 ])
 def test_attention_gqa_ragged(env, B, Hq, Hkv, T, T_cap, kbits, vbits, lens):
+    if lens == "random":
+        lens = [int(x) for x in np.random.default_rng(B).integers(0, T + 1, B)]
+        lens[0], lens[-1] = 0, T
     w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=21)
     k = w["k"].double().numpy()
     v = w["v"].double().numpy()
