@@ -990,7 +990,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc_fence_after();
             const int64_t v0 = tile * kTcRows;
             const int nv = (int)min64(kTcRows, a.n_vec - v0);
-            const uint8_t *tile_s = smem + S::kA + st * kTcTileBytes;
+            const int rows = max(0, min(32, nv - 32 * grp));
+            // destination rows of this warp's group, requested now (one coalesced load) so that
+            // the load is in flight during the quantiser
+            int64_t my_di = 0;
+            if (!a.contiguous)
+                my_di = lane < rows ? (a.dst_index ? __ldg(a.dst_index + v0 + 32 * grp + lane) : v0 + 32 * grp + lane) : 0;
             const uint32_t taddr = tmem + ((uint32_t)(32 * grp) << 16) + (uint32_t)(st * 128 + 64 * hf);
             // ---- norm: sum of squares of u (= 128 ||x||^2), the two halves added in a fixed order
             float2 q2 = make_float2(0.f, 0.f);
@@ -1105,13 +1110,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bars + 32 + 8 * st);
-            const int rows = max(0, min(32, nv - 32 * grp));
-            // destination rows of the group, fetched once (one coalesced load); a run of 32
-            // consecutive, 16-byte aligned slots goes out like a contiguous group
-            int64_t my_di = 0, di0 = v0 + 32 * grp;
+            // a run of 32 consecutive, 16-byte aligned destination slots goes out like a contiguous group
+            int64_t di0 = v0 + 32 * grp;
             bool run = a.contiguous != 0;
             if (!a.contiguous) {
-                my_di = lane < rows ? (a.dst_index ? a.dst_index[v0 + 32 * grp + lane] : v0 + 32 * grp + lane) : 0;
                 di0 = __shfl_sync(kFull, my_di, 0);
                 run = __all_sync(kFull, a.idx_bulk && rows == 32 && my_di == di0 + lane && ((di0 * BB) & 15) == 0);
             }
