@@ -502,12 +502,23 @@ def test_qjl_encode_outlier_keys(env):
 
 # ------------------------------------------------------------------ serde
 
-@pytest.mark.parametrize("L,T,hidden,bs,sf,sl", [(6, 32, 256, 16, 2, 2), (5, 40, 256, 16, 1, 1),
-                                                  (3, 16, 128, 16, 2, 2)])
-def test_serde_roundtrip_matches_oracle(env, L, T, hidden, bs, sf, sl):
+@pytest.mark.parametrize("L,T,hidden,bs,sf,sl,special", [
+    (6, 32, 256, 16, 2, 2, False), (5, 40, 256, 16, 1, 1, False), (3, 16, 128, 16, 2, 2, False),
+    # whole 128-row tiles of slots (one paired launch), with zero, tiny and huge rows in both halves
+    (4, 64, 1024, 16, 1, 1, True)])
+def test_serde_roundtrip_matches_oracle(env, L, T, hidden, bs, sf, sl, special):
     tq = env["tq"]
     dev = env["dev"]
     x = workloads.storage_kv(L=L, T=T, hidden=hidden, seed=12)["kv"]
+    if special:
+        rows = x.view(2, L, T, hidden // D, D)
+        rng = np.random.default_rng(5)
+        for kv in (0, 1):
+            for l in range(sf, L - sl):
+                t = rng.choice(T, 6, replace=False)
+                rows[kv, l, t[0:2]] = 0.0
+                rows[kv, l, t[2:4]] *= 2.0**-110
+                rows[kv, l, t[4:6]] *= 2.0**60
     values = x.double().numpy()
     raw = x.view(torch.uint8).numpy().reshape(2, L, T, hidden * 2)
     (kc, _, kb32), (vc, _, vb32) = env["books"][4], env["books"][4]
@@ -546,8 +557,10 @@ def test_serde_roundtrip_matches_oracle(env, L, T, hidden, bs, sf, sl):
         assert np.array_equal(gbytes[:, l], rraw[:, l])
     grec = out.double().cpu().numpy()
     for l in range(qs, qe):
-        d = np.abs(grec[:, l] - rec[:, l])
-        assert np.all(d <= np.abs(rec[:, l]) * 2.0**-7 + 1e-30)
+        fin = np.isfinite(rec[:, l])   # rows whose fp16 norm overflowed decode to inf / NaN on both sides
+        d = np.abs(grec[:, l][fin] - rec[:, l][fin])
+        assert np.all(d <= np.abs(rec[:, l][fin]) * 2.0**-7 + 1e-30)
+        assert not np.isfinite(grec[:, l][~fin]).any()   # the inf / NaN mix depends on the summation order
 
 
 @pytest.mark.parametrize("kbits,packed_v", [(4, False), (2, True)])

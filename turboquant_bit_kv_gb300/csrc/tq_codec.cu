@@ -24,6 +24,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -399,11 +400,21 @@ extern "C" int tq_serde_serialize(const void *src, int elem_dtype, int num_layer
     if (Lc > 0) {
         const int es = g.es;
         if (g.T % g.bs == 0) {
-            r = tq_encode_kv(s + g.qs * layer_bytes, elem_dtype, Lc * g.T * g.H, kD, kcb, signs, comp, g.slot,
-                             nullptr, stream);
-            if (r != TQ_OK) return r;
-            r = tq_encode_kv(s + (g.L + g.qs) * layer_bytes, elem_dtype, Lc * g.T * g.H, kD, vcb, signs,
-                             comp + g.kbb, g.slot, nullptr, stream);
+            // one paired launch fills whole slots (K block then V block) when both halves use the
+            // same codebook; otherwise one launch per half
+            const bool same = kcb->bits == vcb->bits && g.slot == 2 * g.kbb &&
+                              memcmp(kcb->centroids, vcb->centroids, sizeof(kcb->centroids)) == 0 &&
+                              memcmp(kcb->boundaries, vcb->boundaries, sizeof(kcb->boundaries)) == 0;
+            r = same ? encode_kv_pair(s + g.qs * layer_bytes, s + (g.L + g.qs) * layer_bytes, elem_dtype,
+                                      Lc * g.T * g.H, kD, kcb, signs, comp, st)
+                     : 1;
+            if (r == 1) {
+                r = tq_encode_kv(s + g.qs * layer_bytes, elem_dtype, Lc * g.T * g.H, kD, kcb, signs, comp, g.slot,
+                                 nullptr, stream);
+                if (r != TQ_OK) return r;
+                r = tq_encode_kv(s + (g.L + g.qs) * layer_bytes, elem_dtype, Lc * g.T * g.H, kD, vcb, signs,
+                                 comp + g.kbb, g.slot, nullptr, stream);
+            }
             if (r != TQ_OK) return r;
         } else {
             for (int64_t li = 0; li < Lc; ++li) {

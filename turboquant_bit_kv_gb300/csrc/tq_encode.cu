@@ -52,6 +52,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct EncArgs {
     const uint8_t *x;
+    const uint8_t *x2;  // paired encode: the rows whose blocks fill the second half of each slot
     int64_t n_vec;
     int64_t x_stride;   // bytes
     uint8_t *out;
@@ -781,13 +782,18 @@ constexpr int kTcTileBytes = kTcRows * 256;           // one row tile (two 16 KB
 constexpr uint32_t kTcCols = 256;                     // tensor-memory columns: two 128-column accumulators
 constexpr int kTcFixCap = 240;                        // rows a CTA can list for finishing after its main loop
 
-template <int BITS>
+// PAIR: two row sets encoded into the two halves of 2 BB-byte slots (K then V
+// block of a storage slot), tile i of both by the same CTA; one row-tile
+// buffer (freed when the tile's MMAs complete) keeps two CTAs per SM.
+template <int BITS, bool PAIR = false>
 struct TcSmem {
     static constexpr int BB = 2 + 16 * BITS;
+    static constexpr int kSlotB = PAIR ? 2 * BB : BB;                // bytes per output slot
+    static constexpr int kABufs = PAIR ? 1 : 2;                       // row-tile buffers
     static constexpr int kB = 0;                                     // H D, 32 KB (1024-byte aligned)
-    static constexpr int kA = kB + kTcTileBytes;                     // two row tiles
-    static constexpr int kOut = kA + 2 * kTcTileBytes;               // 128 blocks
-    static constexpr int kTab = kOut + ((kTcRows * BB + 15) & ~15);  // cell table, 128 x 8 B
+    static constexpr int kA = kB + kTcTileBytes;                     // row tiles
+    static constexpr int kOut = kA + kABufs * kTcTileBytes;          // 128 slots
+    static constexpr int kTab = kOut + ((kTcRows * kSlotB + 15) & ~15);  // cell table, 128 x 8 B
     static constexpr int kPart = kTab + kBuckets * 8;                // per-row partial sums of squares, [2][128]
     static constexpr int kFix = kPart + 2 * kTcRows * 4;             // rows finished after the main loop
     static constexpr int kBars = kFix + (4 + kTcFixCap) * 4;          // full[2], mma[2], empty[2]
@@ -838,10 +844,10 @@ __device__ __noinline__ unsigned short exact_norm_row(const uint8_t *tile, int r
 // gets the correctly rounded norm (double-float sum of squares).
 template <int BITS, int DT>
 __device__ __forceinline__ void finish_row_warp(const EncArgs &a, const float2 *tab, int64_t v, bool whole, bool check,
-                                                int lane) {
+                                                int lane, int half = 0) {
     static_assert(DT != TQ_F32, "16-bit rows");
     constexpr int BB = BlockFmt<BITS>::kBytes;
-    const uint8_t *xrow = a.x + v * a.x_stride;
+    const uint8_t *xrow = (half ? a.x2 : a.x) + v * a.x_stride;
     const uint2 raw = *reinterpret_cast<const uint2 *>(xrow + 8 * lane);
     const uint32_t h[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
     SumSq2 acc;
@@ -862,7 +868,7 @@ __device__ __forceinline__ void finish_row_warp(const EncArgs &a, const float2 *
         c1 = c1 + oc + ne;
     }
     const int64_t di = a.dst_index ? a.dst_index[v] : v;
-    uint8_t *dst = a.out + di * a.out_stride;
+    uint8_t *dst = a.out + di * a.out_stride + half * BB;
     if (!__any_sync(kFull, nz)) {
         const uint8_t fill = BITS == 4 ? 0x88 : BITS == 2 ? 0xAA : 0x00;   // code L/2 in every field
         for (int j = lane; j < BB; j += 32) dst[j] = j < 2 ? 0 : (BITS == 3 && j >= 34) ? 0xFF : fill;
@@ -884,11 +890,13 @@ __device__ __forceinline__ void finish_row_warp(const EncArgs &a, const float2 *
     }
 }
 
-template <int BITS, int DT>
-// two CTAs (2 x 288 threads) per SM
+template <int BITS, int DT, bool PAIR = false>
+// two CTAs (2 x 288 threads) per SM; tmap2: the second row set (PAIR only)
 __global__ void __launch_bounds__(kTcThreads, 2)
-    encode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ EncArgs a) {
-    using S = TcSmem<BITS>;
+    encode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap2,
+                     const __grid_constant__ EncArgs a) {
+    using S = TcSmem<BITS, PAIR>;
+    constexpr int NH = PAIR ? 2 : 1;   // row sets per tile
     constexpr int BB = S::BB;
     __shared__ __align__(16) float2 s_tab[kBuckets];   // cell table at a fixed shared address
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -950,16 +958,21 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (lane == 0) {
             const uint32_t idesc = tc_idesc<DT>();
             int i = 0;
-            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+            for (int half = 0; half < NH; ++half, ++i) {
                 const int st = i & 1;
                 const uint32_t use = (uint32_t)(i >> 1);
                 if (i >= 2) tc_mbar_wait(bars + 32 + 8 * st, (use - 1u) & 1u);   // stage released
+                // PAIR: one row-tile buffer, free once the previous tile's MMAs have completed
+                if (PAIR && i >= 1) tc_mbar_wait(bars + 16 + 8 * (st ^ 1), (uint32_t)((i - 1) >> 1) & 1u);
                 tc_fence_after();
-                const uint32_t a_s = base_s + S::kA + st * kTcTileBytes;
-                tc_mbar_expect_tx(bars + 8 * st, kTcTileBytes);
-                tc_tma_load_2d(a_s, &tmap, 0, (int)(tile * kTcRows), bars + 8 * st);
-                tc_tma_load_2d(a_s + 16384, &tmap, 64, (int)(tile * kTcRows), bars + 8 * st);
-                tc_mbar_wait(bars + 8 * st, use & 1u);
+                const int ab = PAIR ? 0 : st;   // row-tile buffer and its full barrier
+                const uint32_t a_s = base_s + S::kA + ab * kTcTileBytes, full = bars + 8 * ab;
+                const CUtensorMap *map = (PAIR && half) ? &tmap2 : &tmap;
+                tc_mbar_expect_tx(full, kTcTileBytes);
+                tc_tma_load_2d(a_s, map, 0, (int)(tile * kTcRows), full);
+                tc_tma_load_2d(a_s + 16384, map, 64, (int)(tile * kTcRows), full);
+                tc_mbar_wait(full, PAIR ? ((uint32_t)i & 1u) : (use & 1u));
                 const uint32_t d = tmem + (uint32_t)(st * 128);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -984,7 +997,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const bool bulk_out = a.contiguous != 0 || a.idx_bulk != 0;
         const float2 off2 = make_float2(1572928.f, 1572928.f);   // 64 + 1.5 * 2^20
         int i = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+        for (int half = 0; half < NH; ++half, ++i) {
             const int st = i & 1;
             tc_mbar_wait(bars + 16 + 8 * st, (uint32_t)(i >> 1) & 1u);
             tc_fence_after();
@@ -1039,7 +1053,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const bool oor = !zero_row && !(ss >= 1.0097419586828951e-28f /* 128 * 2^-100 */ && ss <= 1.2676506002282294e30f);
             const float sc = sqrtf(ss);
             const float nrm = sc * 0.08838834764831845f;
-            uint8_t *blk = sm_out + r * BB;
+            uint8_t *blk = sm_out + r * S::kSlotB + half * BB;
             if (hf == 0) {
                 *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__float2half_rn(nrm));
                 // rows whose norm lies within 2^-20 of an fp16 rounding boundary, or whose sum of
@@ -1053,7 +1067,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     base = __shfl_sync(kFull, base, leader);
                     if (need) {
                         const int slot = base + __popc(m & ((1u << lane) - 1u));
-                        if (slot < kTcFixCap) fix[4 + slot] = (int)(v0 + r) | (oor ? (int)0x80000000 : 0);
+                        if (slot < kTcFixCap)
+                            fix[4 + slot] = (int)(v0 + r) | (half ? 0x40000000 : 0) | (oor ? (int)0x80000000 : 0);
                         else fix[1] = 1;
                     }
                 }
@@ -1118,15 +1133,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 run = __all_sync(kFull, a.idx_bulk && rows == 32 && my_di == di0 + lane && ((di0 * BB) & 15) == 0);
             }
             if (bulk_out && rows == 32 && run) {
-                // 32 * BB bytes at a 16-byte aligned offset (32 * BB is a multiple of 16)
-                if (hf == 0 && lane == 0) {
-                    uint8_t *dst = a.out + di0 * BB;
-                    const uint32_t src = (uint32_t)__cvta_generic_to_shared(sm_out + 32 * grp * BB);
+                // 32 slots (32 * kSlotB bytes, a multiple of 16) at a 16-byte aligned offset; paired:
+                // once both halves of the slots are written
+                if ((!PAIR || half == NH - 1) && hf == 0 && lane == 0) {
+                    uint8_t *dst = a.out + di0 * S::kSlotB;
+                    const uint32_t src = (uint32_t)__cvta_generic_to_shared(sm_out + 32 * grp * S::kSlotB);
                     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
-                                 "r"(32 * BB)
+                                 "r"(32 * S::kSlotB)
                                  : "memory");
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
+            } else if (PAIR) {
+                // not reached: paired calls cover whole 128-row tiles of contiguous slots
             } else if (a.contiguous) {
                 uint8_t *dst = a.out + (v0 + 32 * grp) * BB;
                 const uint8_t *src = sm_out + 32 * grp * BB;
@@ -1161,6 +1179,33 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     }
                 }
             }
+
+            // ---- paired calls cover twice the rows per CTA: keep the list of rows to finish from
+            // overflowing (an overflowing CTA rechecks every row it encoded) -- once the next tile could
+            // fill it, finish the listed rows now, from memory (every block of the CTA has left: the
+            // bulk stores are waited for), and empty it.  The count is read between two barriers, so
+            // every epilogue warp takes the same decision.  (Unpaired calls keep their warps free of
+            // CTA-wide barriers: about one row in 250 is listed, so a list covers ~60 k rows per CTA.)
+            if constexpr (PAIR) {
+            asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
+            const int listed = fix[0], overflowed = fix[1];
+            asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
+            if (listed > kTcFixCap - kTcRows && overflowed == 0) {
+                if (bulk_out && hf == 0 && lane == 0) {
+                    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
+                for (int q = warp; q < listed; q += kTcEpiWarps) {
+                    const uint32_t e = (uint32_t)fix[4 + q];
+                    finish_row_warp<BITS, DT>(a, s_tab, (int64_t)(e & 0x3FFFFFFFu), (e >> 31) != 0, false, lane,
+                                              (int)((e >> 30) & 1u));
+                }
+                asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
+                if (threadIdx.x == 0) fix[0] = 0;
+                asm volatile("bar.sync 5, %0;" ::"n"(32 * kTcEpiWarps) : "memory");
+            }
+            }
         }
 
         // ---- finish the listed rows once every block of this CTA is in memory
@@ -1173,13 +1218,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const int nfix = min(fix[0], kTcFixCap);
             for (int q = warp; q < nfix; q += kTcEpiWarps) {
                 const uint32_t e = (uint32_t)fix[4 + q];
-                finish_row_warp<BITS, DT>(a, s_tab, (int64_t)(e & 0x7FFFFFFFu), (e >> 31) != 0, false, lane);
+                finish_row_warp<BITS, DT>(a, s_tab, (int64_t)(e & 0x3FFFFFFFu), (e >> 31) != 0, false, lane,
+                                          (int)((e >> 30) & 1u));
             }
         } else {
             for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
-                for (int rr = warp; rr < kTcRows; rr += kTcEpiWarps)
-                    if (tile * kTcRows + rr < a.n_vec)
-                        finish_row_warp<BITS, DT>(a, s_tab, tile * kTcRows + rr, false, true, lane);
+                for (int half = 0; half < NH; ++half)
+                    for (int rr = warp; rr < kTcRows; rr += kTcEpiWarps)
+                        if (tile * kTcRows + rr < a.n_vec)
+                            finish_row_warp<BITS, DT>(a, s_tab, tile * kTcRows + rr, false, true, lane, half);
         }
     }
 
@@ -1198,11 +1245,28 @@ int launch_tc(const EncArgs &a, cudaStream_t st) {
     CUtensorMap map;
     if (!make_row_tile_map(&map, a.x, DT, a.n_vec, a.x_stride)) return 1;
     static int done[64] = {0};
-    if (set_smem_limit((const void *)encode_tc_kernel<BITS, DT>, TcSmem<BITS>::kTotal, done) != TQ_OK)
+    if (set_smem_limit((const void *)encode_tc_kernel<BITS, DT, false>, TcSmem<BITS>::kTotal, done) != TQ_OK)
         return TQ_ERR_CUDA;
     const int64_t ntiles = (a.n_vec + kTcRows - 1) / kTcRows;
     const int grid = (int)std::min<int64_t>(ntiles, 2 * (int64_t)sm_count());
-    encode_tc_kernel<BITS, DT><<<grid, kTcThreads, TcSmem<BITS>::kTotal, st>>>(map, a);
+    encode_tc_kernel<BITS, DT, false><<<grid, kTcThreads, TcSmem<BITS>::kTotal, st>>>(map, map, a);
+    return launch_status();
+}
+
+// Paired launch: rows of a.x into the first and rows of a.x2 into the second
+// half of each 2 BB-byte slot; 1 when the rows cannot be described by tensor
+// maps.
+template <int BITS, int DT>
+int launch_tc_pair(const EncArgs &a, cudaStream_t st) {
+    CUtensorMap map, map2;
+    if (!make_row_tile_map(&map, a.x, DT, a.n_vec, a.x_stride) || !make_row_tile_map(&map2, a.x2, DT, a.n_vec, a.x_stride))
+        return 1;
+    static int done[64] = {0};
+    if (set_smem_limit((const void *)encode_tc_kernel<BITS, DT, true>, TcSmem<BITS, true>::kTotal, done) != TQ_OK)
+        return TQ_ERR_CUDA;
+    const int64_t ntiles = a.n_vec / kTcRows;
+    const int grid = (int)std::min<int64_t>(ntiles, 2 * (int64_t)sm_count());
+    encode_tc_kernel<BITS, DT, true><<<grid, kTcThreads, TcSmem<BITS, true>::kTotal, st>>>(map, map2, a);
     return launch_status();
 }
 
@@ -1289,3 +1353,46 @@ extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x
         default: return TQ_ERR_UNSUPPORTED;
     }
 }
+
+namespace tq {
+
+// Paired encode for the storage layout: row i of k into bytes [0, BB) and row
+// i of v into bytes [BB, 2 BB) of slot i (slot = 2 BB bytes, contiguous), both
+// with codebook cb, so that every 32 slots leave as one bulk copy instead of
+// two launches each writing half of every slot.  Returns 1 (nothing
+// enqueued) when the call is not of that form: 16-bit rows, a whole number
+// of 128-row tiles (fewer than 2^30 rows), 16-byte aligned rows and slots.
+int encode_kv_pair(const void *k, const void *v, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
+                   const tq_codebook *cb, tq_signs signs, uint8_t *slots, cudaStream_t st) {
+    if (!cb || !codebook_ok(cb) || (x_dtype != TQ_BF16 && x_dtype != TQ_F16)) return 1;
+    if (n_vec <= 0 || n_vec % kTcRows || n_vec >= (int64_t(1) << 30)) return 1;
+    const int64_t bb = (int64_t)tq_block_bytes(cb->bits);
+    if (!k || !v || !slots || x_stride_elems < kD || (x_stride_elems * 2) % 16 || !aligned(k, 16) ||
+        !aligned(v, 16) || !aligned(slots, 16))
+        return 1;
+    EncArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = static_cast<const uint8_t *>(k);
+    a.x2 = static_cast<const uint8_t *>(v);
+    a.n_vec = n_vec;
+    a.x_stride = x_stride_elems * 2;
+    a.out = slots;
+    a.out_stride = 2 * bb;
+    a.dst_index = nullptr;
+    a.contiguous = 1;
+    a.idx_bulk = 0;
+    a.b0 = cb->boundaries[(1 << cb->bits) / 2];
+    build_table(cb, &a);
+    for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
+    switch (cb->bits * 8 + x_dtype) {
+        case 2 * 8 + TQ_BF16: return launch_tc_pair<2, TQ_BF16>(a, st);
+        case 2 * 8 + TQ_F16: return launch_tc_pair<2, TQ_F16>(a, st);
+        case 3 * 8 + TQ_BF16: return launch_tc_pair<3, TQ_BF16>(a, st);
+        case 3 * 8 + TQ_F16: return launch_tc_pair<3, TQ_F16>(a, st);
+        case 4 * 8 + TQ_BF16: return launch_tc_pair<4, TQ_BF16>(a, st);
+        case 4 * 8 + TQ_F16: return launch_tc_pair<4, TQ_F16>(a, st);
+        default: return 1;
+    }
+}
+
+}  // namespace tq

@@ -35,6 +35,12 @@ int qjl_encode_tc(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_by
                   int64_t block_stride, int bits, const float *centroids, const uint32_t *signs, const float *S,
                   uint8_t *qjl_bits, uint16_t *res_norm_f16, cudaStream_t st);
 
+// Paired encode into 2 BB-byte slots (tq_encode.cu): k rows into the first,
+// v rows into the second half of each slot.  Returns 1 when the call is not
+// of the form it covers (then nothing was enqueued), else a TQ_ status.
+int encode_kv_pair(const void *k, const void *v, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
+                   const tq_codebook *cb, tq_signs signs, uint8_t *slots, cudaStream_t st);
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
