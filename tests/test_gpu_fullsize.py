@@ -68,10 +68,13 @@ def _check_attention_slice(env, q, out, b, h, G, k_hat, v_hat, scale, term2=None
     assert np.all(err < ATTN_TOL), (b, h, err.max())
 
 
-def test_llama_decode_fullsize(env):
-    """Batch 16, 32/8 heads, context 8192, bf16 K/V, K4/V2."""
+@pytest.mark.parametrize("T", [8192, 32768])
+def test_llama_decode_fullsize(env, T):
+    """Batch 16, 32/8 heads, bf16 K/V, K4/V2; context 8192 (the attention
+    kernel's 12-warp variant: fewer than 32 chunks per warp at 16 warps per
+    SM) and 32768 (the 16-warp variant)."""
     tq, dev = env["tq"], env["dev"]
-    B, Hq, Hkv, T = 16, 32, 8, 8192
+    B, Hq, Hkv = 16, 32, 8
     G = Hq // Hkv
     w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=0, device=dev)
     k, v, q = w["k"], w["v"], w["q"]

@@ -7,9 +7,9 @@
 namespace tq {
 
 // CTAs per SM and warps per CTA of a configuration (0 CTAs: not covered).
-void mma_shape_k2(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps);
-void mma_shape_k3(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps);
-void mma_shape_k4(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps);
+void mma_shape_k2(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
+void mma_shape_k3(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
+void mma_shape_k4(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
 int launch_attn_mma_k2(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 int launch_attn_mma_k3(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
@@ -17,15 +17,15 @@ int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int n
 // n-tiles of 4 query heads (times hi / lo parts) for G query heads per KV head
 static int mma_ntiles(int G) { return G <= 4 ? 1 : 2; }
 
-static void mma_shape(int kb, int vb, bool qjl, int G, int *ctas_per_sm, int *warps) {
+static void mma_shape(int kb, int vb, bool qjl, int G, bool wide, int *ctas_per_sm, int *warps) {
     *ctas_per_sm = 0;
     *warps = 0;
     if (G < 1 || G > 8) return;
     const int nt = mma_ntiles(G);
     switch (kb) {
-        case 2: mma_shape_k2(vb, qjl, nt, ctas_per_sm, warps); break;
-        case 3: mma_shape_k3(vb, qjl, nt, ctas_per_sm, warps); break;
-        case 4: mma_shape_k4(vb, qjl, nt, ctas_per_sm, warps); break;
+        case 2: mma_shape_k2(vb, qjl, nt, wide, ctas_per_sm, warps); break;
+        case 3: mma_shape_k3(vb, qjl, nt, wide, ctas_per_sm, warps); break;
+        case 4: mma_shape_k4(vb, qjl, nt, wide, ctas_per_sm, warps); break;
         default: break;
     }
 }
@@ -40,11 +40,13 @@ static int mma_slots(int64_t segs, int64_t C, int64_t W) {
 
 MmaPlan mma_plan(int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G) {
     MmaPlan p;
-    int per_sm = 0, warps = 0;
-    mma_shape(kb, vb, qjl, G, &per_sm, &warps);
     const int64_t segs = (int64_t)B * Hkv;
     p.C = (T + kMmaChunk - 1) / kMmaChunk;
     p.Ctot = segs * p.C;
+    // the 16-warp variant once every warp would get at least 32 chunks, else 12 warps per SM
+    p.wide = p.Ctot >= (int64_t)32 * kMmaMaxWarpsPerSm * sm_count() ? 1 : 0;
+    int per_sm = 0, warps = 0;
+    mma_shape(kb, vb, qjl, G, p.wide != 0, &per_sm, &warps);
     p.P = (int)min64(p.Ctot, (int64_t)(per_sm > 0 ? per_sm : 1) * sm_count());
     // at most one worker per chunk, so that every worker range is non-empty
     p.W = (int)min64(p.Ctot, (int64_t)p.P * (warps > 0 ? warps : 1));
@@ -62,7 +64,7 @@ int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap) {
 
 bool attn_mma_supported(int kb, int vb, bool qjl, int G) {
     int per_sm = 0, warps = 0;
-    mma_shape(kb, vb, qjl, G, &per_sm, &warps);
+    mma_shape(kb, vb, qjl, G, true, &per_sm, &warps);
     return per_sm > 0;
 }
 

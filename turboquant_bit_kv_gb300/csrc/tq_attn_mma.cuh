@@ -73,12 +73,14 @@ constexpr int align16(int x) { return (x + 15) & ~15; }
 // query heads x (hi, lo) fp16 parts (query, sketched query and P are split
 // x = hi + lo so their products keep float32 precision); NT = 2 serves up to
 // 8 query heads per KV head.
-template <int KB, int VB, bool QJL, int NT>
+template <int KB, int VB, bool QJL, int NT, bool WIDE = true>
 struct Cfg {
     // 2-bit values with one n-tile fit in 128 registers: one CTA of 16 warps
-    // per SM; two n-tiles of packed values fit in 168 (12 warps; measured 5%
-    // faster than 8 at 7 query heads per KV head); the rest run 8 warps.
-    static constexpr int kW = (VB == 2 && NT == 1) ? 16 : (NT == 2 && VB != 16) ? 12 : 8;
+    // per SM (WIDE; below 32 chunks per warp at that width, 12 warps -- fewer,
+    // longer ranges -- measured 4% faster); two n-tiles of packed values fit in
+    // 168 (12 warps; measured 5% faster than 8 at 7 query heads per KV head);
+    // the rest run 8 warps.
+    static constexpr int kW = (VB == 2 && NT == 1) ? (WIDE ? 16 : 12) : (NT == 2 && VB != 16) ? 12 : 8;
     static constexpr int kThreads = kW * 32;
     static constexpr int kKBytes = 2 + 16 * KB;
     static constexpr bool kRawV = VB == 16;
@@ -385,10 +387,10 @@ __device__ __forceinline__ void build_value_pair_lut(uint8_t *rows, const float 
 }
 
 
-template <int KB, int VB, bool QJL, int NT>
-__global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT>::kThreads, Cfg<KB, VB, QJL, NT>::kMinBlocks)
+template <int KB, int VB, bool QJL, int NT, bool WIDE>
+__global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, VB, QJL, NT, WIDE>::kMinBlocks)
     attn_mma_kernel(const __grid_constant__ AttnArgs a, const MmaPlan plan) {
-    using C = Cfg<KB, VB, QJL, NT>;
+    using C = Cfg<KB, VB, QJL, NT, WIDE>;
     constexpr int kS = C::kStages;
     uint8_t *smem = tq_attn_dsmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -791,12 +793,12 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT>::kThreads, Cfg<KB, VB, QJ
     }
 }
 
-template <int KB, int VB, bool QJL, int NT>
-int launch_cfg(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
+template <int KB, int VB, bool QJL, int NT, bool WIDE>
+int launch_cfg_w(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
     static_assert(!QJL || NT == 1, "the QJL term covers up to 4 query heads per KV head");
-    using C = Cfg<KB, VB, QJL, NT>;
+    using C = Cfg<KB, VB, QJL, NT, WIDE>;
     static int done[64] = {0};
-    if (set_smem_limit((const void *)attn_mma_kernel<KB, VB, QJL, NT>, C::kSmemTotal, done) != TQ_OK)
+    if (set_smem_limit((const void *)attn_mma_kernel<KB, VB, QJL, NT, WIDE>, C::kSmemTotal, done) != TQ_OK)
         return TQ_ERR_CUDA;
     // a programmatic dependent of the query-prep kernel: its prologue (first copies, tables) overlaps it
     cudaLaunchConfig_t cfg = {};
@@ -809,14 +811,30 @@ int launch_cfg(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, attn_mma_kernel<KB, VB, QJL, NT>, a, plan) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, attn_mma_kernel<KB, VB, QJL, NT, WIDE>, a, plan) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
 }
 
+// Only 2-bit values with one n-tile have a narrow (12-warp) variant.
 template <int KB, int VB, bool QJL, int NT>
-void shape_of(int *ctas_per_sm, int *warps) {
-    *ctas_per_sm = Cfg<KB, VB, QJL, NT>::kMinBlocks;
-    *warps = Cfg<KB, VB, QJL, NT>::kW;
+int launch_cfg(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
+    if constexpr (VB == 2 && NT == 1) {
+        if (!plan.wide) return launch_cfg_w<KB, VB, QJL, NT, false>(a, plan, st);
+    }
+    return launch_cfg_w<KB, VB, QJL, NT, true>(a, plan, st);
+}
+
+template <int KB, int VB, bool QJL, int NT>
+void shape_of(bool wide, int *ctas_per_sm, int *warps) {
+    if constexpr (VB == 2 && NT == 1) {
+        if (!wide) {
+            *ctas_per_sm = Cfg<KB, VB, QJL, NT, false>::kMinBlocks;
+            *warps = Cfg<KB, VB, QJL, NT, false>::kW;
+            return;
+        }
+    }
+    *ctas_per_sm = Cfg<KB, VB, QJL, NT, true>::kMinBlocks;
+    *warps = Cfg<KB, VB, QJL, NT, true>::kW;
 }
 
 }  // namespace

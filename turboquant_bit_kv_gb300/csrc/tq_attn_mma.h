@@ -28,6 +28,7 @@ struct MmaPlan {
     int W;              // workers: min(Ctot, P x warps per CTA)
     int Smax;           // partial slots per (sequence, query head)
     int64_t frag_off;   // float offset of the query fragments in the workspace
+    int wide;           // 2-bit values, one n-tile: 16 warps per SM (else 12)
 };
 
 // kb / vb: key / value bits (vb = 16: raw fp16 values); qjl: two-term

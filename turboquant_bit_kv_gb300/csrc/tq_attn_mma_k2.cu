@@ -5,10 +5,10 @@
 
 namespace tq {
 
-void mma_shape_k2(int vb, bool qjl, int nt, int *ctas_per_sm, int *warps) {
+void mma_shape_k2(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps) {
     *ctas_per_sm = *warps = 0;
 #define TQ_CASE(V, Q, N) \
-    if (vb == V && qjl == Q && nt == N) return shape_of<2, V, Q, N>(ctas_per_sm, warps);
+    if (vb == V && qjl == Q && nt == N) return shape_of<2, V, Q, N>(wide, ctas_per_sm, warps);
     TQ_CASE(2, false, 1) TQ_CASE(3, false, 1) TQ_CASE(4, false, 1) TQ_CASE(16, false, 1)
     TQ_CASE(2, false, 2) TQ_CASE(3, false, 2) TQ_CASE(4, false, 2) TQ_CASE(16, false, 2)
 
