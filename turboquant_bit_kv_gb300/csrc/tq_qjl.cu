@@ -231,18 +231,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
             }
             for (int i = 0; tile < ntiles; ++i, tile += gridDim.x) {
                 const int64_t next = tile + gridDim.x;
+                // U of the next tile is issued as soon as its keys have landed (while the epilogue
+                // still forms R r of tile i), so that the epilogue finds it ready; P of tile i
+                // follows and runs while the epilogue packs signs and starts the next tile
                 if (next < ntiles) {
                     wait(kBarXFree, (uint32_t)i & 1u);   // U of tile i has read X
                     load_x(next);
-                }
-                wait(kBarA2, (uint32_t)i & 1u);          // R r of tile i staged
-                tc_fence_after();
-                const uint32_t p_t = tmem + 256u + 128u * (uint32_t)(i & 1);   // P double-buffered
-                tc_mma_tile<TQ_F16>(p_t, a2_s, sh_s, false);
-                tc_mma_tile<TQ_F16>(p_t, a2_s, sl_s, true);
-                tc_mma_tile<TQ_F16>(p_t, a2_s + kQTile, sh_s, true);
-                tc_commit(bars + 8 * kBarP);
-                if (next < ntiles) {
                     const int n1 = i + 1, st = n1 & 1;
                     wait(kBarFull, (uint32_t)n1 & 1u);
                     if (n1 >= 2) wait(kBarUFree + st, (uint32_t)((n1 >> 1) - 1) & 1u);
@@ -251,6 +245,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     tc_commit(bars + 8 * (kBarURdy + st));
                     tc_commit(bars + 8 * kBarXFree);
                 }
+                wait(kBarA2, (uint32_t)i & 1u);          // R r of tile i staged
+                tc_fence_after();
+                const uint32_t p_t = tmem + 256u + 128u * (uint32_t)(i & 1);   // P double-buffered
+                tc_mma_tile<TQ_F16>(p_t, a2_s, sh_s, false);
+                tc_mma_tile<TQ_F16>(p_t, a2_s, sl_s, true);
+                tc_mma_tile<TQ_F16>(p_t, a2_s + kQTile, sh_s, true);
+                tc_commit(bars + 8 * kBarP);
             }
         }
     } else {
