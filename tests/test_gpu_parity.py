@@ -485,6 +485,8 @@ def test_qjl_encode_matches_oracle(env):
     (4, torch.float16, 128, None, 0),         # exactly one tile
     (3, torch.float16, 1, None, 0),           # a single key
     (4, torch.bfloat16, 40000, None, 0),      # several tiles per CTA (the producer / epilogue pipeline)
+    (3, torch.bfloat16, 40001, None, 0),      # back-to-back 3-bit blocks: 16-byte staging, ragged last group
+    (2, torch.float16, 5000, None, 2),        # padded 2-bit slots: 16-bit staging, pair lookups
     (3, torch.bfloat16, 1000, 192, 4),        # strided key rows, padded block slots (2-byte offsets)
     (2, torch.float32, 300, None, 2),         # float32 keys: CUDA-core kernel
 ])

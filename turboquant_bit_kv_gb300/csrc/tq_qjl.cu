@@ -45,6 +45,7 @@ constexpr unsigned kQFull = 0xffffffffu;
 struct QjlTcArgs {
     const uint8_t *blocks;
     int64_t block_stride;   // bytes
+    int dense;              // blocks back to back (stride = block bytes) from a 16-byte aligned start
     int64_t n_vec;
     const float *S;         // [128][128] row-major
     uint8_t *bits;          // [n_vec][16]
@@ -57,17 +58,24 @@ template <int BITS>
 struct QjlSmem {
     static constexpr int BB = 2 + 16 * BITS;
     static constexpr int kHW = BB / 2;                          // 16-bit words per block
-    static constexpr int kPitch = BB + 2;                       // staged row: 2 pad bytes, norm, codes (4-aligned)
+    static constexpr int kPitch = BB;                           // staged rows back to back, as in memory
     static constexpr int kPre = (32 * kHW + 32 * kQSlices - 1) / (32 * kQSlices);   // block words a thread prefetches
+    static constexpr int kVec = 2 * BB;                         // 16-byte pieces of a row group's 32 blocks
+    static constexpr int kPreV = (kVec + 32 * kQSlices - 1) / (32 * kQSlices);       // pieces a thread prefetches
+    // centroid lookups: 2/3-bit codes by pairs (float2 of both centroids, 2^(2 BITS) entries), 4-bit
+    // codes one at a time (16 floats); each entry replicated 16 times (8-byte entries: per half warp)
+    // or 32 times (4-byte entries), so that lanes never collide on a bank
+    static constexpr bool kPairs = BITS < 4;
+    static constexpr int kTabBytes = kPairs ? (1 << (2 * BITS)) * 128 : 16 * 32 * 4;
     static constexpr int kHD = 0;                               // H D (key dtype)
     static constexpr int kSh = kHD + kQTile;                    // S' hi (fp16)
     static constexpr int kSl = kSh + kQTile;                    // S' lo (fp16)
     static constexpr int kX = kSl + kQTile;                     // key tile (TMA)
     static constexpr int kA2 = kX + kQTile;                     // R r hi tile, then lo tile
     static constexpr int kBlk = kA2 + 2 * kQTile;               // the tile's blocks
-    static constexpr int kCtab = kBlk + ((kQRows * kPitch + 15) & ~15);   // centroids, lane-replicated
-    static constexpr int kPart = kCtab + 16 * 32 * 4;           // per-row partial sums of squares [slice][128]
-    static constexpr int kBars = kPart + kQSlices * kQRows * 4; // 8 mbarriers
+    static constexpr int kCtab = kBlk + ((kQRows * kPitch + 16 + 15) & ~15);   // (+ slack read by the last row)
+    static constexpr int kPart = kCtab + kTabBytes;             // per-row partial sums of squares [2][slice][128]
+    static constexpr int kBars = kPart + 2 * kQSlices * kQRows * 4;   // 8 mbarriers
     static constexpr int kSlot = kBars + 8 * 8;                 // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;            // + alignment slack of the base
 };
@@ -83,6 +91,25 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ float2 lds_f2_q(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
+// N 32-bit words starting at byte offset off (even) of a shared buffer: aligned loads, and a funnel
+// shift by 16 bits when off is 2 mod 4
+template <int N>
+__device__ __forceinline__ void words_at(const uint8_t *buf, int off, uint32_t *out) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(buf + (off & ~3));
+    const uint32_t sh = (uint32_t)(off & 2) * 8u;
+    uint32_t v[N + 1];
+#pragma unroll
+    for (int i = 0; i <= N; ++i) v[i] = w[i];
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -175,8 +202,26 @@ __global__ void __launch_bounds__(kQThreads, 1)
         *reinterpret_cast<uint2 *>(smem + Q::kSh + off) = make_uint2(h0, h1);
         *reinterpret_cast<uint2 *>(smem + Q::kSl + off) = make_uint2(l0, l1);
     }
-    float *ctab = reinterpret_cast<float *>(smem + Q::kCtab);
-    for (int q = threadIdx.x; q < 16 * 32; q += kQThreads) ctab[q] = a.c[q >> 5];
+    if constexpr (Q::kPairs) {
+        // entry p (128 bytes: 16 copies): the centroids of codes (p_lo, p_hi) of two consecutive
+        // elements; 3-bit: p = (low-plane bits of both) | (high-plane bits of both) << 4
+        float2 *ptab = reinterpret_cast<float2 *>(smem + Q::kCtab);
+        for (int q = threadIdx.x; q < (1 << (2 * BITS)) * 16; q += kQThreads) {
+            const int p = q >> 4;
+            int c0, c1;
+            if constexpr (BITS == 2) {
+                c0 = p & 3;
+                c1 = p >> 2;
+            } else {
+                c0 = (p & 3) | ((p >> 2) & 4);
+                c1 = ((p >> 2) & 3) | ((p >> 3) & 4);
+            }
+            ptab[q] = make_float2(a.c[c0], a.c[c1]);
+        }
+    } else {
+        float *ctab = reinterpret_cast<float *>(smem + Q::kCtab);
+        for (int q = threadIdx.x; q < 16 * 32; q += kQThreads) ctab[q] = a.c[q >> 5];
+    }
     if (threadIdx.x == 0) {
         tc_mbar_init(bars + 8 * kBarFull, 1);
         tc_mbar_init(bars + 8 * kBarXFree, 1);
@@ -264,25 +309,47 @@ __global__ void __launch_bounds__(kQThreads, 1)
         uint8_t *blk = smem + Q::kBlk;
         const uint32_t ctab_s = base_s + Q::kCtab + 4u * lane;
         const uint32_t a2_row = base_s + Q::kA2 + (c0 >> 6) * 16384 + r * 128;
-        // the row group's 32 blocks, as 16-bit words, loaded one tile ahead
+        // the row group's 32 blocks, loaded one tile ahead: sixteen bytes at a time when the blocks are
+        // back to back (a group of 32 starts 32 * BB bytes apart, a multiple of 16) and the group is
+        // whole, else as 16-bit words; staged back to back, as in memory
         uint32_t pre[Q::kPre];
+        uint4 prev[Q::kPreV];
+        bool pvec = false;
         auto prefetch = [&](int64_t tile) {
             const int64_t v0 = tile * kQRows + 32 * grp;
+            pvec = a.dense != 0 && tile < ntiles && v0 + 32 <= a.n_vec;
+            if (pvec) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.blocks + v0 * Q::BB);
 #pragma unroll
-            for (int k = 0; k < Q::kPre; ++k) {
-                const int q = tidg + 32 * kQSlices * k, row = q / Q::kHW, h = q - row * Q::kHW;
-                pre[k] = (q < 32 * Q::kHW && tile < ntiles && v0 + row < a.n_vec)
-                             ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(
-                                   a.blocks + (v0 + row) * a.block_stride + 2 * h))
-                             : 0u;
+                for (int k = 0; k < Q::kPreV; ++k) {
+                    const int q = tidg + 32 * kQSlices * k;
+                    if (q < Q::kVec) prev[k] = __ldg(src + q);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < Q::kPre; ++k) {
+                    const int q = tidg + 32 * kQSlices * k, row = q / Q::kHW, h = q - row * Q::kHW;
+                    pre[k] = (q < 32 * Q::kHW && tile < ntiles && v0 + row < a.n_vec)
+                                 ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(
+                                       a.blocks + (v0 + row) * a.block_stride + 2 * h))
+                                 : 0u;
+                }
             }
         };
         auto stage = [&]() {
+            uint8_t *g = blk + 32 * grp * Q::kPitch;
+            if (pvec) {
 #pragma unroll
-            for (int k = 0; k < Q::kPre; ++k) {
-                const int q = tidg + 32 * kQSlices * k, row = q / Q::kHW, h = q - row * Q::kHW;
-                if (q < 32 * Q::kHW)
-                    *reinterpret_cast<uint16_t *>(blk + (32 * grp + row) * Q::kPitch + 2 + 2 * h) = (uint16_t)pre[k];
+                for (int k = 0; k < Q::kPreV; ++k) {
+                    const int q = tidg + 32 * kQSlices * k;
+                    if (q < Q::kVec) *reinterpret_cast<uint4 *>(g + 16 * q) = prev[k];
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < Q::kPre; ++k) {
+                    const int q = tidg + 32 * kQSlices * k;
+                    if (q < 32 * Q::kHW) *reinterpret_cast<uint16_t *>(g + 2 * q) = (uint16_t)pre[k];
+                }
             }
         };
         auto grp_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(grp_bar), "n"(32 * kQSlices) : "memory"); };
@@ -291,6 +358,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         auto wait = [&](int b, uint32_t parity) {
             if (ok) ok = tc_mbar_wait(bars + 8 * b, parity);
         };
+        // signs of P = S r for tile j (this slice): bit k of the row's 128 = [(S r)_k >= 0]; run one
+        // tile late, so that the tensor cores compute P of tile j + 1 meanwhile
         // signs of P = S r for tile j (this slice): bit k of the row's 128 = [(S r)_k >= 0]; run one
         // tile late, so that the tensor cores compute P of tile j + 1 meanwhile
         auto signs_out = [&](int j, int64_t pv0, int pnv, unsigned short prn) {
@@ -314,9 +383,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 if (sl == 0) a.rn[pv0 + r] = prn;
             }
         };
+        // fp16 ||r|| of tile j from the slices' partial sums (double-buffered by tile parity: the
+        // sums of tile j are complete at the group barrier that opens tile j + 1)
+        auto norm_of = [&](int j, float jscale) -> unsigned short {
+            const float *pp = part + (j & 1) * (kQSlices * kQRows);
+            float ss = 0.f;
+#pragma unroll
+            for (int q = 0; q < kQSlices; ++q) ss += pp[q * kQRows + r];
+            return __half_as_ushort(__float2half_rn(sqrtf(ss) * (1.f / jscale)));
+        };
         int64_t pv0 = 0;
         int pnv = 0;
-        unsigned short prn = 0;
+        float pscale = 1.f;
         int i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
             const int st = i & 1;
@@ -324,7 +402,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const int nv = (int)min64(kQRows, a.n_vec - v0);
             stage();
             prefetch(tile + gridDim.x);
-            grp_sync();   // the group's blocks are staged
+            grp_sync();   // the group's blocks are staged, the previous tile's partial sums complete
+            const unsigned short prn = i >= 1 ? norm_of(i - 1, pscale) : (unsigned short)0;
 
             // ---- U of this row slice
             wait(kBarURdy + st, (uint32_t)(i >> 1) & 1u);
@@ -339,8 +418,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             if (lane == 0) tc_mbar_arrive(bars + 8 * (kBarUFree + st));
 
             // ---- R r = u / sqrt(128) - n16 c[code], scaled by 2^(7 - E) with n16 in [2^(E-1), 2^E)
-            const uint8_t *rb = blk + r * Q::kPitch;
-            const float nf = r < nv ? __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(rb + 2))) : 0.f;
+            const int rb = r * Q::kPitch;   // the row's block in the staging buffer (2-byte aligned)
+            const float nf = r < nv ? __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(blk + rb))) : 0.f;
             float scale = 1.f;   // inf / NaN norms: left unscaled
             if (nf == 0.f) {
                 scale = 1073741824.f;   // 2^30
@@ -349,33 +428,40 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 scale = __uint_as_float((uint32_t)(127 + 7 - E) << 23);
             }
             const float inv_rs = 0.08838834764831845f * scale, nn = -(nf * scale);
-            constexpr int NW = BITS == 4 ? kQNC / 8 : BITS == 2 ? kQNC / 16 : kQNC / 16 + kQNC / 32;
-            uint32_t cw[NW];
-            if constexpr (BITS == 4) {
-#pragma unroll
-                for (int q = 0; q < NW; ++q) cw[q] = *reinterpret_cast<const uint32_t *>(rb + 4 + c0 / 2 + 4 * q);
-            } else {
-#pragma unroll
-                for (int q = 0; q < kQNC / 16; ++q) cw[q] = *reinterpret_cast<const uint32_t *>(rb + 4 + c0 / 4 + 4 * q);
-                if constexpr (BITS == 3) {
-#pragma unroll
-                    for (int q = 0; q < kQNC / 32; ++q)
-                        cw[kQNC / 16 + q] = *reinterpret_cast<const uint32_t *>(rb + 36 + c0 / 8 + 4 * q);
-                }
-            }
             float2 q2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int e = 0; e < kQNC; e += 2) {
-                const float cv0 = lds_f32(ctab_s + code_at<BITS, kQNC>(cw, e) * 128u);
-                const float cv1 = lds_f32(ctab_s + code_at<BITS, kQNC>(cw, e + 1) * 128u);
+            auto element_pair = [&](int e, float cv0, float cv1) {
                 const float2 u2 = __fmul2_rn(make_float2(x[e >> 5][e & 31], x[e >> 5][(e & 31) + 1]),
                                              make_float2(inv_rs, inv_rs));
                 const float2 r2 = __ffma2_rn(make_float2(cv0, cv1), make_float2(nn, nn), u2);
                 x[e >> 5][e & 31] = r2.x;
                 x[e >> 5][(e & 31) + 1] = r2.y;
                 q2 = __ffma2_rn(r2, r2, q2);
+            };
+            if constexpr (Q::kPairs) {
+                // one lookup per two elements: both low-plane code pairs sit in 4 adjacent bits, both
+                // high-plane bits (3-bit codes) in 2
+                uint32_t lw[kQNC / 16], hw[1] = {0u};
+                words_at<kQNC / 16>(blk, rb + 2 + c0 / 4, lw);
+                if constexpr (BITS == 3) words_at<1>(blk, rb + 34 + c0 / 8, hw);
+                const uint32_t ptab_s = base_s + Q::kCtab + 8u * (uint32_t)(lane & 15);
+#pragma unroll
+                for (int e = 0; e < kQNC; e += 2) {
+                    uint32_t pidx = (lw[e >> 4] >> (2 * (e & 15))) & 15u;
+                    if constexpr (BITS == 3) pidx |= ((hw[0] >> (e & 31)) & 3u) << 4;
+                    const float2 cv = lds_f2_q(ptab_s + pidx * 128u);
+                    element_pair(e, cv.x, cv.y);
+                }
+            } else {
+                uint32_t cw[kQNC / 8];
+                words_at<kQNC / 8>(blk, rb + 2 + c0 / 2, cw);
+#pragma unroll
+                for (int e = 0; e < kQNC; e += 2) {
+                    const float cv0 = lds_f32(ctab_s + code_at<BITS, kQNC>(cw, e) * 128u);
+                    const float cv1 = lds_f32(ctab_s + code_at<BITS, kQNC>(cw, e + 1) * 128u);
+                    element_pair(e, cv0, cv1);
+                }
             }
-            part[sl * kQRows + r] = q2.x + q2.y;
+            part[(i & 1) * (kQSlices * kQRows) + sl * kQRows + r] = q2.x + q2.y;
             // the previous tile's P is complete: its MMAs have read the R r tiles rewritten below
             if (i >= 1) wait(kBarP, (uint32_t)(i - 1) & 1u);
             tc_fence_after();
@@ -396,18 +482,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bars + 8 * kBarA2);
-            grp_sync();   // every slice's sum of squares
-            float ss = 0.f;
-#pragma unroll
-            for (int q = 0; q < kQSlices; ++q) ss += part[q * kQRows + r];
-            const unsigned short rn16 = __half_as_ushort(__float2half_rn(sqrtf(ss) * (1.f / scale)));
-
             if (i >= 1) signs_out(i - 1, pv0, pnv, prn);
             pv0 = v0;
             pnv = nv;
-            prn = rn16;
+            pscale = scale;
         }
         if (i >= 1) {
+            grp_sync();   // the last tile's partial sums
+            const unsigned short prn = norm_of(i - 1, pscale);
             wait(kBarP, (uint32_t)(i - 1) & 1u);
             tc_fence_after();
             signs_out(i - 1, pv0, pnv, prn);
@@ -444,6 +526,7 @@ int qjl_encode_tc(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_by
     QjlTcArgs a;
     a.blocks = blocks;
     a.block_stride = block_stride;
+    a.dense = block_stride == 2 + 16 * bits && (reinterpret_cast<uintptr_t>(blocks) & 15) == 0 ? 1 : 0;
     a.n_vec = n_vec;
     a.S = S;
     a.bits = qjl_bits;
