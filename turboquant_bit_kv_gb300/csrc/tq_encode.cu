@@ -1079,7 +1079,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const float cs = zero_row ? 0.f : a.grid / sc;   // a zero row: y = 0, code L/2
             const float2 cs2 = make_float2(cs, cs);
             uint16_t *b16 = reinterpret_cast<uint16_t *>(blk + 2);
-            constexpr int PER = BITS == 4 ? 4 : 8;   // codes per 16-bit word of the (low) plane
+            // codes per 16-bit word of the (low) plane; 3-bit codes are first gathered as nibbles, eight
+            // to a word, and the word is then split into its 2-bit and 1-bit planes
+            constexpr int PER = BITS == 4 ? 4 : 8;
+            constexpr int B = BITS == 3 ? 4 : BITS;   // accumulation width of a code
             // 16 columns at a time, re-read from tensor memory (the next chunk's load in flight)
             float ub[2][16];
             tc_ld16(taddr, ub[0]);
@@ -1100,20 +1103,26 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         const float2 tt = __fadd2_rn(yp, off2);
                         const float2 ex = lds_f2(tab_s + (__float_as_uint(tt.x) & 0x3F8u));
                         const float2 ey = lds_f2(tab_s + (__float_as_uint(tt.y) & 0x3F8u));
-                        if constexpr (BITS == 3) {
-                            const uint32_t c0 = __float_as_uint(ex.y) - set_ge(yp.x, ex.x);
-                            const uint32_t c1 = __float_as_uint(ey.y) - set_ge(yp.y, ey.x);
-                            w |= ((c0 & 3u) << (2 * e)) | ((c1 & 3u) << (2 * e + 2));
-                            hi |= ((c0 >> 2) << k) | ((c1 >> 2) << (k + 1));
-                        } else {
-                            constexpr int B = BITS;
-                            w += __float_as_uint(ex.y) << (B * e);
-                            w -= set_ge(yp.x, ex.x) << (B * e);
-                            w += __float_as_uint(ey.y) << (B * e + B);
-                            w -= set_ge(yp.y, ey.x) << (B * e + B);
-                        }
+                        w += __float_as_uint(ex.y) << (B * e);
+                        w -= set_ge(yp.x, ex.x) << (B * e);
+                        w += __float_as_uint(ey.y) << (B * e + B);
+                        w -= set_ge(yp.y, ey.x) << (B * e + B);
                     }
-                    b16[(16 / PER) * cq + g] = (uint16_t)w;
+                    if constexpr (BITS == 3) {
+                        // low plane: bits 0-1 of nibble e to bits 2e, 2e + 1; high plane: bit 2 of nibble e to bit e
+                        uint32_t lo = w & 0x33333333u;
+                        lo = (lo | (lo >> 2)) & 0x0F0F0F0Fu;
+                        lo = (lo | (lo >> 4)) & 0x00FF00FFu;
+                        lo = (lo | (lo >> 8)) & 0x0000FFFFu;
+                        uint32_t hb = (w >> 2) & 0x11111111u;
+                        hb = (hb | (hb >> 3)) & 0x03030303u;
+                        hb = (hb | (hb >> 6)) & 0x000F000Fu;
+                        hb = (hb | (hb >> 12)) & 0x000000FFu;
+                        b16[2 * cq + g] = (uint16_t)lo;
+                        hi |= hb << (8 * g);
+                    } else {
+                        b16[(16 / PER) * cq + g] = (uint16_t)w;
+                    }
                 }
                 if constexpr (BITS == 3) reinterpret_cast<uint16_t *>(blk + 34)[cq] = (uint16_t)hi;
                 if (c < 3) tc_wait_ld16(ub[(c + 1) & 1]);
