@@ -237,21 +237,30 @@ def test_decode_matches_oracle(env, bits, out_dtype):
         assert np.all((got >= lo) & (got <= hi))
 
 
-def test_decode_slot_stride(env):
+@pytest.mark.parametrize("bits,slot,offset,n", [
+    (4, 132, 66, 80),      # V halves of 132-byte storage slots (a 2-byte aligned start)
+    (4, 132, 0, 3001),     # K halves: many tiles per warp, a ragged last tile
+    (3, 144, 6, 1000),     # the longest stride staged as one byte span per tile
+    (2, 70, 2, 777),       # a short stride: tiles that start at every 2-byte offset in 16
+    (2, 146, 10, 500),     # just above the span limit: per-block word staging
+    (3, 1024, 512, 300),   # a long stride
+])
+def test_decode_slot_stride(env, bits, slot, offset, n):
     tq = env["tq"]
     dev = env["dev"]
-    c, _, b32 = env["books"][4]
-    x = workloads.storage_kv(L=1, T=40, hidden=256, seed=1)["kv"][1, 0].reshape(-1, D).double().numpy()
+    c, _, b32 = env["books"][bits]
+    x = workloads.qwen_outlier(B=1, Hq=7, Hkv=1, T=n, seed=11 + bits)["k"].reshape(-1, D).double().numpy()
     idx, n16, _ = codec.encode(x, env["s"], b32)
-    slot = 132
-    buf = np.zeros((x.shape[0], slot), np.uint8)
-    buf[:, 66:] = codec.pack_block(idx, n16, 4)
-    out = torch.empty((x.shape[0], D), dtype=torch.float32, device=dev)
-    tq.tq_decode_kv(torch.from_numpy(buf.reshape(-1)).to(dev), x.shape[0], env["cbs"][4], env["signs"], out,
-                    block_stride_bytes=slot, block_offset=66)
+    bb = 2 + 16 * bits
+    buf = np.full((n, slot), 0xA5, np.uint8)   # bytes outside the blocks hold a pattern, not zeros
+    buf[:, offset:offset + bb] = codec.pack_block(idx, n16, bits)
+    out = torch.empty((n, D), dtype=torch.float32, device=dev)
+    tq.tq_decode_kv(torch.from_numpy(buf.reshape(-1)).to(dev), n, env["cbs"][bits], env["signs"], out,
+                    block_stride_bytes=slot, block_offset=offset)
     torch.cuda.synchronize()
     ref = codec.decode(idx, n16, c, env["s"])
-    assert np.max(np.abs(out.double().cpu().numpy() - ref)) < 1e-5
+    nrm = codec.norm_value(n16)[:, None]
+    assert np.max(np.abs(out.double().cpu().numpy() - ref) / np.maximum(nrm, 1e-30)) < 1e-6
 
 
 # ------------------------------------------------------------------ attention

@@ -28,13 +28,14 @@ constexpr int kDecWarps = 8;
 constexpr int kDecThreads = 32 * kDecWarps;
 constexpr int kDecRows = 16;               // vectors per warp tile
 constexpr int kStridedPitch = 72;          // staged block of a strided input: 18 words
+constexpr int kSpanMaxStride = 144;        // strides up to this stage the 16 blocks' whole byte span
 
 template <int BITS>
 struct DecGeo {
     static constexpr int BB = 2 + 16 * BITS;
     static constexpr int kLutEntries = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
     static constexpr int kLutBytes = kLutEntries * 256;
-    static constexpr int kStage = kDecRows * kStridedPitch;   // >= 16 * BB for every width
+    static constexpr int kStage = kDecRows * kSpanMaxStride + 32;   // >= 16 * 72 and >= 16 * BB
     static constexpr int kSmem = kLutBytes + (64 + 128) * 4 + kDecWarps * 2 * kStage;
     static_assert(kStage >= kDecRows * BB, "stage");
 };
@@ -46,6 +47,7 @@ struct DecArgs {
     uint8_t *out;
     int64_t out_stride;   // bytes
     int contiguous;       // block_stride == block bytes and 16-byte aligned base
+    int span;             // otherwise, block_stride <= kSpanMaxStride: stage the tile's whole byte span
     float c[16];
     uint32_t signs[4];
 };
@@ -106,9 +108,14 @@ __device__ __forceinline__ void stg_cs(uint8_t *p, uint4 v) {
 }
 
 // Stage the warp's blocks [v0, v0 + nv) into `st`.  Contiguous input: one
-// copy of nv * BB bytes (block r at r * BB).  Strided input: block r's
-// enclosing 32-bit words at r * 72 (block at r * 72 + (address & 3)); the
-// last word copies only the bytes that belong to the block.
+// copy of nv * BB bytes (block r at r * BB).  Short strides (e.g. the halves
+// of 132-byte storage slots): the byte span from the 16-byte boundary at or
+// below block v0 to the end of block v0 + nv - 1, in 16-byte copies (block r
+// at (address of block v0 & 15) + r * stride; the first copy may start up to
+// 15 bytes before block v0, inside the same aligned 16 bytes, and the last
+// copies only bytes of the span).  Other strides: block r's enclosing 32-bit
+// words at r * 72 (block at r * 72 + (address & 3)); the last word copies
+// only the bytes that belong to the block.
 template <int BITS>
 __device__ __forceinline__ void stage_tile(const DecArgs &a, uint32_t st, int64_t v0, int nv, int lane) {
     constexpr int BB = DecGeo<BITS>::BB;
@@ -117,6 +124,12 @@ __device__ __forceinline__ void stage_tile(const DecArgs &a, uint32_t st, int64_
         const int nbytes = nv * BB;
         for (int q = lane; q < (nbytes + 15) >> 4; q += 32)
             cp_async_zfill(st + 16 * q, src + 16 * q, 16, min(16, nbytes - 16 * q));
+    } else if (a.span) {
+        const uintptr_t first = reinterpret_cast<uintptr_t>(a.blocks + v0 * a.block_stride);
+        const uintptr_t start = first & ~(uintptr_t)15;
+        const int nbytes = (int)(first - start) + (nv - 1) * (int)a.block_stride + BB;
+        for (int q = lane; q < (nbytes + 15) >> 4; q += 32)
+            cp_async_zfill(st + 16 * q, reinterpret_cast<const void *>(start + 16 * q), 16, min(16, nbytes - 16 * q));
     } else {
         for (int q = lane; q < nv * 18; q += 32) {
             const int r = q / 18, w = q - 18 * r;
@@ -174,6 +187,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_pair_kernel(const __gri
         const int64_t row = v0 + pv;
         uint32_t blk_s = stage_s + (it & 1) * Geo::kStage;
         if (a.contiguous) blk_s += pv * BB;
+        else if (a.span)
+            blk_s += (uint32_t)(reinterpret_cast<uintptr_t>(a.blocks + v0 * a.block_stride) & 15) +
+                     (uint32_t)pv * (uint32_t)a.block_stride;
         else blk_s += pv * kStridedPitch + (row < a.n_vec ? (uint32_t)(reinterpret_cast<uintptr_t>(a.blocks + row * a.block_stride) & 3) : 0u);
 
         // ---- centroids of this thread's 64 elements, as pairs p[c'][k] = (e(c', k), e(c' + 4, k))
@@ -308,6 +324,7 @@ extern "C" int tq_decode_kv(const uint8_t *blocks, int64_t block_stride_bytes, i
     a.out = static_cast<uint8_t *>(out);
     a.out_stride = out_stride_elems * es;
     a.contiguous = (block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
+    a.span = (!a.contiguous && block_stride_bytes <= kSpanMaxStride) ? 1 : 0;
     for (int i = 0; i < 16; ++i) a.c[i] = i < cb->levels ? cb->centroids[i] : 0.f;
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
     cudaStream_t st = (cudaStream_t)stream;

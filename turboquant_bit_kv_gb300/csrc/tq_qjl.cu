@@ -63,10 +63,10 @@ struct QjlSmem {
     static constexpr int kVec = 2 * BB;                         // 16-byte pieces of a row group's 32 blocks
     static constexpr int kPreV = (kVec + 32 * kQSlices - 1) / (32 * kQSlices);       // pieces a thread prefetches
     // centroid lookups: 2/3-bit codes by pairs (float2 of both centroids, 2^(2 BITS) entries), 4-bit
-    // codes one at a time (16 floats); each entry replicated 16 times (8-byte entries: per half warp)
-    // or 32 times (4-byte entries), so that lanes never collide on a bank
+    // codes one at a time (16 floats); each entry replicated once per lane, so that lanes never
+    // collide on a bank
     static constexpr bool kPairs = BITS < 4;
-    static constexpr int kTabBytes = kPairs ? (1 << (2 * BITS)) * 128 : 16 * 32 * 4;
+    static constexpr int kTabBytes = kPairs ? (1 << (2 * BITS)) * 256 : 16 * 32 * 4;
     static constexpr int kHD = 0;                               // H D (key dtype)
     static constexpr int kSh = kHD + kQTile;                    // S' hi (fp16)
     static constexpr int kSl = kSh + kQTile;                    // S' lo (fp16)
@@ -78,6 +78,7 @@ struct QjlSmem {
     static constexpr int kBars = kPart + 2 * kQSlices * kQRows * 4;   // 8 mbarriers
     static constexpr int kSlot = kBars + 8 * 8;                 // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;            // + alignment slack of the base
+    static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
 // mbarriers: key tile landed, key tile consumed, U ready [2], U released [2], R r staged, P ready
@@ -203,11 +204,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
         *reinterpret_cast<uint2 *>(smem + Q::kSl + off) = make_uint2(l0, l1);
     }
     if constexpr (Q::kPairs) {
-        // entry p (128 bytes: 16 copies): the centroids of codes (p_lo, p_hi) of two consecutive
+        // entry p (256 bytes: 32 copies): the centroids of codes (p_lo, p_hi) of two consecutive
         // elements; 3-bit: p = (low-plane bits of both) | (high-plane bits of both) << 4
         float2 *ptab = reinterpret_cast<float2 *>(smem + Q::kCtab);
-        for (int q = threadIdx.x; q < (1 << (2 * BITS)) * 16; q += kQThreads) {
-            const int p = q >> 4;
+        for (int q = threadIdx.x; q < (1 << (2 * BITS)) * 32; q += kQThreads) {
+            const int p = q >> 5;
             int c0, c1;
             if constexpr (BITS == 2) {
                 c0 = p & 3;
@@ -443,12 +444,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 uint32_t lw[kQNC / 16], hw[1] = {0u};
                 words_at<kQNC / 16>(blk, rb + 2 + c0 / 4, lw);
                 if constexpr (BITS == 3) words_at<1>(blk, rb + 34 + c0 / 8, hw);
-                const uint32_t ptab_s = base_s + Q::kCtab + 8u * (uint32_t)(lane & 15);
+                const uint32_t ptab_s = base_s + Q::kCtab + 8u * (uint32_t)lane;
 #pragma unroll
                 for (int e = 0; e < kQNC; e += 2) {
                     uint32_t pidx = (lw[e >> 4] >> (2 * (e & 15))) & 15u;
                     if constexpr (BITS == 3) pidx |= ((hw[0] >> (e & 31)) & 3u) << 4;
-                    const float2 cv = lds_f2_q(ptab_s + pidx * 128u);
+                    const float2 cv = lds_f2_q(ptab_s + pidx * 256u);
                     element_pair(e, cv.x, cv.y);
                 }
             } else {
