@@ -215,6 +215,40 @@ def _pinned(t):
     return t.cpu().pin_memory()
 
 
+class _CopyPipe:
+    """Host-to-device copies of an end-to-end step, issued in chunks on a
+    side stream; the bench stream waits for a chunk right before the call that
+    reads it, so the kernels run while the remaining bytes cross the host link
+    (the link's bandwidth bounds the step; more copy streams do not add to it)."""
+
+    def __init__(self, stream):
+        self.main = stream
+        self.side = torch.cuda.Stream(device=stream.device)
+
+    def begin(self):
+        # the previous step's kernels have read the device buffers before they are overwritten
+        ev = torch.cuda.Event()
+        ev.record(self.main)
+        self.side.wait_event(ev)
+
+    def copy(self, dst, src):
+        with torch.cuda.stream(self.side):
+            dst.copy_(src, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(self.side)
+        return ev
+
+    def wait(self, ev):
+        self.main.wait_event(ev)
+
+
+def _chunks(n, parts, align=1024):
+    """`parts` row ranges covering [0, n), boundaries on multiples of `align` rows."""
+    size = -(-n // parts)
+    size = -(-size // align) * align
+    return [slice(a, min(n, a + size)) for a in range(0, n, size)]
+
+
 def plan_llama(tq, wl, dev, stream, seed, batch):
     from turboquant_bit_kv_gb300 import workloads
     W = WORKLOADS["llama3_8b_decode"]
@@ -241,16 +275,24 @@ def plan_llama(tq, wl, dev, stream, seed, batch):
            Op("attention", "attention", attn, nb["attn"], 3)]
 
     def e2e():
-        hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
+        hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)
         hout = torch.empty_like(out, device="cpu").pin_memory()
-        dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+        dk, dv, dq = (torch.empty_like(t, device=dev) for t in (hk, hv, hq))
+        kb2, vb2 = kb.view(nvec, -1), vb.view(nvec, -1)
+        pipe, parts = _CopyPipe(stream), _chunks(nvec, 4)
 
         def step():
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            dq.copy_(hq, non_blocking=True)
-            tq.tq_encode_kv(dk.view(-1, 128), kcb, signs, kb, stream=stream)
-            tq.tq_encode_kv(dv.view(-1, 128), vcb, signs, vb, stream=stream)
+            pipe.begin()
+            eq = pipe.copy(dq, hq)
+            ek = [pipe.copy(dk[r], hk[r]) for r in parts]
+            ev = [pipe.copy(dv[r], hv[r]) for r in parts]
+            for r, e in zip(parts, ek):
+                pipe.wait(e)
+                tq.tq_encode_kv(dk[r], kcb, signs, kb2[r], stream=stream)
+            for r, e in zip(parts, ev):
+                pipe.wait(e)
+                tq.tq_encode_kv(dv[r], vcb, signs, vb2[r], stream=stream)
+            pipe.wait(eq)
             attn(dq)
             hout.copy_(out, non_blocking=True)
         return step, k.numel() * 2 + v.numel() * 2 + q.numel() * 2, out.numel() * 4
@@ -342,11 +384,19 @@ def plan_qwen(tq, wl, dev, stream, seed, batch):
         dk, dv = torch.empty_like(pre["k"]), torch.empty_like(pre["v"])
         dnk, dnv, dq = torch.empty_like(new["k"]), torch.empty_like(new["v"]), torch.empty_like(q)
 
+        pipe, parts = _CopyPipe(stream), _chunks(n_pre, 4)
+
         def step():
-            for d, h in ((dk, hk), (dv, hv), (dnk, hnk), (dnv, hnv), (dq, hq)):
-                d.copy_(h, non_blocking=True)
-            enc(dk, "k", dst_pre)()
-            enc(dv, "v", dst_pre)()
+            pipe.begin()
+            small = [pipe.copy(d, h) for d, h in ((dnk, hnk), (dnv, hnv), (dq, hq))]
+            ek = [pipe.copy(dk[r], hk[r]) for r in parts]
+            ev = [pipe.copy(dv[r], hv[r]) for r in parts]
+            for n, d, evs in (("k", dk, ek), ("v", dv, ev)):
+                for r, e in zip(parts, evs):
+                    pipe.wait(e)
+                    enc(d[r], n, dst_pre[r])()
+            for e in small:
+                pipe.wait(e)
             enc(dnk, "k", dst_new)()
             enc(dnv, "v", dst_new)()
             attn(dq)
@@ -390,15 +440,23 @@ def plan_qjl(tq, wl, dev, stream, seed, batch):
            Op("attention", "attention", attn, n * (50 + 16 + 2 + 256) + B * Hq * 128 * (2 + 4) + 128 * 128 * 4, 3)]
 
     def e2e():
-        hk, hv, hq = _pinned(k), _pinned(v), _pinned(q)
+        hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v), _pinned(q)
         hout = torch.empty_like(out, device="cpu").pin_memory()
-        dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+        dk, dv, dq = (torch.empty_like(t, device=dev) for t in (hk, hv, hq))
+        kb2, bits2, rn2 = kb.view(n, 50), bits.view(n, 16), rn.view(n)
+        pipe, parts = _CopyPipe(stream), _chunks(n, 4)
 
         def step():
-            for d, h in ((dk, hk), (dv, hv), (dq, hq)):
-                d.copy_(h, non_blocking=True)
-            enc(dk)
-            qjl(dk)
+            pipe.begin()
+            ek = [pipe.copy(dk[r], hk[r]) for r in parts]
+            ev = pipe.copy(dv, hv)
+            eq = pipe.copy(dq, hq)
+            for r, e in zip(parts, ek):
+                pipe.wait(e)
+                tq.tq_encode_kv(dk[r], cb, signs, kb2[r], stream=stream)
+                tq.tq_qjl_encode(dk[r], kb2[r], cb, signs, S, bits2[r], rn2[r], stream=stream)
+            pipe.wait(ev)
+            pipe.wait(eq)
             attn(dq, dv)
             hout.copy_(out, non_blocking=True)
         return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
