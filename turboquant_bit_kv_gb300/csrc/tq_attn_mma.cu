@@ -48,8 +48,14 @@ MmaPlan mma_plan(int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G)
     int per_sm = 0, warps = 0;
     mma_shape(kb, vb, qjl, G, p.wide != 0, &per_sm, &warps);
     p.P = (int)min64(p.Ctot, (int64_t)(per_sm > 0 ? per_sm : 1) * sm_count());
-    // at most one worker per chunk, so that every worker range is non-empty
-    p.W = (int)min64(p.Ctot, (int64_t)p.P * (warps > 0 ? warps : 1));
+    // at most one worker per chunk (every range non-empty), and on small problems no more than
+    // kMmaMaxWorkersPerSeg workers per segment on average, so that a segment has at most 32
+    // partials and the combine merges them in one round of loads (each further round costs ~2 us
+    // of L2 latency) -- unless that would give workers more than kMmaMaxChunksCapped chunks each
+    // (long ranges at low occupancy cost more than the rounds they save)
+    const int64_t capped = max64(segs * kMmaMaxWorkersPerSeg, (p.Ctot + kMmaMaxChunksCapped - 1) / kMmaMaxChunksCapped);
+    p.W = (int)min64(min64(p.Ctot, capped), (int64_t)p.P * (warps > 0 ? warps : 1));
+    if (p.P > p.W) p.P = p.W;   // no CTA without a worker
     p.Smax = mma_slots(segs, p.C, p.W);
     p.frag_off = (int64_t)B * Hq * p.Smax * kPartialFloats;
     return p;
