@@ -11,7 +11,7 @@ namespace tq {
 constexpr int kMmaChunk = 32;        // tokens per chunk
 constexpr int kMmaMaxWarpsPerSm = 16;   // no configuration runs more warps per SM
 constexpr int kMmaMaxWorkersPerSeg = 31;   // workers <= 31 x segments: at most 32 partial slots,
-constexpr int kMmaMaxChunksCapped = 4;     // as long as that leaves each worker 4 chunks or fewer
+constexpr int kMmaMaxChunksCapped = 5;     // as long as that leaves each worker 5 chunks or fewer
 // Query fragments per (sequence, KV head) segment, in 32-bit words: three
 // parts (n-tiles 0 and 1 of the rotated query, the sketched query) x 32
 // lanes x 16 words.
