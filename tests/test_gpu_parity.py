@@ -341,6 +341,10 @@ def test_attention_single_head(env, kbits, vbits):
     (500, 8, 8, 20, 24, 4, 2, "random"),            # G = 1, one chunk per segment
     (300, 32, 8, 70, 72, 3, 3, "random"),           # G = 4, three chunks per segment
     (100, 56, 8, 45, 48, 3, 3, "random"),           # G = 7 (two n-tiles)
+    # few long segments: more than 32 partials per segment, merged by two to four slot groups
+    (2, 8, 2, 9000, 9008, 3, 3, [9000, 4500]),      # 58 slots, a ragged second sequence
+    (1, 4, 1, 20000, 20000, 4, 2, None),            # 126 slots
+    (1, 8, 2, 32768, 32768, 4, 2, None),            # 206 slots: two rounds per group
 ])
 def test_attention_gqa_ragged(env, B, Hq, Hkv, T, T_cap, kbits, vbits, lens):
     if lens == "random":

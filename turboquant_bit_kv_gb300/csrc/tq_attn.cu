@@ -1,6 +1,7 @@
 // Decode attention: split-combine kernel and the C-ABI entry points
 // tq_attn_workspace_bytes / tq_attn_decode.  The split-pass kernels live in
 // tq_attn.cuh and are instantiated in tq_attn_g{1,2,4,8}.cu.
+#include <algorithm>
 #include <cmath>
 
 #include "tq_attn.cuh"
@@ -149,22 +150,24 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prep_mma_kernel(const __gri
 
 // Merge for the tensor-core kernel's partition: the slots of segment
 // j = (sequence, KV head) are the warps whose chunk ranges touch it.  One
-// CTA per (sequence, query head), thread d = output dim d.  Reading what
-// other SMs just wrote costs a full L2 round trip, so each thread issues
-// every load of a batch of up to 32 slots at once (m and l of each slot --
-// the same address across the CTA -- and its dim of acc) and only then
-// reduces: one round trip per 32 slots, running max rescaled between
-// batches.  Launched as a programmatic dependent of the attention kernel:
-// its CTAs wait here until that grid has finished and its writes are
-// visible.
-__global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const float *ws, MmaPlan plan, int Hq,
-                                                                        int Hkv, int rotate_back, uint32_t s0,
-                                                                        uint32_t s1, uint32_t s2, uint32_t s3,
-                                                                        float *out) {
+// CTA per (sequence, query head) of 128 x ng threads: thread d of slot
+// group g reduces output dim d over batches g, g + ng, ... of 32 slots.
+// Reading what other SMs just wrote costs a full L2 round trip, so each
+// thread issues every load of a batch at once (m and l of each slot -- the
+// same address across the group -- and its dim of acc) and only then
+// reduces, with the running max rescaled between batches; the groups run
+// their rounds side by side and meet in shared memory.  Launched as a
+// programmatic dependent of the attention kernel: its CTAs wait here until
+// that grid has finished and its writes are visible.
+__global__ void __launch_bounds__(kAttnThreads * kCombineMaxGroups) attn_combine_mma_kernel(
+    const float *ws, MmaPlan plan, int Hq, int Hkv, int rotate_back, uint32_t s0, uint32_t s1, uint32_t s2,
+    uint32_t s3, float *out) {
     constexpr int kBatch = 32;
     __shared__ float buf[kD];
+    __shared__ float gacc[kCombineMaxGroups][kD];
+    __shared__ float gml[kCombineMaxGroups][2];
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int d = threadIdx.x;
+    const int d = threadIdx.x & (kD - 1), grp = threadIdx.x / kD, ng = blockDim.x / kD;
     const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int G = Hq / Hkv;
     const int64_t j = (int64_t)b * Hkv + h / G;
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const fl
     const int nslots = (int)(mma_worker_of_chunk((j + 1) * plan.C - 1, plan) - first + 1);
     const float *base = ws + (int64_t)blockIdx.x * plan.Smax * kPartialFloats;
     float M = -INFINITY, l = 0.f, acc = 0.f;
-    for (int sb = 0; sb < nslots; sb += kBatch) {
+    for (int sb = grp * kBatch; sb < nslots; sb += ng * kBatch) {
         float mv[kBatch], lv[kBatch], xv[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
@@ -199,17 +202,54 @@ __global__ void __launch_bounds__(kAttnThreads) attn_combine_mma_kernel(const fl
             acc = fmaf(w, xv[i], acc);
         }
     }
+    if (ng > 1) {
+        // the groups' states, rescaled to their common max (every thread of a group holds the same
+        // M and l)
+        gacc[grp][d] = acc;
+        if (d == 0) {
+            gml[grp][0] = M;
+            gml[grp][1] = l;
+        }
+        __syncthreads();
+        if (grp == 0) {
+            float Mt = -INFINITY;
+            for (int g = 0; g < ng; ++g) Mt = fmaxf(Mt, gml[g][0]);
+            l = 0.f;
+            acc = 0.f;
+            if (Mt != -INFINITY) {
+                for (int g = 0; g < ng; ++g) {
+                    const float mg = gml[g][0];
+                    const float w = mg == -INFINITY ? 0.f : exp2f(mg - Mt);
+                    l = fmaf(w, gml[g][1], l);
+                    acc = fmaf(w, gacc[g][d], acc);
+                }
+            }
+        }
+    }
     const float o = (l > 0.f || l != l) ? acc / l : 0.f;   // a NaN l (failed copy) propagates
     if (!rotate_back) {
-        out[(int64_t)blockIdx.x * kD + d] = o;
+        if (grp == 0) out[(int64_t)blockIdx.x * kD + d] = o;
         return;
     }
-    buf[d] = o;
+    // inverse rotation by group 0; every thread passes the same barriers
+    if (grp == 0) buf[d] = o;
     __syncthreads();
-    smem_fwht_rows<1>(buf);
-    const uint32_t sw[4] = {s0, s1, s2, s3};
-    const float v = buf[d] * 0.08838834764831845f;
-    out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -v : v;
+#pragma unroll
+    for (int L = 1; L < kD; L <<= 1) {
+        float v = 0.f, w = 0.f;
+        if (grp == 0) {
+            v = buf[d];
+            w = buf[d ^ L];
+        }
+        __syncthreads();
+        if (grp == 0) buf[d] = (d & L) ? (w - v) : (v + w);
+        __syncthreads();
+    }
+    if (grp == 0) {
+        const uint32_t sw[4] = {s0, s1, s2, s3};
+        const float v = buf[d] * 0.08838834764831845f;
+        out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -v : v;
+    }
 }
 
 static int attn_smem_bytes(int kb, int vb) {
@@ -290,7 +330,9 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
         if (r != TQ_OK) return r;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(B * Hq));
-        cfg.blockDim = dim3(kAttnThreads);
+        // one slot group per 32 slots of the plan's bound, at most kCombineMaxGroups
+        const int ng = std::min(kCombineMaxGroups, std::max(1, (mp.Smax + 31) / 32));
+        cfg.blockDim = dim3(kAttnThreads * ng);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];

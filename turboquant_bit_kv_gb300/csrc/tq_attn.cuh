@@ -21,6 +21,7 @@
 namespace tq {
 
 constexpr int kAttnThreads = 128;
+constexpr int kCombineMaxGroups = 4;   // slot groups of 128 threads in one combine CTA
 constexpr int kTT = 64;                  // tokens per staged tile
 constexpr int kPartialFloats = 132;      // m, l, pad, pad, acc[128]
 constexpr int kTargetCtas = 1216;        // split-count target (8 x 152 SMs)
