@@ -219,17 +219,32 @@ class _CopyPipe:
     """Host-to-device copies of an end-to-end step, issued in chunks on a
     side stream; the bench stream waits for a chunk right before the call that
     reads it, so the kernels run while the remaining bytes cross the host link
-    (the link's bandwidth bounds the step; more copy streams do not add to it)."""
+    (the link's bandwidth bounds the step; more copy streams do not add to it).
+    Steps alternate between `nbuf` sets of device input buffers, so the copies
+    of the next step run while this step's last kernels finish."""
 
-    def __init__(self, stream):
+    def __init__(self, stream, nbuf=2):
         self.main = stream
         self.side = torch.cuda.Stream(device=stream.device)
+        self.free = [None] * nbuf   # per buffer set: its last reader on the bench stream has run
+        self.n = 0
 
     def begin(self):
-        # the previous step's kernels have read the device buffers before they are overwritten
+        """Start a step; returns the index of the buffer set its copies fill."""
+        i = self.n % len(self.free)
+        self.n += 1
+        ev = self.free[i]
+        if ev is None:
+            ev = torch.cuda.Event()
+            ev.record(self.main)
+        self.side.wait_event(ev)
+        return i
+
+    def release(self, i):
+        """Buffer set i has been read by everything enqueued so far on the bench stream."""
         ev = torch.cuda.Event()
         ev.record(self.main)
-        self.side.wait_event(ev)
+        self.free[i] = ev
 
     def copy(self, dst, src):
         with torch.cuda.stream(self.side):
@@ -277,12 +292,13 @@ def plan_llama(tq, wl, dev, stream, seed, batch):
     def e2e():
         hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)
         hout = torch.empty_like(out, device="cpu").pin_memory()
-        dk, dv, dq = (torch.empty_like(t, device=dev) for t in (hk, hv, hq))
+        bufs = [[torch.empty_like(t, device=dev) for t in (hk, hv, hq)] for _ in range(2)]
         kb2, vb2 = kb.view(nvec, -1), vb.view(nvec, -1)
         pipe, parts = _CopyPipe(stream), _chunks(nvec, 4)
 
         def step():
-            pipe.begin()
+            i = pipe.begin()
+            dk, dv, dq = bufs[i]
             eq = pipe.copy(dq, hq)
             ek = [pipe.copy(dk[r], hk[r]) for r in parts]
             ev = [pipe.copy(dv[r], hv[r]) for r in parts]
@@ -294,6 +310,7 @@ def plan_llama(tq, wl, dev, stream, seed, batch):
                 tq.tq_encode_kv(dv[r], vcb, signs, vb2[r], stream=stream)
             pipe.wait(eq)
             attn(dq)
+            pipe.release(i)
             hout.copy_(out, non_blocking=True)
         return step, k.numel() * 2 + v.numel() * 2 + q.numel() * 2, out.numel() * 4
 
@@ -381,13 +398,13 @@ def plan_qwen(tq, wl, dev, stream, seed, batch):
         hk, hv = _pinned(pre["k"]), _pinned(pre["v"])
         hnk, hnv, hq = _pinned(new["k"]), _pinned(new["v"]), _pinned(q)
         hout = torch.empty_like(out, device="cpu").pin_memory()
-        dk, dv = torch.empty_like(pre["k"]), torch.empty_like(pre["v"])
-        dnk, dnv, dq = torch.empty_like(new["k"]), torch.empty_like(new["v"]), torch.empty_like(q)
+        bufs = [[torch.empty_like(t) for t in (pre["k"], pre["v"], new["k"], new["v"], q)] for _ in range(2)]
 
         pipe, parts = _CopyPipe(stream), _chunks(n_pre, 4)
 
         def step():
-            pipe.begin()
+            i = pipe.begin()
+            dk, dv, dnk, dnv, dq = bufs[i]
             small = [pipe.copy(d, h) for d, h in ((dnk, hnk), (dnv, hnv), (dq, hq))]
             ek = [pipe.copy(dk[r], hk[r]) for r in parts]
             ev = [pipe.copy(dv[r], hv[r]) for r in parts]
@@ -400,6 +417,7 @@ def plan_qwen(tq, wl, dev, stream, seed, batch):
             enc(dnk, "k", dst_new)()
             enc(dnv, "v", dst_new)()
             attn(dq)
+            pipe.release(i)
             hout.copy_(out, non_blocking=True)
         return step, (2 * (n_pre + n_new) * 128 + q.numel()) * 2, out.numel() * 4
 
@@ -442,12 +460,13 @@ def plan_qjl(tq, wl, dev, stream, seed, batch):
     def e2e():
         hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v), _pinned(q)
         hout = torch.empty_like(out, device="cpu").pin_memory()
-        dk, dv, dq = (torch.empty_like(t, device=dev) for t in (hk, hv, hq))
+        bufs = [[torch.empty_like(t, device=dev) for t in (hk, hv, hq)] for _ in range(2)]
         kb2, bits2, rn2 = kb.view(n, 50), bits.view(n, 16), rn.view(n)
         pipe, parts = _CopyPipe(stream), _chunks(n, 4)
 
         def step():
-            pipe.begin()
+            i = pipe.begin()
+            dk, dv, dq = bufs[i]
             ek = [pipe.copy(dk[r], hk[r]) for r in parts]
             ev = pipe.copy(dv, hv)
             eq = pipe.copy(dq, hq)
@@ -458,6 +477,7 @@ def plan_qjl(tq, wl, dev, stream, seed, batch):
             pipe.wait(ev)
             pipe.wait(eq)
             attn(dq, dv)
+            pipe.release(i)
             hout.copy_(out, non_blocking=True)
         return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
 
