@@ -14,7 +14,7 @@
 //   P = (R r) S'^T       (fp16 hi / lo splits of R r and S': float32-grade)
 // and the per-element work in between is one centroid lookup and one FMA.
 //
-// One CTA per SM (the operands take ~206 KB of shared memory): a producer
+// One CTA per SM (the operands take ~219 KB of shared memory): a producer
 // warp issues the TMA loads of key tiles and all MMAs; sixteen epilogue warps
 // (four per 32-row group of tensor-memory lanes, one 32-column slice each)
 // read U, form R r from the staged blocks, write its hi / lo fp16 tiles for
