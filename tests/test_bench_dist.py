@@ -84,3 +84,18 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("n,parts", [(1048576, 4), (8388608, 4), (5000, 4), (1000, 4), (1, 4), (4096, 1)])
+def test_end_to_end_chunks_cover_rows_once(n, parts):
+    # the chunked host-to-device copies of an end-to-end step: every row exactly once, in order,
+    # at most `parts` chunks, boundaries on multiples of 1024 rows (16-byte aligned block offsets)
+    sys.path.insert(0, ROOT)
+    import bench
+    ch = bench._chunks(n, parts)
+    assert 1 <= len(ch) <= parts
+    assert ch[0].start == 0 and ch[-1].stop == n
+    for a, b in zip(ch, ch[1:]):
+        assert a.stop == b.start
+    for c in ch:
+        assert c.start < c.stop and c.start % 1024 == 0
