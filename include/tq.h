@@ -132,6 +132,24 @@ int tq_qjl_encode(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_el
  * Returns 0 for an invalid shape. */
 size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap);
 
+/* The work partition tq_attn_decode's tensor-core path uses for a shape
+ * (split-K over the context, [spec] Optimization: Fused dequant-dot), for
+ * tests and tuning.  value_bits 16 stands for raw fp16 values; qjl != 0 for
+ * the two-term score; sms <= 0 takes the current device's SM count.  Fills
+ * out[7] (host memory):
+ *   out[0] C     chunks of 32 tokens per (sequence, KV head) segment,
+ *   out[1] Ctot  B * Hkv * C, chunks ordered by (sequence, KV head, position),
+ *   out[2] P     CTAs,
+ *   out[3] W     warp workers; worker w owns chunks [w Ctot / W, (w+1) Ctot / W),
+ *   out[4] Smax  partial slots per (sequence, query head): no segment meets
+ *                more worker ranges,
+ *   out[5]       slot groups of 128 threads in a combine CTA,
+ *   out[6]       warps per CTA.
+ * Host only: touches no device memory.  TQ_ERR_ARG for a bad shape or a NULL
+ * out; TQ_ERR_UNSUPPORTED for invalid bits or a shape that takes the CUDA-core
+ * split path instead. */
+int tq_attn_plan(int B, int Hq, int Hkv, int T, int key_bits, int value_bits, int qjl, int sms, int64_t *out);
+
 /* Fused decode attention over a packed cache ([spec] Optimization: Fused
  * dequant-dot; [fork] section 2 "fused flash-attention path required";
  * [rotor] Fused Kernel Logic for the QJL term).  One query token per

@@ -330,9 +330,7 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
         if (r != TQ_OK) return r;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(B * Hq));
-        // one slot group per 32 slots of the plan's bound, at most kCombineMaxGroups
-        const int ng = std::min(kCombineMaxGroups, std::max(1, (mp.Smax + 31) / 32));
-        cfg.blockDim = dim3(kAttnThreads * ng);
+        cfg.blockDim = dim3(kAttnThreads * mma_combine_groups(mp));
         cfg.dynamicSmemBytes = 0;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];

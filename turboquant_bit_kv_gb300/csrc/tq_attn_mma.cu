@@ -39,15 +39,20 @@ static int mma_slots(int64_t segs, int64_t C, int64_t W) {
 }
 
 MmaPlan mma_plan(int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G) {
+    return mma_plan_for(sm_count(), B, Hq, Hkv, T, kb, vb, qjl, G);
+}
+
+MmaPlan mma_plan_for(int sms, int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G) {
     MmaPlan p;
     const int64_t segs = (int64_t)B * Hkv;
     p.C = (T + kMmaChunk - 1) / kMmaChunk;
     p.Ctot = segs * p.C;
     // the 16-warp variant once every warp would get at least 32 chunks, else 12 warps per SM
-    p.wide = p.Ctot >= (int64_t)32 * kMmaMaxWarpsPerSm * sm_count() ? 1 : 0;
+    p.wide = p.Ctot >= (int64_t)32 * kMmaMaxWarpsPerSm * sms ? 1 : 0;
     int per_sm = 0, warps = 0;
     mma_shape(kb, vb, qjl, G, p.wide != 0, &per_sm, &warps);
-    p.P = (int)min64(p.Ctot, (int64_t)(per_sm > 0 ? per_sm : 1) * sm_count());
+    p.warps = warps;
+    p.P = (int)min64(p.Ctot, (int64_t)(per_sm > 0 ? per_sm : 1) * sms);
     // at most one worker per chunk (every range non-empty), and on small problems no more than
     // kMmaMaxWorkersPerSeg workers per segment on average, so that a segment has at most 32
     // partials and the combine merges them in one round of loads (each further round costs ~2 us

@@ -56,6 +56,7 @@ def lib():
         L.tq_qjl_encode.argtypes = [vp, c_int, i64, i64, vp, i64, cbp, tq_signs, vp, vp, vp, vp]
         L.tq_attn_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
         L.tq_attn_workspace_bytes.restype = sz
+        L.tq_attn_plan.argtypes = [c_int] * 8 + [ctypes.POINTER(i64)]
         L.tq_attn_decode.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, c_int, c_int, c_int,
                                      ctypes.c_float, tq_signs, vp, vp, vp, vp, vp, sz, vp]
         L.tq_serde_size.argtypes = [c_int] * 10
@@ -167,6 +168,15 @@ def tq_qjl_encode(k, k_blocks, cb, signs, S, qjl_bits, res_norm_f16, block_strid
     bs = block_stride_bytes or tq_block_bytes(cb.bits)
     _check(lib().tq_qjl_encode(_ptr(k), _dtype(k), n, stride, _ptr(k_blocks), bs, ctypes.byref(cb), signs,
                                _ptr(S), _ptr(qjl_bits), _ptr(res_norm_f16), _stream(stream)), "tq_qjl_encode")
+
+
+def tq_attn_plan(B, Hq, Hkv, T, key_bits, value_bits, qjl=False, sms=0):
+    """The tensor-core attention path's work partition for a shape, as a dict
+    (C, Ctot, P, W, Smax, combine_groups, warps); raises TQError when the shape
+    takes the split path or is invalid."""
+    out = (ctypes.c_int64 * 7)()
+    _check(lib().tq_attn_plan(B, Hq, Hkv, T, key_bits, value_bits, 1 if qjl else 0, sms, out), "tq_attn_plan")
+    return dict(zip(("C", "Ctot", "P", "W", "Smax", "combine_groups", "warps"), (int(x) for x in out)))
 
 
 def tq_attn_workspace_bytes(B, Hq, Hkv, T_cap):
