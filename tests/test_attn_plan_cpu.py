@@ -17,7 +17,8 @@ sys.path.insert(0, ROOT)
 
 @pytest.fixture(scope="module")
 def tq():
-    from turboquant_bit_kv_gb300 import tq as t
+    from turboquant_bit_kv_gb300 import build_lib, tq as t
+    build_lib.build()
     t.lib()
     return t
 
