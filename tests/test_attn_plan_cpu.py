@@ -102,3 +102,7 @@ def test_plan_rejects_split_path_and_bad_shapes(tq):
         tq.tq_attn_plan(1, 8, 8, 0, 4, 2)                  # no tokens
     with pytest.raises(tq.TQError):
         tq.tq_attn_plan(1, 8, 8, 64, 5, 2)                 # bits
+    for args in ((1, 8, 1, 64, 3, 16), (1, 4, 1, 64, 2, 16), (1, 4, 1, 64, 3, 3)):
+        with pytest.raises(tq.TQError) as e:                # QJL shapes served by the CUDA-core path
+            tq.tq_attn_plan(*args, qjl=True)
+        assert e.value.status == tq.TQ_ERR_UNSUPPORTED
