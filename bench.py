@@ -1,18 +1,19 @@
 """Benchmark of the TurboQuant KV hot path on GB300.
 
-Default workload (``--workload llama3_8b_decode``): one step = quantise-on-
-insert of the whole K and V cache (tq_encode_kv: K 4-bit, V 2-bit) followed
-by one fused decode-attention step over it (tq_attn_decode), Llama-3-8B
-shaped: batch 16, 32 query heads, 8 KV heads, head_dim 128, context 8192,
-bf16 K/V with log-normal channel scales and AR(1) token correlation 0.9.
+Default workload (``--workload qwen25_7b_append``, the largest decode
+configuration): batch 64, 28 query heads, 4 KV heads, head_dim 128, context
+32768 bf16 K/V with 1% outlier channels, K3/V3.  One step = quantise-on-
+insert of the whole 32768-token K and V prefix into a [B, Hkv, T_cap] cache
+through a destination index (tq_encode_kv), the append of one new token per
+sequence, and one fused decode-attention step over the 32769 tokens
+(tq_attn_decode).
 
 Other workloads (one JSON line each, same keys):
 
+* ``llama3_8b_decode``   -- batch 16, 32/8 heads, context 8192, bf16 K/V with
+                            log-normal channel scales and AR(1) correlation
+                            0.9, K4/V2: encode the cache, one decode step;
 * ``single_head_fp32``   -- one head, 4096 fp32 K/V rows, K4/V2, one query;
-* ``qwen25_7b_append``   -- batch 64, 28/4 heads, context 32768 bf16 with 1%
-                            outlier channels, K3/V3: encode the prefix into a
-                            [B, Hkv, T_cap] cache through a destination index,
-                            append one token per sequence, attend over 32769;
 * ``qjl_two_term``       -- batch 8, 32/8 heads, context 16384: K3 encode,
                             QJL sign bits + residual norms, attention with the
                             two-term score and raw fp16 values;
@@ -20,11 +21,19 @@ Other workloads (one JSON line each, same keys):
                             layers, 28 layers K4/V4 in 132-byte slots) and
                             deserialise.
 
-`value` is the algorithmic bytes of a step (what the method must move:
-inputs read and outputs written by each call) over the device time of a
-step, in GB/s.  `e2e` is the same bytes over the time of a step run through
-the C ABI from pinned host buffers (host->device copy of the inputs, the
-step, and the device->host copy of the result inside the timed region).
+`value` is the metric's decode-attention throughput: the attention call's
+algorithmic bytes (packed K/V blocks with their norms, the query and the
+output; QJL side data where used) over the call's device time inside the
+timed steps, in GB/s (for the storage round trip, which has no attention
+call, the serialise + deserialise bytes over their time).
+`encode_gvec_s` / `encode_frac_hbm` give the prefix encode's vectors per
+second and its bytes over time as a fraction of the HBM peak; `parts` has
+every call of the step.  `e2e` measures the metric through the C ABI from
+pinned host buffers: each step copies the step's new inputs (the query and
+the appended token's K/V rows) from the host, runs the append and the
+attention call against the cache resident in HBM, and reads the output
+back; `e2e.full_step` runs the whole step (the prefix K/V rows copied from
+the host too) and reports the step's bytes over its time.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                        [--workload NAME]
@@ -49,7 +58,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "compressed-KV decode-attention GB/s & % HBM peak; encode Gvec/s (1xGB300)"
-DEFAULT_WORKLOAD = "llama3_8b_decode"
+DEFAULT_WORKLOAD = "qwen25_7b_append"
 WORKLOADS = {
     "llama3_8b_decode": dict(B=16, Hq=32, Hkv=8, T=8192, head_dim=128, key_bits=4, value_bits=2,
                              kv_dtype="bf16", scale="1/sqrt(128)"),
@@ -314,8 +323,29 @@ def plan_llama(tq, wl, dev, stream, seed, batch):
             hout.copy_(out, non_blocking=True)
         return step, k.numel() * 2 + v.numel() * 2 + q.numel() * 2, out.numel() * 4
 
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 2, out.numel() * 4
+
+    def sample():
+        rng = np.random.default_rng(3)
+        res = []
+        for name, x, blk, bits in (("K", k, kb, 4), ("V", v, vb, 2)):
+            pick = torch.from_numpy(np.sort(rng.choice(nvec, 4096, replace=False))).to(dev)
+            res.append((name, bits, x.view(-1, 128)[pick].double().cpu().numpy(),
+                        blk.view(nvec, -1)[pick].cpu().numpy()))
+        return res
+
     cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2 (129 MB); attention also timed after an L2 flush")
-    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="bf16")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, sample=sample, config=cfg,
+                dtype="bf16")
 
 
 def plan_single_head(tq, wl, dev, stream, seed, batch):
@@ -357,8 +387,24 @@ def plan_single_head(tq, wl, dev, stream, seed, batch):
             hout.copy_(out, non_blocking=True)
         return step, (k.numel() + v.numel() + q.numel()) * 4, out.numel() * 4
 
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 4, out.numel() * 4
+
+    def sample():
+        return [("K", 4, k.double().cpu().numpy(), kb.view(T, -1).cpu().numpy()),
+                ("V", 2, v.double().cpu().numpy(), vb.view(T, -1).cpu().numpy())]
+
     cfg = dict(W, l2="inputs (4.6 MB) fit in L2: launch-bound, report microseconds")
-    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="f32")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, sample=sample, config=cfg,
+                dtype="f32")
 
 
 def plan_qwen(tq, wl, dev, stream, seed, batch):
@@ -421,9 +467,36 @@ def plan_qwen(tq, wl, dev, stream, seed, batch):
             hout.copy_(out, non_blocking=True)
         return step, (2 * (n_pre + n_new) * 128 + q.numel()) * 2, out.numel() * 4
 
+    def decode_e2e():
+        hnk, hnv, hq = _pinned(new["k"]), _pinned(new["v"]), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dnk, dnv, dq = torch.empty_like(new["k"]), torch.empty_like(new["v"]), torch.empty_like(q)
+
+        def step():
+            dnk.copy_(hnk, non_blocking=True)
+            dnv.copy_(hnv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            enc(dnk, "k", dst_new)()
+            enc(dnv, "v", dst_new)()
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (2 * n_new * 128 + q.numel()) * 2, out.numel() * 4
+
+    def sample():
+        rng = np.random.default_rng(3)
+        res = []
+        for n in ("k", "v"):
+            pick = torch.from_numpy(np.sort(rng.choice(n_pre, 4096, replace=False))).to(dev)
+            res.append(("prefix " + n.upper(), 3, pre[n][pick].double().cpu().numpy(),
+                        blk[n].view(-1, 50)[dst_pre[pick]].cpu().numpy()))
+            res.append(("append " + n.upper(), 3, new[n].double().cpu().numpy(),
+                        blk[n].view(-1, 50)[dst_new].cpu().numpy()))
+        return res
+
     cfg = dict(W, B=B, l2="inputs (4.3 GB) larger than L2; attention also timed after an L2 flush",
                note="destination-index reads (8 B per vector) are not counted as algorithmic bytes")
-    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="bf16")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, sample=sample, config=cfg,
+                dtype="bf16")
 
 
 def plan_qjl(tq, wl, dev, stream, seed, batch):
@@ -481,9 +554,26 @@ def plan_qjl(tq, wl, dev, stream, seed, batch):
             hout.copy_(out, non_blocking=True)
         return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
 
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 2, out.numel() * 4
+
+    def sample():
+        rng = np.random.default_rng(3)
+        pick = torch.from_numpy(np.sort(rng.choice(n, 4096, replace=False))).to(dev)
+        return [("K", 3, k.view(-1, 128)[pick].double().cpu().numpy(), kb.view(n, 50)[pick].cpu().numpy())]
+
     cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2; attention also timed after an L2 flush",
                note="QJL sketch S: seeded 128x128 N(0,1) float32; resident on the device")
-    return dict(ops=ops, cold="attention", e2e=e2e, config=cfg, dtype="bf16")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, sample=sample, config=cfg,
+                dtype="bf16")
 
 
 def plan_storage(tq, wl, dev, stream, seed, batch):
@@ -524,9 +614,39 @@ def plan_storage(tq, wl, dev, stream, seed, batch):
             hy.copy_(dy, non_blocking=True)
         return step, x.numel() * 2, x.numel() * 2
 
+    H = hidden // 128
+    qs = sf
+    comp_off = 2 * qs * T * hidden * 2
+
+    def sample():
+        rng = np.random.default_rng(3)
+        layer = (sf + L - sl) // 2
+        ti = torch.from_numpy(np.sort(rng.choice(T, 512, replace=False))).to(dev)
+        comp = buf[comp_off:comp_off + Lc * (-(-T // bs) * bs) * H * 132].view(Lc, -1, H, 132)
+        res = []
+        for kv, off in ((0, 0), (1, 66)):
+            rows = x[kv, layer].view(T, H, 128)[ti].reshape(-1, 128)
+            blocks = comp[layer - qs][ti][:, :, off:off + 66].reshape(-1, 66)
+            res.append(("layer %d %s" % (layer, "KV"[kv]), 4, rows.double().cpu().numpy(), blocks.cpu().numpy()))
+        return res
+
+    def mse_per_layer():
+        """Round-trip MSE of every layer (relative to the layer's mean square), K and V."""
+        ser()
+        des()
+        torch.cuda.synchronize(dev)
+        out = {"K": [], "V": []}
+        for layer in range(L):
+            for kv in (0, 1):
+                xd = x[kv, layer].float()
+                m = float(((y[kv, layer].float() - xd) ** 2).mean() / (xd * xd).mean())
+                out["KV"[kv]].append(round(m, 6))
+        return out
+
     cfg = dict(W, T=T, l2="inputs (8.6 GB) larger than L2",
                note="raw layers are device-to-device copies; per way: tensor bytes + serialised bytes")
-    return dict(ops=ops, cold=None, e2e=e2e, config=cfg, dtype="bf16")
+    return dict(ops=ops, cold=None, e2e=e2e, decode_e2e=None, sample=sample, mse=mse_per_layer, config=cfg,
+                dtype="bf16")
 
 
 PLANS = {"llama3_8b_decode": plan_llama, "single_head_fp32": plan_single_head, "qwen25_7b_append": plan_qwen,
@@ -601,23 +721,32 @@ def run_gpu(args, rank, world, local_rank):
         cold_ms = statistics.median(cold)
         del flush
 
-    # end to end through the C ABI from pinned host buffers
-    e2e_step, h2d, d2h = plan["e2e"]()
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    n_e2e = max(1, min(args.steps, 200, int(2e10 // max(1, h2d + d2h))))
-    barrier(world)
-    t0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(t0.elapsed_time(t1) / n_e2e, world)
+    def timed_e2e(make):
+        step, h2d, d2h = make()
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
+        n_iter = max(3, min(args.steps, 200, int(2e10 // max(1, h2d + d2h))))
+        barrier(world)
+        t0.record(stream)
+        for _ in range(n_iter):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        return reduce_max(t0.elapsed_time(t1) / n_iter, world), n_iter, h2d, d2h
+
+    # end to end through the C ABI from pinned host buffers: the decode step
+    # (new inputs from the host, cache resident) and the whole step
+    full_ms, n_full, full_h2d, full_d2h = timed_e2e(plan["e2e"])
+    dec = timed_e2e(plan["decode_e2e"]) if plan.get("decode_e2e") else None
+
+    extra = {}
+    if plan.get("mse"):
+        extra["roundtrip_mse_per_layer"] = plan["mse"]()
+    samples = plan["sample"]() if plan.get("sample") else []
 
     peak, peak_kind = hbm_peak()
     total = sum(op.nbytes for op in ops)
-    value = world * total / (ms_step * 1e-3) / 1e9
     parts, groups = {}, {}
     for op, ms in zip(ops, op_ms):
         gbs = op.nbytes / (ms * 1e-3) / 1e9
@@ -630,10 +759,11 @@ def run_gpu(args, rank, world, local_rank):
             p.update(cold_l2_us=round(cold_ms * 1e3, 2), cold_l2_gbs=round(cg, 1),
                      cold_l2_frac_hbm=round(cg / peak, 4))
         parts[op.name] = p
-        g = groups.setdefault(op.group, {"ms": 0.0, "bytes": 0, "launches": 0})
+        g = groups.setdefault(op.group, {"ms": 0.0, "bytes": 0, "launches": 0, "nvec": 0})
         g["ms"] += ms
         g["bytes"] += op.nbytes
         g["launches"] += op.launches
+        g["nvec"] += op.nvec
 
     def roofline(name):
         g = groups[name]
@@ -643,22 +773,53 @@ def run_gpu(args, rank, world, local_rank):
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "traffic": tr, "algorithmic_bytes": g["bytes"]}
 
-    dominant = max(groups, key=lambda n: groups[n]["ms"])
+    # the metric: the decode-attention call's bytes over its time (per call,
+    # averaged over the timed steps); without an attention call, the step's
+    attn = next((op for op in ops if op.group == "attention"), None)
+    if attn is not None:
+        a_ms = op_ms[ops.index(attn)]
+        value = world * attn.nbytes / (a_ms * 1e-3) / 1e9
+        head = "attention"
+    else:
+        value = world * total / (ms_step * 1e-3) / 1e9
+        head = max(groups, key=lambda n: groups[n]["ms"])
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": plan["dtype"], "data": "synthetic (seeded; no dataset or model weights)",
         "config": dict(plan["config"], workload=args.workload,
                        parallelism="replicas" if world > 1 else "single GPU"),
-        "parts": parts,
-        "roofline": roofline(dominant),
-        "roofline_by_kernel": {n: roofline(n) for n in groups},
-        "e2e": {"value": round(world * total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "steps": n_e2e, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": sum(op.launches for op in ops) * args.steps,
-        "clocks": clk,
+        "frac_hbm": round(value / world / peak, 4),
     }
+    if "encode" in groups:
+        g = groups["encode"]
+        res["encode_gvec_s"] = round(world * g["nvec"] / (g["ms"] * 1e-3) / 1e9, 3)
+        res["encode_gbs"] = round(g["bytes"] / (g["ms"] * 1e-3) / 1e9, 1)
+        res["encode_frac_hbm"] = round(res["encode_gbs"] / peak, 4)
+    res.update({
+        "step_gbs": round(world * total / (ms_step * 1e-3) / 1e9, 2),
+        "parts": parts,
+        "roofline": roofline(head),
+        "roofline_by_kernel": {n: roofline(n) for n in groups},
+    })
+    full = {"value": round(world * total / (full_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "what": "the whole step's algorithmic bytes over the step run from pinned host buffers",
+            "ms_per_step": round(full_ms, 4), "steps": n_full, "h2d_bytes_per_step": full_h2d,
+            "d2h_bytes_per_step": full_d2h}
+    if dec is not None:
+        d_ms, d_n, d_h2d, d_d2h = dec
+        res["e2e"] = {"value": round(world * attn.nbytes / (d_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                      "what": "attention bytes over a decode step through the C ABI: new query (and appended "
+                              "K/V rows) copied from pinned host memory, append + attention against the "
+                              "HBM-resident cache, output read back",
+                      "ms_per_step": round(d_ms, 4), "steps": d_n, "h2d_bytes_per_step": d_h2d,
+                      "d2h_bytes_per_step": d_d2h, "full_step": full}
+    else:
+        res["e2e"] = full
+    res.update(extra)
+    res["gpu_launches"] = sum(op.launches for op in ops) * args.steps
+    res["clocks"] = clk
+    res["_samples"] = samples
     return res
 
 
@@ -813,6 +974,44 @@ def run_reference(args, rank, world):
     }
 
 
+def parity_counts(samples):
+    """Codes and norms of sampled rows of the benchmarked step against the
+    oracle's encoding of the same rows: coordinates within 1e-5 of a decision
+    boundary, code mismatches (allowed only there, below 1e-4 of the
+    coordinates), norms within 2^-22 of an fp16 rounding tie, norm mismatches."""
+    import oracle
+    from oracle import codec
+    from turboquant_bit_kv_gb300 import workloads
+
+    s = oracle.sign_diagonal(workloads.SIGN_SEED)
+    books = {b: oracle.beta_codebook(128, b)[1].astype(np.float32) for b in (2, 3, 4)}
+    rows, tot = [], {"coords": 0, "near_boundary": 0, "code_mismatch": 0, "far_mismatch": 0, "vectors": 0,
+                     "norm_near_tie": 0, "norm_mismatch": 0}
+    for label, bits, x, blocks in samples:
+        b32 = books[bits]
+        idx_o, n16_o, y = codec.encode(x, s, b32)
+        idx_g, n16_g = codec.unpack_block(blocks, bits)
+        near = np.zeros(y.shape, bool)
+        for b in b32.astype(np.float64):
+            near |= np.abs(y - b) < 1e-5
+        mism = idx_g != idx_o
+        n = np.sqrt(np.sum(x * x, axis=-1))
+        h = n.astype(np.float16)
+        mids = [0.5 * (np.nextafter(h, np.float16(0)).astype(np.float64) + h.astype(np.float64)),
+                0.5 * (np.nextafter(h, np.float16(np.inf)).astype(np.float64) + h.astype(np.float64))]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            tie = np.where(n > 0, np.minimum(np.abs(n - mids[0]), np.abs(n - mids[1])) / n, np.inf) < 2.0**-22
+        r = {"sample": label, "bits": bits, "coords": int(mism.size), "near_boundary": int(near.sum()),
+             "code_mismatch": int(mism.sum()), "far_mismatch": int((mism & ~near).sum()), "vectors": int(n.size),
+             "norm_near_tie": int(tie.sum()), "norm_mismatch": int((n16_g != n16_o).sum())}
+        rows.append(r)
+        for k in tot:
+            tot[k] += r[k]
+    out = dict(tot, code_mismatch_frac=tot["code_mismatch"] / max(1, tot["coords"]),
+               norm_mismatch_frac=tot["norm_mismatch"] / max(1, tot["vectors"]), samples=rows)
+    return out
+
+
 def cpu_baseline(workload, groups):
     oracle_sample(workload, 1)
     secs, nbytes, desc = oracle_sample(workload, groups or CPU_GROUPS[workload])
@@ -847,8 +1046,11 @@ def main():
         res = run_reference(args, rank, world)
     else:
         res = run_gpu(args, rank, world, local_rank)
+        samples = res.pop("_samples", []) if res is not None else []
         if rank == 0 and res is not None and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_groups)
+            if samples:
+                res["parity_counts"] = parity_counts(samples)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and args.impl != "reference":

@@ -128,9 +128,15 @@ int tq_qjl_encode(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_el
                   const tq_codebook *cb, tq_signs signs, const float *S,
                   uint8_t *qjl_bits, uint16_t *res_norm_f16, void *stream);
 
-/* Workspace bytes tq_attn_decode needs for this shape (split-K partials).
+/* Workspace bytes tq_attn_decode needs for this shape (split-K partials)
+ * on the current device (the split depends on its SM count).  Host only.
  * Returns 0 for an invalid shape. */
 size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap);
+
+/* The same for a GPU of `sms` SMs (sms <= 0: the current device), for
+ * sizing buffers ahead of time or on a machine without the GPU.  Host only;
+ * touches no device memory.  Returns 0 for an invalid shape. */
+size_t tq_attn_workspace_bytes_sms(int B, int Hq, int Hkv, int T_cap, int sms);
 
 /* The work partition tq_attn_decode's tensor-core path uses for a shape
  * (split-K over the context, [spec] Optimization: Fused dequant-dot), for
@@ -174,8 +180,8 @@ int tq_attn_plan(int B, int Hq, int Hkv, int T, int key_bits, int value_bits, in
  *               all three set (two-term score).
  *   out         device float32 [B][Hq][128].
  *   workspace   device scratch of >= tq_attn_workspace_bytes(B, Hq, Hkv, T_cap)
- *               bytes, 256-byte aligned; clobbered; calls that overlap on the
- *               GPU must use different workspaces.
+ *               bytes, 16-byte aligned (TQ_ERR_ALIGN otherwise); clobbered;
+ *               calls that overlap on the GPU must use different workspaces.
  * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_WORKSPACE,
  * TQ_ERR_CUDA. */
 int tq_attn_decode(const void *q, int q_dtype,
@@ -187,8 +193,12 @@ int tq_attn_decode(const void *q, int q_dtype,
                    float *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Size of the device array that tq_attn_decode_noalloc uses as its split-K
- * scratch (8 MiB; it covers, e.g., batch 64 x 28 query heads at any context). */
-#define TQ_ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+ * scratch: 16 MiB.  On GPUs of 148 to 160 SMs that covers, at any context,
+ * batch 64 x 28 query heads over 4 KV heads (about 11.4 MiB), batch 64 x 32
+ * over 8 (about 9.2 MiB) and batch 128 x 32 over 8 (about 14.3 MiB); batch
+ * 256 x 32 over 8 needs about 24.4 MiB and is refused.
+ * tq_attn_workspace_bytes_sms gives the figure for any shape. */
+#define TQ_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* tq_attn_decode for callers that cannot allocate device memory (the pages
  * have no counterpart: this is a library convenience).  A serving engine
@@ -202,7 +212,8 @@ int tq_attn_decode(const void *q, int q_dtype,
  *     return TQ_ERR_WORKSPACE; an invalid shape returns TQ_ERR_ARG.
  *   - The array's device address is looked up once per device, on the first
  *     call made with that device current; make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept until process exit: after a
+ *     cudaDeviceReset, load the library afresh before calling this again.
  *   - All calls share the array, which keeps the last call's contents (no
  *     part of it needs to start at zero); calls that overlap on the GPU race
  *     on it, so serialise them (one stream, or events).

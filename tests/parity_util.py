@@ -23,6 +23,14 @@ CODE_TOL_Y = 1e-5
 CODE_FRAC = 1e-4
 ATTN_TOL = 1e-3
 
+# One entry per comparison made by check_codes / record(): the counts the
+# parity rule asks to be reported (printed at the end of the pytest session).
+RECORDS = []
+
+
+def record(label, **counts):
+    RECORDS.append(dict(label=label, **counts))
+
 
 def fp16_tie_distance(n):
     """Relative distance of float64 n (>= 0) to the nearest fp16 rounding
@@ -44,6 +52,15 @@ def check_codes(gpu_blocks, bits, x, signs, b32, label=""):
     idx_o, n16_o, y = codec.encode(x, signs, b32)
     idx_g, n16_g = codec.unpack_block(np.asarray(gpu_blocks), bits)
     mism = idx_g != idx_o
+    bd = np.asarray(b32, np.float64)
+    near = np.zeros(y.shape, bool)
+    for b in bd:
+        near |= np.abs(y - b) < CODE_TOL_Y
+    n = np.sqrt(np.sum(x * x, axis=-1))
+    norm_near = fp16_tie_distance(n) < 2.0**-22
+    nm = n16_g != n16_o
+    record(label, bits=bits, coords=int(mism.size), near_boundary=int(near.sum()), code_mismatch=int(mism.sum()),
+           vectors=int(nm.size), norm_near_tie=int(norm_near.sum()), norm_mismatch=int(nm.sum()))
     if mism.any():
         ym = y[mism]
         dist = np.min(np.abs(ym[:, None] - np.asarray(b32, np.float64)[None, :]), axis=-1)
@@ -51,9 +68,7 @@ def check_codes(gpu_blocks, bits, x, signs, b32, label=""):
         assert not far.any(), "%s: %d code mismatches far from a boundary, e.g. y=%s" % (
             label, far.sum(), ym[far][:4])
     assert mism.mean() < CODE_FRAC, "%s: code mismatch fraction %.2e" % (label, mism.mean())
-    nm = n16_g != n16_o
     if nm.any():
-        n = np.sqrt(np.sum(x * x, axis=-1))
         assert np.all(fp16_tie_distance(n[nm]) < 2.0**-22), "%s: norm mismatch away from a tie" % label
     assert nm.mean() < CODE_FRAC, "%s: norm mismatch fraction %.2e" % (label, nm.mean())
     return int(mism.sum()), int(nm.sum())

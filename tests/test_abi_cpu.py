@@ -80,6 +80,32 @@ def test_workspace_bytes(tq):
     assert tq.tq_attn_workspace_bytes(1, 1, 1, 64) <= tq.tq_attn_workspace_bytes(1, 1, 1, 4096)
 
 
+def _noalloc_limit():
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    m = re.search(r"#define TQ_ATTN_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    return int(m.group(1)) << int(m.group(2))
+
+
+@pytest.mark.parametrize("sms", [148, 152, 160])
+def test_noalloc_scratch_covers_the_documented_shapes(tq, sms):
+    """The shapes the header says fit tq_attn_decode_noalloc's fixed array
+    do fit (at short and very long contexts), and the one it says is
+    refused does not."""
+    f = tq.lib().tq_attn_workspace_bytes_sms
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 5
+    limit = _noalloc_limit()
+    assert limit == 16 << 20
+    for B, Hq, Hkv in ((64, 28, 4), (64, 32, 8), (128, 32, 8), (16, 32, 8), (8, 32, 8)):
+        for T_cap in (4096, 32776, 1 << 20):
+            need = f(B, Hq, Hkv, T_cap, sms)
+            assert 0 < need <= limit, (B, Hq, Hkv, T_cap, need)
+    assert f(256, 32, 8, 4096, sms) > limit
+    # the figures quoted in the header, to 0.1 MiB
+    for (B, Hq, Hkv), mib in (((64, 28, 4), 11.4), ((64, 32, 8), 9.2), ((128, 32, 8), 14.3), ((256, 32, 8), 24.4)):
+        assert abs(f(B, Hq, Hkv, 32776, sms) / 2**20 - mib) < 0.1
+
+
 def test_status_strings(tq):
     for s in (0, -1, -2, -3, -4, -5, 7):
         assert isinstance(tq.tq_status_string(s), str) and tq.tq_status_string(s)

@@ -20,7 +20,7 @@ import oracle
 from oracle import codec
 from turboquant_bit_kv_gb300 import workloads
 
-from parity_util import ATTN_TOL, attn_rel_err, check_codes, oracle_books
+from parity_util import ATTN_TOL, attn_rel_err, check_codes, oracle_books, record
 
 pytestmark = pytest.mark.gpu
 
@@ -274,8 +274,19 @@ def test_storage_roundtrip_fullsize(env):
     # the 4-bit codebook (inputs N(0, 1): E||x||^2 / d = 1)
     c, bd, _ = env["books"][4]
     expect_mse = D * oracle.beta_law_moments(c, bd, 64.0)
-    for layer in range(qs, qe):
+    per_layer = {}
+    for layer in range(L):
         for kv in (0, 1):
             xd = x[kv, layer].float()
-            mse = float(((y[kv, layer].float() - xd) ** 2).mean() / (xd * xd).mean())
-            assert abs(mse / expect_mse - 1) < 0.03, (layer, kv, mse, expect_mse)
+            per_layer[(layer, kv)] = float(((y[kv, layer].float() - xd) ** 2).mean() / (xd * xd).mean())
+    for layer in range(L):
+        record("storage mse layer %d" % layer, raw=int(layer < qs or layer >= qe),
+               mse_k="%.6f" % per_layer[(layer, 0)], mse_v="%.6f" % per_layer[(layer, 1)],
+               closed_form="%.6f" % (0.0 if layer < qs or layer >= qe else expect_mse))
+    for layer in range(L):
+        for kv in (0, 1):
+            mse = per_layer[(layer, kv)]
+            if layer < qs or layer >= qe:
+                assert mse == 0.0, (layer, kv, mse)
+            else:
+                assert abs(mse / expect_mse - 1) < 0.03, (layer, kv, mse, expect_mse)

@@ -263,13 +263,17 @@ static int attn_smem_bytes(int kb, int vb) {
 
 using namespace tq;
 
-extern "C" size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap) {
+extern "C" size_t tq_attn_workspace_bytes_sms(int B, int Hq, int Hkv, int T_cap, int sms) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv) return 0;
     int splits, tps;
     attn_split_plan(B, Hkv, T_cap, &splits, &tps);
     const int64_t split_floats = (int64_t)B * Hq * splits * kPartialFloats;
-    const int64_t mma_floats = mma_workspace_floats(B, Hq, Hkv, T_cap);
+    const int64_t mma_floats = mma_workspace_floats(B, Hq, Hkv, T_cap, sms);
     return (size_t)(split_floats > mma_floats ? split_floats : mma_floats) * sizeof(float);
+}
+
+extern "C" size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int T_cap) {
+    return tq_attn_workspace_bytes_sms(B, Hq, Hkv, T_cap, 0);
 }
 
 extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,

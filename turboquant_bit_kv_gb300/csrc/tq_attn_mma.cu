@@ -66,10 +66,10 @@ MmaPlan mma_plan_for(int sms, int B, int Hq, int Hkv, int T, int kb, int vb, boo
     return p;
 }
 
-int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap) {
+int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap, int sms) {
     const int64_t segs = (int64_t)B * Hkv;
     const int64_t C = (T_cap + kMmaChunk - 1) / kMmaChunk;
-    const int smax = mma_slots(segs, C, (int64_t)kMmaMaxWarpsPerSm * sm_count());
+    const int smax = mma_slots(segs, C, (int64_t)kMmaMaxWarpsPerSm * (sms > 0 ? sms : sm_count()));
     return (int64_t)B * Hq * smax * kPartialFloats + segs * kFragWords;
 }
 

@@ -41,8 +41,9 @@ struct MmaPlan {
 // (mma_plan uses the current device's).
 MmaPlan mma_plan_for(int sms, int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G);
 MmaPlan mma_plan(int B, int Hq, int Hkv, int T, int kb, int vb, bool qjl, int G);
-// Workspace floats the tensor-core path needs for any T <= T_cap.
-int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap);
+// Workspace floats the tensor-core path needs for any T <= T_cap on a GPU of
+// `sms` SMs (sms <= 0: the current device's).
+int64_t mma_workspace_floats(int B, int Hq, int Hkv, int T_cap, int sms);
 bool attn_mma_supported(int kb, int vb, bool qjl, int G);
 int launch_attn_mma(const AttnArgs &a, MmaPlan &plan, int kb, int vb, bool qjl, cudaStream_t st);
 

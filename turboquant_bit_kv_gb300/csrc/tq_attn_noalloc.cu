@@ -18,10 +18,13 @@
 // is only a stand-in), so the address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, on the first call made on
 // that device; that first call should therefore come before any stream
-// capture.  All calls share the one array and it keeps what the last call
-// wrote: nothing in it has to start at zero, because each call rewrites every
-// partial result it later reads, but calls that overlap on the GPU (other
-// streams, other threads) race on it.
+// capture.  The looked-up address is kept for the life of the process: after
+// a cudaDeviceReset (or anything else that destroys and re-creates the
+// device's primary context) the library must be loaded afresh before this
+// entry point is called again.  All calls share the one array and it keeps
+// what the last call wrote: nothing in it has to start at zero, because each
+// call rewrites every partial result it later reads, but calls that overlap
+// on the GPU (other streams, other threads) race on it.
 
 #include <mutex>
 
