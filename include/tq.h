@@ -22,6 +22,12 @@
  *     failed check returns a negative tq_status and enqueues nothing.  A CUDA
  *     launch error returns TQ_ERR_CUDA.  Nothing throws across this ABI and no
  *     kernel traps or asserts.
+ *   - Every wait inside a kernel (for a bulk or TMA copy, or a tensor-core
+ *     product) is bounded at about 0.1 s of device time.  A kernel whose wait
+ *     runs out stops issuing copies and waiting, lets the copies it already
+ *     issued land, finishes without hanging (its output is then invalid) and
+ *     records the event in a sticky per-device status that tq_device_status
+ *     returns as TQ_ERR_TIMEOUT.
  */
 #ifndef TQ_H
 #define TQ_H
@@ -39,7 +45,8 @@ typedef enum {
     TQ_ERR_UNSUPPORTED = -2,  /* head_dim != 128, bits not in {2,3,4}, dtype, G > 8 */
     TQ_ERR_ALIGN = -3,        /* a base pointer or stride breaks the stated alignment */
     TQ_ERR_WORKSPACE = -4,    /* workspace smaller than tq_attn_workspace_bytes() */
-    TQ_ERR_CUDA = -5          /* a CUDA runtime call or kernel launch failed */
+    TQ_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
+    TQ_ERR_TIMEOUT = -6       /* a kernel gave up a bounded wait (tq_device_status) */
 } tq_status;
 
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
@@ -257,6 +264,25 @@ int tq_serde_deserialize(const uint8_t *src, int elem_dtype, int num_layers, int
                          int skip_first, int skip_last,
                          const tq_codebook *kcb, const tq_codebook *vcb, tq_signs signs,
                          void *dst, void *stream);
+
+/* Sticky status of the kernels' bounded waits on the current device: waits
+ * for the work already enqueued on `stream` (cudaStreamSynchronize), then
+ * returns TQ_ERR_TIMEOUT if any kernel of this library gave up a wait on this
+ * device since the status was last cleared, else TQ_OK (TQ_ERR_CUDA if a
+ * CUDA call fails).  clear != 0 resets it.  Host call; it synchronises, so it
+ * belongs in diagnostics and tests rather than in a decode loop. */
+int tq_device_status(int clear, void *stream);
+
+/* Fault injection for tests of the bounded waits (the pages have no
+ * counterpart).  While on != 0, kernels launched afterwards with bounded
+ * waits (the tensor-core encode and QJL encode issue none of their TMA
+ * loads; the tensor-core attention sets up its copy barriers to wait for an
+ * arrival that never comes) find their first wait unsatisfiable, so it runs
+ * out after about 0.1 s, as it would for a copy that never lands; their
+ * outputs are then invalid and tq_device_status reports TQ_ERR_TIMEOUT.  No
+ * memory is touched outside the call's own buffers.  Host only; returns
+ * TQ_OK. */
+int tq_debug_drop_copies(int on);
 
 /* Static, human-readable name of a tq_status value. */
 const char *tq_status_string(int status);

@@ -28,7 +28,7 @@ from .codebook import lloyd_max, beta_codebook, gaussian_codebook, beta_law_mome
 from .rotation import hadamard, rotate, rotate_inverse
 from .codec import (block_bytes, quantize, encode, pack_block, unpack_block,
                     decode, decode_rotated, fp16_rne)
-from .attention import attention_dequantized, attention_rotated
+from .attention import attention_dequantized, attention_rotated, attention_causal
 from .qjl import qjl_encode, qjl_term2
 from .serde import serde_ranges, serde_size, serialize, deserialize
 
@@ -37,6 +37,6 @@ __all__ = [
     "gaussian_codebook", "beta_law_moments", "hadamard", "rotate",
     "rotate_inverse", "block_bytes", "quantize", "encode", "pack_block",
     "unpack_block", "decode", "decode_rotated", "fp16_rne",
-    "attention_dequantized", "attention_rotated", "qjl_encode", "qjl_term2",
+    "attention_dequantized", "attention_rotated", "attention_causal", "qjl_encode", "qjl_term2",
     "serde_ranges", "serde_size", "serialize", "deserialize",
 ]

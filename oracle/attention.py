@@ -78,3 +78,38 @@ def attention_rotated(q, k_idx, k_norm16, kc, v_idx, v_norm16, vc, signs, scale,
             p = _softmax_weights(scale * (kr @ q_rot[b, h]))
             out[b, h] = rotate_inverse((p @ vr)[None, :], signs)[0]
     return out
+
+
+def attention_causal(q, k_hat, v_hat, scale, seq_lens=None):
+    """Attention of several new query tokens per sequence over the cache
+    that already holds them (a prefill chunk, or the draft tokens of a
+    speculative verify step): the plain definition above with a causal mask.
+
+    The fork page's section 2 (Requirements) routes every quantised-KV
+    attention through the fused flash-attention path, prefill included; the
+    spec's Integration Points write each new token into the cache before the
+    attention over it.  Reading: the M query tokens of sequence b are the
+    last M tokens of its L_b cached ones, so query token i sits at position
+    p = L_b - M + i and attends to the keys at positions 0..p (p + 1 keys);
+    a query whose position is negative (L_b < M) attends to nothing and its
+    output is zero.
+
+    q [B, M, Hq, 128]; k_hat, v_hat [B, Hkv, T, 128] float64; seq_lens [B]
+    (None: T).  Returns o [B, M, Hq, 128] float64.
+    """
+    q = np.asarray(q, np.float64)
+    B, M, Hq, d = q.shape
+    Hkv, T = k_hat.shape[1], k_hat.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, M, Hq, d))
+    for b in range(B):
+        L = T if seq_lens is None else int(seq_lens[b])
+        for i in range(M):
+            p = L - M + i
+            if p < 0:
+                continue
+            for h in range(Hq):
+                kv = h // G
+                s = k_hat[b, kv, :p + 1] @ q[b, i, h]
+                out[b, i, h] = _softmax_weights(scale * s) @ v_hat[b, kv, :p + 1]
+    return out

@@ -107,7 +107,7 @@ def test_noalloc_scratch_covers_the_documented_shapes(tq, sms):
 
 
 def test_status_strings(tq):
-    for s in (0, -1, -2, -3, -4, -5, 7):
+    for s in (0, -1, -2, -3, -4, -5, -6, 7):
         assert isinstance(tq.tq_status_string(s), str) and tq.tq_status_string(s)
 
 

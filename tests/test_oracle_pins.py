@@ -314,6 +314,56 @@ def test_attention_special_cases(books):
     assert np.allclose(o3, np.repeat(vh.mean(axis=2), G, axis=1), atol=1e-13)
 
 
+def test_causal_attention_matches_torch_sdpa_with_mask(books):
+    """Multi-token (causal) attention against torch's scaled_dot_product_attention
+    with an explicit boolean mask built from the query positions, per
+    sequence, for ragged lengths."""
+    import torch
+    c = _small_cache(books, 4, 3, B=2, Hq=8, Hkv=2, T=41, seed=4)
+    kh, vh = _deq(c)
+    scale = 1 / np.sqrt(D)
+    M = 6
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((2, M, 8, D))
+    lens = np.array([41, 17])
+    got = oracle.attention_causal(q, kh, vh, scale, seq_lens=lens)
+    for b in range(2):
+        L = int(lens[b])
+        pos = L - M + np.arange(M)
+        mask = torch.from_numpy(np.arange(L)[None, :] <= pos[:, None])          # [M, L]
+        kt = torch.from_numpy(np.repeat(kh[b, :, :L], 4, axis=0))               # [Hq, L, D]
+        vt = torch.from_numpy(np.repeat(vh[b, :, :L], 4, axis=0))
+        qt = torch.from_numpy(q[b].transpose(1, 0, 2))                           # [Hq, M, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+        assert np.max(np.abs(ref.numpy().transpose(1, 0, 2) - got[b])) < 1e-12
+
+
+def test_causal_attention_special_cases(books):
+    c = _small_cache(books, 4, 2, B=2, Hq=8, Hkv=2, T=12, seed=5)
+    kh, vh = _deq(c)
+    scale = 0.2
+    rng = np.random.default_rng(2)
+    M = 12
+    q = rng.standard_normal((2, M, 8, D))
+    o = oracle.attention_causal(q, kh, vh, scale)
+    # the first position sees only the first key: its output is that value
+    assert np.allclose(o[:, 0], np.repeat(vh[:, :, 0], 4, axis=1), atol=1e-14)
+    # the last query token sees the whole cache: the decode attention of that token
+    dec = oracle.attention_dequantized(q[:, -1], kh, vh, scale)
+    assert np.allclose(o[:, -1], dec, atol=1e-14)
+    # causality: changing keys / values after a query's position leaves its output unchanged
+    kh2, vh2 = kh.copy(), vh.copy()
+    kh2[:, :, 7:] = rng.standard_normal(kh2[:, :, 7:].shape)
+    vh2[:, :, 7:] = rng.standard_normal(vh2[:, :, 7:].shape)
+    o2 = oracle.attention_causal(q, kh2, vh2, scale)
+    assert np.array_equal(o2[:, :7], o[:, :7])
+    assert not np.allclose(o2[:, 7:], o[:, 7:])
+    # fewer cached tokens than query tokens: the leading queries have no keys and give zeros
+    o3 = oracle.attention_causal(q, kh, vh, scale, seq_lens=np.array([5, 12]))
+    assert np.all(o3[0, :7] == 0) and np.allclose(o3[0, 7:], oracle.attention_causal(
+        q[:1, 7:], kh[:1, :, :5], vh[:1, :, :5], scale)[0], atol=1e-14)
+
+
 def test_attention_cosine_matches_pages_soft(books):
     # The spec's measured quality table (synthetic Gaussian): soft band 0.015.
     rng = np.random.default_rng(11)

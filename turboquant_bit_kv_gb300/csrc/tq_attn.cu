@@ -299,6 +299,7 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     if (workspace_bytes < tq_attn_workspace_bytes(B, Hq, Hkv, T_cap)) return TQ_ERR_WORKSPACE;
 
     AttnArgs a;
+    a.drop = drop_copies();
     a.q = q;
     a.q_dtype = q_dtype;
     a.k = k_blocks;

@@ -40,6 +40,7 @@ struct AttnArgs {
     float qscale;            // scale * log2(e)
     float kc[16], vc[16];
     uint32_t signs[4];
+    int drop;                // test hook: issue no bulk copies (the waits for them run out)
 };
 
 __host__ __device__ inline int attn_tiles(int T) { return (T + kTT - 1) / kTT; }

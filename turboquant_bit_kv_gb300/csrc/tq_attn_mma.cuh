@@ -211,8 +211,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 
 // Wait for the phase with parity `parity` to complete (bounded; false when
-// it gave up).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+// it gave up).  After a wait of this lane gave up (ok false) later waits make
+// a single attempt, so the loop runs on to its end without stalling.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool ok) {
+    return mbar_wait_bounded(bar, parity, ok ? 100000000ull : 0ull);
+}
 
 // Codes of the two dims of a table entry.  4-bit: entry = byte (low nibble
 // first dim); 2-bit: entry = nibble; 3-bit: entry = the pair's 2-bit-plane
@@ -398,8 +401,10 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
     const uint32_t stage_s = smem_s + C::kSmemStages + warp * kS * C::kWarpStage;
     const uint32_t bar_s = smem_s + C::kSmemBars + warp * 3 * 8;
     if (lane == 0) {
+        // (test hook: a second arrival that never comes keeps every phase from completing, so the
+        // first wait runs out while the copies still land)
 #pragma unroll
-        for (int s = 0; s < kS; ++s) mbar_init(bar_s + 8 * s, 1);
+        for (int s = 0; s < kS; ++s) mbar_init(bar_s + 8 * s, a.drop ? 2 : 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
         for (int ci = cb; ci < ce; ++ci) {
             issue_next();
             if (bulk_mask & (1u << cst)) {
-                copies_ok &= mbar_wait(bar_s + 8 * cst, (phase >> cst) & 1u);
+                copies_ok &= mbar_wait(bar_s + 8 * cst, (phase >> cst) & 1u, copies_ok);
                 phase ^= 1u << cst;
             } else {
                 cp_async_wait<0>();
@@ -790,6 +795,12 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                 }
             }
         }
+    }
+    if (!__all_sync(kFull, copies_ok)) {
+        // a wait gave up: the event is recorded, and copies this warp may still have in flight land
+        // before it exits (about 0.1 s)
+        if (lane == 0) note_wait_failed();
+        spin_ns(100000000ull);
     }
 }
 

@@ -25,4 +25,6 @@ int launch_attn_mma_k2(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int n
     return TQ_ERR_UNSUPPORTED;
 }
 
+int wait_failed_attn_k2(unsigned *v, bool clear) { return read_wait_failed(v, clear); }
+
 }  // namespace tq

@@ -268,12 +268,28 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
+// Sticky record of a bounded wait that gave up.  Each translation unit that
+// includes this header has its own word (there is no device-side linking
+// between units); the units whose kernels wait on mbarriers expose a host
+// reader of theirs, and tq_device_status combines them.
+static __device__ unsigned int g_tq_wait_failed;
+
+__device__ __forceinline__ void note_wait_failed() { atomicOr(&g_tq_wait_failed, 1u); }
+
+// Host: this unit's word on the current device (reset when `clear`).
+static inline int read_wait_failed(unsigned *v, bool clear) {
+    if (cudaMemcpyFromSymbol(v, g_tq_wait_failed, sizeof(unsigned)) != cudaSuccess) return TQ_ERR_CUDA;
+    const unsigned zero = 0;
+    if (clear && cudaMemcpyToSymbol(g_tq_wait_failed, &zero, sizeof(unsigned)) != cudaSuccess) return TQ_ERR_CUDA;
+    return TQ_OK;
+}
+
 // Wait for the phase of parity `parity` of the mbarrier at shared address
 // `bar`.  mbarrier.try_wait suspends the warp in hardware for a while instead
 // of spinning on issue slots; the wait gives up (false) after about 100 ms
 // of device time (or 2^22 attempts), so a copy that never lands cannot hang
 // the kernel.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {
     uint64_t t0 = 0;
     for (int i = 0; i < (1 << 22); ++i) {
         uint32_t done;
@@ -286,9 +302,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
         uint64_t now;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
         if (i == 0) t0 = now;
-        else if (now - t0 > 100000000ull) break;
+        else if (now - t0 > limit_ns) break;
     }
     return false;
+}
+
+// Spin for about `ns` of device time (the drain of a kernel whose wait gave up:
+// copies it may still have in flight land meanwhile).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    uint64_t t0, now;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+        __nanosleep(1000);
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+    } while (now - t0 < ns);
 }
 
 // 32-bit word at a 2-byte aligned shared-memory address.

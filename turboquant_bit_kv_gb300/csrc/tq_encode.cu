@@ -64,6 +64,7 @@ struct EncArgs {
     float grid;         // 3/4-bit: cells per unit of y
     float2 table[kBuckets];  // cell j: (boundary inside it in G*y units | +inf, bits of #boundaries below it)
     uint32_t signs[4];
+    int drop;           // test hook: the tensor-core kernel issues no TMA loads (its waits run out)
 };
 
 // Raw 64-element share of a row, as loaded (16-bit inputs: 8 chunks;
@@ -796,8 +797,8 @@ struct TcSmem {
     static constexpr int kTab = kOut + ((kTcRows * kSlotB + 15) & ~15);  // cell table, 128 x 8 B
     static constexpr int kPart = kTab + kBuckets * 8;                // per-row partial sums of squares, [2][128]
     static constexpr int kFix = kPart + 2 * kTcRows * 4;             // rows finished after the main loop
-    static constexpr int kBars = kFix + (4 + kTcFixCap) * 4;          // full[2], mma[2], empty[2]
-    static constexpr int kSlot = kBars + 6 * 8;                      // tensor-memory base address
+    static constexpr int kBars = kFix + (4 + kTcFixCap) * 4;          // full[2], mma[2], empty[2], drain
+    static constexpr int kSlot = kBars + 7 * 8;                      // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;                 // + alignment slack of the base
 };
 
@@ -937,6 +938,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc_mbar_init(bars + 16 + 8 * i, 1);            // mma: tcgen05.commit
             tc_mbar_init(bars + 32 + 8 * i, kTcEpiWarps);  // empty: one arrival per epilogue warp
         }
+        tc_mbar_init(bars + 48, 1);                        // drain: the producer's last tcgen05.commit
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -957,22 +959,41 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // ---- producer: row tiles by TMA, then eight MMAs into the stage's accumulator
         if (lane == 0) {
             const uint32_t idesc = tc_idesc<DT>();
+            // a wait that gives up is recorded and ends the producer's loop: no further load or
+            // product is issued (the epilogue's waits then give up too, or are skipped)
+            bool ok = true;
+            auto wait = [&](uint32_t bar, uint32_t parity) {
+                if (ok && !tc_mbar_wait(bar, parity)) {
+                    ok = false;
+                    note_wait_failed();
+                }
+            };
+            int pend_bar = -1;   // full barrier of a load not yet seen complete, and its parity
+            uint32_t pend_par = 0;
             int i = 0;
-            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
-            for (int half = 0; half < NH; ++half, ++i) {
+            for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x)
+            for (int half = 0; ok && half < NH; ++half, ++i) {
                 const int st = i & 1;
                 const uint32_t use = (uint32_t)(i >> 1);
-                if (i >= 2) tc_mbar_wait(bars + 32 + 8 * st, (use - 1u) & 1u);   // stage released
+                if (i >= 2) wait(bars + 32 + 8 * st, (use - 1u) & 1u);   // stage released
                 // PAIR: one row-tile buffer, free once the previous tile's MMAs have completed
-                if (PAIR && i >= 1) tc_mbar_wait(bars + 16 + 8 * (st ^ 1), (uint32_t)((i - 1) >> 1) & 1u);
+                if (PAIR && i >= 1) wait(bars + 16 + 8 * (st ^ 1), (uint32_t)((i - 1) >> 1) & 1u);
+                if (!ok) break;
                 tc_fence_after();
                 const int ab = PAIR ? 0 : st;   // row-tile buffer and its full barrier
                 const uint32_t a_s = base_s + S::kA + ab * kTcTileBytes, full = bars + 8 * ab;
                 const CUtensorMap *map = (PAIR && half) ? &tmap2 : &tmap;
-                tc_mbar_expect_tx(full, kTcTileBytes);
-                tc_tma_load_2d(a_s, map, 0, (int)(tile * kTcRows), full);
-                tc_tma_load_2d(a_s + 16384, map, 64, (int)(tile * kTcRows), full);
-                tc_mbar_wait(full, PAIR ? ((uint32_t)i & 1u) : (use & 1u));
+                const uint32_t fpar = PAIR ? ((uint32_t)i & 1u) : (use & 1u);
+                if (!a.drop) {   // (test hook: no load, so the wait below runs out)
+                    tc_mbar_expect_tx(full, kTcTileBytes);
+                    tc_tma_load_2d(a_s, map, 0, (int)(tile * kTcRows), full);
+                    tc_tma_load_2d(a_s + 16384, map, 64, (int)(tile * kTcRows), full);
+                    pend_bar = ab;
+                    pend_par = fpar;
+                }
+                wait(full, fpar);
+                if (!ok) break;   // no product on a tile that did not land
+                pend_bar = -1;
                 const uint32_t d = tmem + (uint32_t)(st * 128);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -981,6 +1002,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 }
                 tc_commit(bars + 16 + 8 * st);
             }
+            // before teardown: every product issued here has completed (one more commit, on a barrier
+            // of its own), and a load whose wait gave up has landed (bounded waits)
+            tc_commit(bars + 48);
+            tc_mbar_wait(bars + 48, 0u);
+            if (pend_bar >= 0) tc_mbar_wait(bars + 8 * pend_bar, pend_par);
         }
     } else {
         // ---- epilogue: warp w reads tensor-memory lanes (= tile rows) 32 (w & 3) .. + 31, columns
@@ -996,11 +1022,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // aligned run) leave by one bulk copy each
         const bool bulk_out = a.contiguous != 0 || a.idx_bulk != 0;
         const float2 off2 = make_float2(1572928.f, 1572928.f);   // 64 + 1.5 * 2^20
+        // a wait that gives up is recorded and not repeated: the loop still runs to its end (every
+        // named barrier is met), on an accumulator that is then not valid
+        bool ok = true;
         int i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
         for (int half = 0; half < NH; ++half, ++i) {
             const int st = i & 1;
-            tc_mbar_wait(bars + 16 + 8 * st, (uint32_t)(i >> 1) & 1u);
+            if (ok && !tc_mbar_wait(bars + 16 + 8 * st, (uint32_t)(i >> 1) & 1u)) {
+                ok = false;
+                note_wait_failed();
+            }
             tc_fence_after();
             const int64_t v0 = tile * kTcRows;
             const int nv = (int)min64(kTcRows, a.n_vec - v0);
@@ -1239,7 +1271,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
     }
 
-    // ---- teardown: every MMA was waited for and every tensor-memory load completed
+    // ---- teardown: every MMA has completed (the producer waited for its last commit) and every
+    // tensor-memory load completed
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1337,6 +1370,7 @@ extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x
         return TQ_ERR_ALIGN;
     EncArgs a;
     memset(&a, 0, sizeof(a));
+    a.drop = drop_copies();
     a.x = static_cast<const uint8_t *>(x);
     a.n_vec = n_vec;
     a.x_stride = x_stride_elems * es;
@@ -1365,6 +1399,8 @@ extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x
 
 namespace tq {
 
+int wait_failed_encode(unsigned *v, bool clear) { return read_wait_failed(v, clear); }
+
 // Paired encode for the storage layout: row i of k into bytes [0, BB) and row
 // i of v into bytes [BB, 2 BB) of slot i (slot = 2 BB bytes, contiguous), both
 // with codebook cb, so that every 32 slots leave as one bulk copy instead of
@@ -1381,6 +1417,7 @@ int encode_kv_pair(const void *k, const void *v, int x_dtype, int64_t n_vec, int
         return 1;
     EncArgs a;
     memset(&a, 0, sizeof(a));
+    a.drop = drop_copies();
     a.x = static_cast<const uint8_t *>(k);
     a.x2 = static_cast<const uint8_t *>(v);
     a.n_vec = n_vec;

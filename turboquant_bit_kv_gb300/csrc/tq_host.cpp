@@ -186,6 +186,7 @@ extern "C" const char *tq_status_string(int status) {
         case TQ_ERR_ALIGN: return "misaligned pointer or stride";
         case TQ_ERR_WORKSPACE: return "workspace too small";
         case TQ_ERR_CUDA: return "CUDA error";
+        case TQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait (its output is invalid)";
         default: return "unknown status";
     }
 }

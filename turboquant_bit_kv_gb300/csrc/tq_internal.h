@@ -41,6 +41,18 @@ int qjl_encode_tc(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_by
 int encode_kv_pair(const void *k, const void *v, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
                    const tq_codebook *cb, tq_signs signs, uint8_t *slots, cudaStream_t st);
 
+// Test hook (tq_debug_drop_copies): kernels with bounded waits issue none of
+// their bulk / TMA copies while this is set (tq_status.cu).
+int drop_copies();
+
+// Host readers of the bounded-wait failure word of the units whose kernels
+// wait on mbarriers (see tq_device.cuh).
+int wait_failed_encode(unsigned *v, bool clear);
+int wait_failed_qjl(unsigned *v, bool clear);
+int wait_failed_attn_k2(unsigned *v, bool clear);
+int wait_failed_attn_k3(unsigned *v, bool clear);
+int wait_failed_attn_k4(unsigned *v, bool clear);
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

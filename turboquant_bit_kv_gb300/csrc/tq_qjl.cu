@@ -52,6 +52,7 @@ struct QjlTcArgs {
     uint16_t *rn;           // [n_vec]
     float c[16];            // centroids
     uint32_t signs[4];
+    int drop;               // test hook: issue no TMA loads (the waits for them run out)
 };
 
 template <int BITS>
@@ -75,14 +76,15 @@ struct QjlSmem {
     static constexpr int kBlk = kA2 + 2 * kQTile;               // the tile's blocks
     static constexpr int kCtab = kBlk + ((kQRows * kPitch + 16 + 15) & ~15);   // (+ slack read by the last row)
     static constexpr int kPart = kCtab + kTabBytes;             // per-row partial sums of squares [2][slice][128]
-    static constexpr int kBars = kPart + 2 * kQSlices * kQRows * 4;   // 8 mbarriers
-    static constexpr int kSlot = kBars + 8 * 8;                 // tensor-memory base address
+    static constexpr int kBars = kPart + 2 * kQSlices * kQRows * 4;   // 9 mbarriers
+    static constexpr int kSlot = kBars + 9 * 8;                 // tensor-memory base address
     static constexpr int kTotal = kSlot + 16 + 1024;            // + alignment slack of the base
     static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
-// mbarriers: key tile landed, key tile consumed, U ready [2], U released [2], R r staged, P ready
-enum { kBarFull = 0, kBarXFree = 1, kBarURdy = 2, kBarUFree = 4, kBarA2 = 6, kBarP = 7 };
+// mbarriers: key tile landed, key tile consumed, U ready [2], U released [2], R r staged, P ready,
+// and the producer's last commit before teardown
+enum { kBarFull = 0, kBarXFree = 1, kBarURdy = 2, kBarUFree = 4, kBarA2 = 6, kBarP = 7, kBarDrain = 8 };
 
 __device__ __forceinline__ void sts128_q(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tc_mbar_init(bars + 8 * (kBarUFree + 1), kQEpiWarps);
         tc_mbar_init(bars + 8 * kBarA2, kQEpiWarps);
         tc_mbar_init(bars + 8 * kBarP, 1);
+        tc_mbar_init(bars + 8 * kBarDrain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -255,43 +258,58 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (lane == 0) {
             const uint32_t hd_s = base_s + Q::kHD, x_s = base_s + Q::kX, a2_s = base_s + Q::kA2;
             const uint32_t sh_s = base_s + Q::kSh, sl_s = base_s + Q::kSl;
-            auto load_x = [&](int64_t tile) {
+            // the key-tile load of parity `pend_par` not yet seen complete (-1: none)
+            int pend = -1;
+            uint32_t pend_par = 0;
+            auto load_x = [&](int64_t tile, uint32_t parity) {
+                if (a.drop) return;   // (test hook: no load, so the wait for it runs out)
                 tc_mbar_expect_tx(bars + 8 * kBarFull, kQTile);
                 tc_tma_load_2d(x_s, &tmap, 0, (int)(tile * kQRows), bars + 8 * kBarFull);
                 tc_tma_load_2d(x_s + 16384, &tmap, 64, (int)(tile * kQRows), bars + 8 * kBarFull);
+                pend = 1;
+                pend_par = parity;
             };
-            // a wait that gives up marks the CTA's work failed and is skipped from then on: the
-            // loops still run to the end (no thread is left waiting at a barrier)
+            // a wait that gives up is recorded and ends the producer's loop: no further load or
+            // product is issued (the epilogue's waits then give up too, or are skipped)
             bool ok = true;
             auto wait = [&](int b, uint32_t parity) {
-                if (ok) ok = tc_mbar_wait(bars + 8 * b, parity);
+                if (ok && !tc_mbar_wait(bars + 8 * b, parity)) {
+                    ok = false;
+                    note_wait_failed();
+                }
+                if (ok && b == kBarFull) pend = -1;
             };
             int64_t tile = blockIdx.x;
             if (tile < ntiles) {
-                load_x(tile);
+                load_x(tile, 0u);
                 wait(kBarFull, 0u);
-                tc_fence_after();
-                tc_mma_tile<DT>(tmem, x_s, hd_s, false);
-                tc_commit(bars + 8 * kBarURdy);
-                tc_commit(bars + 8 * kBarXFree);
+                if (ok) {
+                    tc_fence_after();
+                    tc_mma_tile<DT>(tmem, x_s, hd_s, false);
+                    tc_commit(bars + 8 * kBarURdy);
+                    tc_commit(bars + 8 * kBarXFree);
+                }
             }
-            for (int i = 0; tile < ntiles; ++i, tile += gridDim.x) {
+            for (int i = 0; ok && tile < ntiles; ++i, tile += gridDim.x) {
                 const int64_t next = tile + gridDim.x;
                 // U of the next tile is issued as soon as its keys have landed (while the epilogue
                 // still forms R r of tile i), so that the epilogue finds it ready; P of tile i
                 // follows and runs while the epilogue packs signs and starts the next tile
                 if (next < ntiles) {
                     wait(kBarXFree, (uint32_t)i & 1u);   // U of tile i has read X
-                    load_x(next);
+                    if (!ok) break;
                     const int n1 = i + 1, st = n1 & 1;
+                    load_x(next, (uint32_t)n1 & 1u);
                     wait(kBarFull, (uint32_t)n1 & 1u);
                     if (n1 >= 2) wait(kBarUFree + st, (uint32_t)((n1 >> 1) - 1) & 1u);
+                    if (!ok) break;
                     tc_fence_after();
                     tc_mma_tile<DT>(tmem + (uint32_t)(st * 128), x_s, hd_s, false);
                     tc_commit(bars + 8 * (kBarURdy + st));
                     tc_commit(bars + 8 * kBarXFree);
                 }
                 wait(kBarA2, (uint32_t)i & 1u);          // R r of tile i staged
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t p_t = tmem + 256u + 128u * (uint32_t)(i & 1);   // P double-buffered
                 tc_mma_tile<TQ_F16>(p_t, a2_s, sh_s, false);
@@ -299,6 +317,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 tc_mma_tile<TQ_F16>(p_t, a2_s + kQTile, sh_s, true);
                 tc_commit(bars + 8 * kBarP);
             }
+            // before teardown: every product issued here has completed (one more commit, on a barrier
+            // of its own), and a load whose wait gave up has landed (bounded waits)
+            tc_commit(bars + 8 * kBarDrain);
+            tc_mbar_wait(bars + 8 * kBarDrain, 0u);
+            if (pend >= 0) tc_mbar_wait(bars + 8 * kBarFull, pend_par);
         }
     } else {
         // ---- epilogue: warp w owns tensor-memory lanes (= tile rows) 32 (w & 3) .. + 31 and columns
@@ -355,9 +378,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         };
         auto grp_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(grp_bar), "n"(32 * kQSlices) : "memory"); };
         prefetch(blockIdx.x);
-        bool ok = true;   // as in the producer: a wait that gave up is not repeated, the loop runs on
+        // a wait that gives up is recorded and not repeated: the loop still runs to its end (every
+        // named barrier is met), on products that are then not valid
+        bool ok = true;
         auto wait = [&](int b, uint32_t parity) {
-            if (ok) ok = tc_mbar_wait(bars + 8 * b, parity);
+            if (ok && !tc_mbar_wait(bars + 8 * b, parity)) {
+                ok = false;
+                note_wait_failed();
+            }
         };
         // signs of P = S r for tile j (this slice): bit k of the row's 128 = [(S r)_k >= 0]; run one
         // tile late, so that the tensor cores compute P of tile j + 1 meanwhile
@@ -497,7 +525,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
     }
 
-    // ---- teardown: every MMA was waited for and every tensor-memory load completed
+    // ---- teardown: every MMA has completed (the producer waited for its last commit) and every
+    // tensor-memory load completed
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -518,6 +547,8 @@ int launch_qjl_tc(const CUtensorMap &map, const QjlTcArgs &a, cudaStream_t st) {
 
 }  // namespace
 
+int wait_failed_qjl(unsigned *v, bool clear) { return read_wait_failed(v, clear); }
+
 int qjl_encode_tc(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_bytes, const uint8_t *blocks,
                   int64_t block_stride, int bits, const float *centroids, const uint32_t *signs, const float *S,
                   uint8_t *qjl_bits, uint16_t *res_norm_f16, cudaStream_t st) {
@@ -525,6 +556,7 @@ int qjl_encode_tc(const void *k, int k_dtype, int64_t n_vec, int64_t k_stride_by
     CUtensorMap map;
     if (!make_row_tile_map(&map, k, k_dtype, n_vec, k_stride_bytes)) return 1;
     QjlTcArgs a;
+    a.drop = drop_copies();
     a.blocks = blocks;
     a.block_stride = block_stride;
     a.dense = block_stride == 2 + 16 * bits && (reinterpret_cast<uintptr_t>(blocks) & 15) == 0 ? 1 : 0;

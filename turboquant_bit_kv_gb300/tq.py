@@ -15,7 +15,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtq.so")
 
-TQ_OK, TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_WORKSPACE, TQ_ERR_CUDA = 0, -1, -2, -3, -4, -5
+TQ_OK, TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_WORKSPACE, TQ_ERR_CUDA, TQ_ERR_TIMEOUT = \
+    0, -1, -2, -3, -4, -5, -6
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 _DT = {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16, torch.float16: TQ_F16}
 
@@ -64,6 +65,10 @@ def lib():
         ser = [vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, cbp, cbp, tq_signs, vp, vp]
         L.tq_serde_serialize.argtypes = ser
         L.tq_serde_deserialize.argtypes = ser
+        L.tq_device_status.argtypes = [c_int, vp]
+        L.tq_debug_drop_copies.argtypes = [c_int]
+        L.tq_attn_workspace_bytes_sms.argtypes = [c_int] * 5
+        L.tq_attn_workspace_bytes_sms.restype = sz
         L.tq_status_string.argtypes = [c_int]
         L.tq_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -220,3 +225,19 @@ def tq_serde_deserialize(src, kcb, vcb, signs, dst, block_size=16, skip_first=2,
                                       skip_last, ctypes.byref(kcb), ctypes.byref(vcb), signs, _ptr(dst),
                                       _stream(stream)), "tq_serde_deserialize")
     return dst
+
+
+def tq_device_status(clear=False, stream=None):
+    """Sticky status of the kernels' bounded waits on the current device
+    (TQ_OK or TQ_ERR_TIMEOUT; returned, not raised).  Synchronises the stream."""
+    return int(lib().tq_device_status(1 if clear else 0, _stream(stream)))
+
+
+def tq_debug_drop_copies(on):
+    """Test hook: while on, kernels with bounded waits issue no copies, so
+    their waits run out (include/tq.h)."""
+    _check(lib().tq_debug_drop_copies(1 if on else 0), "tq_debug_drop_copies")
+
+
+def tq_attn_workspace_bytes_sms(B, Hq, Hkv, T_cap, sms):
+    return int(lib().tq_attn_workspace_bytes_sms(B, Hq, Hkv, T_cap, sms))
