@@ -199,6 +199,31 @@ int tq_attn_decode(const void *q, int q_dtype,
                    const uint8_t *qjl_bits, const uint16_t *res_norm_f16, const float *S,
                    float *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Attention of M new query tokens per sequence over a packed cache that
+ * already holds them, with the causal mask: a prefill chunk, or the draft
+ * tokens of a speculative verify step ([fork] section 2, Requirements: the
+ * quantised cache is reachable only through the fused flash-attention path;
+ * [spec] Optimization: Fused dequant-dot for the rotated-domain scores and
+ * value sums).  Query token i of sequence b sits at position
+ * p = L_b - M + i (L_b its length) and attends to the keys at positions
+ * 0 .. p:
+ *   s_t = scale * n_t * <R q, cK[code_t]>,  o = sum_{t <= p} softmax(s)_t v_hat_t,
+ * a query with p < 0 gives a zero output row.
+ *   q         device [B][M][Hq][128] of q_dtype (TQ_F32 / TQ_BF16 / TQ_F16).
+ *   k_blocks  device [B][Hkv][T_cap] blocks of kcb->bits; v_blocks the same
+ *             for vcb->bits (packed values only).
+ *   seq_lens  device int32 [B] (each clamped to [0, T]) or NULL for T.
+ *   Hq % Hkv == 0 (query head h reads KV head h / (Hq / Hkv)); 1 <= T <=
+ *   T_cap, T_cap a multiple of 8; q, k_blocks, v_blocks, out 16-byte aligned.
+ *   out       device float32 [B][M][Hq][128].
+ * No workspace.  Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN,
+ * TQ_ERR_CUDA. */
+int tq_attn_prefill(const void *q, int q_dtype,
+                    const uint8_t *k_blocks, const tq_codebook *kcb,
+                    const uint8_t *v_blocks, const tq_codebook *vcb,
+                    const int32_t *seq_lens, int B, int M, int Hq, int Hkv, int T_cap, int T,
+                    float scale, tq_signs signs, float *out, void *stream);
+
 /* Size of the device array that tq_attn_decode_noalloc uses as its split-K
  * scratch: 16 MiB.  On GPUs of 148 to 160 SMs that covers, at any context,
  * batch 64 x 28 query heads over 4 KV heads (about 11.4 MiB), batch 64 x 32

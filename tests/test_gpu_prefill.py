@@ -1,0 +1,104 @@
+"""GPU parity of the multi-token (causal) attention over packed caches
+(tq_attn_prefill, tensor cores): the oracle's brute-force causal attention
+on identical packed caches made by the oracle's encoder, per output vector
+max |o - o_ref| / max |o_ref| <= 1e-3."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import codec
+from turboquant_bit_kv_gb300 import workloads
+
+from parity_util import ATTN_TOL, attn_rel_err, oracle_books
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from turboquant_bit_kv_gb300 import tq
+    tq.lib()
+    return dict(tq=tq, dev=torch.device("cuda:0"), books=oracle_books(),
+                cbs={b: tq.tq_codebook_load(128, b) for b in (2, 3, 4)},
+                signs=tq.tq_signs_from_seed(workloads.SIGN_SEED), s=oracle.sign_diagonal(workloads.SIGN_SEED))
+
+
+def _cache(env, x, bits):
+    """Oracle blocks and reconstructions of x float64 [B, H, T, 128]."""
+    B, H, T, _ = x.shape
+    c, _, b32 = env["books"][bits]
+    idx, n16, _ = codec.encode(x.reshape(-1, D), env["s"], b32)
+    return (codec.pack_block(idx, n16, bits).reshape(B, H, T, -1),
+            codec.decode(idx, n16, c, env["s"]).reshape(B, H, T, D))
+
+
+def _run(env, q, kblk, vblk, kbits, vbits, T, T_cap, scale, lens=None):
+    tq, dev = env["tq"], env["dev"]
+    B, Hkv = kblk.shape[:2]
+    M, Hq = q.shape[1], q.shape[2]
+    kb = torch.zeros((B, Hkv, T_cap, kblk.shape[-1]), dtype=torch.uint8)
+    kb[:, :, :T] = torch.from_numpy(kblk)
+    vb = torch.zeros((B, Hkv, T_cap, vblk.shape[-1]), dtype=torch.uint8)
+    vb[:, :, :T] = torch.from_numpy(vblk)
+    n = B * M * Hq * D
+    out_full = torch.full((n + 32,), 7.0, dtype=torch.float32, device=dev)
+    out = out_full[16:16 + n].view(B, M, Hq, D)
+    sl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
+    tq.tq_attn_prefill(q.to(dev), kb.to(dev), env["cbs"][kbits], vb.to(dev), env["cbs"][vbits], out, T, scale,
+                       env["signs"], seq_lens=sl)
+    torch.cuda.synchronize()
+    o = out_full.cpu().numpy()
+    assert np.all(o[:16] == 7.0) and np.all(o[-16:] == 7.0)
+    return out.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("B,M,Hq,Hkv,T,T_cap,kbits,vbits,lens,qdt", [
+    (2, 16, 8, 2, 300, 304, 4, 2, None, torch.float32),            # one row tile, a ragged key tile
+    (2, 16, 8, 2, 300, 304, 4, 2, [300, 150], torch.bfloat16),     # ragged lengths
+    (1, 24, 28, 4, 257, 264, 3, 3, None, torch.bfloat16),          # 7 heads per KV head: 168 rows, two row tiles
+    (3, 20, 8, 4, 200, 200, 4, 4, [200, 7, 64], torch.float16),    # a sequence shorter than M: zero rows
+    (2, 1, 32, 8, 129, 136, 3, 2, [129, 65], torch.bfloat16),      # one query token: the decode case
+    (1, 64, 32, 8, 1000, 1000, 4, 2, None, torch.bfloat16),        # 256 rows per KV head, 16 key tiles
+])
+def test_prefill_matches_oracle(env, B, M, Hq, Hkv, T, T_cap, kbits, vbits, lens, qdt):
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=30 + M)
+    kblk, khat = _cache(env, w["k"].double().numpy(), kbits)
+    vblk, vhat = _cache(env, w["v"].double().numpy(), vbits)
+    q = torch.randn((B, M, Hq, D), generator=torch.Generator().manual_seed(M + Hq), dtype=torch.float32).to(qdt)
+    scale = 1 / np.sqrt(D)
+    got = _run(env, q, kblk, vblk, kbits, vbits, T, T_cap, scale, lens)
+    ref = oracle.attention_causal(q.double().numpy(), khat, vhat, scale, seq_lens=lens)
+    err = attn_rel_err(got.reshape(-1, D), ref.reshape(-1, D))
+    assert np.all(err < ATTN_TOL), err.max()
+    if lens is not None:
+        for b, L in enumerate(lens):
+            assert np.all(got[b, :max(0, M - L)] == 0)   # queries before the first cached token
+
+
+def test_prefill_decode_agreement(env):
+    """With one query token the causal attention is the decode attention:
+    the two entry points agree on the same cache."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T = 2, 16, 4, 777
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=3)
+    kblk, _ = _cache(env, w["k"].double().numpy(), 4)
+    vblk, _ = _cache(env, w["v"].double().numpy(), 2)
+    scale = 1 / np.sqrt(D)
+    got = _run(env, w["q"][:, None], kblk, vblk, 4, 2, T, 784, scale)
+    kb = torch.zeros((B, Hkv, 784, 66), dtype=torch.uint8)
+    kb[:, :, :T] = torch.from_numpy(kblk)
+    vb = torch.zeros((B, Hkv, 784, 34), dtype=torch.uint8)
+    vb[:, :, :T] = torch.from_numpy(vblk)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, 784), dtype=torch.uint8, device=dev)
+    tq.tq_attn_decode(w["q"].to(dev), kb.to(dev), env["cbs"][4], vb.to(dev), env["cbs"][2], out, ws, T, scale,
+                      env["signs"])
+    torch.cuda.synchronize()
+    err = attn_rel_err(got[:, 0].reshape(-1, D), out.double().cpu().numpy().reshape(-1, D))
+    assert np.all(err < 2 * ATTN_TOL), err.max()

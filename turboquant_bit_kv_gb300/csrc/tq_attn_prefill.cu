@@ -1,0 +1,661 @@
+// tq_attn_prefill: attention of several new query tokens per sequence (a
+// prefill chunk, or the draft tokens of a speculative verify step) over a
+// packed cache that already holds them, with the causal mask, on the
+// 5th-generation tensor cores.
+//
+// "TurboQuant KV Cache (turboq2 / turboq3 / turboq4)", section 2
+// (Requirements): the quantised KV cache is reachable only through the fused
+// flash-attention path, prefill included; "TurboQuant KV Cache Compression —
+// Spec", Optimization: Fused dequant-dot: the query is rotated once, keys are
+// scored as norm x centroid in the rotated domain, values are accumulated in
+// the rotated domain and the output is rotated back once.  With M query
+// tokens and G query heads per KV head, the M x G query rows of a (sequence,
+// KV head) meet every key, so the scores and the value sums are dense
+// contractions: a CTA takes 128 of those rows and streams the keys in tiles
+// of 64.
+//
+//   S[128 rows x 64 keys]  = Q[128 x 128 dims] K^T         (tcgen05, 3 products)
+//   O[128 rows x 128 dims] += P[128 x 64 keys] V[64 x 128]  (tcgen05, 2 products)
+//
+// Precision as in the decode kernel: the rotated, scaled query, the key
+// centroids and the probabilities are split x = hi + lo into fp16 halves
+// (products hi.hi + hi.lo + lo.hi, float32 accumulate in tensor memory); the
+// value centroids are single fp16.  Key norms scale the scores, value norms
+// scale the probabilities.
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-3  row warps: thread r owns query row r = tensor-memory lane r.
+//              Prologue: rotated query rows into the A tiles.  Per key tile:
+//              read S, apply key norms and the causal mask, online softmax
+//              (the reference maximum moves only when a row's maximum
+//              exceeds it by more than 8 in log2 units, so that the
+//              accumulator in tensor memory is rarely rescaled), write P
+//              (times the value norms) as fp16 hi / lo tiles.  Epilogue:
+//              O / l, inverse rotation, store.
+//   warps 4-7  key warps: thread (k, h) dequantises half h of key k of the
+//              tile into the K hi / lo tiles and the V tile (centroid lookups
+//              in lane-replicated tables).
+//   warp 8     producer: bulk copies of the tile's packed K and V blocks.
+//   warp 9     one thread issues the tensor-core products.
+// Key tiles and their packed blocks are double-buffered, as are the score
+// accumulators, so the products of tile j + 1 run while the row warps work on
+// tile j.  Every mbarrier wait is bounded; a wait that gives up is recorded
+// (tq_device_status) and the roles run their loops to the end without further
+// waits or issues.
+
+#include <cmath>
+
+#include "tq_internal.h"
+#include "tq_tc.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kPfRows = 128;                 // query rows per CTA (MMA M, tensor-memory lanes)
+constexpr int kPfKeys = 64;                  // keys per tile (N of the scores, K of P V)
+constexpr int kPfThreads = 320;
+constexpr uint32_t kPfCols = 256;            // tensor memory: S[2] (64 columns each) + O (128)
+constexpr uint32_t kPfColO = 128;
+
+// Shared memory (offsets from a 1024-byte aligned base).  Operand tiles use the
+// K-major 128-byte swizzle of tq_tc.cuh: 64-element blocks of rows x 128 bytes.
+struct PfSmem {
+    static constexpr int kQhi = 0;                         // Q hi: 128 rows x 128 dims (two 16 KB blocks)
+    static constexpr int kQlo = 32768;
+    static constexpr int kKhi = 65536;                     // [2] keys: 64 rows x 128 dims (two 8 KB blocks)
+    static constexpr int kKlo = 98304;                     // [2]
+    static constexpr int kV = 131072;                      // [2] values: 64 keys x 128 dims, same layout
+    static constexpr int kPhi = 163840;                    // P hi: 128 rows x 64 keys (one 16 KB block)
+    static constexpr int kPlo = 180224;
+    static constexpr int kBlk = 196608;                    // [2] packed blocks: 64 K blocks | 64 V blocks
+    static constexpr int kBlkBytes = 8448;                 // 64 x 66 x 2
+    static constexpr int kNorm = kBlk + 2 * kBlkBytes;     // [2] kn[64] | vn[64] (float)
+    static constexpr int kKTab = kNorm + 2 * 512;          // key centroids: 16 codes x 32 lanes x half2 (hi, lo)
+    static constexpr int kVTab = kKTab + 2048;             // value centroids: 16 codes x 32 lanes x half2 (v, v)
+    static constexpr int kBars = kVTab + 2048;             // 16 mbarriers
+    static constexpr int kSlot = kBars + 16 * 8;           // tensor-memory base address, failure flag
+    static constexpr int kTotal = kSlot + 16 + 1024;       // + alignment slack of the base
+    static_assert(kTotal <= 232448, "shared memory of one CTA");
+};
+
+// mbarriers
+enum {
+    kBlkFull = 0,    // [2] packed blocks landed (bulk copy bytes)
+    kBlkEmpty = 2,   // [2] packed blocks read (4 key warps)
+    kKvReady = 4,    // [2] K / V tiles written (4 key warps)
+    kKvFree = 6,     // [2] the products that read the K / V tiles completed (commit)
+    kSReady = 8,     // [2] scores in tensor memory (commit)
+    kSFree = 10,     // [2] scores read (4 row warps)
+    kPReady = 12,    // P written, O rescaled if needed (4 row warps)
+    kPvDone = 13,    // P V completed: P free, O current (commit)
+    kDrain = 14      // the issuing thread's last commit before teardown
+};
+
+struct PfArgs {
+    const void *q;          // [B][M][Hq][128]
+    const uint8_t *k;       // [B][Hkv][T_cap] key blocks
+    const uint8_t *v;       // [B][Hkv][T_cap] value blocks
+    const int32_t *seq_lens;
+    float *out;             // [B][M][Hq][128]
+    int q_dtype, B, M, Hq, Hkv, G, T_cap, T, kbb, vbb, row_tiles;
+    float qscale;           // scale * log2(e)
+    float kc[16], vc[16];
+    uint32_t signs[4];
+    int drop;               // test hook: issue no bulk copies (the waits for them run out)
+};
+
+__device__ __forceinline__ uint64_t pf_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: float32 accumulator, fp16 A and B, A
+// K-major, B K-major (tb = 0) or MN-major (tb = 1), M = 128, N = n.
+__host__ __device__ constexpr uint32_t pf_idesc(uint32_t n, uint32_t tb) {
+    return (1u << 4) | (tb << 16) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void pf_sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void pf_bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+        "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+        "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+        "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pf_lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t pf_lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t pf_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pf_pack(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Code words of dims 64 h .. 64 h + 63 of the block at shared address `blk`
+// (2-byte aligned): 4-bit: 8 words; 2-bit: 4 words; 3-bit: 4 low-plane words
+// then 2 high-plane words.
+template <int BITS>
+__device__ __forceinline__ void pf_code_words(uint32_t blk, int h, uint32_t (&w)[8]) {
+    if constexpr (BITS == 4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pf_lds16(blk + 2 + 32 * h + 4 * i) | (pf_lds16(blk + 4 + 32 * h + 4 * i) << 16);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = pf_lds16(blk + 2 + 16 * h + 4 * i) | (pf_lds16(blk + 4 + 16 * h + 4 * i) << 16);
+        if constexpr (BITS == 3) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                w[4 + i] = pf_lds16(blk + 34 + 8 * h + 4 * i) | (pf_lds16(blk + 36 + 8 * h + 4 * i) << 16);
+        }
+    }
+}
+
+// Code of relative dim e (0..63) from the words above.
+template <int BITS>
+__device__ __forceinline__ uint32_t pf_code(const uint32_t (&w)[8], int e) {
+    if constexpr (BITS == 4) return (w[e >> 3] >> (4 * (e & 7))) & 15u;
+    else if constexpr (BITS == 2) return (w[e >> 4] >> (2 * (e & 15))) & 3u;
+    else return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[4 + (e >> 5)] >> (e & 31)) & 1u) << 2);
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __grid_constant__ PfArgs a) {
+    using S = PfSmem;
+    extern __shared__ __align__(16) uint8_t pf_smem_raw[];
+    const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(pf_smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *smem = pf_smem_raw + (base_s - raw_s);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bars = base_s + S::kBars;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    volatile int *fail_s = reinterpret_cast<volatile int *>(smem + S::kSlot + 4);
+
+    // ---- the CTA's rows and key range
+    const int rt = blockIdx.x % a.row_tiles;
+    const int seg = blockIdx.x / a.row_tiles;
+    const int b = seg / a.Hkv, kvh = seg % a.Hkv;
+    int L = a.T;
+    if (a.seq_lens) {
+        const int sl = a.seq_lens[b];
+        L = sl < 0 ? 0 : (sl > a.T ? a.T : sl);
+    }
+    const int rows_total = a.M * a.G;
+    const int r0 = rt * kPfRows;
+    const int i_hi = min(a.M - 1, (min(r0 + kPfRows, rows_total) - 1) / a.G);
+    const int p_max = L - a.M + i_hi;                      // last key any row of the CTA sees
+    const int n_tiles = p_max < 0 ? 0 : (p_max + kPfKeys) / kPfKeys;
+    const int n_keys8 = p_max < 0 ? 0 : ((p_max + 8) & ~7);   // keys copied, a multiple of 8 (<= T_cap)
+
+    // ---- setup: centroid tables, rotated query rows, barriers, tensor memory
+    for (int q = tid; q < 16 * 32; q += kPfThreads) {
+        const int e = q >> 5, l = q & 31;
+        const float c = a.kc[e];
+        const __half h = __float2half_rn(c);
+        const __half lo = __float2half_rn(c - __half2float(h));
+        *reinterpret_cast<__half2 *>(smem + S::kKTab + e * 128 + l * 4) = __halves2half2(h, lo);
+        const __half vh = __float2half_rn(a.vc[e]);
+        *reinterpret_cast<__half2 *>(smem + S::kVTab + e * 128 + l * 4) = __halves2half2(vh, vh);
+    }
+    // query rows: one warp per row; lane holds dims 4 lane .. + 3; R q = H (D q) / sqrt(128), times scale log2(e)
+    for (int r = warp; r < kPfRows; r += kPfThreads / 32) {
+        const int rg = r0 + r;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (rg < rows_total) {
+            const int i = rg / a.G, hq = kvh * a.G + rg % a.G;
+            const int64_t base = (((int64_t)b * a.M + i) * a.Hq + hq) * kD + 4 * lane;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float x;
+                if (a.q_dtype == TQ_F32) x = reinterpret_cast<const float *>(a.q)[base + k];
+                else if (a.q_dtype == TQ_BF16) x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.q)[base + k]);
+                else x = __half2float(reinterpret_cast<const __half *>(a.q)[base + k]);
+                const int d = 4 * lane + k;
+                v[k] = ((a.signs[d >> 5] >> (d & 31)) & 1u) ? -x : x;
+            }
+        }
+        const float x0 = v[0] + v[1], x1 = v[0] - v[1], x2 = v[2] + v[3], x3 = v[2] - v[3];
+        v[0] = x0 + x2;
+        v[2] = x0 - x2;
+        v[1] = x1 + x3;
+        v[3] = x1 - x3;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[k], m);
+                v[k] = (lane & m) ? (o - v[k]) : (v[k] + o);
+            }
+        }
+        const float f = a.qscale * 0.08838834764831845f;
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float e0 = v[2 * k] * f, e1 = v[2 * k + 1] * f;
+            const __half h0 = __float2half_rn(e0), h1 = __float2half_rn(e1);
+            hi[k] = pf_pack(__half2float(h0), __half2float(h1));
+            lo[k] = pf_pack(e0 - __half2float(h0), e1 - __half2float(h1));
+        }
+        // dims 4 lane .. + 3: block lane >> 4, 16-byte chunk (lane & 15) >> 1, half of it lane & 1
+        const int off = (lane >> 4) * 16384 + r * 128 + ((((lane & 15) >> 1) ^ (r & 7)) << 4) + (lane & 1) * 8;
+        *reinterpret_cast<uint2 *>(smem + S::kQhi + off) = make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2 *>(smem + S::kQlo + off) = make_uint2(lo[0], lo[1]);
+    }
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            tc_mbar_init(bar(kBlkFull + s), 1);
+            tc_mbar_init(bar(kBlkEmpty + s), 4);
+            tc_mbar_init(bar(kKvReady + s), 4);
+            tc_mbar_init(bar(kKvFree + s), 1);
+            tc_mbar_init(bar(kSReady + s), 1);
+            tc_mbar_init(bar(kSFree + s), 4);
+        }
+        tc_mbar_init(bar(kPReady), 4);
+        tc_mbar_init(bar(kPvDone), 1);
+        tc_mbar_init(bar(kDrain), 1);
+        *fail_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base_s + S::kSlot),
+                     "r"(kPfCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // the query tiles were written by ordinary stores and are read by the tensor cores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kSlot);
+
+    // a bounded wait; one that gives up is recorded, and the caller's role makes no further waits
+    auto wait = [&](bool &ok, int b_idx, uint32_t parity) {
+        if (ok && !tc_mbar_wait(bar(b_idx), parity)) {
+            ok = false;
+            *fail_s = 1;
+            note_wait_failed();
+        }
+    };
+
+    if (warp == 8) {
+        // ---- producer: packed K and V blocks of each tile
+        if (lane == 0) {
+            bool ok = true;
+            const int64_t row0 = (int64_t)seg * a.T_cap;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int s = j & 1, u = j >> 1;
+                if (u >= 1) wait(ok, kBlkEmpty + s, (uint32_t)(u - 1) & 1u);
+                if (!ok) break;
+                const int t0 = j * kPfKeys;
+                const int nk = min(kPfKeys, n_keys8 - t0);
+                const uint32_t dst = base_s + S::kBlk + s * S::kBlkBytes;
+                if (!a.drop) {   // (test hook: no copy, so the key warps' wait runs out)
+                    tc_mbar_expect_tx(bar(kBlkFull + s), (uint32_t)(nk * (a.kbb + a.vbb)));
+                    pf_bulk_g2s(dst, a.k + (row0 + t0) * a.kbb, (uint32_t)(nk * a.kbb), bar(kBlkFull + s));
+                    pf_bulk_g2s(dst + kPfKeys * a.kbb, a.v + (row0 + t0) * a.vbb, (uint32_t)(nk * a.vbb),
+                                bar(kBlkFull + s));
+                }
+            }
+        }
+    } else if (warp == 9) {
+        // ---- the tensor-core products
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t id_s = pf_idesc(kPfKeys, 0), id_pv = pf_idesc(128, 1);
+            auto scores = [&](int j) {
+                const int s = j & 1;
+                const uint32_t d = tmem + (uint32_t)(s * kPfKeys);
+                const uint32_t kh = base_s + S::kKhi + s * 16384, kl = base_s + S::kKlo + s * 16384;
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    const uint32_t qa = base_s + (part == 2 ? S::kQlo : S::kQhi);
+                    const uint32_t kb = part == 1 ? kl : kh;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t qo = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
+                        const uint32_t ko = (uint32_t)((ks >> 2) * 8192 + (ks & 3) * 32);
+                        tc_mma(d, pf_desc(qa + qo, 16, 1024), pf_desc(kb + ko, 16, 1024), id_s,
+                               (part > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                tc_commit(bar(kSReady + s));
+            };
+            auto values = [&](int j) {
+                const int s = j & 1;
+                const uint32_t vs = base_s + S::kV + s * 16384;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t pa = base_s + (part ? S::kPlo : S::kPhi);
+#pragma unroll
+                    for (int ks = 0; ks < kPfKeys / 16; ++ks)
+                        tc_mma(tmem + kPfColO, pf_desc(pa + ks * 32, 16, 1024), pf_desc(vs + ks * 2048, 8192, 1024),
+                               id_pv, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(kPvDone));
+                tc_commit(bar(kKvFree + s));
+            };
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int s = j & 1, u = j >> 1;
+                wait(ok, kKvReady + s, (uint32_t)u & 1u);
+                if (u >= 1) wait(ok, kSFree + s, (uint32_t)(u - 1) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                scores(j);
+                if (j >= 1) {
+                    wait(ok, kPReady, (uint32_t)(j - 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    values(j - 1);
+                }
+            }
+            if (ok && n_tiles > 0) {
+                wait(ok, kPReady, (uint32_t)(n_tiles - 1) & 1u);
+                if (ok) {
+                    tc_fence_after();
+                    values(n_tiles - 1);
+                }
+            }
+            // before teardown: every product issued here has completed
+            tc_commit(bar(kDrain));
+            tc_mbar_wait(bar(kDrain), 0u);
+        }
+    } else if (warp >= 4) {
+        // ---- key warps: thread (k, h) = half h of key k of the tile
+        const int kt = tid - 128, k = kt >> 1, h = kt & 1;
+        const uint32_t ktab = base_s + S::kKTab + 4u * lane, vtab = base_s + S::kVTab + 4u * lane;
+        float *norms = reinterpret_cast<float *>(smem + S::kNorm);
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int s = j & 1, u = j >> 1;
+            wait(ok, kBlkFull + s, (uint32_t)u & 1u);
+            if (u >= 1) wait(ok, kKvFree + s, (uint32_t)(u - 1) & 1u);
+            const uint32_t blk = base_s + S::kBlk + s * S::kBlkBytes;
+            const uint32_t kblk = blk + k * a.kbb, vblk = blk + kPfKeys * a.kbb + k * a.vbb;
+            const uint32_t row = (uint32_t)(h * 8192 + k * 128);
+            {
+                uint32_t w[8];
+                pf_code_words<KB>(kblk, h, w);
+                const uint32_t khi = base_s + S::kKhi + s * 16384 + row, klo = base_s + S::kKlo + s * 16384 + row;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t e[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) e[q] = pf_lds32(ktab + pf_code<KB>(w, 8 * c + q) * 128u);
+                    const uint32_t sw = (uint32_t)(((c ^ (k & 7)) << 4));
+                    pf_sts128(khi + sw, pf_prmt(e[0], e[1], 0x5410), pf_prmt(e[2], e[3], 0x5410),
+                              pf_prmt(e[4], e[5], 0x5410), pf_prmt(e[6], e[7], 0x5410));
+                    pf_sts128(klo + sw, pf_prmt(e[0], e[1], 0x7632), pf_prmt(e[2], e[3], 0x7632),
+                              pf_prmt(e[4], e[5], 0x7632), pf_prmt(e[6], e[7], 0x7632));
+                }
+            }
+            {
+                uint32_t w[8];
+                pf_code_words<VB>(vblk, h, w);
+                const uint32_t vt = base_s + S::kV + s * 16384 + row;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t e[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) e[q] = pf_lds32(vtab + pf_code<VB>(w, 8 * c + q) * 128u);
+                    pf_sts128(vt + (uint32_t)(((c ^ (k & 7)) << 4)), pf_prmt(e[0], e[1], 0x5410),
+                              pf_prmt(e[2], e[3], 0x5410), pf_prmt(e[4], e[5], 0x5410), pf_prmt(e[6], e[7], 0x5410));
+                }
+            }
+            if (h == 0) {
+                norms[s * 128 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(kblk)));
+                norms[s * 128 + 64 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(vblk)));
+            }
+            // the tiles were written by ordinary stores and are read by the tensor cores
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                tc_mbar_arrive(bar(kBlkEmpty + s));
+                tc_mbar_arrive(bar(kKvReady + s));
+            }
+        }
+    } else {
+        // ---- row warps: thread r = query row r0 + r = tensor-memory lane r
+        const int r = tid, rg = r0 + r;
+        const bool row_valid = rg < rows_total;
+        const int qi = row_valid ? rg / a.G : 0;
+        const int pos = L - a.M + qi;                  // this row's query position (keys 0 .. pos)
+        const uint32_t lane_t = tmem + ((uint32_t)(32 * warp) << 16);
+        const float *norms = reinterpret_cast<const float *>(smem + S::kNorm);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int s = j & 1, u = j >> 1;
+            wait(ok, kSReady + s, (uint32_t)u & 1u);
+            tc_fence_after();
+            float sv[kPfKeys];
+            {
+                float t32[32];
+                tc_ld32(lane_t + (uint32_t)(s * kPfKeys), t32);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sv[c] = t32[c];
+                tc_ld32(lane_t + (uint32_t)(s * kPfKeys + 32), t32);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sv[32 + c] = t32[c];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(bar(kSFree + s));
+            // key norms and the causal mask (key t visible to the row iff t <= pos)
+            const int t0 = j * kPfKeys;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kPfKeys; ++c) {
+                const bool vis = row_valid && t0 + c <= pos;
+                sv[c] = vis ? sv[c] * norms[s * 128 + c] : -INFINITY;
+                mx = fmaxf(mx, sv[c]);
+            }
+            // the reference maximum moves when the row's maximum exceeds it by more than 8 (log2
+            // units), so probabilities stay below 2^8 and O is rarely rescaled
+            const bool move = mx > m_ref + 8.f;
+            const float m_new = move ? mx : m_ref;
+            const float factor = move ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
+            float sum = 0.f;
+            // P of the previous tile has been consumed (and O is current) before P and O change
+            if (j >= 1) wait(ok, kPvDone, (uint32_t)(j - 1) & 1u);
+            tc_fence_after();
+            if (j >= 1 && __any_sync(0xffffffffu, move)) {
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float o32[32];
+                    tc_ld32(lane_t + kPfColO + 32u * c4, o32);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o32[c] *= factor;
+                    tc_st32(lane_t + kPfColO + 32u * c4, o32);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            const uint32_t prow = (uint32_t)(r * 128);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float pp[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int c = 8 * c8 + 2 * q + e;
+                        const float p = sv[c] == -INFINITY ? 0.f : exp2f(sv[c] - m_new);
+                        sum += p;
+                        pp[e] = sv[c] == -INFINITY ? 0.f : p * norms[s * 128 + 64 + c];
+                    }
+                    const __half h0 = __float2half_rn(pp[0]), h1 = __float2half_rn(pp[1]);
+                    hw[q] = pf_pack(__half2float(h0), __half2float(h1));
+                    lw[q] = pf_pack(pp[0] - __half2float(h0), pp[1] - __half2float(h1));
+                }
+                const uint32_t sw = (uint32_t)(((c8 ^ (r & 7)) << 4));
+                pf_sts128(base_s + S::kPhi + prow + sw, hw[0], hw[1], hw[2], hw[3]);
+                pf_sts128(base_s + S::kPlo + prow + sw, lw[0], lw[1], lw[2], lw[3]);
+            }
+            l = l * factor + sum;
+            m_ref = m_new;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(bar(kPReady));
+        }
+        // ---- epilogue: o = O / l, rotated back: D H o / sqrt(128)
+        if (n_tiles > 0) wait(ok, kPvDone, (uint32_t)(n_tiles - 1) & 1u);
+        tc_fence_after();
+        float o[128];
+        if (n_tiles > 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                float o32[32];
+                tc_ld32(lane_t + kPfColO + 32u * c4, o32);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[32 * c4 + c] = o32[c];
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) o[c] = 0.f;
+        }
+        const float inv = (l > 0.f && ok) ? 0.08838834764831845f / l : (ok ? 0.f : __int_as_float(0x7fc00000));
+#pragma unroll
+        for (int m = 1; m < 128; m <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                if ((c & m) == 0) {
+                    const float x = o[c], y = o[c + m];
+                    o[c] = x + y;
+                    o[c + m] = x - y;
+                }
+            }
+        }
+        if (row_valid) {
+            const int hq = kvh * a.G + rg % a.G;
+            float4 *dst = reinterpret_cast<float4 *>(a.out + (((int64_t)b * a.M + qi) * a.Hq + hq) * kD);
+#pragma unroll
+            for (int c4 = 0; c4 < 32; ++c4) {
+                float e[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int d = 4 * c4 + q;
+                    const float x = o[d] * inv;
+                    e[q] = ((a.signs[d >> 5] >> (d & 31)) & 1u) ? -x : x;
+                }
+                dst[c4] = make_float4(e[0], e[1], e[2], e[3]);
+            }
+        }
+    }
+
+    // ---- teardown: every product completed (the issuing thread waited for its last commit), every
+    // tensor-memory access completed; copies still in flight after a failed wait land first
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*fail_s) {
+        if (tid == 0) spin_ns(100000000ull);
+        __syncthreads();
+    }
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPfCols) : "memory");
+}
+
+template <int KB, int VB>
+int launch_prefill(const PfArgs &a, int grid, cudaStream_t st) {
+    static int done[64] = {0};
+    if (set_smem_limit((const void *)attn_prefill_kernel<KB, VB>, PfSmem::kTotal, done) != TQ_OK) return TQ_ERR_CUDA;
+    attn_prefill_kernel<KB, VB><<<grid, kPfThreads, PfSmem::kTotal, st>>>(a);
+    return launch_status();
+}
+
+template <int KB>
+int launch_prefill_v(const PfArgs &a, int vb, int grid, cudaStream_t st) {
+    switch (vb) {
+        case 2: return launch_prefill<KB, 2>(a, grid, st);
+        case 3: return launch_prefill<KB, 3>(a, grid, st);
+        case 4: return launch_prefill<KB, 4>(a, grid, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int wait_failed_prefill(unsigned *v, bool clear) { return read_wait_failed(v, clear); }
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
+                               const uint8_t *v_blocks, const tq_codebook *vcb, const int32_t *seq_lens, int B,
+                               int M, int Hq, int Hkv, int T_cap, int T, float scale, tq_signs signs, float *out,
+                               void *stream) {
+    if (!q || !k_blocks || !kcb || !v_blocks || !vcb || !out) return TQ_ERR_ARG;
+    if (B <= 0 || M <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || (T_cap & 7))
+        return TQ_ERR_ARG;
+    if (!std::isfinite(scale)) return TQ_ERR_ARG;
+    if (dtype_bytes(q_dtype) == 0 || !codebook_ok(kcb) || !codebook_ok(vcb)) return TQ_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k_blocks, 16) || !aligned(v_blocks, 16) || !aligned(out, 16)) return TQ_ERR_ALIGN;
+    PfArgs a;
+    a.q = q;
+    a.q_dtype = q_dtype;
+    a.k = k_blocks;
+    a.v = v_blocks;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.B = B;
+    a.M = M;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.T_cap = T_cap;
+    a.T = T;
+    a.kbb = 2 + 16 * kcb->bits;
+    a.vbb = 2 + 16 * vcb->bits;
+    a.qscale = scale * 1.4426950408889634f;
+    for (int i = 0; i < 16; ++i) {
+        a.kc[i] = i < kcb->levels ? kcb->centroids[i] : 0.f;
+        a.vc[i] = i < vcb->levels ? vcb->centroids[i] : 0.f;
+    }
+    for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
+    a.drop = drop_copies();
+    const int64_t rows = (int64_t)M * a.G;
+    a.row_tiles = (int)((rows + kPfRows - 1) / kPfRows);
+    const int64_t grid = (int64_t)B * Hkv * a.row_tiles;
+    if (grid > 0x7FFFFFFF || (int64_t)B * M * Hq > ((int64_t)1 << 40)) return TQ_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (kcb->bits) {
+        case 2: return launch_prefill_v<2>(a, vcb->bits, (int)grid, st);
+        case 3: return launch_prefill_v<3>(a, vcb->bits, (int)grid, st);
+        case 4: return launch_prefill_v<4>(a, vcb->bits, (int)grid, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}

@@ -65,6 +65,8 @@ def lib():
         ser = [vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, cbp, cbp, tq_signs, vp, vp]
         L.tq_serde_serialize.argtypes = ser
         L.tq_serde_deserialize.argtypes = ser
+        L.tq_attn_prefill.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
+                                      ctypes.c_float, tq_signs, vp, vp]
         L.tq_device_status.argtypes = [c_int, vp]
         L.tq_debug_drop_copies.argtypes = [c_int]
         L.tq_attn_workspace_bytes_sms.argtypes = [c_int] * 5
@@ -241,3 +243,14 @@ def tq_debug_drop_copies(on):
 
 def tq_attn_workspace_bytes_sms(B, Hq, Hkv, T_cap, sms):
     return int(lib().tq_attn_workspace_bytes_sms(B, Hq, Hkv, T_cap, sms))
+
+
+def tq_attn_prefill(q, k_blocks, kcb, v_blocks, vcb, out, T, scale, signs, seq_lens=None, stream=None):
+    """Causal attention of M query tokens per sequence.  q [B, M, Hq, 128];
+    k_blocks / v_blocks uint8 [B, Hkv, T_cap, bytes]; out float32 [B, M, Hq, 128]."""
+    B, M, Hq, _ = q.shape
+    Hkv, T_cap = k_blocks.shape[1], k_blocks.shape[2]
+    _check(lib().tq_attn_prefill(_ptr(q), _dtype(q), _ptr(k_blocks), ctypes.byref(kcb), _ptr(v_blocks),
+                                 ctypes.byref(vcb), _ptr(seq_lens), B, M, Hq, Hkv, T_cap, T, ctypes.c_float(scale),
+                                 signs, _ptr(out), _stream(stream)), "tq_attn_prefill")
+    return out
