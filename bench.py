@@ -69,6 +69,9 @@ WORKLOADS = {
                              scale="1/sqrt(128)"),
     "qjl_two_term": dict(B=8, Hq=32, Hkv=8, T=16384, head_dim=128, key_bits=3, value="fp16 raw", qjl_m=128,
                          kv_dtype="bf16 keys / fp16 values", scale="1/sqrt(128)"),
+    "llama3_8b_prefill": dict(B=16, Hq=32, Hkv=8, T=8192, M=64, head_dim=128, key_bits=4, value_bits=2,
+                              kv_dtype="bf16", query="64 new tokens per sequence, causal",
+                              scale="1/sqrt(128)"),
     "storage_roundtrip": dict(layout="[2, 32, 65536, 1024]", L=32, T=65536, hidden=1024, head_dim=128,
                               block_size=16, skip_first=2, skip_last=2, key_bits=4, value_bits=4, slot_bytes=132,
                               kv_dtype="bf16"),
@@ -80,6 +83,7 @@ CSRC = os.path.join(ROOT, "turboquant_bit_kv_gb300", "csrc")
 KERNEL_SOURCES = {
     "encode": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "append": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
+    "prefill": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
     "attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
                   "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_g1.cu",
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
@@ -108,6 +112,18 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Measured dense 16-bit tensor throughput (TFLOP/s): the burst figure of
+    MEASURED_PEAKS.json (fp16 and bf16 run at the same rate), else the
+    fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 same rate)"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def source_sha(group):
@@ -218,6 +234,7 @@ class Op:
     def __init__(self, name, group, fn, nbytes, launches, nvec=0):
         self.name, self.group, self.fn, self.nbytes, self.launches, self.nvec = \
             name, group, fn, nbytes, launches, nvec
+        self.flops = 0
 
 
 def _pinned(t):
@@ -576,6 +593,86 @@ def plan_qjl(tq, wl, dev, stream, seed, batch):
                 dtype="bf16")
 
 
+def prefill_flops(B, M, Hq, T):
+    """Algorithmic FLOPs of causal attention of M query tokens per sequence
+    over T cached tokens: query token i (position T - M + i) meets T - M + i + 1
+    keys; 2 * 128 FLOPs for its score and 2 * 128 for its value sum each."""
+    keys = sum(T - M + i + 1 for i in range(M))
+    return B * Hq * keys * 4 * 128
+
+
+def plan_prefill(tq, wl, dev, stream, seed, batch):
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS["llama3_8b_prefill"]
+    B, Hq, Hkv, T, M = batch or W["B"], W["Hq"], W["Hkv"], W["T"], W["M"]
+    kcb, vcb = tq.tq_codebook_load(128, 4), tq.tq_codebook_load(128, 2)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    data = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=seed, device=dev)
+    k, v = data["k"], data["v"]
+    g = torch.Generator(device=dev).manual_seed(seed + 101)
+    q = torch.randn((B, M, Hq, 128), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    kb = torch.empty((B, Hkv, T, 66), dtype=torch.uint8, device=dev)
+    vb = torch.empty((B, Hkv, T, 34), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, M, Hq, 128), dtype=torch.float32, device=dev)
+    scale = 1.0 / np.sqrt(128.0)
+    nvec = B * Hkv * T
+    nb = step_bytes(B, Hq, Hkv, T)
+    # the prefill reads the cache once per 128-row tile of (query token, head) rows
+    attn_bytes = nvec * 100 + q.numel() * 2 + out.numel() * 4
+    flops = prefill_flops(B, M, Hq, T)
+
+    def attn(qq=q):
+        tq.tq_attn_prefill(qq, kb, kcb, vb, vcb, out, T, scale, signs, stream=stream)
+
+    ops = [Op("encode_k", "encode", lambda: tq.tq_encode_kv(k.view(-1, 128), kcb, signs, kb, stream=stream),
+              nb["enc_k"], 1, nvec),
+           Op("encode_v", "encode", lambda: tq.tq_encode_kv(v.view(-1, 128), vcb, signs, vb, stream=stream),
+              nb["enc_v"], 1, nvec),
+           Op("attention", "prefill", attn, attn_bytes, 1)]
+    ops[-1].flops = flops
+
+    def e2e():
+        hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev), torch.empty_like(q)
+
+        def step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            tq.tq_encode_kv(dk, kcb, signs, kb.view(nvec, -1), stream=stream)
+            tq.tq_encode_kv(dv, vcb, signs, vb.view(nvec, -1), stream=stream)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
+
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 2, out.numel() * 4
+
+    def sample():
+        rng = np.random.default_rng(3)
+        res = []
+        for name, x, blk, bits in (("K", k, kb, 4), ("V", v, vb, 2)):
+            pick = torch.from_numpy(np.sort(rng.choice(nvec, 4096, replace=False))).to(dev)
+            res.append((name, bits, x.view(-1, 128)[pick].double().cpu().numpy(),
+                        blk.view(nvec, -1)[pick].cpu().numpy()))
+        return res
+
+    cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2 (129 MB); attention also timed after an L2 flush",
+               note="attention bytes: packed K/V blocks + q + out once; flops: 4 * 128 per (query row, visible "
+                    "key)")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, sample=sample, config=cfg,
+                dtype="bf16", tensor="prefill")
+
+
 def plan_storage(tq, wl, dev, stream, seed, batch):
     from turboquant_bit_kv_gb300 import workloads
     W = WORKLOADS["storage_roundtrip"]
@@ -650,7 +747,7 @@ def plan_storage(tq, wl, dev, stream, seed, batch):
 
 
 PLANS = {"llama3_8b_decode": plan_llama, "single_head_fp32": plan_single_head, "qwen25_7b_append": plan_qwen,
-         "qjl_two_term": plan_qjl, "storage_roundtrip": plan_storage}
+         "qjl_two_term": plan_qjl, "llama3_8b_prefill": plan_prefill, "storage_roundtrip": plan_storage}
 
 
 def _mean_ms(evs, a, b):
@@ -769,17 +866,27 @@ def run_gpu(args, rank, world, local_rank):
         g = groups[name]
         ach = g["bytes"] / (g["ms"] * 1e-3) / 1e9
         tr = profiled_traffic(args.workload, name)
+        if plan.get("tensor") == name:
+            # a dense contraction: useful FLOPs against the measured dense 16-bit tensor peak
+            tf, tkind = tensor_peak()
+            fl = sum(op.flops for op in ops if op.group == name)
+            at = fl / (g["ms"] * 1e-3) / 1e12
+            return {"bound": "tensor", "kernel": name, "launches_per_step": g["launches"], "achieved": round(at, 2),
+                    "peak": tf, "peak_kind": tkind, "unit": "TFLOP/s", "frac": round(at / tf, 4), "traffic": tr,
+                    "algorithmic_flops": fl, "algorithmic_bytes": g["bytes"], "gbs": round(ach, 1)}
         return {"bound": "hbm", "kernel": name, "launches_per_step": g["launches"], "achieved": round(ach, 1),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "traffic": tr, "algorithmic_bytes": g["bytes"]}
 
     # the metric: the decode-attention call's bytes over its time (per call,
     # averaged over the timed steps); without an attention call, the step's
-    attn = next((op for op in ops if op.group == "attention"), None)
+    attn = next((op for op in ops if op.group in ("attention", "prefill")), None)
     if attn is not None:
         a_ms = op_ms[ops.index(attn)]
         value = world * attn.nbytes / (a_ms * 1e-3) / 1e9
-        head = "attention"
+        head = attn.group
+        if attn.flops:
+            parts[attn.name]["tflops"] = round(attn.flops / (a_ms * 1e-3) / 1e12, 2)
     else:
         value = world * total / (ms_step * 1e-3) / 1e9
         head = max(groups, key=lambda n: groups[n]["ms"])
@@ -892,6 +999,23 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
         nbytes = n * (128 * ib * 2 + kbb + vbb) + n * (kbb + vbb) + G * groups * 128 * (ib + 4)
         desc = "%d (sequence, KV head) slice(s) at T=%d: encode K/V rows, attend %d query heads" % (groups, T, G)
         return secs, nbytes, desc
+    if workload == "llama3_8b_prefill":
+        G, M = W["Hq"] // W["Hkv"], W["M"]
+        data = _sample_inputs((workload, groups, T, seed),
+                              lambda: workloads.llama_decode(B=1, Hq=G * groups, Hkv=groups, T=T, seed=seed))
+        k = data["k"][0].double().numpy()
+        v = data["v"][0].double().numpy()
+        q = np.random.default_rng(seed).standard_normal((1, M, G * groups, 128))
+        t0 = time.perf_counter()
+        kh = [_oracle_roundtrip(codec, k[g], s, *books[4], 4)[0] for g in range(groups)]
+        vh = [_oracle_roundtrip(codec, v[g], s, *books[2], 2)[0] for g in range(groups)]
+        oracle.attention_causal(q, np.stack(kh)[None], np.stack(vh)[None], scale)
+        secs = time.perf_counter() - t0
+        n = groups * T
+        nbytes = n * (256 * 2 + 100) + n * 100 + M * G * groups * 128 * 6
+        desc = "%d (sequence, KV head) slice(s) at T=%d: encode K/V rows, causal attention of %d tokens x %d " \
+               "heads" % (groups, T, M, G)
+        return secs, nbytes, desc
     if workload == "qjl_two_term":
         G = W["Hq"] // W["Hkv"]
         data = _sample_inputs((workload, groups, T, seed),
@@ -931,7 +1055,7 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
 
 
 CPU_GROUPS = {"llama3_8b_decode": 128, "single_head_fp32": 1, "qwen25_7b_append": 24, "qjl_two_term": 32,
-              "storage_roundtrip": 64}
+              "llama3_8b_prefill": 8, "storage_roundtrip": 64}
 
 
 def cpu_cores():

@@ -290,3 +290,41 @@ def test_storage_roundtrip_fullsize(env):
                 assert mse == 0.0, (layer, kv, mse)
             else:
                 assert abs(mse / expect_mse - 1) < 0.03, (layer, kv, mse, expect_mse)
+
+
+def test_llama_prefill_fullsize(env):
+    """Causal attention of 64 new query tokens per sequence at the benchmark's
+    size: batch 16, 32/8 heads, context 8192, K4/V2, in the launch the
+    benchmark times; three (sequence, KV head) slices hold oracle-made caches
+    and their 64 x 4 query rows are compared with the oracle."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T, M = 16, 32, 8, 8192, 64
+    G = Hq // Hkv
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=0, device=dev)
+    k, v = w["k"], w["v"]
+    g = torch.Generator(device=dev).manual_seed(101)
+    q = torch.randn((B, M, Hq, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    kb = torch.empty((B, Hkv, T, 66), dtype=torch.uint8, device=dev)
+    vb = torch.empty((B, Hkv, T, 34), dtype=torch.uint8, device=dev)
+    tq.tq_encode_kv(k.view(-1, D), env["cbs"][4], env["signs"], kb)
+    tq.tq_encode_kv(v.view(-1, D), env["cbs"][2], env["signs"], vb)
+    slices = [(0, 0), (9, 5), (15, 7)]
+    hats = {}
+    for b, h in slices:
+        kblk, khat, _ = _oracle_slice(env, _rows(k[b, h]), 4)
+        vblk, vhat, _ = _oracle_slice(env, _rows(v[b, h]), 2)
+        kb[b, h] = torch.from_numpy(kblk).to(dev)
+        vb[b, h] = torch.from_numpy(vblk).to(dev)
+        hats[(b, h)] = (khat, vhat)
+    out = torch.empty((B, M, Hq, D), dtype=torch.float32, device=dev)
+    scale = 1 / np.sqrt(D)
+    tq.tq_attn_prefill(q, kb, env["cbs"][4], vb, env["cbs"][2], out, T, scale, env["signs"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    for b, h in slices:
+        khat, vhat = hats[(b, h)]
+        qs = q[b, :, h * G:(h + 1) * G].double().cpu().numpy()[None]
+        ref = oracle.attention_causal(qs, khat[None, None], vhat[None, None], scale)
+        got = out[b, :, h * G:(h + 1) * G].double().cpu().numpy()[None]
+        err = attn_rel_err(got.reshape(-1, D), ref.reshape(-1, D))
+        assert np.all(err < ATTN_TOL), (b, h, err.max())
