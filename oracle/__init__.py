@@ -18,6 +18,10 @@ Every function cites the page and section it restates.  Pages:
 * "lmcache.v1.distributed.serde.turboquant" (LMCache serde design):
   Configuration, Tensor Layout.
 
+``oracle.ext`` holds the further block formats (norm-corrected encode, the
+dense 8-in-3 packing of 3-bit codes, the 8-bit turboq8 codec) and
+``attention_causal`` the multi-token causal attention.
+
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, textbook tables, library routines or values printed on
 the pages; none is "parity unpinned".
