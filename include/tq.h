@@ -120,6 +120,45 @@ int tq_decode_kv(const uint8_t *blocks, int64_t block_stride_bytes, int64_t n_ve
                  const tq_codebook *cb, tq_signs signs,
                  void *out, int out_dtype, int64_t out_stride_elems, void *stream);
 
+/* Further block formats ([fork] section 4, Encode pipeline step 4: the
+ * corrected norm; [spec] Algorithm Detail Step 3: eight 3-bit values in
+ * three bytes; [fork] At a glance and the turboq8 paragraph: the 8-bit
+ * codec), selected by `flags` of the _ex calls:
+ *   TQ_FMT_NORM_CORRECT  bits 2..4: the stored norm is ||x|| / ||c[idx]||
+ *                        (rounded once to fp16), so the block decodes to a
+ *                        vector of the input's norm; codes, layout and
+ *                        decoding are those of the plain block.
+ *   TQ_FMT_DENSE3        bits 3: 50-byte block [fp16 norm][16 x 3 bytes], the
+ *                        codes of elements 8g .. 8g + 7 in the 24-bit
+ *                        little-endian word of group g, element 8g + p in
+ *                        bits 3p .. 3p + 2.
+ * turboq8 (a codebook of bits 8 from tq_codebook_load(128, 8), no flags):
+ * u = R x, a = max |u_j|, code i_j = nearest level of the grid
+ * (i - 127.5) / 127.5 to u_j / a (decided in float32, ties to the upper),
+ * block [fp16(a)][128 code bytes] (130 bytes); decode x_hat = R^T (a16 (i -
+ * 127.5) / 127.5).  tq_encode_kv / tq_decode_kv accept turboq8 codebooks
+ * as well. */
+#define TQ_FMT_NORM_CORRECT 1
+#define TQ_FMT_DENSE3 2
+
+/* Block bytes of a format: 34 / 50 / 66 for bits 2 / 3 / 4 (any valid
+ * flags), 130 for bits 8; 0 for an invalid combination. */
+size_t tq_block_bytes_ex(int bits, int flags);
+
+/* tq_encode_kv with `flags` (above); same arguments, layout, alignment and
+ * errors, plus TQ_ERR_ARG for unknown flags and TQ_ERR_UNSUPPORTED for a
+ * flag the bit width does not take. */
+int tq_encode_kv_ex(const void *x, int x_dtype, int64_t n_vec, int64_t x_stride_elems,
+                    const tq_codebook *cb, tq_signs signs,
+                    uint8_t *blocks, int64_t block_stride_bytes,
+                    const int64_t *dst_index, int flags, void *stream);
+
+/* tq_decode_kv with `flags` (TQ_FMT_DENSE3 selects the dense 3-bit layout;
+ * TQ_FMT_NORM_CORRECT changes nothing in decoding). */
+int tq_decode_kv_ex(const uint8_t *blocks, int64_t block_stride_bytes, int64_t n_vec,
+                    const tq_codebook *cb, tq_signs signs,
+                    void *out, int out_dtype, int64_t out_stride_elems, int flags, void *stream);
+
 /* QJL residual sketch of keys ([rotor] Implementation Requirements 1-2):
  * k_mse = decode(k_blocks[i]), r = k - k_mse, res_norm_f16[i] = fp16(||r||),
  * bit j of qjl_bits[i] (byte j / 8, position j % 8) = [(S r)_j >= 0].

@@ -310,6 +310,9 @@ extern "C" int tq_decode_kv(const uint8_t *blocks, int64_t block_stride_bytes, i
                             const tq_codebook *cb, tq_signs signs, void *out, int out_dtype,
                             int64_t out_stride_elems, void *stream) {
     if (n_vec < 0 || !cb) return TQ_ERR_ARG;
+    if (cb->bits == 8)   // turboq8 (tq_ext.cu)
+        return tq_decode_kv_ex(blocks, block_stride_bytes, n_vec, cb, signs, out, out_dtype, out_stride_elems, 0,
+                               stream);
     if (!codebook_ok(cb) || dtype_bytes(out_dtype) == 0) return TQ_ERR_UNSUPPORTED;
     if (n_vec == 0) return TQ_OK;
     const int es = dtype_bytes(out_dtype);

@@ -1361,6 +1361,9 @@ extern "C" int tq_encode_kv(const void *x, int x_dtype, int64_t n_vec, int64_t x
                             const tq_codebook *cb, tq_signs signs, uint8_t *blocks,
                             int64_t block_stride_bytes, const int64_t *dst_index, void *stream) {
     if (n_vec < 0 || !cb) return TQ_ERR_ARG;
+    if (cb->bits == 8)   // turboq8 (tq_ext.cu)
+        return tq_encode_kv_ex(x, x_dtype, n_vec, x_stride_elems, cb, signs, blocks, block_stride_bytes, dst_index, 0,
+                               stream);
     if (!codebook_ok(cb) || dtype_bytes(x_dtype) == 0) return TQ_ERR_UNSUPPORTED;
     if (n_vec == 0) return TQ_OK;
     const int es = dtype_bytes(x_dtype);

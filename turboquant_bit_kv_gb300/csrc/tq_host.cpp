@@ -120,6 +120,14 @@ tq_codebook g_cb[5];
 
 extern "C" int tq_codebook_load(int head_dim, int bits, tq_codebook *out) {
     if (!out) return TQ_ERR_ARG;
+    if (head_dim == kD && bits == 8) {
+        // turboq8: the uniform grid (i - 127.5) / 127.5 is implicit; no table
+        std::memset(out, 0, sizeof(*out));
+        out->head_dim = head_dim;
+        out->bits = 8;
+        out->levels = 256;
+        return TQ_OK;
+    }
     if (head_dim != kD || bits < 2 || bits > 4) return TQ_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_cb_mutex);
     if (!g_cb_ready[bits]) {
@@ -156,6 +164,7 @@ extern "C" int tq_signs_from_seed(uint64_t seed, int head_dim, tq_signs *out) {
 }
 
 extern "C" size_t tq_block_bytes(int bits) {
+    if (bits == 8) return 130;
     if (bits < 2 || bits > 4) return 0;
     return 2 + (size_t)kD * bits / 8;
 }

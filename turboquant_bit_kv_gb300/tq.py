@@ -67,6 +67,10 @@ def lib():
         L.tq_serde_deserialize.argtypes = ser
         L.tq_attn_prefill.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
                                       ctypes.c_float, tq_signs, vp, vp]
+        L.tq_block_bytes_ex.argtypes = [c_int, c_int]
+        L.tq_block_bytes_ex.restype = sz
+        L.tq_encode_kv_ex.argtypes = [vp, c_int, i64, i64, cbp, tq_signs, vp, i64, vp, c_int, vp]
+        L.tq_decode_kv_ex.argtypes = [vp, i64, i64, cbp, tq_signs, vp, c_int, i64, c_int, vp]
         L.tq_device_status.argtypes = [c_int, vp]
         L.tq_debug_drop_copies.argtypes = [c_int]
         L.tq_attn_workspace_bytes_sms.argtypes = [c_int] * 5
@@ -254,3 +258,29 @@ def tq_attn_prefill(q, k_blocks, kcb, v_blocks, vcb, out, T, scale, signs, seq_l
                                  ctypes.byref(vcb), _ptr(seq_lens), B, M, Hq, Hkv, T_cap, T, ctypes.c_float(scale),
                                  signs, _ptr(out), _stream(stream)), "tq_attn_prefill")
     return out
+
+
+TQ_FMT_NORM_CORRECT, TQ_FMT_DENSE3 = 1, 2
+
+
+def tq_block_bytes_ex(bits, flags=0):
+    return int(lib().tq_block_bytes_ex(bits, flags))
+
+
+def tq_encode_kv_ex(x, cb, signs, blocks, flags=0, block_stride_bytes=None, dst_index=None, block_offset=0,
+                    stream=None):
+    """tq_encode_kv with format flags (TQ_FMT_NORM_CORRECT, TQ_FMT_DENSE3); an
+    8-bit codebook selects turboq8."""
+    n, stride = _nvec_rows(x)
+    bs = block_stride_bytes or tq_block_bytes_ex(cb.bits, flags)
+    base = ctypes.c_void_p(blocks.data_ptr() + block_offset)
+    _check(lib().tq_encode_kv_ex(_ptr(x), _dtype(x), n, stride, ctypes.byref(cb), signs, base, bs, _ptr(dst_index),
+                                 flags, _stream(stream)), "tq_encode_kv_ex")
+
+
+def tq_decode_kv_ex(blocks, n_vec, cb, signs, out, flags=0, block_stride_bytes=None, block_offset=0, stream=None):
+    bs = block_stride_bytes or tq_block_bytes_ex(cb.bits, flags)
+    n, stride = _nvec_rows(out)
+    base = ctypes.c_void_p(blocks.data_ptr() + block_offset)
+    _check(lib().tq_decode_kv_ex(base, bs, n_vec, ctypes.byref(cb), signs, _ptr(out), _dtype(out), stride, flags,
+                                 _stream(stream)), "tq_decode_kv_ex")
