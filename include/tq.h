@@ -228,6 +228,10 @@ int tq_attn_plan(int B, int Hq, int Hkv, int T, int key_bits, int value_bits, in
  *   workspace   device scratch of >= tq_attn_workspace_bytes(B, Hq, Hkv, T_cap)
  *               bytes, 16-byte aligned (TQ_ERR_ALIGN otherwise); clobbered;
  *               calls that overlap on the GPU must use different workspaces.
+ *   turboq8 keys with 2/3/4-bit values, or 4-bit keys with turboq8 values
+ *   ([fork] section 2, Asymmetric K/V), are served as the one-token case of
+ *   tq_attn_prefill (the workspace is then unused); other combinations with
+ *   turboq8, and QJL with turboq8, return TQ_ERR_UNSUPPORTED.
  * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_WORKSPACE,
  * TQ_ERR_CUDA. */
 int tq_attn_decode(const void *q, int q_dtype,
@@ -250,7 +254,9 @@ int tq_attn_decode(const void *q, int q_dtype,
  * a query with p < 0 gives a zero output row.
  *   q         device [B][M][Hq][128] of q_dtype (TQ_F32 / TQ_BF16 / TQ_F16).
  *   k_blocks  device [B][Hkv][T_cap] blocks of kcb->bits; v_blocks the same
- *             for vcb->bits (packed values only).
+ *             for vcb->bits (packed values only).  Widths: 2, 3, 4 with each
+ *             other, turboq8 (bits 8) keys with 2/3/4-bit values, 4-bit keys
+ *             with turboq8 values.
  *   seq_lens  device int32 [B] (each clamped to [0, T]) or NULL for T.
  *   Hq % Hkv == 0 (query head h reads KV head h / (Hq / Hkv)); 1 <= T <=
  *   T_cap, T_cap a multiple of 8; q, k_blocks, v_blocks, out 16-byte aligned.

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from oracle import codec
+from oracle import codec, ext
 from turboquant_bit_kv_gb300 import workloads
 
 from parity_util import ATTN_TOL, attn_rel_err, oracle_books
@@ -25,13 +25,17 @@ def env():
     from turboquant_bit_kv_gb300 import tq
     tq.lib()
     return dict(tq=tq, dev=torch.device("cuda:0"), books=oracle_books(),
-                cbs={b: tq.tq_codebook_load(128, b) for b in (2, 3, 4)},
+                cbs={b: tq.tq_codebook_load(128, b) for b in (2, 3, 4, 8)},
                 signs=tq.tq_signs_from_seed(workloads.SIGN_SEED), s=oracle.sign_diagonal(workloads.SIGN_SEED))
 
 
 def _cache(env, x, bits):
     """Oracle blocks and reconstructions of x float64 [B, H, T, 128]."""
     B, H, T, _ = x.shape
+    if bits == 8:
+        idx, s16, _ = ext.encode_q8(x.reshape(-1, D), env["s"])
+        return (ext.pack_q8(idx, s16).reshape(B, H, T, -1),
+                ext.decode_q8(idx, s16, env["s"]).reshape(B, H, T, D))
     c, _, b32 = env["books"][bits]
     idx, n16, _ = codec.encode(x.reshape(-1, D), env["s"], b32)
     return (codec.pack_block(idx, n16, bits).reshape(B, H, T, -1),
@@ -65,6 +69,9 @@ def _run(env, q, kblk, vblk, kbits, vbits, T, T_cap, scale, lens=None):
     (3, 20, 8, 4, 200, 200, 4, 4, [200, 7, 64], torch.float16),    # a sequence shorter than M: zero rows
     (2, 1, 32, 8, 129, 136, 3, 2, [129, 65], torch.bfloat16),      # one query token: the decode case
     (1, 64, 32, 8, 1000, 1000, 4, 2, None, torch.bfloat16),        # 256 rows per KV head, 16 key tiles
+    (2, 16, 8, 2, 300, 304, 8, 4, [300, 99], torch.bfloat16),      # turboq8 keys, 4-bit values
+    (1, 24, 28, 4, 257, 264, 8, 2, None, torch.float16),           # turboq8 keys, 2-bit values, 7 heads
+    (2, 12, 8, 4, 150, 152, 4, 8, [150, 40], torch.float32),       # 4-bit keys, turboq8 values
 ])
 def test_prefill_matches_oracle(env, B, M, Hq, Hkv, T, T_cap, kbits, vbits, lens, qdt):
     w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=30 + M)
@@ -102,3 +109,28 @@ def test_prefill_decode_agreement(env):
     torch.cuda.synchronize()
     err = attn_rel_err(got[:, 0].reshape(-1, D), out.double().cpu().numpy().reshape(-1, D))
     assert np.all(err < 2 * ATTN_TOL), err.max()
+
+
+@pytest.mark.parametrize("kbits,vbits", [(8, 4), (8, 3), (4, 8)])
+def test_decode_attention_turboq8_pairs(env, kbits, vbits):
+    """tq_attn_decode over turboq8 keys or values (the asymmetric pairs): the
+    oracle's attention on identical packed caches."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T, T_cap = 3, 12, 3, 500, 504
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=50 + kbits + vbits)
+    kblk, khat = _cache(env, w["k"].double().numpy(), kbits)
+    vblk, vhat = _cache(env, w["v"].double().numpy(), vbits)
+    kb = torch.zeros((B, Hkv, T_cap, kblk.shape[-1]), dtype=torch.uint8)
+    kb[:, :, :T] = torch.from_numpy(kblk)
+    vb = torch.zeros((B, Hkv, T_cap, vblk.shape[-1]), dtype=torch.uint8)
+    vb[:, :, :T] = torch.from_numpy(vblk)
+    lens = [500, 123, 1]
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T_cap), dtype=torch.uint8, device=dev)
+    scale = 1 / np.sqrt(D)
+    tq.tq_attn_decode(w["q"].to(dev), kb.to(dev), env["cbs"][kbits], vb.to(dev), env["cbs"][vbits], out, ws, T,
+                      scale, env["signs"], seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    ref = oracle.attention_dequantized(w["q"].double().numpy(), khat, vhat, scale, seq_lens=lens)
+    err = attn_rel_err(out.double().cpu().numpy().reshape(-1, D), ref.reshape(-1, D))
+    assert np.all(err < ATTN_TOL), err.max()

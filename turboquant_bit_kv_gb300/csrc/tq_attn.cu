@@ -281,6 +281,13 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
                               int Hkv, int T_cap, int T, float scale, tq_signs signs, const uint8_t *qjl_bits,
                               const uint16_t *res_norm_f16, const float *S, float *out, void *workspace,
                               size_t workspace_bytes, void *stream) {
+    if (kcb && (kcb->bits == 8 || (vcb && vcb->bits == 8))) {
+        // turboq8 keys or values (the fork's asymmetric pairs): one query token is the M = 1 case of
+        // the tensor-core causal attention, which needs no workspace
+        if (qjl_bits || res_norm_f16 || S || !vcb) return TQ_ERR_UNSUPPORTED;
+        return tq_attn_prefill(q, q_dtype, k_blocks, kcb, static_cast<const uint8_t *>(v), vcb, seq_lens, B, 1, Hq,
+                               Hkv, T_cap, T, scale, signs, out, stream);
+    }
     if (!q || !k_blocks || !kcb || !v || !out || !workspace) return TQ_ERR_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || (T_cap & 7))
         return TQ_ERR_ARG;

@@ -59,6 +59,7 @@ constexpr uint32_t kPfColO = 128;
 
 // Shared memory (offsets from a 1024-byte aligned base).  Operand tiles use the
 // K-major 128-byte swizzle of tq_tc.cuh: 64-element blocks of rows x 128 bytes.
+template <int KB, int VB>
 struct PfSmem {
     static constexpr int kQhi = 0;                         // Q hi: 128 rows x 128 dims (two 16 KB blocks)
     static constexpr int kQlo = 32768;
@@ -68,7 +69,7 @@ struct PfSmem {
     static constexpr int kPhi = 163840;                    // P hi: 128 rows x 64 keys (one 16 KB block)
     static constexpr int kPlo = 180224;
     static constexpr int kBlk = 196608;                    // [2] packed blocks: 64 K blocks | 64 V blocks
-    static constexpr int kBlkBytes = 8448;                 // 64 x 66 x 2
+    static constexpr int kBlkBytes = kPfKeys * (2 + 16 * KB + 2 + 16 * VB);
     static constexpr int kNorm = kBlk + 2 * kBlkBytes;     // [2] kn[64] | vn[64] (float)
     static constexpr int kKTab = kNorm + 2 * 512;          // key centroids: 16 codes x 32 lanes x half2 (hi, lo)
     static constexpr int kVTab = kKTab + 2048;             // value centroids: 16 codes x 32 lanes x half2 (v, v)
@@ -160,11 +161,14 @@ __device__ __forceinline__ uint32_t pf_pack(float lo, float hi) {
 }
 
 // Code words of dims 64 h .. 64 h + 63 of the block at shared address `blk`
-// (2-byte aligned): 4-bit: 8 words; 2-bit: 4 words; 3-bit: 4 low-plane words
-// then 2 high-plane words.
+// (2-byte aligned): 8-bit (turboq8): 16 words; 4-bit: 8 words; 2-bit: 4
+// words; 3-bit: 4 low-plane words then 2 high-plane words.
 template <int BITS>
-__device__ __forceinline__ void pf_code_words(uint32_t blk, int h, uint32_t (&w)[8]) {
-    if constexpr (BITS == 4) {
+__device__ __forceinline__ void pf_code_words(uint32_t blk, int h, uint32_t (&w)[16]) {
+    if constexpr (BITS == 8) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pf_lds16(blk + 2 + 64 * h + 4 * i) | (pf_lds16(blk + 4 + 64 * h + 4 * i) << 16);
+    } else if constexpr (BITS == 4) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = pf_lds16(blk + 2 + 32 * h + 4 * i) | (pf_lds16(blk + 4 + 32 * h + 4 * i) << 16);
     } else {
@@ -180,15 +184,23 @@ __device__ __forceinline__ void pf_code_words(uint32_t blk, int h, uint32_t (&w)
 
 // Code of relative dim e (0..63) from the words above.
 template <int BITS>
-__device__ __forceinline__ uint32_t pf_code(const uint32_t (&w)[8], int e) {
-    if constexpr (BITS == 4) return (w[e >> 3] >> (4 * (e & 7))) & 15u;
+__device__ __forceinline__ uint32_t pf_code(const uint32_t (&w)[16], int e) {
+    if constexpr (BITS == 8) return (w[e >> 2] >> (8 * (e & 3))) & 255u;
+    else if constexpr (BITS == 4) return (w[e >> 3] >> (4 * (e & 7))) & 15u;
     else if constexpr (BITS == 2) return (w[e >> 4] >> (2 * (e & 15))) & 3u;
     else return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[4 + (e >> 5)] >> (e & 31)) & 1u) << 2);
 }
 
+// turboq8 entry of code i: the grid level (i - 127.5) / 127.5 is (2 i - 255) / 255; the integer
+// 2 i - 255 is exact in fp16, the 1 / 255 goes into the block's norm factor (no lo half needed).
+__device__ __forceinline__ uint32_t pf_q8_entry(uint32_t i, bool dup) {
+    const uint32_t h = __half_as_ushort(__int2half_rn((int)(2 * i) - 255));
+    return dup ? (h | (h << 16)) : h;
+}
+
 template <int KB, int VB>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __grid_constant__ PfArgs a) {
-    using S = PfSmem;
+    using S = PfSmem<KB, VB>;
     extern __shared__ __align__(16) uint8_t pf_smem_raw[];
     const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(pf_smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -401,14 +413,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             const uint32_t kblk = blk + k * a.kbb, vblk = blk + kPfKeys * a.kbb + k * a.vbb;
             const uint32_t row = (uint32_t)(h * 8192 + k * 128);
             {
-                uint32_t w[8];
+                uint32_t w[16];
                 pf_code_words<KB>(kblk, h, w);
                 const uint32_t khi = base_s + S::kKhi + s * 16384 + row, klo = base_s + S::kKlo + s * 16384 + row;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t e[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) e[q] = pf_lds32(ktab + pf_code<KB>(w, 8 * c + q) * 128u);
+                    for (int q = 0; q < 8; ++q)
+                        e[q] = KB == 8 ? pf_q8_entry(pf_code<KB>(w, 8 * c + q), false)
+                                       : pf_lds32(ktab + pf_code<KB>(w, 8 * c + q) * 128u);
                     const uint32_t sw = (uint32_t)(((c ^ (k & 7)) << 4));
                     pf_sts128(khi + sw, pf_prmt(e[0], e[1], 0x5410), pf_prmt(e[2], e[3], 0x5410),
                               pf_prmt(e[4], e[5], 0x5410), pf_prmt(e[6], e[7], 0x5410));
@@ -417,21 +431,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 }
             }
             {
-                uint32_t w[8];
+                uint32_t w[16];
                 pf_code_words<VB>(vblk, h, w);
                 const uint32_t vt = base_s + S::kV + s * 16384 + row;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t e[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) e[q] = pf_lds32(vtab + pf_code<VB>(w, 8 * c + q) * 128u);
+                    for (int q = 0; q < 8; ++q)
+                        e[q] = VB == 8 ? pf_q8_entry(pf_code<VB>(w, 8 * c + q), true)
+                                       : pf_lds32(vtab + pf_code<VB>(w, 8 * c + q) * 128u);
                     pf_sts128(vt + (uint32_t)(((c ^ (k & 7)) << 4)), pf_prmt(e[0], e[1], 0x5410),
                               pf_prmt(e[2], e[3], 0x5410), pf_prmt(e[4], e[5], 0x5410), pf_prmt(e[6], e[7], 0x5410));
                 }
             }
             if (h == 0) {
-                norms[s * 128 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(kblk)));
-                norms[s * 128 + 64 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(vblk)));
+                // the block's norm (turboq8: its scale over 255, the grid's step factor)
+                const float kf = KB == 8 ? (1.f / 255.f) : 1.f, vf = VB == 8 ? (1.f / 255.f) : 1.f;
+                norms[s * 128 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(kblk))) * kf;
+                norms[s * 128 + 64 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(vblk))) * vf;
             }
             // the tiles were written by ordinary stores and are read by the tensor cores
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -590,18 +608,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
 
 template <int KB, int VB>
 int launch_prefill(const PfArgs &a, int grid, cudaStream_t st) {
+    using S = PfSmem<KB, VB>;
     static int done[64] = {0};
-    if (set_smem_limit((const void *)attn_prefill_kernel<KB, VB>, PfSmem::kTotal, done) != TQ_OK) return TQ_ERR_CUDA;
-    attn_prefill_kernel<KB, VB><<<grid, kPfThreads, PfSmem::kTotal, st>>>(a);
+    if (set_smem_limit((const void *)attn_prefill_kernel<KB, VB>, S::kTotal, done) != TQ_OK) return TQ_ERR_CUDA;
+    attn_prefill_kernel<KB, VB><<<grid, kPfThreads, S::kTotal, st>>>(a);
     return launch_status();
 }
 
+// Key / value widths served: 2, 3, 4 with each other; turboq8 keys with 2/3/4-bit values and
+// 4-bit keys with turboq8 values (the asymmetric pairs of the fork page; 8/8 does not fit the
+// shared memory of one CTA).
 template <int KB>
 int launch_prefill_v(const PfArgs &a, int vb, int grid, cudaStream_t st) {
     switch (vb) {
         case 2: return launch_prefill<KB, 2>(a, grid, st);
         case 3: return launch_prefill<KB, 3>(a, grid, st);
         case 4: return launch_prefill<KB, 4>(a, grid, st);
+        case 8:
+            if constexpr (KB == 4) return launch_prefill<4, 8>(a, grid, st);
+            return TQ_ERR_UNSUPPORTED;
         default: return TQ_ERR_UNSUPPORTED;
     }
 }
@@ -622,7 +647,10 @@ extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_bloc
     if (B <= 0 || M <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || (T_cap & 7))
         return TQ_ERR_ARG;
     if (!std::isfinite(scale)) return TQ_ERR_ARG;
-    if (dtype_bytes(q_dtype) == 0 || !codebook_ok(kcb) || !codebook_ok(vcb)) return TQ_ERR_UNSUPPORTED;
+    auto book_ok = [](const tq_codebook *cb) {
+        return codebook_ok(cb) || (cb->head_dim == kD && cb->bits == 8 && cb->levels == 256);
+    };
+    if (dtype_bytes(q_dtype) == 0 || !book_ok(kcb) || !book_ok(vcb)) return TQ_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_blocks, 16) || !aligned(v_blocks, 16) || !aligned(out, 16)) return TQ_ERR_ALIGN;
     PfArgs a;
     a.q = q;
@@ -642,8 +670,8 @@ extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_bloc
     a.vbb = 2 + 16 * vcb->bits;
     a.qscale = scale * 1.4426950408889634f;
     for (int i = 0; i < 16; ++i) {
-        a.kc[i] = i < kcb->levels ? kcb->centroids[i] : 0.f;
-        a.vc[i] = i < vcb->levels ? vcb->centroids[i] : 0.f;
+        a.kc[i] = (kcb->bits != 8 && i < kcb->levels) ? kcb->centroids[i] : 0.f;
+        a.vc[i] = (vcb->bits != 8 && i < vcb->levels) ? vcb->centroids[i] : 0.f;
     }
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
     a.drop = drop_copies();
@@ -656,6 +684,7 @@ extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_bloc
         case 2: return launch_prefill_v<2>(a, vcb->bits, (int)grid, st);
         case 3: return launch_prefill_v<3>(a, vcb->bits, (int)grid, st);
         case 4: return launch_prefill_v<4>(a, vcb->bits, (int)grid, st);
+        case 8: return vcb->bits == 8 ? TQ_ERR_UNSUPPORTED : launch_prefill_v<8>(a, vcb->bits, (int)grid, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
 }
