@@ -269,6 +269,31 @@ int tq_attn_prefill(const void *q, int q_dtype,
                     const int32_t *seq_lens, int B, int M, int Hq, int Hkv, int T_cap, int T,
                     float scale, tq_signs signs, float *out, void *stream);
 
+/* tq_attn_prefill over a paged cache: the serde page's "block/slot mapping"
+ * (Limitations) and the spec's per-position packed cache (Integration
+ * Points).  Packed blocks live in pools of pages of `page_tokens` tokens
+ * (a multiple of 8): k_pool / v_pool are device [num_pages][Hkv][page_tokens]
+ * blocks, and token t of sequence b is slot t % page_tokens of page
+ * block_table[b * max_pages + t / page_tokens] (device int32 [B][max_pages];
+ * the entries for the pages covering tokens 0 .. L_b - 1 must name pages of
+ * the pools).  max_pages * page_tokens >= T; the other arguments, the
+ * causal rule and the errors as tq_attn_prefill. */
+int tq_attn_prefill_paged(const void *q, int q_dtype,
+                          const uint8_t *k_pool, const tq_codebook *kcb,
+                          const uint8_t *v_pool, const tq_codebook *vcb,
+                          const int32_t *block_table, int max_pages, int page_tokens,
+                          const int32_t *seq_lens, int B, int M, int Hq, int Hkv, int T,
+                          float scale, tq_signs signs, float *out, void *stream);
+
+/* Decode attention (one query token per sequence, q [B][Hq][128], out
+ * [B][Hq][128]) over a paged cache: tq_attn_prefill_paged with M = 1. */
+int tq_attn_decode_paged(const void *q, int q_dtype,
+                         const uint8_t *k_pool, const tq_codebook *kcb,
+                         const uint8_t *v_pool, const tq_codebook *vcb,
+                         const int32_t *block_table, int max_pages, int page_tokens,
+                         const int32_t *seq_lens, int B, int Hq, int Hkv, int T,
+                         float scale, tq_signs signs, float *out, void *stream);
+
 /* Size of the device array that tq_attn_decode_noalloc uses as its split-K
  * scratch: 16 MiB.  On GPUs of 148 to 160 SMs that covers, at any context,
  * batch 64 x 28 query heads over 4 KV heads (about 11.4 MiB), batch 64 x 32

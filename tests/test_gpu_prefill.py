@@ -134,3 +134,110 @@ def test_decode_attention_turboq8_pairs(env, kbits, vbits):
     ref = oracle.attention_dequantized(w["q"].double().numpy(), khat, vhat, scale, seq_lens=lens)
     err = attn_rel_err(out.double().cpu().numpy().reshape(-1, D), ref.reshape(-1, D))
     assert np.all(err < ATTN_TOL), err.max()
+
+
+def _paged(kblk, vblk, page, rng):
+    """Scatter contiguous caches [B, Hkv, T, bytes] into shuffled pages of a
+    pool [pages, Hkv, page, bytes]; returns (k_pool, v_pool, table int32)."""
+    B, Hkv, T = kblk.shape[:3]
+    per = -(-T // page)
+    n_pages = B * per + 3                         # spare pages nothing points to
+    order = rng.permutation(n_pages)[:B * per].reshape(B, per)
+    kp = np.full((n_pages, Hkv, page, kblk.shape[-1]), 0xEE, np.uint8)
+    vp = np.full((n_pages, Hkv, page, vblk.shape[-1]), 0xEE, np.uint8)
+    for b in range(B):
+        for p in range(per):
+            t0, t1 = p * page, min(T, (p + 1) * page)
+            kp[order[b, p], :, :t1 - t0] = kblk[b, :, t0:t1]
+            vp[order[b, p], :, :t1 - t0] = vblk[b, :, t0:t1]
+    table = np.concatenate([order, np.full((B, 2), 10**6)], axis=1).astype(np.int32)   # unused tail entries
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("page,M,kbits,vbits,lens", [
+    (16, 16, 4, 2, [300, 77]),     # vLLM-sized pages, ragged lengths
+    (40, 24, 3, 3, [299, 300]),    # a page size that is no power of two
+    (64, 1, 8, 4, [300, 5]),       # decode over a paged turboq8 / 4-bit cache
+])
+def test_paged_matches_oracle(env, page, M, kbits, vbits, lens):
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T = 2, 8, 2, 300
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=70 + page)
+    kblk, khat = _cache(env, w["k"].double().numpy(), kbits)
+    vblk, vhat = _cache(env, w["v"].double().numpy(), vbits)
+    kp, vp, table = _paged(kblk, vblk, page, np.random.default_rng(page))
+    scale = 1 / np.sqrt(D)
+    q = torch.randn((B, M, Hq, D), generator=torch.Generator().manual_seed(page), dtype=torch.float32).to(
+        torch.bfloat16)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    args = (torch.from_numpy(kp).to(dev), env["cbs"][kbits], torch.from_numpy(vp).to(dev), env["cbs"][vbits],
+            torch.from_numpy(table).to(dev), page)
+    if M == 1:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+        tq.tq_attn_decode_paged(q[:, 0].to(dev), *args, out, T, scale, env["signs"], seq_lens=sl)
+        got = out.double().cpu().numpy()[:, None]
+    else:
+        out = torch.empty((B, M, Hq, D), dtype=torch.float32, device=dev)
+        tq.tq_attn_prefill_paged(q.to(dev), *args, out, T, scale, env["signs"], seq_lens=sl)
+        got = out.double().cpu().numpy()
+    torch.cuda.synchronize()
+    ref = oracle.attention_causal(q.double().numpy(), khat, vhat, scale, seq_lens=lens)
+    err = attn_rel_err(got.reshape(-1, D), ref.reshape(-1, D))
+    assert np.all(err < ATTN_TOL), err.max()
+
+
+def test_circular_cache_and_eviction(env):
+    """The spec's Integration Points: a circular cache written at
+    pos % T_cap (through a destination index) holds the last T_cap tokens,
+    and attention over the full window is the attention over those tokens;
+    evicting the oldest tokens by moving packed bytes (a device memmove)
+    keeps every remaining block's value."""
+    tq, dev = env["tq"], env["dev"]
+    B, Hq, Hkv, T_cap, total = 1, 8, 2, 256, 400
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=total, seed=81)
+    k, v = w["k"].to(dev), w["v"].to(dev)
+    kb = torch.zeros((B, Hkv, T_cap, 66), dtype=torch.uint8, device=dev)
+    vb = torch.zeros((B, Hkv, T_cap, 34), dtype=torch.uint8, device=dev)
+    for h in range(Hkv):
+        pos = torch.arange(total, device=dev)
+        dst = h * T_cap + pos % T_cap                # later positions overwrite the oldest slots
+        # positions are written in order, so the last write to a slot is the newest token
+        for start in range(0, total, T_cap):
+            sel = slice(start, min(total, start + T_cap))
+            tq.tq_encode_kv(k[0, h, sel].contiguous(), env["cbs"][4], env["signs"], kb.view(-1, 66),
+                            dst_index=dst[sel].contiguous())
+            tq.tq_encode_kv(v[0, h, sel].contiguous(), env["cbs"][2], env["signs"], vb.view(-1, 34),
+                            dst_index=dst[sel].contiguous())
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T_cap), dtype=torch.uint8, device=dev)
+    scale = 1 / np.sqrt(D)
+    tq.tq_attn_decode(w["q"].to(dev), kb, env["cbs"][4], vb, env["cbs"][2], out, ws, T_cap, scale, env["signs"])
+    torch.cuda.synchronize()
+    # the oracle over the last T_cap tokens (attention does not depend on their slot order)
+    last = slice(total - T_cap, total)
+    khat = _cache(env, w["k"][:, :, last].double().numpy(), 4)[1]
+    vhat = _cache(env, w["v"][:, :, last].double().numpy(), 2)[1]
+    ref = oracle.attention_dequantized(w["q"].double().numpy(), khat, vhat, scale)
+    assert np.all(attn_rel_err(out.double().cpu().numpy().reshape(-1, D), ref.reshape(-1, D)) < ATTN_TOL)
+    # eviction: drop the 100 oldest tokens of a linear cache by moving the packed bytes down
+    lin_k = torch.zeros((B, Hkv, T_cap, 66), dtype=torch.uint8, device=dev)
+    lin_v = torch.zeros((B, Hkv, T_cap, 34), dtype=torch.uint8, device=dev)
+    for h in range(Hkv):
+        tq.tq_encode_kv(k[0, h, :T_cap].contiguous(), env["cbs"][4], env["signs"], lin_k[0, h])
+        tq.tq_encode_kv(v[0, h, :T_cap].contiguous(), env["cbs"][2], env["signs"], lin_v[0, h])
+    before = torch.empty((T_cap - 100, D), dtype=torch.float32, device=dev)
+    tq.tq_decode_kv(lin_k[0, 1, 100:], T_cap - 100, env["cbs"][4], env["signs"], before)
+    kept = lin_k[:, :, 100:].clone()
+    lin_k[:, :, :T_cap - 100] = kept
+    lin_v[:, :, :T_cap - 100] = lin_v[:, :, 100:].clone()
+    after = torch.empty((T_cap - 100, D), dtype=torch.float32, device=dev)
+    tq.tq_decode_kv(lin_k[0, 1, :T_cap - 100], T_cap - 100, env["cbs"][4], env["signs"], after)
+    torch.cuda.synchronize()
+    assert torch.equal(before, after)             # moved bytes decode to the same values
+    tq.tq_attn_decode(w["q"].to(dev), lin_k, env["cbs"][4], lin_v, env["cbs"][2], out, ws, T_cap - 100, scale,
+                      env["signs"])
+    torch.cuda.synchronize()
+    khat = _cache(env, w["k"][:, :, 100:T_cap].double().numpy(), 4)[1]
+    vhat = _cache(env, w["v"][:, :, 100:T_cap].double().numpy(), 2)[1]
+    ref = oracle.attention_dequantized(w["q"].double().numpy(), khat, vhat, scale)
+    assert np.all(attn_rel_err(out.double().cpu().numpy().reshape(-1, D), ref.reshape(-1, D)) < ATTN_TOL)

@@ -103,6 +103,10 @@ struct PfArgs {
     float kc[16], vc[16];
     uint32_t signs[4];
     int drop;               // test hook: issue no bulk copies (the waits for them run out)
+    // paged cache (NULL table: contiguous [B][Hkv][T_cap]): pages of `page` tokens in pools
+    // [pages][Hkv][page]; token t of sequence b is slot t % page of page table[b * max_pages + t / page]
+    const int32_t *table;
+    int max_pages, page;
 };
 
 __device__ __forceinline__ uint64_t pf_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -331,9 +335,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 const uint32_t dst = base_s + S::kBlk + s * S::kBlkBytes;
                 if (!a.drop) {   // (test hook: no copy, so the key warps' wait runs out)
                     tc_mbar_expect_tx(bar(kBlkFull + s), (uint32_t)(nk * (a.kbb + a.vbb)));
-                    pf_bulk_g2s(dst, a.k + (row0 + t0) * a.kbb, (uint32_t)(nk * a.kbb), bar(kBlkFull + s));
-                    pf_bulk_g2s(dst + kPfKeys * a.kbb, a.v + (row0 + t0) * a.vbb, (uint32_t)(nk * a.vbb),
-                                bar(kBlkFull + s));
+                    if (!a.table) {
+                        pf_bulk_g2s(dst, a.k + (row0 + t0) * a.kbb, (uint32_t)(nk * a.kbb), bar(kBlkFull + s));
+                        pf_bulk_g2s(dst + kPfKeys * a.kbb, a.v + (row0 + t0) * a.vbb, (uint32_t)(nk * a.vbb),
+                                    bar(kBlkFull + s));
+                    } else {
+                        // one pair of copies per page the tile touches (pieces of a multiple of 8 tokens)
+                        for (int t = t0; t < t0 + nk;) {
+                            const int pg = t / a.page, off = t - pg * a.page;
+                            const int n = min(t0 + nk - t, a.page - off);
+                            const int64_t slot = ((int64_t)a.table[(int64_t)b * a.max_pages + pg] * a.Hkv + kvh) *
+                                                     a.page + off;
+                            pf_bulk_g2s(dst + (t - t0) * a.kbb, a.k + slot * a.kbb, (uint32_t)(n * a.kbb),
+                                        bar(kBlkFull + s));
+                            pf_bulk_g2s(dst + kPfKeys * a.kbb + (t - t0) * a.vbb, a.v + slot * a.vbb,
+                                        (uint32_t)(n * a.vbb), bar(kBlkFull + s));
+                            t += n;
+                        }
+                    }
                 }
             }
         }
@@ -639,10 +658,12 @@ int wait_failed_prefill(unsigned *v, bool clear) { return read_wait_failed(v, cl
 
 using namespace tq;
 
-extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
-                               const uint8_t *v_blocks, const tq_codebook *vcb, const int32_t *seq_lens, int B,
-                               int M, int Hq, int Hkv, int T_cap, int T, float scale, tq_signs signs, float *out,
-                               void *stream) {
+namespace {
+
+int prefill_call(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb, const uint8_t *v_blocks,
+                 const tq_codebook *vcb, const int32_t *seq_lens, int B, int M, int Hq, int Hkv, int T_cap, int T,
+                 float scale, tq_signs signs, float *out, const int32_t *table, int max_pages, int page,
+                 void *stream) {
     if (!q || !k_blocks || !kcb || !v_blocks || !vcb || !out) return TQ_ERR_ARG;
     if (B <= 0 || M <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || (T_cap & 7))
         return TQ_ERR_ARG;
@@ -675,6 +696,9 @@ extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_bloc
     }
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
     a.drop = drop_copies();
+    a.table = table;
+    a.max_pages = max_pages;
+    a.page = page;
     const int64_t rows = (int64_t)M * a.G;
     a.row_tiles = (int)((rows + kPfRows - 1) / kPfRows);
     const int64_t grid = (int64_t)B * Hkv * a.row_tiles;
@@ -687,4 +711,34 @@ extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_bloc
         case 8: return vcb->bits == 8 ? TQ_ERR_UNSUPPORTED : launch_prefill_v<8>(a, vcb->bits, (int)grid, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
+}
+
+}  // namespace
+
+extern "C" int tq_attn_prefill(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
+                               const uint8_t *v_blocks, const tq_codebook *vcb, const int32_t *seq_lens, int B,
+                               int M, int Hq, int Hkv, int T_cap, int T, float scale, tq_signs signs, float *out,
+                               void *stream) {
+    return prefill_call(q, q_dtype, k_blocks, kcb, v_blocks, vcb, seq_lens, B, M, Hq, Hkv, T_cap, T, scale, signs,
+                        out, nullptr, 0, 0, stream);
+}
+
+extern "C" int tq_attn_prefill_paged(const void *q, int q_dtype, const uint8_t *k_pool, const tq_codebook *kcb,
+                                     const uint8_t *v_pool, const tq_codebook *vcb, const int32_t *block_table,
+                                     int max_pages, int page_tokens, const int32_t *seq_lens, int B, int M, int Hq,
+                                     int Hkv, int T, float scale, tq_signs signs, float *out, void *stream) {
+    if (!block_table || max_pages <= 0 || page_tokens <= 0 || (page_tokens & 7)) return TQ_ERR_ARG;
+    if ((int64_t)max_pages * page_tokens < T || (int64_t)max_pages * page_tokens > 0x7FFFFFFF) return TQ_ERR_ARG;
+    // the kernel's key range never passes T: T_cap = T rounded up to 8 stands for the table's span
+    const int T_cap = (T + 7) & ~7;
+    return prefill_call(q, q_dtype, k_pool, kcb, v_pool, vcb, seq_lens, B, M, Hq, Hkv, T_cap, T, scale, signs, out,
+                        block_table, max_pages, page_tokens, stream);
+}
+
+extern "C" int tq_attn_decode_paged(const void *q, int q_dtype, const uint8_t *k_pool, const tq_codebook *kcb,
+                                    const uint8_t *v_pool, const tq_codebook *vcb, const int32_t *block_table,
+                                    int max_pages, int page_tokens, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                                    int T, float scale, tq_signs signs, float *out, void *stream) {
+    return tq_attn_prefill_paged(q, q_dtype, k_pool, kcb, v_pool, vcb, block_table, max_pages, page_tokens, seq_lens,
+                                 B, 1, Hq, Hkv, T, scale, signs, out, stream);
 }

@@ -71,6 +71,10 @@ def lib():
         L.tq_block_bytes_ex.restype = sz
         L.tq_encode_kv_ex.argtypes = [vp, c_int, i64, i64, cbp, tq_signs, vp, i64, vp, c_int, vp]
         L.tq_decode_kv_ex.argtypes = [vp, i64, i64, cbp, tq_signs, vp, c_int, i64, c_int, vp]
+        L.tq_attn_prefill_paged.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, vp, c_int, c_int, c_int,
+                                            c_int, c_int, ctypes.c_float, tq_signs, vp, vp]
+        L.tq_attn_decode_paged.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, vp, c_int, c_int, c_int,
+                                           c_int, ctypes.c_float, tq_signs, vp, vp]
         L.tq_device_status.argtypes = [c_int, vp]
         L.tq_debug_drop_copies.argtypes = [c_int]
         L.tq_attn_workspace_bytes_sms.argtypes = [c_int] * 5
@@ -284,3 +288,28 @@ def tq_decode_kv_ex(blocks, n_vec, cb, signs, out, flags=0, block_stride_bytes=N
     base = ctypes.c_void_p(blocks.data_ptr() + block_offset)
     _check(lib().tq_decode_kv_ex(base, bs, n_vec, ctypes.byref(cb), signs, _ptr(out), _dtype(out), stride, flags,
                                  _stream(stream)), "tq_decode_kv_ex")
+
+
+def tq_attn_prefill_paged(q, k_pool, kcb, v_pool, vcb, block_table, page_tokens, out, T, scale, signs,
+                          seq_lens=None, stream=None):
+    """Causal attention over a paged cache: q [B, M, Hq, 128]; k_pool / v_pool
+    uint8 [pages, Hkv, page_tokens, bytes]; block_table int32 [B, max_pages]."""
+    B, M, Hq, _ = q.shape
+    Hkv = k_pool.shape[1]
+    _check(lib().tq_attn_prefill_paged(_ptr(q), _dtype(q), _ptr(k_pool), ctypes.byref(kcb), _ptr(v_pool),
+                                       ctypes.byref(vcb), _ptr(block_table), block_table.shape[1], page_tokens,
+                                       _ptr(seq_lens), B, M, Hq, Hkv, T, ctypes.c_float(scale), signs, _ptr(out),
+                                       _stream(stream)), "tq_attn_prefill_paged")
+    return out
+
+
+def tq_attn_decode_paged(q, k_pool, kcb, v_pool, vcb, block_table, page_tokens, out, T, scale, signs,
+                         seq_lens=None, stream=None):
+    """Decode attention over a paged cache: q [B, Hq, 128], out [B, Hq, 128]."""
+    B, Hq, _ = q.shape
+    Hkv = k_pool.shape[1]
+    _check(lib().tq_attn_decode_paged(_ptr(q), _dtype(q), _ptr(k_pool), ctypes.byref(kcb), _ptr(v_pool),
+                                      ctypes.byref(vcb), _ptr(block_table), block_table.shape[1], page_tokens,
+                                      _ptr(seq_lens), B, Hq, Hkv, T, ctypes.c_float(scale), signs, _ptr(out),
+                                      _stream(stream)), "tq_attn_decode_paged")
+    return out
