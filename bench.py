@@ -72,6 +72,11 @@ WORKLOADS = {
     "llama3_8b_prefill": dict(B=16, Hq=32, Hkv=8, T=8192, M=64, head_dim=128, key_bits=4, value_bits=2,
                               kv_dtype="bf16", query="64 new tokens per sequence, causal",
                               scale="1/sqrt(128)"),
+    "llama3_8b_turboq8_pair": dict(B=16, Hq=32, Hkv=8, T=8192, head_dim=128, key_format="turboq8 (130 B)",
+                                   value_format="4-bit norm-corrected (66 B)", kv_dtype="bf16",
+                                   scale="1/sqrt(128)"),
+    "llama3_8b_paged_decode": dict(B=16, Hq=32, Hkv=8, T=8192, head_dim=128, key_bits=4, value_bits=2,
+                                   page_tokens=16, kv_dtype="bf16", scale="1/sqrt(128)"),
     "storage_roundtrip": dict(layout="[2, 32, 65536, 1024]", L=32, T=65536, hidden=1024, head_dim=128,
                               block_size=16, skip_first=2, skip_last=2, key_bits=4, value_bits=4, slot_bytes=132,
                               kv_dtype="bf16"),
@@ -84,6 +89,8 @@ KERNEL_SOURCES = {
     "encode": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "append": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "prefill": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
+    "pair_attention": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
+    "paged_attention": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
     "attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
                   "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_g1.cu",
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
@@ -673,6 +680,131 @@ def plan_prefill(tq, wl, dev, stream, seed, batch):
                 dtype="bf16", tensor="prefill")
 
 
+def plan_turboq8_pair(tq, wl, dev, stream, seed, batch):
+    """Llama-shaped decode step with the fork's high-precision asymmetric pair:
+    turboq8 keys, 4-bit norm-corrected values (encode the cache, one decode
+    step; the pair's attention runs as the one-token case of the tensor-core
+    causal attention)."""
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS[wl]
+    B, Hq, Hkv, T = batch or W["B"], W["Hq"], W["Hkv"], W["T"]
+    k8, v4 = tq.tq_codebook_load(128, 8), tq.tq_codebook_load(128, 4)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    data = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=seed, device=dev)
+    k, v, q = data["k"], data["v"], data["q"]
+    nvec = B * Hkv * T
+    kb = torch.empty((B, Hkv, T, 130), dtype=torch.uint8, device=dev)
+    vb = torch.empty((B, Hkv, T, 66), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(16, dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(128.0)
+
+    def attn(qq=q):
+        tq.tq_attn_decode(qq, kb, k8, vb, v4, out, ws, T, scale, signs, stream=stream)
+
+    ops = [Op("encode_k", "encode", lambda: tq.tq_encode_kv_ex(k.view(-1, 128), k8, signs, kb, stream=stream),
+              nvec * (256 + 130), 1, nvec),
+           Op("encode_v", "encode", lambda: tq.tq_encode_kv_ex(v.view(-1, 128), v4, signs, vb,
+                                                                flags=tq.TQ_FMT_NORM_CORRECT, stream=stream),
+              nvec * (256 + 66), 1, nvec),
+           Op("attention", "pair_attention", attn, nvec * (130 + 66) + q.numel() * 2 + out.numel() * 4, 1)]
+
+    def e2e():
+        hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev), torch.empty_like(q)
+
+        def step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            tq.tq_encode_kv_ex(dk, k8, signs, kb.view(nvec, -1), stream=stream)
+            tq.tq_encode_kv_ex(dv, v4, signs, vb.view(nvec, -1), flags=tq.TQ_FMT_NORM_CORRECT, stream=stream)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
+
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 2, out.numel() * 4
+
+    cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2; attention also timed after an L2 flush")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, config=cfg, dtype="bf16")
+
+
+def plan_paged(tq, wl, dev, stream, seed, batch):
+    """Llama-shaped decode step over a paged cache: the cache lives in a pool
+    of 16-token pages assigned to sequences in a seeded shuffled order; the
+    step encodes every token into its page slot (through a destination index)
+    and runs one decode step through the block table."""
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS[wl]
+    B, Hq, Hkv, T, P = batch or W["B"], W["Hq"], W["Hkv"], W["T"], W["page_tokens"]
+    kcb, vcb = tq.tq_codebook_load(128, 4), tq.tq_codebook_load(128, 2)
+    signs = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    data = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=seed, device=dev)
+    k, v, q = data["k"], data["v"], data["q"]
+    per = T // P
+    g = torch.Generator(device="cpu").manual_seed(seed + 7)
+    table = torch.randperm(B * per, generator=g).view(B, per).to(torch.int32).to(dev)
+    # destination slot of token t of (b, kvh): (page * Hkv + kvh) * P + t % P
+    t = torch.arange(T, device=dev)
+    pg = table.long()[:, None, t // P]                                   # [B, 1, T]
+    dst = ((pg * Hkv + torch.arange(Hkv, device=dev)[None, :, None]) * P + (t % P)[None, None, :]).reshape(-1)
+    nvec = B * Hkv * T
+    kp = torch.empty((B * per, Hkv, P, 66), dtype=torch.uint8, device=dev)
+    vp = torch.empty((B * per, Hkv, P, 34), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    scale = 1.0 / np.sqrt(128.0)
+    nb = step_bytes(B, Hq, Hkv, T)
+
+    def attn(qq=q):
+        tq.tq_attn_decode_paged(qq, kp, kcb, vp, vcb, table, P, out, T, scale, signs, stream=stream)
+
+    ops = [Op("encode_k", "encode", lambda: tq.tq_encode_kv(k.view(-1, 128), kcb, signs, kp.view(-1, 66),
+                                                            dst_index=dst, stream=stream), nb["enc_k"], 1, nvec),
+           Op("encode_v", "encode", lambda: tq.tq_encode_kv(v.view(-1, 128), vcb, signs, vp.view(-1, 34),
+                                                            dst_index=dst, stream=stream), nb["enc_v"], 1, nvec),
+           Op("attention", "paged_attention", attn, nb["attn"], 1)]
+
+    def e2e():
+        hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev), torch.empty_like(q)
+
+        def step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            tq.tq_encode_kv(dk, kcb, signs, kp.view(-1, 66), dst_index=dst, stream=stream)
+            tq.tq_encode_kv(dv, vcb, signs, vp.view(-1, 34), dst_index=dst, stream=stream)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
+
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 2, out.numel() * 4
+
+    cfg = dict(W, B=B, l2="inputs (537 MB) larger than L2; attention also timed after an L2 flush",
+               note="destination-index and block-table reads are not counted as algorithmic bytes")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, config=cfg, dtype="bf16")
+
+
 def plan_storage(tq, wl, dev, stream, seed, batch):
     from turboquant_bit_kv_gb300 import workloads
     W = WORKLOADS["storage_roundtrip"]
@@ -747,7 +879,8 @@ def plan_storage(tq, wl, dev, stream, seed, batch):
 
 
 PLANS = {"llama3_8b_decode": plan_llama, "single_head_fp32": plan_single_head, "qwen25_7b_append": plan_qwen,
-         "qjl_two_term": plan_qjl, "llama3_8b_prefill": plan_prefill, "storage_roundtrip": plan_storage}
+         "qjl_two_term": plan_qjl, "llama3_8b_prefill": plan_prefill, "llama3_8b_turboq8_pair": plan_turboq8_pair,
+         "llama3_8b_paged_decode": plan_paged, "storage_roundtrip": plan_storage}
 
 
 def _mean_ms(evs, a, b):
@@ -880,7 +1013,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # the metric: the decode-attention call's bytes over its time (per call,
     # averaged over the timed steps); without an attention call, the step's
-    attn = next((op for op in ops if op.group in ("attention", "prefill")), None)
+    attn = next((op for op in ops if op.name == "attention"), None)
     if attn is not None:
         a_ms = op_ms[ops.index(attn)]
         value = world * attn.nbytes / (a_ms * 1e-3) / 1e9
@@ -971,6 +1104,9 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
     books = _oracle_books()
     scale = 1 / np.sqrt(128)
     T = max(64, int(W["T"] * frac)) if "Hq" in W else 0
+    if workload in ("llama3_8b_turboq8_pair", "llama3_8b_paged_decode"):
+        workload = "llama3_8b_decode"
+        W = WORKLOADS[workload]
     if workload in ("llama3_8b_decode", "single_head_fp32", "qwen25_7b_append"):
         G = W["Hq"] // W["Hkv"]
         kbits, vbits = W["key_bits"], W["value_bits"]
@@ -1055,7 +1191,8 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
 
 
 CPU_GROUPS = {"llama3_8b_decode": 128, "single_head_fp32": 1, "qwen25_7b_append": 24, "qjl_two_term": 32,
-              "llama3_8b_prefill": 8, "storage_roundtrip": 64}
+              "llama3_8b_prefill": 8, "llama3_8b_turboq8_pair": 128, "llama3_8b_paged_decode": 128,
+              "storage_roundtrip": 64}
 
 
 def cpu_cores():
