@@ -76,7 +76,7 @@ WORKLOADS = {
                                    value_format="4-bit norm-corrected (66 B)", kv_dtype="bf16",
                                    scale="1/sqrt(128)"),
     "llama3_8b_paged_decode": dict(B=16, Hq=32, Hkv=8, T=8192, head_dim=128, key_bits=4, value_bits=2,
-                                   page_tokens=16, kv_dtype="bf16", scale="1/sqrt(128)"),
+                                   page_tokens=32, kv_dtype="bf16", scale="1/sqrt(128)"),
     "storage_roundtrip": dict(layout="[2, 32, 65536, 1024]", L=32, T=65536, hidden=1024, head_dim=128,
                               block_size=16, skip_first=2, skip_last=2, key_bits=4, value_bits=4, slot_bytes=132,
                               kv_dtype="bf16"),
@@ -90,7 +90,8 @@ KERNEL_SOURCES = {
     "append": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "prefill": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
     "pair_attention": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
-    "paged_attention": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
+    "paged_attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
+                        "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_device.cuh"],
     "attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
                   "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_g1.cu",
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
@@ -741,7 +742,7 @@ def plan_turboq8_pair(tq, wl, dev, stream, seed, batch):
 
 def plan_paged(tq, wl, dev, stream, seed, batch):
     """Llama-shaped decode step over a paged cache: the cache lives in a pool
-    of 16-token pages assigned to sequences in a seeded shuffled order; the
+    of 32-token pages assigned to sequences in a seeded shuffled order; the
     step encodes every token into its page slot (through a destination index)
     and runs one decode step through the block table."""
     from turboquant_bit_kv_gb300 import workloads
@@ -765,14 +766,16 @@ def plan_paged(tq, wl, dev, stream, seed, batch):
     scale = 1.0 / np.sqrt(128.0)
     nb = step_bytes(B, Hq, Hkv, T)
 
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+
     def attn(qq=q):
-        tq.tq_attn_decode_paged(qq, kp, kcb, vp, vcb, table, P, out, T, scale, signs, stream=stream)
+        tq.tq_attn_decode_paged(qq, kp, kcb, vp, vcb, table, P, out, T, scale, signs, workspace=ws, stream=stream)
 
     ops = [Op("encode_k", "encode", lambda: tq.tq_encode_kv(k.view(-1, 128), kcb, signs, kp.view(-1, 66),
                                                             dst_index=dst, stream=stream), nb["enc_k"], 1, nvec),
            Op("encode_v", "encode", lambda: tq.tq_encode_kv(v.view(-1, 128), vcb, signs, vp.view(-1, 34),
                                                             dst_index=dst, stream=stream), nb["enc_v"], 1, nvec),
-           Op("attention", "paged_attention", attn, nb["attn"], 1)]
+           Op("attention", "paged_attention", attn, nb["attn"], 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)

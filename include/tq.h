@@ -286,13 +286,20 @@ int tq_attn_prefill_paged(const void *q, int q_dtype,
                           float scale, tq_signs signs, float *out, void *stream);
 
 /* Decode attention (one query token per sequence, q [B][Hq][128], out
- * [B][Hq][128]) over a paged cache: tq_attn_prefill_paged with M = 1. */
+ * [B][Hq][128]) over a paged cache laid out as for tq_attn_prefill_paged.
+ * With 2/3/4-bit keys and values, pages of a multiple of 32 tokens and a
+ * workspace of >= tq_attn_workspace_bytes(B, Hq, Hkv, T rounded up to 8)
+ * bytes (16-byte aligned; clobbered), it runs the split-K tensor-core decode
+ * kernels of tq_attn_decode through the block table; otherwise (no
+ * workspace, other page sizes, turboq8) the one-token case of
+ * tq_attn_prefill_paged.  Errors as tq_attn_decode. */
 int tq_attn_decode_paged(const void *q, int q_dtype,
                          const uint8_t *k_pool, const tq_codebook *kcb,
                          const uint8_t *v_pool, const tq_codebook *vcb,
                          const int32_t *block_table, int max_pages, int page_tokens,
                          const int32_t *seq_lens, int B, int Hq, int Hkv, int T,
-                         float scale, tq_signs signs, float *out, void *stream);
+                         float scale, tq_signs signs, float *out,
+                         void *workspace, size_t workspace_bytes, void *stream);
 
 /* Size of the device array that tq_attn_decode_noalloc uses as its split-K
  * scratch: 16 MiB.  On GPUs of 148 to 160 SMs that covers, at any context,

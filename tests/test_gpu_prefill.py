@@ -241,3 +241,28 @@ def test_circular_cache_and_eviction(env):
     vhat = _cache(env, w["v"][:, :, 100:T_cap].double().numpy(), 2)[1]
     ref = oracle.attention_dequantized(w["q"].double().numpy(), khat, vhat, scale)
     assert np.all(attn_rel_err(out.double().cpu().numpy().reshape(-1, D), ref.reshape(-1, D)) < ATTN_TOL)
+
+
+@pytest.mark.parametrize("page,kbits,vbits,Hq,Hkv,lens", [
+    (32, 4, 2, 16, 4, [700, 333, 32]),      # the split-K decode kernels through the block table
+    (64, 3, 3, 28, 4, [700, 701, 1]),       # 7 heads per KV head (two n-tiles), a one-token sequence
+    (96, 2, 4, 8, 8, [650, 96, 95]),        # page boundaries at 96-token steps
+])
+def test_paged_decode_split_k(env, page, kbits, vbits, Hq, Hkv, lens):
+    tq, dev = env["tq"], env["dev"]
+    B, T = 3, 701
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=90 + page)
+    kblk, khat = _cache(env, w["k"].double().numpy(), kbits)
+    vblk, vhat = _cache(env, w["v"].double().numpy(), vbits)
+    kp, vp, table = _paged(kblk, vblk, page, np.random.default_rng(page + 1))
+    scale = 1 / np.sqrt(D)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, (T + 7) // 8 * 8), dtype=torch.uint8, device=dev)
+    tq.tq_attn_decode_paged(w["q"].to(dev), torch.from_numpy(kp).to(dev), env["cbs"][kbits],
+                            torch.from_numpy(vp).to(dev), env["cbs"][vbits], torch.from_numpy(table).to(dev), page,
+                            out, T, scale, env["signs"], seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev),
+                            workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.attention_dequantized(w["q"].double().numpy(), khat, vhat, scale, seq_lens=lens)
+    err = attn_rel_err(out.double().cpu().numpy().reshape(-1, D), ref.reshape(-1, D))
+    assert np.all(err < ATTN_TOL), err.max()

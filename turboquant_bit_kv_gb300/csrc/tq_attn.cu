@@ -263,6 +263,49 @@ static int attn_smem_bytes(int kb, int vb) {
 
 using namespace tq;
 
+namespace tq {
+
+int launch_attn_mma_paged_k2(const AttnArgs &a, MmaPlan &plan, int vb, int nt, cudaStream_t st);
+int launch_attn_mma_paged_k3(const AttnArgs &a, MmaPlan &plan, int vb, int nt, cudaStream_t st);
+int launch_attn_mma_paged_k4(const AttnArgs &a, MmaPlan &plan, int vb, int nt, cudaStream_t st);
+
+namespace {
+
+// The tensor-core decode path: query prep -> attention (contiguous or paged cache) -> combine,
+// chained as programmatic dependents.
+int mma_path(AttnArgs &a, int kb, int vb, bool qjl, bool packed_v, tq_signs signs, float *out, bool paged,
+             cudaStream_t st) {
+    MmaPlan mp = mma_plan(a.B, a.Hq, a.Hkv, a.T, kb, vb, qjl, a.G);
+    attn_prep_mma_kernel<<<a.B * a.Hkv, kAttnThreads, 0, st>>>(a, mp, qjl ? 1 : 0);
+    if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+    int r;
+    if (paged) {
+        const int nt = a.G <= 4 ? 1 : 2;
+        r = kb == 2 ? launch_attn_mma_paged_k2(a, mp, vb, nt, st)
+                    : kb == 3 ? launch_attn_mma_paged_k3(a, mp, vb, nt, st) : launch_attn_mma_paged_k4(a, mp, vb, nt, st);
+    } else {
+        r = launch_attn_mma(a, mp, kb, vb, qjl, st);
+    }
+    if (r != TQ_OK) return r;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
+    cfg.blockDim = dim3(kAttnThreads * mma_combine_groups(mp));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn_combine_mma_kernel, (const float *)a.ws, mp, a.Hq, a.Hkv, packed_v ? 1 : 0,
+                           signs.w[0], signs.w[1], signs.w[2], signs.w[3], out) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace tq
+
 extern "C" size_t tq_attn_workspace_bytes_sms(int B, int Hq, int Hkv, int T_cap, int sms) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv) return 0;
     int splits, tps;
@@ -307,6 +350,9 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
 
     AttnArgs a;
     a.drop = drop_copies();
+    a.table = nullptr;
+    a.max_pages = 0;
+    a.page = 0;
     a.q = q;
     a.q_dtype = q_dtype;
     a.k = k_blocks;
@@ -334,27 +380,7 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     const int smem = attn_smem_bytes(kb, vb);
     cudaStream_t st = (cudaStream_t)stream;
     dim3 grid(a.splits, Hkv, B);
-    if (attn_mma_supported(kb, vb, qjl, G)) {
-        MmaPlan mp = mma_plan(B, Hq, Hkv, T, kb, vb, qjl, G);
-        attn_prep_mma_kernel<<<B * Hkv, kAttnThreads, 0, st>>>(a, mp, qjl ? 1 : 0);
-        if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
-        int r = launch_attn_mma(a, mp, kb, vb, qjl, st);
-        if (r != TQ_OK) return r;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(B * Hq));
-        cfg.blockDim = dim3(kAttnThreads * mma_combine_groups(mp));
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, attn_combine_mma_kernel, (const float *)a.ws, mp, Hq, Hkv, vcb ? 1 : 0,
-                               signs.w[0], signs.w[1], signs.w[2], signs.w[3], out) != cudaSuccess)
-            return TQ_ERR_CUDA;
-        return launch_status();
-    }
+    if (attn_mma_supported(kb, vb, qjl, G)) return mma_path(a, kb, vb, qjl, vcb != nullptr, signs, out, false, st);
     int r;
     if (G == 1) r = launch_attn_split_g1(kb, vb, a, grid, smem, st);
     else if (G == 2) r = launch_attn_split_g2(kb, vb, a, grid, smem, st);
@@ -364,4 +390,59 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     attn_combine_kernel<<<B * Hq, kAttnThreads, 0, st>>>(a.ws, a.splits, vcb ? 1 : 0, signs.w[0], signs.w[1],
                                                           signs.w[2], signs.w[3], out);
     return launch_status();
+}
+
+extern "C" int tq_attn_decode_paged(const void *q, int q_dtype, const uint8_t *k_pool, const tq_codebook *kcb,
+                                    const uint8_t *v_pool, const tq_codebook *vcb, const int32_t *block_table,
+                                    int max_pages, int page_tokens, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                                    int T, float scale, tq_signs signs, float *out, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    if (!q || !k_pool || !kcb || !v_pool || !vcb || !out || !block_table) return TQ_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T < 1 || max_pages <= 0 || page_tokens <= 0 ||
+        (page_tokens & 7) || (int64_t)max_pages * page_tokens < T)
+        return TQ_ERR_ARG;
+    const int G = Hq / Hkv, kb = kcb->bits, vb = vcb->bits;
+    const int T8 = (T + 7) & ~7;
+    // the split-K tensor-core decode kernel: packed 2/3/4-bit keys and values, pages of a multiple
+    // of 32 tokens (a 32-token chunk never straddles two pages), a workspace
+    if (workspace && (page_tokens & 31) == 0 && codebook_ok(kcb) && codebook_ok(vcb) &&
+        attn_mma_supported(kb, vb, false, G)) {
+        if (!std::isfinite(scale)) return TQ_ERR_ARG;
+        if (dtype_bytes(q_dtype) == 0) return TQ_ERR_UNSUPPORTED;
+        if (!aligned(q, dtype_bytes(q_dtype)) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+            !aligned(workspace, 16))
+            return TQ_ERR_ALIGN;
+        if (workspace_bytes < tq_attn_workspace_bytes(B, Hq, Hkv, T8)) return TQ_ERR_WORKSPACE;
+        AttnArgs a;
+        a.drop = drop_copies();
+        a.q = q;
+        a.q_dtype = q_dtype;
+        a.k = k_pool;
+        a.v = v_pool;
+        a.seq_lens = seq_lens;
+        a.qjl_bits = nullptr;
+        a.rn = nullptr;
+        a.S = nullptr;
+        a.ws = static_cast<float *>(workspace);
+        a.B = B;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.G = G;
+        a.T_cap = T8;
+        a.T = T;
+        attn_split_plan(B, Hkv, T, &a.splits, &a.tiles_per_split);
+        a.qscale = scale * 1.4426950408889634f;
+        for (int i = 0; i < 16; ++i) {
+            a.kc[i] = kcb->centroids[i];
+            a.vc[i] = vcb->centroids[i];
+        }
+        for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
+        a.table = block_table;
+        a.max_pages = max_pages;
+        a.page = page_tokens;
+        return mma_path(a, kb, vb, false, true, signs, out, true, static_cast<cudaStream_t>(stream));
+    }
+    // otherwise the one-token case of the tensor-core causal attention (no workspace)
+    return tq_attn_prefill_paged(q, q_dtype, k_pool, kcb, v_pool, vcb, block_table, max_pages, page_tokens, seq_lens,
+                                 B, 1, Hq, Hkv, T, scale, signs, out, stream);
 }

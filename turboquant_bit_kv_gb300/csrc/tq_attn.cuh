@@ -41,6 +41,10 @@ struct AttnArgs {
     float kc[16], vc[16];
     uint32_t signs[4];
     int drop;                // test hook: issue no bulk copies (the waits for them run out)
+    // paged cache (the paged kernels only): token t of sequence b is slot t % page of page
+    // table[b * max_pages + t / page] of pools [pages][Hkv][page]; page a multiple of 32
+    const int32_t *table;
+    int max_pages, page;
 };
 
 __host__ __device__ inline int attn_tiles(int T) { return (T + kTT - 1) / kTT; }

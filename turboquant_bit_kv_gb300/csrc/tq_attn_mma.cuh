@@ -390,7 +390,15 @@ __device__ __forceinline__ void build_value_pair_lut(uint8_t *rows, const float 
 }
 
 
-template <int KB, int VB, bool QJL, int NT, bool WIDE>
+// Paged cache: the chunk of segment j starting at token t0 lies in one page (pages are multiples of
+// 32 tokens); the slot of token t0 in the pools, less t0 (so that row0 + t0 is that slot).
+__device__ __forceinline__ int64_t paged_row0(const AttnArgs &a, int j, int t0) {
+    const int pg = t0 / a.page;
+    return ((int64_t)a.table[(int64_t)(j / a.Hkv) * a.max_pages + pg] * a.Hkv + j % a.Hkv) * a.page +
+           (t0 - pg * a.page) - t0;
+}
+
+template <int KB, int VB, bool QJL, int NT, bool WIDE, bool PAGED = false>
 __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, VB, QJL, NT, WIDE>::kMinBlocks)
     attn_mma_kernel(const __grid_constant__ AttnArgs a, const MmaPlan plan) {
     using C = Cfg<KB, VB, QJL, NT, WIDE>;
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
     auto issue = [&](int buf, int j, int ci, int L) {
         const int t0 = ci * kMmaChunk;
         const int n = min(kMmaChunk, L - t0);
-        const int64_t row0 = (int64_t)j * a.T_cap;
+        const int64_t row0 = PAGED ? paged_row0(a, j, t0) : (int64_t)j * a.T_cap;
         const uint8_t *kbase = a.k + row0 * C::kKBytes;
         const uint8_t *vbase = a.v + row0 * C::kVBytes;
         const uint8_t *sgbase = QJL ? a.qjl_bits + row0 * 16 : nullptr;
@@ -468,17 +476,19 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
         }
         // partial chunk (the end of a sequence): 16-byte cp.async pieces, zero-filled past the tokens
         bulk_mask &= ~(1u << buf);
+        // (the address given with a zero-byte copy: the segment's start, or under paging the chunk's own)
+        const uint8_t *kz = PAGED ? sk : kbase, *vz = PAGED ? sv : vbase;
         const int nk = (n * C::kKBytes + 15) >> 4;
-        for (int q = lane; q < C::kKStage / 16; q += 32) cp16_zfill(dk + 16 * q, q < nk ? sk + 16 * q : kbase, q < nk);
+        for (int q = lane; q < C::kKStage / 16; q += 32) cp16_zfill(dk + 16 * q, q < nk ? sk + 16 * q : kz, q < nk);
         if constexpr (C::kRawV) {
             for (int q = lane; q < kMmaChunk * 16; q += 32) {
                 const int r = q >> 4, col = q & 15;
-                cp16_zfill(dv + r * kVtPitch + 16 * col, r < n ? sv + r * 256 + 16 * col : vbase, r < n);
+                cp16_zfill(dv + r * kVtPitch + 16 * col, r < n ? sv + r * 256 + 16 * col : vz, r < n);
             }
         } else {
             const int nvb = (n * C::kVBytes + 15) >> 4;
             for (int q = lane; q < C::kVStage / 16; q += 32)
-                cp16_zfill(dv + 16 * q, q < nvb ? sv + 16 * q : vbase, q < nvb);
+                cp16_zfill(dv + 16 * q, q < nvb ? sv + 16 * q : vz, q < nvb);
         }
         if constexpr (QJL) {
             const uint32_t ds = dv + C::kVStage, dr = ds + C::kSStage;
@@ -804,12 +814,13 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
     }
 }
 
-template <int KB, int VB, bool QJL, int NT, bool WIDE>
+template <int KB, int VB, bool QJL, int NT, bool WIDE, bool PAGED = false>
 int launch_cfg_w(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
     static_assert(!QJL || NT == 1, "the QJL term covers up to 4 query heads per KV head");
+    static_assert(!(QJL && PAGED), "paged caches hold packed keys and values only");
     using C = Cfg<KB, VB, QJL, NT, WIDE>;
     static int done[64] = {0};
-    if (set_smem_limit((const void *)attn_mma_kernel<KB, VB, QJL, NT, WIDE>, C::kSmemTotal, done) != TQ_OK)
+    if (set_smem_limit((const void *)attn_mma_kernel<KB, VB, QJL, NT, WIDE, PAGED>, C::kSmemTotal, done) != TQ_OK)
         return TQ_ERR_CUDA;
     // a programmatic dependent of the query-prep kernel: its prologue (first copies, tables) overlaps it
     cudaLaunchConfig_t cfg = {};
@@ -822,17 +833,18 @@ int launch_cfg_w(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, attn_mma_kernel<KB, VB, QJL, NT, WIDE>, a, plan) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, attn_mma_kernel<KB, VB, QJL, NT, WIDE, PAGED>, a, plan) != cudaSuccess)
+        return TQ_ERR_CUDA;
     return launch_status();
 }
 
 // Only 2-bit values with one n-tile have a narrow (12-warp) variant.
-template <int KB, int VB, bool QJL, int NT>
+template <int KB, int VB, bool QJL, int NT, bool PAGED = false>
 int launch_cfg(const AttnArgs &a, MmaPlan &plan, cudaStream_t st) {
     if constexpr (VB == 2 && NT == 1) {
-        if (!plan.wide) return launch_cfg_w<KB, VB, QJL, NT, false>(a, plan, st);
+        if (!plan.wide) return launch_cfg_w<KB, VB, QJL, NT, false, PAGED>(a, plan, st);
     }
-    return launch_cfg_w<KB, VB, QJL, NT, true>(a, plan, st);
+    return launch_cfg_w<KB, VB, QJL, NT, true, PAGED>(a, plan, st);
 }
 
 template <int KB, int VB, bool QJL, int NT>

@@ -25,6 +25,15 @@ int launch_attn_mma_k3(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int n
     return TQ_ERR_UNSUPPORTED;
 }
 
+// Paged caches (packed keys and values, no QJL term).
+int launch_attn_mma_paged_k3(const AttnArgs &a, MmaPlan &plan, int vb, int nt, cudaStream_t st) {
+#define TQ_CASE(V, N) \
+    if (vb == V && nt == N) return launch_cfg<3, V, false, N, true>(a, plan, st);
+    TQ_CASE(2, 1) TQ_CASE(3, 1) TQ_CASE(4, 1) TQ_CASE(2, 2) TQ_CASE(3, 2) TQ_CASE(4, 2)
+#undef TQ_CASE
+    return TQ_ERR_UNSUPPORTED;
+}
+
 int wait_failed_attn_k3(unsigned *v, bool clear) { return read_wait_failed(v, clear); }
 
 }  // namespace tq

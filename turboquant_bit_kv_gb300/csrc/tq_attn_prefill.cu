@@ -734,11 +734,3 @@ extern "C" int tq_attn_prefill_paged(const void *q, int q_dtype, const uint8_t *
     return prefill_call(q, q_dtype, k_pool, kcb, v_pool, vcb, seq_lens, B, M, Hq, Hkv, T_cap, T, scale, signs, out,
                         block_table, max_pages, page_tokens, stream);
 }
-
-extern "C" int tq_attn_decode_paged(const void *q, int q_dtype, const uint8_t *k_pool, const tq_codebook *kcb,
-                                    const uint8_t *v_pool, const tq_codebook *vcb, const int32_t *block_table,
-                                    int max_pages, int page_tokens, const int32_t *seq_lens, int B, int Hq, int Hkv,
-                                    int T, float scale, tq_signs signs, float *out, void *stream) {
-    return tq_attn_prefill_paged(q, q_dtype, k_pool, kcb, v_pool, vcb, block_table, max_pages, page_tokens, seq_lens,
-                                 B, 1, Hq, Hkv, T, scale, signs, out, stream);
-}

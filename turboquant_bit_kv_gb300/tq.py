@@ -74,7 +74,7 @@ def lib():
         L.tq_attn_prefill_paged.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, vp, c_int, c_int, c_int,
                                             c_int, c_int, ctypes.c_float, tq_signs, vp, vp]
         L.tq_attn_decode_paged.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, vp, c_int, c_int, c_int,
-                                           c_int, ctypes.c_float, tq_signs, vp, vp]
+                                           c_int, ctypes.c_float, tq_signs, vp, vp, sz, vp]
         L.tq_device_status.argtypes = [c_int, vp]
         L.tq_debug_drop_copies.argtypes = [c_int]
         L.tq_attn_workspace_bytes_sms.argtypes = [c_int] * 5
@@ -304,12 +304,14 @@ def tq_attn_prefill_paged(q, k_pool, kcb, v_pool, vcb, block_table, page_tokens,
 
 
 def tq_attn_decode_paged(q, k_pool, kcb, v_pool, vcb, block_table, page_tokens, out, T, scale, signs,
-                         seq_lens=None, stream=None):
-    """Decode attention over a paged cache: q [B, Hq, 128], out [B, Hq, 128]."""
+                         seq_lens=None, workspace=None, stream=None):
+    """Decode attention over a paged cache: q [B, Hq, 128], out [B, Hq, 128];
+    with a workspace (uint8 device tensor) the split-K decode kernels run."""
     B, Hq, _ = q.shape
     Hkv = k_pool.shape[1]
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().tq_attn_decode_paged(_ptr(q), _dtype(q), _ptr(k_pool), ctypes.byref(kcb), _ptr(v_pool),
                                       ctypes.byref(vcb), _ptr(block_table), block_table.shape[1], page_tokens,
                                       _ptr(seq_lens), B, Hq, Hkv, T, ctypes.c_float(scale), signs, _ptr(out),
-                                      _stream(stream)), "tq_attn_decode_paged")
+                                      _ptr(workspace), nbytes, _stream(stream)), "tq_attn_decode_paged")
     return out
