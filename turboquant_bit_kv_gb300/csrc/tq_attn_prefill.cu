@@ -23,20 +23,23 @@
 // value centroids are single fp16.  Key norms scale the scores, value norms
 // scale the probabilities.
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warps 0-3  row warps: thread r owns query row r = tensor-memory lane r.
-//              Prologue: rotated query rows into the A tiles.  Per key tile:
-//              read S, apply key norms and the causal mask, online softmax
-//              (the reference maximum moves only when a row's maximum
-//              exceeds it by more than 8 in log2 units, so that the
-//              accumulator in tensor memory is rarely rescaled), write P
-//              (times the value norms) as fp16 hi / lo tiles.  Epilogue:
-//              O / l, inverse rotation, store.
-//   warps 4-7  key warps: thread (k, h) dequantises half h of key k of the
-//              tile into the K hi / lo tiles and the V tile (centroid lookups
-//              in lane-replicated tables).
-//   warp 8     producer: bulk copies of the tile's packed K and V blocks.
-//   warp 9     one thread issues the tensor-core products.
+// Warp roles (448 threads, one CTA per SM):
+//   warps 0-7  row warps: threads (r, h) own query row r = tensor-memory
+//              lane r, keys 32 h .. 32 h + 31 of each tile (warps w and w + 4
+//              read the same lanes).  Per key tile: read S, apply key norms
+//              and the causal mask, share the row maximum with the other
+//              thread of the row, online softmax (the reference maximum
+//              moves only when a row's maximum exceeds it by more than 8 in
+//              log2 units, so that the accumulator in tensor memory is
+//              rarely rescaled), write P (times the value norms) as fp16
+//              hi / lo tiles.  Epilogue: O / l, inverse rotation (its last
+//              stage across the row's two threads), store.
+//   warps 8-11 key warps: thread (k, h) dequantises dims 64 h .. + 63 of key
+//              k of the tile into the K hi / lo tiles and the V tile
+//              (centroid lookups in lane-replicated tables).
+//   warp 12    producer: bulk copies of the tile's packed K and V blocks.
+//   warp 13    one thread issues the tensor-core products.
+// All warps prepare the rotated query rows in the prologue.
 // Key tiles and their packed blocks are double-buffered, as are the score
 // accumulators, so the products of tile j + 1 run while the row warps work on
 // tile j.  Every mbarrier wait is bounded; a wait that gives up is recorded
@@ -53,7 +56,11 @@ namespace {
 
 constexpr int kPfRows = 128;                 // query rows per CTA (MMA M, tensor-memory lanes)
 constexpr int kPfKeys = 64;                  // keys per tile (N of the scores, K of P V)
-constexpr int kPfThreads = 320;
+constexpr int kPfRowWarps = 8;               // two threads per query row (32 keys of a tile each)
+constexpr int kPfKeyWarps = 4;               // two threads per key (64 dims each)
+constexpr int kPfProducerWarp = kPfRowWarps + kPfKeyWarps;
+constexpr int kPfMmaWarp = kPfProducerWarp + 1;
+constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);   // 448
 constexpr uint32_t kPfCols = 256;            // tensor memory: S[2] (64 columns each) + O (128)
 constexpr uint32_t kPfColO = 128;
 
@@ -73,7 +80,8 @@ struct PfSmem {
     static constexpr int kNorm = kBlk + 2 * kBlkBytes;     // [2] kn[64] | vn[64] (float)
     static constexpr int kKTab = kNorm + 2 * 512;          // key centroids: 16 codes x 32 lanes x half2 (hi, lo)
     static constexpr int kVTab = kKTab + 2048;             // value centroids: 16 codes x 32 lanes x half2 (v, v)
-    static constexpr int kBars = kVTab + 2048;             // 16 mbarriers
+    static constexpr int kXch = kVTab + 2048;              // row max / sum exchange: [2][2][128] float
+    static constexpr int kBars = kXch + 2048;              // 16 mbarriers
     static constexpr int kSlot = kBars + 16 * 8;           // tensor-memory base address, failure flag
     static constexpr int kTotal = kSlot + 16 + 1024;       // + alignment slack of the base
     static_assert(kTotal <= 232448, "shared memory of one CTA");
@@ -164,35 +172,41 @@ __device__ __forceinline__ uint32_t pf_pack(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Code words of dims 64 h .. 64 h + 63 of the block at shared address `blk`
-// (2-byte aligned): 8-bit (turboq8): 16 words; 4-bit: 8 words; 2-bit: 4
-// words; 3-bit: 4 low-plane words then 2 high-plane words.
+// Code words of dims 32 q .. 32 q + 31 of the block at shared address `blk`
+// (2-byte aligned): 8-bit (turboq8): 8 words; 4-bit: 4 words; 2-bit: 2
+// words; 3-bit: 2 low-plane words then 1 high-plane word.
 template <int BITS>
-__device__ __forceinline__ void pf_code_words(uint32_t blk, int h, uint32_t (&w)[16]) {
+__device__ __forceinline__ void pf_code_words(uint32_t blk, int q, uint32_t (&w)[8]) {
+    auto word = [&](uint32_t at) { return pf_lds16(at) | (pf_lds16(at + 2) << 16); };
     if constexpr (BITS == 8) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pf_lds16(blk + 2 + 64 * h + 4 * i) | (pf_lds16(blk + 4 + 64 * h + 4 * i) << 16);
+        for (int i = 0; i < 8; ++i) w[i] = word(blk + 2 + 32 * q + 4 * i);
     } else if constexpr (BITS == 4) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = pf_lds16(blk + 2 + 32 * h + 4 * i) | (pf_lds16(blk + 4 + 32 * h + 4 * i) << 16);
+        for (int i = 0; i < 4; ++i) w[i] = word(blk + 2 + 16 * q + 4 * i);
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = pf_lds16(blk + 2 + 16 * h + 4 * i) | (pf_lds16(blk + 4 + 16 * h + 4 * i) << 16);
-        if constexpr (BITS == 3) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                w[4 + i] = pf_lds16(blk + 34 + 8 * h + 4 * i) | (pf_lds16(blk + 36 + 8 * h + 4 * i) << 16);
-        }
+        for (int i = 0; i < 2; ++i) w[i] = word(blk + 2 + 8 * q + 4 * i);
+        if constexpr (BITS == 3) w[2] = word(blk + 34 + 4 * q);
     }
 }
 
-// Code of relative dim e (0..63) from the words above.
+// Code of relative dim e (0..31) from the words above.
 template <int BITS>
-__device__ __forceinline__ uint32_t pf_code(const uint32_t (&w)[16], int e) {
+__device__ __forceinline__ uint32_t pf_code(const uint32_t (&w)[8], int e) {
     if constexpr (BITS == 8) return (w[e >> 2] >> (8 * (e & 3))) & 255u;
     else if constexpr (BITS == 4) return (w[e >> 3] >> (4 * (e & 7))) & 15u;
     else if constexpr (BITS == 2) return (w[e >> 4] >> (2 * (e & 15))) & 3u;
-    else return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[4 + (e >> 5)] >> (e & 31)) & 1u) << 2);
+    else return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[2] >> e) & 1u) << 2);
+}
+
+// (hi, lo) fp16 splits of two floats, packed as half2 words: x = hi + lo to about 2^-22.
+__device__ __forceinline__ void pf_split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 // turboq8 entry of code i: the grid level (i - 127.5) / 127.5 is (2 i - 255) / 255; the integer
@@ -273,12 +287,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         const float f = a.qscale * 0.08838834764831845f;
         uint32_t hi[2], lo[2];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const float e0 = v[2 * k] * f, e1 = v[2 * k + 1] * f;
-            const __half h0 = __float2half_rn(e0), h1 = __float2half_rn(e1);
-            hi[k] = pf_pack(__half2float(h0), __half2float(h1));
-            lo[k] = pf_pack(e0 - __half2float(h0), e1 - __half2float(h1));
-        }
+        for (int k = 0; k < 2; ++k) pf_split2(v[2 * k] * f, v[2 * k + 1] * f, hi[k], lo[k]);
         // dims 4 lane .. + 3: block lane >> 4, 16-byte chunk (lane & 15) >> 1, half of it lane & 1
         const int off = (lane >> 4) * 16384 + r * 128 + ((((lane & 15) >> 1) ^ (r & 7)) << 4) + (lane & 1) * 8;
         *reinterpret_cast<uint2 *>(smem + S::kQhi + off) = make_uint2(hi[0], hi[1]);
@@ -287,13 +296,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             tc_mbar_init(bar(kBlkFull + s), 1);
-            tc_mbar_init(bar(kBlkEmpty + s), 4);
-            tc_mbar_init(bar(kKvReady + s), 4);
+            tc_mbar_init(bar(kBlkEmpty + s), kPfKeyWarps);
+            tc_mbar_init(bar(kKvReady + s), kPfKeyWarps);
             tc_mbar_init(bar(kKvFree + s), 1);
             tc_mbar_init(bar(kSReady + s), 1);
-            tc_mbar_init(bar(kSFree + s), 4);
+            tc_mbar_init(bar(kSFree + s), kPfRowWarps);
         }
-        tc_mbar_init(bar(kPReady), 4);
+        tc_mbar_init(bar(kPReady), kPfRowWarps);
         tc_mbar_init(bar(kPvDone), 1);
         tc_mbar_init(bar(kDrain), 1);
         *fail_s = 0;
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         }
     };
 
-    if (warp == 8) {
+    if (warp == kPfProducerWarp) {
         // ---- producer: packed K and V blocks of each tile
         if (lane == 0) {
             bool ok = true;
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kPfMmaWarp) {
         // ---- the tensor-core products
         if (lane == 0) {
             bool ok = true;
@@ -365,10 +374,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 const int s = j & 1;
                 const uint32_t d = tmem + (uint32_t)(s * kPfKeys);
                 const uint32_t kh = base_s + S::kKhi + s * 16384, kl = base_s + S::kKlo + s * 16384;
+                // turboq8 keys are exact in fp16: no lo product
+                constexpr int kParts = KB == 8 ? 2 : 3;
 #pragma unroll
-                for (int part = 0; part < 3; ++part) {
-                    const uint32_t qa = base_s + (part == 2 ? S::kQlo : S::kQhi);
-                    const uint32_t kb = part == 1 ? kl : kh;
+                for (int part = 0; part < kParts; ++part) {
+                    const uint32_t qa = base_s + ((part == 2 || (KB == 8 && part == 1)) ? S::kQlo : S::kQhi);
+                    const uint32_t kb = (KB != 8 && part == 1) ? kl : kh;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t qo = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
@@ -418,9 +429,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             tc_commit(bar(kDrain));
             tc_mbar_wait(bar(kDrain), 0u);
         }
-    } else if (warp >= 4) {
-        // ---- key warps: thread (k, h) = half h of key k of the tile
-        const int kt = tid - 128, k = kt >> 1, h = kt & 1;
+    } else if (warp >= kPfRowWarps) {
+        // ---- key warps: thread (k, hk) = dims 64 hk .. 64 hk + 63 of key k of the tile, taken as the
+        // 32-dim quarters q = 2 hk, 2 hk + 1
+        const int kt = tid - 32 * kPfRowWarps, k = kt >> 1, hk = kt & 1;
         const uint32_t ktab = base_s + S::kKTab + 4u * lane, vtab = base_s + S::kVTab + 4u * lane;
         float *norms = reinterpret_cast<float *>(smem + S::kNorm);
         bool ok = true;
@@ -430,41 +442,45 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             if (u >= 1) wait(ok, kKvFree + s, (uint32_t)(u - 1) & 1u);
             const uint32_t blk = base_s + S::kBlk + s * S::kBlkBytes;
             const uint32_t kblk = blk + k * a.kbb, vblk = blk + kPfKeys * a.kbb + k * a.vbb;
-            const uint32_t row = (uint32_t)(h * 8192 + k * 128);
-            {
-                uint32_t w[16];
-                pf_code_words<KB>(kblk, h, w);
+            // dims 32 q .. + 31: 64-dim block q >> 1, 16-byte chunks 4 (q & 1) .. + 3 of row k
+            const uint32_t row = (uint32_t)(hk * 8192 + k * 128);
+#pragma unroll
+            for (int q = 2 * hk; q < 2 * hk + 2; ++q) {
+                uint32_t w[8];
+                pf_code_words<KB>(kblk, q, w);
                 const uint32_t khi = base_s + S::kKhi + s * 16384 + row, klo = base_s + S::kKlo + s * 16384 + row;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t e[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        e[q] = KB == 8 ? pf_q8_entry(pf_code<KB>(w, 8 * c + q), false)
-                                       : pf_lds32(ktab + pf_code<KB>(w, 8 * c + q) * 128u);
-                    const uint32_t sw = (uint32_t)(((c ^ (k & 7)) << 4));
+                    for (int i = 0; i < 8; ++i)
+                        e[i] = KB == 8 ? pf_q8_entry(pf_code<KB>(w, 8 * c + i), false)
+                                       : pf_lds32(ktab + pf_code<KB>(w, 8 * c + i) * 128u);
+                    const uint32_t sw = (uint32_t)((((4 * (q & 1) + c) ^ (k & 7)) << 4));
                     pf_sts128(khi + sw, pf_prmt(e[0], e[1], 0x5410), pf_prmt(e[2], e[3], 0x5410),
                               pf_prmt(e[4], e[5], 0x5410), pf_prmt(e[6], e[7], 0x5410));
-                    pf_sts128(klo + sw, pf_prmt(e[0], e[1], 0x7632), pf_prmt(e[2], e[3], 0x7632),
-                              pf_prmt(e[4], e[5], 0x7632), pf_prmt(e[6], e[7], 0x7632));
+                    if constexpr (KB != 8)
+                        pf_sts128(klo + sw, pf_prmt(e[0], e[1], 0x7632), pf_prmt(e[2], e[3], 0x7632),
+                                  pf_prmt(e[4], e[5], 0x7632), pf_prmt(e[6], e[7], 0x7632));
                 }
             }
-            {
-                uint32_t w[16];
-                pf_code_words<VB>(vblk, h, w);
+#pragma unroll
+            for (int q = 2 * hk; q < 2 * hk + 2; ++q) {
+                uint32_t w[8];
+                pf_code_words<VB>(vblk, q, w);
                 const uint32_t vt = base_s + S::kV + s * 16384 + row;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t e[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        e[q] = VB == 8 ? pf_q8_entry(pf_code<VB>(w, 8 * c + q), true)
-                                       : pf_lds32(vtab + pf_code<VB>(w, 8 * c + q) * 128u);
-                    pf_sts128(vt + (uint32_t)(((c ^ (k & 7)) << 4)), pf_prmt(e[0], e[1], 0x5410),
+                    for (int i = 0; i < 8; ++i)
+                        e[i] = VB == 8 ? pf_q8_entry(pf_code<VB>(w, 8 * c + i), true)
+                                       : pf_lds32(vtab + pf_code<VB>(w, 8 * c + i) * 128u);
+                    pf_sts128(vt + (uint32_t)((((4 * (q & 1) + c) ^ (k & 7)) << 4)), pf_prmt(e[0], e[1], 0x5410),
                               pf_prmt(e[2], e[3], 0x5410), pf_prmt(e[4], e[5], 0x5410), pf_prmt(e[6], e[7], 0x5410));
                 }
             }
-            if (h == 0) {
+            if (hk == 0) {
                 // the block's norm (turboq8: its scale over 255, the grid's step factor)
                 const float kf = KB == 8 ? (1.f / 255.f) : 1.f, vf = VB == 8 ? (1.f / 255.f) : 1.f;
                 norms[s * 128 + k] = __half2float(__ushort_as_half((unsigned short)pf_lds16(kblk))) * kf;
@@ -479,83 +495,80 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             }
         }
     } else {
-        // ---- row warps: thread r = query row r0 + r = tensor-memory lane r
-        const int r = tid, rg = r0 + r;
+        // ---- row warps: thread (r, h) = keys 32 h .. 32 h + 31 of each tile for query row r0 + r
+        // (tensor-memory lane r); the two threads of a row meet through shared memory on named
+        // barrier 1 (the eight row warps) to share the row maximum, the row sum and the output
+        const int r = tid & 127, h = tid >> 7, rg = r0 + r;
         const bool row_valid = rg < rows_total;
         const int qi = row_valid ? rg / a.G : 0;
         const int pos = L - a.M + qi;                  // this row's query position (keys 0 .. pos)
-        const uint32_t lane_t = tmem + ((uint32_t)(32 * warp) << 16);
+        const uint32_t lane_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const float *norms = reinterpret_cast<const float *>(smem + S::kNorm);
+        float *xch = reinterpret_cast<float *>(smem + S::kXch);   // [tile parity][half][128 rows]
+        auto rows_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kPfRowWarps) : "memory"); };
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int s = j & 1, u = j >> 1;
             wait(ok, kSReady + s, (uint32_t)u & 1u);
             tc_fence_after();
-            float sv[kPfKeys];
-            {
-                float t32[32];
-                tc_ld32(lane_t + (uint32_t)(s * kPfKeys), t32);
-                tc_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) sv[c] = t32[c];
-                tc_ld32(lane_t + (uint32_t)(s * kPfKeys + 32), t32);
-                tc_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) sv[32 + c] = t32[c];
-            }
+            float sv[32];
+            tc_ld32(lane_t + (uint32_t)(s * kPfKeys + 32 * h), sv);
+            tc_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bar(kSFree + s));
             // key norms and the causal mask (key t visible to the row iff t <= pos)
-            const int t0 = j * kPfKeys;
+            const int t0 = j * kPfKeys + 32 * h;
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kPfKeys; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 const bool vis = row_valid && t0 + c <= pos;
-                sv[c] = vis ? sv[c] * norms[s * 128 + c] : -INFINITY;
+                sv[c] = vis ? sv[c] * norms[s * 128 + 32 * h + c] : -INFINITY;
                 mx = fmaxf(mx, sv[c]);
             }
+            xch[(s * 2 + h) * 128 + r] = mx;
+            rows_sync();
+            mx = fmaxf(mx, xch[(s * 2 + (h ^ 1)) * 128 + r]);
             // the reference maximum moves when the row's maximum exceeds it by more than 8 (log2
             // units), so probabilities stay below 2^8 and O is rarely rescaled
             const bool move = mx > m_ref + 8.f;
             const float m_new = move ? mx : m_ref;
             const float factor = move ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
-            float sum = 0.f;
             // P of the previous tile has been consumed (and O is current) before P and O change
             if (j >= 1) wait(ok, kPvDone, (uint32_t)(j - 1) & 1u);
             tc_fence_after();
             if (j >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int c4 = 0; c4 < 2; ++c4) {
                     float o32[32];
-                    tc_ld32(lane_t + kPfColO + 32u * c4, o32);
+                    const uint32_t col = kPfColO + 64u * h + 32u * c4;
+                    tc_ld32(lane_t + col, o32);
                     tc_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) o32[c] *= factor;
-                    tc_st32(lane_t + kPfColO + 32u * c4, o32);
+                    tc_st32(lane_t + col, o32);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
+            float sum = 0.f;
             const uint32_t prow = (uint32_t)(r * 128);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int c8 = 0; c8 < 4; ++c8) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int qq = 0; qq < 4; ++qq) {
                     float pp[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int c = 8 * c8 + 2 * q + e;
+                        const int c = 8 * c8 + 2 * qq + e;
                         const float p = sv[c] == -INFINITY ? 0.f : exp2f(sv[c] - m_new);
                         sum += p;
-                        pp[e] = sv[c] == -INFINITY ? 0.f : p * norms[s * 128 + 64 + c];
+                        pp[e] = sv[c] == -INFINITY ? 0.f : p * norms[s * 128 + 64 + 32 * h + c];
                     }
-                    const __half h0 = __float2half_rn(pp[0]), h1 = __float2half_rn(pp[1]);
-                    hw[q] = pf_pack(__half2float(h0), __half2float(h1));
-                    lw[q] = pf_pack(pp[0] - __half2float(h0), pp[1] - __half2float(h1));
+                    pf_split2(pp[0], pp[1], hw[qq], lw[qq]);
                 }
-                const uint32_t sw = (uint32_t)(((c8 ^ (r & 7)) << 4));
+                const uint32_t sw = (uint32_t)((((4 * h + c8) ^ (r & 7)) << 4));
                 pf_sts128(base_s + S::kPhi + prow + sw, hw[0], hw[1], hw[2], hw[3]);
                 pf_sts128(base_s + S::kPlo + prow + sw, lw[0], lw[1], lw[2], lw[3]);
             }
@@ -566,28 +579,33 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bar(kPReady));
         }
-        // ---- epilogue: o = O / l, rotated back: D H o / sqrt(128)
+        // ---- epilogue: o = O / l, rotated back: D H o / sqrt(128); this thread holds dims 64 h .. + 63
         if (n_tiles > 0) wait(ok, kPvDone, (uint32_t)(n_tiles - 1) & 1u);
         tc_fence_after();
-        float o[128];
+        // (the exchange slot of parity n_tiles was last read before the last tile's barrier)
+        const int se = n_tiles & 1;
+        xch[(se * 2 + h) * 128 + r] = l;
+        rows_sync();
+        const float lt = l + xch[(se * 2 + (h ^ 1)) * 128 + r];
+        float o[64];
         if (n_tiles > 0) {
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c4 = 0; c4 < 2; ++c4) {
                 float o32[32];
-                tc_ld32(lane_t + kPfColO + 32u * c4, o32);
+                tc_ld32(lane_t + kPfColO + 64u * h + 32u * c4, o32);
                 tc_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 32; ++c) o[32 * c4 + c] = o32[c];
             }
         } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) o[c] = 0.f;
+            for (int c = 0; c < 64; ++c) o[c] = 0.f;
         }
-        const float inv = (l > 0.f && ok) ? 0.08838834764831845f / l : (ok ? 0.f : __int_as_float(0x7fc00000));
+        const float inv = (lt > 0.f && ok) ? 0.08838834764831845f / lt : (ok ? 0.f : __int_as_float(0x7fc00000));
 #pragma unroll
-        for (int m = 1; m < 128; m <<= 1) {
+        for (int m = 1; m < 64; m <<= 1) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
+            for (int c = 0; c < 64; ++c) {
                 if ((c & m) == 0) {
                     const float x = o[c], y = o[c + m];
                     o[c] = x + y;
@@ -595,17 +613,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 }
             }
         }
+        // the last butterfly stage pairs dim d of the low half with d + 64 of the high half: through
+        // shared memory (the query tiles, no longer read once every product has completed)
+        float *ox = reinterpret_cast<float *>(smem + S::kQhi);   // [128 rows][2 halves][64]
+#pragma unroll
+        for (int c = 0; c < 64; ++c) ox[(r * 2 + h) * 64 + ((c + r) & 63)] = o[c];
+        rows_sync();
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            const float other = ox[(r * 2 + (h ^ 1)) * 64 + ((c + r) & 63)];
+            o[c] = h ? (other - o[c]) : (o[c] + other);
+        }
         if (row_valid) {
             const int hq = kvh * a.G + rg % a.G;
-            float4 *dst = reinterpret_cast<float4 *>(a.out + (((int64_t)b * a.M + qi) * a.Hq + hq) * kD);
+            float4 *dst = reinterpret_cast<float4 *>(a.out + (((int64_t)b * a.M + qi) * a.Hq + hq) * kD + 64 * h);
 #pragma unroll
-            for (int c4 = 0; c4 < 32; ++c4) {
+            for (int c4 = 0; c4 < 16; ++c4) {
                 float e[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int d = 4 * c4 + q;
-                    const float x = o[d] * inv;
-                    e[q] = ((a.signs[d >> 5] >> (d & 31)) & 1u) ? -x : x;
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int d = 64 * h + 4 * c4 + qq;
+                    const float x = o[4 * c4 + qq] * inv;
+                    e[qq] = ((a.signs[d >> 5] >> (d & 31)) & 1u) ? -x : x;
                 }
                 dst[c4] = make_float4(e[0], e[1], e[2], e[3]);
             }

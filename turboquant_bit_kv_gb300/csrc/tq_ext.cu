@@ -27,6 +27,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -48,6 +49,9 @@ struct ExtArgs {
     float c[16];             // centroids
     float b[16];             // boundaries (ascending; unused entries +inf)
     uint32_t signs[4];
+    float grid;              // cells per unit of y of the table below
+    float2 cells[128];       // cell j = floor(grid y + 64): (boundary inside it | +inf, #boundaries below as bits)
+    int contiguous;          // blocks back to back from a 16-byte aligned start, no destination index
 };
 
 __device__ __forceinline__ float sign_of(const uint32_t (&s)[4], int d) {
@@ -135,14 +139,18 @@ __device__ __forceinline__ uint32_t level_of(float y, const float *b) {
 
 __device__ __forceinline__ void st16(uint8_t *p, uint32_t v) { *reinterpret_cast<uint16_t *>(p) = (uint16_t)v; }
 
+// Staged output blocks of a CTA pass: up to 128 rows of the largest (130-byte) block, back to back.
+constexpr int kExtStage = (kExtThreads / 2) * 130;
+
 template <int BITS, int DT>
-__global__ void __launch_bounds__(kExtThreads) encode_ext_kernel(const __grid_constant__ ExtArgs a) {
-    __shared__ float s_b[16], s_c[16];
-    if (threadIdx.x < 16) {
-        s_b[threadIdx.x] = a.b[threadIdx.x];
-        s_c[threadIdx.x] = a.c[threadIdx.x];
-    }
+__global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid_constant__ ExtArgs a) {
+    __shared__ float s_c[16];
+    __shared__ float2 s_cell[128];
+    __shared__ __align__(16) uint8_t s_out[kExtStage];
+    if (threadIdx.x < 16) s_c[threadIdx.x] = a.c[threadIdx.x];
+    if (threadIdx.x < 128) s_cell[threadIdx.x] = a.cells[threadIdx.x];
     __syncthreads();
+    constexpr int BB = BITS == 8 ? 130 : 2 + 16 * BITS;
     const int h = threadIdx.x & 1;
     for (int64_t base = (int64_t)blockIdx.x * (kExtThreads / 2); base < a.n_vec;
          base += (int64_t)gridDim.x * (kExtThreads / 2)) {
@@ -213,7 +221,11 @@ __global__ void __launch_bounds__(kExtThreads) encode_ext_kernel(const __grid_co
             float csq = 0.f;
 #pragma unroll
             for (int e = 0; e < 64; ++e) {
-                const uint32_t c = level_of<BITS>(v[e] * inv, s_b);
+                // #{i : b_i <= y}: the cell's count below plus its one inner boundary
+                const float y = v[e] * inv;
+                const int j = min(127, max(0, (int)fmaf(a.grid, y, 64.f)));
+                const float2 cell = s_cell[j];
+                const uint32_t c = __float_as_uint(cell.y) + (y >= cell.x ? 1u : 0u);
                 code[e] = (uint8_t)c;
                 csq = fmaf(s_c[c], s_c[c], csq);
             }
@@ -237,9 +249,7 @@ __global__ void __launch_bounds__(kExtThreads) encode_ext_kernel(const __grid_co
             }
             if (!(n > 0.f)) n16 = 0;
         }
-        if (!valid) continue;
-        const int64_t di = a.dst_index ? a.dst_index[row] : row;
-        uint8_t *blk = a.blocks + di * a.block_stride;
+        uint8_t *blk = s_out + (threadIdx.x >> 1) * BB;   // staged back to back, then stored by the CTA
         if (h == 0) st16(blk, n16);
         if constexpr (BITS == 8) {
 #pragma unroll
@@ -288,13 +298,33 @@ __global__ void __launch_bounds__(kExtThreads) encode_ext_kernel(const __grid_co
                 st16(blk + 34 + 8 * h + 2 * k, w);
             }
         }
+        __syncthreads();
+        // the CTA's blocks: contiguous ones as 16-byte pieces, others row by row in 2-byte pieces
+        const int nrows = (int)min64(kExtThreads / 2, a.n_vec - base);
+        if (a.contiguous) {
+            // the pass's blocks form one run starting 16-byte aligned (128 x BB is a multiple of 16)
+            uint4 *dst = reinterpret_cast<uint4 *>(a.blocks + base * BB);
+            const uint4 *src = reinterpret_cast<const uint4 *>(s_out);
+            const int n16 = nrows * BB / 16;
+            for (int q = threadIdx.x; q < n16; q += kExtThreads) dst[q] = src[q];
+            for (int q = 16 * n16 + threadIdx.x; q < nrows * BB; q += kExtThreads) a.blocks[base * BB + q] = s_out[q];
+        } else {
+            constexpr int NH = BB / 2;
+            for (int q = threadIdx.x; q < nrows * NH; q += kExtThreads) {
+                const int r = q / NH, o = 2 * (q - r * NH);
+                const int64_t di = a.dst_index ? a.dst_index[base + r] : base + r;
+                *reinterpret_cast<uint16_t *>(a.blocks + di * a.block_stride + o) =
+                    *reinterpret_cast<const uint16_t *>(s_out + r * BB + o);
+            }
+        }
+        __syncthreads();
     }
 }
 
 __device__ __forceinline__ uint32_t ld16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
 
 template <int BITS, int DT>
-__global__ void __launch_bounds__(kExtThreads) decode_ext_kernel(const __grid_constant__ ExtArgs a) {
+__global__ void __launch_bounds__(kExtThreads, 2) decode_ext_kernel(const __grid_constant__ ExtArgs a) {
     __shared__ float s_c[16];
     if (threadIdx.x < 16) s_c[threadIdx.x] = a.c[threadIdx.x];
     __syncthreads();
@@ -445,6 +475,28 @@ void ext_tables(const tq_codebook *cb, ExtArgs *a) {
         a->c[i] = (cb->bits != 8 && i < cb->levels) ? cb->centroids[i] : 0.f;
         a->b[i] = (cb->bits != 8 && i + 1 < cb->levels) ? cb->boundaries[i] : INFINITY;
     }
+    // cells of width 1 / grid over y in [-1, 1], each holding at most one boundary: cell j covers
+    // grid y + 64 in [j, j + 1); it lists the boundaries at or below its start and the one inside it
+    a->grid = 1.f;
+    for (int j = 0; j < 128; ++j) a->cells[j] = make_float2(INFINITY, 0.f);
+    if (cb->bits == 8) return;
+    const int L = cb->levels;
+    double gap = 2.0;
+    for (int i = 0; i + 2 < L; ++i) gap = std::min(gap, (double)cb->boundaries[i + 1] - (double)cb->boundaries[i]);
+    const float G = (float)std::min(62.0, std::floor(1.0 / gap) + 1.0);
+    a->grid = G;
+    for (int j = 0; j < 128; ++j) {
+        uint32_t below = 0;
+        float inner = INFINITY;
+        for (int i = 0; i + 1 < L; ++i) {
+            const double z = (double)G * (double)cb->boundaries[i] + 64.0;
+            if (z <= (double)j) ++below;
+            else if (z < (double)j + 1.0) inner = cb->boundaries[i];
+        }
+        float bf;
+        std::memcpy(&bf, &below, 4);
+        a->cells[j] = make_float2(inner, bf);
+    }
 }
 
 }  // namespace
@@ -482,6 +534,7 @@ extern "C" int tq_encode_kv_ex(const void *x, int x_dtype, int64_t n_vec, int64_
     a.block_stride = block_stride_bytes;
     a.nc = (flags & TQ_FMT_NORM_CORRECT) ? 1 : 0;
     a.dense = (flags & TQ_FMT_DENSE3) ? 1 : 0;
+    a.contiguous = (!dst_index && block_stride_bytes == bb && aligned(blocks, 16)) ? 1 : 0;
     ext_tables(cb, &a);
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -517,6 +570,7 @@ extern "C" int tq_decode_kv_ex(const uint8_t *blocks, int64_t block_stride_bytes
     a.block_stride = block_stride_bytes;
     a.nc = 0;
     a.dense = (flags & TQ_FMT_DENSE3) ? 1 : 0;
+    a.contiguous = 0;
     ext_tables(cb, &a);
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
     cudaStream_t st = static_cast<cudaStream_t>(stream);
