@@ -285,7 +285,7 @@ def _oracle_cache(env, k, v, kbits, vbits):
     return out
 
 
-def _run_attn(env, q, kblk, vblk, kbits, vbits, T, T_cap, scale, seq_lens=None, qjl=None, v_raw=None):
+def _run_attn(env, q, kblk, vblk, kbits, vbits, T, T_cap, scale, seq_lens=None, qjl=None, v_raw=None, vcb=None):
     tq = env["tq"]
     dev = env["dev"]
     B, Hkv = kblk.shape[:2]
@@ -296,7 +296,7 @@ def _run_attn(env, q, kblk, vblk, kbits, vbits, T, T_cap, scale, seq_lens=None, 
     if v_raw is None:
         vb = torch.zeros((B, Hkv, T_cap, vblk.shape[-1]), dtype=torch.uint8)
         vb[:, :, :T] = torch.from_numpy(vblk)
-        vcb = env["cbs"][vbits]
+        vcb = env["cbs"][vbits] if vcb is None else vcb
     else:
         vb = torch.zeros((B, Hkv, T_cap, D), dtype=torch.float16)
         vb[:, :, :T] = v_raw
@@ -375,6 +375,33 @@ def test_attention_gqa_ragged(env, B, Hq, Hkv, T, T_cap, kbits, vbits, lens):
                                            seq_lens=lens)
     err = attn_rel_err(got, ref)
     assert np.all(err < ATTN_TOL), err.max()
+
+
+def test_attention_asymmetric_value_codebook(env):
+    """A caller's own value codebook (here the library's 3-bit one with one
+    centroid moved, so it is no longer symmetric) is looked up as given: the
+    decode matches the oracle decoded with the same centroids."""
+    from turboquant_bit_kv_gb300 import tq as tqm
+    B, Hq, Hkv, T, T_cap = 2, 14, 2, 300, 304
+    w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=23)
+    k = w["k"].double().numpy()
+    v = w["v"].double().numpy()
+    cache = _oracle_cache(env, k, v, 4, 3)
+    moved = np.asarray(env["books"][3][0], np.float32).copy()
+    moved[7] = np.float32(moved[7] * 1.25)
+    vcb = tqm.tq_codebook.from_buffer_copy(env["cbs"][3])
+    vcb.centroids[7] = float(moved[7])
+    idx, n16 = cache["v"]
+    v_hat = codec.decode(idx.reshape(-1, D), n16.reshape(-1), moved.astype(np.float64),
+                         env["s"]).reshape(v.shape)
+    scale = 1 / np.sqrt(D)
+    got = _run_attn(env, w["q"], cache["k_blk"], cache["v_blk"], 4, 3, T, T_cap, scale, vcb=vcb)
+    ref = oracle.attention_dequantized(w["q"].double().numpy(), cache["k_hat"], v_hat, scale)
+    err = attn_rel_err(got, ref)
+    assert np.all(err < ATTN_TOL), err.max()
+    # the library codebook gives a different result (the moved centroid matters)
+    lib = _run_attn(env, w["q"], cache["k_blk"], cache["v_blk"], 4, 3, T, T_cap, scale)
+    assert attn_rel_err(lib, got).max() > 10 * ATTN_TOL
 
 
 def test_attention_identical_keys_give_mean_value(env):

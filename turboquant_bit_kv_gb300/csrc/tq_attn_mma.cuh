@@ -15,11 +15,15 @@
 //   values  O[128 dims x 8 heads]  += Vhat^T[128 x 16] * P[16 tokens x 8]
 //   * Keys: a thread reads the code slice of its dims 32t..32t+31 per token
 //     (the MMA's k-columns permuted to match) and turns each pair of codes
-//     into the (hi, lo) pair of half2 fragment registers with one 8-byte
-//     lookup in a table replicated for 16 lanes; one byte permute yields
-//     the lookup offset (entry * 256 + lane offset).  The pair's table index
-//     is the code byte (4-bit), the nibble (2-bit), or the low nibble of the
-//     2-bit plane plus the two high-plane bits (3-bit).
+//     into the (hi, lo) pair of half2 fragment registers: two 4-byte lookups
+//     in a table with a copy per lane and the hi and lo halves in separate
+//     128-byte halves of each 256-byte row (so each lands straight in its
+//     MMA operand register), or, where the rows share space with the 2-bit
+//     value pairs or only 128-byte rows fit, one 8-byte lookup in a table
+//     replicated for 16 lanes; one byte permute yields the lookup offset
+//     (entry * 256 + lane offset).  The pair's table index is the code byte
+//     (4-bit), the nibble (2-bit), or the low nibble of the 2-bit plane plus
+//     the two high-plane bits (3-bit).
 //   * 2-bit values: a thread owns dims 16g..16g+15 (the MMA's m-rows
 //     permuted so that the two rows of an m-tile are dims d and d + 1), one
 //     32-bit code word per token; the code words of two tokens are
@@ -95,7 +99,10 @@ struct Cfg {
     static constexpr int kVtile = (kRegV || kRawV) ? 0 : 16 * kVtPitch;   // per-warp dequantised tile
     static constexpr int kKLutEntries = KB == 4 ? 256 : KB == 3 ? 64 : 16;
     static constexpr int kVLutEntries = VB == 4 ? 256 : VB == 3 ? 64 : 0;
-    static constexpr int kVLutBytes = kVLutEntries * 128 + (QJL ? 16 * 256 : 0);
+    // value-pair table rows: 256 bytes for 3-bit values (one byte permute yields entry * 256 + lane
+    // offset), 128 for the 256 entries of 4-bit values (offset by a multiply)
+    static constexpr int kVRow = VB == 3 ? 256 : 128;
+    static constexpr int kVLutBytes = kVLutEntries * kVRow + (QJL ? 16 * 256 : 0);
     static constexpr int kVtileBytes = kW * kVtile + kW * 3 * 8;
     // key-table rows of 256 bytes (offset from one byte permute) where they fit, else 128
     static constexpr int kKRow =
@@ -105,7 +112,7 @@ struct Cfg {
     static constexpr int kKRows = kRegV ? 256 : kKLutEntries;
     static constexpr int kSmemKLut = 0;
     static constexpr int kSmemVLut = kSmemKLut + kKRows * kKRow;
-    static constexpr int kSmemSLut = kSmemVLut + kVLutEntries * 128;
+    static constexpr int kSmemSLut = kSmemVLut + kVLutEntries * kVRow;
     static constexpr int kSmemVt = kSmemSLut + (QJL ? 16 * 256 : 0);
     static constexpr int kSmemBars = kSmemVt + kW * kVtile;
     static constexpr int kFixed = kSmemBars + kW * 3 * 8;                 // up to 3 mbarriers per warp
@@ -119,6 +126,10 @@ struct Cfg {
     static constexpr int kMinBlocks = (kW == 8 && NT == 1 && kSmemTotal <= 113 * 1024) ? 2 : 1;
     static_assert(kSmemTotal <= 227 * 1024, "shared memory");
     static_assert(!kRegV || kKRow == 256, "2-bit value pairs live in the upper half of 256-byte rows");
+    // key rows of 256 bytes not shared with value pairs hold the hi and lo halves in separate
+    // 128-byte halves, one word per lane: two 4-byte loads put them straight into the MMA's
+    // operand registers (an 8-byte (hi, lo) load would need register moves to regroup them)
+    static constexpr bool kKSplit = !kRegV && kKRow == 256;
     static_assert(kW * kMinBlocks <= kMmaMaxWarpsPerSm, "warps per SM");
 };
 
@@ -234,10 +245,10 @@ __device__ __forceinline__ void pair_codes(int e, int &c0, int &c1) {
     }
 }
 
-// Lane-replicated half2 table of a codebook: word e * 32 + l = (c[c0(e)],
-// c[c1(e)]) for every lane l; stores rotated by e so a warp's stores are
-// conflict-free.
-template <int BITS>
+// Lane-replicated half2 table of a codebook in rows of ROW bytes: word
+// e * ROW / 4 + l = (c[c0(e)], c[c1(e)]) for every lane l; stores rotated by
+// e so a warp's stores are conflict-free.
+template <int BITS, int ROW>
 __device__ __forceinline__ void build_pair_lut(uint32_t *lut, const float *cb, int tid, int nthreads) {
     constexpr int E = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
     for (int e = tid; e < E; e += nthreads) {
@@ -245,7 +256,7 @@ __device__ __forceinline__ void build_pair_lut(uint32_t *lut, const float *cb, i
         pair_codes<BITS>(e, c0, c1);
         const uint32_t val = pack_half2(cb[c0], cb[c1]);
 #pragma unroll 8
-        for (int j = 0; j < 32; ++j) lut[e * 32 + ((j + e) & 31)] = val;
+        for (int j = 0; j < 32; ++j) lut[e * (ROW / 4) + ((j + e) & 31)] = val;
     }
 }
 
@@ -266,6 +277,22 @@ __device__ __forceinline__ void build_split_lut(uint2 *lut, const float *cb, int
         const uint32_t hi = pack_half2(__half2float(h0), __half2float(h1));
         const uint32_t lo = pack_half2(cb[c0] - __half2float(h0), cb[c1] - __half2float(h1));
         lut[e * row_words + l] = make_uint2(hi, lo);
+    }
+}
+
+// The same table with 256-byte rows split by half: entry e holds hi at byte
+// e * 256 + 4 l and lo at e * 256 + 128 + 4 l for every lane l (conflict-free
+// 4-byte loads, one word per lane).
+template <int BITS>
+__device__ __forceinline__ void build_split_lut_hl(uint32_t *lut, const float *cb, int tid, int nthreads) {
+    constexpr int E = BITS == 4 ? 256 : BITS == 3 ? 64 : 16;
+    for (int q = tid; q < E * 32; q += nthreads) {
+        const int e = q >> 5, l = q & 31;
+        int c0, c1;
+        pair_codes<BITS>(e, c0, c1);
+        const __half h0 = __float2half_rn(cb[c0]), h1 = __float2half_rn(cb[c1]);
+        lut[e * 64 + l] = pack_half2(__half2float(h0), __half2float(h1));
+        lut[e * 64 + 32 + l] = pack_half2(cb[c0] - __half2float(h0), cb[c1] - __half2float(h1));
     }
 }
 
@@ -349,10 +376,11 @@ __device__ __forceinline__ void dequant_value_half(uint32_t blk_s, int hf, uint3
             sts128(row_s + 128 * hf + 32 * q, h[0], h[1], h[2], h[3]);
             sts128(row_s + 128 * hf + 32 * q + 16, h[4], h[5], h[6], h[7]);
         }
-    } else {  // VB == 3
+    } else {  // VB == 3: 256-byte rows, one byte permute yields entry * 256 + the lane offset
         uint32_t c[4], hb[2];
         lds_words_a2<4>(blk_s + 2 + 16 * hf, c);
         lds_words_a2<2>(blk_s + 34 + 8 * hf, hb);
+        const uint32_t lo8 = (threadIdx.x & 31) * 4;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t ev, od;
@@ -360,8 +388,8 @@ __device__ __forceinline__ void dequant_value_half(uint32_t blk_s, int hf, uint3
             uint32_t h[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                h[2 * i] = lds32(lut_s + prmt(ev, 0, 0x4440u + i) * 128u);
-                h[2 * i + 1] = lds32(lut_s + prmt(od, 0, 0x4440u + i) * 128u);
+                h[2 * i] = lds32(lut_s + prmt(ev, lo8, 0x6504u + 16u * i));
+                h[2 * i + 1] = lds32(lut_s + prmt(od, lo8, 0x6504u + 16u * i));
             }
             sts128(row_s + 128 * hf + 32 * q, h[0], h[1], h[2], h[3]);
             sts128(row_s + 128 * hf + 32 * q + 16, h[4], h[5], h[6], h[7]);
@@ -532,9 +560,12 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
         for (int s = 0; s + 1 < kS; ++s) issue_next();
     }
 
-    build_split_lut<KB>(reinterpret_cast<uint2 *>(smem + C::kSmemKLut), a.kc, tid, C::kThreads, C::kKRow / 8);
+    if constexpr (C::kKSplit)
+        build_split_lut_hl<KB>(reinterpret_cast<uint32_t *>(smem + C::kSmemKLut), a.kc, tid, C::kThreads);
+    else
+        build_split_lut<KB>(reinterpret_cast<uint2 *>(smem + C::kSmemKLut), a.kc, tid, C::kThreads, C::kKRow / 8);
     if constexpr (VB == 3 || VB == 4)
-        build_pair_lut<VB>(reinterpret_cast<uint32_t *>(smem + C::kSmemVLut), a.vc, tid, C::kThreads);
+        build_pair_lut<VB, C::kVRow>(reinterpret_cast<uint32_t *>(smem + C::kSmemVLut), a.vc, tid, C::kThreads);
     if constexpr (QJL) {
         // sign table: entry e (4 sign bits) = (half2(s0, s1), half2(s2, s3)), s = bit ? +1 : -1,
         // at byte e * 256 + lane * 8
@@ -548,8 +579,9 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
         }
     }
     if constexpr (C::kRegV) build_value_pair_lut(smem + C::kSmemKLut, a.vc, tid, C::kThreads);
-    const uint32_t klut_s = smem_s + C::kSmemKLut, klane = (lane & 15) * 8, vlane = 128 + klane;
-    const uint32_t vlut_s = smem_s + C::kSmemVLut + lane * 4;
+    const uint32_t klut_s = smem_s + C::kSmemKLut, klane = C::kKSplit ? lane * 4 : (lane & 15) * 8;
+    const uint32_t vlane = 128 + (lane & 15) * 8;
+    const uint32_t vlut_s = smem_s + C::kSmemVLut + (C::kVRow == 256 ? 0 : lane * 4);
     const uint32_t slut_s = smem_s + C::kSmemSLut + lane * 8;
     const uint32_t vt_s = smem_s + C::kSmemVt + warp * C::kVtile;
     __syncthreads();
@@ -632,12 +664,24 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                     uint32_t x0, y0, x1, y1;
                     ksl[mt][0].template pick<C::kKRow>(ks, klane, x0, y0);
                     ksl[mt][1].template pick<C::kKRow>(ks, klane, x1, y1);
-                    const uint2 a0 = lds64(klut_s + x0), a2 = lds64(klut_s + y0);
-                    const uint2 a1 = lds64(klut_s + x1), a3 = lds64(klut_s + y1);
+                    if constexpr (C::kKSplit) {
+                        const uint32_t h0 = lds32(klut_s + x0), h1 = lds32(klut_s + x1);
+                        const uint32_t h2 = lds32(klut_s + y0), h3 = lds32(klut_s + y1);
+                        const uint32_t l0 = lds32(klut_s + x0 + 128), l1 = lds32(klut_s + x1 + 128);
+                        const uint32_t l2 = lds32(klut_s + y0 + 128), l3 = lds32(klut_s + y1 + 128);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma16816(acc[nt][mt], a0.x, a1.x, a2.x, a3.x, qb[nt][ks][0], qb[nt][ks][1]);
-                        mma16816(acc[nt][mt], a0.y, a1.y, a2.y, a3.y, qb[nt][ks][0], qb[nt][ks][1]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816(acc[nt][mt], h0, h1, h2, h3, qb[nt][ks][0], qb[nt][ks][1]);
+                            mma16816(acc[nt][mt], l0, l1, l2, l3, qb[nt][ks][0], qb[nt][ks][1]);
+                        }
+                    } else {
+                        const uint2 a0 = lds64(klut_s + x0), a2 = lds64(klut_s + y0);
+                        const uint2 a1 = lds64(klut_s + x1), a3 = lds64(klut_s + y1);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816(acc[nt][mt], a0.x, a1.x, a2.x, a3.x, qb[nt][ks][0], qb[nt][ks][1]);
+                            mma16816(acc[nt][mt], a0.y, a1.y, a2.y, a3.y, qb[nt][ks][0], qb[nt][ks][1]);
+                        }
                     }
                 }
             }
