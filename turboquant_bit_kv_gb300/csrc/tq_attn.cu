@@ -129,13 +129,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prep_mma_kernel(const __gri
     const int p = warp;
     if (p < 2 || (p == 2 && qjl)) {
         const float *buf = p == 2 ? raw : qs;
+        // column g of n-tile nt: head 4 nt + g / 2, part g & 1 (hi, lo); with 5 to 8 query heads per
+        // KV head, head g, part nt
         const int nt = p == 2 ? 0 : p, g = lane >> 2, t = lane & 3;
+        const bool h8 = a.G > 4 && p < 2;
+        const int head = h8 ? g : 4 * nt + (g >> 1);
+        const bool lo_part = h8 ? nt == 1 : (g & 1) != 0;
         uint32_t w[16];
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const float4 q4 = reinterpret_cast<const float4 *>(buf + (4 * nt + (g >> 1)) * kD + 32 * t + 4 * ks)[0];
+            const float4 q4 = reinterpret_cast<const float4 *>(buf + head * kD + 32 * t + 4 * ks)[0];
             float e[4] = {q4.x, q4.y, q4.z, q4.w};
-            if (g & 1) {
+            if (lo_part) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) e[i] -= __half2float(__float2half_rn(e[i]));
             }

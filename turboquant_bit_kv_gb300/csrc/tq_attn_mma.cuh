@@ -9,7 +9,11 @@
 //
 // Once a tile of codes is looked up, every product is a dense contraction,
 // run as mma.sync m16n8k16 (fp16 operands, float32 accumulate; the G <= 8
-// query heads sharing a KV head fill N = 8, zero-padded):
+// query heads sharing a KV head fill N = 8, zero-padded; the query and P are
+// split hi + lo: with G <= 4 the n-tile's 8 columns are 4 heads x (hi, lo),
+// with G = 5..8 they are the 8 heads and the hi and lo parts go through
+// separate products into the same accumulators -- Khi Qhi, Khi Qlo, Klo Qhi
+// for the scores, V Phi and V Plo for the values):
 //   scores  S[16 tokens x 8 heads]  = Khat[16 x 128] * Qrot^T[128 x 8]
 //   QJL     S2[16 tokens x 8 heads] = Sgn[16 x 128] * (S q)^T[128 x 8]
 //   values  O[128 dims x 8 heads]  += Vhat^T[128 x 16] * P[16 tokens x 8]
@@ -73,10 +77,11 @@ constexpr unsigned kFull = 0xffffffffu;
 
 constexpr int align16(int x) { return (x + 15) & ~15; }
 
-// NT: n-tiles of the score / PV products.  Every tile has 8 columns = 4
-// query heads x (hi, lo) fp16 parts (query, sketched query and P are split
-// x = hi + lo so their products keep float32 precision); NT = 2 serves up to
-// 8 query heads per KV head.
+// NT: 1 serves up to 4 query heads per KV head with n-tiles of 8 columns =
+// 4 heads x (hi, lo) fp16 parts (query, sketched query and P are split
+// x = hi + lo so their products keep float32 precision); NT = 2 serves 5 to 8
+// heads with one n-tile of the 8 heads, the hi and lo parts as two operands
+// (kH8).
 template <int KB, int VB, bool QJL, int NT, bool WIDE = true>
 struct Cfg {
     // 2-bit values with one n-tile fit in 128 registers: one CTA of 16 warps
@@ -86,6 +91,8 @@ struct Cfg {
     // the rest run 8 warps.
     static constexpr int kW = (VB == 2 && NT == 1) ? (WIDE ? 16 : 12) : (NT == 2 && VB != 16) ? 12 : 8;
     static constexpr int kThreads = kW * 32;
+    static constexpr bool kH8 = NT == 2;   // one n-tile of 8 heads; hi / lo parts as separate products
+    static constexpr int kNO = kH8 ? 1 : NT;   // accumulator n-tiles
     static constexpr int kKBytes = 2 + 16 * KB;
     static constexpr bool kRawV = VB == 16;
     static constexpr bool kRegV = VB == 2;                 // value fragments straight from a pair table
@@ -294,6 +301,16 @@ __device__ __forceinline__ void build_split_lut_hl(uint32_t *lut, const float *c
         lut[e * 64 + l] = pack_half2(__half2float(h0), __half2float(h1));
         lut[e * 64 + 32 + l] = pack_half2(cb[c0] - __half2float(h0), cb[c1] - __half2float(h1));
     }
+}
+
+// (hi, lo) fp16 splits of two floats, packed as the half2 words hi = (hi0,
+// hi1) and lo = (lo0, lo1): x = hi + lo to about 2^-22.
+__device__ __forceinline__ void split2_half2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 // (hi, lo) fp16 split of x packed as one half2: x = hi + lo to about 2^-22.
@@ -593,7 +610,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
         const int L = seg_len(j);
         const int cb = j == j0 ? cb0 : 0, ce = seg_end(j, L);
         const int b = j / a.Hkv, kvh = j % a.Hkv;
-        // B fragments (n-tile nt, k-step ks) of the rotated, scaled query split hi | lo, and of S q
+        // B fragments (k-step ks) of the rotated, scaled query and of S q: n-tile nt of 4 heads x
+        // (hi, lo), or (kH8) nt = 0: the 8 heads' hi parts, nt = 1: their lo parts
         uint32_t qb[NT][8][2];
         uint32_t sb[QJL ? 8 : 1][2];
         {
@@ -620,10 +638,11 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
             }
         }
 
-        // accumulators: n-tile nt, m-tile m; columns (2t, 2t+1) = head 4 nt + t, (hi, lo) parts
-        float o[NT][8][4];
+        // accumulators: n-tile nt, m-tile m; columns (2t, 2t+1) = head 4 nt + t, (hi, lo) parts, or
+        // (kH8) heads 2t, 2t + 1.  Softmax slot i of this thread: head 4 i + t, or (kH8) 2t + i.
+        float o[C::kNO][8][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < C::kNO; ++nt)
 #pragma unroll
             for (int m = 0; m < 8; ++m) o[nt][m][0] = o[nt][m][1] = o[nt][m][2] = o[nt][m][3] = 0.f;
         float mrun[NT], lrun[NT];
@@ -652,9 +671,9 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
                 for (int rh = 0; rh < 2; ++rh) ksl[mt][rh].load(ks_s + (16 * mt + g + 8 * rh) * C::kKBytes, t);
-            float acc[NT][2][4];                 // [n-tile][m-tile][fragment]
+            float acc[C::kNO][2][4];             // [n-tile][m-tile][fragment]
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < C::kNO; ++nt)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
 #pragma unroll
@@ -669,11 +688,23 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                         const uint32_t h2 = lds32(klut_s + y0), h3 = lds32(klut_s + y1);
                         const uint32_t l0 = lds32(klut_s + x0 + 128), l1 = lds32(klut_s + x1 + 128);
                         const uint32_t l2 = lds32(klut_s + y0 + 128), l3 = lds32(klut_s + y1 + 128);
+                        if constexpr (C::kH8) {
+                            mma16816(acc[0][mt], h0, h1, h2, h3, qb[0][ks][0], qb[0][ks][1]);
+                            mma16816(acc[0][mt], h0, h1, h2, h3, qb[1][ks][0], qb[1][ks][1]);
+                            mma16816(acc[0][mt], l0, l1, l2, l3, qb[0][ks][0], qb[0][ks][1]);
+                        } else {
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            mma16816(acc[nt][mt], h0, h1, h2, h3, qb[nt][ks][0], qb[nt][ks][1]);
-                            mma16816(acc[nt][mt], l0, l1, l2, l3, qb[nt][ks][0], qb[nt][ks][1]);
+                            for (int nt = 0; nt < NT; ++nt) {
+                                mma16816(acc[nt][mt], h0, h1, h2, h3, qb[nt][ks][0], qb[nt][ks][1]);
+                                mma16816(acc[nt][mt], l0, l1, l2, l3, qb[nt][ks][0], qb[nt][ks][1]);
+                            }
                         }
+                    } else if constexpr (C::kH8) {
+                        const uint2 a0 = lds64(klut_s + x0), a2 = lds64(klut_s + y0);
+                        const uint2 a1 = lds64(klut_s + x1), a3 = lds64(klut_s + y1);
+                        mma16816(acc[0][mt], a0.x, a1.x, a2.x, a3.x, qb[0][ks][0], qb[0][ks][1]);
+                        mma16816(acc[0][mt], a0.x, a1.x, a2.x, a3.x, qb[1][ks][0], qb[1][ks][1]);
+                        mma16816(acc[0][mt], a0.y, a1.y, a2.y, a3.y, qb[0][ks][0], qb[0][ks][1]);
                     } else {
                         const uint2 a0 = lds64(klut_s + x0), a2 = lds64(klut_s + y0);
                         const uint2 a1 = lds64(klut_s + x1), a3 = lds64(klut_s + y1);
@@ -700,7 +731,7 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                     }
                 }
             }
-            // s[nt][mt][r]: head 4 nt + t, token 16 mt + g + 8 r
+            // s[i][mt][r]: softmax slot i, token 16 mt + g + 8 r
             float s[NT][2][2];
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
@@ -714,8 +745,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float ea = (acc[nt][mt][0] + acc[nt][mt][1]) * na;
-                    float eb = (acc[nt][mt][2] + acc[nt][mt][3]) * nb;
+                    float ea = (C::kH8 ? acc[0][mt][nt] : acc[nt][mt][0] + acc[nt][mt][1]) * na;
+                    float eb = (C::kH8 ? acc[0][mt][2 + nt] : acc[nt][mt][2] + acc[nt][mt][3]) * nb;
                     if constexpr (QJL) {
                         ea = fmaf(acc2[mt][0] + acc2[mt][1], ra, ea);
                         eb = fmaf(acc2[mt][2] + acc2[mt][3], rb, eb);
@@ -740,11 +771,11 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
             }
             if (__any_sync(kFull, moved)) {   // the running max rarely moves once it has settled
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < C::kNO; ++nt)
 #pragma unroll
                     for (int m = 0; m < 8; ++m)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) o[nt][m][q] *= corr[nt];
+                        for (int q = 0; q < 4; ++q) o[nt][m][q] *= corr[C::kH8 ? (q & 1) : nt];
             }
             // ---- P (times the value norm, split hi | lo) and P V for each 16-token tile
 #pragma unroll
@@ -755,15 +786,31 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                     nva = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + ta * C::kVBytes)));
                     nvb = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + tb * C::kVBytes)));
                 }
+                // B fragments of P (8 x 8 blocks of token rows g / g + 8, transposed): per n-tile, or
+                // (kH8) index 0: the hi parts of the 8 heads, 1: the lo parts
                 uint32_t b0[NT], b1[NT];
+                float pa[NT], pb[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float mm = mrun[nt];
-                    const float pa = mm == -INFINITY ? 0.f : exp2f(s[nt][mt][0] - mm);
-                    const float pb = mm == -INFINITY ? 0.f : exp2f(s[nt][mt][1] - mm);
-                    lrun[nt] += pa + pb;
-                    b0[nt] = movmatrix_trans(split_half2(pa * nva));
-                    b1[nt] = movmatrix_trans(split_half2(pb * nvb));
+                    pa[nt] = mm == -INFINITY ? 0.f : exp2f(s[nt][mt][0] - mm);
+                    pb[nt] = mm == -INFINITY ? 0.f : exp2f(s[nt][mt][1] - mm);
+                    lrun[nt] += pa[nt] + pb[nt];
+                }
+                if constexpr (C::kH8) {
+                    uint32_t ha, la, hb, lb;
+                    split2_half2(pa[0] * nva, pa[1] * nva, ha, la);
+                    split2_half2(pb[0] * nvb, pb[1] * nvb, hb, lb);
+                    b0[0] = movmatrix_trans(ha);
+                    b1[0] = movmatrix_trans(hb);
+                    b0[1] = movmatrix_trans(la);
+                    b1[1] = movmatrix_trans(lb);
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        b0[nt] = movmatrix_trans(split_half2(pa[nt] * nva));
+                        b1[nt] = movmatrix_trans(split_half2(pb[nt] * nvb));
+                    }
                 }
                 if constexpr (C::kRegV) {
                     // value codes of tokens 2t, 2t+1, 2t+8, 2t+9 of the tile: dims 16g..16g+15
@@ -787,7 +834,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                         const uint2 p = lds64(klut_s + prmt(xs, vlane, sel));
                         const uint2 r = lds64(klut_s + prmt(ys, vlane, sel));
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], p.x, p.y, r.x, r.y, b0[nt], b1[nt]);
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816(o[C::kH8 ? 0 : nt][m], p.x, p.y, r.x, r.y, b0[nt], b1[nt]);
                     }
                 } else {
                     uint32_t tile_s;
@@ -807,7 +855,8 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4_trans(arow + 32 * m, a0, a1, a2, a3);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][m], a0, a1, a2, a3, b0[nt], b1[nt]);
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816(o[C::kH8 ? 0 : nt][m], a0, a1, a2, a3, b0[nt], b1[nt]);
                     }
                     if constexpr (!C::kRawV) __syncwarp();   // the tile is rewritten for the next 16 tokens
                 }
@@ -817,7 +866,7 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
             cst = cst + 1 == kS ? 0 : cst + 1;
         }
 
-        // ---- this warp's partial of segment j: fold the (hi, lo) columns, sum l over the rows g
+        // ---- this warp's partial of segment j: fold the (hi, lo) columns (G <= 4), sum l over the rows g
         const bool ok = __all_sync(kFull, copies_ok);
         const int slot = (int)(gw - mma_worker_of_chunk((int64_t)j * plan.C, plan));
 #pragma unroll
@@ -825,7 +874,12 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
             float l = lrun[nt];
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(kFull, l, off);
-            const int head = 4 * nt + t;
+            const int head = C::kH8 ? 2 * t + nt : 4 * nt + t;
+            // output of this slot's head at accumulator n-tile no, fragment entries 2r (+ 1)
+            const int no = C::kH8 ? 0 : nt;
+            auto out_at = [&](int m, int r) {
+                return C::kH8 ? o[0][m][2 * r + nt] : o[no][m][2 * r] + o[no][m][2 * r + 1];
+            };
             if (head < a.G) {
                 float *pr = a.ws + (((int64_t)b * a.Hq + kvh * a.G + head) * plan.Smax + slot) * kPartialFloats;
                 if constexpr (C::kRegV) {
@@ -834,14 +888,13 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                     for (int q = 0; q < 4; ++q) {
                         const int m0 = 2 * q;
                         reinterpret_cast<float4 *>(pr + 4 + 16 * g)[q] =
-                            make_float4(o[nt][m0][0] + o[nt][m0][1], o[nt][m0][2] + o[nt][m0][3],
-                                        o[nt][m0 + 1][0] + o[nt][m0 + 1][1], o[nt][m0 + 1][2] + o[nt][m0 + 1][3]);
+                            make_float4(out_at(m0, 0), out_at(m0, 1), out_at(m0 + 1, 0), out_at(m0 + 1, 1));
                     }
                 } else {
 #pragma unroll
                     for (int m = 0; m < 8; ++m)
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) pr[4 + acc_dim<false>(m, r, g)] = o[nt][m][2 * r] + o[nt][m][2 * r + 1];
+                        for (int r = 0; r < 2; ++r) pr[4 + acc_dim<false>(m, r, g)] = out_at(m, r);
                 }
                 if (g == 0) {
                     pr[0] = mrun[nt];
