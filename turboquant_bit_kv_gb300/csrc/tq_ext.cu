@@ -19,7 +19,8 @@
 //
 // Kernels: two threads per row, each holding 64 of its elements in registers
 // (six butterfly stages of the 128-point transform in registers, the seventh
-// across the pair); codes by binary search of the boundaries (Lloyd-Max
+// across the pair); a warp takes 16 rows at a time and stages and stores its
+// own blocks (no CTA-wide barrier in the loop); codes by binary search of the boundaries (Lloyd-Max
 // codebooks) or by rounding to the uniform grid (turboq8), decided in
 // float32; stored norms and scales rounded once to fp16, recomputed in
 // double precision when the float32 value lies within 2^-20 of an fp16
@@ -139,8 +140,11 @@ __device__ __forceinline__ uint32_t level_of(float y, const float *b) {
 
 __device__ __forceinline__ void st16(uint8_t *p, uint32_t v) { *reinterpret_cast<uint16_t *>(p) = (uint16_t)v; }
 
-// Staged output blocks of a CTA pass: up to 128 rows of the largest (130-byte) block, back to back.
-constexpr int kExtStage = (kExtThreads / 2) * 130;
+// Staged output blocks: per warp, the 16 rows of its pass, up to the largest (130-byte) block, back to
+// back.  Warps work on their own (their own rows, staging and stores): no CTA-wide barrier in the loop.
+constexpr int kExtWarpRows = 16;
+constexpr int kExtWarpStage = kExtWarpRows * 130;
+constexpr int kExtStage = (kExtThreads / 32) * kExtWarpStage;
 
 template <int BITS, int DT>
 __global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid_constant__ ExtArgs a) {
@@ -151,10 +155,12 @@ __global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid
     if (threadIdx.x < 128) s_cell[threadIdx.x] = a.cells[threadIdx.x];
     __syncthreads();
     constexpr int BB = BITS == 8 ? 130 : 2 + 16 * BITS;
-    const int h = threadIdx.x & 1;
-    for (int64_t base = (int64_t)blockIdx.x * (kExtThreads / 2); base < a.n_vec;
-         base += (int64_t)gridDim.x * (kExtThreads / 2)) {
-        const int64_t row = base + (threadIdx.x >> 1);
+    const int h = threadIdx.x & 1, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *w_out = s_out + warp * kExtWarpStage;
+    const int64_t gw = (int64_t)blockIdx.x * (kExtThreads / 32) + warp;
+    const int64_t wstride = (int64_t)gridDim.x * (kExtThreads / 32) * kExtWarpRows;
+    for (int64_t base = gw * kExtWarpRows; base < a.n_vec; base += wstride) {
+        const int64_t row = base + (lane >> 1);
         const bool valid = row < a.n_vec;           // both threads of a pair agree
         const uint8_t *xr = a.x + (valid ? row : 0) * a.x_stride;
         float v[64];
@@ -195,9 +201,9 @@ __global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid
             const float inv = amax > 0.f ? 1.f / amax : 0.f;
 #pragma unroll
             for (int e = 0; e < 64; ++e) {
-                const float y = v[e] * inv;   // u / a (the 1 / sqrt(128) cancels)
-                const float t = floorf(fmaf(127.5f, y, 128.f));
-                code[e] = (uint8_t)fminf(fmaxf(t, 0.f), 255.f);
+                // u / a (the 1 / sqrt(128) cancels), in [-1, 1]: 127.5 y + 128 lies in [0.5, 255.5]
+                const float y = v[e] * inv;
+                code[e] = (uint8_t)(uint32_t)floorf(fmaf(127.5f, y, 128.f));
             }
             n16 = __half_as_ushort(__float2half_rn(a32));
             if (__any_sync(0xffffffffu, near_half_tie(a32))) {
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid
             }
             if (!(n > 0.f)) n16 = 0;
         }
-        uint8_t *blk = s_out + (threadIdx.x >> 1) * BB;   // staged back to back, then stored by the CTA
+        uint8_t *blk = w_out + (lane >> 1) * BB;   // staged back to back, then stored by the warp
         if (h == 0) st16(blk, n16);
         if constexpr (BITS == 8) {
 #pragma unroll
@@ -298,26 +304,26 @@ __global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid
                 st16(blk + 34 + 8 * h + 2 * k, w);
             }
         }
-        __syncthreads();
-        // the CTA's blocks: contiguous ones as 16-byte pieces, others row by row in 2-byte pieces
-        const int nrows = (int)min64(kExtThreads / 2, a.n_vec - base);
+        __syncwarp();
+        // the warp's blocks: contiguous ones as 16-byte pieces, others row by row in 2-byte pieces
+        const int nrows = (int)min64(kExtWarpRows, a.n_vec - base);
         if (a.contiguous) {
-            // the pass's blocks form one run starting 16-byte aligned (128 x BB is a multiple of 16)
+            // the pass's blocks form one run starting 16-byte aligned (16 x BB is a multiple of 16)
             uint4 *dst = reinterpret_cast<uint4 *>(a.blocks + base * BB);
-            const uint4 *src = reinterpret_cast<const uint4 *>(s_out);
+            const uint4 *src = reinterpret_cast<const uint4 *>(w_out);
             const int n16 = nrows * BB / 16;
-            for (int q = threadIdx.x; q < n16; q += kExtThreads) dst[q] = src[q];
-            for (int q = 16 * n16 + threadIdx.x; q < nrows * BB; q += kExtThreads) a.blocks[base * BB + q] = s_out[q];
+            for (int q = lane; q < n16; q += 32) dst[q] = src[q];
+            for (int q = 16 * n16 + lane; q < nrows * BB; q += 32) a.blocks[base * BB + q] = w_out[q];
         } else {
             constexpr int NH = BB / 2;
-            for (int q = threadIdx.x; q < nrows * NH; q += kExtThreads) {
+            for (int q = lane; q < nrows * NH; q += 32) {
                 const int r = q / NH, o = 2 * (q - r * NH);
                 const int64_t di = a.dst_index ? a.dst_index[base + r] : base + r;
                 *reinterpret_cast<uint16_t *>(a.blocks + di * a.block_stride + o) =
-                    *reinterpret_cast<const uint16_t *>(s_out + r * BB + o);
+                    *reinterpret_cast<const uint16_t *>(w_out + r * BB + o);
             }
         }
-        __syncthreads();
+        __syncwarp();
     }
 }
 
@@ -431,7 +437,7 @@ int launch_ext(K kernel, const ExtArgs &a, cudaStream_t st) {
             occ = 1;
         if (dev < 64) per_sm[dev] = occ;
     }
-    const int64_t ctas = (a.n_vec + kExtThreads / 2 - 1) / (kExtThreads / 2);
+    const int64_t ctas = (a.n_vec + kExtThreads / 2 - 1) / (kExtThreads / 2);   // (16 rows per warp)
     const int grid = (int)std::min<int64_t>(ctas, (int64_t)occ * sm_count());
     kernel<<<grid, kExtThreads, 0, st>>>(a);
     return launch_status();
