@@ -97,17 +97,29 @@ __device__ __forceinline__ void load_half_row(const uint8_t *row, int h, float (
 
 // The 128-point Hadamard transform of the pair's row: stages over bits 0..5 of
 // the element index in registers, bit 6 across the two threads (lane ^ 1).
+// Bits 0..4 run on packed pairs (v[i], v[i + 32]) (one paired add and one
+// paired fused multiply-add by -1, exact like the subtraction, per two
+// butterflies); bit 5 pairs the two halves of each packed pair.
 __device__ __forceinline__ void fwht_pair(float (&v)[64], int h) {
+    float2 p[32];
 #pragma unroll
-    for (int m = 1; m < 64; m <<= 1) {
+    for (int i = 0; i < 32; ++i) p[i] = make_float2(v[i], v[i + 32]);
+    const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-            if ((e & m) == 0) {
-                const float x = v[e], y = v[e + m];
-                v[e] = x + y;
-                v[e + m] = x - y;
+    for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if ((i & m) == 0) {
+                const float2 x = p[i], y = p[i + m];
+                p[i] = __fadd2_rn(x, y);
+                p[i + m] = __ffma2_rn(y, neg1, x);
             }
         }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v[i] = p[i].x + p[i].y;
+        v[i + 32] = p[i].x - p[i].y;
     }
 #pragma unroll
     for (int e = 0; e < 64; ++e) {
@@ -173,8 +185,16 @@ __global__ void __launch_bounds__(kExtThreads, 2) encode_ext_kernel(const __grid
 #pragma unroll
         for (int e = 0; e < 64; ++e) ss = fmaf(v[e], v[e], ss);
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        {
+            // D x: the sign bits of elements 64 h .. 64 h + 63 flip the float sign bits
+            const uint32_t s0 = a.signs[2 * h], s1 = a.signs[2 * h + 1];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) v[e] *= sign_of(a.signs, 64 * h + e);
+            for (int e = 0; e < 64; ++e) {
+                const uint32_t w = e < 32 ? s0 : s1;
+                const uint32_t m = (w << (31 - (e & 31))) & 0x80000000u;
+                v[e] = __uint_as_float(__float_as_uint(v[e]) ^ m);
+            }
+        }
         fwht_pair(v, h);
         const float rs = 0.08838834764831845f;   // 1 / sqrt(128)
         uint8_t code[64];
