@@ -90,7 +90,8 @@ KERNEL_SOURCES = {
     "ext_encode": ["tq_ext.cu", "tq_device.cuh"],
     "append": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "prefill": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
-    "pair_attention": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
+    "pair_attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
+                       "tq_attn_mma_k4.cu", "tq_attn_mma_k8.cu", "tq_device.cuh"],
     "paged_attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
                         "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_device.cuh"],
     "attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
@@ -685,8 +686,8 @@ def plan_prefill(tq, wl, dev, stream, seed, batch):
 def plan_turboq8_pair(tq, wl, dev, stream, seed, batch):
     """Llama-shaped decode step with the fork's high-precision asymmetric pair:
     turboq8 keys, 4-bit norm-corrected values (encode the cache, one decode
-    step; the pair's attention runs as the one-token case of the tensor-core
-    causal attention)."""
+    step on the split-K tensor-core decode kernels: query prep, attention,
+    combine)."""
     from turboquant_bit_kv_gb300 import workloads
     W = WORKLOADS[wl]
     B, Hq, Hkv, T = batch or W["B"], W["Hq"], W["Hkv"], W["T"]
@@ -698,7 +699,7 @@ def plan_turboq8_pair(tq, wl, dev, stream, seed, batch):
     kb = torch.empty((B, Hkv, T, 130), dtype=torch.uint8, device=dev)
     vb = torch.empty((B, Hkv, T, 66), dtype=torch.uint8, device=dev)
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
-    ws = torch.empty(16, dtype=torch.uint8, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
     scale = 1.0 / np.sqrt(128.0)
 
     def attn(qq=q):
@@ -709,7 +710,7 @@ def plan_turboq8_pair(tq, wl, dev, stream, seed, batch):
            Op("encode_v", "ext_encode", lambda: tq.tq_encode_kv_ex(v.view(-1, 128), v4, signs, vb,
                                                                 flags=tq.TQ_FMT_NORM_CORRECT, stream=stream),
               nvec * (256 + 66), 1, nvec),
-           Op("attention", "pair_attention", attn, nvec * (130 + 66) + q.numel() * 2 + out.numel() * 4, 1)]
+           Op("attention", "pair_attention", attn, nvec * (130 + 66) + q.numel() * 2 + out.numel() * 4, 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k).view(-1, 128), _pinned(v).view(-1, 128), _pinned(q)

@@ -111,12 +111,18 @@ def test_prefill_decode_agreement(env):
     assert np.all(err < 2 * ATTN_TOL), err.max()
 
 
-@pytest.mark.parametrize("kbits,vbits", [(8, 4), (8, 3), (4, 8)])
-def test_decode_attention_turboq8_pairs(env, kbits, vbits):
+@pytest.mark.parametrize("kbits,vbits,Hq,ws_full", [
+    (8, 4, 12, True), (8, 3, 12, True), (8, 2, 12, True), (4, 8, 12, True),   # split-K tensor-core path, G = 4
+    (8, 4, 21, True), (4, 8, 21, True),                                      # G = 7 (the eight-head n-tile)
+    (8, 4, 12, False), (4, 8, 21, False),                                    # no workspace: the causal kernel
+])
+def test_decode_attention_turboq8_pairs(env, kbits, vbits, Hq, ws_full):
     """tq_attn_decode over turboq8 keys or values (the asymmetric pairs): the
-    oracle's attention on identical packed caches."""
+    oracle's attention on identical packed caches, on the split-K decode path
+    (a full workspace) and on the one-token causal kernel (a workspace too
+    small for the split-K partials)."""
     tq, dev = env["tq"], env["dev"]
-    B, Hq, Hkv, T, T_cap = 3, 12, 3, 500, 504
+    B, Hkv, T, T_cap = 3, 3, 500, 504
     w = workloads.llama_decode(B=B, Hq=Hq, Hkv=Hkv, T=T, seed=50 + kbits + vbits)
     kblk, khat = _cache(env, w["k"].double().numpy(), kbits)
     vblk, vhat = _cache(env, w["v"].double().numpy(), vbits)
@@ -126,7 +132,7 @@ def test_decode_attention_turboq8_pairs(env, kbits, vbits):
     vb[:, :, :T] = torch.from_numpy(vblk)
     lens = [500, 123, 1]
     out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
-    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T_cap), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes(B, Hq, Hkv, T_cap) if ws_full else 16, dtype=torch.uint8, device=dev)
     scale = 1 / np.sqrt(D)
     tq.tq_attn_decode(w["q"].to(dev), kb.to(dev), env["cbs"][kbits], vb.to(dev), env["cbs"][vbits], out, ws, T,
                       scale, env["signs"], seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev))

@@ -330,11 +330,16 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
                               const uint16_t *res_norm_f16, const float *S, float *out, void *workspace,
                               size_t workspace_bytes, void *stream) {
     if (kcb && (kcb->bits == 8 || (vcb && vcb->bits == 8))) {
-        // turboq8 keys or values (the fork's asymmetric pairs): one query token is the M = 1 case of
-        // the tensor-core causal attention, which needs no workspace
+        // turboq8 keys with 2/3/4-bit values, or 4-bit keys with turboq8 values (the fork's asymmetric
+        // pairs): the split-K tensor-core path when a workspace of the usual size is given, else the
+        // M = 1 case of the tensor-core causal attention, which needs none
         if (qjl_bits || res_norm_f16 || S || !vcb) return TQ_ERR_UNSUPPORTED;
-        return tq_attn_prefill(q, q_dtype, k_blocks, kcb, static_cast<const uint8_t *>(v), vcb, seq_lens, B, 1, Hq,
-                               Hkv, T_cap, T, scale, signs, out, stream);
+        const bool pair = (kcb->bits == 8 && vcb->bits >= 2 && vcb->bits <= 4) || (kcb->bits == 4 && vcb->bits == 8);
+        const bool ws_ok = workspace && aligned(workspace, 16) && B > 0 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0 &&
+                           Hq / Hkv <= 8 && T_cap > 0 && workspace_bytes >= tq_attn_workspace_bytes(B, Hq, Hkv, T_cap);
+        if (!pair || !ws_ok)
+            return tq_attn_prefill(q, q_dtype, k_blocks, kcb, static_cast<const uint8_t *>(v), vcb, seq_lens, B, 1,
+                                   Hq, Hkv, T_cap, T, scale, signs, out, stream);
     }
     if (!q || !k_blocks || !kcb || !v || !out || !workspace) return TQ_ERR_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || (T_cap & 7))
@@ -342,9 +347,12 @@ extern "C" int tq_attn_decode(const void *q, int q_dtype, const uint8_t *k_block
     if (!std::isfinite(scale)) return TQ_ERR_ARG;
     const int G = Hq / Hkv;
     if (G > 8 || dtype_bytes(q_dtype) == 0) return TQ_ERR_UNSUPPORTED;
-    if (kcb->head_dim != kD || kcb->bits < 2 || kcb->bits > 4 || kcb->levels != (1 << kcb->bits))
+    // (bits 8: the turboq8 pairs admitted above)
+    if (kcb->head_dim != kD || ((kcb->bits < 2 || kcb->bits > 4) && kcb->bits != 8) ||
+        kcb->levels != (1 << kcb->bits))
         return TQ_ERR_UNSUPPORTED;
-    if (vcb && (vcb->head_dim != kD || vcb->bits < 2 || vcb->bits > 4 || vcb->levels != (1 << vcb->bits)))
+    if (vcb && (vcb->head_dim != kD || ((vcb->bits < 2 || vcb->bits > 4) && vcb->bits != 8) ||
+                vcb->levels != (1 << vcb->bits)))
         return TQ_ERR_UNSUPPORTED;
     const bool qjl = qjl_bits || res_norm_f16 || S;
     if (qjl && !(qjl_bits && res_norm_f16 && S)) return TQ_ERR_ARG;

@@ -10,9 +10,11 @@ namespace tq {
 void mma_shape_k2(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
 void mma_shape_k3(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
 void mma_shape_k4(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
+void mma_shape_k8(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *warps);
 int launch_attn_mma_k2(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 int launch_attn_mma_k3(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
+int launch_attn_mma_k8(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int nt, cudaStream_t st);
 
 // n-tiles of 4 query heads (times hi / lo parts) for G query heads per KV head
 static int mma_ntiles(int G) { return G <= 4 ? 1 : 2; }
@@ -26,6 +28,7 @@ static void mma_shape(int kb, int vb, bool qjl, int G, bool wide, int *ctas_per_
         case 2: mma_shape_k2(vb, qjl, nt, wide, ctas_per_sm, warps); break;
         case 3: mma_shape_k3(vb, qjl, nt, wide, ctas_per_sm, warps); break;
         case 4: mma_shape_k4(vb, qjl, nt, wide, ctas_per_sm, warps); break;
+        case 8: mma_shape_k8(vb, qjl, nt, wide, ctas_per_sm, warps); break;
         default: break;
     }
 }
@@ -85,6 +88,7 @@ int launch_attn_mma(const AttnArgs &a, MmaPlan &plan, int kb, int vb, bool qjl, 
         case 2: return launch_attn_mma_k2(a, plan, vb, qjl, nt, st);
         case 3: return launch_attn_mma_k3(a, plan, vb, qjl, nt, st);
         case 4: return launch_attn_mma_k4(a, plan, vb, qjl, nt, st);
+        case 8: return launch_attn_mma_k8(a, plan, vb, qjl, nt, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
 }

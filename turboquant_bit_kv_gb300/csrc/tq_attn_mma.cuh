@@ -88,15 +88,18 @@ struct Cfg {
     // per SM (WIDE; below 32 chunks per warp at that width, 12 warps -- fewer,
     // longer ranges -- measured 4% faster); two n-tiles of packed values fit in
     // 168 (12 warps; measured 5% faster than 8 at 7 query heads per KV head);
-    // the rest run 8 warps.
-    static constexpr int kW = (VB == 2 && NT == 1) ? (WIDE ? 16 : 12) : (NT == 2 && VB != 16) ? 12 : 8;
+    // the rest, and every turboq8 configuration (130-byte blocks: larger
+    // stages), run 8 warps.
+    static constexpr int kW = (KB == 8 || VB == 8) ? 8
+                              : (VB == 2 && NT == 1) ? (WIDE ? 16 : 12) : (NT == 2 && VB != 16) ? 12 : 8;
     static constexpr int kThreads = kW * 32;
     static constexpr bool kH8 = NT == 2;   // one n-tile of 8 heads; hi / lo parts as separate products
     static constexpr int kNO = kH8 ? 1 : NT;   // accumulator n-tiles
-    static constexpr int kKBytes = 2 + 16 * KB;
+    // turboq8 blocks: [fp16 scale][128 code bytes]
+    static constexpr int kKBytes = KB == 8 ? 130 : 2 + 16 * KB;
     static constexpr bool kRawV = VB == 16;
     static constexpr bool kRegV = VB == 2;                 // value fragments straight from a pair table
-    static constexpr int kVBytes = kRawV ? 256 : 2 + 16 * VB;
+    static constexpr int kVBytes = kRawV ? 256 : VB == 8 ? 130 : 2 + 16 * VB;
     static constexpr int kKStage = align16(kMmaChunk * kKBytes);
     static constexpr int kVStage = kRawV ? kMmaChunk * kVtPitch : align16(kMmaChunk * kVBytes);
     static constexpr int kSStage = QJL ? kMmaChunk * 16 : 0;      // sign bits
@@ -104,7 +107,9 @@ struct Cfg {
     // +16: word reads past a 2-byte aligned slice stay inside the warp's stage
     static constexpr int kWarpStage = kKStage + kVStage + kSStage + kRStage + 16;
     static constexpr int kVtile = (kRegV || kRawV) ? 0 : 16 * kVtPitch;   // per-warp dequantised tile
-    static constexpr int kKLutEntries = KB == 4 ? 256 : KB == 3 ? 64 : 16;
+    // turboq8 codes need no table: the level 2i - 255 is an integer, exact in fp16 (the 1 / 255
+    // goes into the block's norm factor)
+    static constexpr int kKLutEntries = KB == 8 ? 0 : KB == 4 ? 256 : KB == 3 ? 64 : 16;
     static constexpr int kVLutEntries = VB == 4 ? 256 : VB == 3 ? 64 : 0;
     // value-pair table rows: 256 bytes for 3-bit values (one byte permute yields entry * 256 + lane
     // offset), 128 for the 256 entries of 4-bit values (offset by a multiply)
@@ -328,14 +333,29 @@ __device__ __forceinline__ void pair_index3(uint32_t L, uint32_t Hh, uint32_t &e
     od = ((L >> 4) & 0x0F0F0F0Fu) | ((v << 2) & 0x00300030u) | ((v >> 2) & 0x30003000u);
 }
 
+// half2(2 i - 255) of the two turboq8 codes i that selector `sel` (0x4140:
+// bytes 0, 1 of w; 0x4342: bytes 2, 3) picks: one byte permute makes the fp16
+// bit patterns of 1024 + i (exponent byte 0x64 over the code byte), then
+// (1024 + i) - 1024 and 2 i - 255, each exact (2303 itself has no fp16).
+__device__ __forceinline__ uint32_t q8_levels(uint32_t w, uint32_t sel) {
+    const uint32_t p = prmt(w, 0x64u, sel);
+    const __half2 i2 = __hsub2(*reinterpret_cast<const __half2 *>(&p), __floats2half2_rn(1024.f, 1024.f));
+    const __half2 l2 = __hfma2(i2, __floats2half2_rn(2.f, 2.f), __floats2half2_rn(-255.f, -255.f));
+    return *reinterpret_cast<const uint32_t *>(&l2);
+}
+
 // Half2 key fragments for k-step ks of one token row: pairs 2ks (dims
 // 32t + 4ks + {0, 1}) and 2ks + 1 (dims 32t + 4ks + {2, 3}) of the slice.
 template <int KB>
 struct KeySlice {
-    uint32_t w[4];   // 4-bit: the 16 code bytes; 2/3-bit: even / odd pair indices of halves 0, 1
+    // 8-bit: the 32 code bytes; 4-bit: the 16 code bytes; 2/3-bit: even / odd pair indices of
+    // halves 0, 1
+    uint32_t w[KB == 8 ? 8 : 4];
 
     __device__ __forceinline__ void load(uint32_t row_s, int t) {
-        if constexpr (KB == 4) {
+        if constexpr (KB == 8) {
+            lds_words_a2<8>(row_s + 2 + 32 * t, w);
+        } else if constexpr (KB == 4) {
             lds_words_a2<4>(row_s + 2 + 16 * t, w);
         } else if constexpr (KB == 2) {
             uint32_t c[2];
@@ -351,6 +371,12 @@ struct KeySlice {
             pair_index3(c[0], hb[0], w[0], w[1]);
             pair_index3(c[1], hb[0] >> 16, w[2], w[3]);
         }
+    }
+    // turboq8: the fragment words of pair 2ks (x) and pair 2ks + 1 (y) themselves, half2(2 i - 255)
+    // per code i (see q8_levels)
+    __device__ __forceinline__ void levels(int ks, uint32_t &x, uint32_t &y) const {
+        x = q8_levels(w[ks], 0x4140u);
+        y = q8_levels(w[ks], 0x4342u);
     }
     // key-table byte offsets of pair 2ks (x) and pair 2ks + 1 (y) for rows of
     // ROW bytes: with 256-byte rows one byte permute puts the pair index in
@@ -382,7 +408,19 @@ struct KeySlice {
 // into an fp16 row of the value tile (pairs through the pair table).
 template <int VB>
 __device__ __forceinline__ void dequant_value_half(uint32_t blk_s, int hf, uint32_t lut_s, uint32_t row_s) {
-    if constexpr (VB == 4) {
+    if constexpr (VB == 8) {
+        // turboq8: half2(2 i - 255) per code pair (q8_levels), no table
+        uint32_t c[16];
+        lds_words_a2<16>(blk_s + 2 + 64 * hf, c);
+        uint32_t h[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            h[2 * i] = q8_levels(c[i], 0x4140u);
+            h[2 * i + 1] = q8_levels(c[i], 0x4342u);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sts128(row_s + 128 * hf + 16 * q, h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    } else if constexpr (VB == 4) {
         uint32_t c[8];
         lds_words_a2<8>(blk_s + 2 + 32 * hf, c);
 #pragma unroll
@@ -577,10 +615,13 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
         for (int s = 0; s + 1 < kS; ++s) issue_next();
     }
 
-    if constexpr (C::kKSplit)
+    if constexpr (KB == 8) {
+        // (turboq8 keys: no table)
+    } else if constexpr (C::kKSplit) {
         build_split_lut_hl<KB>(reinterpret_cast<uint32_t *>(smem + C::kSmemKLut), a.kc, tid, C::kThreads);
-    else
+    } else {
         build_split_lut<KB>(reinterpret_cast<uint2 *>(smem + C::kSmemKLut), a.kc, tid, C::kThreads, C::kKRow / 8);
+    }
     if constexpr (VB == 3 || VB == 4)
         build_pair_lut<VB, C::kVRow>(reinterpret_cast<uint32_t *>(smem + C::kSmemVLut), a.vc, tid, C::kThreads);
     if constexpr (QJL) {
@@ -681,6 +722,20 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     uint32_t x0, y0, x1, y1;
+                    if constexpr (KB == 8) {
+                        // turboq8 keys: exact fp16 levels, no lo part
+                        ksl[mt][0].levels(ks, x0, y0);
+                        ksl[mt][1].levels(ks, x1, y1);
+                        if constexpr (C::kH8) {
+                            mma16816(acc[0][mt], x0, x1, y0, y1, qb[0][ks][0], qb[0][ks][1]);
+                            mma16816(acc[0][mt], x0, x1, y0, y1, qb[1][ks][0], qb[1][ks][1]);
+                        } else {
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma16816(acc[nt][mt], x0, x1, y0, y1, qb[nt][ks][0], qb[nt][ks][1]);
+                        }
+                        continue;
+                    }
                     ksl[mt][0].template pick<C::kKRow>(ks, klane, x0, y0);
                     ksl[mt][1].template pick<C::kKRow>(ks, klane, x1, y1);
                     if constexpr (C::kKSplit) {
@@ -736,8 +791,10 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 const int ta = 16 * mt + g, tb = ta + 8;
-                const float na = __half2float(__ushort_as_half((unsigned short)lds_u16(ks_s + ta * C::kKBytes)));
-                const float nb = __half2float(__ushort_as_half((unsigned short)lds_u16(ks_s + tb * C::kKBytes)));
+                // the block norms (turboq8: the scale over 255, the grid's step factor)
+                constexpr float kf = KB == 8 ? 1.f / 255.f : 1.f;
+                const float na = __half2float(__ushort_as_half((unsigned short)lds_u16(ks_s + ta * C::kKBytes))) * kf;
+                const float nb = __half2float(__ushort_as_half((unsigned short)lds_u16(ks_s + tb * C::kKBytes))) * kf;
                 float ra = 0.f, rb = 0.f;
                 if constexpr (QJL) {
                     ra = __half2float(__ushort_as_half((unsigned short)lds_u16(rn_s + 2 * ta)));
@@ -783,8 +840,9 @@ __global__ void __launch_bounds__(Cfg<KB, VB, QJL, NT, WIDE>::kThreads, Cfg<KB, 
                 const int ta = 16 * mt + g, tb = ta + 8;
                 float nva = 1.f, nvb = 1.f;
                 if constexpr (!C::kRawV) {
-                    nva = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + ta * C::kVBytes)));
-                    nvb = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + tb * C::kVBytes)));
+                    constexpr float vf = VB == 8 ? 1.f / 255.f : 1.f;
+                    nva = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + ta * C::kVBytes))) * vf;
+                    nvb = __half2float(__ushort_as_half((unsigned short)lds_u16(vs_s + tb * C::kVBytes))) * vf;
                 }
                 // B fragments of P (8 x 8 blocks of token rows g / g + 8, transposed): per n-tile, or
                 // (kH8) index 0: the hi parts of the 8 heads, 1: the lo parts

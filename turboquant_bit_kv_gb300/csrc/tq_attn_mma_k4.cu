@@ -1,6 +1,6 @@
 // Tensor-core decode attention, 4-bit keys: instantiations of the kernel
-// template in tq_attn_mma.cuh for every value format (2/3/4-bit codes, raw
-// fp16).
+// template in tq_attn_mma.cuh for every value format (2/3/4-bit codes,
+// turboq8, raw fp16).
 #include "tq_attn_mma.cuh"
 
 namespace tq {
@@ -11,6 +11,7 @@ void mma_shape_k4(int vb, bool qjl, int nt, bool wide, int *ctas_per_sm, int *wa
     if (vb == V && qjl == Q && nt == N) return shape_of<4, V, Q, N>(wide, ctas_per_sm, warps);
     TQ_CASE(2, false, 1) TQ_CASE(3, false, 1) TQ_CASE(4, false, 1) TQ_CASE(16, false, 1)
     TQ_CASE(2, false, 2) TQ_CASE(3, false, 2) TQ_CASE(4, false, 2) TQ_CASE(16, false, 2)
+    TQ_CASE(8, false, 1) TQ_CASE(8, false, 2)
 
 #undef TQ_CASE
 }
@@ -20,6 +21,7 @@ int launch_attn_mma_k4(const AttnArgs &a, MmaPlan &plan, int vb, bool qjl, int n
     if (vb == V && qjl == Q && nt == N) return launch_cfg<4, V, Q, N>(a, plan, st);
     TQ_CASE(2, false, 1) TQ_CASE(3, false, 1) TQ_CASE(4, false, 1) TQ_CASE(16, false, 1)
     TQ_CASE(2, false, 2) TQ_CASE(3, false, 2) TQ_CASE(4, false, 2) TQ_CASE(16, false, 2)
+    TQ_CASE(8, false, 1) TQ_CASE(8, false, 2)
 
 #undef TQ_CASE
     return TQ_ERR_UNSUPPORTED;

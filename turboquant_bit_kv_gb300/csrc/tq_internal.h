@@ -52,6 +52,7 @@ int wait_failed_qjl(unsigned *v, bool clear);
 int wait_failed_attn_k2(unsigned *v, bool clear);
 int wait_failed_attn_k3(unsigned *v, bool clear);
 int wait_failed_attn_k4(unsigned *v, bool clear);
+int wait_failed_attn_k8(unsigned *v, bool clear);
 int wait_failed_prefill(unsigned *v, bool clear);
 
 inline int launch_status() {
