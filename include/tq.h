@@ -229,9 +229,12 @@ int tq_attn_plan(int B, int Hq, int Hkv, int T, int key_bits, int value_bits, in
  *               bytes, 16-byte aligned (TQ_ERR_ALIGN otherwise); clobbered;
  *               calls that overlap on the GPU must use different workspaces.
  *   turboq8 keys with 2/3/4-bit values, or 4-bit keys with turboq8 values
- *   ([fork] section 2, Asymmetric K/V), are served as the one-token case of
- *   tq_attn_prefill (the workspace is then unused); other combinations with
- *   turboq8, and QJL with turboq8, return TQ_ERR_UNSUPPORTED.
+ *   ([fork] section 2, Asymmetric K/V), run on the same split-K tensor-core
+ *   path when workspace holds tq_attn_workspace_bytes(...) bytes (16-byte
+ *   aligned, G <= 8); with a smaller or NULL workspace they are served as
+ *   the one-token case of tq_attn_prefill (the workspace is then unused).
+ *   Other combinations with turboq8, and QJL with turboq8, return
+ *   TQ_ERR_UNSUPPORTED.
  * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_WORKSPACE,
  * TQ_ERR_CUDA. */
 int tq_attn_decode(const void *q, int q_dtype,
