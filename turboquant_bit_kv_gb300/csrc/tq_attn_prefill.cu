@@ -200,6 +200,13 @@ __device__ __forceinline__ uint32_t pf_code(const uint32_t (&w)[8], int e) {
     else return ((w[e >> 4] >> (2 * (e & 15))) & 3u) | (((w[2] >> e) & 1u) << 2);
 }
 
+// 2^x (the special-function unit's approximation, a few ulp; 2^-inf = 0).
+__device__ __forceinline__ float pf_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // (hi, lo) fp16 splits of two floats, packed as half2 words: x = hi + lo to about 2^-22.
 __device__ __forceinline__ void pf_split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
     const __half2 h = __floats2half2_rn(x0, x1);
@@ -518,14 +525,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             tc_fence_before();
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(bar(kSFree + s));
-            // key norms and the causal mask (key t visible to the row iff t <= pos)
+            // key norms and the causal mask (key t visible to the row iff t <= pos); a warp whose 32
+            // keys are all visible to all its rows (every tile but the last few) skips the mask
             const int t0 = j * kPfKeys + 32 * h;
+            const float4 *kn4 = reinterpret_cast<const float4 *>(norms + s * 128 + 32 * h);
+            const float4 *vn4 = reinterpret_cast<const float4 *>(norms + s * 128 + 64 + 32 * h);
+            const bool full = __all_sync(0xffffffffu, row_valid && t0 + 31 <= pos);
             float mx = -INFINITY;
+            if (full) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const bool vis = row_valid && t0 + c <= pos;
-                sv[c] = vis ? sv[c] * norms[s * 128 + 32 * h + c] : -INFINITY;
-                mx = fmaxf(mx, sv[c]);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 n = kn4[q4];
+                    const float2 a = __fmul2_rn(make_float2(sv[4 * q4], sv[4 * q4 + 1]), make_float2(n.x, n.y));
+                    const float2 b = __fmul2_rn(make_float2(sv[4 * q4 + 2], sv[4 * q4 + 3]), make_float2(n.z, n.w));
+                    sv[4 * q4] = a.x;
+                    sv[4 * q4 + 1] = a.y;
+                    sv[4 * q4 + 2] = b.x;
+                    sv[4 * q4 + 3] = b.y;
+                    mx = fmaxf(mx, fmaxf(fmaxf(a.x, a.y), fmaxf(b.x, b.y)));
+                }
+            } else {
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 n = kn4[q4];
+                    const float nn[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * q4 + e;
+                        const bool vis = row_valid && t0 + c <= pos;
+                        sv[c] = vis ? sv[c] * nn[e] : -INFINITY;
+                        mx = fmaxf(mx, sv[c]);
+                    }
+                }
             }
             xch[(s * 2 + h) * 128 + r] = mx;
             rows_sync();
@@ -551,28 +582,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            float sum = 0.f;
+            float2 sum2 = make_float2(0.f, 0.f);
             const uint32_t prow = (uint32_t)(r * 128);
+            // (a row that has seen no visible key yet has m_new = -inf and only masked keys here)
+            const float mref = m_new == -INFINITY ? 0.f : m_new;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
-                    float pp[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int c = 8 * c8 + 2 * qq + e;
-                        const float p = sv[c] == -INFINITY ? 0.f : exp2f(sv[c] - m_new);
-                        sum += p;
-                        pp[e] = sv[c] == -INFINITY ? 0.f : p * norms[s * 128 + 64 + 32 * h + c];
+                    const int c = 8 * c8 + 2 * qq;
+                    // p = 2^(s - m): exp2 of -inf is 0, so masked keys give p = 0; their value norms may
+                    // be anything (keys past the copied ones), hence the select on the product
+                    const float2 p = make_float2(pf_ex2(sv[c] - mref), pf_ex2(sv[c + 1] - mref));
+                    sum2 = __fadd2_rn(sum2, p);
+                    const float4 vn = vn4[c >> 2];
+                    const float2 nv = (c & 2) ? make_float2(vn.z, vn.w) : make_float2(vn.x, vn.y);
+                    float2 pp = __fmul2_rn(p, nv);
+                    if (!full) {
+                        pp.x = sv[c] == -INFINITY ? 0.f : pp.x;
+                        pp.y = sv[c + 1] == -INFINITY ? 0.f : pp.y;
                     }
-                    pf_split2(pp[0], pp[1], hw[qq], lw[qq]);
+                    pf_split2(pp.x, pp.y, hw[qq], lw[qq]);
                 }
                 const uint32_t sw = (uint32_t)((((4 * h + c8) ^ (r & 7)) << 4));
                 pf_sts128(base_s + S::kPhi + prow + sw, hw[0], hw[1], hw[2], hw[3]);
                 pf_sts128(base_s + S::kPlo + prow + sw, lw[0], lw[1], lw[2], lw[3]);
             }
-            l = l * factor + sum;
+            l = l * factor + (sum2.x + sum2.y);
             m_ref = m_new;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
