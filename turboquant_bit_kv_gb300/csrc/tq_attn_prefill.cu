@@ -32,7 +32,9 @@
 //              moves only when a row's maximum exceeds it by more than 8 in
 //              log2 units, so that the accumulator in tensor memory is
 //              rarely rescaled), write P (times the value norms) as fp16
-//              hi / lo tiles.  Epilogue: O / l, inverse rotation (its last
+//              hi / lo parts into tensor memory, the A operand of P V (two
+//              stages, so the row warps wait for the products of tile j - 2,
+//              not j - 1).  Epilogue: O / l, inverse rotation (its last
 //              stage across the row's two threads), store.
 //   warps 8-11 key warps: thread (k, h) dequantises dims 64 h .. + 63 of key
 //              k of the tile into the K hi / lo tiles and the V tile
@@ -61,8 +63,11 @@ constexpr int kPfKeyWarps = 4;               // two threads per key (64 dims eac
 constexpr int kPfProducerWarp = kPfRowWarps + kPfKeyWarps;
 constexpr int kPfMmaWarp = kPfProducerWarp + 1;
 constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);   // 448
-constexpr uint32_t kPfCols = 256;            // tensor memory: S[2] (64 columns each) + O (128)
+// tensor memory: S[2] (64 columns each) at 0, O (128) at 128, P[2] at 256: each P stage holds the
+// hi parts (32 columns: 64 keys of fp16 pairs) then the lo parts
+constexpr uint32_t kPfCols = 512;
 constexpr uint32_t kPfColO = 128;
+constexpr uint32_t kPfColP = 256;
 
 // Shared memory (offsets from a 1024-byte aligned base).  Operand tiles use the
 // K-major 128-byte swizzle of tq_tc.cuh: 64-element blocks of rows x 128 bytes.
@@ -73,16 +78,14 @@ struct PfSmem {
     static constexpr int kKhi = 65536;                     // [2] keys: 64 rows x 128 dims (two 8 KB blocks)
     static constexpr int kKlo = 98304;                     // [2]
     static constexpr int kV = 131072;                      // [2] values: 64 keys x 128 dims, same layout
-    static constexpr int kPhi = 163840;                    // P hi: 128 rows x 64 keys (one 16 KB block)
-    static constexpr int kPlo = 180224;
-    static constexpr int kBlk = 196608;                    // [2] packed blocks: 64 K blocks | 64 V blocks
+    static constexpr int kBlk = 163840;                    // [2] packed blocks: 64 K blocks | 64 V blocks
     static constexpr int kBlkBytes = kPfKeys * (2 + 16 * KB + 2 + 16 * VB);
     static constexpr int kNorm = kBlk + 2 * kBlkBytes;     // [2] kn[64] | vn[64] (float)
     static constexpr int kKTab = kNorm + 2 * 512;          // key centroids: 16 codes x 32 lanes x half2 (hi, lo)
     static constexpr int kVTab = kKTab + 2048;             // value centroids: 16 codes x 32 lanes x half2 (v, v)
     static constexpr int kXch = kVTab + 2048;              // row max / sum exchange: [2][2][128] float
-    static constexpr int kBars = kXch + 2048;              // 16 mbarriers
-    static constexpr int kSlot = kBars + 16 * 8;           // tensor-memory base address, failure flag
+    static constexpr int kBars = kXch + 2048;              // 24 mbarriers
+    static constexpr int kSlot = kBars + 24 * 8;           // tensor-memory base address, failure flag
     static constexpr int kTotal = kSlot + 16 + 1024;       // + alignment slack of the base
     static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
@@ -95,9 +98,9 @@ enum {
     kKvFree = 6,     // [2] the products that read the K / V tiles completed (commit)
     kSReady = 8,     // [2] scores in tensor memory (commit)
     kSFree = 10,     // [2] scores read (4 row warps)
-    kPReady = 12,    // P written, O rescaled if needed (4 row warps)
-    kPvDone = 13,    // P V completed: P free, O current (commit)
-    kDrain = 14      // the issuing thread's last commit before teardown
+    kPReady = 12,    // [2] P written, O rescaled if needed (8 row warps)
+    kPvDone = 14,    // [2] P V completed: P stage free, O current (commit)
+    kDrain = 16      // the issuing thread's last commit before teardown
 };
 
 struct PfArgs {
@@ -136,6 +139,27 @@ __device__ __forceinline__ void pf_bulk_g2s(uint32_t dst, const void *src, uint3
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+// D (+)= A B with A (M 128 x K 16, fp16) in tensor memory at column a_tmem (rows in lanes, K pairs
+// packed per 32-bit column) and B from a shared-memory descriptor.
+__device__ __forceinline__ void pf_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::
+            "r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
@@ -309,8 +333,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             tc_mbar_init(bar(kSReady + s), 1);
             tc_mbar_init(bar(kSFree + s), kPfRowWarps);
         }
-        tc_mbar_init(bar(kPReady), kPfRowWarps);
-        tc_mbar_init(bar(kPvDone), 1);
+        for (int s = 0; s < 2; ++s) {
+            tc_mbar_init(bar(kPReady + s), kPfRowWarps);
+            tc_mbar_init(bar(kPvDone + s), 1);
+        }
         tc_mbar_init(bar(kDrain), 1);
         *fail_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -402,13 +428,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 const uint32_t vs = base_s + S::kV + s * 16384;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
-                    const uint32_t pa = base_s + (part ? S::kPlo : S::kPhi);
+                    // A = P of stage s in tensor memory (rows in lanes, 16 keys = 8 columns per step)
+                    const uint32_t pa = tmem + kPfColP + 64u * (uint32_t)s + 32u * (uint32_t)part;
 #pragma unroll
                     for (int ks = 0; ks < kPfKeys / 16; ++ks)
-                        tc_mma(tmem + kPfColO, pf_desc(pa + ks * 32, 16, 1024), pf_desc(vs + ks * 2048, 8192, 1024),
-                               id_pv, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                        pf_mma_ts(tmem + kPfColO, pa + 8u * (uint32_t)ks, pf_desc(vs + ks * 2048, 8192, 1024), id_pv,
+                                  (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
                 }
-                tc_commit(bar(kPvDone));
+                tc_commit(bar(kPvDone + s));
                 tc_commit(bar(kKvFree + s));
             };
             for (int j = 0; j < n_tiles && ok; ++j) {
@@ -419,14 +446,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 tc_fence_after();
                 scores(j);
                 if (j >= 1) {
-                    wait(ok, kPReady, (uint32_t)(j - 1) & 1u);
+                    wait(ok, kPReady + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     values(j - 1);
                 }
             }
             if (ok && n_tiles > 0) {
-                wait(ok, kPReady, (uint32_t)(n_tiles - 1) & 1u);
+                wait(ok, kPReady + ((n_tiles - 1) & 1), (uint32_t)((n_tiles - 1) >> 1) & 1u);
                 if (ok) {
                     tc_fence_after();
                     values(n_tiles - 1);
@@ -566,10 +593,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             const bool move = mx > m_ref + 8.f;
             const float m_new = move ? mx : m_ref;
             const float factor = move ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
-            // P of the previous tile has been consumed (and O is current) before P and O change
-            if (j >= 1) wait(ok, kPvDone, (uint32_t)(j - 1) & 1u);
+            // P stage s is free once the products of tile j - 2 have completed; O is rescaled only
+            // after those of tile j - 1, so that it holds exactly the earlier tiles
+            if (j >= 2) wait(ok, kPvDone + s, (uint32_t)((j - 2) >> 1) & 1u);
+            const bool resc = j >= 1 && __any_sync(0xffffffffu, move);
+            if (resc) wait(ok, kPvDone + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u);
             tc_fence_after();
-            if (j >= 1 && __any_sync(0xffffffffu, move)) {
+            if (resc) {
 #pragma unroll
                 for (int c4 = 0; c4 < 2; ++c4) {
                     float o32[32];
@@ -583,12 +613,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
             float2 sum2 = make_float2(0.f, 0.f);
-            const uint32_t prow = (uint32_t)(r * 128);
+            uint32_t hw[16], lw[16];   // P of keys 32 h .. + 31 as fp16 pairs: hi and lo parts
             // (a row that has seen no visible key yet has m_new = -inf and only masked keys here)
             const float mref = m_new == -INFINITY ? 0.f : m_new;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     const int c = 8 * c8 + 2 * qq;
@@ -603,21 +632,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                         pp.x = sv[c] == -INFINITY ? 0.f : pp.x;
                         pp.y = sv[c + 1] == -INFINITY ? 0.f : pp.y;
                     }
-                    pf_split2(pp.x, pp.y, hw[qq], lw[qq]);
+                    pf_split2(pp.x, pp.y, hw[4 * c8 + qq], lw[4 * c8 + qq]);
                 }
-                const uint32_t sw = (uint32_t)((((4 * h + c8) ^ (r & 7)) << 4));
-                pf_sts128(base_s + S::kPhi + prow + sw, hw[0], hw[1], hw[2], hw[3]);
-                pf_sts128(base_s + S::kPlo + prow + sw, lw[0], lw[1], lw[2], lw[3]);
             }
+            // P of stage s: this row's lane, keys 32 h .. + 31 = columns 16 h .. + 15 of each part
+            tc_st16u(lane_t + kPfColP + 64u * (uint32_t)s + 16u * (uint32_t)h, hw);
+            tc_st16u(lane_t + kPfColP + 64u * (uint32_t)s + 32u + 16u * (uint32_t)h, lw);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             l = l * factor + (sum2.x + sum2.y);
             m_ref = m_new;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc_mbar_arrive(bar(kPReady));
+            if (lane == 0) tc_mbar_arrive(bar(kPReady + s));
         }
         // ---- epilogue: o = O / l, rotated back: D H o / sqrt(128); this thread holds dims 64 h .. + 63
-        if (n_tiles > 0) wait(ok, kPvDone, (uint32_t)(n_tiles - 1) & 1u);
+        if (n_tiles > 0) wait(ok, kPvDone + ((n_tiles - 1) & 1), (uint32_t)((n_tiles - 1) >> 1) & 1u);
         tc_fence_after();
         // (the exchange slot of parity n_tiles was last read before the last tile's barrier)
         const int se = n_tiles & 1;
