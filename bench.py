@@ -897,7 +897,9 @@ def run_gpu(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    stream = torch.cuda.current_stream(dev)
+    # a stream of our own (CUDA graphs cannot be captured on the legacy default stream)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
     plan = PLANS[args.workload](tq, args.workload, dev, stream, args.seed + rank, args.batch)
     ops = plan["ops"]
 
@@ -915,8 +917,29 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         return None
 
+    # the step as one CUDA graph (the library's calls, captured as they are issued), with a timing
+    # event between the calls, so that the device time of each call excludes the host's launch
+    # overhead; without graph support (or with --eager) the calls are issued one by one
+    graph = None
+    gev = None
+    if not args.eager:
+        try:
+            gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ops) + 1)]
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                gev[0].record(stream)
+                for j, op in enumerate(ops):
+                    op.fn()
+                    gev[j + 1].record(stream)
+            for _ in range(2):
+                graph.replay()
+            torch.cuda.synchronize(dev)
+        except Exception as exc:   # (an older torch without external events, or a capture error)
+            print("bench: CUDA graph capture unavailable (%s); timing eager calls" % exc, file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize(dev)
+
     # timed region: an event after every call, on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -924,19 +947,38 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        e = evs[i]
-        e[0].record(stream)
-        for j, op in enumerate(ops):
-            op.fn()
-            e[j + 1].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clk = clocks.stop()
-    ms_step = reduce_max(t0.elapsed_time(t1) / args.steps, world)
-    op_ms = [_mean_ms(evs, j, j + 1) for j in range(len(ops))]
+    if graph is not None:
+        # one replay per step; the events inside are read back after each replay
+        per_op = [[] for _ in ops]
+        step_ms = []
+        t0.record(stream)
+        for i in range(args.steps):
+            graph.replay()
+            gev[-1].synchronize()
+            for j in range(len(ops)):
+                per_op[j].append(gev[j].elapsed_time(gev[j + 1]))
+            step_ms.append(gev[0].elapsed_time(gev[-1]))
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        clk = clocks.stop()
+        ms_step = reduce_max(statistics.mean(step_ms), world)
+        op_ms = [statistics.mean(v) for v in per_op]
+    else:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
+        t0.record(stream)
+        for i in range(args.steps):
+            e = evs[i]
+            e[0].record(stream)
+            for j, op in enumerate(ops):
+                op.fn()
+                e[j + 1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        clk = clocks.stop()
+        ms_step = reduce_max(t0.elapsed_time(t1) / args.steps, world)
+        op_ms = [_mean_ms(evs, j, j + 1) for j in range(len(ops))]
 
     # the attention call alone with a cold L2 (the cache was just written by
     # the encode, so the in-step time partly reads L2)
@@ -1033,6 +1075,7 @@ def run_gpu(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": plan["dtype"], "data": "synthetic (seeded; no dataset or model weights)",
         "config": dict(plan["config"], workload=args.workload,
+                       launch="cuda_graph (one replay per step)" if graph is not None else "eager calls",
                        parallelism="replicas" if world > 1 else "single GPU"),
         "frac_hbm": round(value / world / peak, 4),
     }
@@ -1297,6 +1340,7 @@ def main():
     ap.add_argument("--cpu-groups", type=int, default=0, help="oracle sample size (0: the workload's default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
+    ap.add_argument("--eager", action="store_true", help="time the calls as issued one by one (no CUDA graph)")
     ap.add_argument("--profile-only", action="store_true",
                     help="run warm-up + steps without timing or extras (for ncu captures)")
     args = ap.parse_args()
