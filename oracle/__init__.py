@@ -19,8 +19,10 @@ Every function cites the page and section it restates.  Pages:
   Configuration, Tensor Layout.
 
 ``oracle.ext`` holds the further block formats (norm-corrected encode, the
-dense 8-in-3 packing of 3-bit codes, the 8-bit turboq8 codec) and
-``attention_causal`` the multi-token causal attention.
+dense 8-in-3 packing of 3-bit codes, the 8-bit turboq8 codec),
+``oracle.headdim`` the codec at head dims 64, 96 and 160 (a dense orthogonal
+rotation as an input) and ``attention_causal`` the multi-token causal
+attention.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, textbook tables, library routines or values printed on
