@@ -75,8 +75,9 @@ typedef struct {
  * for `bits` ([spec] Codebook Generation: conditional means of cells,
  * midpoint boundaries, iterated to a fixed point).  Host only; the first
  * call per (head_dim, bits) runs the iteration (milliseconds) and caches it;
- * thread-safe.  head_dim must be 128.  Errors: TQ_ERR_ARG (out NULL),
- * TQ_ERR_UNSUPPORTED. */
+ * thread-safe.  head_dim 64, 96, 128 or 160 ([spec] Types / Codebook
+ * Generation: the target dimensions) for bits 2-4; 128 for bits 8
+ * (turboq8).  Errors: TQ_ERR_ARG (out NULL), TQ_ERR_UNSUPPORTED. */
 int tq_codebook_load(int head_dim, int bits, tq_codebook *out);
 
 /* Fill *out with the sign diagonal drawn from `seed` ([spec] Lifecycle,
@@ -391,6 +392,62 @@ int tq_debug_drop_copies(int on);
 
 /* Static, human-readable name of a tq_status value. */
 const char *tq_status_string(int status);
+
+/* ---- Head dims other than 128 ([spec] Types / Codebook Generation: target
+ * dimensions 64, 96, 128, 160; Hadamard Transform Detail: for a head dim that
+ * is not a power of two, "a dense random orthogonal matrix").  The rotation
+ * is an input: R, a device float32 [head_dim][head_dim] row-major orthogonal
+ * matrix (R R^T = I), owned by the caller; y = R x / ||x||, and a block
+ * decodes to n16 R^T c[code].  Blocks: [fp16 norm][codes], 2-bit four per
+ * byte, 4-bit two per byte, 3-bit a 2-bit low plane of head_dim / 4 bytes
+ * then a 1-bit high plane of head_dim / 8 bytes (the 128-element layout
+ * generalised); 2 + head_dim * bits / 8 bytes, back to back.  head_dim is
+ * 64, 96, 128 or 160 and the codebook one of tq_codebook_load(head_dim, .).
+ * These run on CUDA cores (the rotation as a dense product per row); the
+ * 128-element entry points above remain the fast path for head_dim 128. */
+
+/* Bytes of one block at head_dim: 2 + head_dim * bits / 8; 0 if unsupported. */
+size_t tq_block_bytes_d(int head_dim, int bits);
+
+/* Host: R = H D / sqrt(head_dim) for a power-of-two head_dim (64 or 128),
+ * H the Sylvester-Hadamard matrix, D the first head_dim signs of `signs`
+ * (bit set = -1), written row-major to R_host [head_dim * head_dim].
+ * Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED (other head dims). */
+int tq_rotation_hadamard(int head_dim, tq_signs signs, float *R_host);
+
+/* Encode n_vec rows x [n_vec][head_dim] (x_dtype TQ_F32 / TQ_BF16 / TQ_F16)
+ * into blocks [n_vec][tq_block_bytes_d(head_dim, cb->bits)].  Codes decided
+ * in float32 (y = R x / ||x|| against the float32 boundaries); the norm is
+ * rounded once to fp16 (recomputed in double precision near an fp16
+ * rounding boundary); a zero row stores norm 0 and code L/2.  n_vec 0 is a
+ * no-op.  x 4-byte aligned, R 16-byte aligned.  Errors: TQ_ERR_ARG,
+ * TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_encode_kv_d(const void *x, int x_dtype, int64_t n_vec, int head_dim, const tq_codebook *cb,
+                   const float *R, uint8_t *blocks, void *stream);
+
+/* Decode blocks back to rows out [n_vec][head_dim] of out_dtype:
+ * x_hat = n16 R^T c[code] (float32 arithmetic, one rounding to the output
+ * type).  Errors as tq_encode_kv_d. */
+int tq_decode_kv_d(const uint8_t *blocks, int64_t n_vec, int head_dim, const tq_codebook *cb, const float *R,
+                   void *out, int out_dtype, void *stream);
+
+/* Scratch bytes tq_attn_decode_d needs (0 for a bad shape). */
+size_t tq_attn_workspace_bytes_d(int B, int Hq, int Hkv, int T_cap, int head_dim);
+
+/* Decode attention at head_dim (one query token per sequence and query
+ * head), the same computation as tq_attn_decode: q rotated once (R q),
+ * scores n_t <R q, cK[code_t]> in the rotated domain, online softmax, values
+ * accumulated there, one inverse rotation per output; split over the
+ * context with a merge.  q [B][Hq][head_dim] (q_dtype), k_blocks / v_blocks
+ * [B][Hkv][T_cap] blocks of kcb->bits / vcb->bits at head_dim, seq_lens as
+ * for tq_attn_decode, 1 <= T <= T_cap, G = Hq / Hkv <= 8, out float32
+ * [B][Hq][head_dim], workspace >= tq_attn_workspace_bytes_d(...) bytes
+ * (16-byte aligned).  Errors: TQ_ERR_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN,
+ * TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
+                     const uint8_t *v_blocks, const tq_codebook *vcb, const int32_t *seq_lens, int B, int Hq,
+                     int Hkv, int T_cap, int T, int head_dim, float scale, const float *R, float *out,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

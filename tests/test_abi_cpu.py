@@ -121,7 +121,7 @@ def test_argument_errors_return_before_enqueue(tq):
     U = ctypes.c_void_p(0x10002)          # misaligned fake address
     st = ctypes.c_void_p(0)
     assert L.tq_codebook_load(128, 5, ctypes.byref(tq.tq_codebook())) == tq.TQ_ERR_UNSUPPORTED
-    assert L.tq_codebook_load(64, 4, ctypes.byref(tq.tq_codebook())) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_codebook_load(80, 4, ctypes.byref(tq.tq_codebook())) == tq.TQ_ERR_UNSUPPORTED   # not a target dim
     assert L.tq_signs_from_seed(1, 96, ctypes.byref(tq.tq_signs())) == tq.TQ_ERR_UNSUPPORTED
     # encode
     assert L.tq_encode_kv(None, 1, 10, 128, ctypes.byref(cb4), sg, A, 66, None, st) == tq.TQ_ERR_ARG
@@ -166,3 +166,45 @@ def test_argument_errors_return_before_enqueue(tq):
                                 st) == tq.TQ_ERR_UNSUPPORTED
     assert L.tq_serde_serialize(U, 1, 4, 16, 256, 128, 16, 1, 1, ctypes.byref(cb4), ctypes.byref(cb4), sg, A,
                                 st) == tq.TQ_ERR_ALIGN
+
+
+@pytest.mark.parametrize("d", (64, 96, 160))
+@pytest.mark.parametrize("bits", (2, 3, 4))
+def test_library_codebook_other_head_dims(tq, d, bits):
+    """Codebooks of the spec's other target dims: the library's Lloyd-Max of
+    Beta(d/2, d/2) equals the oracle's in float32."""
+    cb = tq.tq_codebook_load(d, bits)
+    c, b, _ = oracle.beta_codebook(d, bits)
+    assert cb.head_dim == d and cb.levels == 1 << bits
+    assert np.array_equal(np.array(cb.centroids[:1 << bits], np.float32), c.astype(np.float32))
+    assert np.array_equal(np.array(cb.boundaries[:(1 << bits) - 1], np.float32), b.astype(np.float32))
+    assert tq.tq_block_bytes_d(d, bits) == 2 + d * bits // 8
+    with pytest.raises(tq.TQError):
+        tq.tq_codebook_load(80, bits)
+
+
+def test_library_hadamard_rotation(tq):
+    from oracle import headdim
+    from turboquant_bit_kv_gb300 import workloads
+    s = tq.tq_signs_from_seed(workloads.SIGN_SEED)
+    sd = oracle.sign_diagonal(workloads.SIGN_SEED)
+    for d in (64, 128):
+        R = tq.tq_rotation_hadamard(d, s).double().numpy()
+        assert np.allclose(R, headdim.hadamard_rotation(d, sd), rtol=0, atol=1e-7)
+    with pytest.raises(tq.TQError):
+        tq.tq_rotation_hadamard(96, s)
+
+
+def test_head_dim_calls_validate_before_launching(tq):
+    """Argument errors of the head-dim calls come from the host checks (no GPU needed)."""
+    import ctypes
+    L = tq.lib()
+    cb = tq.tq_codebook_load(96, 3)
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.tq_encode_kv_d(fake, tq.TQ_F32, 4, 80, ctypes.byref(cb), fake, fake, None) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_encode_kv_d(fake, tq.TQ_F32, 4, 64, ctypes.byref(cb), fake, fake, None) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_encode_kv_d(fake, tq.TQ_F32, 0, 96, ctypes.byref(cb), fake, fake, None) == tq.TQ_OK
+    assert L.tq_encode_kv_d(fake, tq.TQ_F32, 4, 96, ctypes.byref(cb), ctypes.c_void_p((1 << 20) + 4), fake,
+                            None) == tq.TQ_ERR_ALIGN
+    assert L.tq_attn_workspace_bytes_d(2, 8, 2, 1000, 96) > 0
+    assert L.tq_attn_workspace_bytes_d(2, 8, 3, 1000, 96) == 0

@@ -113,8 +113,10 @@ void lloyd_beta(int d, int bits, double *c, double *b) {
 }
 
 std::mutex g_cb_mutex;
-bool g_cb_ready[5] = {false, false, false, false, false};
-tq_codebook g_cb[5];
+// cached codebooks per (head dim 64 / 96 / 128 / 160, bits)
+constexpr int kCbDims[4] = {64, 96, 128, 160};
+bool g_cb_ready[4][5] = {};
+tq_codebook g_cb[4][5];
 
 }  // namespace
 
@@ -128,9 +130,12 @@ extern "C" int tq_codebook_load(int head_dim, int bits, tq_codebook *out) {
         out->levels = 256;
         return TQ_OK;
     }
-    if (head_dim != kD || bits < 2 || bits > 4) return TQ_ERR_UNSUPPORTED;
+    int di = -1;
+    for (int i = 0; i < 4; ++i)
+        if (kCbDims[i] == head_dim) di = i;
+    if (di < 0 || bits < 2 || bits > 4) return TQ_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_cb_mutex);
-    if (!g_cb_ready[bits]) {
+    if (!g_cb_ready[di][bits]) {
         double c[16] = {0}, b[15] = {0};
         lloyd_beta(head_dim, bits, c, b);
         tq_codebook cb;
@@ -140,10 +145,10 @@ extern "C" int tq_codebook_load(int head_dim, int bits, tq_codebook *out) {
         cb.levels = 1 << bits;
         for (int i = 0; i < cb.levels; ++i) cb.centroids[i] = (float)c[i];
         for (int i = 0; i + 1 < cb.levels; ++i) cb.boundaries[i] = (float)b[i];
-        g_cb[bits] = cb;
-        g_cb_ready[bits] = true;
+        g_cb[di][bits] = cb;
+        g_cb_ready[di][bits] = true;
     }
-    *out = g_cb[bits];
+    *out = g_cb[di][bits];
     return TQ_OK;
 }
 

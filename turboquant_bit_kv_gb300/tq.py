@@ -81,6 +81,15 @@ def lib():
         L.tq_attn_workspace_bytes_sms.restype = sz
         L.tq_status_string.argtypes = [c_int]
         L.tq_status_string.restype = ctypes.c_char_p
+        L.tq_block_bytes_d.argtypes = [c_int, c_int]
+        L.tq_block_bytes_d.restype = sz
+        L.tq_rotation_hadamard.argtypes = [c_int, tq_signs, vp]
+        L.tq_encode_kv_d.argtypes = [vp, c_int, i64, c_int, cbp, vp, vp, vp]
+        L.tq_decode_kv_d.argtypes = [vp, i64, c_int, cbp, vp, vp, c_int, vp]
+        L.tq_attn_workspace_bytes_d.argtypes = [c_int] * 5
+        L.tq_attn_workspace_bytes_d.restype = sz
+        L.tq_attn_decode_d.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
+                                       ctypes.c_float, vp, vp, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -314,4 +323,49 @@ def tq_attn_decode_paged(q, k_pool, kcb, v_pool, vcb, block_table, page_tokens, 
                                       ctypes.byref(vcb), _ptr(block_table), block_table.shape[1], page_tokens,
                                       _ptr(seq_lens), B, Hq, Hkv, T, ctypes.c_float(scale), signs, _ptr(out),
                                       _ptr(workspace), nbytes, _stream(stream)), "tq_attn_decode_paged")
+    return out
+
+
+# ---- head dims 64 / 96 / 128 / 160 (the rotation R is a device float32 [d, d] orthogonal matrix)
+
+def tq_block_bytes_d(head_dim, bits):
+    return int(lib().tq_block_bytes_d(head_dim, bits))
+
+
+def tq_rotation_hadamard(head_dim, signs):
+    """R = H D / sqrt(head_dim) (head_dim 64 or 128) as a CPU float32 tensor [d, d]."""
+    R = torch.empty((head_dim, head_dim), dtype=torch.float32)
+    _check(lib().tq_rotation_hadamard(head_dim, signs, ctypes.c_void_p(R.data_ptr())), "tq_rotation_hadamard")
+    return R
+
+
+def tq_encode_kv_d(x, cb, R, blocks, stream=None):
+    """Encode contiguous rows x [n, d] into blocks [n, tq_block_bytes_d(d, bits)]."""
+    d = x.shape[-1]
+    n = x.numel() // d if d else 0
+    _check(lib().tq_encode_kv_d(_ptr(x), _dtype(x), n, d, ctypes.byref(cb), _ptr(R), _ptr(blocks), _stream(stream)),
+           "tq_encode_kv_d")
+    return blocks
+
+
+def tq_decode_kv_d(blocks, n_vec, cb, R, out, stream=None):
+    """Decode n_vec blocks into contiguous rows out [n_vec, d]."""
+    _check(lib().tq_decode_kv_d(_ptr(blocks), n_vec, out.shape[-1], ctypes.byref(cb), _ptr(R), _ptr(out),
+                                _dtype(out), _stream(stream)), "tq_decode_kv_d")
+    return out
+
+
+def tq_attn_workspace_bytes_d(B, Hq, Hkv, T_cap, head_dim):
+    return int(lib().tq_attn_workspace_bytes_d(B, Hq, Hkv, T_cap, head_dim))
+
+
+def tq_attn_decode_d(q, k_blocks, kcb, v_blocks, vcb, R, out, workspace, T, scale, seq_lens=None, stream=None):
+    """Decode attention at head dim d = q.shape[-1]: q [B, Hq, d]; k/v blocks
+    [B, Hkv, T_cap, bytes]; out float32 [B, Hq, d]."""
+    B, Hq, d = q.shape
+    Hkv, T_cap = k_blocks.shape[1], k_blocks.shape[2]
+    _check(lib().tq_attn_decode_d(_ptr(q), _dtype(q), _ptr(k_blocks), ctypes.byref(kcb), _ptr(v_blocks),
+                                  ctypes.byref(vcb), _ptr(seq_lens), B, Hq, Hkv, T_cap, T, d, ctypes.c_float(scale),
+                                  _ptr(R), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "tq_attn_decode_d")
     return out
