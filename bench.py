@@ -77,6 +77,8 @@ WORKLOADS = {
                                    scale="1/sqrt(128)"),
     "llama3_8b_paged_decode": dict(B=16, Hq=32, Hkv=8, T=8192, head_dim=128, key_bits=4, value_bits=2,
                                    page_tokens=32, kv_dtype="bf16", scale="1/sqrt(128)"),
+    "headdim_160_decode": dict(B=8, Hq=32, Hkv=8, T=8192, head_dim=160, key_bits=4, value_bits=2, kv_dtype="bf16",
+                               rotation="seeded random orthogonal 160 x 160 (QR), float32", scale="1/sqrt(160)"),
     "storage_roundtrip": dict(layout="[2, 32, 65536, 1024]", L=32, T=65536, hidden=1024, head_dim=128,
                               block_size=16, skip_first=2, skip_last=2, key_bits=4, value_bits=4, slot_bytes=132,
                               kv_dtype="bf16"),
@@ -98,6 +100,8 @@ KERNEL_SOURCES = {
                   "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_g1.cu",
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
     "qjl": ["tq_qjl.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
+    "hd_encode": ["tq_headdim.cu", "tq_device.cuh"],
+    "hd_attention": ["tq_headdim.cu", "tq_device.cuh"],
     "serialize": ["tq_encode.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "deserialize": ["tq_decode.cu", "tq_codec.cu", "tq_device.cuh"],
 }
@@ -883,9 +887,76 @@ def plan_storage(tq, wl, dev, stream, seed, batch):
                 dtype="bf16")
 
 
+def _rotation_160(seed=160):
+    """A seeded random orthogonal 160 x 160 matrix (QR of a Gaussian matrix), float32."""
+    a = np.random.default_rng(seed).standard_normal((160, 160))
+    q, r = np.linalg.qr(a)
+    return (q * np.sign(np.diag(r))[None, :]).astype(np.float32)
+
+
+def plan_headdim(tq, wl, dev, stream, seed, batch):
+    """Decode step at head dim 160 (a spec target dim that is not a power of
+    two): encode K (4-bit) and V (2-bit) through the dense rotation, then
+    one decode attention step."""
+    from turboquant_bit_kv_gb300 import workloads
+    W = WORKLOADS[wl]
+    B, Hq, Hkv, T, d = batch or W["B"], W["Hq"], W["Hkv"], W["T"], W["head_dim"]
+    kcb, vcb = tq.tq_codebook_load(d, 4), tq.tq_codebook_load(d, 2)
+    R = torch.from_numpy(_rotation_160()).to(dev)
+    g = torch.Generator(device=dev).manual_seed(seed + 160)
+    k = torch.randn((B, Hkv, T, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, T, d), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((B, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+    kbb, vbb = tq.tq_block_bytes_d(d, 4), tq.tq_block_bytes_d(d, 2)
+    kb = torch.empty((B, Hkv, T, kbb), dtype=torch.uint8, device=dev)
+    vb = torch.empty((B, Hkv, T, vbb), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes_d(B, Hq, Hkv, T, d), dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(d)
+    nvec = B * Hkv * T
+
+    def attn(qq=q):
+        tq.tq_attn_decode_d(qq, kb, kcb, vb, vcb, R, out, ws, T, scale, stream=stream)
+
+    ops = [Op("encode_k", "hd_encode", lambda: tq.tq_encode_kv_d(k.view(-1, d), kcb, R, kb.view(nvec, -1),
+                                                                 stream=stream), nvec * (2 * d + kbb), 1, nvec),
+           Op("encode_v", "hd_encode", lambda: tq.tq_encode_kv_d(v.view(-1, d), vcb, R, vb.view(nvec, -1),
+                                                                 stream=stream), nvec * (2 * d + vbb), 1, nvec),
+           Op("attention", "hd_attention", attn, nvec * (kbb + vbb) + q.numel() * 2 + out.numel() * 4, 2)]
+
+    def e2e():
+        hk, hv, hq = _pinned(k).view(-1, d), _pinned(v).view(-1, d), _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dk, dv, dq = torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev), torch.empty_like(q)
+
+        def step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            tq.tq_encode_kv_d(dk, kcb, R, kb.view(nvec, -1), stream=stream)
+            tq.tq_encode_kv_d(dv, vcb, R, vb.view(nvec, -1), stream=stream)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, (k.numel() + v.numel() + q.numel()) * 2, out.numel() * 4
+
+    def decode_e2e():
+        hq = _pinned(q)
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq = torch.empty_like(q)
+
+        def step():
+            dq.copy_(hq, non_blocking=True)
+            attn(dq)
+            hout.copy_(out, non_blocking=True)
+        return step, q.numel() * 2, out.numel() * 4
+
+    cfg = dict(W, B=B, l2="inputs (671 MB) larger than L2 (129 MB); attention also timed after an L2 flush")
+    return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, config=cfg, dtype="bf16")
+
+
 PLANS = {"llama3_8b_decode": plan_llama, "single_head_fp32": plan_single_head, "qwen25_7b_append": plan_qwen,
          "qjl_two_term": plan_qjl, "llama3_8b_prefill": plan_prefill, "llama3_8b_turboq8_pair": plan_turboq8_pair,
-         "llama3_8b_paged_decode": plan_paged, "storage_roundtrip": plan_storage}
+         "llama3_8b_paged_decode": plan_paged, "storage_roundtrip": plan_storage, "headdim_160_decode": plan_headdim}
 
 
 def _mean_ms(evs, a, b):
@@ -1184,6 +1255,30 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
         nbytes = n * (128 * ib * 2 + kbb + vbb) + n * (kbb + vbb) + G * groups * 128 * (ib + 4)
         desc = "%d (sequence, KV head) slice(s) at T=%d: encode K/V rows, attend %d query heads" % (groups, T, G)
         return secs, nbytes, desc
+    if workload == "headdim_160_decode":
+        from oracle import headdim
+        G, d = W["Hq"] // W["Hkv"], W["head_dim"]
+        R = _rotation_160().astype(np.float64)
+        rng = np.random.default_rng(seed)
+        k = rng.standard_normal((groups, T, d))
+        v = rng.standard_normal((groups, T, d))
+        q = rng.standard_normal((1, G * groups, d))
+        ck, bk, _ = oracle.beta_codebook(d, 4)
+        cv, bv, _ = oracle.beta_codebook(d, 2)
+        t0 = time.perf_counter()
+        kh, vh = [], []
+        for g in range(groups):
+            i, n16, _ = headdim.encode_d(k[g], R, bk.astype(np.float32))
+            kh.append(headdim.decode_d(i, n16, ck, R))
+            i, n16, _ = headdim.encode_d(v[g], R, bv.astype(np.float32))
+            vh.append(headdim.decode_d(i, n16, cv, R))
+        oracle.attention_dequantized(q, np.stack(kh)[None], np.stack(vh)[None], 1 / np.sqrt(d))
+        secs = time.perf_counter() - t0
+        n = groups * T
+        kbb, vbb = 2 + d * 4 // 8, 2 + d * 2 // 8
+        nbytes = n * (2 * d * 2 + kbb + vbb) + n * (kbb + vbb) + G * groups * d * 6
+        return secs, nbytes, "%d (sequence, KV head) slice(s) at T=%d, head dim %d: encode K/V rows, attend %d query heads" % (
+            groups, T, d, G)
     if workload == "llama3_8b_prefill":
         G, M = W["Hq"] // W["Hkv"], W["M"]
         data = _sample_inputs((workload, groups, T, seed),
@@ -1241,7 +1336,7 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
 
 CPU_GROUPS = {"llama3_8b_decode": 128, "single_head_fp32": 1, "qwen25_7b_append": 24, "qjl_two_term": 32,
               "llama3_8b_prefill": 8, "llama3_8b_turboq8_pair": 128, "llama3_8b_paged_decode": 128,
-              "storage_roundtrip": 64}
+              "storage_roundtrip": 64, "headdim_160_decode": 32}
 
 
 def cpu_cores():

@@ -12,19 +12,22 @@
 // byte, 3-bit a 2-bit low plane of d / 4 bytes then a 1-bit high plane of
 // d / 8 bytes.
 //
-// Kernels (CUDA cores, float32; d = 32 ND): one warp per row, lane l holds
+// Kernels (CUDA cores, float32; d = 32 ND): a warp per row, lane l holds
 // elements l + 32 k.  R sits in shared memory with rows padded to d + 1
 // floats, so that the 32 lanes reading one column (encode: outputs
 // l + 32 k, input j) hit 32 different banks.  The rotation of a row is d
 // shuffles of its inputs and d ND fused multiply-adds per lane.  Codes are
 // the count of float32 boundaries <= y; norms are rounded once to fp16 and
 // recomputed in double precision when the float32 norm lies within 2^-20 of
-// an fp16 rounding boundary.  Decode attention: one CTA of 8 warps per
-// (sequence, KV head, context split); the CTA rotates its G queries once,
-// each warp scores tokens t = warp, warp + 8, ... of the split against
-// n_t c[code_t] (a warp sum per head), keeps an online softmax and the value
-// sums per head in the rotated domain, the warps merge in shared memory, and
-// a combine kernel merges the splits and rotates back (R^T).
+// an fp16 rounding boundary.  The codec kernels rotate four rows per warp at
+// once, so every element of R read from shared memory serves four rows.
+// Decode attention: a prep kernel rotates every query once (R q, scale
+// log2(e) folded in); one CTA of 8 warps per (sequence, KV head, context
+// split) then takes 32 tokens per warp step: lane t scores its token
+// against n_t c[code_t] for every head (no cross-lane sums), the warp keeps
+// an online softmax per head, and the value sums run with lanes over dims,
+// each token's probabilities broadcast by shuffles; the warps merge in shared
+// memory, and a combine kernel merges the splits and rotates back (R^T).
 
 #include <cmath>
 #include <cstring>
@@ -139,6 +142,35 @@ __device__ __forceinline__ void hd_rotate(const float *Rs, const float (&v)[ND],
     }
 }
 
+// The same for NR rows at once: every element of R read from shared memory serves NR rows.
+template <int ND, bool TRANSPOSE, int NR>
+__device__ __forceinline__ void hd_rotate_rows(const float *Rs, const float (&v)[NR][ND], float (&out)[NR][ND],
+                                               int lane) {
+    constexpr int D = 32 * ND, P = D + 1;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int k = 0; k < ND; ++k) out[r][k] = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < ND; ++jj) {
+#pragma unroll 4
+        for (int src = 0; src < 32; ++src) {
+            float vj[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) vj[r] = __shfl_sync(kHdFull, v[r][jj], src);
+            const int j = 32 * jj + src;
+#pragma unroll
+            for (int k = 0; k < ND; ++k) {
+                const float m = TRANSPOSE ? Rs[j * P + lane + 32 * k] : Rs[(lane + 32 * k) * P + j];
+#pragma unroll
+                for (int r = 0; r < NR; ++r) out[r][k] = fmaf(m, vj[r], out[r][k]);
+            }
+        }
+    }
+}
+
+constexpr int kHdRows = 4;   // rows a warp rotates at once in the codec kernels
+
 template <int ND>
 __global__ void __launch_bounds__(kHdThreads) encode_d_kernel(const __grid_constant__ HdArgs a) {
     constexpr int D = 32 * ND;
@@ -150,42 +182,52 @@ __global__ void __launch_bounds__(kHdThreads) encode_d_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *wc = codes + warp * D;
     const int L = 1 << a.bits, BB = 2 + D * a.bits / 8;
-    for (int64_t row = (int64_t)blockIdx.x * kHdWarps + warp; row < a.n_vec; row += (int64_t)gridDim.x * kHdWarps) {
-        float x[ND], y[ND];
-        float ss = 0.f;
+    for (int64_t r0 = ((int64_t)blockIdx.x * kHdWarps + warp) * kHdRows; r0 < a.n_vec;
+         r0 += (int64_t)gridDim.x * kHdWarps * kHdRows) {
+        float x[kHdRows][ND], y[kHdRows][ND], ss[kHdRows];
 #pragma unroll
-        for (int k = 0; k < ND; ++k) {
-            x[k] = hd_load(a.x, a.dt, row * D + lane + 32 * k);
-            ss = fmaf(x[k], x[k], ss);
-        }
-        ss = hd_warp_sum(ss);
-        hd_rotate<ND, false>(Rs, x, y, lane);
-        const float n = sqrtf(ss);
-        const float inv = n > 0.f ? 1.f / n : 0.f;
+        for (int r = 0; r < kHdRows; ++r) {
+            const bool valid = r0 + r < a.n_vec;
+            ss[r] = 0.f;
 #pragma unroll
-        for (int k = 0; k < ND; ++k) {
-            const float yk = y[k] * inv;   // a zero row: y = 0, code L / 2
-            uint32_t code = 0;
-            for (int i = 0; i + 1 < L; ++i) code += (yk >= a.b[i]) ? 1u : 0u;
-            wc[lane + 32 * k] = (uint8_t)code;
+            for (int k = 0; k < ND; ++k) {
+                x[r][k] = valid ? hd_load(a.x, a.dt, (r0 + r) * D + lane + 32 * k) : 0.f;
+                ss[r] = fmaf(x[r][k], x[r][k], ss[r]);
+            }
+            ss[r] = hd_warp_sum(ss[r]);
         }
-        uint32_t n16 = __half_as_ushort(__float2half_rn(n));
-        if (__any_sync(kHdFull, n > 0.f && near_fp16_tie_fast(n))) {
-            double sd = 0.0;
+        hd_rotate_rows<ND, false, kHdRows>(Rs, x, y, lane);
 #pragma unroll
-            for (int k = 0; k < ND; ++k) sd += (double)x[k] * (double)x[k];
-            sd = hd_warp_sum_d(sd);
-            n16 = __half_as_ushort(__double2half(sqrt(sd)));
+        for (int r = 0; r < kHdRows; ++r) {
+            if (r0 + r >= a.n_vec) break;   // (warp-uniform)
+            const int64_t row = r0 + r;
+            const float n = sqrtf(ss[r]);
+            const float inv = n > 0.f ? 1.f / n : 0.f;
+#pragma unroll
+            for (int k = 0; k < ND; ++k) {
+                const float yk = y[r][k] * inv;   // a zero row: y = 0, code L / 2
+                uint32_t code = 0;
+                for (int i = 0; i + 1 < L; ++i) code += (yk >= a.b[i]) ? 1u : 0u;
+                wc[lane + 32 * k] = (uint8_t)code;
+            }
+            uint32_t n16 = __half_as_ushort(__float2half_rn(n));
+            if (__any_sync(kHdFull, n > 0.f && near_fp16_tie_fast(n))) {
+                double sd = 0.0;
+#pragma unroll
+                for (int k = 0; k < ND; ++k) sd += (double)x[r][k] * (double)x[r][k];
+                sd = hd_warp_sum_d(sd);
+                n16 = __half_as_ushort(__double2half(sqrt(sd)));
+            }
+            if (!(n > 0.f)) n16 = 0;
+            __syncwarp();
+            uint8_t *blk = a.blocks + row * BB;
+            if (lane == 0) {
+                blk[0] = (uint8_t)(n16 & 0xFFu);
+                blk[1] = (uint8_t)(n16 >> 8);
+            }
+            for (int q = lane; q < BB - 2; q += 32) blk[2 + q] = (uint8_t)hd_code_byte<D>(wc, a.bits, q);
+            __syncwarp();
         }
-        if (!(n > 0.f)) n16 = 0;
-        __syncwarp();
-        uint8_t *blk = a.blocks + row * BB;
-        if (lane == 0) {
-            blk[0] = (uint8_t)(n16 & 0xFFu);
-            blk[1] = (uint8_t)(n16 >> 8);
-        }
-        for (int q = lane; q < BB - 2; q += 32) blk[2 + q] = (uint8_t)hd_code_byte<D>(wc, a.bits, q);
-        __syncwarp();
     }
 }
 
@@ -198,15 +240,24 @@ __global__ void __launch_bounds__(kHdThreads) decode_d_kernel(const __grid_const
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BB = 2 + D * a.bits / 8;
-    for (int64_t row = (int64_t)blockIdx.x * kHdWarps + warp; row < a.n_vec; row += (int64_t)gridDim.x * kHdWarps) {
-        const uint8_t *blk = a.blocks + row * BB;
-        const float n = __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
-        float v[ND], x[ND];
+    for (int64_t r0 = ((int64_t)blockIdx.x * kHdWarps + warp) * kHdRows; r0 < a.n_vec;
+         r0 += (int64_t)gridDim.x * kHdWarps * kHdRows) {
+        float v[kHdRows][ND], x[kHdRows][ND];
 #pragma unroll
-        for (int k = 0; k < ND; ++k) v[k] = a.c[hd_code<D>(blk, a.bits, lane + 32 * k)] * n;
-        hd_rotate<ND, true>(Rs, v, x, lane);
+        for (int r = 0; r < kHdRows; ++r) {
+            const bool valid = r0 + r < a.n_vec;
+            const uint8_t *blk = a.blocks + (valid ? r0 + r : 0) * BB;
+            const float n = valid ? __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8)))) : 0.f;
 #pragma unroll
-        for (int k = 0; k < ND; ++k) hd_store(a.out, a.dt, row * D + lane + 32 * k, x[k]);
+            for (int k = 0; k < ND; ++k) v[r][k] = a.c[hd_code<D>(blk, a.bits, lane + 32 * k)] * n;
+        }
+        hd_rotate_rows<ND, true, kHdRows>(Rs, v, x, lane);
+#pragma unroll
+        for (int r = 0; r < kHdRows; ++r) {
+            if (r0 + r >= a.n_vec) break;
+#pragma unroll
+            for (int k = 0; k < ND; ++k) hd_store(a.out, a.dt, (r0 + r) * D + lane + 32 * k, x[r][k]);
+        }
     }
 }
 
@@ -219,8 +270,8 @@ int hd_launch_codec(const HdArgs &a, bool encode, cudaStream_t st) {
     const int smem = hd_smem_bytes(D, encode);
     const void *k = encode ? (const void *)encode_d_kernel<ND> : (const void *)decode_d_kernel<ND>;
     if (set_smem_limit(k, smem, encode ? done_e : done_d) != TQ_OK) return TQ_ERR_CUDA;
-    const int64_t ctas = (a.n_vec + kHdWarps - 1) / kHdWarps;
-    const int grid = (int)(ctas < (int64_t)sm_count() * 4 ? ctas : (int64_t)sm_count() * 4);
+    const int64_t ctas = (a.n_vec + kHdWarps * kHdRows - 1) / (kHdWarps * kHdRows);
+    const int grid = (int)(ctas < (int64_t)sm_count() * 2 ? ctas : (int64_t)sm_count() * 2);
     if (encode) encode_d_kernel<ND><<<grid, kHdThreads, smem, st>>>(a);
     else decode_d_kernel<ND><<<grid, kHdThreads, smem, st>>>(a);
     return launch_status();
@@ -244,6 +295,7 @@ struct HdAttnArgs {
     const int32_t *seq_lens;
     const float *R;
     float *ws;               // partials [B][Hq][splits][2 + d]: m (log2 units), l, acc[d]
+    float *qrot;             // rotated, scaled queries [B][Hq][d] (after the partials)
     float *out;
     int q_dtype, B, Hq, Hkv, G, T_cap, T, kbits, vbits, splits, tps;
     float qscale;            // scale * log2(e)
@@ -261,25 +313,45 @@ void hd_split_plan(int B, int Hkv, int T, int *splits, int *tps) {
     *splits = (T + *tps - 1) / *tps;
 }
 
+// R q times scale log2(e) for every (sequence, query head), kHdRows per warp.
+template <int ND>
+__global__ void __launch_bounds__(kHdThreads) attn_d_prep_kernel(const __grid_constant__ HdAttnArgs a) {
+    constexpr int D = 32 * ND;
+    extern __shared__ __align__(16) float hd_smem[];
+    float *Rs = hd_smem;
+    hd_load_R<D>(Rs, a.R);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)a.B * a.Hq;
+    const int64_t r0 = ((int64_t)blockIdx.x * kHdWarps + warp) * kHdRows;
+    if (r0 >= rows) return;
+    float x[kHdRows][ND], y[kHdRows][ND];
+#pragma unroll
+    for (int r = 0; r < kHdRows; ++r)
+#pragma unroll
+        for (int k = 0; k < ND; ++k) x[r][k] = r0 + r < rows ? hd_load(a.q, a.q_dtype, (r0 + r) * D + lane + 32 * k) : 0.f;
+    hd_rotate_rows<ND, false, kHdRows>(Rs, x, y, lane);
+#pragma unroll
+    for (int r = 0; r < kHdRows; ++r)
+        if (r0 + r < rows)
+#pragma unroll
+            for (int k = 0; k < ND; ++k) a.qrot[(r0 + r) * D + lane + 32 * k] = y[r][k] * a.qscale;
+}
+
 template <int ND>
 __global__ void __launch_bounds__(kHdThreads) attn_d_kernel(const __grid_constant__ HdAttnArgs a) {
     constexpr int D = 32 * ND;
     extern __shared__ __align__(16) float hd_smem[];
-    float *Rs = hd_smem;                              // [D][D + 1]
-    float *qs = Rs + D * (D + 1);                     // [8 heads][D] rotated, scaled queries
-    float *part = qs + 8 * D;                         // [8 warps][8 heads][2 + D]
-    hd_load_R<D>(Rs, a.R);
-    __syncthreads();
+    float *qs = hd_smem;                              // [8 heads][D] this KV head's rotated queries
+    float *ctab = qs + 8 * D;                         // key centroids [16] | value centroids [16]
+    float *part = ctab + 32;                          // [8 warps][8 heads][2 + D]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y, sp = blockIdx.x;
-    if (warp < a.G) {
-        float x[ND], y[ND];
-        const int64_t qrow = ((int64_t)b * a.Hq + kvh * a.G + warp) * D;
-#pragma unroll
-        for (int k = 0; k < ND; ++k) x[k] = hd_load(a.q, a.q_dtype, qrow + lane + 32 * k);
-        hd_rotate<ND, false>(Rs, x, y, lane);
-#pragma unroll
-        for (int k = 0; k < ND; ++k) qs[warp * D + lane + 32 * k] = y[k] * a.qscale;
+    const float *qg = a.qrot + ((int64_t)b * a.Hq + kvh * a.G) * D;
+    for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) qs[i] = qg[i];
+    if (threadIdx.x < 16) {
+        ctab[threadIdx.x] = a.kc[threadIdx.x];
+        ctab[16 + threadIdx.x] = a.vc[threadIdx.x];
     }
     __syncthreads();
     int L = a.T;
@@ -290,50 +362,96 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_kernel(const __grid_constan
     const int t0 = sp * a.tps, t1 = min(L, t0 + a.tps);
     const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8;
     const int64_t seg = ((int64_t)b * a.Hkv + kvh) * a.T_cap;
-    float qv[8][ND], m[8], l[8], acc[8][ND];
+    // per head: the warp's running maximum (uniform), this lane's share of l, and the value sums of
+    // dims lane + 32 k
+    float m[8], l[8], acc[8][ND];
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
         m[h] = -INFINITY;
         l[h] = 0.f;
 #pragma unroll
-        for (int k = 0; k < ND; ++k) {
-            qv[h][k] = h < a.G ? qs[h * D + lane + 32 * k] : 0.f;
-            acc[h][k] = 0.f;
-        }
+        for (int k = 0; k < ND; ++k) acc[h][k] = 0.f;
     }
-    for (int t = t0 + warp; t < t1; t += kHdWarps) {
-        const uint8_t *kb = a.k + (seg + t) * KB, *vb = a.v + (seg + t) * VB;
-        const float kn = __half2float(__ushort_as_half((unsigned short)(kb[0] | (kb[1] << 8))));
-        const float vn = __half2float(__ushort_as_half((unsigned short)(vb[0] | (vb[1] << 8))));
-        float kc[ND], vc[ND];
+    // 32 tokens per warp step: lane = token for the scores, lane = dims for the value sums
+    for (int base = t0 + 32 * warp; base < t1; base += 32 * kHdWarps) {
+        const int t = base + lane;
+        const bool valid = t < t1;
+        const uint8_t *kb = a.k + (seg + (valid ? t : base)) * KB;
+        float s[8];
 #pragma unroll
-        for (int k = 0; k < ND; ++k) {
-            kc[k] = a.kc[hd_code<D>(kb, a.kbits, lane + 32 * k)];
-            vc[k] = a.vc[hd_code<D>(vb, a.vbits, lane + 32 * k)] * vn;
+        for (int h = 0; h < 8; ++h) s[h] = 0.f;
+        // the token's D codes, 16 bits at a time (blocks are 2-byte aligned)
+        const uint16_t *kw = reinterpret_cast<const uint16_t *>(kb);
+        if (a.kbits == 3) {
+            for (int w = 0; w < D / 8; ++w) {   // 2-bit plane word w: dims 8w .. 8w + 7
+                const uint32_t lo = kw[1 + w];
+                const uint32_t hb = (kw[1 + D / 8 + (w >> 1)] >> (8 * (w & 1))) & 0xFFu;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float c = ctab[((lo >> (2 * e)) & 3u) | (((hb >> e) & 1u) << 2)];
+                    const int j = 8 * w + e;
+#pragma unroll
+                    for (int h = 0; h < 8; ++h)
+                        if (h < a.G) s[h] = fmaf(qs[h * D + j], c, s[h]);
+                }
+            }
+        } else {
+            const int per = 16 / a.kbits;        // codes per 16-bit word
+            const uint32_t mask = (1u << a.kbits) - 1u;
+            for (int w = 0; w < D / per; ++w) {
+                const uint32_t word = kw[1 + w];
+                for (int e = 0; e < per; ++e) {
+                    const float c = ctab[(word >> (a.kbits * e)) & mask];
+                    const int j = per * w + e;
+#pragma unroll
+                    for (int h = 0; h < 8; ++h)
+                        if (h < a.G) s[h] = fmaf(qs[h * D + j], c, s[h]);
+                }
+            }
         }
+        const float kn = __half2float(__ushort_as_half(kw[0]));
+        float p[8];
 #pragma unroll
         for (int h = 0; h < 8; ++h) {
             if (h >= a.G) break;
-            float s = 0.f;
+            const float sh = valid ? s[h] * kn : -INFINITY;
+            float mx = sh;
 #pragma unroll
-            for (int k = 0; k < ND; ++k) s = fmaf(qv[h][k], kc[k], s);
-            s = hd_warp_sum(s) * kn;
-            const float mn = fmaxf(m[h], s);
-            const float corr = exp2f(m[h] - mn), p = exp2f(s - mn);
-            l[h] = fmaf(l[h], corr, p);
+            for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kHdFull, mx, o));
+            const float mn = fmaxf(m[h], mx);   // finite: the step holds at least one valid token
+            const float corr = exp2f(m[h] - mn);
+            p[h] = valid ? exp2f(sh - mn) : 0.f;
+            l[h] = fmaf(l[h], corr, p[h]);
 #pragma unroll
-            for (int k = 0; k < ND; ++k) acc[h][k] = fmaf(acc[h][k], corr, p * vc[k]);
+            for (int k = 0; k < ND; ++k) acc[h][k] *= corr;
             m[h] = mn;
         }
+        // value sums: token base + tt broadcast to the warp, lanes over dims
+        const int nt = min(32, t1 - base);
+        for (int tt = 0; tt < nt; ++tt) {
+            const uint8_t *vb = a.v + (seg + base + tt) * VB;
+            const float vn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(vb)));
+            float vv[ND];
+#pragma unroll
+            for (int k = 0; k < ND; ++k) vv[k] = ctab[16 + hd_code<D>(vb, a.vbits, lane + 32 * k)] * vn;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                if (h >= a.G) break;
+                const float ph = __shfl_sync(kHdFull, p[h], tt);
+#pragma unroll
+                for (int k = 0; k < ND; ++k) acc[h][k] = fmaf(ph, vv[k], acc[h][k]);
+            }
+        }
     }
-    // the warps' states into shared memory, then warp h merges head h over the 8 warps
+    // l over the warp's lanes, then the warps' states into shared memory; warp h merges head h
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
         if (h >= a.G) break;
+        const float lw = hd_warp_sum(l[h]);
         float *pw = part + (warp * 8 + h) * (2 + D);
         if (lane == 0) {
             pw[0] = m[h];
-            pw[1] = l[h];
+            pw[1] = lw;
         }
 #pragma unroll
         for (int k = 0; k < ND; ++k) pw[2 + lane + 32 * k] = acc[h][k];
@@ -402,15 +520,18 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_combine_kernel(const __grid
 template <int ND>
 int hd_launch_attn(const HdAttnArgs &a, cudaStream_t st) {
     constexpr int D = 32 * ND;
-    static int done_a[64] = {0}, done_c[64] = {0};
-    const int smem_a = D * (D + 1) * 4 + 8 * D * 4 + kHdWarps * 8 * (2 + D) * 4;
-    const int smem_c = D * (D + 1) * 4;
+    static int done_p[64] = {0}, done_a[64] = {0}, done_c[64] = {0};
+    const int smem_a = (8 * D + 32 + kHdWarps * 8 * (2 + D)) * 4;
+    const int smem_r = D * (D + 1) * 4;
+    if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_r, done_p) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_kernel<ND>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
-    if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_c, done_c) != TQ_OK) return TQ_ERR_CUDA;
+    if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_r, done_c) != TQ_OK) return TQ_ERR_CUDA;
+    const int64_t rows = (int64_t)a.B * a.Hq;
+    attn_d_prep_kernel<ND><<<(int)((rows + kHdWarps * kHdRows - 1) / (kHdWarps * kHdRows)), kHdThreads, smem_r, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     attn_d_kernel<ND><<<dim3(a.splits, a.Hkv, a.B), kHdThreads, smem_a, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
-    const int rows = a.B * a.Hq;
-    attn_d_combine_kernel<ND><<<(rows + kHdWarps - 1) / kHdWarps, kHdThreads, smem_c, st>>>(a);
+    attn_d_combine_kernel<ND><<<(int)((rows + kHdWarps - 1) / kHdWarps), kHdThreads, smem_r, st>>>(a);
     return launch_status();
 }
 
@@ -483,7 +604,7 @@ extern "C" size_t tq_attn_workspace_bytes_d(int B, int Hq, int Hkv, int T_cap, i
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv || !hd_dim_ok(head_dim)) return 0;
     int splits, tps;
     hd_split_plan(B, Hkv, T_cap, &splits, &tps);
-    return (size_t)B * Hq * splits * (2 + head_dim) * sizeof(float);
+    return ((size_t)B * Hq * splits * (2 + head_dim) + (size_t)B * Hq * head_dim) * sizeof(float);
 }
 
 extern "C" int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
@@ -519,6 +640,12 @@ extern "C" int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blo
     a.kbits = kcb->bits;
     a.vbits = vcb->bits;
     hd_split_plan(B, Hkv, T, &a.splits, &a.tps);
+    // the rotated queries after the partials of the plan for T_cap (the workspace's size)
+    {
+        int sc, tc;
+        hd_split_plan(B, Hkv, T_cap, &sc, &tc);
+        a.qrot = a.ws + (int64_t)B * Hq * sc * (2 + head_dim);
+    }
     a.qscale = scale * 1.4426950408889634f;
     for (int i = 0; i < 16; ++i) {
         a.kc[i] = i < kcb->levels ? kcb->centroids[i] : 0.f;
