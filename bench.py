@@ -1150,7 +1150,7 @@ def run_gpu(args, rank, world, local_rank):
                        parallelism="replicas" if world > 1 else "single GPU"),
         "frac_hbm": round(value / world / peak, 4),
     }
-    enc_group = next((n for n in ("encode", "ext_encode") if n in groups), None)
+    enc_group = next((n for n in ("encode", "ext_encode", "hd_encode") if n in groups), None)
     if enc_group is not None:
         g = groups[enc_group]
         res["encode_gvec_s"] = round(world * g["nvec"] / (g["ms"] * 1e-3) / 1e9, 3)
