@@ -208,3 +208,13 @@ def test_head_dim_calls_validate_before_launching(tq):
                             None) == tq.TQ_ERR_ALIGN
     assert L.tq_attn_workspace_bytes_d(2, 8, 2, 1000, 96) > 0
     assert L.tq_attn_workspace_bytes_d(2, 8, 3, 1000, 96) == 0
+    # decode attention: T_cap a multiple of 8, block arrays 16-byte aligned
+    f = lambda off=0: ctypes.c_void_p((1 << 20) + off)
+    big = 1 << 40
+
+    def attn(T_cap, k_off=0, v_off=0):
+        return L.tq_attn_decode_d(f(), tq.TQ_F32, f(k_off), ctypes.byref(cb), f(v_off), ctypes.byref(cb), None, 2, 8,
+                                  2, T_cap, 50, 96, ctypes.c_float(0.1), f(), f(), f(), big, None)
+    assert attn(100) == tq.TQ_ERR_ARG
+    assert attn(104, k_off=2) == tq.TQ_ERR_ALIGN
+    assert attn(104, v_off=8) == tq.TQ_ERR_ALIGN

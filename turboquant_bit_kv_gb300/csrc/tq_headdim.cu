@@ -23,11 +23,13 @@
 // once, so every element of R read from shared memory serves four rows.
 // Decode attention: a prep kernel rotates every query once (R q, scale
 // log2(e) folded in); one CTA of 8 warps per (sequence, KV head, context
-// split) then takes 32 tokens per warp step: lane t scores its token
-// against n_t c[code_t] for every head (no cross-lane sums), the warp keeps
-// an online softmax per head, and the value sums run with lanes over dims,
-// each token's probabilities broadcast by shuffles; the warps merge in shared
-// memory, and a combine kernel merges the splits and rotates back (R^T).
+// split) then takes 32 tokens per warp step, each step's K and V blocks
+// staged in shared memory by asynchronous copies while the previous step
+// computes: lane t scores its token against n_t c[code_t] for every head (no
+// cross-lane sums), the warp keeps an online softmax per head, and the value
+// sums run with lanes over dims; the warps merge in shared memory, and a
+// combine kernel merges the splits and rotates back (R^T).  The split count
+// is chosen from the kernel's occupancy so that the CTAs fill whole waves.
 
 #include <cmath>
 #include <cstring>
@@ -302,14 +304,33 @@ struct HdAttnArgs {
     float kc[16], vc[16];
 };
 
-// Context splits: enough CTAs for about two per SM, at least 64 tokens each.
-void hd_split_plan(int B, int Hkv, int T, int *splits, int *tps) {
-    const int segs = B * Hkv;
-    const int want = (2 * sm_count() + segs - 1) / segs;
-    const int most = (T + 63) / 64;
-    int s = want < most ? want : most;
-    if (s < 1) s = 1;
-    *tps = (T + s - 1) / s;
+// Context splits of a (sequence, KV head).  A split is a whole number of 32-token chunks, at least
+// kHdMinChunks of them (two warp steps per warp), so the most splits a context of T tokens takes is
+// hd_max_splits(T); the workspace holds that many partials per (sequence, query head).
+constexpr int kHdMinChunks = 16;
+
+int hd_max_splits(int T) {
+    const int s = ((T + 31) / 32) / kHdMinChunks;
+    return s < 1 ? 1 : s;
+}
+
+// Of those split counts, the one with the shortest makespan for `slots` CTAs resident at once:
+// waves of CTAs times warp steps per CTA (plus one for the CTA's start and merge).
+void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps) {
+    const int64_t segs = (int64_t)B * Hkv;
+    const int C = (T + 31) / 32, smax = hd_max_splits(T);
+    if (slots < 1) slots = 1;
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= smax; ++s) {
+        const int64_t waves = (segs * s + slots - 1) / slots;
+        const int64_t steps = ((C + s - 1) / s + kHdWarps - 1) / kHdWarps + 1;
+        if (best_cost < 0 || waves * steps < best_cost) {
+            best_cost = waves * steps;
+            best = s;
+        }
+    }
+    *tps = (C + best - 1) / best * 32;
     *splits = (T + *tps - 1) / *tps;
 }
 
@@ -338,139 +359,218 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_prep_kernel(const __grid_co
             for (int k = 0; k < ND; ++k) a.qrot[(r0 + r) * D + lane + 32 * k] = y[r][k] * a.qscale;
 }
 
-template <int ND>
-__global__ void __launch_bounds__(kHdThreads) attn_d_kernel(const __grid_constant__ HdAttnArgs a) {
+// s[h] += q[h][j] c: the query of head h at dim j times the centroid (qj: dim j's GB heads).
+template <int GB>
+__device__ __forceinline__ void hd_fma_heads(float (&s)[GB], const float *qj, float c) {
+    const float4 qa = *reinterpret_cast<const float4 *>(qj);
+    s[0] = fmaf(qa.x, c, s[0]);
+    s[1] = fmaf(qa.y, c, s[1]);
+    s[2] = fmaf(qa.z, c, s[2]);
+    s[3] = fmaf(qa.w, c, s[3]);
+    if constexpr (GB == 8) {
+        const float4 qb = *reinterpret_cast<const float4 *>(qj + 4);
+        s[4] = fmaf(qb.x, c, s[4]);
+        s[5] = fmaf(qb.y, c, s[5]);
+        s[6] = fmaf(qb.z, c, s[6]);
+        s[7] = fmaf(qb.w, c, s[7]);
+    }
+}
+
+// One token's scores against the GB heads: s[h] = sum_j q[h][j] kc[code_j] over the D codes of its
+// block (blk, in shared memory; the code area read 16 bits at a time, the 3-bit high plane a byte
+// per eight dims).
+template <int D, int GB, int BITS>
+__device__ __forceinline__ void hd_score(const uint8_t *blk, const float *qs, const float *kc, float (&s)[GB]) {
+    const uint16_t *kw = reinterpret_cast<const uint16_t *>(blk + 2);
+    constexpr int PER = BITS == 4 ? 4 : 8;   // codes per 16-bit word of the (low) plane
+    constexpr int SH = BITS == 4 ? 4 : 2;
+    constexpr uint32_t MASK = BITS == 4 ? 15u : 3u;
+#pragma unroll 2
+    for (int w = 0; w < D / PER; ++w) {
+        const uint32_t word = kw[w];
+        uint32_t hb = 0;
+        if constexpr (BITS == 3) hb = blk[2 + D / 4 + w];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            uint32_t code = (word >> (SH * e)) & MASK;
+            if constexpr (BITS == 3) code |= ((hb >> e) & 1u) << 2;
+            hd_fma_heads<GB>(s, qs + (PER * w + e) * GB, kc[code]);
+        }
+    }
+}
+
+// acc[h][k] += p[t][h] vc[code of dim lane + 32 k of token t] over the step's n tokens (vst: their
+// blocks in shared memory, VB bytes apart; pw: [32][GB] probabilities times value norms).
+template <int D, int GB, int BITS>
+__device__ __forceinline__ void hd_values(const uint8_t *vst, int VB, int n, const float *pw, const float *vc,
+                                          float (&acc)[GB][D / 32], int lane) {
+    constexpr int ND = D / 32;
+#pragma unroll 2
+    for (int tt = 0; tt < n; ++tt) {
+        const uint8_t *vb = vst + tt * VB + 2;
+        float p[GB];
+#pragma unroll
+        for (int h = 0; h < GB; h += 4) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(pw + tt * GB + h);
+            p[h] = q4.x;
+            p[h + 1] = q4.y;
+            p[h + 2] = q4.z;
+            p[h + 3] = q4.w;
+        }
+#pragma unroll
+        for (int k = 0; k < ND; ++k) {
+            const int j = lane + 32 * k;
+            uint32_t code;
+            if constexpr (BITS == 2) code = (vb[j >> 2] >> (2 * (j & 3))) & 3u;
+            else if constexpr (BITS == 4) code = (vb[j >> 1] >> (4 * (j & 1))) & 15u;
+            else code = ((vb[j >> 2] >> (2 * (j & 3))) & 3u) | (((vb[D / 4 + (j >> 3)] >> (j & 7)) & 1u) << 2);
+            const float c = vc[code];
+#pragma unroll
+            for (int h = 0; h < GB; ++h) acc[h][k] = fmaf(p[h], c, acc[h][k]);
+        }
+    }
+}
+
+// One CTA of 8 warps per (sequence, KV head, context split); GB = 4 or 8 head slots (G <= GB).
+// Each warp takes 32-token steps t0 + 32 (warp + 8 i): the step's K and V blocks are copied into a
+// two-stage buffer of the warp's own with 16-byte cp.async pieces while the previous step is
+// computed (chunk starts are 16-byte aligned: T_cap a multiple of 8, 32 blocks a multiple of 16
+// bytes, splits whole chunks).  Lane t scores token t against every head from shared memory (no
+// cross-lane sums), the warp keeps an online softmax per head, and the value sums run with lanes over
+// dims, the step's probabilities times value norms read back from shared memory.
+template <int ND, int GB>
+__global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(const __grid_constant__ HdAttnArgs a) {
     constexpr int D = 32 * ND;
     extern __shared__ __align__(16) float hd_smem[];
-    float *qs = hd_smem;                              // [8 heads][D] this KV head's rotated queries
-    float *ctab = qs + 8 * D;                         // key centroids [16] | value centroids [16]
-    float *part = ctab + 32;                          // [8 warps][8 heads][2 + D]
+    float *qs = hd_smem;                                                   // [D][GB] queries, dim-major
+    float *ctab = qs + D * GB;                                             // key | value centroids
+    float *pvs = ctab + 32;                                                // [warp][32][GB]
+    uint8_t *stg = reinterpret_cast<uint8_t *>(pvs + kHdWarps * 32 * GB);  // [warp][2][32 (KB + VB)]
+    float *part = reinterpret_cast<float *>(stg);                          // [warp][GB][2 + D], at the end
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y, sp = blockIdx.x;
-    const float *qg = a.qrot + ((int64_t)b * a.Hq + kvh * a.G) * D;
-    for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) qs[i] = qg[i];
-    if (threadIdx.x < 16) {
-        ctab[threadIdx.x] = a.kc[threadIdx.x];
-        ctab[16 + threadIdx.x] = a.vc[threadIdx.x];
-    }
-    __syncthreads();
     int L = a.T;
     if (a.seq_lens) {
         const int sl = a.seq_lens[b];
         L = sl < 0 ? 0 : (sl > a.T ? a.T : sl);
     }
     const int t0 = sp * a.tps, t1 = min(L, t0 + a.tps);
-    const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8;
+    const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8, SB = 32 * (KB + VB);
     const int64_t seg = ((int64_t)b * a.Hkv + kvh) * a.T_cap;
-    // per head: the warp's running maximum (uniform), this lane's share of l, and the value sums of
-    // dims lane + 32 k
-    float m[8], l[8], acc[8][ND];
+    const uint8_t *kseg = a.k + seg * KB, *vseg = a.v + seg * VB;
+    uint8_t *wst = stg + warp * 2 * SB;
+    // the K then V blocks of tokens [base, base + n) into stage buf, in whole 16-byte pieces (the
+    // last piece may run up to 15 bytes past the n-th block, still inside the segment's T_cap blocks)
+    auto issue = [&](int base, int buf) {
+        const int n = min(32, t1 - base);
+        const int nk = (n * KB + 15) >> 4, nv = (n * VB + 15) >> 4;
+        const uint8_t *sk = kseg + (int64_t)base * KB, *sv = vseg + (int64_t)base * VB;
+        uint8_t *dk = wst + buf * SB, *dv = dk + 32 * KB;
+        for (int q = lane; q < nk; q += 32) cp_async16(dk + 16 * q, sk + 16 * q);
+        for (int q = lane; q < nv; q += 32) cp_async16(dv + 16 * q, sv + 16 * q);
+        cp_async_commit();
+    };
+    int base = t0 + 32 * warp;
+    if (base < t1) issue(base, 0);   // the first step is on its way while the queries are gathered
+
+    const float *qg = a.qrot + ((int64_t)b * a.Hq + kvh * a.G) * D;
+    for (int i = threadIdx.x; i < D * GB; i += blockDim.x) {
+        const int j = i / GB, h = i % GB;
+        qs[i] = h < a.G ? qg[h * D + j] : 0.f;
+    }
+    if (threadIdx.x < 16) {
+        ctab[threadIdx.x] = a.kc[threadIdx.x];
+        ctab[16 + threadIdx.x] = a.vc[threadIdx.x];
+    }
+    __syncthreads();
+
+    // per head: the warp's running maximum (uniform), this lane's share of l, the value sums of dims
+    // lane + 32 k
+    float m[GB], l[GB], acc[GB][ND];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
+    for (int h = 0; h < GB; ++h) {
         m[h] = -INFINITY;
         l[h] = 0.f;
 #pragma unroll
         for (int k = 0; k < ND; ++k) acc[h][k] = 0.f;
     }
-    // 32 tokens per warp step: lane = token for the scores, lane = dims for the value sums
-    for (int base = t0 + 32 * warp; base < t1; base += 32 * kHdWarps) {
-        const int t = base + lane;
-        const bool valid = t < t1;
-        const uint8_t *kb = a.k + (seg + (valid ? t : base)) * KB;
-        float s[8];
+    float *pw = pvs + warp * 32 * GB;
+    int buf = 0;
+    for (; base < t1; base += 32 * kHdWarps) {
+        const int nb = base + 32 * kHdWarps;
+        if (nb < t1) issue(nb, buf ^ 1);
+        else cp_async_commit();   // (an empty group: the wait below always leaves one group)
+        cp_async_wait<1>();
+        __syncwarp();
+        const uint8_t *sk = wst + buf * SB, *sv = sk + 32 * KB;
+        const int n = min(32, t1 - base);
+        const bool valid = lane < n;
+        const uint8_t *kb = sk + lane * KB;
+        float s[GB];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) s[h] = 0.f;
-        // the token's D codes, 16 bits at a time (blocks are 2-byte aligned)
-        const uint16_t *kw = reinterpret_cast<const uint16_t *>(kb);
-        if (a.kbits == 3) {
-            for (int w = 0; w < D / 8; ++w) {   // 2-bit plane word w: dims 8w .. 8w + 7
-                const uint32_t lo = kw[1 + w];
-                const uint32_t hb = (kw[1 + D / 8 + (w >> 1)] >> (8 * (w & 1))) & 0xFFu;
+        for (int h = 0; h < GB; ++h) s[h] = 0.f;
+        if (a.kbits == 2) hd_score<D, GB, 2>(kb, qs, ctab, s);
+        else if (a.kbits == 3) hd_score<D, GB, 3>(kb, qs, ctab, s);
+        else hd_score<D, GB, 4>(kb, qs, ctab, s);
+        // (past the n-th token a stage holds stale bytes: every use below is selected away)
+        const float kn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(kb)));
+        const float vn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(sv + lane * VB)));
+        float pn[GB];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float c = ctab[((lo >> (2 * e)) & 3u) | (((hb >> e) & 1u) << 2)];
-                    const int j = 8 * w + e;
-#pragma unroll
-                    for (int h = 0; h < 8; ++h)
-                        if (h < a.G) s[h] = fmaf(qs[h * D + j], c, s[h]);
-                }
-            }
-        } else {
-            const int per = 16 / a.kbits;        // codes per 16-bit word
-            const uint32_t mask = (1u << a.kbits) - 1u;
-            for (int w = 0; w < D / per; ++w) {
-                const uint32_t word = kw[1 + w];
-                for (int e = 0; e < per; ++e) {
-                    const float c = ctab[(word >> (a.kbits * e)) & mask];
-                    const int j = per * w + e;
-#pragma unroll
-                    for (int h = 0; h < 8; ++h)
-                        if (h < a.G) s[h] = fmaf(qs[h * D + j], c, s[h]);
-                }
-            }
-        }
-        const float kn = __half2float(__ushort_as_half(kw[0]));
-        float p[8];
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            if (h >= a.G) break;
+        for (int h = 0; h < GB; ++h) {
             const float sh = valid ? s[h] * kn : -INFINITY;
             float mx = sh;
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kHdFull, mx, o));
-            const float mn = fmaxf(m[h], mx);   // finite: the step holds at least one valid token
+            const float mn = fmaxf(m[h], mx);   // finite: the step holds at least one token
             const float corr = exp2f(m[h] - mn);
-            p[h] = valid ? exp2f(sh - mn) : 0.f;
-            l[h] = fmaf(l[h], corr, p[h]);
+            const float p = valid ? exp2f(sh - mn) : 0.f;
+            l[h] = fmaf(l[h], corr, p);
 #pragma unroll
             for (int k = 0; k < ND; ++k) acc[h][k] *= corr;
             m[h] = mn;
+            pn[h] = valid ? p * vn : 0.f;
         }
-        // value sums: token base + tt broadcast to the warp, lanes over dims
-        const int nt = min(32, t1 - base);
-        for (int tt = 0; tt < nt; ++tt) {
-            const uint8_t *vb = a.v + (seg + base + tt) * VB;
-            const float vn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(vb)));
-            float vv[ND];
 #pragma unroll
-            for (int k = 0; k < ND; ++k) vv[k] = ctab[16 + hd_code<D>(vb, a.vbits, lane + 32 * k)] * vn;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                if (h >= a.G) break;
-                const float ph = __shfl_sync(kHdFull, p[h], tt);
-#pragma unroll
-                for (int k = 0; k < ND; ++k) acc[h][k] = fmaf(ph, vv[k], acc[h][k]);
-            }
-        }
+        for (int h = 0; h < GB; h += 4)
+            *reinterpret_cast<float4 *>(pw + lane * GB + h) = make_float4(pn[h], pn[h + 1], pn[h + 2], pn[h + 3]);
+        __syncwarp();
+        if (a.vbits == 2) hd_values<D, GB, 2>(sv, VB, n, pw, ctab + 16, acc, lane);
+        else if (a.vbits == 3) hd_values<D, GB, 3>(sv, VB, n, pw, ctab + 16, acc, lane);
+        else hd_values<D, GB, 4>(sv, VB, n, pw, ctab + 16, acc, lane);
+        __syncwarp();   // the stage and pw are free for the next step
+        buf ^= 1;
     }
+    cp_async_wait<0>();
+    __syncthreads();   // every warp is done with its stages: part takes their place
     // l over the warp's lanes, then the warps' states into shared memory; warp h merges head h
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
+    for (int h = 0; h < GB; ++h) {
         if (h >= a.G) break;
         const float lw = hd_warp_sum(l[h]);
-        float *pw = part + (warp * 8 + h) * (2 + D);
+        float *pp = part + (warp * GB + h) * (2 + D);
         if (lane == 0) {
-            pw[0] = m[h];
-            pw[1] = lw;
+            pp[0] = m[h];
+            pp[1] = lw;
         }
 #pragma unroll
-        for (int k = 0; k < ND; ++k) pw[2 + lane + 32 * k] = acc[h][k];
+        for (int k = 0; k < ND; ++k) pp[2 + lane + 32 * k] = acc[h][k];
     }
     __syncthreads();
     if (warp < a.G) {
         const int h = warp;
         float M = -INFINITY;
-        for (int w = 0; w < kHdWarps; ++w) M = fmaxf(M, part[(w * 8 + h) * (2 + D)]);
+        for (int w = 0; w < kHdWarps; ++w) M = fmaxf(M, part[(w * GB + h) * (2 + D)]);
         float lt = 0.f, o[ND];
 #pragma unroll
         for (int k = 0; k < ND; ++k) o[k] = 0.f;
         if (M != -INFINITY) {
             for (int w = 0; w < kHdWarps; ++w) {
-                const float *pw = part + (w * 8 + h) * (2 + D);
-                const float f = pw[0] == -INFINITY ? 0.f : exp2f(pw[0] - M);
-                lt = fmaf(pw[1], f, lt);
+                const float *pp = part + (w * GB + h) * (2 + D);
+                const float f = pp[0] == -INFINITY ? 0.f : exp2f(pp[0] - M);
+                lt = fmaf(pp[1], f, lt);
 #pragma unroll
-                for (int k = 0; k < ND; ++k) o[k] = fmaf(pw[2 + lane + 32 * k], f, o[k]);
+                for (int k = 0; k < ND; ++k) o[k] = fmaf(pp[2 + lane + 32 * k], f, o[k]);
             }
         }
         float *dst = a.ws + (((int64_t)b * a.Hq + kvh * a.G + h) * a.splits + sp) * (2 + D);
@@ -517,22 +617,35 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_combine_kernel(const __grid
     for (int k = 0; k < ND; ++k) a.out[row * D + lane + 32 * k] = x[k];
 }
 
-template <int ND>
-int hd_launch_attn(const HdAttnArgs &a, cudaStream_t st) {
+template <int ND, int GB>
+int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     constexpr int D = 32 * ND;
     static int done_p[64] = {0}, done_a[64] = {0}, done_c[64] = {0};
-    const int smem_a = (8 * D + 32 + kHdWarps * 8 * (2 + D)) * 4;
+    static int resident[5][5] = {{0}};   // CTAs per SM by (key bits, value bits)
+    const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8;
+    const int stages = kHdWarps * 2 * 32 * (KB + VB), part = kHdWarps * GB * (2 + D) * 4;
+    const int smem_a = (D * GB + 32 + kHdWarps * 32 * GB) * 4 + (stages > part ? stages : part);
     const int smem_r = D * (D + 1) * 4;
     if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_r, done_p) != TQ_OK) return TQ_ERR_CUDA;
-    if (set_smem_limit((const void *)attn_d_kernel<ND>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
+    if (set_smem_limit((const void *)attn_d_kernel<ND, GB>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_r, done_c) != TQ_OK) return TQ_ERR_CUDA;
+    int &per_sm = resident[a.kbits][a.vbits];
+    if (per_sm <= 0 &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_d_kernel<ND, GB>, kHdThreads, smem_a) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), &a.splits, &a.tps);
     const int64_t rows = (int64_t)a.B * a.Hq;
     attn_d_prep_kernel<ND><<<(int)((rows + kHdWarps * kHdRows - 1) / (kHdWarps * kHdRows)), kHdThreads, smem_r, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
-    attn_d_kernel<ND><<<dim3(a.splits, a.Hkv, a.B), kHdThreads, smem_a, st>>>(a);
+    attn_d_kernel<ND, GB><<<dim3(a.splits, a.Hkv, a.B), kHdThreads, smem_a, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     attn_d_combine_kernel<ND><<<(int)((rows + kHdWarps - 1) / kHdWarps), kHdThreads, smem_r, st>>>(a);
     return launch_status();
+}
+
+template <int ND>
+int hd_launch_attn(HdAttnArgs &a, cudaStream_t st) {
+    return a.G <= 4 ? hd_launch_attn_g<ND, 4>(a, st) : hd_launch_attn_g<ND, 8>(a, st);
 }
 
 }  // namespace
@@ -602,9 +715,7 @@ extern "C" int tq_decode_kv_d(const uint8_t *blocks, int64_t n_vec, int head_dim
 
 extern "C" size_t tq_attn_workspace_bytes_d(int B, int Hq, int Hkv, int T_cap, int head_dim) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || T_cap <= 0 || Hq % Hkv || !hd_dim_ok(head_dim)) return 0;
-    int splits, tps;
-    hd_split_plan(B, Hkv, T_cap, &splits, &tps);
-    return ((size_t)B * Hq * splits * (2 + head_dim) + (size_t)B * Hq * head_dim) * sizeof(float);
+    return ((size_t)B * Hq * hd_max_splits(T_cap) * (2 + head_dim) + (size_t)B * Hq * head_dim) * sizeof(float);
 }
 
 extern "C" int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,
@@ -612,13 +723,15 @@ extern "C" int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blo
                                 int Hq, int Hkv, int T_cap, int T, int head_dim, float scale, const float *R,
                                 float *out, void *workspace, size_t workspace_bytes, void *stream) {
     if (!q || !k_blocks || !kcb || !v_blocks || !vcb || !R || !out || !workspace) return TQ_ERR_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || !std::isfinite(scale))
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T_cap <= 0 || T < 1 || T > T_cap || (T_cap & 7) ||
+        !std::isfinite(scale))
         return TQ_ERR_ARG;
     const int G = Hq / Hkv;
     if (G > 8 || !hd_dim_ok(head_dim) || !hd_codebook_ok(kcb, head_dim) || !hd_codebook_ok(vcb, head_dim) ||
         dtype_bytes(q_dtype) == 0)
         return TQ_ERR_UNSUPPORTED;
-    if (!aligned(q, dtype_bytes(q_dtype)) || !aligned(out, 4) || !aligned(R, 16) || !aligned(workspace, 16))
+    if (!aligned(q, dtype_bytes(q_dtype)) || !aligned(k_blocks, 16) || !aligned(v_blocks, 16) || !aligned(out, 4) ||
+        !aligned(R, 16) || !aligned(workspace, 16))
         return TQ_ERR_ALIGN;
     if (workspace_bytes < tq_attn_workspace_bytes_d(B, Hq, Hkv, T_cap, head_dim)) return TQ_ERR_WORKSPACE;
     HdAttnArgs a;
@@ -639,13 +752,9 @@ extern "C" int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blo
     a.T = T;
     a.kbits = kcb->bits;
     a.vbits = vcb->bits;
-    hd_split_plan(B, Hkv, T, &a.splits, &a.tps);
-    // the rotated queries after the partials of the plan for T_cap (the workspace's size)
-    {
-        int sc, tc;
-        hd_split_plan(B, Hkv, T_cap, &sc, &tc);
-        a.qrot = a.ws + (int64_t)B * Hq * sc * (2 + head_dim);
-    }
+    // the rotated queries after room for the most partials a context of T_cap tokens takes (the
+    // split plan itself is made at launch, from the kernel's occupancy)
+    a.qrot = a.ws + (int64_t)B * Hq * hd_max_splits(T_cap) * (2 + head_dim);
     a.qscale = scale * 1.4426950408889634f;
     for (int i = 0; i < 16; ++i) {
         a.kc[i] = i < kcb->levels ? kcb->centroids[i] : 0.f;
