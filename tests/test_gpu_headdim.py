@@ -90,6 +90,92 @@ def test_encode_decode_match_oracle(env, d, bits, dtype):
     assert np.max(np.abs(out.double().cpu().numpy() - ref) / np.maximum(nrm, 1e-30)) < 1e-5
 
 
+@pytest.mark.parametrize("d", (64, 96, 128, 160))
+@pytest.mark.parametrize("bits", (2, 3, 4))
+@pytest.mark.parametrize("dtype", (torch.bfloat16, torch.float16))
+def test_encode_tensor_core_rows_match_oracle(env, d, bits, dtype):
+    """More than 1024 bf16 / fp16 rows take the tensor-core encode (R as two
+    16-bit terms): a ragged last tile, a zero row, rows whose float32 sum of
+    squares leaves the safe range (bf16) or is small (fp16), into a 16-byte
+    aligned block array (bulk stores) and into one that is only 2-byte
+    aligned (2-byte stores)."""
+    tq, dev = env["tq"], env["dev"]
+    R, Rd = _rotation(env, d)
+    c, b32 = _books(d, bits)
+    cb = tq.tq_codebook_load(d, bits)
+    n = 128 * 23 + 37
+    x = torch.randn((n, d), generator=torch.Generator().manual_seed(7 * d + bits), dtype=torch.float32)
+    x[7] = 0
+    if dtype == torch.bfloat16:
+        x[300] *= 1e-22      # squares underflow float32
+        x[301] *= 1e17       # squares overflow float32
+    else:
+        x[300] *= 1e-3
+        x[301] *= 1000.0
+    x = x.to(dtype)
+    xd = x.to(dev)
+    bb = tq.tq_block_bytes_d(d, bits)
+    ridx, rn16, y = headdim.encode_d(x.double().numpy(), R, b32)
+    aligned = torch.empty((n, bb), dtype=torch.uint8, device=dev)
+    padded = torch.full((n + 2, bb), 0xA5, dtype=torch.uint8, device=dev)
+    tq.tq_encode_kv_d(xd, cb, Rd, aligned)
+    tq.tq_encode_kv_d(xd, cb, Rd, padded[1:n + 1])
+    torch.cuda.synchronize()
+    got_p = padded.cpu().numpy()
+    assert np.all(got_p[0] == 0xA5) and np.all(got_p[-1] == 0xA5)   # nothing written outside
+    for label, got in (("aligned", aligned.cpu().numpy()), ("2-byte aligned", got_p[1:n + 1])):
+        idx, n16 = headdim.unpack_d(got, d, bits)
+        _check("tensor-core head dim %d %s %s" % (d, str(dtype), label), bits, idx, ridx, y, b32, n16, rn16,
+               x.double().numpy())
+        assert np.all(idx[7] == (1 << bits) // 2) and n16[7] == 0
+    assert np.array_equal(aligned.cpu().numpy(), got_p[1:n + 1])
+
+
+def _near_tie_pairs(rng, k):
+    """fp16 pairs (a, b) whose norm sqrt(a^2 + b^2) lies within 2^-20 (relative)
+    of an fp16 rounding boundary, but not within 2^-30."""
+    out = []
+    while len(out) < k:
+        a = rng.uniform(0.5, 2.0, 200000).astype(np.float16).astype(np.float64)
+        b = rng.uniform(0.5, 2.0, 200000).astype(np.float16).astype(np.float64)
+        dist = fp16_tie_distance(np.sqrt(a * a + b * b))
+        sel = (dist < 2.0**-20) & (dist > 2.0**-30)
+        out.extend(zip(a[sel], b[sel]))
+    return np.array(out[:k])
+
+
+@pytest.mark.parametrize("d", (64, 160))
+def test_encode_tensor_core_norms_near_fp16_ties(env, d):
+    """Rows whose norm lies within 2^-20 of an fp16 rounding boundary take the
+    exact norm (listed in the main loop, rewritten after it): nine rows in ten
+    here, so most CTAs' lists (512 rows) overflow and every row of such a CTA
+    is redone; the norms must still be the correctly rounded ones."""
+    tq, dev = env["tq"], env["dev"]
+    R, Rd = _rotation(env, d)
+    c, b32 = _books(d, 4)
+    rng = np.random.default_rng(d)
+    n = 152 * 5 * 128
+    x = np.zeros((n, d))
+    pairs = _near_tie_pairs(rng, n)
+    rows = np.arange(n)
+    i = rows % d
+    j = (i + 1 + rows % (d - 1)) % d
+    sg = rng.choice([-1.0, 1.0], (n, 2))
+    x[rows, i] = pairs[:, 0] * sg[:, 0]
+    x[rows, j] = pairs[:, 1] * sg[:, 1]
+    plain = rng.random(n) < 0.1
+    x[plain] = rng.standard_normal((int(plain.sum()), d))
+    xt = torch.from_numpy(x).to(torch.float16)
+    blocks = torch.empty((n, tq.tq_block_bytes_d(d, 4)), dtype=torch.uint8, device=dev)
+    tq.tq_encode_kv_d(xt.to(dev), tq.tq_codebook_load(d, 4), Rd, blocks)
+    torch.cuda.synchronize()
+    idx, n16 = headdim.unpack_d(blocks.cpu().numpy(), d, 4)
+    ridx, rn16, y = headdim.encode_d(xt.double().numpy(), R, b32)
+    nn = np.sqrt(np.sum(xt.double().numpy() ** 2, axis=1))
+    assert np.mean(fp16_tie_distance(nn) < 2.0**-20) > 0.85      # the rows are where they should be
+    _check("near-tie norms head dim %d" % d, 4, idx, ridx, y, b32, n16, rn16, xt.double().numpy())
+
+
 @pytest.mark.parametrize("d,kbits,vbits,B,Hq,Hkv,T,lens", [
     (64, 4, 2, 3, 8, 2, 700, [700, 1, 333]),
     (96, 3, 3, 2, 14, 2, 1000, None),

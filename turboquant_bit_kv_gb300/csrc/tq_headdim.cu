@@ -691,6 +691,9 @@ extern "C" int tq_encode_kv_d(const void *x, int x_dtype, int64_t n_vec, int hea
     a.bits = cb->bits;
     a.dt = x_dtype;
     hd_fill(a, cb);
+    // bf16 / fp16 rows: the tensor-core kernel (1: not its form, e.g. few rows)
+    const int r = hd_encode_tc(x, x_dtype, n_vec, head_dim, cb, R, blocks, static_cast<cudaStream_t>(stream));
+    if (r != 1) return r;
     return hd_codec(a, head_dim, true, static_cast<cudaStream_t>(stream));
 }
 

@@ -54,6 +54,15 @@ int wait_failed_attn_k3(unsigned *v, bool clear);
 int wait_failed_attn_k4(unsigned *v, bool clear);
 int wait_failed_attn_k8(unsigned *v, bool clear);
 int wait_failed_prefill(unsigned *v, bool clear);
+int wait_failed_headdim(unsigned *v, bool clear);
+
+// Encode at head dims 64 / 96 / 128 / 160 with the caller's rotation R on
+// the tensor cores (tq_headdim_tc.cu): bf16 / fp16 rows, at least
+// kHdTcMinRows of them, contiguous.  Returns 1 when it does not handle the
+// call (then nothing was enqueued), else a TQ_ status.
+constexpr int64_t kHdTcMinRows = 1024;
+int hd_encode_tc(const void *x, int x_dtype, int64_t n_vec, int d, const tq_codebook *cb, const float *R,
+                 uint8_t *blocks, cudaStream_t st);
 
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

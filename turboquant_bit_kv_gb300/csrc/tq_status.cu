@@ -27,7 +27,7 @@ extern "C" int tq_device_status(int clear, void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TQ_ERR_CUDA;
     int (*const readers[])(unsigned *, bool) = {wait_failed_encode, wait_failed_qjl, wait_failed_attn_k2,
                                                wait_failed_attn_k3, wait_failed_attn_k4, wait_failed_attn_k8,
-                                               wait_failed_prefill};
+                                               wait_failed_prefill, wait_failed_headdim};
     unsigned any = 0;
     for (auto rd : readers) {
         unsigned v = 0;
