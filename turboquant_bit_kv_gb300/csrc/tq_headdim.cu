@@ -115,10 +115,31 @@ __device__ __forceinline__ double hd_warp_sum_d(double v) {
     return v;
 }
 
-// R into shared memory, rows padded to D + 1 floats.
+// R into shared memory, rows padded to D + 1 floats: 16-byte loads (R is 16-byte aligned and a
+// row holds D / 4 of them), all of a thread's loads issued before its stores.
 template <int D>
 __device__ __forceinline__ void hd_load_R(float *Rs, const float *R) {
-    for (int i = threadIdx.x; i < D * D; i += blockDim.x) Rs[(i / D) * (D + 1) + i % D] = R[i];
+    constexpr int N4 = D * D / 4;
+    const float4 *R4 = reinterpret_cast<const float4 *>(R);
+    for (int q0 = threadIdx.x; q0 < N4; q0 += 8 * blockDim.x) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u * blockDim.x;
+            if (q < N4) v[u] = __ldg(R4 + q);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u * blockDim.x;
+            if (q < N4) {
+                float *d = Rs + (4 * q / D) * (D + 1) + (4 * q) % D;
+                d[0] = v[u].x;
+                d[1] = v[u].y;
+                d[2] = v[u].z;
+                d[3] = v[u].w;
+            }
+        }
+    }
 }
 
 // out[k] += sum_j M(lane + 32 k, j) v_j over the warp's D inputs v (element j in lane j % 32,
@@ -334,45 +355,40 @@ void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps) {
     *splits = (T + *tps - 1) / *tps;
 }
 
-// R q times scale log2(e) for every (sequence, query head), kHdRows per warp.
+// R q times scale log2(e) for every (sequence, query head), one per warp (the rows are few: more
+// CTAs, each with a shorter chain, finish sooner).
 template <int ND>
 __global__ void __launch_bounds__(kHdThreads) attn_d_prep_kernel(const __grid_constant__ HdAttnArgs a) {
     constexpr int D = 32 * ND;
+    // the attention kernel may start now: its first copies do not depend on this grid
+    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(16) float hd_smem[];
     float *Rs = hd_smem;
     hd_load_R<D>(Rs, a.R);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t rows = (int64_t)a.B * a.Hq;
-    const int64_t r0 = ((int64_t)blockIdx.x * kHdWarps + warp) * kHdRows;
-    if (r0 >= rows) return;
-    float x[kHdRows][ND], y[kHdRows][ND];
+    const int64_t row = (int64_t)blockIdx.x * kHdWarps + warp;
+    if (row >= (int64_t)a.B * a.Hq) return;
+    float x[ND], y[ND];
 #pragma unroll
-    for (int r = 0; r < kHdRows; ++r)
+    for (int k = 0; k < ND; ++k) x[k] = hd_load(a.q, a.q_dtype, row * D + lane + 32 * k);
+    hd_rotate<ND, false>(Rs, x, y, lane);
 #pragma unroll
-        for (int k = 0; k < ND; ++k) x[r][k] = r0 + r < rows ? hd_load(a.q, a.q_dtype, (r0 + r) * D + lane + 32 * k) : 0.f;
-    hd_rotate_rows<ND, false, kHdRows>(Rs, x, y, lane);
-#pragma unroll
-    for (int r = 0; r < kHdRows; ++r)
-        if (r0 + r < rows)
-#pragma unroll
-            for (int k = 0; k < ND; ++k) a.qrot[(r0 + r) * D + lane + 32 * k] = y[r][k] * a.qscale;
+    for (int k = 0; k < ND; ++k) a.qrot[row * D + lane + 32 * k] = y[k] * a.qscale;
 }
 
-// s[h] += q[h][j] c: the query of head h at dim j times the centroid (qj: dim j's GB heads).
+// s[h] += q[h][j] c: the query of head h at dim j times the centroid (qj: dim j's GB heads), two
+// heads per packed float32 pair (s[i] = heads 2i, 2i + 1).
 template <int GB>
-__device__ __forceinline__ void hd_fma_heads(float (&s)[GB], const float *qj, float c) {
+__device__ __forceinline__ void hd_fma_heads(float2 (&s)[GB / 2], const float *qj, float c) {
+    const float2 cc = make_float2(c, c);
     const float4 qa = *reinterpret_cast<const float4 *>(qj);
-    s[0] = fmaf(qa.x, c, s[0]);
-    s[1] = fmaf(qa.y, c, s[1]);
-    s[2] = fmaf(qa.z, c, s[2]);
-    s[3] = fmaf(qa.w, c, s[3]);
+    s[0] = __ffma2_rn(make_float2(qa.x, qa.y), cc, s[0]);
+    s[1] = __ffma2_rn(make_float2(qa.z, qa.w), cc, s[1]);
     if constexpr (GB == 8) {
         const float4 qb = *reinterpret_cast<const float4 *>(qj + 4);
-        s[4] = fmaf(qb.x, c, s[4]);
-        s[5] = fmaf(qb.y, c, s[5]);
-        s[6] = fmaf(qb.z, c, s[6]);
-        s[7] = fmaf(qb.w, c, s[7]);
+        s[2] = __ffma2_rn(make_float2(qb.x, qb.y), cc, s[2]);
+        s[3] = __ffma2_rn(make_float2(qb.z, qb.w), cc, s[3]);
     }
 }
 
@@ -380,7 +396,7 @@ __device__ __forceinline__ void hd_fma_heads(float (&s)[GB], const float *qj, fl
 // block (blk, in shared memory; the code area read 16 bits at a time, the 3-bit high plane a byte
 // per eight dims).
 template <int D, int GB, int BITS>
-__device__ __forceinline__ void hd_score(const uint8_t *blk, const float *qs, const float *kc, float (&s)[GB]) {
+__device__ __forceinline__ void hd_score(const uint8_t *blk, const float *qs, const float *kc, float2 (&s)[GB / 2]) {
     const uint16_t *kw = reinterpret_cast<const uint16_t *>(blk + 2);
     constexpr int PER = BITS == 4 ? 4 : 8;   // codes per 16-bit word of the (low) plane
     constexpr int SH = BITS == 4 ? 4 : 2;
@@ -399,34 +415,44 @@ __device__ __forceinline__ void hd_score(const uint8_t *blk, const float *qs, co
     }
 }
 
-// acc[h][k] += p[t][h] vc[code of dim lane + 32 k of token t] over the step's n tokens (vst: their
-// blocks in shared memory, VB bytes apart; pw: [32][GB] probabilities times value norms).
+// 32 bits of a code area (2-byte aligned, 16 bytes readable past it) from bit `bit` on: the two
+// 16-bit words that hold them, shifted (at least 17 valid bits).
+__device__ __forceinline__ uint32_t hd_window(const uint8_t *area, int bit) {
+    const uint16_t *w = reinterpret_cast<const uint16_t *>(area) + (bit >> 4);
+    return ((uint32_t)w[0] | ((uint32_t)w[1] << 16)) >> (bit & 15);
+}
+
+// acc[h][k] += p[t][h] vc[code of dim ND lane + k of token t] over the step's n tokens (vst: their
+// blocks in shared memory, VB bytes apart; pw: [32][GB] probabilities times value norms), two heads
+// per packed float32 pair (acc[i][k] = heads 2i, 2i + 1).  A lane's ND consecutive codes are one bit
+// window of the code area (the 3-bit high plane a second).
 template <int D, int GB, int BITS>
 __device__ __forceinline__ void hd_values(const uint8_t *vst, int VB, int n, const float *pw, const float *vc,
-                                          float (&acc)[GB][D / 32], int lane) {
+                                          float2 (&acc)[GB / 2][D / 32], int lane) {
     constexpr int ND = D / 32;
+    constexpr int CB = BITS == 4 ? 4 : 2;   // bits per code in the (low) plane
+    const int lo_bit = CB * ND * lane, hi_bit = 8 * (D / 4) + ND * lane;
 #pragma unroll 2
     for (int tt = 0; tt < n; ++tt) {
-        const uint8_t *vb = vst + tt * VB + 2;
-        float p[GB];
+        const uint8_t *area = vst + tt * VB + 2;
+        float2 p[GB / 2];
 #pragma unroll
         for (int h = 0; h < GB; h += 4) {
             const float4 q4 = *reinterpret_cast<const float4 *>(pw + tt * GB + h);
-            p[h] = q4.x;
-            p[h + 1] = q4.y;
-            p[h + 2] = q4.z;
-            p[h + 3] = q4.w;
+            p[h / 2] = make_float2(q4.x, q4.y);
+            p[h / 2 + 1] = make_float2(q4.z, q4.w);
         }
+        const uint32_t wl = hd_window(area, lo_bit);
+        uint32_t wh = 0;
+        if constexpr (BITS == 3) wh = hd_window(area, hi_bit);
 #pragma unroll
         for (int k = 0; k < ND; ++k) {
-            const int j = lane + 32 * k;
-            uint32_t code;
-            if constexpr (BITS == 2) code = (vb[j >> 2] >> (2 * (j & 3))) & 3u;
-            else if constexpr (BITS == 4) code = (vb[j >> 1] >> (4 * (j & 1))) & 15u;
-            else code = ((vb[j >> 2] >> (2 * (j & 3))) & 3u) | (((vb[D / 4 + (j >> 3)] >> (j & 7)) & 1u) << 2);
+            uint32_t code = (wl >> (CB * k)) & ((1u << CB) - 1u);
+            if constexpr (BITS == 3) code |= ((wh >> k) & 1u) << 2;
             const float c = vc[code];
+            const float2 cc = make_float2(c, c);
 #pragma unroll
-            for (int h = 0; h < GB; ++h) acc[h][k] = fmaf(p[h], c, acc[h][k]);
+            for (int i = 0; i < GB / 2; ++i) acc[i][k] = __ffma2_rn(p[i], cc, acc[i][k]);
         }
     }
 }
@@ -472,28 +498,32 @@ __global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(con
     };
     int base = t0 + 32 * warp;
     if (base < t1) issue(base, 0);   // the first step is on its way while the queries are gathered
-
+    if (threadIdx.x < 16) {
+        ctab[threadIdx.x] = a.kc[threadIdx.x];
+        ctab[16 + threadIdx.x] = a.vc[threadIdx.x];
+    }
+    // the rotated queries come from the prep kernel this one depends on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *qg = a.qrot + ((int64_t)b * a.Hq + kvh * a.G) * D;
     for (int i = threadIdx.x; i < D * GB; i += blockDim.x) {
         const int j = i / GB, h = i % GB;
         qs[i] = h < a.G ? qg[h * D + j] : 0.f;
     }
-    if (threadIdx.x < 16) {
-        ctab[threadIdx.x] = a.kc[threadIdx.x];
-        ctab[16 + threadIdx.x] = a.vc[threadIdx.x];
-    }
     __syncthreads();
 
     // per head: the warp's running maximum (uniform), this lane's share of l, the value sums of dims
-    // lane + 32 k
-    float m[GB], l[GB], acc[GB][ND];
+    // ND lane + k
+    float m[GB], l[GB];
+    float2 acc[GB / 2][ND];   // heads 2i, 2i + 1
 #pragma unroll
     for (int h = 0; h < GB; ++h) {
         m[h] = -INFINITY;
         l[h] = 0.f;
-#pragma unroll
-        for (int k = 0; k < ND; ++k) acc[h][k] = 0.f;
     }
+#pragma unroll
+    for (int i = 0; i < GB / 2; ++i)
+#pragma unroll
+        for (int k = 0; k < ND; ++k) acc[i][k] = make_float2(0.f, 0.f);
     float *pw = pvs + warp * 32 * GB;
     int buf = 0;
     for (; base < t1; base += 32 * kHdWarps) {
@@ -506,30 +536,34 @@ __global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(con
         const int n = min(32, t1 - base);
         const bool valid = lane < n;
         const uint8_t *kb = sk + lane * KB;
-        float s[GB];
+        float2 s2[GB / 2];
 #pragma unroll
-        for (int h = 0; h < GB; ++h) s[h] = 0.f;
-        if (a.kbits == 2) hd_score<D, GB, 2>(kb, qs, ctab, s);
-        else if (a.kbits == 3) hd_score<D, GB, 3>(kb, qs, ctab, s);
-        else hd_score<D, GB, 4>(kb, qs, ctab, s);
+        for (int i = 0; i < GB / 2; ++i) s2[i] = make_float2(0.f, 0.f);
+        if (a.kbits == 2) hd_score<D, GB, 2>(kb, qs, ctab, s2);
+        else if (a.kbits == 3) hd_score<D, GB, 3>(kb, qs, ctab, s2);
+        else hd_score<D, GB, 4>(kb, qs, ctab, s2);
         // (past the n-th token a stage holds stale bytes: every use below is selected away)
         const float kn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(kb)));
         const float vn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(sv + lane * VB)));
-        float pn[GB];
+        float pn[GB], corr[GB];
 #pragma unroll
         for (int h = 0; h < GB; ++h) {
-            const float sh = valid ? s[h] * kn : -INFINITY;
+            const float sh = valid ? ((h & 1) ? s2[h >> 1].y : s2[h >> 1].x) * kn : -INFINITY;
             float mx = sh;
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kHdFull, mx, o));
             const float mn = fmaxf(m[h], mx);   // finite: the step holds at least one token
-            const float corr = exp2f(m[h] - mn);
+            corr[h] = exp2f(m[h] - mn);
             const float p = valid ? exp2f(sh - mn) : 0.f;
-            l[h] = fmaf(l[h], corr, p);
-#pragma unroll
-            for (int k = 0; k < ND; ++k) acc[h][k] *= corr;
+            l[h] = fmaf(l[h], corr[h], p);
             m[h] = mn;
             pn[h] = valid ? p * vn : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < GB / 2; ++i) {
+            const float2 c2 = make_float2(corr[2 * i], corr[2 * i + 1]);
+#pragma unroll
+            for (int k = 0; k < ND; ++k) acc[i][k] = __fmul2_rn(acc[i][k], c2);
         }
 #pragma unroll
         for (int h = 0; h < GB; h += 4)
@@ -542,6 +576,9 @@ __global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(con
         buf ^= 1;
     }
     cp_async_wait<0>();
+    // the combine kernel may take its place on the SMs now (its R load overlaps this grid's tail);
+    // it waits for this grid to finish before it reads the partials
+    asm volatile("griddepcontrol.launch_dependents;");
     __syncthreads();   // every warp is done with its stages: part takes their place
     // l over the warp's lanes, then the warps' states into shared memory; warp h merges head h
 #pragma unroll
@@ -554,7 +591,7 @@ __global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(con
             pp[1] = lw;
         }
 #pragma unroll
-        for (int k = 0; k < ND; ++k) pp[2 + lane + 32 * k] = acc[h][k];
+        for (int k = 0; k < ND; ++k) pp[2 + ND * lane + k] = (h & 1) ? acc[h >> 1][k].y : acc[h >> 1][k].x;
     }
     __syncthreads();
     if (warp < a.G) {
@@ -591,24 +628,41 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_combine_kernel(const __grid
     float *Rs = hd_smem;
     hd_load_R<D>(Rs, a.R);
     __syncthreads();
+    // the partials come from the attention kernel this one depends on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kHdWarps + warp;   // b * Hq + head
     if (row >= (int64_t)a.B * a.Hq) return;
     const float *src = a.ws + row * a.splits * (2 + D);
+    // the splits' maxima, one split per lane (the loads issued together), then the warp's maximum
     float M = -INFINITY;
-    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, src[s * (2 + D)]);
-    float lt = 0.f, o[ND], x[ND];
+    for (int s = lane; s < a.splits; s += 32) M = fmaxf(M, src[s * (2 + D)]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kHdFull, M, o));
+    float lp = 0.f, o[ND], x[ND];
 #pragma unroll
     for (int k = 0; k < ND; ++k) o[k] = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < a.splits; ++s) {
-            const float *ps = src + s * (2 + D);
-            const float f = ps[0] == -INFINITY ? 0.f : exp2f(ps[0] - M);
-            lt = fmaf(ps[1], f, lt);
+        for (int s0 = 0; s0 < a.splits; s0 += 32) {
+            // split s0 + lane's weight, then its sums broadcast split by split (loads independent
+            // of the weights, so several are in flight)
+            float f = 0.f;
+            if (s0 + lane < a.splits) {
+                const float *ps = src + (s0 + lane) * (2 + D);
+                f = ps[0] == -INFINITY ? 0.f : exp2f(ps[0] - M);
+                lp = fmaf(ps[1], f, lp);
+            }
+            const int ns = min(32, a.splits - s0);
+#pragma unroll 4
+            for (int t = 0; t < ns; ++t) {
+                const float ft = __shfl_sync(kHdFull, f, t);
+                const float *ps = src + (s0 + t) * (2 + D) + 2;
 #pragma unroll
-            for (int k = 0; k < ND; ++k) o[k] = fmaf(ps[2 + lane + 32 * k], f, o[k]);
+                for (int k = 0; k < ND; ++k) o[k] = fmaf(ps[lane + 32 * k], ft, o[k]);
+            }
         }
     }
+    const float lt = hd_warp_sum(lp);
     const float inv = lt > 0.f ? 1.f / lt : 0.f;   // an empty sequence gives a zero row
 #pragma unroll
     for (int k = 0; k < ND; ++k) o[k] *= inv;
@@ -624,7 +678,8 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     static int resident[5][5] = {{0}};   // CTAs per SM by (key bits, value bits)
     const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8;
     const int stages = kHdWarps * 2 * 32 * (KB + VB), part = kHdWarps * GB * (2 + D) * 4;
-    const int smem_a = (D * GB + 32 + kHdWarps * 32 * GB) * 4 + (stages > part ? stages : part);
+    // (16 bytes past the stages: a lane's value-code window may read a word beyond the last block)
+    const int smem_a = (D * GB + 32 + kHdWarps * 32 * GB) * 4 + (stages > part ? stages : part) + 16;
     const int smem_r = D * (D + 1) * 4;
     if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_r, done_p) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_kernel<ND, GB>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
@@ -635,11 +690,24 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
         return TQ_ERR_CUDA;
     hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), &a.splits, &a.tps);
     const int64_t rows = (int64_t)a.B * a.Hq;
-    attn_d_prep_kernel<ND><<<(int)((rows + kHdWarps * kHdRows - 1) / (kHdWarps * kHdRows)), kHdThreads, smem_r, st>>>(a);
+    attn_d_prep_kernel<ND><<<(int)((rows + kHdWarps - 1) / kHdWarps), kHdThreads, smem_r, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
-    attn_d_kernel<ND, GB><<<dim3(a.splits, a.Hkv, a.B), kHdThreads, smem_a, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
-    attn_d_combine_kernel<ND><<<(int)((rows + kHdWarps - 1) / kHdWarps), kHdThreads, smem_r, st>>>(a);
+    // the attention and combine kernels are programmatic dependents of the kernel before them: each
+    // starts its independent part (first copies; R) while its predecessor finishes
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(kHdThreads);
+    cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
+    cfg.dynamicSmemBytes = smem_a;
+    if (cudaLaunchKernelEx(&cfg, attn_d_kernel<ND, GB>, a) != cudaSuccess) return TQ_ERR_CUDA;
+    cfg.gridDim = dim3((unsigned)((rows + kHdWarps - 1) / kHdWarps));
+    cfg.dynamicSmemBytes = smem_r;
+    if (cudaLaunchKernelEx(&cfg, attn_d_combine_kernel<ND>, a) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
 }
 
