@@ -100,7 +100,7 @@ KERNEL_SOURCES = {
                   "tq_attn_mma_k2.cu", "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_g1.cu",
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
     "qjl": ["tq_qjl.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
-    "hd_encode": ["tq_headdim.cu", "tq_device.cuh"],
+    "hd_encode": ["tq_headdim.cu", "tq_headdim_tc.cu", "tq_tc.cuh", "tq_device.cuh"],
     "hd_attention": ["tq_headdim.cu", "tq_device.cuh"],
     "serialize": ["tq_encode.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "deserialize": ["tq_decode.cu", "tq_codec.cu", "tq_device.cuh"],
@@ -922,7 +922,7 @@ def plan_headdim(tq, wl, dev, stream, seed, batch):
                                                                  stream=stream), nvec * (2 * d + kbb), 1, nvec),
            Op("encode_v", "hd_encode", lambda: tq.tq_encode_kv_d(v.view(-1, d), vcb, R, vb.view(nvec, -1),
                                                                  stream=stream), nvec * (2 * d + vbb), 1, nvec),
-           Op("attention", "hd_attention", attn, nvec * (kbb + vbb) + q.numel() * 2 + out.numel() * 4, 2)]
+           Op("attention", "hd_attention", attn, nvec * (kbb + vbb) + q.numel() * 2 + out.numel() * 4, 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k).view(-1, d), _pinned(v).view(-1, d), _pinned(q)
