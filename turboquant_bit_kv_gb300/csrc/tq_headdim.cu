@@ -142,30 +142,9 @@ __device__ __forceinline__ void hd_load_R(float *Rs, const float *R) {
     }
 }
 
-// out[k] += sum_j M(lane + 32 k, j) v_j over the warp's D inputs v (element j in lane j % 32,
+// out[r][k] = sum_j M(lane + 32 k, j) v[r]_j for NR rows of D inputs v (element j in lane j % 32,
 // register j / 32): the rows of M are those of R (TRANSPOSE false: y = R v) or its columns
-// (TRANSPOSE true: y = R^T v).
-template <int ND, bool TRANSPOSE>
-__device__ __forceinline__ void hd_rotate(const float *Rs, const float (&v)[ND], float (&out)[ND], int lane) {
-    constexpr int D = 32 * ND, P = D + 1;
-#pragma unroll
-    for (int k = 0; k < ND; ++k) out[k] = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < ND; ++jj) {
-#pragma unroll 8
-        for (int src = 0; src < 32; ++src) {
-            const float vj = __shfl_sync(kHdFull, v[jj], src);
-            const int j = 32 * jj + src;
-#pragma unroll
-            for (int k = 0; k < ND; ++k) {
-                const float r = TRANSPOSE ? Rs[j * P + lane + 32 * k] : Rs[(lane + 32 * k) * P + j];
-                out[k] = fmaf(r, vj, out[k]);
-            }
-        }
-    }
-}
-
-// The same for NR rows at once: every element of R read from shared memory serves NR rows.
+// (TRANSPOSE true: y = R^T v); every element of R read from shared memory serves NR rows.
 template <int ND, bool TRANSPOSE, int NR>
 __device__ __forceinline__ void hd_rotate_rows(const float *Rs, const float (&v)[NR][ND], float (&out)[NR][ND],
                                                int lane) {
@@ -355,26 +334,66 @@ void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps) {
     *splits = (T + *tps - 1) / *tps;
 }
 
-// R q times scale log2(e) for every (sequence, query head), one per warp (the rows are few: more
-// CTAs, each with a shorter chain, finish sooner).
+// R q times scale log2(e) for every (sequence, query head): a small tiled product, one CTA per
+// 32 rows x 32 outputs (R's 32 output rows and the 32 query rows staged in shared memory, rows padded
+// to D + 1 floats); thread (tx, ty) forms outputs 32 c + tx of rows ty + 8 m, m < 4.
+constexpr int kHdTile = 32;
+
 template <int ND>
 __global__ void __launch_bounds__(kHdThreads) attn_d_prep_kernel(const __grid_constant__ HdAttnArgs a) {
-    constexpr int D = 32 * ND;
+    constexpr int D = 32 * ND, P = D + 1;
     // the attention kernel may start now: its first copies do not depend on this grid
     asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(16) float hd_smem[];
-    float *Rs = hd_smem;
-    hd_load_R<D>(Rs, a.R);
+    float *Rs = hd_smem;                  // [32 outputs][P]
+    float *Qs = Rs + kHdTile * P;         // [32 rows][P]
+    const int c0 = blockIdx.x * kHdTile;
+    const int64_t rows = (int64_t)a.B * a.Hq, r0 = (int64_t)blockIdx.y * kHdTile;
+    // R's 32 output rows: 16-byte loads, all of a thread's issued before its stores
+    constexpr int N4 = kHdTile * D / 4;
+    constexpr int U = (N4 + kHdThreads - 1) / kHdThreads;
+    float4 rv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int q = threadIdx.x + u * kHdThreads;
+        if (q < N4) rv[u] = __ldg(reinterpret_cast<const float4 *>(a.R + (int64_t)c0 * D) + q);
+    }
+    float qv[(kHdTile * D + kHdThreads - 1) / kHdThreads];
+#pragma unroll
+    for (int u = 0; u < (kHdTile * D + kHdThreads - 1) / kHdThreads; ++u) {
+        const int i = threadIdx.x + u * kHdThreads, r = i / D;
+        qv[u] = (i < kHdTile * D && r0 + r < rows) ? hd_load(a.q, a.q_dtype, r0 * D + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int q = threadIdx.x + u * kHdThreads;
+        if (q < N4) {
+            float *d = Rs + (4 * q / D) * P + (4 * q) % D;
+            d[0] = rv[u].x;
+            d[1] = rv[u].y;
+            d[2] = rv[u].z;
+            d[3] = rv[u].w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < (kHdTile * D + kHdThreads - 1) / kHdThreads; ++u) {
+        const int i = threadIdx.x + u * kHdThreads;
+        if (i < kHdTile * D) Qs[(i / D) * P + i % D] = qv[u];
+    }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * kHdWarps + warp;
-    if (row >= (int64_t)a.B * a.Hq) return;
-    float x[ND], y[ND];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) {
+        const float r = Rs[tx * P + i];
 #pragma unroll
-    for (int k = 0; k < ND; ++k) x[k] = hd_load(a.q, a.q_dtype, row * D + lane + 32 * k);
-    hd_rotate<ND, false>(Rs, x, y, lane);
+        for (int m = 0; m < 4; ++m) y[m] = fmaf(r, Qs[(ty + 8 * m) * P + i], y[m]);
+    }
 #pragma unroll
-    for (int k = 0; k < ND; ++k) a.qrot[row * D + lane + 32 * k] = y[k] * a.qscale;
+    for (int m = 0; m < 4; ++m) {
+        const int64_t row = r0 + ty + 8 * m;
+        if (row < rows) a.qrot[row * D + c0 + tx] = y[m] * a.qscale;
+    }
 }
 
 // s[h] += q[h][j] c: the query of head h at dim j times the centroid (qj: dim j's GB heads), two
@@ -620,55 +639,101 @@ __global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(con
     }
 }
 
-// One warp per (sequence, query head): merge the splits, o = R^T (acc / l).
+// The merged, normalised value sums of one (sequence, query head) row, lanes over dims
+// lane + 32 k: up to eight splits at a time, all their loads issued before any is used, folded
+// into a running maximum.
 template <int ND>
-__global__ void __launch_bounds__(kHdThreads) attn_d_combine_kernel(const __grid_constant__ HdAttnArgs a) {
+__device__ __forceinline__ void hd_merge_row(const HdAttnArgs &a, int64_t row, int lane, float (&o)[ND]) {
     constexpr int D = 32 * ND;
-    extern __shared__ __align__(16) float hd_smem[];
-    float *Rs = hd_smem;
-    hd_load_R<D>(Rs, a.R);
-    __syncthreads();
-    // the partials come from the attention kernel this one depends on
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * kHdWarps + warp;   // b * Hq + head
-    if (row >= (int64_t)a.B * a.Hq) return;
     const float *src = a.ws + row * a.splits * (2 + D);
-    // the splits' maxima, one split per lane (the loads issued together), then the warp's maximum
-    float M = -INFINITY;
-    for (int s = lane; s < a.splits; s += 32) M = fmaxf(M, src[s * (2 + D)]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kHdFull, M, o));
-    float lp = 0.f, o[ND], x[ND];
+    float M = -INFINITY, L = 0.f;
 #pragma unroll
     for (int k = 0; k < ND; ++k) o[k] = 0.f;
-    if (M != -INFINITY) {
-        for (int s0 = 0; s0 < a.splits; s0 += 32) {
-            // split s0 + lane's weight, then its sums broadcast split by split (loads independent
-            // of the weights, so several are in flight)
-            float f = 0.f;
-            if (s0 + lane < a.splits) {
-                const float *ps = src + (s0 + lane) * (2 + D);
-                f = ps[0] == -INFINITY ? 0.f : exp2f(ps[0] - M);
-                lp = fmaf(ps[1], f, lp);
-            }
-            const int ns = min(32, a.splits - s0);
-#pragma unroll 4
-            for (int t = 0; t < ns; ++t) {
-                const float ft = __shfl_sync(kHdFull, f, t);
-                const float *ps = src + (s0 + t) * (2 + D) + 2;
+    for (int s0 = 0; s0 < a.splits; s0 += 8) {
+        const int ns = min(8, a.splits - s0);
+        float ms[8], ls[8], av[8][ND];
 #pragma unroll
-                for (int k = 0; k < ND; ++k) o[k] = fmaf(ps[lane + 32 * k], ft, o[k]);
+        for (int t = 0; t < 8; ++t) {
+            ms[t] = -INFINITY;
+            ls[t] = 0.f;
+#pragma unroll
+            for (int k = 0; k < ND; ++k) av[t][k] = 0.f;
+            if (t < ns) {
+                const float *ps = src + (s0 + t) * (2 + D);
+                ms[t] = ps[0];
+                ls[t] = ps[1];
+#pragma unroll
+                for (int k = 0; k < ND; ++k) av[t][k] = ps[2 + lane + 32 * k];
             }
         }
+        float mn = M;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mn = fmaxf(mn, ms[t]);
+        if (mn == -INFINITY) continue;   // no tokens so far
+        const float cr = exp2f(M - mn);  // 0 while M is -inf
+        L *= cr;
+#pragma unroll
+        for (int k = 0; k < ND; ++k) o[k] *= cr;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float f = ms[t] == -INFINITY ? 0.f : exp2f(ms[t] - mn);
+            L = fmaf(ls[t], f, L);
+#pragma unroll
+            for (int k = 0; k < ND; ++k) o[k] = fmaf(av[t][k], f, o[k]);
+        }
+        M = mn;
     }
-    const float lt = hd_warp_sum(lp);
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;   // an empty sequence gives a zero row
+    const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty sequence gives a zero row
 #pragma unroll
     for (int k = 0; k < ND; ++k) o[k] *= inv;
-    hd_rotate<ND, true>(Rs, o, x, lane);
+}
+
+// Merge the splits and rotate back, x = R^T (acc / l): one CTA per 16 rows x 32 outputs.  Warp w
+// merges rows w and w + 8 into shared memory; R's 32 output columns are staged beside them (before
+// the wait: R does not depend on the attention kernel); thread (tx, ty) forms outputs 32 c + tx of
+// rows ty and ty + 8.
+constexpr int kHdCRows = 16;
+
+template <int ND>
+__global__ void __launch_bounds__(kHdThreads) attn_d_combine_kernel(const __grid_constant__ HdAttnArgs a) {
+    constexpr int D = 32 * ND, P = D + 1;
+    extern __shared__ __align__(16) float hd_smem[];
+    float *Os = hd_smem;                  // [16 rows][P]: merged, normalised value sums
+    float *Rc = Os + kHdCRows * P;        // [D][33]: R[j][32 c + t]
+    const int c0 = blockIdx.x * kHdTile;
+    const int64_t rows = (int64_t)a.B * a.Hq, r0 = (int64_t)blockIdx.y * kHdCRows;
+    for (int i = threadIdx.x; i < D * kHdTile; i += blockDim.x) {
+        const int j = i / kHdTile, t = i % kHdTile;
+        Rc[j * (kHdTile + 1) + t] = a.R[(int64_t)j * D + c0 + t];
+    }
+    // the partials come from the attention kernel this one depends on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int k = 0; k < ND; ++k) a.out[row * D + lane + 32 * k] = x[k];
+    for (int m = 0; m < kHdCRows / kHdWarps; ++m) {
+        const int rr = warp + kHdWarps * m;
+        float o[ND];
+        if (r0 + rr < rows) hd_merge_row<ND>(a, r0 + rr, lane, o);
+        else
+#pragma unroll
+            for (int k = 0; k < ND; ++k) o[k] = 0.f;
+#pragma unroll
+        for (int k = 0; k < ND; ++k) Os[rr * P + lane + 32 * k] = o[k];
+    }
+    __syncthreads();
+    const int tx = lane, ty = warp;
+    float x[kHdCRows / kHdWarps] = {};
+#pragma unroll 8
+    for (int j = 0; j < D; ++j) {
+        const float r = Rc[j * (kHdTile + 1) + tx];
+#pragma unroll
+        for (int m = 0; m < kHdCRows / kHdWarps; ++m) x[m] = fmaf(r, Os[(ty + kHdWarps * m) * P + j], x[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < kHdCRows / kHdWarps; ++m) {
+        const int64_t row = r0 + ty + kHdWarps * m;
+        if (row < rows) a.out[row * D + c0 + tx] = x[m];
+    }
 }
 
 template <int ND, int GB>
@@ -680,17 +745,18 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     const int stages = kHdWarps * 2 * 32 * (KB + VB), part = kHdWarps * GB * (2 + D) * 4;
     // (16 bytes past the stages: a lane's value-code window may read a word beyond the last block)
     const int smem_a = (D * GB + 32 + kHdWarps * 32 * GB) * 4 + (stages > part ? stages : part) + 16;
-    const int smem_r = D * (D + 1) * 4;
-    if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_r, done_p) != TQ_OK) return TQ_ERR_CUDA;
+    const int smem_p = 2 * kHdTile * (D + 1) * 4, smem_c = (kHdCRows * (D + 1) + D * (kHdTile + 1)) * 4;
+    if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_p, done_p) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_kernel<ND, GB>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
-    if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_r, done_c) != TQ_OK) return TQ_ERR_CUDA;
+    if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_c, done_c) != TQ_OK) return TQ_ERR_CUDA;
     int &per_sm = resident[a.kbits][a.vbits];
     if (per_sm <= 0 &&
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_d_kernel<ND, GB>, kHdThreads, smem_a) != cudaSuccess)
         return TQ_ERR_CUDA;
     hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), &a.splits, &a.tps);
     const int64_t rows = (int64_t)a.B * a.Hq;
-    attn_d_prep_kernel<ND><<<(int)((rows + kHdWarps - 1) / kHdWarps), kHdThreads, smem_r, st>>>(a);
+    const dim3 tiles(D / kHdTile, (unsigned)((rows + kHdTile - 1) / kHdTile));
+    attn_d_prep_kernel<ND><<<tiles, kHdThreads, smem_p, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     // the attention and combine kernels are programmatic dependents of the kernel before them: each
     // starts its independent part (first copies; R) while its predecessor finishes
@@ -705,8 +771,8 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
     cfg.dynamicSmemBytes = smem_a;
     if (cudaLaunchKernelEx(&cfg, attn_d_kernel<ND, GB>, a) != cudaSuccess) return TQ_ERR_CUDA;
-    cfg.gridDim = dim3((unsigned)((rows + kHdWarps - 1) / kHdWarps));
-    cfg.dynamicSmemBytes = smem_r;
+    cfg.gridDim = dim3(D / kHdTile, (unsigned)((rows + kHdCRows - 1) / kHdCRows));
+    cfg.dynamicSmemBytes = smem_c;
     if (cudaLaunchKernelEx(&cfg, attn_d_combine_kernel<ND>, a) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
 }
