@@ -35,13 +35,12 @@
 #include <cstring>
 
 #include "tq_device.cuh"
+#include "tq_headdim.cuh"
 #include "tq_internal.h"
 
 namespace tq {
 namespace {
 
-constexpr int kHdThreads = 256;     // 8 warps
-constexpr int kHdWarps = kHdThreads / 32;
 constexpr unsigned kHdFull = 0xffffffffu;
 
 bool hd_dim_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 160; }
@@ -291,18 +290,7 @@ int hd_codec(const HdArgs &a, int d, bool encode, cudaStream_t st) {
 
 // ---------------------------------------------------------------- decode attention
 
-struct HdAttnArgs {
-    const void *q;
-    const uint8_t *k, *v;
-    const int32_t *seq_lens;
-    const float *R;
-    float *ws;               // partials [B][Hq][splits][2 + d]: m (log2 units), l, acc[d]
-    float *qrot;             // rotated, scaled queries [B][Hq][d] (after the partials)
-    float *out;
-    int q_dtype, B, Hq, Hkv, G, T_cap, T, kbits, vbits, splits, tps;
-    float qscale;            // scale * log2(e)
-    float kc[16], vc[16];
-};
+}  // namespace
 
 // Context splits of a (sequence, KV head).  A split is a whole number of 32-token chunks, at least
 // kHdMinChunks of them (two warp steps per warp), so the most splits a context of T tokens takes is
@@ -333,6 +321,8 @@ void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps) {
     *tps = (C + best - 1) / best * 32;
     *splits = (T + *tps - 1) / *tps;
 }
+
+namespace {
 
 // R q times scale log2(e) for every (sequence, query head): a small tiled product, one CTA per
 // 32 rows x 32 outputs (R's 32 output rows and the 32 query rows staged in shared memory, rows padded
@@ -747,13 +737,19 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     const int smem_a = (D * GB + 32 + kHdWarps * 32 * GB) * 4 + (stages > part ? stages : part) + 16;
     const int smem_p = 2 * kHdTile * (D + 1) * 4, smem_c = (kHdCRows * (D + 1) + D * (kHdTile + 1)) * 4;
     if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_p, done_p) != TQ_OK) return TQ_ERR_CUDA;
-    if (set_smem_limit((const void *)attn_d_kernel<ND, GB>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_c, done_c) != TQ_OK) return TQ_ERR_CUDA;
-    int &per_sm = resident[a.kbits][a.vbits];
-    if (per_sm <= 0 &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_d_kernel<ND, GB>, kHdThreads, smem_a) != cudaSuccess)
-        return TQ_ERR_CUDA;
-    hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), &a.splits, &a.tps);
+    // up to four heads per KV head and 2- or 4-bit values: the tensor-core kernel (tq_headdim_mma.cu);
+    // otherwise the CUDA-core kernel above
+    const int mma = hd_attn_mma_plan(a, D);
+    if (mma != 1 && mma != TQ_OK) return mma;
+    if (mma == 1) {
+        if (set_smem_limit((const void *)attn_d_kernel<ND, GB>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
+        int &per_sm = resident[a.kbits][a.vbits];
+        if (per_sm <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_d_kernel<ND, GB>, kHdThreads,
+                                                                         smem_a) != cudaSuccess)
+            return TQ_ERR_CUDA;
+        hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), &a.splits, &a.tps);
+    }
     const int64_t rows = (int64_t)a.B * a.Hq;
     const dim3 tiles(D / kHdTile, (unsigned)((rows + kHdTile - 1) / kHdTile));
     attn_d_prep_kernel<ND><<<tiles, kHdThreads, smem_p, st>>>(a);
@@ -768,9 +764,14 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(kHdThreads);
-    cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
-    cfg.dynamicSmemBytes = smem_a;
-    if (cudaLaunchKernelEx(&cfg, attn_d_kernel<ND, GB>, a) != cudaSuccess) return TQ_ERR_CUDA;
+    if (mma == TQ_OK) {
+        const int r = hd_attn_mma_launch(a, D, st);
+        if (r != TQ_OK) return r;
+    } else {
+        cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
+        cfg.dynamicSmemBytes = smem_a;
+        if (cudaLaunchKernelEx(&cfg, attn_d_kernel<ND, GB>, a) != cudaSuccess) return TQ_ERR_CUDA;
+    }
     cfg.gridDim = dim3(D / kHdTile, (unsigned)((rows + kHdCRows - 1) / kHdCRows));
     cfg.dynamicSmemBytes = smem_c;
     if (cudaLaunchKernelEx(&cfg, attn_d_combine_kernel<ND>, a) != cudaSuccess) return TQ_ERR_CUDA;
