@@ -302,9 +302,9 @@ int hd_max_splits(int T) {
     return s < 1 ? 1 : s;
 }
 
-// Of those split counts, the one with the shortest makespan for `slots` CTAs resident at once:
-// waves of CTAs times warp steps per CTA (plus one for the CTA's start and merge).
-void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps) {
+// Of those split counts, the one with the shortest makespan for `slots` CTAs of `warps` warps
+// resident at once: waves of CTAs times warp steps per CTA (plus one for the CTA's start and merge).
+void hd_split_plan(int B, int Hkv, int T, int slots, int warps, int *splits, int *tps) {
     const int64_t segs = (int64_t)B * Hkv;
     const int C = (T + 31) / 32, smax = hd_max_splits(T);
     if (slots < 1) slots = 1;
@@ -312,7 +312,7 @@ void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps) {
     int64_t best_cost = -1;
     for (int s = 1; s <= smax; ++s) {
         const int64_t waves = (segs * s + slots - 1) / slots;
-        const int64_t steps = ((C + s - 1) / s + kHdWarps - 1) / kHdWarps + 1;
+        const int64_t steps = ((C + s - 1) / s + warps - 1) / warps + 1;
         if (best_cost < 0 || waves * steps < best_cost) {
             best_cost = waves * steps;
             best = s;
@@ -748,7 +748,7 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
         if (per_sm <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_d_kernel<ND, GB>, kHdThreads,
                                                                          smem_a) != cudaSuccess)
             return TQ_ERR_CUDA;
-        hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), &a.splits, &a.tps);
+        hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), kHdWarps, &a.splits, &a.tps);
     }
     const int64_t rows = (int64_t)a.B * a.Hq;
     const dim3 tiles(D / kHdTile, (unsigned)((rows + kHdTile - 1) / kHdTile));

@@ -26,9 +26,10 @@ struct HdAttnArgs {
     float kc[16], vc[16];
 };
 
-// Most context splits of T tokens, and the split plan for `slots` CTAs resident at once.
+// Most context splits of T tokens, and the split plan for `slots` CTAs of `warps` warps resident
+// at once.
 int hd_max_splits(int T);
-void hd_split_plan(int B, int Hkv, int T, int slots, int *splits, int *tps);
+void hd_split_plan(int B, int Hkv, int T, int slots, int warps, int *splits, int *tps);
 
 // The tensor-core attention kernel (tq_headdim_mma.cu), G <= 4 and 2- or 4-bit values:
 // hd_attn_mma_plan returns 1 when it does not cover the call, else sets a.splits / a.tps from the

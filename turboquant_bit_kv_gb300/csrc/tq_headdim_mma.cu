@@ -8,8 +8,8 @@
 // call's query prep and combine (R q, and the merge of the splits with R^T)
 // are those of tq_headdim.cu; this unit holds the attention kernel only.
 //
-// One CTA of 8 warps per (sequence, KV head, context split); a warp takes
-// 32-token chunks t0 + 32 (warp + 8 i), staged in shared memory by
+// One CTA of 4 warps per (sequence, KV head, context split); a warp takes
+// 32-token chunks t0 + 32 (warp + 4 i), staged in shared memory by
 // double-buffered 16-byte cp.async copies.
 //   * Scores: S[32 tokens x 8] = K Q^T over the d dims as d / 16 k-steps.
 //     The contraction order is free as long as both operands follow it:
@@ -42,6 +42,8 @@ namespace tq {
 namespace {
 
 constexpr unsigned kHmFull = 0xffffffffu;
+constexpr int kHmWarps = 4;   // per CTA: small CTAs fill the SMs' slots in whole waves
+constexpr int kHmThreads = 32 * kHmWarps;
 constexpr int kHmPsRow = 68;   // bytes per column of the probability tile (32 fp16 + padding)
 
 template <int ND, int KB, int VB>
@@ -53,8 +55,8 @@ struct HmCfg {
     static constexpr int kVT = kKT + NK * 128;                     // [NV][32] words
     static constexpr int kPs = kVT + NV * 128;                     // [warp][8 columns][kHmPsRow]
     static constexpr int kStage = 32 * (KBB + VBB);                // one chunk's K then V blocks
-    static constexpr int kSt = kPs + kHdWarps * 8 * kHmPsRow;      // [warp][2][kStage], then the merge
-    static constexpr int kStages = kHdWarps * 2 * kStage, kPart = kHdWarps * 4 * (2 + D) * 4;
+    static constexpr int kSt = kPs + kHmWarps * 8 * kHmPsRow;      // [warp][2][kStage], then the merge
+    static constexpr int kStages = kHmWarps * 2 * kStage, kPart = kHmWarps * 4 * (2 + D) * 4;
     static constexpr int kTotal = kSt + (kStages > kPart ? kStages : kPart);
     static_assert(kSt % 16 == 0 && kStage % 16 == 0, "16-byte aligned stages");
 };
@@ -178,7 +180,7 @@ __device__ __forceinline__ void hm_value_slice(const uint8_t *blk, int g, uint64
 }
 
 template <int ND, int KB, int VB>
-__global__ void __launch_bounds__(kHdThreads, 2) attn_dm_kernel(const __grid_constant__ HdAttnArgs a) {
+__global__ void __launch_bounds__(kHmThreads, 3) attn_dm_kernel(const __grid_constant__ HdAttnArgs a) {
     using C = HmCfg<ND, KB, VB>;
     constexpr int D = C::D, KBB = C::KBB, VBB = C::VBB, NKS = D / 16;
     extern __shared__ __align__(16) uint8_t hm_smem[];
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kHdThreads, 2) attn_dm_kernel(const __grid_con
     // ---- pair tables: keys (hi, lo) words, 16 copies; values one word, 32 copies
     {
         uint2 *kt = reinterpret_cast<uint2 *>(hm_smem + C::kKT);
-        for (int i = threadIdx.x; i < C::NK * 16; i += kHdThreads) {
+        for (int i = threadIdx.x; i < C::NK * 16; i += kHmThreads) {
             int c0, c1;
             hm_key_pair<KB>(i >> 4, c0, c1);
             float h0, l0, h1, l1;
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kHdThreads, 2) attn_dm_kernel(const __grid_con
             kt[i] = make_uint2(hm_h2(h0, h1), hm_h2(l0, l1));
         }
         uint32_t *vt = reinterpret_cast<uint32_t *>(hm_smem + C::kVT);
-        for (int i = threadIdx.x; i < C::NV * 32; i += kHdThreads) {
+        for (int i = threadIdx.x; i < C::NV * 32; i += kHmThreads) {
             const int e = i >> 5;
             vt[i] = hm_h2(a.vc[e & ((1 << VB) - 1)], a.vc[e >> VB]);
         }
@@ -264,8 +266,8 @@ __global__ void __launch_bounds__(kHdThreads, 2) attn_dm_kernel(const __grid_con
     for (int mt = 0; mt < NKS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     int buf = 0;
-    for (; base < t1; base += 32 * kHdWarps) {
-        const int nb = base + 32 * kHdWarps;
+    for (; base < t1; base += 32 * kHmWarps) {
+        const int nb = base + 32 * kHmWarps;
         if (nb < t1) issue(nb, buf ^ 1);
         else cp_async_commit();   // (an empty group: the wait below always leaves one group)
         cp_async_wait<1>();
@@ -405,12 +407,12 @@ __global__ void __launch_bounds__(kHdThreads, 2) attn_dm_kernel(const __grid_con
     if (warp < a.G) {
         const int h = warp;
         float M = -INFINITY;
-        for (int w = 0; w < kHdWarps; ++w) M = fmaxf(M, part[(w * 4 + h) * (2 + D)]);
+        for (int w = 0; w < kHmWarps; ++w) M = fmaxf(M, part[(w * 4 + h) * (2 + D)]);
         float lt = 0.f, acc[ND];
 #pragma unroll
         for (int k = 0; k < ND; ++k) acc[k] = 0.f;
         if (M != -INFINITY) {
-            for (int w = 0; w < kHdWarps; ++w) {
+            for (int w = 0; w < kHmWarps; ++w) {
                 const float *pp = part + (w * 4 + h) * (2 + D);
                 const float f = pp[0] == -INFINITY ? 0.f : exp2f(pp[0] - M);
                 lt = fmaf(pp[1], f, lt);
@@ -462,9 +464,9 @@ int hd_attn_mma_plan(HdAttnArgs &a, int d) {
     if (!k.fn) return 1;
     if (set_smem_limit(k.fn, k.smem, k.done) != TQ_OK) return TQ_ERR_CUDA;
     if (*k.resident <= 0 &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(k.resident, k.fn, kHdThreads, k.smem) != cudaSuccess)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(k.resident, k.fn, kHmThreads, k.smem) != cudaSuccess)
         return TQ_ERR_CUDA;
-    hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (*k.resident > 0 ? *k.resident : 1), &a.splits, &a.tps);
+    hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (*k.resident > 0 ? *k.resident : 1), kHmWarps, &a.splits, &a.tps);
     return TQ_OK;
 }
 
@@ -479,7 +481,7 @@ int hd_attn_mma_launch(const HdAttnArgs &a, int d, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(kHdThreads);
+    cfg.blockDim = dim3(kHmThreads);
     cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
     cfg.dynamicSmemBytes = smem;
     void *args[] = {const_cast<HdAttnArgs *>(&a)};

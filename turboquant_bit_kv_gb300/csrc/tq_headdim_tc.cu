@@ -62,8 +62,9 @@ struct HtSmem {
     static constexpr int kPart = (kOut + kHtRows * BB + 15) / 16 * 16;   // [4 column groups][128] partial sums
     static constexpr int kFix = kPart + 4 * kHtRows * 4;       // [0] count, [1] overflow, [4 ..] rows
     static constexpr int kTab = kFix + (4 + kHtFixCap) * 4;
-    static constexpr int kBars = kTab + kHtBuckets * 8;        // full[2] at 0, mma[2] at 16, empty[2] at 32, drain 48
-    static constexpr int kSlot = kBars + 56;
+    // full[2] at 0, mma[2] at 16, row tile free[2] at 32, drain at 48, accumulator free[2] at 56
+    static constexpr int kBars = kTab + kHtBuckets * 8;
+    static constexpr int kSlot = kBars + 72;
     static constexpr int kUsed = kSlot + 8;
     // at least 116 KB, so one CTA per SM: each holds a tensor-memory allocation of its own
     static constexpr int kTotal = kUsed + 1024 > 118784 ? kUsed + 1024 : 118784;
@@ -221,7 +222,8 @@ __global__ void __launch_bounds__(kHtThreads, 1)
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(bars + 8 * i, 1);                  // full: the producer's arrival + the TMA bytes
             tc_mbar_init(bars + 16 + 8 * i, 1);             // mma: tcgen05.commit
-            tc_mbar_init(bars + 32 + 8 * i, kHtEpiWarps);   // empty: one arrival per epilogue warp
+            tc_mbar_init(bars + 32 + 8 * i, kHtEpiWarps);   // row tile free: each epilogue warp, after the norms
+            tc_mbar_init(bars + 56 + 8 * i, kHtEpiWarps);   // accumulator free: each epilogue warp, after its loads
         }
         tc_mbar_init(bars + 48, 1);                         // drain: the producer's last commit
         reinterpret_cast<int *>(smem + S::kFix)[0] = 0;     // listed rows
@@ -260,9 +262,8 @@ __global__ void __launch_bounds__(kHtThreads, 1)
             for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
                 const int st = i & 1;
                 const uint32_t use = (uint32_t)(i >> 1);
-                if (i >= 2) wait(bars + 32 + 8 * st, (use - 1u) & 1u);   // stage released by the epilogue
+                if (i >= 2) wait(bars + 32 + 8 * st, (use - 1u) & 1u);   // row tile read by the epilogue
                 if (!ok) break;
-                tc_fence_after();
                 const uint32_t a_s = base_s + S::kA + st * S::kStage, full = bars + 8 * st;
                 if (!a.drop) {   // (test hook: no load, so the wait below runs out)
                     tc_mbar_expect_tx(full, S::kStage);
@@ -274,6 +275,9 @@ __global__ void __launch_bounds__(kHtThreads, 1)
                 wait(full, use & 1u);
                 if (!ok) break;   // no product on a tile that did not land
                 pend = -1;
+                if (i >= 2) wait(bars + 56 + 8 * st, (use - 1u) & 1u);   // accumulator read by the epilogue
+                if (!ok) break;
+                tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(st * S::kTS);
                 const uint32_t b_s = base_s + S::kB;
 #pragma unroll
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kHtThreads, 1)
         uint8_t *sm_out = smem + S::kOut;
         const uint32_t tab_s = base_s + S::kTab;
         const bool bulk_out = ((uintptr_t)a.blocks & 15u) == 0;
-        const float off = 1572928.f;   // 64 + 1.5 * 2^20: z + 64 rounded to 1/8, the cell in bits 3..9
+        const float2 off2 = make_float2(1572928.f, 1572928.f);   // 64 + 1.5 * 2^20: z + 64 to 1/8, the cell in bits 3..9
         bool ok = true;
         int i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
@@ -353,6 +357,9 @@ __global__ void __launch_bounds__(kHtThreads, 1)
                 n16 = __half_as_ushort(__double2half(nd));
                 inv = sd > 0.0 ? (float)(1.0 / nd) : 0.f;   // a zero row: y = 0, code L/2
             }
+            // the row tile is read: the next load may take its place while this tile is quantised
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(bars + 32 + 8 * st);
             // within 2^-20 of an fp16 rounding boundary: listed; the norm is rewritten after the loop
             if (cg == 0) {
                 const bool need = r < nv && !oor && near_fp16_tie_fast(nrm);
@@ -370,8 +377,13 @@ __global__ void __launch_bounds__(kHtThreads, 1)
                 }
             }
             ht_wait_ld(u);
+            // the accumulator is in registers: the next products may take its place
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(bars + 56 + 8 * st);
             // ---- quantise and pack: code = #{boundaries <= y} from the cell of G y and one comparison
             const float cs = a.grid * inv;
+            const float2 cs2 = make_float2(cs, cs);
             uint8_t *blk = sm_out + r * BB;
             if (cg == 0) *reinterpret_cast<uint16_t *>(blk) = (uint16_t)n16;
             constexpr int B = BITS == 2 ? 2 : 4;   // accumulation width of a code (3-bit: nibbles)
@@ -379,11 +391,15 @@ __global__ void __launch_bounds__(kHtThreads, 1)
             for (int g = 0; g < CW / 8; ++g) {
                 uint32_t w = 0;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float y = u[8 * g + e] * cs;
-                    const float2 cell = ht_lds_f2(tab_s + (__float_as_uint(y + off) & 0x3F8u));
-                    w += __float_as_uint(cell.y) << (B * e);
-                    w -= ht_set_ge(y, cell.x) << (B * e);
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 y = __fmul2_rn(make_float2(u[8 * g + e], u[8 * g + e + 1]), cs2);
+                    const float2 t = __fadd2_rn(y, off2);
+                    const float2 c0 = ht_lds_f2(tab_s + (__float_as_uint(t.x) & 0x3F8u));
+                    const float2 c1 = ht_lds_f2(tab_s + (__float_as_uint(t.y) & 0x3F8u));
+                    w += __float_as_uint(c0.y) << (B * e);
+                    w -= ht_set_ge(y.x, c0.x) << (B * e);
+                    w += __float_as_uint(c1.y) << (B * e + B);
+                    w -= ht_set_ge(y.y, c1.x) << (B * e + B);
                 }
                 const int j0 = cg * CW + 8 * g;   // first column of the 8
                 if constexpr (BITS == 4) {
@@ -409,10 +425,7 @@ __global__ void __launch_bounds__(kHtThreads, 1)
             if (bulk_out) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // blocks -> bulk copy
             asm volatile("bar.sync %0, 128;" ::"r"(qbar) : "memory");   // the quarter's 32 blocks are written
 
-            // ---- release the stage (accumulator and row tile), then store the quarter's 32 blocks
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc_mbar_arrive(bars + 32 + 8 * st);
+            // ---- store the quarter's 32 blocks
             uint8_t *dst = a.blocks + (v0 + 32 * grp) * BB;
             const uint8_t *src = sm_out + 32 * grp * BB;
             if (bulk_out && rows == 32) {
