@@ -17,6 +17,10 @@
 // element 8g + p in bits 3p .. 3p + 2; a turboq8 block is [fp16 scale][128
 // code bytes].
 //
+// bf16 / fp16 rows (1024 or more, blocks back to back) go to the tensor-core
+// encode of tq_headdim_tc.cu (the rotation H D as one exact contraction);
+// the kernels here take the rest.
+//
 // Kernels: two threads per row, each holding 64 of its elements in registers
 // (six butterfly stages of the 128-point transform in registers, the seventh
 // across the pair); a warp takes 16 rows at a time and stages and stores its
@@ -564,6 +568,11 @@ extern "C" int tq_encode_kv_ex(const void *x, int x_dtype, int64_t n_vec, int64_
     ext_tables(cb, &a);
     for (int i = 0; i < 4; ++i) a.signs[i] = signs.w[i];
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // bf16 / fp16 rows into blocks back to back: the tensor-core encode (1: not its form)
+    if (!dst_index && block_stride_bytes == bb) {
+        const int t = ext_encode_tc(x, x_dtype, n_vec, a.x_stride, cb, signs.w, a.nc, a.dense, blocks, st);
+        if (t != 1) return t;
+    }
     switch (cb->bits) {
         case 2: return encode_ext_bits<2>(a, x_dtype, st);
         case 3: return encode_ext_bits<3>(a, x_dtype, st);

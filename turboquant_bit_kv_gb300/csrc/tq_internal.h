@@ -64,6 +64,13 @@ constexpr int64_t kHdTcMinRows = 1024;
 int hd_encode_tc(const void *x, int x_dtype, int64_t n_vec, int d, const tq_codebook *cb, const float *R,
                  uint8_t *blocks, cudaStream_t st);
 
+// The further formats at d = 128 on the same tensor-core encode (tq_headdim_tc.cu), rotation H D:
+// norm-corrected and dense 3-bit blocks of a 2/3/4-bit codebook, or turboq8 (bits 8); bf16 / fp16
+// rows, at least kHdTcMinRows of them, blocks back to back.  Returns 1 when it does not handle the
+// call (then nothing was enqueued), else a TQ_ status.
+int ext_encode_tc(const void *x, int x_dtype, int64_t n_vec, int64_t x_stride_bytes, const tq_codebook *cb,
+                  const uint32_t *signs, int nc, int dense, uint8_t *blocks, cudaStream_t st);
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
