@@ -89,7 +89,7 @@ CSRC = os.path.join(ROOT, "turboquant_bit_kv_gb300", "csrc")
 # reported while these are unchanged since the capture)
 KERNEL_SOURCES = {
     "encode": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
-    "ext_encode": ["tq_ext.cu", "tq_device.cuh"],
+    "ext_encode": ["tq_ext.cu", "tq_headdim_tc.cu", "tq_tc.cuh", "tq_device.cuh"],
     "append": ["tq_encode.cu", "tq_tc.cuh", "tq_device.cuh"],
     "prefill": ["tq_attn_prefill.cu", "tq_tc.cuh", "tq_device.cuh"],
     "pair_attention": ["tq_attn.cu", "tq_attn.cuh", "tq_attn_mma.cu", "tq_attn_mma.h", "tq_attn_mma.cuh",
