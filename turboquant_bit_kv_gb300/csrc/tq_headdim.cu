@@ -12,9 +12,14 @@
 // byte, 3-bit a 2-bit low plane of d / 4 bytes then a 1-bit high plane of
 // d / 8 bytes.
 //
-// Kernels (CUDA cores, float32; d = 32 ND): a warp per row, lane l holds
-// elements l + 32 k.  R sits in shared memory with rows padded to d + 1
-// floats, so that the 32 lanes reading one column (encode: outputs
+// This unit holds the CUDA-core kernels and the C ABI; bf16 / fp16 encodes of
+// 1024 rows or more run on the tensor cores (tq_headdim_tc.cu), and so does
+// the attention for up to four heads per KV head with 2- or 4-bit values
+// (tq_headdim_mma.cu).
+//
+// Codec kernels (CUDA cores, float32; d = 32 ND): a warp per row, lane l
+// holds elements l + 32 k.  R sits in shared memory with rows padded to
+// d + 1 floats, so that the 32 lanes reading one column (encode: outputs
 // l + 32 k, input j) hit 32 different banks.  The rotation of a row is d
 // shuffles of its inputs and d ND fused multiply-adds per lane.  Codes are
 // the count of float32 boundaries <= y; norms are rounded once to fp16 and
@@ -22,14 +27,16 @@
 // an fp16 rounding boundary.  The codec kernels rotate four rows per warp at
 // once, so every element of R read from shared memory serves four rows.
 // Decode attention: a prep kernel rotates every query once (R q, scale
-// log2(e) folded in); one CTA of 8 warps per (sequence, KV head, context
-// split) then takes 32 tokens per warp step, each step's K and V blocks
-// staged in shared memory by asynchronous copies while the previous step
-// computes: lane t scores its token against n_t c[code_t] for every head (no
-// cross-lane sums), the warp keeps an online softmax per head, and the value
-// sums run with lanes over dims; the warps merge in shared memory, and a
-// combine kernel merges the splits and rotates back (R^T).  The split count
-// is chosen from the kernel's occupancy so that the CTAs fill whole waves.
+// log2(e) folded in; a small tiled product); the attention kernel (here: one
+// CTA of 8 warps per (sequence, KV head, context split), 32 tokens per warp
+// step, each step's K and V blocks staged in shared memory by asynchronous
+// copies while the previous step computes; lane t scores its token against
+// n_t c[code_t] for every head, the warp keeps an online softmax per head,
+// and the value sums run with lanes over dims; the warps merge in shared
+// memory) writes one partial per head and split; a combine kernel merges
+// the splits and rotates back (R^T, a small tiled product).  The three are
+// chained as programmatic dependents; the split count is chosen from the
+// attention kernel's occupancy so that the CTAs fill whole waves.
 
 #include <cmath>
 #include <cstring>
