@@ -117,6 +117,28 @@ def test_dense3_encode(env, dtype, flags, n):
     _check("dense3 %d" % flags, idx_g, idx_o, dist, n_g, n_o, exact)
 
 
+@pytest.mark.parametrize("bits,flags", [(4, NC), (3, DENSE3 | NC), (8, 0)])
+def test_tensor_core_encode_strided_rows_unaligned_blocks(env, bits, flags):
+    """The tensor-core encode with rows 272 bytes apart (a strided view) into
+    a block array that starts 2 bytes past a 16-byte boundary (2-byte stores
+    instead of bulk copies): the same blocks as the contiguous, aligned call."""
+    tq, dev = env["tq"], env["dev"]
+    n = 2100
+    x = _rows(n, 17, torch.bfloat16)
+    wide = torch.zeros((n, 136), dtype=torch.bfloat16)
+    wide[:, :D] = x
+    xs = wide.to(dev)[:, :D]                      # row stride 136 elements
+    assert xs.stride(0) == 136
+    bb = tq.tq_block_bytes_ex(bits, flags)
+    ref = _encode(env, x, bits, flags)
+    out = torch.full((n * bb + 64,), 0xA5, dtype=torch.uint8, device=dev)
+    tq.tq_encode_kv_ex(xs, env["cbs"][bits], env["signs"], out[34:34 + n * bb], flags=flags)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.all(o[:34] == 0xA5) and np.all(o[34 + n * bb:] == 0xA5)
+    assert np.array_equal(o[34:34 + n * bb].reshape(n, bb), ref)
+
+
 def _decode(env, blocks, bits, flags, dtype, stride=None, offset=0):
     tq, dev = env["tq"], env["dev"]
     n, bb = blocks.shape

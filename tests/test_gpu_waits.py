@@ -64,7 +64,7 @@ def test_wait_that_runs_out_is_reported(env):
     good_out = out.cpu().numpy().copy()
 
     # each kernel with its copies dropped: it returns (no hang), and the event is recorded
-    for which in range(4):
+    for which in range(5):
         tq.tq_debug_drop_copies(True)
         try:
             if which == 0:
@@ -75,11 +75,15 @@ def test_wait_that_runs_out_is_reported(env):
             elif which == 2:
                 kb.copy_(torch.from_numpy(good))
                 tq.tq_attn_decode(q, kb, env["cbs"][4], vb, env["cbs"][2], out, ws, T, 1 / np.sqrt(D), env["signs"])
-            else:
+            elif which == 3:
                 # the tensor-core encode at another head dim (bf16 rows, more than 1024)
                 R = torch.eye(64, dtype=torch.float32, device=dev)
                 hb = torch.empty((x.numel() // 64, tq.tq_block_bytes_d(64, 4)), dtype=torch.uint8, device=dev)
                 tq.tq_encode_kv_d(x.reshape(-1, 64), tq.tq_codebook_load(64, 4), R, hb)
+            else:
+                # the same kernel's turboq8 mode (bf16 rows, more than 1024)
+                q8 = torch.empty((x.numel() // D, 130), dtype=torch.uint8, device=dev)
+                tq.tq_encode_kv_ex(x.view(-1, D), tq.tq_codebook_load(128, 8), env["signs"], q8)
         finally:
             tq.tq_debug_drop_copies(False)
         assert tq.tq_device_status(clear=True) == tq.TQ_ERR_TIMEOUT, which
