@@ -57,7 +57,7 @@ struct HmCfg {
     static constexpr int kStage = 32 * (KBB + VBB);                // one chunk's K then V blocks
     static constexpr int kSt = kPs + kHmWarps * 8 * kHmPsRow;      // [warp][2][kStage], then the merge
     static constexpr int kStages = kHmWarps * 2 * kStage, kPart = kHmWarps * 4 * (2 + D) * 4;
-    static constexpr int kTotal = kSt + (kStages > kPart ? kStages : kPart);
+    static constexpr int kTotal = kSt + (kStages > kPart ? kStages : kPart) + 16;   // (+ 16: see hm_bytes)
     static_assert(kSt % 16 == 0 && kStage % 16 == 0, "16-byte aligned stages");
 };
 
@@ -105,25 +105,19 @@ __device__ __forceinline__ void hm_key_pair(int e, int &c0, int &c1) {
     }
 }
 
-// n bytes from a 2-byte aligned shared address as little-endian 32-bit words (16-bit loads).
-template <int N>
-__device__ __forceinline__ void hm_bytes_a2(const uint8_t *p, uint32_t (&w)[(N + 3) / 4]) {
-    const uint16_t *h = reinterpret_cast<const uint16_t *>(p);
-#pragma unroll
-    for (int i = 0; i < (N + 3) / 4; ++i) {
-        const uint32_t lo = 4 * i < N ? h[2 * i] : 0u;
-        const uint32_t hi = 4 * i + 2 < N ? h[2 * i + 1] : 0u;
-        w[i] = lo | (hi << 16);
-    }
-}
-
-// n bytes from any shared address (byte loads).
+// The 4 (N + 3) / 4 bytes from any shared address p on, as little-endian 32-bit words: aligned
+// 32-bit loads from the word at or below p, joined by funnel shifts (may read up to 7 bytes past the
+// last word: the shared-memory layout leaves 16 bytes after the stages).
 template <int N>
 __device__ __forceinline__ void hm_bytes(const uint8_t *p, uint32_t (&w)[(N + 3) / 4]) {
+    constexpr int NW = (N + 3) / 4;
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    const uint32_t base = a & ~3u, sh = (a & 3u) * 8u;
+    uint32_t raw[NW + 1];
 #pragma unroll
-    for (int i = 0; i < (N + 3) / 4; ++i) w[i] = 0u;
+    for (int i = 0; i <= NW; ++i) raw[i] = hm_lds32(base + 4 * i);
 #pragma unroll
-    for (int i = 0; i < N; ++i) w[i >> 2] |= (uint32_t)p[i] << (8 * (i & 3));
+    for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
 }
 
 __device__ __forceinline__ uint32_t hm_byte(const uint32_t *w, int i) { return (w[i >> 2] >> (8 * (i & 3))) & 0xFFu; }
@@ -139,9 +133,9 @@ struct HmKeySlice {
     __device__ __forceinline__ void load(const uint8_t *blk, int t) {
         constexpr int D = 32 * ND;
         if constexpr (KB == 4) {
-            hm_bytes_a2<4 * ND>(blk + 2 + t * 4 * ND, w);
+            hm_bytes<4 * ND>(blk + 2 + t * 4 * ND, w);
         } else {
-            hm_bytes_a2<2 * ND>(blk + 2 + t * 2 * ND, w);
+            hm_bytes<2 * ND>(blk + 2 + t * 2 * ND, w);
             if constexpr (KB == 3) hm_bytes<ND>(blk + 2 + D / 4 + t * ND, h);
         }
     }
