@@ -160,17 +160,24 @@ struct HmKeySlice {
     }
 };
 
-// Value slice of one token for this lane (dims [g d/8, (g + 1) d/8)) as a bit string: 2-bit codes in
-// x[0] (d/4 = 8 ND bits <= 40), 4-bit codes in x[0..1] (16 ND bits <= 80).
+// Value slice of one token for this lane (dims [g d/8, (g + 1) d/8)) as 32-bit words: word w holds
+// slice dims 16 w .. (2-bit codes) or 8 w .. (4-bit codes).
 template <int ND, int VB>
-__device__ __forceinline__ void hm_value_slice(const uint8_t *blk, int g, uint64_t (&x)[2]) {
-    constexpr int NB = ND * VB / 2;   // bytes of the slice
-    uint32_t w[(NB + 3) / 4];
-    hm_bytes<NB>(blk + 2 + g * NB, w);
-    x[0] = (uint64_t)w[0];
-    x[1] = 0ull;
-    if constexpr (NB > 4) x[0] |= (uint64_t)w[1] << 32;
-    if constexpr (NB > 8) x[1] = (uint64_t)w[2];
+struct HmValueSlice {
+    static constexpr int NB = ND * VB / 2;   // bytes of the slice
+    static constexpr int NW = (NB + 3) / 4;
+    uint32_t w[NW];
+    __device__ __forceinline__ void load(const uint8_t *blk, int g) { hm_bytes<NB>(blk + 2 + g * NB, w); }
+};
+
+// ((x >> (B k)) & (2^B - 1)) << 7 for a constant field k of width B (4 or 8): a pair-table byte
+// offset, in two operations.
+template <int B, int K>
+__device__ __forceinline__ uint32_t hm_field7(uint32_t x) {
+    constexpr uint32_t mask = ((1u << B) - 1u) << 7;
+    if constexpr (B * K >= 32) return 0u;   // (a field past the word: not reached)
+    else if constexpr (B * K >= 7) return (x >> (B * K - 7)) & mask;
+    else return (x << (7 - B * K)) & mask;
 }
 
 template <int ND, int KB, int VB>
@@ -330,46 +337,48 @@ __global__ void __launch_bounds__(kHmThreads, 3) attn_dm_kernel(const __grid_con
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             const int ta = 16 * kk + 2 * t;   // tokens ta, ta + 1 (k-slots 2t, 2t + 1) and ta + 8, ta + 9
-            uint64_t xa[2], xb[2], xc[2], xd[2];
-            hm_value_slice<ND, VB>(sv + ta * VBB, g, xa);
-            hm_value_slice<ND, VB>(sv + (ta + 1) * VBB, g, xb);
-            hm_value_slice<ND, VB>(sv + (ta + 8) * VBB, g, xc);
-            hm_value_slice<ND, VB>(sv + (ta + 9) * VBB, g, xd);
+            HmValueSlice<ND, VB> xa, xb, xc, xd;
+            xa.load(sv + ta * VBB, g);
+            xb.load(sv + (ta + 1) * VBB, g);
+            xc.load(sv + (ta + 8) * VBB, g);
+            xd.load(sv + (ta + 9) * VBB, g);
             const uint32_t b0 = hm_lds32(ps_s + g * kHmPsRow + 2 * ta);
             const uint32_t b1 = hm_lds32(ps_s + g * kHmPsRow + 2 * (ta + 8));
-            if constexpr (VB == 2) {
-                // nibble mt of e*: (code of the first token, of the second) at slice dim 2 mt; of o*: 2 mt + 1
-                constexpr uint64_t M = 0x3333333333333333ull;
-                const uint64_t eab = (xa[0] & M) | ((xb[0] & M) << 2), oab = ((xa[0] >> 2) & M) | (xb[0] & (M << 2));
-                const uint64_t ecd = (xc[0] & M) | ((xd[0] & M) << 2), ocd = ((xc[0] >> 2) & M) | (xd[0] & (M << 2));
+            // per slice word: e* field k = (code of the first token, of the second) at an even slice dim,
+            // o* field k at the odd dim after it (nibbles for 2-bit codes, bytes for 4-bit)
+            constexpr int NW = HmValueSlice<ND, VB>::NW;
+            constexpr uint32_t M = VB == 2 ? 0x33333333u : 0x0F0F0F0Fu;
+            constexpr int SH = VB;   // (2-bit: shift 2; 4-bit: shift 4)
+            uint32_t eab[NW], oab[NW], ecd[NW], ocd[NW];
 #pragma unroll
-                for (int mt = 0; mt < NKS; ++mt) {
-                    const uint32_t a0 = hm_lds32(vt_s + (((uint32_t)(eab >> (4 * mt)) & 15u) << 7));
-                    const uint32_t a1 = hm_lds32(vt_s + (((uint32_t)(oab >> (4 * mt)) & 15u) << 7));
-                    const uint32_t a2 = hm_lds32(vt_s + (((uint32_t)(ecd >> (4 * mt)) & 15u) << 7));
-                    const uint32_t a3 = hm_lds32(vt_s + (((uint32_t)(ocd >> (4 * mt)) & 15u) << 7));
-                    hm_mma(o[mt], a0, a1, a2, a3, b0, b1);
-                }
-            } else {
-                // byte mt of e*: (code of the first token, of the second) at slice dim 2 mt; of o*: 2 mt + 1
-                constexpr uint64_t M = 0x0F0F0F0F0F0F0F0Full;
-                uint64_t eab[2], oab[2], ecd[2], ocd[2];
+            for (int w = 0; w < NW; ++w) {
+                eab[w] = (xa.w[w] & M) | ((xb.w[w] & M) << SH);
+                oab[w] = ((xa.w[w] >> SH) & M) | (xb.w[w] & (M << SH));
+                ecd[w] = (xc.w[w] & M) | ((xd.w[w] & M) << SH);
+                ocd[w] = ((xc.w[w] >> SH) & M) | (xd.w[w] & (M << SH));
+            }
+            // m-tile mt: slice dims 2 mt (row g) and 2 mt + 1 (row g + 8)
+            constexpr int FPW = VB == 2 ? 8 : 4;   // fields per word
+            constexpr int FB = VB == 2 ? 4 : 8;    // field width
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    eab[h] = (xa[h] & M) | ((xb[h] & M) << 4);
-                    oab[h] = ((xa[h] >> 4) & M) | (xb[h] & (M << 4));
-                    ecd[h] = (xc[h] & M) | ((xd[h] & M) << 4);
-                    ocd[h] = ((xc[h] >> 4) & M) | (xd[h] & (M << 4));
+            for (int mt = 0; mt < NKS; ++mt) {
+                const int w = mt / FPW;
+                uint32_t f0, f1, f2, f3;
+                switch (mt % FPW) {
+#define HM_FIELDS(K)                                                                        \
+    case K:                                                                                 \
+        f0 = hm_field7<FB, K>(eab[w]);                                                      \
+        f1 = hm_field7<FB, K>(oab[w]);                                                      \
+        f2 = hm_field7<FB, K>(ecd[w]);                                                      \
+        f3 = hm_field7<FB, K>(ocd[w]);                                                      \
+        break;
+                    HM_FIELDS(0) HM_FIELDS(1) HM_FIELDS(2) HM_FIELDS(3)
+                    HM_FIELDS(4) HM_FIELDS(5) HM_FIELDS(6)
+                    default: HM_FIELDS(7)
+#undef HM_FIELDS
                 }
-#pragma unroll
-                for (int mt = 0; mt < NKS; ++mt) {
-                    const int h = mt >> 3, sh = 8 * (mt & 7);
-                    const uint32_t a0 = hm_lds32(vt_s + (((uint32_t)(eab[h] >> sh) & 255u) << 7));
-                    const uint32_t a1 = hm_lds32(vt_s + (((uint32_t)(oab[h] >> sh) & 255u) << 7));
-                    const uint32_t a2 = hm_lds32(vt_s + (((uint32_t)(ecd[h] >> sh) & 255u) << 7));
-                    const uint32_t a3 = hm_lds32(vt_s + (((uint32_t)(ocd[h] >> sh) & 255u) << 7));
-                    hm_mma(o[mt], a0, a1, a2, a3, b0, b1);
-                }
+                hm_mma(o[mt], hm_lds32(vt_s + f0), hm_lds32(vt_s + f1), hm_lds32(vt_s + f2), hm_lds32(vt_s + f3), b0,
+                       b1);
             }
         }
         __syncwarp();   // the stage and the probability tile are free for the next chunk
