@@ -442,8 +442,9 @@ size_t tq_attn_workspace_bytes_d(int B, int Hq, int Hkv, int T_cap, int head_dim
  * [B][Hkv][T_cap] blocks of kcb->bits / vcb->bits at head_dim (both arrays
  * 16-byte aligned, T_cap a multiple of 8: the kernel copies 32-block runs
  * in 16-byte pieces), seq_lens as for tq_attn_decode, 1 <= T <= T_cap,
- * G = Hq / Hkv <= 8, out float32 [B][Hq][head_dim], workspace >=
- * tq_attn_workspace_bytes_d(...) bytes (16-byte aligned).  Errors:
+ * G = Hq / Hkv <= 8 (B, Hkv <= 65535, B * Hq <= 1048560), out float32
+ * [B][Hq][head_dim], workspace >= tq_attn_workspace_bytes_d(...) bytes
+ * (16-byte aligned).  Errors:
  * TQ_ERR_ARG (T_cap not a multiple of 8 among them), TQ_ERR_UNSUPPORTED,
  * TQ_ERR_ALIGN, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
 int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blocks, const tq_codebook *kcb,

@@ -872,8 +872,10 @@ extern "C" int tq_attn_decode_d(const void *q, int q_dtype, const uint8_t *k_blo
         !std::isfinite(scale))
         return TQ_ERR_ARG;
     const int G = Hq / Hkv;
+    // (grid limits: the attention grid is [splits][Hkv][B], the prep and combine grids take 32 and 16
+    // (sequence, query head) rows per CTA row)
     if (G > 8 || !hd_dim_ok(head_dim) || !hd_codebook_ok(kcb, head_dim) || !hd_codebook_ok(vcb, head_dim) ||
-        dtype_bytes(q_dtype) == 0)
+        dtype_bytes(q_dtype) == 0 || B > 65535 || Hkv > 65535 || (int64_t)B * Hq > 65535LL * 16)
         return TQ_ERR_UNSUPPORTED;
     if (!aligned(q, dtype_bytes(q_dtype)) || !aligned(k_blocks, 16) || !aligned(v_blocks, 16) || !aligned(out, 4) ||
         !aligned(R, 16) || !aligned(workspace, 16))
