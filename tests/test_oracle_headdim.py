@@ -68,6 +68,14 @@ def test_pack_unpack_identity(d, bits):
     assert np.unpackbits(headdim.pack_d(one, np.zeros(1, np.uint16), bits)).sum() == 1
 
 
+@pytest.mark.parametrize("d", headdim.HEAD_DIMS)
+@pytest.mark.parametrize("bits", (2, 3, 4))
+def test_code_bytes_are_the_pages_packed_size(d, bits):
+    """The spec's Memory Layout gives ceil(head_dim * bits / 8) packed bytes per
+    head; a block adds the fp16 norm."""
+    assert headdim.block_bytes_d(d, bits) - 2 == -(-(d * bits) // 8)
+
+
 @pytest.mark.parametrize("d", (64, 96, 160))
 @pytest.mark.parametrize("bits", (2, 4))
 def test_codebook_is_the_beta_lloyd_max_fixed_point(d, bits):
