@@ -236,30 +236,24 @@ __global__ void __launch_bounds__(kAttnThreads * kCombineMaxGroups) attn_combine
         if (grp == 0) out[(int64_t)blockIdx.x * kD + d] = o;
         return;
     }
-    // inverse rotation by group 0 (whole warps): the butterfly stages within a warp by shuffles, the
-    // two across warps through shared memory; every thread passes the same barriers
-    float v = o;
-    if (grp == 0) {
+    // inverse rotation by group 0; every thread passes the same barriers
+    if (grp == 0) buf[d] = o;
+    __syncthreads();
 #pragma unroll
-        for (int L = 1; L < 32; L <<= 1) {
-            const float w = __shfl_xor_sync(0xffffffffu, v, L);
-            v = (d & L) ? (w - v) : (v + w);
-        }
-    }
-#pragma unroll
-    for (int L = 32; L < kD; L <<= 1) {
-        if (grp == 0) buf[d] = v;
-        __syncthreads();
+    for (int L = 1; L < kD; L <<= 1) {
+        float v = 0.f, w = 0.f;
         if (grp == 0) {
-            const float w = buf[d ^ L];
-            v = (d & L) ? (w - v) : (v + w);
+            v = buf[d];
+            w = buf[d ^ L];
         }
+        __syncthreads();
+        if (grp == 0) buf[d] = (d & L) ? (w - v) : (v + w);
         __syncthreads();
     }
     if (grp == 0) {
         const uint32_t sw[4] = {s0, s1, s2, s3};
-        const float r = v * 0.08838834764831845f;
-        out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -r : r;
+        const float v = buf[d] * 0.08838834764831845f;
+        out[(int64_t)blockIdx.x * kD + d] = ((sw[d >> 5] >> (d & 31)) & 1u) ? -v : v;
     }
 }
 
