@@ -177,7 +177,7 @@ def test_encode_tensor_core_norms_near_fp16_ties(env, d):
 
 
 @pytest.mark.parametrize("d,kbits,vbits,B,Hq,Hkv,T,lens", [
-    # up to four heads per KV head with 2- or 4-bit values: the tensor-core kernel
+    # up to four heads per KV head: the tensor-core kernel
     (64, 4, 2, 3, 8, 2, 700, [700, 1, 333]),
     (160, 4, 4, 2, 4, 4, 520, [0, 517]),
     (64, 2, 2, 2, 4, 2, 1000, None),
@@ -185,10 +185,14 @@ def test_encode_tensor_core_norms_near_fp16_ties(env, d):
     (128, 4, 2, 4, 16, 4, 2100, [2100, 0, 1, 1057]),
     (160, 3, 2, 2, 12, 4, 1500, [33, 1500]),
     (160, 2, 4, 1, 2, 2, 3000, None),
-    # more heads, or 3-bit values: the CUDA-core kernel
+    (96, 4, 3, 2, 8, 2, 600, [600, 599]),
+    (64, 3, 3, 3, 3, 3, 1100, [1, 1100, 40]),
+    (160, 4, 3, 2, 16, 4, 1300, [1300, 777]),
+    (128, 2, 3, 1, 2, 1, 2600, None),
+    # more heads per KV head: the CUDA-core kernel
     (96, 3, 3, 2, 14, 2, 1000, None),
     (128, 2, 3, 1, 8, 1, 4096, None),
-    (96, 4, 3, 2, 8, 2, 600, [600, 599]),
+    (64, 4, 2, 1, 16, 2, 900, [900]),
 ])
 def test_attention_matches_oracle(env, d, kbits, vbits, B, Hq, Hkv, T, lens):
     tq, dev = env["tq"], env["dev"]

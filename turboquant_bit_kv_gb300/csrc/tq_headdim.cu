@@ -14,7 +14,7 @@
 //
 // This unit holds the CUDA-core kernels and the C ABI; bf16 / fp16 encodes of
 // 1024 rows or more run on the tensor cores (tq_headdim_tc.cu), and so does
-// the attention for up to four heads per KV head with 2- or 4-bit values
+// the attention for up to four heads per KV head
 // (tq_headdim_mma.cu).
 //
 // Codec kernels (CUDA cores, float32; d = 32 ND): a warp per row, lane l
@@ -745,7 +745,7 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     const int smem_p = 2 * kHdTile * (D + 1) * 4, smem_c = (kHdCRows * (D + 1) + D * (kHdTile + 1)) * 4;
     if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_p, done_p) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_c, done_c) != TQ_OK) return TQ_ERR_CUDA;
-    // up to four heads per KV head and 2- or 4-bit values: the tensor-core kernel (tq_headdim_mma.cu);
+    // up to four heads per KV head: the tensor-core kernel (tq_headdim_mma.cu);
     // otherwise the CUDA-core kernel above
     const int mma = hd_attn_mma_plan(a, D);
     if (mma != 1 && mma != TQ_OK) return mma;

@@ -31,7 +31,7 @@ struct HdAttnArgs {
 int hd_max_splits(int T);
 void hd_split_plan(int B, int Hkv, int T, int slots, int warps, int *splits, int *tps);
 
-// The tensor-core attention kernel (tq_headdim_mma.cu), G <= 4 and 2- or 4-bit values:
+// The tensor-core attention kernel (tq_headdim_mma.cu), G <= 4 (any key and value width):
 // hd_attn_mma_plan returns 1 when it does not cover the call, else sets a.splits / a.tps from the
 // kernel's occupancy and returns a TQ_ status; hd_attn_mma_launch enqueues it as a programmatic
 // dependent of the kernel before it.

@@ -1,6 +1,6 @@
 // Decode attention at head dims 64, 96, 128 and 160 on the tensor cores
 // (mma.sync m16n8k16, fp16 operands, float32 accumulation), for up to four
-// query heads per KV head and 2- or 4-bit values.
+// query heads per KV head and 2-, 3- or 4-bit values.
 //
 // "TurboQuant KV Cache Compression — Spec", Optimization: Fused dequant-dot
 // (scores of the rotated query against centroid lookups, no per-key inverse
@@ -27,7 +27,9 @@
 //     are dims (lane group g takes the contiguous dims [g d/8, (g + 1) d/8)),
 //     the k-slots tokens in order; A-fragment words come from a table of
 //     (token 2j, token 2j + 1) code pairs at one dim, their indices built by
-//     interleaving the two tokens' code slices; B from the probability tile.
+//     interleaving the two tokens' code slices (3-bit: the 2-bit planes as
+//     for 2-bit codes, the two high bits in index bits 4 and 5); B from the
+//     probability tile.
 // The warps' states are merged in shared memory into one partial per head
 // and split, in the layout the combine kernel reads.
 
@@ -93,7 +95,7 @@ __device__ __forceinline__ void hm_split(float v, float &hi, float &lo) {
     lo = v - hi;
 }
 
-// The two codes of key pair-table entry e (3-bit: e = low bits of both | high bits of both << 4).
+// The two codes of pair-table entry e (3-bit: e = low bits of both | high bits of both << 4).
 template <int KB>
 __device__ __forceinline__ void hm_key_pair(int e, int &c0, int &c1) {
     if constexpr (KB == 3) {
@@ -161,13 +163,24 @@ struct HmKeySlice {
 };
 
 // Value slice of one token for this lane (dims [g d/8, (g + 1) d/8)) as 32-bit words: word w holds
-// slice dims 16 w .. (2-bit codes) or 8 w .. (4-bit codes).
+// slice dims 16 w .. (2-bit codes and the 2-bit plane of 3-bit codes) or 8 w .. (4-bit codes); for
+// 3-bit codes h holds the slice's 4 ND high bits (bit i: slice dim i).
 template <int ND, int VB>
 struct HmValueSlice {
-    static constexpr int NB = ND * VB / 2;   // bytes of the slice
+    static constexpr int NB = ND * (VB == 3 ? 2 : VB) / 2;   // bytes of the slice (of the 2-bit plane)
     static constexpr int NW = (NB + 3) / 4;
     uint32_t w[NW];
-    __device__ __forceinline__ void load(const uint8_t *blk, int g) { hm_bytes<NB>(blk + 2 + g * NB, w); }
+    uint32_t h;
+    __device__ __forceinline__ void load(const uint8_t *blk, int g) {
+        hm_bytes<NB>(blk + 2 + g * NB, w);
+        if constexpr (VB == 3) {
+            // the slice starts at bit 4 ND g of the high plane: a byte, plus a nibble when ND g is odd
+            constexpr int D = 32 * ND;
+            const uint32_t a = (uint32_t)__cvta_generic_to_shared(blk + 2 + D / 4 + ((g * ND) >> 1));
+            const uint32_t base = a & ~3u, sh = (a & 3u) * 8u + 4u * ((g * ND) & 1);   // < 32
+            h = __funnelshift_r(hm_lds32(base), hm_lds32(base + 4), sh);
+        }
+    }
 };
 
 // ((x >> (B k)) & (2^B - 1)) << 7 for a constant field k of width B (4 or 8): a pair-table byte
@@ -178,6 +191,12 @@ __device__ __forceinline__ uint32_t hm_field7(uint32_t x) {
     if constexpr (B * K >= 32) return 0u;   // (a field past the word: not reached)
     else if constexpr (B * K >= 7) return (x >> (B * K - 7)) & mask;
     else return (x << (7 - B * K)) & mask;
+}
+
+// ((x >> 2 k) & 3) << 11: the two high bits of a 3-bit value pair as pair-table index bits 4 and 5
+// (byte offset bits 11 and 12); k is a constant once the m-tile loop is unrolled.
+__device__ __forceinline__ uint32_t hm_hfield(uint32_t x, int k) {
+    return 2 * k >= 11 ? (x >> (2 * k - 11)) & (3u << 11) : (x << (11 - 2 * k)) & (3u << 11);
 }
 
 template <int ND, int KB, int VB>
@@ -224,8 +243,9 @@ __global__ void __launch_bounds__(kHmThreads, 3) attn_dm_kernel(const __grid_con
         }
         uint32_t *vt = reinterpret_cast<uint32_t *>(hm_smem + C::kVT);
         for (int i = threadIdx.x; i < C::NV * 32; i += kHmThreads) {
-            const int e = i >> 5;
-            vt[i] = hm_h2(a.vc[e & ((1 << VB) - 1)], a.vc[e >> VB]);
+            int c0, c1;
+            hm_key_pair<VB>(i >> 5, c0, c1);   // (the same pair-index layout as the keys)
+            vt[i] = hm_h2(a.vc[c0], a.vc[c1]);
         }
     }
     // the rotated queries come from the prep kernel this one depends on
@@ -345,10 +365,11 @@ __global__ void __launch_bounds__(kHmThreads, 3) attn_dm_kernel(const __grid_con
             const uint32_t b0 = hm_lds32(ps_s + g * kHmPsRow + 2 * ta);
             const uint32_t b1 = hm_lds32(ps_s + g * kHmPsRow + 2 * (ta + 8));
             // per slice word: e* field k = (code of the first token, of the second) at an even slice dim,
-            // o* field k at the odd dim after it (nibbles for 2-bit codes, bytes for 4-bit)
+            // o* field k at the odd dim after it (nibbles for 2-bit codes and 3-bit low planes, bytes
+            // for 4-bit)
             constexpr int NW = HmValueSlice<ND, VB>::NW;
-            constexpr uint32_t M = VB == 2 ? 0x33333333u : 0x0F0F0F0Fu;
-            constexpr int SH = VB;   // (2-bit: shift 2; 4-bit: shift 4)
+            constexpr uint32_t M = VB == 4 ? 0x0F0F0F0Fu : 0x33333333u;
+            constexpr int SH = VB == 4 ? 4 : 2;
             uint32_t eab[NW], oab[NW], ecd[NW], ocd[NW];
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
@@ -357,9 +378,18 @@ __global__ void __launch_bounds__(kHmThreads, 3) attn_dm_kernel(const __grid_con
                 ecd[w] = (xc.w[w] & M) | ((xd.w[w] & M) << SH);
                 ocd[w] = ((xc.w[w] >> SH) & M) | (xd.w[w] & (M << SH));
             }
+            // 3-bit high bits, 2-bit fields in the same pattern: field k = (high bit of the first token,
+            // of the second) at slice dim 2 k (eh*) or 2 k + 1 (oh*)
+            uint32_t ehab = 0u, ohab = 0u, ehcd = 0u, ohcd = 0u;
+            if constexpr (VB == 3) {
+                ehab = (xa.h & 0x55555555u) | ((xb.h & 0x55555555u) << 1);
+                ohab = ((xa.h >> 1) & 0x55555555u) | (xb.h & 0xAAAAAAAAu);
+                ehcd = (xc.h & 0x55555555u) | ((xd.h & 0x55555555u) << 1);
+                ohcd = ((xc.h >> 1) & 0x55555555u) | (xd.h & 0xAAAAAAAAu);
+            }
             // m-tile mt: slice dims 2 mt (row g) and 2 mt + 1 (row g + 8)
-            constexpr int FPW = VB == 2 ? 8 : 4;   // fields per word
-            constexpr int FB = VB == 2 ? 4 : 8;    // field width
+            constexpr int FPW = VB == 4 ? 4 : 8;   // fields per word
+            constexpr int FB = VB == 4 ? 8 : 4;    // field width
 #pragma unroll
             for (int mt = 0; mt < NKS; ++mt) {
                 const int w = mt / FPW;
@@ -376,6 +406,12 @@ __global__ void __launch_bounds__(kHmThreads, 3) attn_dm_kernel(const __grid_con
                     HM_FIELDS(4) HM_FIELDS(5) HM_FIELDS(6)
                     default: HM_FIELDS(7)
 #undef HM_FIELDS
+                }
+                if constexpr (VB == 3) {
+                    f0 |= hm_hfield(ehab, mt);
+                    f1 |= hm_hfield(ohab, mt);
+                    f2 |= hm_hfield(ehcd, mt);
+                    f3 |= hm_hfield(ohcd, mt);
                 }
                 hm_mma(o[mt], hm_lds32(vt_s + f0), hm_lds32(vt_s + f1), hm_lds32(vt_s + f2), hm_lds32(vt_s + f3), b0,
                        b1);
@@ -453,9 +489,11 @@ HmKernel hm_kernel() {
 HmKernel hm_select(int d, int kb, int vb) {
 #define HM_CASE(ND, KBv, VBv) \
     if (d == 32 * ND && kb == KBv && vb == VBv) return hm_kernel<ND, KBv, VBv>();
-#define HM_DIM(ND) HM_CASE(ND, 2, 2) HM_CASE(ND, 3, 2) HM_CASE(ND, 4, 2) HM_CASE(ND, 2, 4) HM_CASE(ND, 3, 4) HM_CASE(ND, 4, 4)
+#define HM_VB(ND, VBv) HM_CASE(ND, 2, VBv) HM_CASE(ND, 3, VBv) HM_CASE(ND, 4, VBv)
+#define HM_DIM(ND) HM_VB(ND, 2) HM_VB(ND, 3) HM_VB(ND, 4)
     HM_DIM(2) HM_DIM(3) HM_DIM(4) HM_DIM(5)
 #undef HM_DIM
+#undef HM_VB
 #undef HM_CASE
     return HmKernel{nullptr, 0, nullptr, nullptr};
 }
