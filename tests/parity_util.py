@@ -46,6 +46,21 @@ def fp16_tie_distance(n):
         return np.where(n > 0, np.minimum(d1, d2) / n, np.inf)
 
 
+def check_counted(label, idx_g, idx_o, dist_y, n_g, n_o, exact, tie=2.0**-21):
+    """The codes rule for given per-coordinate distances to a decision point
+    (dist_y) and a scale or norm whose exact float64 value is `exact`: codes
+    bit-exact except within CODE_TOL_Y, the stored fp16 bit-exact except within
+    `tie` (relative) of an fp16 rounding boundary; mismatches counted."""
+    mism = idx_g != idx_o
+    assert np.all(dist_y[mism] < CODE_TOL_Y), (label, np.sum(mism & (dist_y >= CODE_TOL_Y)))
+    assert mism.mean() < CODE_FRAC, (label, mism.mean())
+    nm = n_g != n_o
+    assert np.all(fp16_tie_distance(exact[nm]) < tie), (label, exact[nm][:4])
+    assert nm.mean() < CODE_FRAC
+    record(label, coords=int(mism.size), near_boundary=int((dist_y < CODE_TOL_Y).sum()),
+           code_mismatch=int(mism.sum()), vectors=int(nm.size), norm_mismatch=int(nm.sum()))
+
+
 def check_codes(gpu_blocks, bits, x, signs, b32, label=""):
     """Compare GPU blocks [N, bb] (uint8) with the oracle's encoding of x."""
     x = np.asarray(x, np.float64)

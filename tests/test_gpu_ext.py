@@ -17,7 +17,7 @@ import oracle
 from oracle import codec, ext
 from turboquant_bit_kv_gb300 import workloads
 
-from parity_util import CODE_FRAC, CODE_TOL_Y, fp16_tie_distance, record, rne
+from parity_util import check_counted as _check, rne
 
 pytestmark = pytest.mark.gpu
 
@@ -45,17 +45,6 @@ def _rows(n, seed, dtype):
     x[5] = 0.0                                   # a zero row
     x[7] *= 2.0 ** -30                           # a tiny one
     return x.to(dtype)
-
-
-def _check(label, idx_g, idx_o, dist_y, n_g, n_o, exact):
-    mism = idx_g != idx_o
-    assert np.all(dist_y[mism] < CODE_TOL_Y), (label, np.sum(mism & (dist_y >= CODE_TOL_Y)))
-    assert mism.mean() < CODE_FRAC, (label, mism.mean())
-    nm = n_g != n_o
-    assert np.all(fp16_tie_distance(exact[nm]) < 2.0**-21), (label, exact[nm][:4])
-    assert nm.mean() < CODE_FRAC
-    record(label, coords=int(mism.size), near_boundary=int((dist_y < CODE_TOL_Y).sum()),
-           code_mismatch=int(mism.sum()), vectors=int(nm.size), norm_mismatch=int(nm.sum()))
 
 
 def _nc_norm(x, idx, c):

@@ -86,7 +86,7 @@ def test_llama_decode_fullsize(env, T):
     _sampled_codes(env, kb.view(-1, 66), k.view(-1, D), 4, 8192, 1, "llama K")
     _sampled_codes(env, vb.view(-1, 34), v.view(-1, D), 2, 8192, 2, "llama V")
 
-    slices = [(0, 0), (7, 3), (15, 7)]
+    slices = [(0, 0), (2, 6), (7, 3), (9, 1), (12, 4), (15, 7)]
     hats = {}
     for b, h in slices:
         kblk, khat, _ = _oracle_slice(env, _rows(k[b, h]), 4)
@@ -140,7 +140,7 @@ def test_qwen_outlier_append_fullsize(env):
         assert torch.all(blk[:, :, T:] == 0)
         caches[name] = blk
 
-    slices = [(0, 0), (31, 2), (63, 3)]
+    slices = [(0, 0), (10, 1), (31, 2), (42, 0), (55, 2), (63, 3)]
     hats = {}
     for b, h in slices:
         kblk, khat, _ = _oracle_slice(env, _rows(w["k"][b, h]), 3)
@@ -173,7 +173,7 @@ def test_qjl_two_term_fullsize(env):
 
     Sd = S.double().cpu().numpy()
     c3 = env["books"][3][0]
-    slices = [(0, 0), (3, 5), (7, 7)]
+    slices = [(0, 0), (2, 2), (3, 5), (5, 4), (6, 1), (7, 7)]
     ref = {}
     for b, h in slices:
         x = _rows(k[b, h])
@@ -308,7 +308,7 @@ def test_llama_prefill_fullsize(env):
     vb = torch.empty((B, Hkv, T, 34), dtype=torch.uint8, device=dev)
     tq.tq_encode_kv(k.view(-1, D), env["cbs"][4], env["signs"], kb)
     tq.tq_encode_kv(v.view(-1, D), env["cbs"][2], env["signs"], vb)
-    slices = [(0, 0), (9, 5), (15, 7)]
+    slices = [(0, 0), (4, 2), (9, 5), (11, 6), (13, 0), (15, 7)]
     hats = {}
     for b, h in slices:
         kblk, khat, _ = _oracle_slice(env, _rows(k[b, h]), 4)
