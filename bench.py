@@ -101,7 +101,7 @@ KERNEL_SOURCES = {
                   "tq_attn_g2.cu", "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_device.cuh"],
     "qjl": ["tq_qjl.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "hd_encode": ["tq_headdim.cu", "tq_headdim.cuh", "tq_headdim_tc.cu", "tq_tc.cuh", "tq_device.cuh"],
-    "hd_attention": ["tq_headdim.cu", "tq_headdim.cuh", "tq_headdim_mma.cu", "tq_device.cuh"],
+    "hd_attention": ["tq_headdim.cu", "tq_headdim.cuh", "tq_headdim_mma.cuh", "tq_headdim_mma.cu", "tq_device.cuh"],
     "serialize": ["tq_encode.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "deserialize": ["tq_decode.cu", "tq_codec.cu", "tq_device.cuh"],
 }

@@ -177,7 +177,7 @@ def test_encode_tensor_core_norms_near_fp16_ties(env, d):
 
 
 @pytest.mark.parametrize("d,kbits,vbits,B,Hq,Hkv,T,lens", [
-    # up to four heads per KV head: the tensor-core kernel
+    # up to four heads per KV head: one n-tile of 4 heads x (hi, lo)
     (64, 4, 2, 3, 8, 2, 700, [700, 1, 333]),
     (160, 4, 4, 2, 4, 4, 520, [0, 517]),
     (64, 2, 2, 2, 4, 2, 1000, None),
@@ -189,10 +189,13 @@ def test_encode_tensor_core_norms_near_fp16_ties(env, d):
     (64, 3, 3, 3, 3, 3, 1100, [1, 1100, 40]),
     (160, 4, 3, 2, 16, 4, 1300, [1300, 777]),
     (128, 2, 3, 1, 2, 1, 2600, None),
-    # more heads per KV head: the CUDA-core kernel
+    # five to eight heads per KV head: the eight-head n-tile (hi and lo as separate products)
     (96, 3, 3, 2, 14, 2, 1000, None),
     (128, 2, 3, 1, 8, 1, 4096, None),
     (64, 4, 2, 1, 16, 2, 900, [900]),
+    (160, 4, 4, 2, 20, 4, 1100, [1100, 613]),
+    (64, 2, 3, 3, 18, 3, 700, [0, 700, 31]),
+    (128, 3, 2, 2, 16, 2, 1500, [1, 1500]),
 ])
 def test_attention_matches_oracle(env, d, kbits, vbits, B, Hq, Hkv, T, lens):
     tq, dev = env["tq"], env["dev"]

@@ -15,8 +15,10 @@ LIB = os.path.join(HERE, "libtq.so")
 SOURCES = ["tq_host.cpp", "tq_encode.cu", "tq_decode.cu", "tq_codec.cu", "tq_qjl.cu", "tq_attn.cu", "tq_attn_g1.cu", "tq_attn_g2.cu",
            "tq_attn_g4.cu", "tq_attn_g8.cu", "tq_attn_noalloc.cu", "tq_attn_plan.cu", "tq_attn_mma.cu", "tq_attn_mma_k2.cu",
            "tq_attn_mma_k3.cu", "tq_attn_mma_k4.cu", "tq_attn_mma_k8.cu", "tq_status.cu",
-           "tq_attn_prefill.cu", "tq_ext.cu", "tq_headdim.cu", "tq_headdim_tc.cu", "tq_headdim_mma.cu"]
-HEADERS = ["tq_device.cuh", "tq_tc.cuh", "tq_attn.cuh", "tq_attn_mma.h", "tq_attn_mma.cuh", "tq_internal.h"]
+           "tq_attn_prefill.cu", "tq_ext.cu", "tq_headdim.cu", "tq_headdim_tc.cu", "tq_headdim_mma.cu",
+           "tq_headdim_mma8.cu"]
+HEADERS = ["tq_device.cuh", "tq_tc.cuh", "tq_attn.cuh", "tq_attn_mma.h", "tq_attn_mma.cuh", "tq_internal.h", "tq_headdim.cuh",
+           "tq_headdim_mma.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

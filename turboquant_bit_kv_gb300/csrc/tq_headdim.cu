@@ -12,10 +12,10 @@
 // byte, 3-bit a 2-bit low plane of d / 4 bytes then a 1-bit high plane of
 // d / 8 bytes.
 //
-// This unit holds the CUDA-core kernels and the C ABI; bf16 / fp16 encodes of
-// 1024 rows or more run on the tensor cores (tq_headdim_tc.cu), and so does
-// the attention for up to four heads per KV head
-// (tq_headdim_mma.cu).
+// This unit holds the CUDA-core codec kernels, the decode attention's query
+// prep and combine kernels and the C ABI; bf16 / fp16 encodes of 1024 rows or
+// more run on the tensor cores (tq_headdim_tc.cu), and so does the attention
+// kernel itself (tq_headdim_mma.cuh).
 //
 // Codec kernels (CUDA cores, float32; d = 32 ND): a warp per row, lane l
 // holds elements l + 32 k.  R sits in shared memory with rows padded to
@@ -27,16 +27,12 @@
 // an fp16 rounding boundary.  The codec kernels rotate four rows per warp at
 // once, so every element of R read from shared memory serves four rows.
 // Decode attention: a prep kernel rotates every query once (R q, scale
-// log2(e) folded in; a small tiled product); the attention kernel (here: one
-// CTA of 8 warps per (sequence, KV head, context split), 32 tokens per warp
-// step, each step's K and V blocks staged in shared memory by asynchronous
-// copies while the previous step computes; lane t scores its token against
-// n_t c[code_t] for every head, the warp keeps an online softmax per head,
-// and the value sums run with lanes over dims; the warps merge in shared
-// memory) writes one partial per head and split; a combine kernel merges
-// the splits and rotates back (R^T, a small tiled product).  The three are
-// chained as programmatic dependents; the split count is chosen from the
-// attention kernel's occupancy so that the CTAs fill whole waves.
+// log2(e) folded in; a small tiled product); the attention kernel (one CTA
+// of 4 warps per (sequence, KV head, context split) on the tensor cores)
+// writes one partial per head and split; a combine kernel merges the splits
+// and rotates back (R^T, a small tiled product).  The three are chained as
+// programmatic dependents; the split count is chosen from the attention
+// kernel's occupancy so that the CTAs fill whole waves.
 
 #include <cmath>
 #include <cstring>
@@ -393,249 +389,6 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_prep_kernel(const __grid_co
     }
 }
 
-// s[h] += q[h][j] c: the query of head h at dim j times the centroid (qj: dim j's GB heads), two
-// heads per packed float32 pair (s[i] = heads 2i, 2i + 1).
-template <int GB>
-__device__ __forceinline__ void hd_fma_heads(float2 (&s)[GB / 2], const float *qj, float c) {
-    const float2 cc = make_float2(c, c);
-    const float4 qa = *reinterpret_cast<const float4 *>(qj);
-    s[0] = __ffma2_rn(make_float2(qa.x, qa.y), cc, s[0]);
-    s[1] = __ffma2_rn(make_float2(qa.z, qa.w), cc, s[1]);
-    if constexpr (GB == 8) {
-        const float4 qb = *reinterpret_cast<const float4 *>(qj + 4);
-        s[2] = __ffma2_rn(make_float2(qb.x, qb.y), cc, s[2]);
-        s[3] = __ffma2_rn(make_float2(qb.z, qb.w), cc, s[3]);
-    }
-}
-
-// One token's scores against the GB heads: s[h] = sum_j q[h][j] kc[code_j] over the D codes of its
-// block (blk, in shared memory; the code area read 16 bits at a time, the 3-bit high plane a byte
-// per eight dims).
-template <int D, int GB, int BITS>
-__device__ __forceinline__ void hd_score(const uint8_t *blk, const float *qs, const float *kc, float2 (&s)[GB / 2]) {
-    const uint16_t *kw = reinterpret_cast<const uint16_t *>(blk + 2);
-    constexpr int PER = BITS == 4 ? 4 : 8;   // codes per 16-bit word of the (low) plane
-    constexpr int SH = BITS == 4 ? 4 : 2;
-    constexpr uint32_t MASK = BITS == 4 ? 15u : 3u;
-#pragma unroll 2
-    for (int w = 0; w < D / PER; ++w) {
-        const uint32_t word = kw[w];
-        uint32_t hb = 0;
-        if constexpr (BITS == 3) hb = blk[2 + D / 4 + w];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            uint32_t code = (word >> (SH * e)) & MASK;
-            if constexpr (BITS == 3) code |= ((hb >> e) & 1u) << 2;
-            hd_fma_heads<GB>(s, qs + (PER * w + e) * GB, kc[code]);
-        }
-    }
-}
-
-// 32 bits of a code area (2-byte aligned, 16 bytes readable past it) from bit `bit` on: the two
-// 16-bit words that hold them, shifted (at least 17 valid bits).
-__device__ __forceinline__ uint32_t hd_window(const uint8_t *area, int bit) {
-    const uint16_t *w = reinterpret_cast<const uint16_t *>(area) + (bit >> 4);
-    return ((uint32_t)w[0] | ((uint32_t)w[1] << 16)) >> (bit & 15);
-}
-
-// acc[h][k] += p[t][h] vc[code of dim ND lane + k of token t] over the step's n tokens (vst: their
-// blocks in shared memory, VB bytes apart; pw: [32][GB] probabilities times value norms), two heads
-// per packed float32 pair (acc[i][k] = heads 2i, 2i + 1).  A lane's ND consecutive codes are one bit
-// window of the code area (the 3-bit high plane a second).
-template <int D, int GB, int BITS>
-__device__ __forceinline__ void hd_values(const uint8_t *vst, int VB, int n, const float *pw, const float *vc,
-                                          float2 (&acc)[GB / 2][D / 32], int lane) {
-    constexpr int ND = D / 32;
-    constexpr int CB = BITS == 4 ? 4 : 2;   // bits per code in the (low) plane
-    const int lo_bit = CB * ND * lane, hi_bit = 8 * (D / 4) + ND * lane;
-#pragma unroll 2
-    for (int tt = 0; tt < n; ++tt) {
-        const uint8_t *area = vst + tt * VB + 2;
-        float2 p[GB / 2];
-#pragma unroll
-        for (int h = 0; h < GB; h += 4) {
-            const float4 q4 = *reinterpret_cast<const float4 *>(pw + tt * GB + h);
-            p[h / 2] = make_float2(q4.x, q4.y);
-            p[h / 2 + 1] = make_float2(q4.z, q4.w);
-        }
-        const uint32_t wl = hd_window(area, lo_bit);
-        uint32_t wh = 0;
-        if constexpr (BITS == 3) wh = hd_window(area, hi_bit);
-#pragma unroll
-        for (int k = 0; k < ND; ++k) {
-            uint32_t code = (wl >> (CB * k)) & ((1u << CB) - 1u);
-            if constexpr (BITS == 3) code |= ((wh >> k) & 1u) << 2;
-            const float c = vc[code];
-            const float2 cc = make_float2(c, c);
-#pragma unroll
-            for (int i = 0; i < GB / 2; ++i) acc[i][k] = __ffma2_rn(p[i], cc, acc[i][k]);
-        }
-    }
-}
-
-// One CTA of 8 warps per (sequence, KV head, context split); GB = 4 or 8 head slots (G <= GB).
-// Each warp takes 32-token steps t0 + 32 (warp + 8 i): the step's K and V blocks are copied into a
-// two-stage buffer of the warp's own with 16-byte cp.async pieces while the previous step is
-// computed (chunk starts are 16-byte aligned: T_cap a multiple of 8, 32 blocks a multiple of 16
-// bytes, splits whole chunks).  Lane t scores token t against every head from shared memory (no
-// cross-lane sums), the warp keeps an online softmax per head, and the value sums run with lanes over
-// dims, the step's probabilities times value norms read back from shared memory.
-template <int ND, int GB>
-__global__ void __launch_bounds__(kHdThreads, GB == 4 ? 3 : 2) attn_d_kernel(const __grid_constant__ HdAttnArgs a) {
-    constexpr int D = 32 * ND;
-    extern __shared__ __align__(16) float hd_smem[];
-    float *qs = hd_smem;                                                   // [D][GB] queries, dim-major
-    float *ctab = qs + D * GB;                                             // key | value centroids
-    float *pvs = ctab + 32;                                                // [warp][32][GB]
-    uint8_t *stg = reinterpret_cast<uint8_t *>(pvs + kHdWarps * 32 * GB);  // [warp][2][32 (KB + VB)]
-    float *part = reinterpret_cast<float *>(stg);                          // [warp][GB][2 + D], at the end
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.z, kvh = blockIdx.y, sp = blockIdx.x;
-    int L = a.T;
-    if (a.seq_lens) {
-        const int sl = a.seq_lens[b];
-        L = sl < 0 ? 0 : (sl > a.T ? a.T : sl);
-    }
-    const int t0 = sp * a.tps, t1 = min(L, t0 + a.tps);
-    const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8, SB = 32 * (KB + VB);
-    const int64_t seg = ((int64_t)b * a.Hkv + kvh) * a.T_cap;
-    const uint8_t *kseg = a.k + seg * KB, *vseg = a.v + seg * VB;
-    uint8_t *wst = stg + warp * 2 * SB;
-    // the K then V blocks of tokens [base, base + n) into stage buf, in whole 16-byte pieces (the
-    // last piece may run up to 15 bytes past the n-th block, still inside the segment's T_cap blocks)
-    auto issue = [&](int base, int buf) {
-        const int n = min(32, t1 - base);
-        const int nk = (n * KB + 15) >> 4, nv = (n * VB + 15) >> 4;
-        const uint8_t *sk = kseg + (int64_t)base * KB, *sv = vseg + (int64_t)base * VB;
-        uint8_t *dk = wst + buf * SB, *dv = dk + 32 * KB;
-        for (int q = lane; q < nk; q += 32) cp_async16(dk + 16 * q, sk + 16 * q);
-        for (int q = lane; q < nv; q += 32) cp_async16(dv + 16 * q, sv + 16 * q);
-        cp_async_commit();
-    };
-    int base = t0 + 32 * warp;
-    if (base < t1) issue(base, 0);   // the first step is on its way while the queries are gathered
-    if (threadIdx.x < 16) {
-        ctab[threadIdx.x] = a.kc[threadIdx.x];
-        ctab[16 + threadIdx.x] = a.vc[threadIdx.x];
-    }
-    // the rotated queries come from the prep kernel this one depends on
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const float *qg = a.qrot + ((int64_t)b * a.Hq + kvh * a.G) * D;
-    for (int i = threadIdx.x; i < D * GB; i += blockDim.x) {
-        const int j = i / GB, h = i % GB;
-        qs[i] = h < a.G ? qg[h * D + j] : 0.f;
-    }
-    __syncthreads();
-
-    // per head: the warp's running maximum (uniform), this lane's share of l, the value sums of dims
-    // ND lane + k
-    float m[GB], l[GB];
-    float2 acc[GB / 2][ND];   // heads 2i, 2i + 1
-#pragma unroll
-    for (int h = 0; h < GB; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < GB / 2; ++i)
-#pragma unroll
-        for (int k = 0; k < ND; ++k) acc[i][k] = make_float2(0.f, 0.f);
-    float *pw = pvs + warp * 32 * GB;
-    int buf = 0;
-    for (; base < t1; base += 32 * kHdWarps) {
-        const int nb = base + 32 * kHdWarps;
-        if (nb < t1) issue(nb, buf ^ 1);
-        else cp_async_commit();   // (an empty group: the wait below always leaves one group)
-        cp_async_wait<1>();
-        __syncwarp();
-        const uint8_t *sk = wst + buf * SB, *sv = sk + 32 * KB;
-        const int n = min(32, t1 - base);
-        const bool valid = lane < n;
-        const uint8_t *kb = sk + lane * KB;
-        float2 s2[GB / 2];
-#pragma unroll
-        for (int i = 0; i < GB / 2; ++i) s2[i] = make_float2(0.f, 0.f);
-        if (a.kbits == 2) hd_score<D, GB, 2>(kb, qs, ctab, s2);
-        else if (a.kbits == 3) hd_score<D, GB, 3>(kb, qs, ctab, s2);
-        else hd_score<D, GB, 4>(kb, qs, ctab, s2);
-        // (past the n-th token a stage holds stale bytes: every use below is selected away)
-        const float kn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(kb)));
-        const float vn = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(sv + lane * VB)));
-        float pn[GB], corr[GB];
-#pragma unroll
-        for (int h = 0; h < GB; ++h) {
-            const float sh = valid ? ((h & 1) ? s2[h >> 1].y : s2[h >> 1].x) * kn : -INFINITY;
-            float mx = sh;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kHdFull, mx, o));
-            const float mn = fmaxf(m[h], mx);   // finite: the step holds at least one token
-            corr[h] = exp2f(m[h] - mn);
-            const float p = valid ? exp2f(sh - mn) : 0.f;
-            l[h] = fmaf(l[h], corr[h], p);
-            m[h] = mn;
-            pn[h] = valid ? p * vn : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < GB / 2; ++i) {
-            const float2 c2 = make_float2(corr[2 * i], corr[2 * i + 1]);
-#pragma unroll
-            for (int k = 0; k < ND; ++k) acc[i][k] = __fmul2_rn(acc[i][k], c2);
-        }
-#pragma unroll
-        for (int h = 0; h < GB; h += 4)
-            *reinterpret_cast<float4 *>(pw + lane * GB + h) = make_float4(pn[h], pn[h + 1], pn[h + 2], pn[h + 3]);
-        __syncwarp();
-        if (a.vbits == 2) hd_values<D, GB, 2>(sv, VB, n, pw, ctab + 16, acc, lane);
-        else if (a.vbits == 3) hd_values<D, GB, 3>(sv, VB, n, pw, ctab + 16, acc, lane);
-        else hd_values<D, GB, 4>(sv, VB, n, pw, ctab + 16, acc, lane);
-        __syncwarp();   // the stage and pw are free for the next step
-        buf ^= 1;
-    }
-    cp_async_wait<0>();
-    // the combine kernel may take its place on the SMs now (its R load overlaps this grid's tail);
-    // it waits for this grid to finish before it reads the partials
-    asm volatile("griddepcontrol.launch_dependents;");
-    __syncthreads();   // every warp is done with its stages: part takes their place
-    // l over the warp's lanes, then the warps' states into shared memory; warp h merges head h
-#pragma unroll
-    for (int h = 0; h < GB; ++h) {
-        if (h >= a.G) break;
-        const float lw = hd_warp_sum(l[h]);
-        float *pp = part + (warp * GB + h) * (2 + D);
-        if (lane == 0) {
-            pp[0] = m[h];
-            pp[1] = lw;
-        }
-#pragma unroll
-        for (int k = 0; k < ND; ++k) pp[2 + ND * lane + k] = (h & 1) ? acc[h >> 1][k].y : acc[h >> 1][k].x;
-    }
-    __syncthreads();
-    if (warp < a.G) {
-        const int h = warp;
-        float M = -INFINITY;
-        for (int w = 0; w < kHdWarps; ++w) M = fmaxf(M, part[(w * GB + h) * (2 + D)]);
-        float lt = 0.f, o[ND];
-#pragma unroll
-        for (int k = 0; k < ND; ++k) o[k] = 0.f;
-        if (M != -INFINITY) {
-            for (int w = 0; w < kHdWarps; ++w) {
-                const float *pp = part + (w * GB + h) * (2 + D);
-                const float f = pp[0] == -INFINITY ? 0.f : exp2f(pp[0] - M);
-                lt = fmaf(pp[1], f, lt);
-#pragma unroll
-                for (int k = 0; k < ND; ++k) o[k] = fmaf(pp[2 + lane + 32 * k], f, o[k]);
-            }
-        }
-        float *dst = a.ws + (((int64_t)b * a.Hq + kvh * a.G + h) * a.splits + sp) * (2 + D);
-        if (lane == 0) {
-            dst[0] = M;
-            dst[1] = lt;
-        }
-#pragma unroll
-        for (int k = 0; k < ND; ++k) dst[2 + lane + 32 * k] = o[k];
-    }
-}
-
 // The merged, normalised value sums of one (sequence, query head) row, lanes over dims
 // lane + 32 k: up to eight splits at a time, all their loads issued before any is used, folded
 // into a running maximum.
@@ -733,36 +486,26 @@ __global__ void __launch_bounds__(kHdThreads) attn_d_combine_kernel(const __grid
     }
 }
 
-template <int ND, int GB>
-int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
+template <int ND>
+int hd_launch_attn(HdAttnArgs &a, cudaStream_t st) {
     constexpr int D = 32 * ND;
-    static int done_p[64] = {0}, done_a[64] = {0}, done_c[64] = {0};
-    static int resident[5][5] = {{0}};   // CTAs per SM by (key bits, value bits)
-    const int KB = 2 + D * a.kbits / 8, VB = 2 + D * a.vbits / 8;
-    const int stages = kHdWarps * 2 * 32 * (KB + VB), part = kHdWarps * GB * (2 + D) * 4;
-    // (16 bytes past the stages: a lane's value-code window may read a word beyond the last block)
-    const int smem_a = (D * GB + 32 + kHdWarps * 32 * GB) * 4 + (stages > part ? stages : part) + 16;
+    static int done_p[64] = {0}, done_c[64] = {0};
     const int smem_p = 2 * kHdTile * (D + 1) * 4, smem_c = (kHdCRows * (D + 1) + D * (kHdTile + 1)) * 4;
     if (set_smem_limit((const void *)attn_d_prep_kernel<ND>, smem_p, done_p) != TQ_OK) return TQ_ERR_CUDA;
     if (set_smem_limit((const void *)attn_d_combine_kernel<ND>, smem_c, done_c) != TQ_OK) return TQ_ERR_CUDA;
-    // up to four heads per KV head: the tensor-core kernel (tq_headdim_mma.cu);
-    // otherwise the CUDA-core kernel above
-    const int mma = hd_attn_mma_plan(a, D);
-    if (mma != 1 && mma != TQ_OK) return mma;
-    if (mma == 1) {
-        if (set_smem_limit((const void *)attn_d_kernel<ND, GB>, smem_a, done_a) != TQ_OK) return TQ_ERR_CUDA;
-        int &per_sm = resident[a.kbits][a.vbits];
-        if (per_sm <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_d_kernel<ND, GB>, kHdThreads,
-                                                                         smem_a) != cudaSuccess)
-            return TQ_ERR_CUDA;
-        hd_split_plan(a.B, a.Hkv, a.T, sm_count() * (per_sm > 0 ? per_sm : 1), kHdWarps, &a.splits, &a.tps);
-    }
+    // the attention kernel (tq_headdim_mma.cu) covers every width and up to eight heads per KV head
+    // (the only shapes the entry point accepts); its plan sets the split count from its occupancy
+    const int plan = hd_attn_mma_plan(a, D);
+    if (plan == 1) return TQ_ERR_UNSUPPORTED;
+    if (plan != TQ_OK) return plan;
     const int64_t rows = (int64_t)a.B * a.Hq;
     const dim3 tiles(D / kHdTile, (unsigned)((rows + kHdTile - 1) / kHdTile));
     attn_d_prep_kernel<ND><<<tiles, kHdThreads, smem_p, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     // the attention and combine kernels are programmatic dependents of the kernel before them: each
     // starts its independent part (first copies; R) while its predecessor finishes
+    const int r = hd_attn_mma_launch(a, D, st);
+    if (r != TQ_OK) return r;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -771,23 +514,10 @@ int hd_launch_attn_g(HdAttnArgs &a, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(kHdThreads);
-    if (mma == TQ_OK) {
-        const int r = hd_attn_mma_launch(a, D, st);
-        if (r != TQ_OK) return r;
-    } else {
-        cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
-        cfg.dynamicSmemBytes = smem_a;
-        if (cudaLaunchKernelEx(&cfg, attn_d_kernel<ND, GB>, a) != cudaSuccess) return TQ_ERR_CUDA;
-    }
     cfg.gridDim = dim3(D / kHdTile, (unsigned)((rows + kHdCRows - 1) / kHdCRows));
     cfg.dynamicSmemBytes = smem_c;
     if (cudaLaunchKernelEx(&cfg, attn_d_combine_kernel<ND>, a) != cudaSuccess) return TQ_ERR_CUDA;
     return launch_status();
-}
-
-template <int ND>
-int hd_launch_attn(HdAttnArgs &a, cudaStream_t st) {
-    return a.G <= 4 ? hd_launch_attn_g<ND, 4>(a, st) : hd_launch_attn_g<ND, 8>(a, st);
 }
 
 }  // namespace
