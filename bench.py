@@ -1351,6 +1351,18 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def busy_threads(fn):
+    """fn() and the threads it kept busy on average: the process's user + system CPU time over
+    the wall time of the call (the oracle's elementwise numpy work runs on one thread, its matrix
+    products on as many as the BLAS library starts)."""
+    import resource
+    r0, w0 = resource.getrusage(resource.RUSAGE_SELF), time.perf_counter()
+    out = fn()
+    r1, w1 = resource.getrusage(resource.RUSAGE_SELF), time.perf_counter()
+    cpu = (r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)
+    return out, round(cpu / max(w1 - w0, 1e-9), 1)
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on the host cores; each step is a
     bounded sample sized so that warm-up + steps stay near a minute and a half."""
@@ -1367,10 +1379,11 @@ def run_reference(args, rank, world):
         frac = max(1.0 / 64, per_step / t1)   # a leading part of one slice's context
     for _ in range(args.warmup):
         oracle_sample(wl, groups, frac=frac)
-    times, nbytes, desc = [], 0, ""
+    times, nbytes, desc, busy = [], 0, "", []
     for _ in range(args.steps):
-        secs, nbytes, desc = oracle_sample(wl, groups, frac=frac)
+        (secs, nbytes, desc), b = busy_threads(lambda: oracle_sample(wl, groups, frac=frac))
         times.append(secs)
+        busy.append(b)
     sec = statistics.mean(times)
     val = nbytes / sec / 1e9
     return {
@@ -1378,8 +1391,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": dict(WORKLOADS[wl], workload=wl),
-        "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": max(busy), "cores_available": cpu_cores(),
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": round(val, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -1424,9 +1437,9 @@ def parity_counts(samples):
 
 def cpu_baseline(workload, groups):
     oracle_sample(workload, 1)
-    secs, nbytes, desc = oracle_sample(workload, groups or CPU_GROUPS[workload])
-    return {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": "%s, %.1f s" % (desc, secs)}
+    (secs, nbytes, desc), busy = busy_threads(lambda: oracle_sample(workload, groups or CPU_GROUPS[workload]))
+    return {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": busy, "cores_available": cpu_cores(),
+            "kind": "oracle", "sample": "%s, %.1f s" % (desc, secs)}
 
 
 def main():
