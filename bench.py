@@ -1439,7 +1439,24 @@ def cpu_baseline(workload, groups):
     oracle_sample(workload, 1)
     (secs, nbytes, desc), busy = busy_threads(lambda: oracle_sample(workload, groups or CPU_GROUPS[workload]))
     return {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": busy, "cores_available": cpu_cores(),
-            "kind": "oracle", "sample": "%s, %.1f s" % (desc, secs)}
+            "kind": "oracle", "sample": "%s, %.1f s" % (desc, secs), "single_thread": single_thread_baseline(workload)}
+
+
+def single_thread_baseline(workload):
+    """The oracle on one (sequence, KV head) slice of the workload with every thread pool of
+    numpy's libraries held to one thread (a child process: the pools are sized when numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; bench.oracle_sample(%r, 1); "
+            "r, b = bench.busy_threads(lambda: bench.oracle_sample(%r, 1)); "
+            "print(json.dumps([r[0], r[1], r[2], b]))" % (ROOT, workload, workload))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        secs, nbytes, desc, busy = json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:   # (reported, not fatal: the baseline is context, not a result)
+        return {"unavailable": "%s" % type(e).__name__}
+    return {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": busy,
+            "sample": "%s, %.2f s" % (desc, secs)}
 
 
 def main():
