@@ -403,8 +403,11 @@ const char *tq_status_string(int status);
  * then a 1-bit high plane of head_dim / 8 bytes (the 128-element layout
  * generalised); 2 + head_dim * bits / 8 bytes, back to back.  head_dim is
  * 64, 96, 128 or 160 and the codebook one of tq_codebook_load(head_dim, .).
- * These run on CUDA cores (the rotation as a dense product per row); the
- * 128-element entry points above remain the fast path for head_dim 128. */
+ * The encode of 1024 or more bf16 / fp16 rows and the decode attention run
+ * on the tensor cores, the rest of the encode and the decode on CUDA cores
+ * (the rotation as a dense product per row); the 128-element entry points
+ * above remain the fast path for head_dim 128 (the rotation there is the
+ * exact H D transform). */
 
 /* Bytes of one block at head_dim: 2 + head_dim * bits / 8; 0 if unsupported. */
 size_t tq_block_bytes_d(int head_dim, int bits);
