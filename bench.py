@@ -81,6 +81,9 @@ WORKLOADS = {
                                    page_tokens=32, kv_dtype="bf16", scale="1/sqrt(128)"),
     "headdim_160_decode": dict(B=8, Hq=32, Hkv=8, T=8192, head_dim=160, key_bits=4, value_bits=2, kv_dtype="bf16",
                                rotation="seeded random orthogonal 160 x 160 (QR), float32", scale="1/sqrt(160)"),
+    "headdim_128_g8_decode": dict(B=8, Hq=64, Hkv=8, T=8192, head_dim=128, key_bits=4, value_bits=2,
+                                  kv_dtype="bf16", rotation="seeded random orthogonal 128 x 128 (QR), float32",
+                                  scale="1/sqrt(128)"),
     "storage_roundtrip": dict(layout="[2, 32, 65536, 1024]", L=32, T=65536, hidden=1024, head_dim=128,
                               block_size=16, skip_first=2, skip_last=2, key_bits=4, value_bits=4, slot_bytes=132,
                               kv_dtype="bf16"),
@@ -105,6 +108,8 @@ KERNEL_SOURCES = {
     "qjl": ["tq_qjl.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "hd_encode": ["tq_headdim.cu", "tq_headdim.cuh", "tq_headdim_tc.cu", "tq_tc.cuh", "tq_device.cuh"],
     "hd_attention": ["tq_headdim.cu", "tq_headdim.cuh", "tq_headdim_mma.cuh", "tq_headdim_mma.cu", "tq_device.cuh"],
+    "hd_attention_g8": ["tq_headdim.cu", "tq_headdim.cuh", "tq_headdim_mma.cuh", "tq_headdim_mma.cu",
+                        "tq_headdim_mma8.cu", "tq_device.cuh"],
     "serialize": ["tq_encode.cu", "tq_tc.cuh", "tq_codec.cu", "tq_device.cuh"],
     "deserialize": ["tq_decode.cu", "tq_codec.cu", "tq_device.cuh"],
 }
@@ -890,27 +895,28 @@ def plan_storage(tq, wl, dev, stream, seed, batch):
                 dtype="bf16")
 
 
-def _rotation_160(seed=160):
-    """A seeded random orthogonal 160 x 160 matrix (QR of a Gaussian matrix), float32."""
-    a = np.random.default_rng(seed).standard_normal((160, 160))
+def _rotation_d(d):
+    """A seeded (seed d) random orthogonal d x d matrix (QR of a Gaussian matrix), float32."""
+    a = np.random.default_rng(d).standard_normal((d, d))
     q, r = np.linalg.qr(a)
     return (q * np.sign(np.diag(r))[None, :]).astype(np.float32)
 
 
 def plan_headdim(tq, wl, dev, stream, seed, batch):
-    """Decode step at head dim 160 (a spec target dim that is not a power of
-    two): encode K (4-bit) and V (2-bit) through the dense rotation, then
-    one decode attention step."""
-    from turboquant_bit_kv_gb300 import workloads
+    """Decode step at another head dim through the caller's dense rotation:
+    head dim 160 (a spec target dim that is not a power of two) with 4
+    query heads per KV head, or head dim 128 with 8 (the attention kernel's
+    eight-head variant): encode K (4-bit) and V (2-bit), then one decode
+    attention step."""
     W = WORKLOADS[wl]
     B, Hq, Hkv, T, d = batch or W["B"], W["Hq"], W["Hkv"], W["T"], W["head_dim"]
-    kcb, vcb = tq.tq_codebook_load(d, 4), tq.tq_codebook_load(d, 2)
-    R = torch.from_numpy(_rotation_160()).to(dev)
-    g = torch.Generator(device=dev).manual_seed(seed + 160)
+    kcb, vcb = tq.tq_codebook_load(d, W["key_bits"]), tq.tq_codebook_load(d, W["value_bits"])
+    R = torch.from_numpy(_rotation_d(d)).to(dev)
+    g = torch.Generator(device=dev).manual_seed(seed + d)
     k = torch.randn((B, Hkv, T, d), generator=g, device=dev).to(torch.bfloat16)
     v = torch.randn((B, Hkv, T, d), generator=g, device=dev).to(torch.bfloat16)
     q = torch.randn((B, Hq, d), generator=g, device=dev).to(torch.bfloat16)
-    kbb, vbb = tq.tq_block_bytes_d(d, 4), tq.tq_block_bytes_d(d, 2)
+    kbb, vbb = tq.tq_block_bytes_d(d, W["key_bits"]), tq.tq_block_bytes_d(d, W["value_bits"])
     kb = torch.empty((B, Hkv, T, kbb), dtype=torch.uint8, device=dev)
     vb = torch.empty((B, Hkv, T, vbb), dtype=torch.uint8, device=dev)
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
@@ -925,7 +931,8 @@ def plan_headdim(tq, wl, dev, stream, seed, batch):
                                                                  stream=stream), nvec * (2 * d + kbb), 1, nvec),
            Op("encode_v", "hd_encode", lambda: tq.tq_encode_kv_d(v.view(-1, d), vcb, R, vb.view(nvec, -1),
                                                                  stream=stream), nvec * (2 * d + vbb), 1, nvec),
-           Op("attention", "hd_attention", attn, nvec * (kbb + vbb) + q.numel() * 2 + out.numel() * 4, 3)]
+           Op("attention", "hd_attention" if Hq // Hkv <= 4 else "hd_attention_g8", attn,
+              nvec * (kbb + vbb) + q.numel() * 2 + out.numel() * 4, 3)]
 
     def e2e():
         hk, hv, hq = _pinned(k).view(-1, d), _pinned(v).view(-1, d), _pinned(q)
@@ -953,13 +960,15 @@ def plan_headdim(tq, wl, dev, stream, seed, batch):
             hout.copy_(out, non_blocking=True)
         return step, q.numel() * 2, out.numel() * 4
 
-    cfg = dict(W, B=B, l2="inputs (671 MB) larger than L2 (129 MB); attention also timed after an L2 flush")
+    cfg = dict(W, B=B, l2="inputs (%d MB) larger than L2 (129 MB); attention also timed after an L2 flush" %
+               ((k.numel() + v.numel()) * 2 // 10**6))
     return dict(ops=ops, cold="attention", e2e=e2e, decode_e2e=decode_e2e, config=cfg, dtype="bf16")
 
 
 PLANS = {"llama3_8b_decode": plan_llama, "single_head_fp32": plan_single_head, "qwen25_7b_append": plan_qwen,
          "qjl_two_term": plan_qjl, "llama3_8b_prefill": plan_prefill, "llama3_8b_turboq8_pair": plan_turboq8_pair,
-         "llama3_8b_paged_decode": plan_paged, "storage_roundtrip": plan_storage, "headdim_160_decode": plan_headdim}
+         "llama3_8b_paged_decode": plan_paged, "storage_roundtrip": plan_storage, "headdim_160_decode": plan_headdim,
+         "headdim_128_g8_decode": plan_headdim}
 
 
 def _mean_ms(evs, a, b):
@@ -1260,16 +1269,17 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
         nbytes = n * (128 * ib * 2 + kbb + vbb) + n * (kbb + vbb) + G * groups * 128 * (ib + 4)
         desc = "%d (sequence, KV head) slice(s) at T=%d: encode K/V rows, attend %d query heads" % (groups, T, G)
         return secs, nbytes, desc
-    if workload == "headdim_160_decode":
+    if workload.startswith("headdim_"):
         from oracle import headdim
         G, d = W["Hq"] // W["Hkv"], W["head_dim"]
-        R = _rotation_160().astype(np.float64)
+        R = _rotation_d(d).astype(np.float64)
         rng = np.random.default_rng(seed)
         k = rng.standard_normal((groups, T, d))
         v = rng.standard_normal((groups, T, d))
         q = rng.standard_normal((1, G * groups, d))
-        ck, bk, _ = oracle.beta_codebook(d, 4)
-        cv, bv, _ = oracle.beta_codebook(d, 2)
+        kbits, vbits = W["key_bits"], W["value_bits"]
+        ck, bk, _ = oracle.beta_codebook(d, kbits)
+        cv, bv, _ = oracle.beta_codebook(d, vbits)
         t0 = time.perf_counter()
         kh, vh = [], []
         for g in range(groups):
@@ -1280,7 +1290,7 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
         oracle.attention_dequantized(q, np.stack(kh)[None], np.stack(vh)[None], 1 / np.sqrt(d))
         secs = time.perf_counter() - t0
         n = groups * T
-        kbb, vbb = 2 + d * 4 // 8, 2 + d * 2 // 8
+        kbb, vbb = 2 + d * kbits // 8, 2 + d * vbits // 8
         nbytes = n * (2 * d * 2 + kbb + vbb) + n * (kbb + vbb) + G * groups * d * 6
         return secs, nbytes, "%d (sequence, KV head) slice(s) at T=%d, head dim %d: encode K/V rows, attend %d query heads" % (
             groups, T, d, G)
@@ -1341,7 +1351,7 @@ def oracle_sample(workload, groups, seed=0, frac=1.0):
 
 CPU_GROUPS = {"llama3_8b_decode": 128, "single_head_fp32": 1, "qwen25_7b_append": 24, "qjl_two_term": 32,
               "llama3_8b_prefill": 8, "llama3_8b_turboq8_pair": 128, "llama3_8b_paged_decode": 128,
-              "storage_roundtrip": 64, "headdim_160_decode": 32}
+              "storage_roundtrip": 64, "headdim_160_decode": 32, "headdim_128_g8_decode": 32}
 
 
 def cpu_cores():

@@ -1,5 +1,6 @@
 """GPU parity at full size for the further decode workloads (the asymmetric
-turboq8 / 4-bit norm-corrected pair, the paged cache, head dim 160), each in
+turboq8 / 4-bit norm-corrected pair, the paged cache, head dims 160 and 128
+through a dense rotation), each in
 the launch configuration the benchmark times.  As in the other full-size
 tests, the oracle checks sampled outputs one by one:
 
@@ -164,21 +165,25 @@ def test_paged_decode_fullsize(env):
         _compare_heads(q, out, b, h, *hats[(b, h)], scale)
 
 
-def test_headdim_160_fullsize(env):
-    """Batch 8, 32/8 heads, context 8192, head dim 160 with a seeded dense
-    orthogonal rotation, bf16 K/V, K4/V2: the tensor-core encodes and one
-    decode step (prep, tensor-core attention, combine)."""
+@pytest.mark.parametrize("d,Hq", [(160, 32), (128, 64)])
+def test_headdim_fullsize(env, d, Hq):
+    """Batch 8, 8 KV heads, context 8192, bf16 K/V, K4/V2 through a seeded
+    dense orthogonal rotation: head dim 160 with 32 query heads (4 per KV
+    head) and head dim 128 with 64 (8 per KV head: the attention kernel's
+    eight-head variant); the tensor-core encodes and one decode step (prep,
+    tensor-core attention, combine)."""
     tq, dev = env["tq"], env["dev"]
-    d, Bh = 160, 8
-    a = np.random.default_rng(160).standard_normal((d, d))
+    Bh = 8
+    Gh = Hq // HKV
+    a = np.random.default_rng(d).standard_normal((d, d))
     qm, r = np.linalg.qr(a)
     R32 = (qm * np.sign(np.diag(r))[None, :]).astype(np.float32)
     R = R32.astype(np.float64)
     Rd = torch.from_numpy(R32).to(dev)
-    g = torch.Generator(device=dev).manual_seed(160)
+    g = torch.Generator(device=dev).manual_seed(d)
     k = torch.randn((Bh, HKV, T, d), generator=g, device=dev).to(torch.bfloat16)
     v = torch.randn((Bh, HKV, T, d), generator=g, device=dev).to(torch.bfloat16)
-    q = torch.randn((Bh, HQ, d), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((Bh, Hq, d), generator=g, device=dev).to(torch.bfloat16)
     books = {}
     for bits in (2, 4):
         c, bd, _ = oracle.beta_codebook(d, bits)
@@ -194,7 +199,7 @@ def test_headdim_160_fullsize(env):
         idx_o, n16_o, y = headdim.encode_d(xs, R, books[bits][1])
         idx_g, n16_g = headdim.unpack_d(blk.view(nvec, -1)[rows].cpu().numpy(), d, bits)
         dist = np.min(np.abs(y[..., None] - books[bits][1].astype(np.float64)[None, None, :]), axis=-1)
-        check_counted("head dim 160 %s (full size)" % name, idx_g, idx_o, dist, n16_g, n16_o,
+        check_counted("head dim %d %s (full size)" % (d, name), idx_g, idx_o, dist, n16_g, n16_o,
                       np.linalg.norm(xs, axis=1), tie=2.0**-22)
         blocks[name] = blk
 
@@ -206,15 +211,15 @@ def test_headdim_160_fullsize(env):
             blocks[name][b, h] = torch.from_numpy(headdim.pack_d(idx, n16, bits)).to(dev)
             pair.append(headdim.decode_d(idx, n16, books[bits][0], R))
         hats[(b, h)] = tuple(pair)
-    out = torch.empty((Bh, HQ, d), dtype=torch.float32, device=dev)
-    ws = torch.empty(tq.tq_attn_workspace_bytes_d(Bh, HQ, HKV, T, d), dtype=torch.uint8, device=dev)
+    out = torch.empty((Bh, Hq, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_attn_workspace_bytes_d(Bh, Hq, HKV, T, d), dtype=torch.uint8, device=dev)
     scale = 1 / np.sqrt(d)
     tq.tq_attn_decode_d(q, blocks["K"], tq.tq_codebook_load(d, 4), blocks["V"], tq.tq_codebook_load(d, 2), Rd, out,
                         ws, T, scale)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
     for (b, h), (k_hat, v_hat) in hats.items():
-        qs = q[b, h * G:(h + 1) * G].double().cpu().numpy()[None]
+        qs = q[b, h * Gh:(h + 1) * Gh].double().cpu().numpy()[None]
         ref = oracle.attention_dequantized(qs, k_hat[None, None], v_hat[None, None], scale)
-        err = attn_rel_err(out[b, h * G:(h + 1) * G].double().cpu().numpy()[None], ref)
+        err = attn_rel_err(out[b, h * Gh:(h + 1) * Gh].double().cpu().numpy()[None], ref)
         assert np.all(err < ATTN_TOL), (b, h, err.max())
