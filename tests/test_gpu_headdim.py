@@ -196,6 +196,9 @@ def test_encode_tensor_core_norms_near_fp16_ties(env, d):
     (160, 4, 4, 2, 20, 4, 1100, [1100, 613]),
     (64, 2, 3, 3, 18, 3, 700, [0, 700, 31]),
     (128, 3, 2, 2, 16, 2, 1500, [1, 1500]),
+    # a short batch over a long context: many splits per (sequence, KV head)
+    (64, 4, 2, 1, 4, 1, 16384, None),
+    (160, 3, 3, 2, 16, 2, 12000, [12000, 9001]),
 ])
 def test_attention_matches_oracle(env, d, kbits, vbits, B, Hq, Hkv, T, lens):
     tq, dev = env["tq"], env["dev"]
