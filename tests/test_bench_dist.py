@@ -99,3 +99,21 @@ def test_end_to_end_chunks_cover_rows_once(n, parts):
         assert a.stop == b.start
     for c in ch:
         assert c.start < c.stop and c.start % 1024 == 0
+
+
+def test_every_workload_has_a_plan_an_oracle_sample_and_kernel_sources():
+    """Each workload the bench accepts has a plan, an oracle sample size for
+    the CPU baseline, and every traffic row names a workload and a kernel
+    group whose sources the bench can hash."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert set(bench.PLANS) == set(bench.WORKLOADS) == set(bench.CPU_GROUPS)
+    assert bench.DEFAULT_WORKLOAD in bench.WORKLOADS
+    for group, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(bench.CSRC, f)), (group, f)
+    rows = [l.split("|")[1:3] for l in open(bench.TRAFFIC_TABLE) if l.startswith("| ") and l.count("|") >= 8]
+    rows = [(w.strip(), g.strip()) for w, g in rows if w.strip() not in ("workload", "---")]
+    assert rows
+    for w, g in rows:
+        assert w in bench.WORKLOADS and g in bench.KERNEL_SOURCES, (w, g)
