@@ -26,7 +26,9 @@ algorithmic bytes (packed K/V blocks with their norms, the query and the
 output; QJL side data where used) over the call's device time inside the
 timed steps, in GB/s (for the storage round trip, which has no attention
 call, the serialise + deserialise bytes over their time).
-`encode_gvec_s` / `encode_frac_hbm` give the prefix encode's vectors per
+`dtype` is the arithmetic type of the path (float32: every product exact or
+split into fp16 hi / lo parts, every sum in float32), `io_dtype` that of the
+inputs.  `encode_gvec_s` / `encode_frac_hbm` give the prefix encode's vectors per
 second and its bytes over time as a fraction of the HBM peak (`frac_hbm` and
 `encode_frac_hbm` against the measured copy bandwidth, the `_nominal`
 fields against the nominal 8 TB/s); `parts` has
@@ -1156,7 +1158,10 @@ def run_gpu(args, rank, world, local_rank):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": plan["dtype"], "data": "synthetic (seeded; no dataset or model weights)",
+        "vs_baseline": None, "dtype": "f32",
+        "dtype_note": "float32 arithmetic: exact 16-bit tensor-core products (encode), fp16 hi / lo operand splits "
+                      "(attention) and every sum in float32; inputs %s, codes packed bytes" % plan["dtype"],
+        "io_dtype": plan["dtype"], "data": "synthetic (seeded; no dataset or model weights)",
         "config": dict(plan["config"], workload=args.workload,
                        launch="cuda_graph (one replay per step)" if graph is not None else "eager calls",
                        parallelism="replicas" if world > 1 else "single GPU"),
