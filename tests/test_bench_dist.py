@@ -117,3 +117,15 @@ def test_every_workload_has_a_plan_an_oracle_sample_and_kernel_sources():
     assert rows
     for w, g in rows:
         assert w in bench.WORKLOADS and g in bench.KERNEL_SOURCES, (w, g)
+
+
+def test_cpu_baseline_reports_busy_threads_and_a_single_thread_figure():
+    """The oracle's CPU baseline carries the threads it kept busy (CPU time
+    over wall time) and a figure with numpy's thread pools held to one."""
+    sys.path.insert(0, ROOT)
+    import bench
+    (out, busy) = bench.busy_threads(lambda: sum(i * i for i in range(200000)))
+    assert out > 0 and 0.5 <= busy <= 1.5          # a pure-Python loop keeps one thread busy
+    st = bench.single_thread_baseline("single_head_fp32")
+    assert "unavailable" not in st, st
+    assert st["cores"] <= 1.2 and st["value"] > 0 and st["unit"] == "GB/s"
