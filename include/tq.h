@@ -203,6 +203,19 @@ size_t tq_attn_workspace_bytes_sms(int B, int Hq, int Hkv, int T_cap, int sms);
  * split path instead. */
 int tq_attn_plan(int B, int Hq, int Hkv, int T, int key_bits, int value_bits, int qjl, int sms, int64_t *out);
 
+/* The context splits tq_attn_decode_d makes for B sequences x Hkv KV heads
+ * over T tokens when ctas_resident attention CTAs of warps_per_cta warps fit
+ * on the device at once (its tensor-core attention kernel runs 4 warps per
+ * CTA; ctas_resident is the SM count times its CTAs per SM): of the split
+ * counts s = 1 .. max(1, ceil(T / 32) / 16) (every split keeps at least 16
+ * chunks of 32 tokens), the first with the fewest waves of CTAs times
+ * 32-token steps per warp (plus one); then tokens per split = ceil(ceil(T /
+ * 32) / s) * 32 and splits = ceil(T / tokens per split).
+ *   out[0] splits, out[1] tokens per split (a multiple of 32), out[2] the most
+ *   splits a context of T tokens takes.
+ * Host only.  TQ_ERR_ARG for a non-positive size or a NULL out. */
+int tq_attn_plan_d(int B, int Hkv, int T, int ctas_resident, int warps_per_cta, int32_t *out);
+
 /* Fused decode attention over a packed cache ([spec] Optimization: Fused
  * dequant-dot; [fork] section 2 "fused flash-attention path required";
  * [rotor] Fused Kernel Logic for the QJL term).  One query token per

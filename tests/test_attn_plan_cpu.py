@@ -106,3 +106,30 @@ def test_plan_rejects_split_path_and_bad_shapes(tq):
         with pytest.raises(tq.TQError) as e:                # QJL shapes served by the CUDA-core path
             tq.tq_attn_plan(*args, qjl=True)
         assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,Hkv,T,slots", [
+    (8, 8, 8192, 456),        # the head-dim-160 workload: 3 CTAs per SM on 152 SMs
+    (8, 8, 8192, 304),        # 2 CTAs per SM (4-bit values at d = 160)
+    (1, 1, 16384, 456),       # one long sequence: many splits
+    (2, 4, 32, 456),          # one chunk: one split
+    (3, 2, 700, 456),
+    (64, 8, 32768, 456),      # more segments than slots: several waves
+    (1, 1, 1, 1),
+])
+def test_headdim_split_plan_matches_its_definition(tq, B, Hkv, T, slots):
+    """tq_attn_plan_d against its stated rule, by brute force: of s = 1 .. max(1, C / 16)
+    (C = ceil(T / 32) chunks), the first s with the fewest waves x (steps per warp + 1); then
+    whole chunks per split and no empty split."""
+    warps = 4
+    splits, tps, smax = tq.tq_attn_plan_d(B, Hkv, T, slots, warps)
+    C = -(-T // 32)
+    assert smax == max(1, C // 16)
+    costs = [(-(-B * Hkv * s // slots)) * (-(-(-(-C // s)) // warps) + 1) for s in range(1, smax + 1)]
+    best = 1 + costs.index(min(costs))
+    assert tps == -(-C // best) * 32 and tps % 32 == 0
+    assert splits == -(-T // tps)
+    assert 1 <= splits <= best <= smax
+    assert splits * tps >= T and (splits - 1) * tps < T     # every split holds tokens
+    with pytest.raises(Exception):
+        tq.tq_attn_plan_d(B, Hkv, 0, slots, warps)

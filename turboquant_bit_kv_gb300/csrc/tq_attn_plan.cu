@@ -1,10 +1,13 @@
 // tq_attn_plan: the work partition tq_attn_decode's tensor-core path uses
 // for a shape (split-K over the context of "TurboQuant KV Cache Compression
-// — Spec", Optimization: Fused dequant-dot), for tests and tuning.  Host
-// only: it computes the plan and touches no device memory.
+// — Spec", Optimization: Fused dequant-dot), for tests and tuning; and
+// tq_attn_plan_d, the context splits of tq_attn_decode_d for a given count
+// of resident CTAs.  Host only: they compute the plan and touch no device
+// memory.
 
 #include "tq.h"
 #include "tq_attn_mma.h"
+#include "tq_headdim.cuh"
 #include "tq_internal.h"
 
 using namespace tq;
@@ -24,5 +27,15 @@ extern "C" int tq_attn_plan(int B, int Hq, int Hkv, int T, int key_bits, int val
     out[4] = p.Smax;
     out[5] = mma_combine_groups(p);
     out[6] = p.warps;
+    return TQ_OK;
+}
+
+extern "C" int tq_attn_plan_d(int B, int Hkv, int T, int ctas_resident, int warps_per_cta, int32_t *out) {
+    if (!out || B <= 0 || Hkv <= 0 || T <= 0 || ctas_resident <= 0 || warps_per_cta <= 0) return TQ_ERR_ARG;
+    int splits = 0, tps = 0;
+    hd_split_plan(B, Hkv, T, ctas_resident, warps_per_cta, &splits, &tps);
+    out[0] = splits;
+    out[1] = tps;
+    out[2] = hd_max_splits(T);
     return TQ_OK;
 }

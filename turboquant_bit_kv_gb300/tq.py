@@ -58,6 +58,7 @@ def lib():
         L.tq_attn_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
         L.tq_attn_workspace_bytes.restype = sz
         L.tq_attn_plan.argtypes = [c_int] * 8 + [ctypes.POINTER(i64)]
+        L.tq_attn_plan_d.argtypes = [c_int] * 5 + [ctypes.POINTER(ctypes.c_int32)]
         L.tq_attn_decode.argtypes = [vp, c_int, vp, cbp, vp, cbp, vp, c_int, c_int, c_int, c_int, c_int,
                                      ctypes.c_float, tq_signs, vp, vp, vp, vp, vp, sz, vp]
         L.tq_serde_size.argtypes = [c_int] * 10
@@ -201,6 +202,13 @@ def tq_attn_plan(B, Hq, Hkv, T, key_bits, value_bits, qjl=False, sms=0):
     out = (ctypes.c_int64 * 7)()
     _check(lib().tq_attn_plan(B, Hq, Hkv, T, key_bits, value_bits, 1 if qjl else 0, sms, out), "tq_attn_plan")
     return dict(zip(("C", "Ctot", "P", "W", "Smax", "combine_groups", "warps"), (int(x) for x in out)))
+
+
+def tq_attn_plan_d(B, Hkv, T, ctas_resident, warps_per_cta=4):
+    """Host-only split plan of tq_attn_decode_d: (splits, tokens per split, most splits)."""
+    out = (ctypes.c_int32 * 3)()
+    _check(lib().tq_attn_plan_d(B, Hkv, T, ctas_resident, warps_per_cta, out), "tq_attn_plan_d")
+    return int(out[0]), int(out[1]), int(out[2])
 
 
 def tq_attn_workspace_bytes(B, Hq, Hkv, T_cap):
